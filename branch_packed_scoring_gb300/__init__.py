@@ -1,0 +1,322 @@
+"""Python binding of the branch-packed scoring C ABI (``include/spinf.h``).
+
+Argument marshalling only: every step of the path runs in ``libspinf.so``
+(host planner and collect in C++, attention and scoring in sm_103a kernels).
+There is no fallback: if the library is missing, every call raises.
+
+Device tensors are passed as ``torch.Tensor`` (or raw integer addresses);
+torch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libspinf.so")
+
+OK, E_INVALID, E_LIMIT, E_NOMEM, E_CUDA, E_UNSUPPORTED, E_DEVICE_TIMEOUT, E_DEVICE_CHECK = range(8)
+STATUS_NAMES = {0: "OK", 1: "INVALID", 2: "LIMIT", 3: "NOMEM", 4: "CUDA", 5: "UNSUPPORTED",
+                6: "DEVICE_TIMEOUT", 7: "DEVICE_CHECK"}
+DTYPE_BF16, DTYPE_E4M3 = 0, 1
+
+#: every symbol the header declares
+SYMBOLS = [
+    "spinf_plan_opts_default", "spinf_pack_plan", "spinf_plan_num_passes", "spinf_plan_pass_info",
+    "spinf_plan_counts", "spinf_plan_upload", "spinf_branch_attention", "spinf_score_workspace_bytes",
+    "spinf_score", "spinf_collect", "spinf_device_status", "spinf_plan_free", "spinf_fingerprint",
+    "spinf_status_string", "spinf_last_error",
+]
+
+
+class SpinfError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+        self.status_name = STATUS_NAMES.get(status, str(status))
+
+
+class _Tokens(ctypes.Structure):
+    _fields_ = [("ids", ctypes.c_void_p), ("n", ctypes.c_int32)]
+
+
+class _Opts(ctypes.Structure):
+    _fields_ = [("token_budget", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
+                ("max_content_tokens", ctypes.c_int32), ("max_query_tokens", ctypes.c_int32),
+                ("max_options", ctypes.c_int32), ("max_option_tokens", ctypes.c_int32),
+                ("max_prompts_per_input", ctypes.c_int32), ("floors", ctypes.c_int32),
+                ("floor_prefix", _Tokens), ("vocab", ctypes.c_int32)]
+
+
+_P = ctypes.POINTER(ctypes.c_int32)
+
+
+class _PassInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("T", "T_pad", "n_qtiles", "n_sched", "M", "G", "n_units")] + \
+               [(n, _P) for n in ("tok", "parent", "pos", "end", "anchor", "tile_ptr", "tile_kv", "slot_row",
+                                  "gather_m", "gather_tok", "unit_start", "unit_source")]
+
+
+_D = ctypes.POINTER(ctypes.c_double)
+
+
+class _Result(ctypes.Structure):
+    _fields_ = [(n, _D) for n in ("option_lp", "option_p", "option_floor_lp", "option_floor_p", "residual",
+                                  "floor_residual")]
+
+
+# numpy views of the request structs (same layout as the header on LP64)
+_TOK = np.dtype([("ids", "<u8"), ("n", "<i4"), ("_pad", "<i4")])
+_QUE = np.dtype([("tmpl_ids", "<u8"), ("tmpl_n", "<i4"), ("_p0", "<i4"), ("options", "<u8"),
+                 ("n_options", "<i4"), ("_p1", "<i4")])
+_INP = np.dtype([("content_ids", "<u8"), ("content_n", "<i4"), ("_p0", "<i4"), ("questions", "<u8"),
+                 ("n_questions", "<i4"), ("_p1", "<i4")])
+
+_lib = None
+
+
+def lib():
+    """The loaded ``libspinf.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m branch_packed_scoring_gb300.build` "
+                           "(or __graft_entry__.build()); there is no fallback implementation")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    L.spinf_plan_opts_default.argtypes = [ctypes.POINTER(_Opts)]
+    L.spinf_plan_opts_default.restype = None
+    L.spinf_pack_plan.argtypes = [vp, i32, ctypes.POINTER(_Opts), ctypes.POINTER(vp)]
+    L.spinf_plan_num_passes.argtypes = [vp]
+    L.spinf_plan_num_passes.restype = i32
+    L.spinf_plan_pass_info.argtypes = [vp, i32, ctypes.POINTER(_PassInfo)]
+    L.spinf_plan_counts.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    L.spinf_plan_upload.argtypes = [vp, i32, vp]
+    L.spinf_branch_attention.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, f32, i32, vp]
+    L.spinf_score_workspace_bytes.argtypes = [vp, i32, i32, i32, i32]
+    L.spinf_score_workspace_bytes.restype = sz
+    L.spinf_score.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.spinf_collect.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(_Result)]
+    L.spinf_device_status.argtypes = [vp, vp]
+    L.spinf_plan_free.argtypes = [vp]
+    L.spinf_plan_free.restype = None
+    L.spinf_fingerprint.restype = ctypes.c_char_p
+    L.spinf_status_string.argtypes = [i32]
+    L.spinf_status_string.restype = ctypes.c_char_p
+    L.spinf_last_error.restype = ctypes.c_char_p
+    for name in ("spinf_pack_plan", "spinf_plan_pass_info", "spinf_plan_counts", "spinf_plan_upload",
+                 "spinf_branch_attention", "spinf_score", "spinf_collect", "spinf_device_status"):
+        getattr(L, name).restype = i32
+    _lib = L
+    return L
+
+
+def _check(status):
+    if status != OK:
+        raise SpinfError(status, lib().spinf_last_error().decode())
+
+
+def _ptr(x):
+    """Device/host address of a torch tensor, numpy array or int (None -> 0)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    raise TypeError(f"cannot take the address of {type(x)}")
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def fingerprint() -> str:
+    return lib().spinf_fingerprint().decode()
+
+
+@dataclass
+class PassInfo:
+    T: int
+    T_pad: int
+    n_qtiles: int
+    n_sched: int
+    M: int
+    G: int
+    n_units: int
+    tok: np.ndarray
+    parent: np.ndarray
+    pos: np.ndarray
+    end: np.ndarray
+    anchor: np.ndarray
+    tile_ptr: np.ndarray
+    tile_kv: np.ndarray
+    slot_row: np.ndarray
+    gather_m: np.ndarray
+    gather_tok: np.ndarray
+    unit_start: np.ndarray
+    unit_source: np.ndarray
+
+
+def _marshal(inputs):
+    """Lay the request out as the header's structs in numpy buffers (kept alive by the caller)."""
+    ids = []
+    n_q = sum(len(q) for _, q in inputs)
+    n_o = sum(len(opts) for _, q in inputs for _, opts in q)
+    inp = np.zeros(len(inputs), dtype=_INP)
+    que = np.zeros(max(n_q, 1), dtype=_QUE)
+    tok = np.zeros(max(n_o, 1), dtype=_TOK)
+    off = 0
+    spans_c, spans_t, spans_o = [], [], []
+    qi = oi = 0
+    for i, (content, questions) in enumerate(inputs):
+        spans_c.append((off, len(content)))
+        ids.append(np.asarray(content, dtype=np.int32).ravel())
+        off += len(content)
+        inp[i]["questions"] = qi
+        inp[i]["n_questions"] = len(questions)
+        for template, options in questions:
+            spans_t.append((qi, off, len(template)))
+            ids.append(np.asarray(template, dtype=np.int32).ravel())
+            off += len(template)
+            que[qi]["options"] = oi
+            que[qi]["n_options"] = len(options)
+            for opt in options:
+                spans_o.append((oi, off, len(opt)))
+                ids.append(np.asarray(opt, dtype=np.int32).ravel())
+                off += len(opt)
+                oi += 1
+            qi += 1
+    flat = np.concatenate(ids) if ids else np.zeros(1, dtype=np.int32)
+    flat = np.ascontiguousarray(flat, dtype=np.int32)
+    base = flat.ctypes.data
+    qbase, obase = que.ctypes.data, tok.ctypes.data
+    for i, (o, n) in enumerate(spans_c):
+        inp[i]["content_ids"] = base + 4 * o if n else 0
+        inp[i]["content_n"] = n
+        inp[i]["questions"] = qbase + que.itemsize * int(inp[i]["questions"])
+    for q, o, n in spans_t:
+        que[q]["tmpl_ids"] = base + 4 * o
+        que[q]["tmpl_n"] = n
+        que[q]["options"] = obase + tok.itemsize * int(que[q]["options"])
+    for k, o, n in spans_o:
+        tok[k]["ids"] = base + 4 * o
+        tok[k]["n"] = n
+    return inp, (flat, que, tok)
+
+
+class Plan:
+    """A packed layout of a request (``spinf_pack_plan``).  Owns its device copies."""
+
+    def __init__(self, inputs, *, token_budget=None, max_tokens=None, max_content_tokens=None,
+                 max_query_tokens=None, max_options=None, max_option_tokens=None, max_prompts_per_input=None,
+                 floors=True, floor_prefix=(), vocab=0):
+        L = lib()
+        self._h = None
+        opts = _Opts()
+        L.spinf_plan_opts_default(ctypes.byref(opts))
+        for name, val in (("token_budget", token_budget), ("max_tokens", max_tokens),
+                          ("max_content_tokens", max_content_tokens), ("max_query_tokens", max_query_tokens),
+                          ("max_options", max_options), ("max_option_tokens", max_option_tokens),
+                          ("max_prompts_per_input", max_prompts_per_input)):
+            if val is not None:
+                setattr(opts, name, int(val))
+        opts.floors = 1 if floors else 0
+        fp = np.ascontiguousarray(np.asarray(floor_prefix, dtype=np.int32).ravel())
+        opts.floor_prefix.ids = fp.ctypes.data if len(fp) else None
+        opts.floor_prefix.n = len(fp)
+        opts.vocab = int(vocab)
+        inp, keep = _marshal(inputs)
+        h = ctypes.c_void_p()
+        _check(L.spinf_pack_plan(inp.ctypes.data if len(inp) else None, len(inputs), ctypes.byref(opts),
+                                 ctypes.byref(h)))
+        del keep, fp
+        self._h = h
+        self.num_passes = L.spinf_plan_num_passes(h)
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise RuntimeError("plan is closed")
+        return self._h
+
+    def pass_info(self, p) -> PassInfo:
+        info = _PassInfo()
+        _check(lib().spinf_plan_pass_info(self.handle, p, ctypes.byref(info)))
+
+        def arr(ptr, n):
+            return np.ctypeslib.as_array(ptr, shape=(n,)).copy() if n > 0 else np.zeros(0, dtype=np.int32)
+
+        return PassInfo(
+            T=info.T, T_pad=info.T_pad, n_qtiles=info.n_qtiles, n_sched=info.n_sched, M=info.M, G=info.G,
+            n_units=info.n_units, tok=arr(info.tok, info.T_pad), parent=arr(info.parent, info.T_pad),
+            pos=arr(info.pos, info.T_pad), end=arr(info.end, info.T_pad), anchor=arr(info.anchor, info.T_pad),
+            tile_ptr=arr(info.tile_ptr, info.n_qtiles + 1), tile_kv=arr(info.tile_kv, info.n_sched),
+            slot_row=arr(info.slot_row, info.M), gather_m=arr(info.gather_m, info.G),
+            gather_tok=arr(info.gather_tok, info.G), unit_start=arr(info.unit_start, info.n_units + 1),
+            unit_source=arr(info.unit_source, info.n_units))
+
+    def counts(self):
+        nq, no = ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().spinf_plan_counts(self.handle, ctypes.byref(nq), ctypes.byref(no)))
+        return nq.value, no.value
+
+    def upload(self, p, stream=None):
+        _check(lib().spinf_plan_upload(self.handle, p, _stream(stream)))
+
+    def collect(self, token_lp_per_pass):
+        """Per option lp / p / floor and per question residuals from host fp32 token lps."""
+        nq, no = self.counts()
+        out = {k: np.full(n, np.nan) for k, n in (("option_lp", no), ("option_p", no), ("option_floor_lp", no),
+                                                 ("option_floor_p", no), ("residual", nq),
+                                                 ("floor_residual", nq))}
+        res = _Result(*[v.ctypes.data_as(_D) for v in out.values()])
+        arrs = [np.ascontiguousarray(a, dtype=np.float32) for a in token_lp_per_pass]
+        if len(arrs) != self.num_passes:
+            raise ValueError("one token-lp array per pass is needed")
+        ptrs = (ctypes.c_void_p * max(1, len(arrs)))(*[a.ctypes.data for a in arrs])
+        _check(lib().spinf_collect(self.handle, ptrs, ctypes.byref(res)))
+        return out
+
+    def device_status(self, stream=None):
+        _check(lib().spinf_device_status(self.handle, _stream(stream)))
+
+    def close(self):
+        if self._h is not None and _lib is not None:
+            _lib.spinf_plan_free(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def branch_attention(plan, p, q, k, v, o, n_q_heads, n_kv_heads, d_head, scale=0.0, window=0, stream=None):
+    _check(lib().spinf_branch_attention(plan.handle, p, _ptr(q), _ptr(k), _ptr(v), _ptr(o), n_q_heads,
+                                        n_kv_heads, d_head, float(scale), int(window), _stream(stream)))
+
+
+def score_workspace_bytes(plan, p, vocab, d_model, w_dtype=DTYPE_BF16):
+    return lib().spinf_score_workspace_bytes(plan.handle, p, vocab, d_model, w_dtype)
+
+
+def score(plan, p, hidden, w, w_scale, w_dtype, d_model, vocab, row_lse, token_lp, workspace, workspace_bytes=None,
+          stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().spinf_score(plan.handle, p, _ptr(hidden), _ptr(w), _ptr(w_scale), w_dtype, d_model, vocab,
+                             _ptr(row_lse), _ptr(token_lp), _ptr(workspace), int(workspace_bytes),
+                             _stream(stream)))

@@ -1,0 +1,338 @@
+// Tree-masked GQA attention over one packed pass (sm_103a, tcgen05 + TMA).
+//
+// The method ("spinf-serve 0.1.1", PyPI page, "What it does" and "Speed and
+// scale"): every question is a branch of the same pass; a branch token attends
+// to its own content and causally to its own branch, never to a sibling or to
+// another packed input.  The planner encodes that as: key k is visible to the
+// rows [k, end[k]).
+//
+// One CTA computes one 128-row Q tile of one query head:
+//   warp 0      TMA producer: Q once, then K and V tiles (128 keys x d) in the
+//               order of the tile's schedule
+//   warp 1      TMEM owner and MMA issuer: S = Q K^T (SS form, fp32 in TMEM),
+//               O += P V (P read from TMEM, V from shared memory, MN-major)
+//   warps 2-5   one thread per Q row: mask, online softmax, P (bf16) into TMEM,
+//               rescale O in TMEM when the row maximum grows, final O / l
+//
+// Batch invariance ("What it does": an input's scores are bit-identical alone
+// or packed with thousands of others): KV tiles start at the first row of the
+// input that owns them, so a key always lands in the same MMA column whatever
+// precedes its input in the pass; tiles are visited in a fixed order; a tile
+// with no visible key for a row is an exact no-op for that row (its maximum
+// stays, P is exactly 0 and O is not rescaled).  O starts at zero and is always
+// accumulated, so the first visible tile takes the same path alone or packed.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "runtime.h"
+
+namespace spinf {
+namespace {
+
+using namespace dev;
+
+constexpr int kAttnThreads = 192;
+constexpr int kBoxBytes = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128-byte swizzled rows)
+
+enum { Q_FULL = 0, K_FULL, K_EMPTY, V_FULL, V_EMPTY, S_FULL, P_FULL, O_DONE, N_BARS };
+
+template <int D>
+struct AttnSmem {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kTileBytes = kChunks * kBoxBytes;
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + kTileBytes;
+    static constexpr int kV = kK + kTileBytes;
+    static constexpr int kKvEnd = kV + kTileBytes;        // int32 [2][128]
+    static constexpr int kKvPos = kKvEnd + 2 * 128 * 4;   // int32 [2][128]
+    static constexpr int kBars = kKvPos + 2 * 128 * 4;
+    static constexpr int kHolder = kBars + N_BARS * 8;
+    static constexpr int kBytes = kHolder + 16;
+    static constexpr int kAlloc = kBytes + 1024;           // room to align the base to 1024
+};
+
+// TMEM columns: S [0,128), P (bf16 pairs) [128,192), O after P.  A CTA owns
+// kTmemCols columns; the shared-memory request caps the CTAs per SM so that
+// co-resident CTAs never wait on each other's TMEM.
+constexpr uint32_t kColS = 0, kColP = 128;
+template <int D> constexpr uint32_t kColO = D <= 64 ? 192 : 256;
+template <int D> constexpr uint32_t kTmemCols = D <= 64 ? 256 : 512;
+template <int D> constexpr int kMinSmem = D <= 64 ? 80 * 1024 : 116 * 1024;   // <= 2 resp. 1 CTA per SM
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    branch_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
+                            const int32_t* __restrict__ end, const int32_t* __restrict__ pos,
+                            const int32_t* __restrict__ tile_ptr, const int32_t* __restrict__ tile_kv, int T,
+                            int T_pad, int Hq, int Hkv, float scale_log2, int window, int* __restrict__ err) {
+    using L = AttnSmem<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = smem + L::kQ;
+    uint8_t* sK = smem + L::kK;
+    uint8_t* sV = smem + L::kV;
+    int32_t* kv_end = reinterpret_cast<int32_t*>(smem + L::kKvEnd);
+    int32_t* kv_pos = reinterpret_cast<int32_t*>(smem + L::kKvPos);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
+    uint32_t* holder = reinterpret_cast<uint32_t*>(smem + L::kHolder);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = blockIdx.x, h = blockIdx.y;
+    const int g = h / (Hq / Hkv);
+    const int s0 = tile_ptr[qt];
+    const int n = tile_ptr[qt + 1] - s0;
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < N_BARS; ++b) mbar_init(&bars[b], b == P_FULL ? 128 : 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(holder, kTmemCols<D>);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *holder;
+
+    if (warp == 0) {
+        if (lane == 0 && n > 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            mbar_arrive_expect_tx(&bars[Q_FULL], L::kTileBytes);
+            for (int c = 0; c < L::kChunks; ++c) tma_load_3d(sQ + c * kBoxBytes, &tm_q, &bars[Q_FULL], c * 64, h, qt * 128);
+            for (int j = 0; j < n; ++j) {
+                const int kv0 = tile_kv[s0 + j];
+                if (j > 0) mbar_wait(&bars[K_EMPTY], (j - 1) & 1, err);
+                mbar_arrive_expect_tx(&bars[K_FULL], L::kTileBytes);
+                for (int c = 0; c < L::kChunks; ++c) tma_load_3d(sK + c * kBoxBytes, &tm_k, &bars[K_FULL], c * 64, g, kv0);
+                if (j > 0) mbar_wait(&bars[V_EMPTY], (j - 1) & 1, err);
+                mbar_arrive_expect_tx(&bars[V_FULL], L::kTileBytes);
+                for (int c = 0; c < L::kChunks; ++c) tma_load_3d(sV + c * kBoxBytes, &tm_v, &bars[V_FULL], c * 64, g, kv0);
+            }
+            // our last copies have landed before the CTA may retire
+            mbar_wait(&bars[K_FULL], (n - 1) & 1, err);
+            mbar_wait(&bars[V_FULL], (n - 1) & 1, err);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && n > 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
+            const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+            mbar_wait(&bars[Q_FULL], 0, err);
+            auto issue_s = [&](int j) {
+                mbar_wait(&bars[K_FULL], j & 1, err);
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+                    mma_f16_ss(tmem + kColS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024),
+                               idesc_qk, kk > 0);
+                }
+                mma_commit(&bars[K_EMPTY]);
+                mma_commit(&bars[S_FULL]);
+            };
+            issue_s(0);
+            for (int j = 0; j < n; ++j) {
+                mbar_wait(&bars[P_FULL], j & 1, err);
+                tc_fence_after();
+                if (j + 1 < n) issue_s(j + 1);
+                mbar_wait(&bars[V_FULL], j & 1, err);
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_f16_ts(tmem + kColO<D>, tmem + kColP + kk * 8, sdesc_sw128(aV + kk * 2048, kBoxBytes, 1024),
+                               idesc_pv, 1);
+                mma_commit(&bars[V_EMPTY]);
+                mma_commit(&bars[O_DONE]);
+            }
+        }
+    } else {
+        const int quarter = warp & 3;                 // TMEM lanes this warp may touch
+        const int r = quarter * 32 + lane;            // Q-tile row of this thread
+        const int t = (warp - 2) * 32 + lane;         // 0..127 for cooperative loads
+        const int q_row = qt * 128 + r;
+        const bool real = q_row < T;
+        const int pos_q = pos[q_row];
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_off + kColS, tP = tmem + lane_off + kColP, tO = tmem + lane_off + kColO<D>;
+
+        {
+            uint32_t z[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) z[i] = 0u;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tmem_st32(tO + c * 32, z);
+            tmem_st_wait();
+        }
+        float m = -INFINITY, l = 0.f;
+        for (int j = 0; j < n; ++j) {
+            const int kv0 = tile_kv[s0 + j];
+            int32_t* e_buf = kv_end + (j & 1) * 128;
+            int32_t* p_buf = kv_pos + (j & 1) * 128;
+            {
+                const int k = kv0 + t;
+                e_buf[t] = k < T_pad ? end[k] : -1;
+                p_buf[t] = k < T_pad ? pos[k] : 0;
+            }
+            named_bar_sync(1, 128);
+            mbar_wait(&bars[S_FULL], j & 1, err);
+            tc_fence_after();
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t rr[32];
+                tmem_ld32(tS + c * 32, rr);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(rr[i]);
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                const int k = kv0 + c;
+                const bool vis = real && k <= q_row && q_row < e_buf[c] && (window <= 0 || pos_q - p_buf[c] < window);
+                s[c] = vis ? s[c] : -INFINITY;
+                mx = fmaxf(mx, s[c]);
+            }
+            const float m_new = fmaxf(m, mx);
+            if (j > 0) {   // PV of the previous tile has read P and written O
+                mbar_wait(&bars[O_DONE], (j - 1) & 1, err);
+                tc_fence_after();
+            }
+            uint32_t pk0[32], pk1[32];
+            bool grow = false;
+            float alpha = 1.f;
+            if (m_new == -INFINITY) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) pk0[i] = pk1[i] = 0u;
+            } else {
+                const float mb = m_new * scale_log2;
+                float rowsum = 0.f;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const float p0 = fast_exp2(fmaf(s[2 * c], scale_log2, -mb));
+                    const float p1 = fast_exp2(fmaf(s[2 * c + 1], scale_log2, -mb));
+                    const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
+                    const float2 f = __bfloat1622float2(b);
+                    rowsum += f.x;
+                    rowsum += f.y;
+                    const uint32_t w = *reinterpret_cast<const uint32_t*>(&b);
+                    if (c < 32) pk0[c] = w; else pk1[c - 32] = w;
+                }
+                // the row maximum grew: O and l shrink by alpha
+                grow = m != -INFINITY && m_new > m;
+                if (grow) alpha = fast_exp2(fmaf(m, scale_log2, -mb));
+                l = l * alpha + rowsum;
+                m = m_new;
+            }
+            // TMEM traffic is warp-collective: lanes whose maximum did not move multiply by exactly 1
+            if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t rr[32];
+                    tmem_ld32(tO + c * 32, rr);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+                    tmem_st32(tO + c * 32, rr);
+                }
+            }
+            tmem_st32(tP, pk0);
+            tmem_st32(tP + 32, pk1);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bars[P_FULL]);
+        }
+        if (n > 0) {
+            mbar_wait(&bars[O_DONE], (n - 1) & 1, err);
+            tc_fence_after();
+        }
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16* dst = out + (static_cast<size_t>(q_row) * Hq + h) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t rr[32];
+            tmem_ld32(tO + c * 32, rr);
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                w[i] = real ? pack_bf16x2(__uint_as_float(rr[2 * i]) * inv, __uint_as_float(rr[2 * i + 1]) * inv) : 0u;
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols<D>);
+    }
+}
+
+template <int D>
+spinf_status launch_attention(const Pass& P, const void* q, const void* k, const void* v, void* o, int Hq,
+                              int Hkv, float scale, int window, int* err, cudaStream_t stream) {
+    CUtensorMap tq, tk, tv;
+    const uint64_t dq[3] = {(uint64_t)D, (uint64_t)Hq, (uint64_t)P.T_pad};
+    const uint64_t sq[2] = {(uint64_t)D * 2, (uint64_t)Hq * D * 2};
+    const uint64_t dk[3] = {(uint64_t)D, (uint64_t)Hkv, (uint64_t)P.T_pad};
+    const uint64_t sk[2] = {(uint64_t)D * 2, (uint64_t)Hkv * D * 2};
+    const uint32_t box[3] = {64, 1, 128};
+    spinf_status st;
+    if ((st = make_tmap(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dq, sq, box, CU_TENSOR_MAP_SWIZZLE_128B)))
+        return st;
+    if ((st = make_tmap(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k, dk, sk, box, CU_TENSOR_MAP_SWIZZLE_128B)))
+        return st;
+    if ((st = make_tmap(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v, dk, sk, box, CU_TENSOR_MAP_SWIZZLE_128B)))
+        return st;
+    const int smem = AttnSmem<D>::kAlloc > kMinSmem<D> ? AttnSmem<D>::kAlloc : kMinSmem<D>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(branch_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
+        configured = true;
+    }
+    const float scale_log2 = scale * 1.4426950408889634f;
+    dim3 grid(P.T_pad / 128, Hq);
+    branch_attention_kernel<D><<<grid, kAttnThreads, smem, stream>>>(
+        tq, tk, tv, static_cast<__nv_bfloat16*>(o), P.dev.end, P.dev.pos, P.dev.tile_ptr, P.dev.tile_kv, P.T,
+        P.T_pad, Hq, Hkv, scale_log2, window, err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+    return SPINF_OK;
+}
+
+}  // namespace
+}  // namespace spinf
+
+using namespace spinf;
+
+extern "C" spinf_status spinf_branch_attention(const spinf_plan* plan, int32_t pass, const void* q, const void* k,
+                                               const void* v, void* o, int32_t n_q_heads, int32_t n_kv_heads,
+                                               int32_t d_head, float scale, int32_t window, spinf_stream stream) {
+    spinf_status st = ensure_device_ready(plan, pass);
+    if (st) return st;
+    if (!q || !k || !v || !o) return fail(SPINF_E_INVALID, "NULL tensor");
+    for (const void* p : {q, k, v, (const void*)o})
+        if (reinterpret_cast<uintptr_t>(p) & 15) return fail(SPINF_E_INVALID, "tensor not 16-byte aligned");
+    if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads) return fail(SPINF_E_INVALID, "bad head counts");
+    if (window < 0) return fail(SPINF_E_INVALID, "negative window");
+    const Pass& P = plan->passes[pass];
+    if (P.T == 0) return SPINF_OK;
+    if (!(scale > 0.f)) scale = 1.0f / std::sqrt(static_cast<float>(d_head));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    switch (d_head) {
+        case 64: return launch_attention<64>(P, q, k, v, o, n_q_heads, n_kv_heads, scale, window, plan->d_err, s);
+        case 128: return launch_attention<128>(P, q, k, v, o, n_q_heads, n_kv_heads, scale, window, plan->d_err, s);
+        case 256: return launch_attention<256>(P, q, k, v, o, n_q_heads, n_kv_heads, scale, window, plan->d_err, s);
+        default: return fail(SPINF_E_UNSUPPORTED, "d_head must be 64, 128 or 256");
+    }
+}

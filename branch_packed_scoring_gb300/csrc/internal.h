@@ -1,0 +1,63 @@
+// Internal state shared by the planner, the runtime glue and the kernels' host
+// launchers.  Not part of the C ABI.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "spinf.h"
+
+namespace spinf {
+
+constexpr int kTile = 128;  // rows of a Q tile and of a KV tile
+
+// Device copies of one pass's descriptors, in one allocation.
+struct PassDevice {
+    void* block = nullptr;
+    int32_t* end = nullptr;        // [T_pad]
+    int32_t* pos = nullptr;        // [T_pad]
+    int32_t* tile_ptr = nullptr;   // [n_qtiles + 1]
+    int32_t* tile_kv = nullptr;    // [n_sched]
+    int32_t* slot_row = nullptr;   // [M]
+    int32_t* gather_m = nullptr;   // [G]
+    int32_t* gather_tok = nullptr; // [G]
+    int32_t* row_gptr = nullptr;   // [M + 1] gathers of each scoring row ...
+    int32_t* row_glist = nullptr;  // [G]     ... sorted by token id, then gather index
+};
+
+struct Pass {
+    int32_t T = 0, T_pad = 0;
+    std::vector<int32_t> tok, parent, pos, end, anchor;
+    std::vector<int32_t> tile_ptr, tile_kv;
+    std::vector<int32_t> slot_row, gather_m, gather_tok;
+    std::vector<int32_t> row_gptr, row_glist;
+    std::vector<int32_t> unit_start, unit_source;
+    PassDevice dev;
+};
+
+// Where the option tokens of one laid-out question sit in its pass's gather list.
+struct QuestionSite {
+    int32_t pass = -1;
+    int32_t g0 = 0;          // first gather entry
+    int32_t opt0 = 0;        // first entry in Plan::opt_len
+    int32_t n_options = 0;
+};
+
+}  // namespace spinf
+
+struct spinf_plan {
+    std::vector<spinf::Pass> passes;
+    std::vector<int32_t> opt_len;                // token count of every option, question by question
+    std::vector<spinf::QuestionSite> user_q;     // every user question, input by input
+    std::vector<int32_t> user_q_floor;           // floor index per user question, or -1
+    std::vector<spinf::QuestionSite> floor_q;    // every floor question
+    int64_t n_options_total = 0;
+    int32_t* d_err = nullptr;                    // device error word (allocated at first upload)
+    int device = -1;
+};
+
+namespace spinf {
+spinf_status fail(spinf_status s, const std::string& msg);
+spinf_status ok();
+}  // namespace spinf

@@ -1,0 +1,154 @@
+// Runtime glue of the C ABI: descriptor upload, the device error word, TMA
+// tensor-map encoding, plan teardown and the result fingerprint.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "runtime.h"
+
+namespace spinf {
+
+spinf_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(SPINF_E_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+spinf_status make_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                       CUtensorMapSwizzle swizzle) {
+    auto fn = encode_fn();
+    if (!fn) return fail(SPINF_E_CUDA, "cuTensorMapEncodeTiled is not available");
+    cuuint64_t d[5], s[4];
+    cuuint32_t b[5], e[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        e[i] = 1;
+        if (i + 1 < rank) s[i] = strides_bytes[i];
+    }
+    CUresult r = fn(map, dtype, rank, const_cast<void*>(base), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(SPINF_E_INVALID, "tensor map encoding failed (alignment or sizes)");
+    return SPINF_OK;
+}
+
+spinf_status ensure_device_ready(const spinf_plan* plan, int32_t pass) {
+    if (!plan) return fail(SPINF_E_INVALID, "plan is NULL");
+    if (pass < 0 || pass >= (int32_t)plan->passes.size()) return fail(SPINF_E_INVALID, "bad pass index");
+    if (!plan->passes[pass].dev.block || !plan->d_err) return fail(SPINF_E_INVALID, "pass not uploaded");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != plan->device) return fail(SPINF_E_INVALID, "pass uploaded to another device");
+    return SPINF_OK;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+}  // namespace spinf
+
+using namespace spinf;
+
+extern "C" spinf_status spinf_plan_upload(spinf_plan* plan, int32_t pass, spinf_stream stream) {
+    if (!plan) return fail(SPINF_E_INVALID, "plan is NULL");
+    if (pass < 0 || pass >= (int32_t)plan->passes.size()) return fail(SPINF_E_INVALID, "bad pass index");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (plan->device >= 0 && plan->device != dev) return fail(SPINF_E_INVALID, "plan belongs to another device");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!plan->d_err) {
+        e = cudaMalloc(&plan->d_err, sizeof(int32_t));
+        if (e != cudaSuccess) return fail(SPINF_E_NOMEM, "device allocation of the error word failed");
+        e = cudaMemsetAsync(plan->d_err, 0, sizeof(int32_t), s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+        plan->device = dev;
+    }
+    Pass& P = plan->passes[pass];
+    if (P.dev.block) return SPINF_OK;
+    const std::vector<int32_t>* arrays[] = {&P.end,      &P.pos,        &P.tile_ptr, &P.tile_kv,  &P.slot_row,
+                                           &P.gather_m, &P.gather_tok, &P.row_gptr, &P.row_glist};
+    int32_t** dst[] = {&P.dev.end,      &P.dev.pos,        &P.dev.tile_ptr, &P.dev.tile_kv,  &P.dev.slot_row,
+                       &P.dev.gather_m, &P.dev.gather_tok, &P.dev.row_gptr, &P.dev.row_glist};
+    const int n = sizeof(arrays) / sizeof(arrays[0]);
+    size_t off[16], total = 0;
+    for (int i = 0; i < n; ++i) {
+        off[i] = total;
+        total += (arrays[i]->size() * sizeof(int32_t) + 255) / 256 * 256;
+    }
+    void* block = nullptr;
+    e = cudaMalloc(&block, total > 0 ? total : 256);
+    if (e != cudaSuccess) return fail(SPINF_E_NOMEM, "device allocation of pass descriptors failed");
+    // one staging buffer so the copy is a single transfer
+    std::vector<unsigned char> host(total, 0);
+    for (int i = 0; i < n; ++i) {
+        if (!arrays[i]->empty()) std::memcpy(host.data() + off[i], arrays[i]->data(), arrays[i]->size() * 4);
+        *dst[i] = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(block) + off[i]);
+    }
+    if (total) {
+        e = cudaMemcpyAsync(block, host.data(), total, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);   // the staging buffer dies here
+        if (e != cudaSuccess) {
+            cudaFree(block);
+            return cuda_fail(e, "descriptor upload");
+        }
+    }
+    P.dev.block = block;
+    return SPINF_OK;
+}
+
+extern "C" spinf_status spinf_device_status(const spinf_plan* plan, spinf_stream stream) {
+    if (!plan) return fail(SPINF_E_INVALID, "plan is NULL");
+    if (!plan->d_err) return SPINF_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, plan->d_err, sizeof word, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "device status");
+    if (word == 0) return SPINF_OK;
+    e = cudaMemsetAsync(plan->d_err, 0, sizeof(int32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "device status reset");
+    if (word == SPINF_E_DEVICE_TIMEOUT) return fail(SPINF_E_DEVICE_TIMEOUT, "a device wait timed out");
+    return fail(SPINF_E_DEVICE_CHECK, "a device-side check failed");
+}
+
+extern "C" void spinf_plan_free(spinf_plan* plan) {
+    if (!plan) return;
+    for (Pass& P : plan->passes)
+        if (P.dev.block) cudaFree(P.dev.block);
+    if (plan->d_err) cudaFree(plan->d_err);
+    delete plan;
+}
+
+extern "C" const char* spinf_fingerprint(void) {
+    return "spinf-gb300 k1=branch_attention/tcgen05 q128xkv128 input-anchored fp32-acc bf16-p;"
+           " k2=score/tcgen05 m128xv256xk64 fp32-acc lse-chunk256 fixed-order;"
+           " fp8=e4m3 row-absmax/448 rne-sat; sm_103a";
+}

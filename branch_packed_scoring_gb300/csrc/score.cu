@@ -1,0 +1,406 @@
+// Slot scoring: the lm head at the slot rows of a pass, a full-vocabulary
+// log-sum-exp, and the log-probabilities of the option tokens.
+//
+// The method ("spinf-serve 0.1.1", PyPI page, "What it does"): the engine
+// returns each option's log-probability at the place where the template ends;
+// the man page (PARAMETERS, --lm-head) makes fp32 output of the lm head the
+// default.  Logits are never written out: each CTA of the main kernel reduces
+// its 128 x 256 logit tile to a (max, sum of exp) pair per row and picks out the
+// option-token logits that fall in the tile.
+//
+//   K4 gather_rows   hidden[slot_row[m]] -> Hs[m]   (e4m3: per-row absmax/448
+//                    scale, fp32 division, round-to-nearest-even, saturating)
+//   K2 score_main    persistent; z = Hs W^T on tcgen05 (128 slot rows x 256 vocab
+//                    rows per tile, fp32 in TMEM, double-buffered), then per row
+//                    an online (max, sum exp) over the tile in column order
+//   K3 combine       per row, merge the vocabulary chunks in ascending order ->
+//                    lse; token_lp = z_gathered - lse
+//
+// Every reduction runs in a fixed order that depends only on the row's own
+// values and the vocabulary size, so a row's results do not depend on M or on
+// which other rows share its tile.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "runtime.h"
+
+namespace spinf {
+namespace {
+
+using namespace dev;
+
+constexpr int kBM = 128;   // slot rows per tile (MMA M, TMEM lanes)
+constexpr int kBN = 256;   // vocabulary rows per tile (MMA N, TMEM columns)
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * 128;
+constexpr int kBBytes = kBN * 128;
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kScoreThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum { FULL0 = 0, EMPTY0 = kStages, ACC_FULL0 = 2 * kStages, ACC_EMPTY0 = 2 * kStages + 2, N_SBARS = 2 * kStages + 4 };
+
+constexpr int kSmemBars = kStages * kStageBytes;
+constexpr int kSmemHolder = kSmemBars + N_SBARS * 8;
+constexpr int kScoreSmem = kSmemHolder + 16 + 1024;
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct ScoreLayout {
+    int M, M_pad, G, n_vt, n_st;
+    size_t hs, sa, part, zg, total;
+};
+
+ScoreLayout score_layout(const Pass& P, int vocab, int d_model, int w_dtype) {
+    ScoreLayout s;
+    s.M = (int)P.slot_row.size();
+    s.G = (int)P.gather_tok.size();
+    s.M_pad = std::max(1, (s.M + kBM - 1) / kBM) * kBM;
+    s.n_st = s.M_pad / kBM;
+    s.n_vt = (vocab + kBN - 1) / kBN;
+    const size_t elt = w_dtype == SPINF_DTYPE_E4M3 ? 1 : 2;
+    s.hs = 0;
+    s.sa = s.hs + align256((size_t)s.M_pad * d_model * elt);
+    s.part = s.sa + align256((size_t)s.M_pad * 4);
+    s.zg = s.part + align256((size_t)s.M_pad * s.n_vt * 8);
+    s.total = s.zg + align256((size_t)std::max(s.G, 1) * 4);
+    return s;
+}
+
+// ---------------------------------------------------------------- K4
+template <bool FP8>
+__global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* __restrict__ hidden,
+                                                          const int32_t* __restrict__ slot_row, int M, int D,
+                                                          void* __restrict__ out, float* __restrict__ s_act) {
+    const int m = blockIdx.x;
+    const int nv = D / 8;   // 8 elements per vector
+    const uint4* src = m < M ? reinterpret_cast<const uint4*>(hidden + (size_t)slot_row[m] * D) : nullptr;
+    if (!FP8) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + (size_t)m * D);
+        for (int i = threadIdx.x; i < nv; i += blockDim.x) dst[i] = src ? src[i] : make_uint4(0, 0, 0, 0);
+        return;
+    }
+    __shared__ float red[8];
+    float amax = 0.f;
+    if (src)
+        for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+            uint4 u = src[i];
+            const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float2 f = __bfloat1622float2(b[j]);
+                amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+        }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float a = 0.f;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) a = fmaxf(a, red[w]);
+        red[0] = a > 0.f ? __fdiv_rn(a, 448.f) : 1.f;
+        s_act[m] = red[0];
+    }
+    __syncthreads();
+    const float sc = red[0];
+    uint2* dst = reinterpret_cast<uint2*>(static_cast<uint8_t*>(out) + (size_t)m * D);
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+        uint32_t w[2] = {0u, 0u};
+        if (src) {
+            uint4 u = src[i];
+            const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float2 f = __bfloat1622float2(b[j]);
+                float2 q = make_float2(__fdiv_rn(f.x, sc), __fdiv_rn(f.y, sc));
+                __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(q, __NV_SATFINITE, __NV_E4M3);
+                w[j >> 1] |= static_cast<uint32_t>(c) << ((j & 1) * 16);
+            }
+        }
+        dst[i] = make_uint2(w[0], w[1]);
+    }
+}
+
+// ---------------------------------------------------------------- K2
+template <bool FP8>
+__global__ void __launch_bounds__(kScoreThreads, 1)
+    score_main_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
+                      const float* __restrict__ s_act, const float* __restrict__ s_w, float2* __restrict__ part,
+                      float* __restrict__ zg, const int32_t* __restrict__ row_gptr,
+                      const int32_t* __restrict__ row_glist, const int32_t* __restrict__ gather_tok, int M, int V,
+                      int n_kb, int n_st, int n_vt, int* __restrict__ err) {
+    constexpr int kPerMma = FP8 ? 32 : 16;           // K elements of one MMA instruction
+    constexpr int kMmaPerStage = (FP8 ? 128 : 64) / kPerMma;
+    constexpr int kBK = FP8 ? 128 : 64;              // K elements per 128-byte row
+    constexpr uint32_t idesc = FP8 ? idesc_e4m3(kBM, kBN) : idesc_bf16(kBM, kBN, false, false);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemBars);
+    uint32_t* holder = reinterpret_cast<uint32_t*>(smem + kSmemHolder);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = n_vt * n_st;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars[FULL0 + s], 1);
+            mbar_init(&bars[EMPTY0 + s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&bars[ACC_FULL0 + a], 1);
+            mbar_init(&bars[ACC_EMPTY0 + a], 128);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(holder, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_h);
+            tma_prefetch_desc(&tm_w);
+            uint32_t it = 0;
+            for (int u = blockIdx.x; u < total; u += gridDim.x) {
+                const int vt = u / n_st, st = u % n_st;
+                for (int kb = 0; kb < n_kb; ++kb, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1;
+                    mbar_wait(&bars[EMPTY0 + s], ph ^ 1, err);
+                    uint8_t* sa = smem + s * kStageBytes;
+                    mbar_arrive_expect_tx(&bars[FULL0 + s], kStageBytes);
+                    tma_load_2d(sa, &tm_h, &bars[FULL0 + s], kb * kBK, st * kBM);
+                    tma_load_2d(sa + kABytes, &tm_w, &bars[FULL0 + s], kb * kBK, vt * kBN);
+                }
+            }
+            // our last copies have landed before the CTA may retire
+            for (uint32_t i = it > (uint32_t)kStages ? it - kStages : 0; i < it; ++i)
+                mbar_wait(&bars[FULL0 + i % kStages], (i / kStages) & 1, err);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t it = 0, tcount = 0;
+            for (int u = blockIdx.x; u < total; u += gridDim.x, ++tcount) {
+                const int acc = tcount & 1;
+                const uint32_t aph = (tcount >> 1) & 1;
+                mbar_wait(&bars[ACC_EMPTY0 + acc], aph ^ 1, err);
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + acc * kBN;
+                for (int kb = 0; kb < n_kb; ++kb, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1;
+                    mbar_wait(&bars[FULL0 + s], ph, err);
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(smem + s * kStageBytes);
+                    const uint32_t b_base = a_base + kABytes;
+#pragma unroll
+                    for (int kk = 0; kk < kMmaPerStage; ++kk) {
+                        const uint64_t da = sdesc_sw128(a_base + kk * 32, 16, 1024);
+                        const uint64_t db = sdesc_sw128(b_base + kk * 32, 16, 1024);
+                        if (FP8) mma_f8_ss(d_tmem, da, db, idesc, (kb | kk) != 0);
+                        else mma_f16_ss(d_tmem, da, db, idesc, (kb | kk) != 0);
+                    }
+                    mma_commit(&bars[EMPTY0 + s]);
+                }
+                mma_commit(&bars[ACC_FULL0 + acc]);
+            }
+        }
+    } else {
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        uint32_t tcount = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x, ++tcount) {
+            const int vt = u / n_st, st = u % n_st;
+            const int acc = tcount & 1;
+            const uint32_t aph = (tcount >> 1) & 1;
+            const int m = st * kBM + r;
+            const bool valid = m < M;
+            const int v0 = vt * kBN;
+            int gc = 0, ge = 0;
+            if (valid) {   // first gather of this row whose token is >= v0 (tokens sorted per row)
+                int lo = row_gptr[m], hi = row_gptr[m + 1];
+                ge = hi;
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (gather_tok[row_glist[mid]] < v0) lo = mid + 1; else hi = mid;
+                }
+                gc = lo;
+            }
+            const float sa = (FP8 && valid) ? s_act[m] : 1.f;
+            mbar_wait(&bars[ACC_FULL0 + acc], aph, err);
+            tc_fence_after();
+            float mx = -INFINITY, sum = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t rr[32];
+                tmem_ld32(tmem + lane_off + acc * kBN + c * 32, rr);
+                const int vc = v0 + c * 32;
+                float z[32];
+                float cmax = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float x = __uint_as_float(rr[i]);
+                    if (FP8) x = (x * (vc + i < V ? s_w[vc + i] : 0.f)) * sa;
+                    z[i] = vc + i < V ? x : -INFINITY;
+                    cmax = fmaxf(cmax, z[i]);
+                }
+                const float nm = fmaxf(mx, cmax);
+                float add = 0.f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) add += fast_exp2((z[i] - nm) * kLog2e);
+                sum = (mx == -INFINITY ? 0.f : sum * fast_exp2((mx - nm) * kLog2e)) + add;
+                mx = nm;
+                while (gc < ge) {
+                    const int g = row_glist[gc];
+                    const int tk = gather_tok[g];
+                    if (tk >= vc + 32) break;
+                    const int idx = tk - vc;
+                    float val = z[0];
+#pragma unroll
+                    for (int i = 1; i < 32; ++i) val = (i == idx) ? z[i] : val;
+                    zg[g] = val;
+                    ++gc;
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars[ACC_EMPTY0 + acc]);
+            if (valid) part[(size_t)m * n_vt + vt] = make_float2(mx, sum);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------- K3
+__device__ __forceinline__ float2 lse_merge(float2 a, float2 b) {
+    if (a.x == -INFINITY) return b;
+    if (b.x == -INFINITY) return a;
+    const float m = fmaxf(a.x, b.x);
+    return make_float2(m, a.y * expf(a.x - m) + b.y * expf(b.x - m));
+}
+
+__global__ void __launch_bounds__(128) score_combine_kernel(const float2* __restrict__ part,
+                                                            const float* __restrict__ zg,
+                                                            const int32_t* __restrict__ row_gptr,
+                                                            const int32_t* __restrict__ row_glist, int M, int n_vt,
+                                                            float* __restrict__ row_lse,
+                                                            float* __restrict__ token_lp) {
+    const int m = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (m >= M) return;
+    float2 acc = make_float2(-INFINITY, 0.f);
+    for (int vt = lane; vt < n_vt; vt += 32) acc = lse_merge(acc, part[(size_t)m * n_vt + vt]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        float2 other;
+        other.x = __shfl_xor_sync(0xffffffffu, acc.x, o);
+        other.y = __shfl_xor_sync(0xffffffffu, acc.y, o);
+        acc = (lane & o) ? lse_merge(other, acc) : lse_merge(acc, other);
+    }
+    const float lse = acc.x + logf(acc.y);
+    if (lane == 0) row_lse[m] = lse;
+    for (int i = row_gptr[m] + lane; i < row_gptr[m + 1]; i += 32) {
+        const int g = row_glist[i];
+        token_lp[g] = zg[g] - lse;
+    }
+}
+
+template <bool FP8>
+spinf_status launch_score(const Pass& P, const ScoreLayout& L, const void* hidden, const void* w, const float* w_scale,
+                          int D, int V, float* row_lse, float* token_lp, uint8_t* ws, int* err, cudaStream_t stream) {
+    void* hs = ws + L.hs;
+    float* sa = reinterpret_cast<float*>(ws + L.sa);
+    float2* part = reinterpret_cast<float2*>(ws + L.part);
+    float* zg = reinterpret_cast<float*>(ws + L.zg);
+    gather_rows_kernel<FP8><<<L.M_pad, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(hidden), P.dev.slot_row,
+                                                         L.M, D, hs, sa);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+
+    CUtensorMap th, tw;
+    const uint64_t elt = FP8 ? 1 : 2;
+    const uint64_t dh[2] = {(uint64_t)D, (uint64_t)L.M_pad};
+    const uint64_t dw[2] = {(uint64_t)D, (uint64_t)V};
+    const uint64_t st[1] = {(uint64_t)D * elt};
+    const uint32_t bh[2] = {FP8 ? 128u : 64u, (uint32_t)kBM};
+    const uint32_t bw[2] = {FP8 ? 128u : 64u, (uint32_t)kBN};
+    const CUtensorMapDataType dt = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    spinf_status s;
+    if ((s = make_tmap(&th, dt, 2, hs, dh, st, bh, CU_TENSOR_MAP_SWIZZLE_128B))) return s;
+    if ((s = make_tmap(&tw, dt, 2, w, dw, st, bw, CU_TENSOR_MAP_SWIZZLE_128B))) return s;
+    static bool configured = false;
+    if (!configured) {
+        e = cudaFuncSetAttribute(score_main_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(score)");
+        configured = true;
+    }
+    const int kbk = FP8 ? 128 : 64;
+    const int n_kb = (D + kbk - 1) / kbk;
+    const int total = L.n_vt * L.n_st;
+    const int grid = std::min(total, sm_count());
+    score_main_kernel<FP8><<<grid, kScoreThreads, kScoreSmem, stream>>>(
+        th, tw, sa, w_scale, part, zg, P.dev.row_gptr, P.dev.row_glist, P.dev.gather_tok, L.M, V, n_kb, L.n_st,
+        L.n_vt, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "score launch");
+    score_combine_kernel<<<(L.M + 3) / 4, 128, 0, stream>>>(part, zg, P.dev.row_gptr, P.dev.row_glist, L.M, L.n_vt,
+                                                           row_lse, token_lp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    return SPINF_OK;
+}
+
+}  // namespace
+}  // namespace spinf
+
+using namespace spinf;
+
+extern "C" size_t spinf_score_workspace_bytes(const spinf_plan* plan, int32_t pass, int32_t vocab, int32_t d_model,
+                                              int32_t w_dtype) {
+    if (!plan || pass < 0 || pass >= (int32_t)plan->passes.size() || vocab <= 0 || d_model <= 0) return 0;
+    return score_layout(plan->passes[pass], vocab, d_model, w_dtype).total;
+}
+
+extern "C" spinf_status spinf_score(const spinf_plan* plan, int32_t pass, const void* hidden, const void* w,
+                                    const float* w_scale, int32_t w_dtype, int32_t d_model, int32_t vocab,
+                                    float* row_lse, float* token_lp, void* workspace, size_t workspace_bytes,
+                                    spinf_stream stream) {
+    spinf_status st = ensure_device_ready(plan, pass);
+    if (st) return st;
+    if (w_dtype != SPINF_DTYPE_BF16 && w_dtype != SPINF_DTYPE_E4M3) return fail(SPINF_E_UNSUPPORTED, "w_dtype");
+    if (d_model <= 0 || d_model % 16) return fail(SPINF_E_UNSUPPORTED, "d_model must be a positive multiple of 16");
+    if (vocab <= 0) return fail(SPINF_E_INVALID, "vocab must be positive");
+    const Pass& P = plan->passes[pass];
+    if (P.slot_row.empty()) return SPINF_OK;
+    if (!hidden || !w || !row_lse || !token_lp || !workspace) return fail(SPINF_E_INVALID, "NULL buffer");
+    if (w_dtype == SPINF_DTYPE_E4M3 && !w_scale) return fail(SPINF_E_INVALID, "e4m3 weights need w_scale");
+    for (const void* p : {hidden, w, (const void*)workspace})
+        if (reinterpret_cast<uintptr_t>(p) & 15) return fail(SPINF_E_INVALID, "buffer not 16-byte aligned");
+    for (int32_t t : P.gather_tok)
+        if (t < 0 || t >= vocab) return fail(SPINF_E_INVALID, "option token outside the vocabulary");
+    const ScoreLayout L = score_layout(P, vocab, d_model, w_dtype);
+    if (workspace_bytes < L.total) return fail(SPINF_E_NOMEM, "workspace too small");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (w_dtype == SPINF_DTYPE_E4M3)
+        return launch_score<true>(P, L, hidden, w, w_scale, d_model, vocab, row_lse, token_lp, ws, plan->d_err, s);
+    return launch_score<false>(P, L, hidden, w, nullptr, d_model, vocab, row_lse, token_lp, ws, plan->d_err, s);
+}

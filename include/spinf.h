@@ -1,0 +1,253 @@
+/*
+ * spinf.h -- C ABI of the branch-packed scoring hot path for GB300 (sm_103a).
+ *
+ * The problem, as the pages state it ("spinf-serve 0.1.1", PyPI project page,
+ * sections "What it does" and "Install and run"): a request holds contents and,
+ * per content, questions; a question is a template that ends where the answer
+ * goes ({?}) with the options to score there.  The engine reads each content
+ * once, lays every question out as a branch of the same packed pass, and
+ * returns per option its log-probability, its probability renormalised over the
+ * options (p), the same on empty content (the floor), and the mass that went
+ * outside the options (residual).  There is no tokenizer here: every text is
+ * given as token ids.
+ *
+ * The path, in call order:
+ *   spinf_pack_plan         host: inputs -> packed passes of <= token_budget rows
+ *   spinf_plan_upload       host -> device: one pass's descriptors
+ *   spinf_branch_attention  device: tree-masked GQA attention over the pass
+ *   spinf_score             device: lm-head at slot rows, full-vocabulary
+ *                           log-sum-exp, option-token log-probabilities
+ *   spinf_collect           host: per option lp, p, residual and floor
+ *
+ * Conventions for every call:
+ *   - Status codes only; nothing throws across this boundary.  The text of the
+ *     last error of the calling thread is returned by spinf_last_error().
+ *   - The caller owns every device buffer (passed as raw device pointers) and
+ *     every host array it passes in.  The planner copies what it keeps.  A plan
+ *     owns its host tables and the device copies made by spinf_plan_upload
+ *     until spinf_plan_free.
+ *   - Device calls are asynchronous on the given stream (NULL = legacy default
+ *     stream) and allocate nothing: scratch memory is the caller's workspace.
+ *   - Device buffers must be 16-byte aligned; all device tensors are dense,
+ *     row-major, tokens the slowest dimension.
+ *   - There is no CPU fallback: a device call on a machine without an sm_103a
+ *     GPU returns SPINF_E_CUDA.
+ */
+#ifndef SPINF_H
+#define SPINF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                      /* the same type as cudaStream_t */
+typedef struct CUstream_st* spinf_stream;
+
+typedef enum {
+    SPINF_OK = 0,
+    SPINF_E_INVALID = 1,        /* malformed request or argument */
+    SPINF_E_LIMIT = 2,          /* a limit of spinf_plan_opts exceeded */
+    SPINF_E_NOMEM = 3,          /* host or device allocation failed, or workspace too small */
+    SPINF_E_CUDA = 4,           /* a CUDA runtime call failed (no device, launch error, ...) */
+    SPINF_E_UNSUPPORTED = 5,    /* a shape or dtype this build does not implement */
+    SPINF_E_DEVICE_TIMEOUT = 6, /* a bounded device wait ran out (reported by spinf_device_status) */
+    SPINF_E_DEVICE_CHECK = 7    /* a device-side descriptor check failed */
+} spinf_status;
+
+enum { SPINF_DTYPE_BF16 = 0, SPINF_DTYPE_E4M3 = 1 };
+
+/* A token-id array (host memory). */
+typedef struct {
+    const int32_t* ids;
+    int32_t n;
+} spinf_tokens;
+
+/* One scored question: template tokens up to and including the last token
+ * before the {?} slot, and the options to score there (1 to max_option_tokens
+ * tokens each; no duplicates). */
+typedef struct {
+    spinf_tokens tmpl;
+    const spinf_tokens* options;
+    int32_t n_options;
+} spinf_question;
+
+/* One input: a content (may be empty) read once, and its questions. */
+typedef struct {
+    spinf_tokens content;
+    const spinf_question* questions;
+    int32_t n_questions;
+} spinf_input;
+
+/* Planner options.  Defaults (spinf_plan_opts_default) follow the man page
+ * ("spinf-serve", linuxcommandlibrary, PARAMETERS): --token-budget 16384,
+ * --max-content-tokens 4096, --max-query-tokens 256, --max-options 1000,
+ * --max-option-tokens 5, --max-prompts-per-input 10000.  --max-tokens has no
+ * printed default; it defaults to 2,000,000 (the per-request processed-token
+ * limit on the same page). */
+typedef struct {
+    int32_t token_budget;           /* rows per packed pass */
+    int32_t max_tokens;             /* largest single input: content plus its laid-out questions */
+    int32_t max_content_tokens;
+    int32_t max_query_tokens;       /* template length */
+    int32_t max_options;
+    int32_t max_option_tokens;
+    int32_t max_prompts_per_input;  /* questions per input */
+    int32_t floors;                 /* 1: add one floor input per distinct (template, options) */
+    spinf_tokens floor_prefix;      /* content of every floor input (default: empty) */
+    int32_t vocab;                  /* > 0: reject token ids outside [0, vocab) */
+} spinf_plan_opts;
+
+typedef struct spinf_plan spinf_plan;
+
+/* Read-only host views of one packed pass (valid until spinf_plan_free). */
+typedef struct {
+    int32_t T;          /* rows holding tokens */
+    int32_t T_pad;      /* T rounded up to a multiple of 128; device tensors have T_pad rows */
+    int32_t n_qtiles;   /* T_pad / 128 */
+    int32_t n_sched;    /* entries of tile_kv */
+    int32_t M;          /* scoring rows (slots and option-prefix rows) */
+    int32_t G;          /* gathered option tokens */
+    int32_t n_units;    /* laid-out inputs (chunks of user inputs, then floors) */
+    const int32_t* tok;       /* [T_pad] token id per row (0 on pad rows) */
+    const int32_t* parent;    /* [T_pad] previous row on the root path, -1 at a root or pad */
+    const int32_t* pos;       /* [T_pad] depth on the root path (position id) */
+    const int32_t* end;       /* [T_pad] key k is visible to rows k <= q < end[k] */
+    const int32_t* anchor;    /* [T_pad] first row of the row's input (pad: itself) */
+    const int32_t* tile_ptr;  /* [n_qtiles + 1] CSR of the KV-tile schedule */
+    const int32_t* tile_kv;   /* [n_sched] first row of each scheduled 128-row KV tile */
+    const int32_t* slot_row;  /* [M] packed row of each scoring row, ascending */
+    const int32_t* gather_m;  /* [G] scoring-row index of each option token */
+    const int32_t* gather_tok;/* [G] option token id; order: unit, question, option, token */
+    const int32_t* unit_start;/* [n_units + 1] first row of each unit, then T */
+    const int32_t* unit_source;/* [n_units] user input index, or -1 for a floor */
+} spinf_pass_info;
+
+/* Per-option and per-question results, caller-owned host arrays (fp64).
+ * Options are numbered input by input, question by question, in the order
+ * given; questions likewise.  Floor fields are NaN when floors are off. */
+typedef struct {
+    double* option_lp;        /* [n_options] sum of the option's token log-probabilities */
+    double* option_p;         /* [n_options] exp(lp) renormalised over the question's options */
+    double* option_floor_lp;  /* [n_options] the same question on empty content */
+    double* option_floor_p;   /* [n_options] */
+    double* residual;         /* [n_questions] 1 - sum of exp(lp) over the options */
+    double* floor_residual;   /* [n_questions] */
+} spinf_result;
+
+/* Fill *opts with the defaults above. */
+void spinf_plan_opts_default(spinf_plan_opts* opts);
+
+/* Lay inputs out in packed passes ("spinf-serve 0.1.1" PyPI page, "What it does"
+ * and "Speed and scale": the content once, every question a branch that sees its
+ * own content and itself, never a sibling or another input; passes of 16k rows).
+ *
+ * Layout of one input: content rows, then per question its template rows, then
+ * the rows of its option trie (proper prefixes of options, pre-order, children
+ * in order of first insertion).  Floors (one per distinct question) follow all
+ * user inputs.  Inputs larger than token_budget are split into chunks (the full
+ * content plus a greedy run of questions); packing is next-fit.  The KV-tile
+ * schedule of each 128-row Q tile lists, per intersecting input in layout order,
+ * the 128-row KV tiles anchored at that input's first row that hold a key
+ * visible to some row of the tile.
+ *
+ * inputs: host array of n_inputs (n_inputs >= 0); opts: NULL for defaults.
+ * On success *out owns a new plan.  Errors: SPINF_E_INVALID (empty template,
+ * empty or duplicate option, token id out of range, empty input),
+ * SPINF_E_LIMIT (a limit exceeded, or a content and one question do not fit a
+ * pass), SPINF_E_NOMEM. */
+spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inputs,
+                             const spinf_plan_opts* opts, spinf_plan** out);
+
+int32_t spinf_plan_num_passes(const spinf_plan* plan);
+
+/* Host views of pass `pass`.  SPINF_E_INVALID for a bad index. */
+spinf_status spinf_plan_pass_info(const spinf_plan* plan, int32_t pass, spinf_pass_info* out);
+
+/* Number of user questions and options over the whole request (sizes of spinf_result). */
+spinf_status spinf_plan_counts(const spinf_plan* plan, int64_t* n_questions, int64_t* n_options);
+
+/* Copy pass `pass`'s descriptors to the current device (allocated once per pass
+ * and kept by the plan; later calls are no-ops).  Synchronous with respect to the
+ * host for the allocation; the copies are enqueued on `stream`. */
+spinf_status spinf_plan_upload(spinf_plan* plan, int32_t pass, spinf_stream stream);
+
+/* Tree-masked GQA attention over one packed pass (spec: the branch
+ * attention kernel; pages: "spinf-serve 0.1.1", "Speed and scale").
+ *
+ * For every row q < T and query head h (kv head g = h * Hkv / Hq):
+ *   o[q,h,:] = sum_k softmax_k(scale * q[q,h,:] . k[k,g,:]) v[k,g,:]
+ * over the keys k visible to q: k <= q < end[k], and, when window > 0,
+ * pos[q] - pos[k] < window.  Pad rows (q >= T) are written as zeros.
+ *
+ * q, o: device [T_pad, Hq, d_head] bf16; k, v: device [T_pad, Hkv, d_head] bf16.
+ * d_head in {64, 128, 256}; Hq a multiple of Hkv; scale <= 0 means 1/sqrt(d_head).
+ * Accumulation is fp32.  Key tiles are anchored at each input's first row and
+ * visited in a fixed order, so a row's output is bit-identical whatever else is
+ * packed in the pass.  The pass must have been uploaded.
+ * Errors: SPINF_E_INVALID (pointers, alignment, not uploaded),
+ * SPINF_E_UNSUPPORTED (d_head), SPINF_E_CUDA (launch). */
+spinf_status spinf_branch_attention(const spinf_plan* plan, int32_t pass,
+                                    const void* q, const void* k, const void* v, void* o,
+                                    int32_t n_q_heads, int32_t n_kv_heads, int32_t d_head,
+                                    float scale, int32_t window, spinf_stream stream);
+
+/* Bytes of device workspace spinf_score needs for this pass and shape. */
+size_t spinf_score_workspace_bytes(const spinf_plan* plan, int32_t pass,
+                                   int32_t vocab, int32_t d_model, int32_t w_dtype);
+
+/* Slot scoring ("spinf-serve 0.1.1", "What it does"; man page, --lm-head f32out).
+ *
+ * For every scoring row m (packed row slot_row[m]):
+ *   z[m, v]    = hidden[slot_row[m], :] . w[v, :]                       (fp32 accumulate)
+ *   row_lse[m] = log sum_v exp(z[m, v])        over the whole vocabulary
+ *   token_lp[g]= z[gather_m[g], gather_tok[g]] - row_lse[gather_m[g]]
+ * Logits never leave the chip.  With w_dtype SPINF_DTYPE_E4M3 the weights are
+ * e4m3 codes with one fp32 scale per vocabulary row (w_scale[V]), the hidden
+ * row is quantised to e4m3 with scale absmax/448 (fp32 division, round to
+ * nearest even, saturating), and z = scale_row * w_scale[v] * (codes . codes).
+ *
+ * hidden: device [T_pad, d_model] bf16; w: device [vocab, d_model] bf16 or e4m3;
+ * w_scale: device [vocab] fp32 (NULL for bf16); row_lse: device [M] fp32;
+ * token_lp: device [G] fp32; workspace: device, >= spinf_score_workspace_bytes.
+ * d_model a multiple of 16.  The vocabulary is reduced in a fixed chunk order,
+ * so results do not depend on M or on the other rows of the pass.
+ * Errors: SPINF_E_INVALID, SPINF_E_NOMEM (workspace too small),
+ * SPINF_E_UNSUPPORTED (d_model, dtype), SPINF_E_CUDA. */
+spinf_status spinf_score(const spinf_plan* plan, int32_t pass,
+                         const void* hidden, const void* w, const float* w_scale, int32_t w_dtype,
+                         int32_t d_model, int32_t vocab,
+                         float* row_lse, float* token_lp,
+                         void* workspace, size_t workspace_bytes, spinf_stream stream);
+
+/* Per option lp, p, residual and floor (host, fp64), from each pass's token
+ * log-probabilities copied to the host (token_lp_per_pass[p] has G_p floats).
+ * Option lp = sum of its token lps in token order; p_o = exp(lp_o - m) /
+ * sum_j exp(lp_j - m), m = max_j lp_j; residual = -expm1(logsumexp_j lp_j)
+ * ("spinf-serve" news repost, English part: the refund example's response). */
+spinf_status spinf_collect(const spinf_plan* plan, const float* const* token_lp_per_pass,
+                           const spinf_result* out);
+
+/* Wait for `stream`, then report the plan's device error word:
+ * SPINF_OK, SPINF_E_DEVICE_TIMEOUT or SPINF_E_DEVICE_CHECK (the word is cleared). */
+spinf_status spinf_device_status(const spinf_plan* plan, spinf_stream stream);
+
+void spinf_plan_free(spinf_plan* plan);
+
+/* Kernel version, tile configuration and precision: two results are bitwise
+ * comparable only when their fingerprints match ("spinf-serve 0.1.1",
+ * "What it does": system_fingerprint). */
+const char* spinf_fingerprint(void);
+
+const char* spinf_status_string(spinf_status status);
+
+/* Text of the calling thread's last error ("" if none). */
+const char* spinf_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPINF_H */

@@ -25,3 +25,13 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def spinf():
+    """The product binding with its library built (nvcc cross-compiles without a GPU)."""
+    from branch_packed_scoring_gb300 import build as _build
+    _build.build()
+    import branch_packed_scoring_gb300 as b
+    b.lib()
+    return b

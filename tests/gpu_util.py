@@ -1,0 +1,47 @@
+"""Shared helpers of the GPU parity tests (inputs from synth, layouts from the oracle)."""
+import numpy as np
+import torch
+
+from oracle import plan as op
+from synth import values as sv
+
+
+def pass_values(lay, shape, device="cuda", hidden_rows=True):
+    """bf16 q, k, v (and hidden at the scoring rows) of one laid-out pass, on the device."""
+    keys = sv.path_keys(lay.tok, lay.parent, lay.T)
+    q, k, v = sv.qkv(keys, lay.T_pad, shape.n_q_heads, shape.n_kv_heads, shape.d_head)
+    h = None
+    if hidden_rows:
+        h = sv.hidden(keys, lay.T_pad, shape.d_model, rows=lay.slot_row.tolist())
+    dev = lambda t: None if t is None else t.to(device)  # noqa: E731
+    return dev(q), dev(k), dev(v), dev(h)
+
+
+def run_attention(spinf, plan, p, q, k, v, shape, window=0):
+    o = torch.full_like(q, float("nan"))
+    plan.upload(p)
+    spinf.branch_attention(plan, p, q, k, v, o, shape.n_q_heads, shape.n_kv_heads, shape.d_head, window=window)
+    plan.device_status()
+    torch.cuda.synchronize()
+    return o
+
+
+def run_score(spinf, plan, p, hidden, w, w_scale, w_dtype, shape):
+    info = plan.pass_info(p)
+    plan.upload(p)
+    nbytes = spinf.score_workspace_bytes(plan, p, shape.vocab, shape.d_model, w_dtype)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    lse = torch.full((max(info.M, 1),), float("nan"), device="cuda")
+    tlp = torch.full((max(info.G, 1),), float("nan"), device="cuda")
+    spinf.score(plan, p, hidden, w, w_scale, w_dtype, shape.d_model, shape.vocab, lse, tlp, ws)
+    plan.device_status()
+    torch.cuda.synchronize()
+    return lse[:info.M].cpu().numpy(), tlp[:info.G].cpu().numpy(), ws
+
+
+def oracle_plan(inputs, **kw):
+    return op.plan(inputs, **kw)
+
+
+def real_rows(lay):
+    return np.arange(lay.T)

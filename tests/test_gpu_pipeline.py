@@ -1,0 +1,37 @@
+"""End to end on the GPU: plan, attention, scoring and collect against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import oracle_plan, pass_values, run_attention, run_score
+from oracle import collect as oc
+from oracle import score as osc
+from synth import values as sv
+from synth import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_pipeline(spinf):
+    inputs, shape = wl.tiny(), wl.TINY
+    P = oracle_plan(inputs, vocab=shape.vocab)
+    plan = spinf.Plan(inputs, vocab=shape.vocab)
+    w = sv.lm_head(shape.vocab, shape.d_model)
+    gpu_lp, ref_lp = [], []
+    for p, lay in enumerate(P.passes):
+        q, k, v, h = pass_values(lay, shape)
+        run_attention(spinf, plan, p, q, k, v, shape)
+        _, tlp, _ = run_score(spinf, plan, p, h, w.cuda(), None, spinf.DTYPE_BF16, shape)
+        gpu_lp.append(tlp)
+        ref_lp.append(osc.score_rows(h.float().cpu().numpy()[lay.slot_row], lay.gather_m, lay.gather_tok,
+                                     w=w.float().numpy())[1])
+    ours = plan.collect(gpu_lp)
+    ref = oc.collect(P, ref_lp)
+    flat_lp = np.concatenate([r["lp"] for per_q in ref for r in per_q])
+    flat_p = np.concatenate([r["p"] for per_q in ref for r in per_q])
+    flat_fp = np.concatenate([r["floor_p"] for per_q in ref for r in per_q])
+    res = np.array([r["residual"] for per_q in ref for r in per_q])
+    assert np.abs(ours["option_lp"] - flat_lp).max() <= 4e-3
+    assert np.abs(ours["option_p"] - flat_p).max() <= 4e-3
+    assert np.abs(ours["option_floor_p"] - flat_fp).max() <= 4e-3
+    assert np.abs(ours["residual"] - res).max() <= 4e-3

@@ -1,0 +1,134 @@
+"""The product planner (C++, through the C ABI) against the oracle planner: bit-exact layouts.
+
+Covers every workload shape, splits of long inputs, multi-token option tries,
+fuzzed requests, the error statuses, and the collect step.
+"""
+import numpy as np
+import pytest
+
+from oracle import collect as oc
+from oracle import plan as op
+from synth import workloads as wl
+
+FIELDS = ("tok", "parent", "pos", "end", "anchor", "tile_ptr", "tile_kv", "slot_row", "gather_m", "gather_tok")
+
+
+def _compare(spinf, inputs, **opts):
+    P = op.plan(inputs, **opts)
+    Q = spinf.Plan(inputs, **opts)
+    assert Q.num_passes == len(P.passes)
+    for p, lay in enumerate(P.passes):
+        info = Q.pass_info(p)
+        assert (info.T, info.T_pad) == (lay.T, lay.T_pad)
+        for f in FIELDS:
+            a, b = getattr(info, f), getattr(lay, f)
+            assert np.array_equal(a, b), (p, f)
+        assert info.unit_start.tolist() == [u.start for u in lay.units] + [lay.T]
+        assert info.unit_source.tolist() == [u.source for u in lay.units]
+    return P, Q
+
+
+@pytest.mark.parametrize("name", ["tiny", "wikinews", "moderation", "stress"])
+def test_workloads_bit_exact(spinf, name):
+    f, shape = wl.WORKLOADS[name]
+    _compare(spinf, f(), vocab=shape.vocab)
+
+
+def test_invariance_packing_bit_exact(spinf):
+    inputs, _ = wl.invariance_packing(1)
+    _compare(spinf, inputs, vocab=262144)
+    _compare(spinf, [wl.invariance_target()], vocab=262144)
+
+
+@pytest.mark.parametrize("budget", [256, 700, 2048])
+def test_splits_and_tries(spinf, budget):
+    inputs = wl.stress(n_questions=60, content_tokens=150, vocab=1000)
+    _compare(spinf, inputs, token_budget=budget, vocab=1000)
+    _compare(spinf, inputs, token_budget=budget, floors=False, floor_prefix=[1, 2])
+    _compare(spinf, inputs, token_budget=budget, floor_prefix=[5, 6, 7])
+
+
+def test_fuzzed_requests(spinf):
+    g = np.random.default_rng(7)
+    for trial in range(40):
+        inputs = []
+        for _ in range(int(g.integers(1, 12))):
+            content = g.integers(0, 50, size=int(g.integers(0, 300))).tolist()
+            qs = []
+            for _ in range(int(g.integers(0 if content else 1, 6))):
+                opts, seen = [], set()
+                for _ in range(int(g.integers(1, 5))):
+                    o = tuple(g.integers(0, 6, size=int(g.integers(1, 4))).tolist())
+                    if o not in seen:
+                        seen.add(o)
+                        opts.append(list(o))
+                qs.append((g.integers(0, 50, size=int(g.integers(1, 20))).tolist(), opts))
+            if not content and not qs:
+                content = [1]
+            inputs.append((content, qs))
+        budget = int(g.choice([128, 300, 1000, 16384]))
+        try:
+            op.plan(inputs, token_budget=budget)
+        except op.PlanError as e:
+            with pytest.raises(spinf.SpinfError) as ee:
+                spinf.Plan(inputs, token_budget=budget)
+            assert ee.value.status_name == e.status
+            continue
+        _compare(spinf, inputs, token_budget=budget)
+
+
+@pytest.mark.parametrize("bad", [
+    [([1], [([], [[1]])])],
+    [([1], [([1], [])])],
+    [([1], [([1], [[]])])],
+    [([1], [([1], [[2], [2]])])],
+    [([], [])],
+    [([1] * 4097, [([1], [[2]])])],
+    [([1], [([1] * 257, [[2]])])],
+    [([1], [([1], [[i] for i in range(1001)])])],
+    [([1], [([1], [[2] * 6])])],
+    [([1], [([1], [[2000]])])],
+])
+def test_error_statuses_match(spinf, bad):
+    with pytest.raises(op.PlanError) as e:
+        op.plan(bad, vocab=1024)
+    with pytest.raises(spinf.SpinfError) as ee:
+        spinf.Plan(bad, vocab=1024)
+    assert ee.value.status_name == e.value.status
+
+
+def test_split_error_status(spinf):
+    bad = [([1] * 8, [([1, 2, 3], [[1]])])]
+    with pytest.raises(spinf.SpinfError) as ee:
+        spinf.Plan(bad, token_budget=10)
+    assert ee.value.status_name == "LIMIT"
+
+
+def test_empty_request(spinf):
+    Q = spinf.Plan([])
+    assert Q.num_passes == 0 and Q.counts() == (0, 0)
+    assert Q.collect([])["option_lp"].shape == (0,)
+
+
+def test_collect_matches_oracle_collect(spinf):
+    inputs = wl.stress(n_questions=50, content_tokens=100, vocab=1000)
+    inputs = inputs + wl.tiny(vocab=1000)
+    P, Q = _compare(spinf, inputs, token_budget=600)
+    g = np.random.default_rng(3)
+    tlps = [(-g.random(len(lay.gather_tok)) * 5).astype(np.float32) for lay in P.passes]
+    ours = Q.collect(tlps)
+    ref = oc.collect(P, tlps)
+    flat = {k: [] for k in ("lp", "p", "floor_lp", "floor_p")}
+    res, fres = [], []
+    for per_q in ref:
+        for r in per_q:
+            for k in flat:
+                flat[k].extend(r[k])
+            res.append(r["residual"])
+            fres.append(r["floor_residual"])
+    np.testing.assert_allclose(ours["option_lp"], flat["lp"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ours["option_p"], flat["p"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ours["option_floor_lp"], flat["floor_lp"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ours["option_floor_p"], flat["floor_p"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ours["residual"], res, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ours["floor_residual"], fres, rtol=0, atol=1e-12)
