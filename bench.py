@@ -1,0 +1,506 @@
+#!/usr/bin/env python
+"""Throughput of the branch-packed scoring hot path on one or more GB300s.
+
+Workload (default): the Wikinews-shaped job -- 24 contents of 400-540 tokens
+sharing 56 two-option questions of 8-16 tokens, plus one floor per question,
+packed into two 16384-token passes; Gemma-12B-class attention (16 query heads,
+8 kv heads, d_head 256) and lm head (d_model 3840, vocabulary 262144, bf16).
+Inputs are synthetic (seeded) and resident in HBM before the timed region.
+
+One step = the whole job: per pass, tree-masked attention (one layer) and slot
+scoring (gather, lm head with full-vocabulary log-sum-exp, option log-probs),
+then the token log-probs to the host and the per-option collect.  The layout
+(planner output) is part of the resident input; the planner, the descriptor
+upload and every host<->device copy of the activations are inside the ``e2e``
+number, measured through the public API with host buffers.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores on a bounded
+sample of the same job and extrapolates to the whole job.
+
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "packed tokens/s and scored questions/s per GB300; % of tensor/HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _peak_value(d, *names):
+    for n in names:
+        for k, v in d.items():
+            if k == n and isinstance(v, (int, float)):
+                return float(v)
+    for n in names:   # nested forms, e.g. {"bf16_tflops": {"value": ...}}
+        v = d.get(n)
+        if isinstance(v, dict):
+            for kk in ("value", "median", "max"):
+                if isinstance(v.get(kk), (int, float)):
+                    return float(v[kk])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def max_over_ranks(ms, world, device):
+    """The slowest rank's step time (the only collective of the replica path)."""
+    if world <= 1:
+        return ms
+    import torch
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(tokens_per_replica, world, ms):
+    """Whole-job throughput: every rank runs its own replica of the job (weak scaling)."""
+    return world * tokens_per_replica / (ms * 1e-3)
+
+
+def build_job(workload, device, spinf, sv, wl, w_dtype):
+    f, shape = wl.WORKLOADS[workload]
+    inputs = f()
+    plan = spinf.Plan(inputs, vocab=shape.vocab)
+    passes = []
+    for p in range(plan.num_passes):
+        info = plan.pass_info(p)
+        keys = sv.path_keys(info.tok, info.parent, info.T)
+        q, k, v = sv.qkv(keys, info.T_pad, shape.n_q_heads, shape.n_kv_heads, shape.d_head)
+        h = sv.hidden(keys, info.T_pad, shape.d_model, rows=info.slot_row.tolist())
+        passes.append({"info": info, "host": (q, k, v, h)})
+    w = sv.lm_head(shape.vocab, shape.d_model, device=device)
+    w_scale = None
+    if w_dtype == spinf.DTYPE_E4M3:
+        w, w_scale = sv.e4m3_rows(w)
+    return inputs, shape, plan, passes, w, w_scale
+
+
+def work_counts(inputs, plan, passes, shape):
+    """Tokens, user questions, unmasked attention pairs and scoring FLOPs of the job."""
+    import numpy as np
+
+    tokens = sum(p["info"].T for p in passes)
+    questions = sum(len(qs) for _, qs in inputs)
+    pairs = 0
+    flops_score = 0
+    for p in passes:
+        info = p["info"]
+        T = info.T
+        end = info.end[:T].astype(np.int64)
+        pairs += int((end - np.arange(T)).sum())     # key k is seen by rows [k, end[k])
+        flops_score += 2 * info.M * shape.vocab * shape.d_model
+    flops_attn = 4 * shape.d_head * shape.n_q_heads * pairs
+    bytes_attn = sum(p["info"].T for p in passes) * (2 * shape.n_q_heads + 2 * shape.n_kv_heads) * shape.d_head * 2
+    return tokens, questions, pairs, flops_attn, bytes_attn, flops_score
+
+
+def run_ours(args, rank, world):
+    import numpy as np
+    import torch
+
+    import branch_packed_scoring_gb300 as spinf
+    from synth import values as sv
+    from synth import workloads as wl
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w_dtype = spinf.DTYPE_E4M3 if args.fp8 else spinf.DTYPE_BF16
+    inputs, shape, plan, passes, w, w_scale = build_job(args.workload, dev, spinf, sv, wl, w_dtype)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for pi, p in enumerate(passes):
+            info = p["info"]
+            q, k, v, h = (t.to(dev) for t in p["host"])
+            p["dev"] = (q, k, v, h)
+            p["o"] = torch.empty_like(q)
+            plan.upload(pi, stream)
+            nbytes = spinf.score_workspace_bytes(plan, pi, shape.vocab, shape.d_model, w_dtype)
+            p["ws"] = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            p["lse"] = torch.empty(max(info.M, 1), device=dev)
+            p["tlp"] = torch.empty(max(info.G, 1), device=dev)
+            p["tlp_host"] = torch.empty(max(info.G, 1), dtype=torch.float32, pin_memory=True)
+    stream.synchronize()
+    tokens, questions, pairs, flops_attn, bytes_attn, flops_score = work_counts(inputs, plan, passes, shape)
+
+    ev = {"attn": [], "score": []}
+
+    def step(record=False):
+        for pi, p in enumerate(passes):
+            q, k, v, h = p["dev"]
+            if record:
+                a0, a1, s1 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                a0.record(stream)
+            spinf.branch_attention(plan, pi, q, k, v, p["o"], shape.n_q_heads, shape.n_kv_heads, shape.d_head,
+                                   stream=stream)
+            if record:
+                a1.record(stream)
+            spinf.score(plan, pi, h, w, w_scale, w_dtype, shape.d_model, shape.vocab, p["lse"], p["tlp"], p["ws"],
+                        stream=stream)
+            if record:
+                s1.record(stream)
+                ev["attn"].append((a0, a1))
+                ev["score"].append((a1, s1))
+            p["tlp_host"].copy_(p["tlp"], non_blocking=True)
+        stream.synchronize()
+        return plan.collect([p["tlp_host"][:p["info"].G].numpy() for p in passes])
+
+    for _ in range(args.warmup):
+        step()
+    plan.device_status(stream)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        res = step(record=True)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end) / args.steps
+    plan.device_status(stream)
+    assert np.isfinite(res["option_lp"]).all()
+    ms = max_over_ranks(ms, world, dev)
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["attn"]) * len(passes)
+    score_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["score"]) * len(passes)
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev) if not args.no_e2e else None
+
+    peaks, peak_src = _peaks()
+    bf16_peak = _peak_value(peaks, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"]
+    hbm_peak = _peak_value(peaks, "hbm_gbs") or FALLBACK_PEAKS["hbm_gbs"]
+    mma_peak = bf16_peak * (2.0 if args.fp8 else 1.0)
+    score_tflops = flops_score / (score_ms * 1e-3) / 1e12
+    attn_tflops = flops_attn / (attn_ms * 1e-3) / 1e12
+    attn_gbs = bytes_attn / (attn_ms * 1e-3) / 1e9
+    out = {
+        "metric": METRIC,
+        "value": replica_value(tokens, world, ms),
+        "unit": "packed tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if not args.fp8 else "e4m3",
+        "data": "synthetic",
+        "scored_questions_per_s": world * questions / (ms * 1e-3),
+        "config": {"workload": f"{args.workload}: {len(inputs)} contents, {questions} questions, "
+                               f"{len(passes)} passes of <=16384 tokens ({tokens} tokens)",
+                   "attention": f"Hq={shape.n_q_heads} Hkv={shape.n_kv_heads} d_head={shape.d_head} (1 layer)",
+                   "lm_head": f"d_model={shape.d_model} vocab={shape.vocab} "
+                              f"{'e4m3 per-row scaled' if args.fp8 else 'bf16'}, fp32 logits",
+                   "l2": "inputs larger than L2 (per pass q/k/v/o ~0.4 GB, lm head 2 GB)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "value_covers": "attention + scoring per pass, token-lp D2H, collect; layout resident"},
+        "roofline": {"kernel": "spinf_score (gather + tcgen05 lm head + lse + combine)", "bound": "tensor",
+                     "achieved": score_tflops, "peak": mma_peak, "unit": "TFLOP/s",
+                     "frac": score_tflops / mma_peak, "traffic": None,
+                     "peak_source": f"{peak_src} {'bf16_tflops_sustained' if peak_src == 'measured' else ''}".strip()},
+        "roofline_attention": {"kernel": "spinf_branch_attention", "tensor_tflops_unmasked": attn_tflops,
+                               "tensor_frac": attn_tflops / bf16_peak, "hbm_gbs": attn_gbs,
+                               "hbm_frac": attn_gbs / hbm_peak, "unmasked_pairs": pairs},
+        "kernel_ms_per_step": {"attention": attn_ms, "score": score_ms},
+        "clocks": clk,
+        "gpu_launches": 4 * len(passes) * args.steps,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args, inputs, shape, plan, passes, w, w_scale, budget_s=args.cpu_seconds)
+    return out
+
+
+def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
+    """Same job through the public API from pinned host buffers: plan, upload, H2D, kernels, D2H, collect."""
+    import torch
+
+    host = []
+    for p in passes:
+        host.append(tuple(t.pin_memory() for t in p["host"]))
+    stream = torch.cuda.Stream()
+    dbufs = [tuple(torch.empty_like(t, device=dev) for t in hp) for hp in host]
+    obufs = [torch.empty_like(db[0]) for db in dbufs]
+    h2d = sum(t.numel() * t.element_size() for hp in host for t in hp)
+
+    def step():
+        plan = spinf.Plan(inputs, vocab=shape.vocab)
+        outs = []
+        for pi in range(plan.num_passes):
+            info = plan.pass_info(pi)
+            plan.upload(pi, stream)
+            with torch.cuda.stream(stream):
+                for src, dst in zip(host[pi], dbufs[pi]):
+                    dst.copy_(src, non_blocking=True)
+                q, k, v, h = dbufs[pi]
+                spinf.branch_attention(plan, pi, q, k, v, obufs[pi], shape.n_q_heads, shape.n_kv_heads,
+                                       shape.d_head, stream=stream)
+                ws = torch.empty(spinf.score_workspace_bytes(plan, pi, shape.vocab, shape.d_model, w_dtype),
+                                 dtype=torch.uint8, device=dev)
+                lse = torch.empty(max(info.M, 1), device=dev)
+                tlp = torch.empty(max(info.G, 1), device=dev)
+                spinf.score(plan, pi, h, w, w_scale, w_dtype, shape.d_model, shape.vocab, lse, tlp, ws,
+                            stream=stream)
+                th = torch.empty(max(info.G, 1), dtype=torch.float32, pin_memory=True)
+                th.copy_(tlp, non_blocking=True)
+                outs.append((th, info.G))
+        stream.synchronize()
+        res = plan.collect([th[:G].numpy() for th, G in outs])
+        plan.close()
+        return res, sum(G for _, G in outs) * 4
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, args.steps // 2)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        _, d2h = step()
+    torch.cuda.synchronize()
+    ms = (time.perf_counter() - t0) * 1e3 / n
+    tokens = sum(p["info"].T for p in passes)
+    return {"value": tokens / (ms * 1e-3), "unit": "packed tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "covers": "marshal + plan + upload + H2D q/k/v/hidden + kernels + D2H token lps + collect"}
+
+
+def cpu_baseline(args, inputs, shape, plan, passes, w, w_scale, budget_s=20.0):
+    """The fp64 oracle on the host cores on a bounded sample, extrapolated to the whole job."""
+    import numpy as np
+
+    from oracle import attention as oa
+    from oracle import plan as op
+    from oracle import score as osc
+
+    t0 = time.perf_counter()
+    P = op.plan(inputs, vocab=shape.vocab)
+    t_plan = time.perf_counter() - t0
+    lay = P.passes[0]
+    q, k, v, h = (t.float().numpy() for t in passes[0]["host"])
+    g = np.random.default_rng(0)
+    # attention: time a row sample
+    rows = g.choice(lay.T, size=min(lay.T, 96), replace=False)
+    t0 = time.perf_counter()
+    oa.attention_rows(lay, q, k, v, shape.n_q_heads, shape.n_kv_heads, rows)
+    t_attn_row = (time.perf_counter() - t0) / len(rows)
+    # scoring: two sample sizes give the per-row cost and the fixed cost of reading the lm head
+    hs = h[lay.slot_row]
+    gm, gt = lay.gather_m, lay.gather_tok
+    if w_scale is None:
+        wkw = {"w": _BF16Rows(w.cpu())}
+    else:
+        wkw = {"w_codes": w.cpu().numpy(), "w_scale": w_scale.cpu().numpy()}
+
+    def score_sample(n_rows):
+        sel = np.isin(gm, np.arange(n_rows))
+        t1 = time.perf_counter()
+        osc.score_rows(hs[:n_rows], gm[sel], gt[sel], **wkw)
+        return time.perf_counter() - t1
+
+    s1, s2 = 8, 24
+    ta = score_sample(s1)
+    tb = score_sample(s2)
+    per_row = max((tb - ta) / (s2 - s1), 1e-9)
+    fixed = max(ta - per_row * s1, 0.0)
+    total_rows = sum(p["info"].M for p in passes)
+    tokens = sum(p["info"].T for p in passes)
+    job_s = t_plan + t_attn_row * tokens + fixed * len(passes) + per_row * total_rows
+    return {"value": tokens / job_s, "unit": "packed tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"oracle planner on the whole job; attention on {len(rows)} rows of pass 0 (all heads); "
+                      f"scoring on {s1} and {s2} slot rows of pass 0 (full vocabulary); extrapolated to "
+                      f"{tokens} tokens and {total_rows} scoring rows",
+            "job_seconds_estimate": job_s}
+
+
+class _BF16Rows:
+    """Lazy fp64 view of a bf16 torch matrix, row slices converted on demand (bounded host memory)."""
+
+    def __init__(self, t):
+        self.t = t
+        self.shape = tuple(t.shape)
+
+    def __getitem__(self, sl):
+        return self.t[sl].float().numpy()
+
+
+def run_reference(args):
+    """--impl reference: the oracle, as it stands, on the host cores; one bounded sample per step."""
+    import torch  # noqa: F401  (bf16 rounding of the inputs)
+
+    import branch_packed_scoring_gb300 as spinf  # noqa: F401  (not used on this arm)
+    from synth import values as sv
+    from synth import workloads as wl
+    from oracle import attention as oa
+    from oracle import collect as oc
+    from oracle import plan as op
+    from oracle import score as osc
+    import numpy as np
+
+    f, shape = wl.WORKLOADS[args.workload]
+    inputs = f()
+    P = op.plan(inputs, vocab=shape.vocab)
+    lay = P.passes[0]
+    keys = sv.path_keys(lay.tok, lay.parent, lay.T)
+    q, k, v = (t.float().numpy() for t in sv.qkv(keys, lay.T_pad, shape.n_q_heads, shape.n_kv_heads, shape.d_head))
+    h = sv.hidden(keys, lay.T_pad, shape.d_model, rows=lay.slot_row.tolist()).float().numpy()
+    w = _BF16Rows(sv.lm_head(shape.vocab, shape.d_model, device="cpu") if shape.vocab * shape.d_model < (1 << 28)
+                  else _cpu_lm_head(shape))
+    tokens = sum(p.T for p in P.passes)
+    rows_total = sum(len(p.slot_row) for p in P.passes)
+    g = np.random.default_rng(0)
+    n_attn, n_score = 24, 4
+
+    def sample_step():
+        t0 = time.perf_counter()
+        op.plan(inputs, vocab=shape.vocab)
+        t_plan = time.perf_counter() - t0
+        rows = g.choice(lay.T, size=n_attn, replace=False)
+        t0 = time.perf_counter()
+        oa.attention_rows(lay, q, k, v, shape.n_q_heads, shape.n_kv_heads, rows)
+        t_attn = (time.perf_counter() - t0) / n_attn
+        ms = g.choice(len(lay.slot_row), size=n_score, replace=False)
+        sel = np.isin(lay.gather_m, ms)
+        remap = {m: i for i, m in enumerate(ms)}
+        t0 = time.perf_counter()
+        _, lp = osc.score_rows(h[lay.slot_row[ms]], np.array([remap[m] for m in lay.gather_m[sel]]),
+                               lay.gather_tok[sel], w=w)
+        t_score = (time.perf_counter() - t0) / n_score
+        oc.option_stats(lp[:2])
+        return t_plan + t_attn * tokens + t_score * rows_total
+
+    for _ in range(args.warmup):
+        sample_step()
+    est = [sample_step() for _ in range(args.steps)]
+    job_s = statistics.mean(est)
+    value = tokens / job_s
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "packed tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": job_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {len(inputs)} contents, {sum(len(x) for _, x in inputs)} "
+                               f"questions, {len(P.passes)} passes ({tokens} tokens)"},
+        "cpu_baseline": {"kind": "oracle", "cores": os.cpu_count(), "value": value, "unit": "packed tokens/s",
+                         "sample": f"per step: planner on the whole job, attention on {n_attn} rows, scoring on "
+                                   f"{n_score} slot rows (full vocabulary), extrapolated to the whole job"},
+        "e2e": {"value": value, "unit": "packed tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def _cpu_lm_head(shape):
+    import torch
+
+    g = torch.Generator().manual_seed(0x1E4D)
+    return (torch.randn(shape.vocab, shape.d_model, generator=g) / math.sqrt(shape.d_model)).to(torch.bfloat16)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="wikinews", choices=["wikinews", "moderation", "stress"])
+    ap.add_argument("--fp8", action="store_true", help="e4m3 lm head with per-row scales")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    import torch
+
+    if world > 1:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        torch.distributed.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    out = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -56,7 +56,7 @@ _P = ctypes.POINTER(ctypes.c_int32)
 
 class _PassInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("T", "T_pad", "n_qtiles", "n_sched", "M", "G", "n_units")] + \
-               [(n, _P) for n in ("tok", "parent", "pos", "end", "anchor", "tile_ptr", "tile_kv", "slot_row",
+               [(n, _P) for n in ("tok", "parent", "pos", "end", "anchor", "tile_ptr", "tile_kv", "tile_len", "slot_row",
                                   "gather_m", "gather_tok", "unit_start", "unit_source")]
 
 
@@ -162,6 +162,7 @@ class PassInfo:
     anchor: np.ndarray
     tile_ptr: np.ndarray
     tile_kv: np.ndarray
+    tile_len: np.ndarray
     slot_row: np.ndarray
     gather_m: np.ndarray
     gather_tok: np.ndarray
@@ -171,48 +172,49 @@ class PassInfo:
 
 def _marshal(inputs):
     """Lay the request out as the header's structs in numpy buffers (kept alive by the caller)."""
-    ids = []
-    n_q = sum(len(q) for _, q in inputs)
-    n_o = sum(len(opts) for _, q in inputs for _, opts in q)
-    inp = np.zeros(len(inputs), dtype=_INP)
-    que = np.zeros(max(n_q, 1), dtype=_QUE)
-    tok = np.zeros(max(n_o, 1), dtype=_TOK)
-    off = 0
-    spans_c, spans_t, spans_o = [], [], []
-    qi = oi = 0
-    for i, (content, questions) in enumerate(inputs):
-        spans_c.append((off, len(content)))
-        ids.append(np.asarray(content, dtype=np.int32).ravel())
-        off += len(content)
-        inp[i]["questions"] = qi
-        inp[i]["n_questions"] = len(questions)
+    ids, c_off, c_n, nq, t_off, t_n, no, o_off, o_n = [], [], [], [], [], [], [], [], []
+    pos = 0
+    for content, questions in inputs:
+        c_off.append(pos)
+        c_n.append(len(content))
+        ids.extend(content)
+        pos += len(content)
+        nq.append(len(questions))
         for template, options in questions:
-            spans_t.append((qi, off, len(template)))
-            ids.append(np.asarray(template, dtype=np.int32).ravel())
-            off += len(template)
-            que[qi]["options"] = oi
-            que[qi]["n_options"] = len(options)
+            t_off.append(pos)
+            t_n.append(len(template))
+            ids.extend(template)
+            pos += len(template)
+            no.append(len(options))
             for opt in options:
-                spans_o.append((oi, off, len(opt)))
-                ids.append(np.asarray(opt, dtype=np.int32).ravel())
-                off += len(opt)
-                oi += 1
-            qi += 1
-    flat = np.concatenate(ids) if ids else np.zeros(1, dtype=np.int32)
-    flat = np.ascontiguousarray(flat, dtype=np.int32)
-    base = flat.ctypes.data
-    qbase, obase = que.ctypes.data, tok.ctypes.data
-    for i, (o, n) in enumerate(spans_c):
-        inp[i]["content_ids"] = base + 4 * o if n else 0
-        inp[i]["content_n"] = n
-        inp[i]["questions"] = qbase + que.itemsize * int(inp[i]["questions"])
-    for q, o, n in spans_t:
-        que[q]["tmpl_ids"] = base + 4 * o
-        que[q]["tmpl_n"] = n
-        que[q]["options"] = obase + tok.itemsize * int(que[q]["options"])
-    for k, o, n in spans_o:
-        tok[k]["ids"] = base + 4 * o
-        tok[k]["n"] = n
+                o_off.append(pos)
+                o_n.append(len(opt))
+                ids.extend(opt)
+                pos += len(opt)
+    flat = np.array(ids, dtype=np.int32) if ids else np.zeros(1, dtype=np.int32)
+    base = np.uint64(flat.ctypes.data)
+    four = np.uint64(4)
+    tok = np.zeros(max(len(o_off), 1), dtype=_TOK)
+    que = np.zeros(max(len(t_off), 1), dtype=_QUE)
+    inp = np.zeros(len(inputs), dtype=_INP)
+    if o_off:
+        tok["ids"][:len(o_off)] = base + four * np.asarray(o_off, dtype=np.uint64)
+        tok["n"][:len(o_n)] = o_n
+    if t_off:
+        nt = len(t_off)
+        que["tmpl_ids"][:nt] = base + four * np.asarray(t_off, dtype=np.uint64)
+        que["tmpl_n"][:nt] = t_n
+        first_opt = np.concatenate([[0], np.cumsum(no)[:-1]]).astype(np.uint64)
+        que["options"][:nt] = np.uint64(tok.ctypes.data) + np.uint64(_TOK.itemsize) * first_opt
+        que["n_options"][:nt] = no
+    if len(inputs):
+        c_n = np.asarray(c_n, dtype=np.int64)
+        inp["content_ids"] = np.where(c_n > 0, base + four * np.asarray(c_off, dtype=np.uint64), np.uint64(0))
+        inp["content_n"] = c_n
+        first_q = np.concatenate([[0], np.cumsum(nq)[:-1]]).astype(np.uint64)
+        inp["questions"] = np.where(np.asarray(nq) > 0, np.uint64(que.ctypes.data) +
+                                    np.uint64(_QUE.itemsize) * first_q, np.uint64(0))
+        inp["n_questions"] = nq
     return inp, (flat, que, tok)
 
 
@@ -262,7 +264,7 @@ class Plan:
             T=info.T, T_pad=info.T_pad, n_qtiles=info.n_qtiles, n_sched=info.n_sched, M=info.M, G=info.G,
             n_units=info.n_units, tok=arr(info.tok, info.T_pad), parent=arr(info.parent, info.T_pad),
             pos=arr(info.pos, info.T_pad), end=arr(info.end, info.T_pad), anchor=arr(info.anchor, info.T_pad),
-            tile_ptr=arr(info.tile_ptr, info.n_qtiles + 1), tile_kv=arr(info.tile_kv, info.n_sched),
+            tile_ptr=arr(info.tile_ptr, info.n_qtiles + 1), tile_kv=arr(info.tile_kv, info.n_sched), tile_len=arr(info.tile_len, info.n_sched),
             slot_row=arr(info.slot_row, info.M), gather_m=arr(info.gather_m, info.G),
             gather_tok=arr(info.gather_tok, info.G), unit_start=arr(info.unit_start, info.n_units + 1),
             unit_source=arr(info.unit_source, info.n_units))

@@ -69,7 +69,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     branch_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
                             const int32_t* __restrict__ end, const int32_t* __restrict__ pos,
-                            const int32_t* __restrict__ tile_ptr, const int32_t* __restrict__ tile_kv, int T,
+                            const int32_t* __restrict__ tile_ptr, const int32_t* __restrict__ tile_kv,
+                            const int32_t* __restrict__ tile_len, int T,
                             int T_pad, int Hq, int Hkv, float scale_log2, int window, int* __restrict__ err) {
     using L = AttnSmem<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -177,10 +178,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int kv0 = tile_kv[s0 + j];
             int32_t* e_buf = kv_end + (j & 1) * 128;
             int32_t* p_buf = kv_pos + (j & 1) * 128;
-            {
+            {   // keys past the tile's own input are read through that input's tiles: never here
                 const int k = kv0 + t;
-                e_buf[t] = k < T_pad ? end[k] : -1;
-                p_buf[t] = k < T_pad ? pos[k] : 0;
+                const bool own = t < tile_len[s0 + j];
+                e_buf[t] = own ? end[k] : -1;
+                p_buf[t] = own ? pos[k] : 0;
             }
             named_bar_sync(1, 128);
             mbar_wait(&bars[S_FULL], j & 1, err);
@@ -303,7 +305,7 @@ spinf_status launch_attention(const Pass& P, const void* q, const void* k, const
     const float scale_log2 = scale * 1.4426950408889634f;
     dim3 grid(P.T_pad / 128, Hq);
     branch_attention_kernel<D><<<grid, kAttnThreads, smem, stream>>>(
-        tq, tk, tv, static_cast<__nv_bfloat16*>(o), P.dev.end, P.dev.pos, P.dev.tile_ptr, P.dev.tile_kv, P.T,
+        tq, tk, tv, static_cast<__nv_bfloat16*>(o), P.dev.end, P.dev.pos, P.dev.tile_ptr, P.dev.tile_kv, P.dev.tile_len, P.T,
         P.T_pad, Hq, Hkv, scale_log2, window, err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");

@@ -19,6 +19,7 @@ struct PassDevice {
     int32_t* pos = nullptr;        // [T_pad]
     int32_t* tile_ptr = nullptr;   // [n_qtiles + 1]
     int32_t* tile_kv = nullptr;    // [n_sched]
+    int32_t* tile_len = nullptr;   // [n_sched]
     int32_t* slot_row = nullptr;   // [M]
     int32_t* gather_m = nullptr;   // [G]
     int32_t* gather_tok = nullptr; // [G]
@@ -29,7 +30,7 @@ struct PassDevice {
 struct Pass {
     int32_t T = 0, T_pad = 0;
     std::vector<int32_t> tok, parent, pos, end, anchor;
-    std::vector<int32_t> tile_ptr, tile_kv;
+    std::vector<int32_t> tile_ptr, tile_kv, tile_len;
     std::vector<int32_t> slot_row, gather_m, gather_tok;
     std::vector<int32_t> row_gptr, row_glist;
     std::vector<int32_t> unit_start, unit_source;

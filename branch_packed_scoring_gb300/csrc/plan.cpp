@@ -393,7 +393,10 @@ extern "C" spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inp
                         bool any = false;
                         for (int32_t k = kb; k < ke && !any; ++k)
                             any = std::max(k, lo) < std::min(P.end[k], hi);
-                        if (any) P.tile_kv.push_back(kb);
+                        if (any) {
+                            P.tile_kv.push_back(kb);
+                            P.tile_len.push_back(ke - kb);
+                        }
                     }
                 }
                 P.tile_ptr.push_back((int32_t)P.tile_kv.size());
@@ -453,6 +456,7 @@ extern "C" spinf_status spinf_plan_pass_info(const spinf_plan* plan, int32_t pas
     out->anchor = P.anchor.data();
     out->tile_ptr = P.tile_ptr.data();
     out->tile_kv = P.tile_kv.data();
+    out->tile_len = P.tile_len.data();
     out->slot_row = P.slot_row.data();
     out->gather_m = P.gather_m.data();
     out->gather_tok = P.gather_tok.data();

@@ -118,6 +118,7 @@ typedef struct {
     const int32_t* anchor;    /* [T_pad] first row of the row's input (pad: itself) */
     const int32_t* tile_ptr;  /* [n_qtiles + 1] CSR of the KV-tile schedule */
     const int32_t* tile_kv;   /* [n_sched] first row of each scheduled 128-row KV tile */
+    const int32_t* tile_len;  /* [n_sched] keys of that tile that belong to its input (1..128) */
     const int32_t* slot_row;  /* [M] packed row of each scoring row, ascending */
     const int32_t* gather_m;  /* [G] scoring-row index of each option token */
     const int32_t* gather_tok;/* [G] option token id; order: unit, question, option, token */
@@ -151,7 +152,8 @@ void spinf_plan_opts_default(spinf_plan_opts* opts);
  * content plus a greedy run of questions); packing is next-fit.  The KV-tile
  * schedule of each 128-row Q tile lists, per intersecting input in layout order,
  * the 128-row KV tiles anchored at that input's first row that hold a key
- * visible to some row of the tile.
+ * visible to some row of the tile; a tile's keys beyond its input's last row
+ * (tile_len) are not part of it, they are seen through their own input's tiles.
  *
  * inputs: host array of n_inputs (n_inputs >= 0); opts: NULL for defaults.
  * On success *out owns a new plan.  Errors: SPINF_E_INVALID (empty template,

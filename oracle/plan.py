@@ -134,6 +134,7 @@ class PassLayout:
     anchor: np.ndarray
     tile_ptr: np.ndarray
     tile_kv: np.ndarray
+    tile_len: np.ndarray
     slot_row: np.ndarray
     gather_m: np.ndarray
     gather_tok: np.ndarray
@@ -349,10 +350,12 @@ def _layout_pass(units):
         end.append(r + 1)
         anchor.append(r)
     # schedule: per 128-row Q tile, per intersecting unit in layout order, the
-    # unit-anchored KV tiles holding at least one key visible to a row of the tile
+    # unit-anchored KV tiles holding at least one key visible to a row of the tile;
+    # a tile holds only the keys of its own unit (a key past the unit's end belongs
+    # to the next unit and is read through that unit's own tiles)
     n_qt = T_pad // TILE
     tile_ptr = [0]
-    tile_kv = []
+    tile_kv, tile_len = [], []
     for qt in range(n_qt):
         r0, r1 = qt * TILE, (qt + 1) * TILE
         for u in units:
@@ -366,14 +369,16 @@ def _layout_pass(units):
                     hit.update(range(0, (content_hi[q] - 1 - s) // TILE + 1))
                 for k in chain[q]:
                     hit.add((k - s) // TILE)
-            tile_kv.extend(s + TILE * j for j in sorted(hit))
+            for j in sorted(hit):
+                tile_kv.append(s + TILE * j)
+                tile_len.append(min(TILE, e - (s + TILE * j)))   # keys of the tile inside this input
         tile_ptr.append(len(tile_kv))
     rows = sorted(set(gather_rows))
     m_of = {r: m for m, r in enumerate(rows)}
     i32 = lambda a: np.asarray(a, dtype=np.int32)  # noqa: E731
     return PassLayout(
         T=T, T_pad=T_pad, tok=i32(tok), parent=i32(parent), pos=i32(pos), end=i32(end), anchor=i32(anchor),
-        tile_ptr=i32(tile_ptr), tile_kv=i32(tile_kv), slot_row=i32(rows),
+        tile_ptr=i32(tile_ptr), tile_kv=i32(tile_kv), tile_len=i32(tile_len), slot_row=i32(rows),
         gather_m=i32([m_of[r] for r in gather_rows]), gather_tok=i32(gather_tok),
         units=units, questions=records,
         content_lo=i32(content_lo), content_hi=i32(content_hi), chain=chain,

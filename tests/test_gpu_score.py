@@ -99,5 +99,5 @@ def test_scores_do_not_depend_on_other_rows(spinf):
         gs = [g for r in rec for gg in r.option_gather for g in gg]
         ms = sorted({int(lay.gather_m[g]) for g in gs})
         results.append((lse[ms], tlp[gs]))
-    for a, b in results[1:]:
-        assert np.array_equal(a[0], results[0][0]) and np.array_equal(a[1], results[0][1])
+    for lse_i, tlp_i in results[1:]:
+        assert np.array_equal(lse_i, results[0][0]) and np.array_equal(tlp_i, results[0][1])

@@ -35,6 +35,7 @@ def test_single_question_with_floor():
     assert L.gather_tok.tolist() == [30, 31, 30, 31]
     assert L.tile_ptr.tolist() == [0, 2]
     assert L.tile_kv.tolist() == [0, 5]
+    assert L.tile_len.tolist() == [5, 2]
     _check_pads(L)
 
 
@@ -193,6 +194,8 @@ def test_schedule_is_exact():
                     continue
                 js = sorted({(k - s) // 128 for q in rows for k in lay.visible(q)})
                 want += [s + 128 * j for j in js]
+                for j in js:   # every key a row of this unit sees lies inside its unit
+                    assert lay.tile_len[list(lay.tile_kv).index(s + 128 * j)] == min(128, e - s - 128 * j)
             assert sched[qt] == want
 
 

@@ -10,7 +10,8 @@ from oracle import collect as oc
 from oracle import plan as op
 from synth import workloads as wl
 
-FIELDS = ("tok", "parent", "pos", "end", "anchor", "tile_ptr", "tile_kv", "slot_row", "gather_m", "gather_tok")
+FIELDS = ("tok", "parent", "pos", "end", "anchor", "tile_ptr", "tile_kv", "tile_len", "slot_row", "gather_m",
+          "gather_tok")
 
 
 def _compare(spinf, inputs, **opts):
