@@ -468,6 +468,51 @@ def _cpu_lm_head(shape):
     return (torch.randn(shape.vocab, shape.d_model, generator=g) / math.sqrt(shape.d_model)).to(torch.bfloat16)
 
 
+def run_ncu_case(args):
+    """Pass 0 of the workload, one boundary call repeated: the small case for ncu captures."""
+    import torch
+
+    import branch_packed_scoring_gb300 as spinf
+    from synth import values as sv
+    from synth import workloads as wl
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    f, shape = wl.WORKLOADS[args.workload]
+    inputs = f()
+    plan = spinf.Plan(inputs, vocab=shape.vocab)
+    info = plan.pass_info(0)
+    keys = sv.path_keys(info.tok, info.parent, info.T)
+    plan.upload(0)
+    w_dtype = spinf.DTYPE_E4M3 if args.fp8 else spinf.DTYPE_BF16
+    if args.ncu_case == "attention":
+        q, k, v = (t.to(dev) for t in sv.qkv(keys, info.T_pad, shape.n_q_heads, shape.n_kv_heads, shape.d_head))
+        o = torch.empty_like(q)
+
+        def call():
+            spinf.branch_attention(plan, 0, q, k, v, o, shape.n_q_heads, shape.n_kv_heads, shape.d_head,
+                                   window=args.window)
+    else:
+        h = sv.hidden(keys, info.T_pad, shape.d_model, rows=info.slot_row.tolist()).to(dev)
+        w = sv.lm_head(shape.vocab, shape.d_model, device=dev)
+        w_scale = None
+        if args.fp8:
+            w, w_scale = sv.e4m3_rows(w)
+        ws = torch.empty(spinf.score_workspace_bytes(plan, 0, shape.vocab, shape.d_model, w_dtype),
+                         dtype=torch.uint8, device=dev)
+        lse = torch.empty(info.M, device=dev)
+        tlp = torch.empty(info.G, device=dev)
+
+        def call():
+            spinf.score(plan, 0, h, w, w_scale, w_dtype, shape.d_model, shape.vocab, lse, tlp, ws)
+    for _ in range(args.warmup + args.steps):
+        call()
+    torch.cuda.synchronize()
+    plan.device_status()
+    print(json.dumps({"ncu_case": args.ncu_case, "workload": args.workload, "T": info.T, "M": info.M,
+                      "calls": args.warmup + args.steps}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -479,11 +524,17 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--ncu-case", choices=["score", "attention"], default=None,
+                    help="run one boundary call on pass 0 only (small case for profiler captures)")
+    ap.add_argument("--window", type=int, default=0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.ncu_case:
+        run_ncu_case(args)
+        return
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
