@@ -27,7 +27,7 @@ DTYPE_BF16, DTYPE_E4M3 = 0, 1
 SYMBOLS = [
     "spinf_plan_opts_default", "spinf_pack_plan", "spinf_plan_num_passes", "spinf_plan_pass_info",
     "spinf_plan_counts", "spinf_plan_upload", "spinf_branch_attention", "spinf_score_workspace_bytes",
-    "spinf_score", "spinf_collect", "spinf_device_status", "spinf_plan_free", "spinf_fingerprint",
+    "spinf_score", "spinf_score_static", "spinf_collect", "spinf_device_status", "spinf_plan_free", "spinf_fingerprint",
     "spinf_status_string", "spinf_last_error",
 ]
 
@@ -100,6 +100,7 @@ def lib():
     L.spinf_score_workspace_bytes.argtypes = [vp, i32, i32, i32, i32]
     L.spinf_score_workspace_bytes.restype = sz
     L.spinf_score.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.spinf_score_static.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp]
     L.spinf_collect.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(_Result)]
     L.spinf_device_status.argtypes = [vp, vp]
     L.spinf_plan_free.argtypes = [vp]
@@ -109,7 +110,8 @@ def lib():
     L.spinf_status_string.restype = ctypes.c_char_p
     L.spinf_last_error.restype = ctypes.c_char_p
     for name in ("spinf_pack_plan", "spinf_plan_pass_info", "spinf_plan_counts", "spinf_plan_upload",
-                 "spinf_branch_attention", "spinf_score", "spinf_collect", "spinf_device_status"):
+                 "spinf_branch_attention", "spinf_score", "spinf_score_static", "spinf_collect",
+                 "spinf_device_status"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -322,3 +324,9 @@ def score(plan, p, hidden, w, w_scale, w_dtype, d_model, vocab, row_lse, token_l
     _check(lib().spinf_score(plan.handle, p, _ptr(hidden), _ptr(w), _ptr(w_scale), w_dtype, d_model, vocab,
                              _ptr(row_lse), _ptr(token_lp), _ptr(workspace), int(workspace_bytes),
                              _stream(stream)))
+
+
+def score_static(plan, p, hidden, w, w_scale, w_dtype, d_model, vocab, row_lse, token_lp, stream=None):
+    """``spinf_score_static``: scoring with the library's own fixed device scratch (no allocation)."""
+    _check(lib().spinf_score_static(plan.handle, p, _ptr(hidden), _ptr(w), _ptr(w_scale), w_dtype, d_model, vocab,
+                                    _ptr(row_lse), _ptr(token_lp), _stream(stream)))

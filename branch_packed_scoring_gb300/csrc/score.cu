@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -400,6 +401,71 @@ extern "C" spinf_status spinf_score(const spinf_plan* plan, int32_t pass, const 
     if (workspace_bytes < L.total) return fail(SPINF_E_NOMEM, "workspace too small");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (w_dtype == SPINF_DTYPE_E4M3)
+        return launch_score<true>(P, L, hidden, w, w_scale, d_model, vocab, row_lse, token_lp, ws, plan->d_err, s);
+    return launch_score<false>(P, L, hidden, w, nullptr, d_model, vocab, row_lse, token_lp, ws, plan->d_err, s);
+}
+
+// ---------------------------------------------------------------- allocation-free variant
+// For callers that may not allocate device memory: the scratch of the scoring
+// kernels lives in one file-scope device array per GPU.  Host code must not use
+// the array's name as a device address (on the host it only names the symbol);
+// its device address is looked up once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) uint8_t g_score_scratch[SPINF_SCORE_STATIC_SCRATCH_BYTES];
+
+namespace spinf {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of this GPU's scratch array; the first call per device looks it up.
+spinf_status static_scratch(void** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(SPINF_E_UNSUPPORTED, "device index beyond the static scratch table");
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_score_scratch);
+        if (e != cudaSuccess || !p) return cuda_fail(e, "cudaGetSymbolAddress(scoring scratch)");
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return SPINF_OK;
+}
+
+}  // namespace
+}  // namespace spinf
+
+extern "C" spinf_status spinf_score_static(const spinf_plan* plan, int32_t pass, const void* hidden, const void* w,
+                                           const float* w_scale, int32_t w_dtype, int32_t d_model, int32_t vocab,
+                                           float* row_lse, float* token_lp, spinf_stream stream) {
+    spinf_status st = ensure_device_ready(plan, pass);
+    if (st) return st;
+    if (w_dtype != SPINF_DTYPE_BF16 && w_dtype != SPINF_DTYPE_E4M3) return fail(SPINF_E_UNSUPPORTED, "w_dtype");
+    if (d_model <= 0 || d_model % 16) return fail(SPINF_E_UNSUPPORTED, "d_model must be a positive multiple of 16");
+    if (vocab <= 0) return fail(SPINF_E_INVALID, "vocab must be positive");
+    const Pass& P = plan->passes[pass];
+    if (P.slot_row.empty()) return SPINF_OK;
+    const ScoreLayout L = score_layout(P, vocab, d_model, w_dtype);
+    if (L.total > (size_t)SPINF_SCORE_STATIC_SCRATCH_BYTES)
+        return fail(SPINF_E_LIMIT, "this pass needs " + std::to_string(L.total) +
+                                       " bytes of scoring scratch; the static area holds " +
+                                       std::to_string((size_t)SPINF_SCORE_STATIC_SCRATCH_BYTES) +
+                                       " (use spinf_score with a caller workspace)");
+    if (!hidden || !w || !row_lse || !token_lp) return fail(SPINF_E_INVALID, "NULL buffer");
+    if (w_dtype == SPINF_DTYPE_E4M3 && !w_scale) return fail(SPINF_E_INVALID, "e4m3 weights need w_scale");
+    for (const void* p : {hidden, w})
+        if (reinterpret_cast<uintptr_t>(p) & 15) return fail(SPINF_E_INVALID, "buffer not 16-byte aligned");
+    for (int32_t t : P.gather_tok)
+        if (t < 0 || t >= vocab) return fail(SPINF_E_INVALID, "option token outside the vocabulary");
+    void* scratch = nullptr;
+    if ((st = static_scratch(&scratch))) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(scratch);
     if (w_dtype == SPINF_DTYPE_E4M3)
         return launch_score<true>(P, L, hidden, w, w_scale, d_model, vocab, row_lse, token_lp, ws, plan->d_err, s);
     return launch_score<false>(P, L, hidden, w, nullptr, d_model, vocab, row_lse, token_lp, ws, plan->d_err, s);

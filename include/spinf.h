@@ -224,6 +224,35 @@ spinf_status spinf_score(const spinf_plan* plan, int32_t pass,
                          float* row_lse, float* token_lp,
                          void* workspace, size_t workspace_bytes, spinf_stream stream);
 
+/* Size of the device scratch area behind spinf_score_static: 64 MiB, reserved on
+ * every GPU that loads this library, for as long as the process runs. */
+#define SPINF_SCORE_STATIC_SCRATCH_BYTES (64u << 20)
+
+/* spinf_score without a workspace argument, for callers that cannot allocate
+ * device memory: code running where cudaMalloc is off limits (a host that
+ * hands out only pre-planned memory, an allocator hook, a process whose memory
+ * is fixed at start-up) or that must not grow its footprint while serving.
+ * The pages have no counterpart for this call; it is a deployment convenience.
+ *
+ * Same arguments, results and errors as spinf_score, minus workspace and
+ * workspace_bytes.  The scratch is one file-scope device array of
+ * SPINF_SCORE_STATIC_SCRATCH_BYTES per GPU; a pass whose scratch need
+ * (spinf_score_workspace_bytes) exceeds it is rejected with SPINF_E_LIMIT
+ * before anything is launched.  This call allocates nothing (no cudaMalloc,
+ * no cudaFree, no allocating library routine); the pass must already have been
+ * uploaded with spinf_plan_upload.
+ *
+ * The first call on a device looks up the device address of its scratch array
+ * (cudaGetSymbolAddress, with that device current); make that first call before
+ * any stream capture.  Every call on a device shares the one array and leaves
+ * its contents behind; nothing in it has to start at zero (each call writes
+ * every byte it later reads).  Calls whose kernels overlap on the GPU -- two
+ * streams, or two host threads -- race on the array: order them. */
+spinf_status spinf_score_static(const spinf_plan* plan, int32_t pass,
+                                const void* hidden, const void* w, const float* w_scale, int32_t w_dtype,
+                                int32_t d_model, int32_t vocab,
+                                float* row_lse, float* token_lp, spinf_stream stream);
+
 /* Per option lp, p, residual and floor (host, fp64), from each pass's token
  * log-probabilities copied to the host (token_lp_per_pass[p] has G_p floats).
  * Option lp = sum of its token lps in token order; p_o = exp(lp_o - m) /
