@@ -4,23 +4,28 @@
 // scale"): every question is a branch of the same pass; a branch token attends
 // to its own content and causally to its own branch, never to a sibling or to
 // another packed input.  The planner encodes that as: key k is visible to the
-// rows [k, end[k]).
+// rows [k, end[k]), and each scheduled KV tile holds only its own input's keys.
 //
 // One CTA computes one 128-row Q tile of one query head:
 //   warp 0      TMA producer: Q once, then K and V tiles (128 keys x d) in the
 //               order of the tile's schedule
-//   warp 1      TMEM owner and MMA issuer: S = Q K^T (SS form, fp32 in TMEM),
-//               O += P V (P read from TMEM, V from shared memory, MN-major)
-//   warps 2-5   one thread per Q row: mask, online softmax, P (bf16) into TMEM,
-//               rescale O in TMEM when the row maximum grows, final O / l
+//   warp 1      TMEM owner and MMA issuer: S = Q K^T into one of two TMEM
+//               buffers (SS form, fp32), O += P V (P read from TMEM, V MN-major
+//               from shared memory)
+//   warps 2-5   one thread per Q row: mask, online softmax, P (bf16) into TMEM
+//               over its S, rescale O when the row maximum grows, final O / l
+//               staged in shared memory and written by a TMA store
+// With two S buffers the tensor core computes S(j+1) and PV(j-1) while the
+// softmax warps work on tile j.
 //
 // Batch invariance ("What it does": an input's scores are bit-identical alone
 // or packed with thousands of others): KV tiles start at the first row of the
 // input that owns them, so a key always lands in the same MMA column whatever
 // precedes its input in the pass; tiles are visited in a fixed order; a tile
 // with no visible key for a row is an exact no-op for that row (its maximum
-// stays, P is exactly 0 and O is not rescaled).  O starts at zero and is always
-// accumulated, so the first visible tile takes the same path alone or packed.
+// stays, P is exactly 0 and O is multiplied by exactly 1).  O starts at zero and
+// is always accumulated, so the first visible tile takes the same path alone or
+// packed.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -38,40 +43,44 @@ using namespace dev;
 
 constexpr int kAttnThreads = 192;
 constexpr int kBoxBytes = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128-byte swizzled rows)
+constexpr int kSchedSmem = 256;        // schedule entries staged in shared memory (later ones read from global)
 
-enum { Q_FULL = 0, K_FULL, K_EMPTY, V_FULL, V_EMPTY, S_FULL, P_FULL, O_DONE, N_BARS };
+enum { Q_FULL = 0, K_FULL, K_EMPTY, V_FULL, V_EMPTY, S_FULL0, S_FULL1, P_FULL, O_DONE, N_BARS };
 
 template <int D>
 struct AttnSmem {
     static constexpr int kChunks = D / 64;
     static constexpr int kTileBytes = kChunks * kBoxBytes;
-    static constexpr int kQ = 0;
+    static constexpr int kQ = 0;                            // Q tile; stages O for the TMA store at the end
     static constexpr int kK = kQ + kTileBytes;
     static constexpr int kV = kK + kTileBytes;
-    static constexpr int kKvEnd = kV + kTileBytes;        // int32 [2][128]
-    static constexpr int kKvPos = kKvEnd + 2 * 128 * 4;   // int32 [2][128]
-    static constexpr int kBars = kKvPos + 2 * 128 * 4;
+    static constexpr int kKvEnd = kV + kTileBytes;          // int32 [2][128]
+    static constexpr int kKvPos = kKvEnd + 2 * 128 * 4;     // int32 [2][128]
+    static constexpr int kSched = kKvPos + 2 * 128 * 4;     // int2 [kSchedSmem]: (first row, own keys)
+    static constexpr int kBars = kSched + kSchedSmem * 8;
     static constexpr int kHolder = kBars + N_BARS * 8;
     static constexpr int kBytes = kHolder + 16;
-    static constexpr int kAlloc = kBytes + 1024;           // room to align the base to 1024
+    static constexpr int kAlloc = kBytes + 1024;            // room to align the base to 1024
 };
 
-// TMEM columns: S [0,128), P (bf16 pairs) [128,192), O after P.  A CTA owns
-// kTmemCols columns; the shared-memory request caps the CTAs per SM so that
-// co-resident CTAs never wait on each other's TMEM.
-constexpr uint32_t kColS = 0, kColP = 128;
-template <int D> constexpr uint32_t kColO = D <= 64 ? 192 : 256;
-template <int D> constexpr uint32_t kTmemCols = D <= 64 ? 256 : 512;
-template <int D> constexpr int kMinSmem = D <= 64 ? 80 * 1024 : 116 * 1024;   // <= 2 resp. 1 CTA per SM
+// TMEM columns: two S buffers [0,128) and [128,256) -- tile j uses buffer j&1,
+// and its P (bf16 pairs, 64 columns) overwrites the start of that buffer once
+// the softmax has read S -- then O [256, 256 + D).  512 columns, so one CTA per
+// SM (the shared-memory request enforces it and no allocation ever waits).
+constexpr uint32_t kColO = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kMinSmem = 116 * 1024;
+// Log2 headroom of the lazy softmax reference maximum: P values stay <= 2^8.
+constexpr float kRescaleLog2 = 8.f;
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     branch_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                            const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
+                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                             const int32_t* __restrict__ end, const int32_t* __restrict__ pos,
                             const int32_t* __restrict__ tile_ptr, const int32_t* __restrict__ tile_kv,
-                            const int32_t* __restrict__ tile_len, int T,
-                            int T_pad, int Hq, int Hkv, float scale_log2, int window, int* __restrict__ err) {
+                            const int32_t* __restrict__ tile_len, int T, int Hkv, float scale_log2, int window,
+                            int* __restrict__ err) {
     using L = AttnSmem<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -80,27 +89,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint8_t* sV = smem + L::kV;
     int32_t* kv_end = reinterpret_cast<int32_t*>(smem + L::kKvEnd);
     int32_t* kv_pos = reinterpret_cast<int32_t*>(smem + L::kKvPos);
+    int2* sched = reinterpret_cast<int2*>(smem + L::kSched);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
     uint32_t* holder = reinterpret_cast<uint32_t*>(smem + L::kHolder);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qt = blockIdx.x, h = blockIdx.y;
+    const int Hq = gridDim.y;
     const int g = h / (Hq / Hkv);
     const int s0 = tile_ptr[qt];
     const int n = tile_ptr[qt + 1] - s0;
 
+    for (int i = threadIdx.x; i < n && i < kSchedSmem; i += blockDim.x)
+        sched[i] = make_int2(tile_kv[s0 + i], tile_len[s0 + i]);
     if (threadIdx.x == 0) {
         for (int b = 0; b < N_BARS; ++b) mbar_init(&bars[b], b == P_FULL ? 128 : 1);
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(holder, kTmemCols<D>);
+        tmem_alloc(holder, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *holder;
+    auto entry = [&](int j) {
+        return j < kSchedSmem ? sched[j] : make_int2(tile_kv[s0 + j], tile_len[s0 + j]);
+    };
 
     if (warp == 0) {
         if (lane == 0 && n > 0) {
@@ -110,7 +126,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_arrive_expect_tx(&bars[Q_FULL], L::kTileBytes);
             for (int c = 0; c < L::kChunks; ++c) tma_load_3d(sQ + c * kBoxBytes, &tm_q, &bars[Q_FULL], c * 64, h, qt * 128);
             for (int j = 0; j < n; ++j) {
-                const int kv0 = tile_kv[s0 + j];
+                const int kv0 = entry(j).x;
                 if (j > 0) mbar_wait(&bars[K_EMPTY], (j - 1) & 1, err);
                 mbar_arrive_expect_tx(&bars[K_FULL], L::kTileBytes);
                 for (int c = 0; c < L::kChunks; ++c) tma_load_3d(sK + c * kBoxBytes, &tm_k, &bars[K_FULL], c * 64, g, kv0);
@@ -131,26 +147,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             auto issue_s = [&](int j) {
                 mbar_wait(&bars[K_FULL], j & 1, err);
                 tc_fence_after();
+                const uint32_t dS = tmem + (j & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                    mma_f16_ss(tmem + kColS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024),
-                               idesc_qk, kk > 0);
+                    mma_f16_ss(dS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024), idesc_qk,
+                               kk > 0);
                 }
                 mma_commit(&bars[K_EMPTY]);
-                mma_commit(&bars[S_FULL]);
+                mma_commit(&bars[S_FULL0 + (j & 1)]);
             };
             issue_s(0);
             for (int j = 0; j < n; ++j) {
+                if (j + 1 < n) {
+                    // buffer (j+1)&1 still holds P(j-1) until PV(j-1) has completed
+                    if (j >= 1) mbar_wait(&bars[O_DONE], (j - 1) & 1, err);
+                    issue_s(j + 1);
+                }
                 mbar_wait(&bars[P_FULL], j & 1, err);
-                tc_fence_after();
-                if (j + 1 < n) issue_s(j + 1);
                 mbar_wait(&bars[V_FULL], j & 1, err);
                 tc_fence_after();
+                const uint32_t aP = tmem + (j & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_f16_ts(tmem + kColO<D>, tmem + kColP + kk * 8, sdesc_sw128(aV + kk * 2048, kBoxBytes, 1024),
-                               idesc_pv, 1);
+                    mma_f16_ts(tmem + kColO, aP + kk * 8, sdesc_sw128(aV + kk * 2048, kBoxBytes, 1024), idesc_pv, 1);
                 mma_commit(&bars[V_EMPTY]);
                 mma_commit(&bars[O_DONE]);
             }
@@ -163,7 +183,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const bool real = q_row < T;
         const int pos_q = pos[q_row];
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_off + kColS, tP = tmem + lane_off + kColP, tO = tmem + lane_off + kColO<D>;
+        const uint32_t tO = tmem + lane_off + kColO;
 
         {
             uint32_t z[32];
@@ -173,50 +193,82 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int c = 0; c < D / 32; ++c) tmem_st32(tO + c * 32, z);
             tmem_st_wait();
         }
+        // end/pos of the next tile's keys are loaded one tile ahead (keys past the
+        // tile's own input are read through that input's tiles: never here)
+        int e_next = -1, p_next = 0;
+        if (n > 0) {
+            const int2 en = entry(0);
+            if (t < en.y) {
+                e_next = end[en.x + t];
+                p_next = pos[en.x + t];
+            }
+        }
         float m = -INFINITY, l = 0.f;
         for (int j = 0; j < n; ++j) {
-            const int kv0 = tile_kv[s0 + j];
+            const int kv0 = entry(j).x;
             int32_t* e_buf = kv_end + (j & 1) * 128;
             int32_t* p_buf = kv_pos + (j & 1) * 128;
-            {   // keys past the tile's own input are read through that input's tiles: never here
-                const int k = kv0 + t;
-                const bool own = t < tile_len[s0 + j];
-                e_buf[t] = own ? end[k] : -1;
-                p_buf[t] = own ? pos[k] : 0;
-            }
+            e_buf[t] = e_next;
+            p_buf[t] = p_next;
             named_bar_sync(1, 128);
-            mbar_wait(&bars[S_FULL], j & 1, err);
-            tc_fence_after();
-            float s[128];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t rr[32];
-                tmem_ld32(tS + c * 32, rr);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(rr[i]);
+            if (j + 1 < n) {
+                const int2 en = entry(j + 1);
+                e_next = -1;
+                p_next = 0;
+                if (t < en.y) {
+                    e_next = end[en.x + t];
+                    p_next = pos[en.x + t];
+                }
             }
+            mbar_wait(&bars[S_FULL0 + (j & 1)], (j >> 1) & 1, err);
+            tc_fence_after();
+            const uint32_t tS = tmem + lane_off + (j & 1) * 128;
+            float s[128];
+            {
+                uint32_t rr[128];
+                tmem_ld128(tS, rr);
+#pragma unroll
+                for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(rr[i]);
+            }
+            // visible: kv0 + c <= q_row (causal), q_row < end[key], window on depth
+            const int cmax = real ? q_row - kv0 : -1;
+            const int4* e4 = reinterpret_cast<const int4*>(e_buf);
+            const int4* p4 = reinterpret_cast<const int4*>(p_buf);
             float mx = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                const int k = kv0 + c;
-                const bool vis = real && k <= q_row && q_row < e_buf[c] && (window <= 0 || pos_q - p_buf[c] < window);
-                s[c] = vis ? s[c] : -INFINITY;
-                mx = fmaxf(mx, s[c]);
+            for (int c4 = 0; c4 < 32; ++c4) {
+                const int4 e = e4[c4];
+                bool v0 = 4 * c4 + 0 <= cmax && q_row < e.x;
+                bool v1 = 4 * c4 + 1 <= cmax && q_row < e.y;
+                bool v2 = 4 * c4 + 2 <= cmax && q_row < e.z;
+                bool v3 = 4 * c4 + 3 <= cmax && q_row < e.w;
+                if (window > 0) {
+                    const int4 pp = p4[c4];
+                    v0 = v0 && pos_q - pp.x < window;
+                    v1 = v1 && pos_q - pp.y < window;
+                    v2 = v2 && pos_q - pp.z < window;
+                    v3 = v3 && pos_q - pp.w < window;
+                }
+                s[4 * c4 + 0] = v0 ? s[4 * c4 + 0] : -INFINITY;
+                s[4 * c4 + 1] = v1 ? s[4 * c4 + 1] : -INFINITY;
+                s[4 * c4 + 2] = v2 ? s[4 * c4 + 2] : -INFINITY;
+                s[4 * c4 + 3] = v3 ? s[4 * c4 + 3] : -INFINITY;
+                mx = fmaxf(mx, fmaxf(fmaxf(s[4 * c4], s[4 * c4 + 1]), fmaxf(s[4 * c4 + 2], s[4 * c4 + 3])));
             }
-            const float m_new = fmaxf(m, mx);
-            if (j > 0) {   // PV of the previous tile has read P and written O
-                mbar_wait(&bars[O_DONE], (j - 1) & 1, err);
-                tc_fence_after();
-            }
+            // Lazy rescaling: P and l are taken relative to a reference maximum m that
+            // only moves when the row maximum exceeds it by more than 2^8 (so P <= 256);
+            // the final O / l is the same softmax whichever reference was used.
+            const float m_hi = fmaxf(m, mx);
+            const bool grow = m != -INFINITY && (m_hi - m) * scale_log2 > kRescaleLog2;
+            const float m_new = (m == -INFINITY || grow) ? m_hi : m;
             uint32_t pk0[32], pk1[32];
-            bool grow = false;
             float alpha = 1.f;
+            float rowsum = 0.f;
             if (m_new == -INFINITY) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) pk0[i] = pk1[i] = 0u;
             } else {
                 const float mb = m_new * scale_log2;
-                float rowsum = 0.f;
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const float p0 = fast_exp2(fmaf(s[2 * c], scale_log2, -mb));
@@ -228,25 +280,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const uint32_t w = *reinterpret_cast<const uint32_t*>(&b);
                     if (c < 32) pk0[c] = w; else pk1[c - 32] = w;
                 }
-                // the row maximum grew: O and l shrink by alpha
-                grow = m != -INFINITY && m_new > m;
                 if (grow) alpha = fast_exp2(fmaf(m, scale_log2, -mb));
+            }
+            if (j > 0) {   // PV of the previous tile has written O and read its P
+                mbar_wait(&bars[O_DONE], (j - 1) & 1, err);
+                tc_fence_after();
+            }
+            if (m_new != -INFINITY) {
                 l = l * alpha + rowsum;
                 m = m_new;
             }
             // TMEM traffic is warp-collective: lanes whose maximum did not move multiply by exactly 1
             if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld32(tO + c * 32, rr);
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t rr[64];
+                    tmem_ld64(tO + c * 64, rr);
+                    uint32_t* half = rr;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-                    tmem_st32(tO + c * 32, rr);
+                    for (int i = 0; i < 64; ++i) half[i] = __float_as_uint(__uint_as_float(half[i]) * alpha);
+                    tmem_st32(tO + c * 64, *reinterpret_cast<uint32_t(*)[32]>(rr));
+                    tmem_st32(tO + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(rr + 32));
                 }
             }
-            tmem_st32(tP, pk0);
-            tmem_st32(tP + 32, pk1);
+            tmem_st32(tS, pk0);
+            tmem_st32(tS + 32, pk1);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bars[P_FULL]);
@@ -255,19 +313,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_wait(&bars[O_DONE], (n - 1) & 1, err);
             tc_fence_after();
         }
+        // O / l in bf16 into the (now free) Q tile, in the TMA box layout: 128-byte rows,
+        // 16-byte chunks swizzled by the row's low three bits
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16* dst = out + (static_cast<size_t>(q_row) * Hq + h) * D;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t rr[32];
-            tmem_ld32(tO + c * 32, rr);
-            uint32_t w[16];
+        for (int c = 0; c < D / 64; ++c) {   // one 64-column TMA box per load
+            uint32_t rr[64];
+            tmem_ld64(tO + c * 64, rr);
+            uint32_t w[32];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
+            for (int i = 0; i < 32; ++i)
                 w[i] = real ? pack_bf16x2(__uint_as_float(rr[2 * i]) * inv, __uint_as_float(rr[2 * i + 1]) * inv) : 0u;
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+            uint8_t* row = sQ + c * kBoxBytes + r * 128;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            for (int i = 0; i < 8; ++i) {
+                const int chunk = i ^ (r & 7);
+                *reinterpret_cast<uint4*>(row + chunk * 16) = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (t == 0) {
+            for (int c = 0; c < L::kChunks; ++c) tma_store_3d(&tm_o, sQ + c * kBoxBytes, c * 64, h, qt * 128);
+            tma_store_commit_and_wait_read();
         }
     }
 
@@ -275,14 +343,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols<D>);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
 template <int D>
 spinf_status launch_attention(const Pass& P, const void* q, const void* k, const void* v, void* o, int Hq,
                               int Hkv, float scale, int window, int* err, cudaStream_t stream) {
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     const uint64_t dq[3] = {(uint64_t)D, (uint64_t)Hq, (uint64_t)P.T_pad};
     const uint64_t sq[2] = {(uint64_t)D * 2, (uint64_t)Hq * D * 2};
     const uint64_t dk[3] = {(uint64_t)D, (uint64_t)Hkv, (uint64_t)P.T_pad};
@@ -295,7 +363,9 @@ spinf_status launch_attention(const Pass& P, const void* q, const void* k, const
         return st;
     if ((st = make_tmap(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v, dk, sk, box, CU_TENSOR_MAP_SWIZZLE_128B)))
         return st;
-    const int smem = AttnSmem<D>::kAlloc > kMinSmem<D> ? AttnSmem<D>::kAlloc : kMinSmem<D>;
+    if ((st = make_tmap(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, o, dq, sq, box, CU_TENSOR_MAP_SWIZZLE_128B)))
+        return st;
+    const int smem = AttnSmem<D>::kAlloc > kMinSmem ? AttnSmem<D>::kAlloc : kMinSmem;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(branch_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -305,8 +375,8 @@ spinf_status launch_attention(const Pass& P, const void* q, const void* k, const
     const float scale_log2 = scale * 1.4426950408889634f;
     dim3 grid(P.T_pad / 128, Hq);
     branch_attention_kernel<D><<<grid, kAttnThreads, smem, stream>>>(
-        tq, tk, tv, static_cast<__nv_bfloat16*>(o), P.dev.end, P.dev.pos, P.dev.tile_ptr, P.dev.tile_kv, P.dev.tile_len, P.T,
-        P.T_pad, Hq, Hkv, scale_log2, window, err);
+        tq, tk, tv, to, P.dev.end, P.dev.pos, P.dev.tile_ptr, P.dev.tile_kv, P.dev.tile_len, P.T, Hkv, scale_log2,
+        window, err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
     return SPINF_OK;
@@ -325,7 +395,8 @@ extern "C" spinf_status spinf_branch_attention(const spinf_plan* plan, int32_t p
     if (!q || !k || !v || !o) return fail(SPINF_E_INVALID, "NULL tensor");
     for (const void* p : {q, k, v, (const void*)o})
         if (reinterpret_cast<uintptr_t>(p) & 15) return fail(SPINF_E_INVALID, "tensor not 16-byte aligned");
-    if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads) return fail(SPINF_E_INVALID, "bad head counts");
+    if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads || n_q_heads > 65535)
+        return fail(SPINF_E_INVALID, "bad head counts");
     if (window < 0) return fail(SPINF_E_INVALID, "negative window");
     const Pass& P = plan->passes[pass];
     if (P.T == 0) return SPINF_OK;
