@@ -12,9 +12,12 @@
 //   warp 1      TMEM owner and MMA issuer: S = Q K^T into one of two TMEM
 //               buffers (SS form, fp32), O += P V (P read from TMEM, V MN-major
 //               from shared memory)
-//   warps 2-5   one thread per Q row: mask, online softmax, P (bf16) into TMEM
-//               over its S, rescale O when the row maximum grows, final O / l
-//               staged in shared memory and written by a TMA store
+//   warps 2-9   softmax, two warps per TMEM lane quarter: each thread owns half
+//               of one Q row (64 of the 128 key columns, D/2 of the O columns):
+//               mask, online softmax with the row maximum exchanged between the
+//               two halves, P (bf16) into TMEM over its S, rescale O when the
+//               reference maximum moves, final O / l staged in shared memory
+//               and written by a TMA store
 // With two S buffers the tensor core computes S(j+1) and PV(j-1) while the
 // softmax warps work on tile j.
 //
@@ -41,7 +44,8 @@ namespace {
 
 using namespace dev;
 
-constexpr int kAttnThreads = 192;
+constexpr int kAttnThreads = 320;   // producer, MMA, 8 softmax warps
+constexpr int kSoftmaxThreads = 256;
 constexpr int kBoxBytes = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128-byte swizzled rows)
 constexpr int kSchedSmem = 256;        // schedule entries staged in shared memory (later ones read from global)
 
@@ -57,7 +61,10 @@ struct AttnSmem {
     static constexpr int kKvEnd = kV + kTileBytes;          // int32 [2][128]
     static constexpr int kKvPos = kKvEnd + 2 * 128 * 4;     // int32 [2][128]
     static constexpr int kSched = kKvPos + 2 * 128 * 4;     // int2 [kSchedSmem]: (first row, own keys)
-    static constexpr int kBars = kSched + kSchedSmem * 8;
+    static constexpr int kXmax = kSched + kSchedSmem * 8;   // float [2][2][128]: row maxima of the two halves
+    static constexpr int kLx = kXmax + 2 * 2 * 128 * 4;     // float [2][128]: the halves' row sums, at the end
+    static constexpr int kTmin = kLx + 2 * 128 * 4;         // int [2][8]: per-warp minima of end / pos
+    static constexpr int kBars = kTmin + 2 * 8 * 4;
     static constexpr int kHolder = kBars + N_BARS * 8;
     static constexpr int kBytes = kHolder + 16;
     static constexpr int kAlloc = kBytes + 1024;            // room to align the base to 1024
@@ -103,7 +110,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int i = threadIdx.x; i < n && i < kSchedSmem; i += blockDim.x)
         sched[i] = make_int2(tile_kv[s0 + i], tile_len[s0 + i]);
     if (threadIdx.x == 0) {
-        for (int b = 0; b < N_BARS; ++b) mbar_init(&bars[b], b == P_FULL ? 128 : 1);
+        for (int b = 0; b < N_BARS; ++b) mbar_init(&bars[b], b == P_FULL ? kSoftmaxThreads : 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -177,108 +184,119 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
     } else {
         const int quarter = warp & 3;                 // TMEM lanes this warp may touch
+        const int half = (warp - 2) >> 2;             // which half of the row's columns
         const int r = quarter * 32 + lane;            // Q-tile row of this thread
-        const int t = (warp - 2) * 32 + lane;         // 0..127 for cooperative loads
+        const int t = (warp - 2) * 32 + lane;         // 0..255 for cooperative loads
+        const int key = t & 127;                      // staging: half 0 loads end[], half 1 pos[]
         const int q_row = qt * 128 + r;
         const bool real = q_row < T;
         const int pos_q = pos[q_row];
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tO = tmem + lane_off + kColO;
+        const uint32_t tO = tmem + lane_off + kColO + half * (D / 2);
+        const uint32_t pair_bar = 2 + quarter;        // the two warps that share these TMEM lanes
+        float* xmax = reinterpret_cast<float*>(smem + L::kXmax);
+        float* lx = reinterpret_cast<float*>(smem + L::kLx);
+        int* tmin = reinterpret_cast<int*>(smem + L::kTmin);
 
         {
             uint32_t z[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) z[i] = 0u;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) tmem_st32(tO + c * 32, z);
+            for (int c = 0; c < D / 64; ++c) tmem_st32(tO + c * 32, z);
             tmem_st_wait();
         }
         // end/pos of the next tile's keys are loaded one tile ahead (keys past the
         // tile's own input are read through that input's tiles: never here)
-        int e_next = -1, p_next = 0;
-        if (n > 0) {
-            const int2 en = entry(0);
-            if (t < en.y) {
-                e_next = end[en.x + t];
-                p_next = pos[en.x + t];
-            }
-        }
-        float m = -INFINITY, l = 0.f;
+        auto stage_value = [&](int2 en) {
+            if (key >= en.y) return half == 0 ? -1 : 0;
+            return half == 0 ? end[en.x + key] : pos[en.x + key];
+        };
+        int next = n > 0 ? stage_value(entry(0)) : 0;
+        float m = -INFINITY, l = 0.f;   // l: this half's share of the row sum
         for (int j = 0; j < n; ++j) {
             const int kv0 = entry(j).x;
-            int32_t* e_buf = kv_end + (j & 1) * 128;
-            int32_t* p_buf = kv_pos + (j & 1) * 128;
-            e_buf[t] = e_next;
-            p_buf[t] = p_next;
-            named_bar_sync(1, 128);
-            if (j + 1 < n) {
-                const int2 en = entry(j + 1);
-                e_next = -1;
-                p_next = 0;
-                if (t < en.y) {
-                    e_next = end[en.x + t];
-                    p_next = pos[en.x + t];
-                }
+            const int b = j & 1;
+            int32_t* e_buf = kv_end + b * 128;
+            int32_t* p_buf = kv_pos + b * 128;
+            (half == 0 ? e_buf : p_buf)[key] = next;
+            {   // per-warp minimum of end[] (half 0) or pos[] (half 1) over this tile's keys
+                const int wmin = __reduce_min_sync(0xffffffffu, next);
+                if (lane == 0) tmin[b * 8 + (warp - 2)] = wmin;
             }
-            mbar_wait(&bars[S_FULL0 + (j & 1)], (j >> 1) & 1, err);
+            named_bar_sync(1, kSoftmaxThreads);
+            if (j + 1 < n) next = stage_value(entry(j + 1));
+            mbar_wait(&bars[S_FULL0 + b], (j >> 1) & 1, err);
             tc_fence_after();
-            const uint32_t tS = tmem + lane_off + (j & 1) * 128;
-            float s[128];
+            const uint32_t tS = tmem + lane_off + b * 128;
+            float s[64];
             {
-                uint32_t rr[128];
-                tmem_ld128(tS, rr);
+                uint32_t rr[64];
+                tmem_ld64(tS + half * 64, rr);
 #pragma unroll
-                for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(rr[i]);
+                for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(rr[i]);
             }
-            // visible: kv0 + c <= q_row (causal), q_row < end[key], window on depth
+            // visible: kv0 + c <= q_row (causal), q_row < end[key], window on depth.
+            // A tile whose every key is visible to this row skips the per-key test.
             const int cmax = real ? q_row - kv0 : -1;
-            const int4* e4 = reinterpret_cast<const int4*>(e_buf);
-            const int4* p4 = reinterpret_cast<const int4*>(p_buf);
+            const int* tm = tmin + b * 8;
+            const int emin = min(min(tm[0], tm[1]), min(tm[2], tm[3]));
+            const int pmin = min(min(tm[4], tm[5]), min(tm[6], tm[7]));
+            const bool all_visible = cmax >= 127 && emin > q_row && (window <= 0 || pos_q - pmin < window);
             float mx = -INFINITY;
+            if (all_visible) {
 #pragma unroll
-            for (int c4 = 0; c4 < 32; ++c4) {
-                const int4 e = e4[c4];
-                bool v0 = 4 * c4 + 0 <= cmax && q_row < e.x;
-                bool v1 = 4 * c4 + 1 <= cmax && q_row < e.y;
-                bool v2 = 4 * c4 + 2 <= cmax && q_row < e.z;
-                bool v3 = 4 * c4 + 3 <= cmax && q_row < e.w;
-                if (window > 0) {
-                    const int4 pp = p4[c4];
-                    v0 = v0 && pos_q - pp.x < window;
-                    v1 = v1 && pos_q - pp.y < window;
-                    v2 = v2 && pos_q - pp.z < window;
-                    v3 = v3 && pos_q - pp.w < window;
+                for (int i = 0; i < 64; ++i) mx = fmaxf(mx, s[i]);
+            } else {
+                const int4* e4 = reinterpret_cast<const int4*>(e_buf + half * 64);
+                const int4* p4 = reinterpret_cast<const int4*>(p_buf + half * 64);
+                const int cm = cmax - half * 64;
+#pragma unroll
+                for (int c4 = 0; c4 < 16; ++c4) {
+                    const int4 e = e4[c4];
+                    bool v0 = 4 * c4 + 0 <= cm && q_row < e.x;
+                    bool v1 = 4 * c4 + 1 <= cm && q_row < e.y;
+                    bool v2 = 4 * c4 + 2 <= cm && q_row < e.z;
+                    bool v3 = 4 * c4 + 3 <= cm && q_row < e.w;
+                    if (window > 0) {
+                        const int4 pp = p4[c4];
+                        v0 = v0 && pos_q - pp.x < window;
+                        v1 = v1 && pos_q - pp.y < window;
+                        v2 = v2 && pos_q - pp.z < window;
+                        v3 = v3 && pos_q - pp.w < window;
+                    }
+                    s[4 * c4 + 0] = v0 ? s[4 * c4 + 0] : -INFINITY;
+                    s[4 * c4 + 1] = v1 ? s[4 * c4 + 1] : -INFINITY;
+                    s[4 * c4 + 2] = v2 ? s[4 * c4 + 2] : -INFINITY;
+                    s[4 * c4 + 3] = v3 ? s[4 * c4 + 3] : -INFINITY;
+                    mx = fmaxf(mx, fmaxf(fmaxf(s[4 * c4], s[4 * c4 + 1]), fmaxf(s[4 * c4 + 2], s[4 * c4 + 3])));
                 }
-                s[4 * c4 + 0] = v0 ? s[4 * c4 + 0] : -INFINITY;
-                s[4 * c4 + 1] = v1 ? s[4 * c4 + 1] : -INFINITY;
-                s[4 * c4 + 2] = v2 ? s[4 * c4 + 2] : -INFINITY;
-                s[4 * c4 + 3] = v3 ? s[4 * c4 + 3] : -INFINITY;
-                mx = fmaxf(mx, fmaxf(fmaxf(s[4 * c4], s[4 * c4 + 1]), fmaxf(s[4 * c4 + 2], s[4 * c4 + 3])));
             }
+            // the row maximum of the tile, from both halves
+            xmax[(b * 2 + half) * 128 + r] = mx;
+            named_bar_sync(pair_bar, 64);
+            const float mx_row = fmaxf(xmax[(b * 2) * 128 + r], xmax[(b * 2 + 1) * 128 + r]);
             // Lazy rescaling: P and l are taken relative to a reference maximum m that
             // only moves when the row maximum exceeds it by more than 2^8 (so P <= 256);
             // the final O / l is the same softmax whichever reference was used.
-            const float m_hi = fmaxf(m, mx);
+            const float m_hi = fmaxf(m, mx_row);
             const bool grow = m != -INFINITY && (m_hi - m) * scale_log2 > kRescaleLog2;
             const float m_new = (m == -INFINITY || grow) ? m_hi : m;
-            uint32_t pk0[32], pk1[32];
+            uint32_t pk[32];
             float alpha = 1.f;
             float rowsum = 0.f;
             if (m_new == -INFINITY) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) pk0[i] = pk1[i] = 0u;
+                for (int i = 0; i < 32; ++i) pk[i] = 0u;
             } else {
                 const float mb = m_new * scale_log2;
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
+                for (int c = 0; c < 32; ++c) {
                     const float p0 = fast_exp2(fmaf(s[2 * c], scale_log2, -mb));
                     const float p1 = fast_exp2(fmaf(s[2 * c + 1], scale_log2, -mb));
-                    const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
-                    const float2 f = __bfloat1622float2(b);
-                    rowsum += f.x;
-                    rowsum += f.y;
-                    const uint32_t w = *reinterpret_cast<const uint32_t*>(&b);
-                    if (c < 32) pk0[c] = w; else pk1[c - 32] = w;
+                    rowsum += p0;
+                    rowsum += p1;
+                    pk[c] = pack_bf16x2(p0, p1);
                 }
                 if (grow) alpha = fast_exp2(fmaf(m, scale_log2, -mb));
             }
@@ -294,17 +312,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
                 for (int c = 0; c < D / 64; ++c) {
-                    uint32_t rr[64];
-                    tmem_ld64(tO + c * 64, rr);
-                    uint32_t* half = rr;
+                    uint32_t rr[32];
+                    tmem_ld32(tO + c * 32, rr);
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) half[i] = __float_as_uint(__uint_as_float(half[i]) * alpha);
-                    tmem_st32(tO + c * 64, *reinterpret_cast<uint32_t(*)[32]>(rr));
-                    tmem_st32(tO + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(rr + 32));
+                    for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+                    tmem_st32(tO + c * 32, rr);
                 }
             }
-            tmem_st32(tS, pk0);
-            tmem_st32(tS + 32, pk1);
+            // P of keys [64 half, 64 half + 64) -> bf16 pairs in columns [32 half, 32 half + 32) of
+            // this tile's S buffer (both halves have read their S columns before the pair barrier)
+            tmem_st32(tS + half * 32, pk);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bars[P_FULL]);
@@ -313,26 +330,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_wait(&bars[O_DONE], (n - 1) & 1, err);
             tc_fence_after();
         }
+        // the row sum, halves added in a fixed order
+        lx[half * 128 + r] = l;
+        named_bar_sync(pair_bar, 64);
+        const float lrow = lx[r] + lx[128 + r];
         // O / l in bf16 into the (now free) Q tile, in the TMA box layout: 128-byte rows,
         // 16-byte chunks swizzled by the row's low three bits
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
 #pragma unroll 1
-        for (int c = 0; c < D / 64; ++c) {   // one 64-column TMA box per load
-            uint32_t rr[64];
-            tmem_ld64(tO + c * 64, rr);
-            uint32_t w[32];
+        for (int c = 0; c < D / 64; ++c) {
+            const int col = half * (D / 2) + c * 32;      // first O column of these 32
+            uint32_t rr[32];
+            tmem_ld32(tO + c * 32, rr);
+            uint32_t w[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
+            for (int i = 0; i < 16; ++i)
                 w[i] = real ? pack_bf16x2(__uint_as_float(rr[2 * i]) * inv, __uint_as_float(rr[2 * i + 1]) * inv) : 0u;
-            uint8_t* row = sQ + c * kBoxBytes + r * 128;
+            uint8_t* row = sQ + (col >> 6) * kBoxBytes + r * 128;
+            const int chunk0 = (col & 63) >> 3;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int chunk = i ^ (r & 7);
+            for (int i = 0; i < 4; ++i) {
+                const int chunk = (chunk0 + i) ^ (r & 7);
                 *reinterpret_cast<uint4*>(row + chunk * 16) = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
             }
         }
         fence_proxy_async_smem();
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kSoftmaxThreads);
         if (t == 0) {
             for (int c = 0; c < L::kChunks; ++c) tma_store_3d(&tm_o, sQ + c * kBoxBytes, c * 64, h, qt * 128);
             tma_store_commit_and_wait_read();

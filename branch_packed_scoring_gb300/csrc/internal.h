@@ -35,6 +35,7 @@ struct Pass {
     std::vector<int32_t> row_gptr, row_glist;
     std::vector<int32_t> unit_start, unit_source;
     PassDevice dev;
+    std::vector<unsigned char> staging;   // host source of the descriptor upload, kept until the plan is freed
 };
 
 // Where the option tokens of one laid-out question sit in its pass's gather list.

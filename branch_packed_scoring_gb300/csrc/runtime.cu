@@ -105,15 +105,16 @@ extern "C" spinf_status spinf_plan_upload(spinf_plan* plan, int32_t pass, spinf_
     void* block = nullptr;
     e = cudaMalloc(&block, total > 0 ? total : 256);
     if (e != cudaSuccess) return fail(SPINF_E_NOMEM, "device allocation of pass descriptors failed");
-    // one staging buffer so the copy is a single transfer
-    std::vector<unsigned char> host(total, 0);
+    // one staging buffer so the copy is a single transfer; the plan keeps it, so
+    // the copy may still be in flight when this call returns
+    std::vector<unsigned char>& host = P.staging;
+    host.assign(total, 0);
     for (int i = 0; i < n; ++i) {
         if (!arrays[i]->empty()) std::memcpy(host.data() + off[i], arrays[i]->data(), arrays[i]->size() * 4);
         *dst[i] = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(block) + off[i]);
     }
     if (total) {
         e = cudaMemcpyAsync(block, host.data(), total, cudaMemcpyHostToDevice, s);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(s);   // the staging buffer dies here
         if (e != cudaSuccess) {
             cudaFree(block);
             return cuda_fail(e, "descriptor upload");

@@ -172,8 +172,9 @@ spinf_status spinf_plan_pass_info(const spinf_plan* plan, int32_t pass, spinf_pa
 spinf_status spinf_plan_counts(const spinf_plan* plan, int64_t* n_questions, int64_t* n_options);
 
 /* Copy pass `pass`'s descriptors to the current device (allocated once per pass
- * and kept by the plan; later calls are no-ops).  Synchronous with respect to the
- * host for the allocation; the copies are enqueued on `stream`. */
+ * and kept by the plan; later calls are no-ops).  The allocation is synchronous;
+ * the copy is enqueued on `stream` from a host buffer the plan keeps, so kernels
+ * of this pass must run on `stream` or after it. */
 spinf_status spinf_plan_upload(spinf_plan* plan, int32_t pass, spinf_stream stream);
 
 /* Tree-masked GQA attention over one packed pass (spec: the branch
