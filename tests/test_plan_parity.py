@@ -133,3 +133,16 @@ def test_collect_matches_oracle_collect(spinf):
     np.testing.assert_allclose(ours["option_floor_p"], flat["floor_p"], rtol=0, atol=1e-12)
     np.testing.assert_allclose(ours["residual"], res, rtol=0, atol=1e-12)
     np.testing.assert_allclose(ours["floor_residual"], fres, rtol=0, atol=1e-12)
+
+
+def test_request_object_plans_identically(spinf):
+    inputs = wl.stress(n_questions=30, content_tokens=120, vocab=1000) + wl.tiny(vocab=1000)
+    req = spinf.Request(inputs)
+    a, b = spinf.Plan(inputs, token_budget=700), spinf.Plan(req, token_budget=700)
+    c = spinf.Plan(req, token_budget=700)
+    assert a.num_passes == b.num_passes == c.num_passes
+    for p in range(a.num_passes):
+        ia, ib, ic = a.pass_info(p), b.pass_info(p), c.pass_info(p)
+        for f in FIELDS:
+            assert np.array_equal(getattr(ia, f), getattr(ib, f))
+            assert np.array_equal(getattr(ia, f), getattr(ic, f))
