@@ -9,7 +9,11 @@
 // Persistent kernel: one CTA per SM walks a static list of work items, an item
 // being one 128-row Q tile of one query head (items of the same Q tile and
 // neighbouring heads run side by side on neighbouring SMs, so a kv head's tiles
-// are read from L2 by its query heads at about the same time).  Warp roles:
+// are read from L2 by its query heads at about the same time).  When a kv group
+// has an even number of query heads, CTAs run as clusters of two that take two
+// heads of one group on the same Q tile: each CTA loads half of every K and V
+// tile and multicasts it to both, so each tile leaves L2 once per pair, and a
+// buffer is refilled only when both CTAs' MMAs have released it.  Warp roles:
 //   warp 0      TMA producer of Q (once per item) and K tiles (two buffers for
 //               d_head <= 128; one for 256, where Q, K and V fill shared memory)
 //   warp 1      TMEM owner and MMA issuer: S = Q K^T into one of two TMEM
@@ -98,7 +102,7 @@ __device__ __forceinline__ Item item_at(int it, int Hq, const int32_t* __restric
     return I;
 }
 
-template <int D>
+template <int D, bool PAIR>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     branch_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
@@ -119,13 +123,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int group = Hq / Hkv;
+    // PAIR: item = (Q tile, pair of heads 2p, 2p+1 of one kv group); this CTA takes head 2p + rank
+    const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+    const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int n_units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    const int heads_per_item = PAIR ? 2 : 1;
+    auto item = [&](int it) {
+        Item I = item_at(it, Hq / heads_per_item, tile_ptr);
+        I.h = I.h * heads_per_item + rank;
+        return I;
+    };
 
     uint64_t* k_full = bars + N_FIXED_BARS;
     uint64_t* k_empty = k_full + L::kStages;
     uint64_t* v_full = k_empty + L::kStages;
     uint64_t* v_empty = v_full + L::kStages;
     if (threadIdx.x == 0) {
-        for (int b = 0; b < L::kNumBars; ++b) mbar_init(&bars[b], b == P_FULL ? kSoftmaxThreads : 1);
+        for (int b = 0; b < N_FIXED_BARS; ++b) mbar_init(&bars[b], b == P_FULL ? kSoftmaxThreads : 1);
+        for (int st = 0; st < L::kStages; ++st) {
+            mbar_init(&k_full[st], 1);
+            mbar_init(&v_full[st], 1);
+            mbar_init(&k_empty[st], PAIR ? 2 : 1);   // released by the MMAs of both CTAs of a pair
+            mbar_init(&v_empty[st], PAIR ? 2 : 1);
+        }
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -134,8 +154,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();   // the peer's barriers exist before anything is multicast to them
     tc_fence_after();
     const uint32_t tmem = *holder;
+    constexpr uint16_t kBoth = 0x3;
 
     if (warp == 0) {
         // ---------------------------------------------------------- Q and K producer
@@ -143,8 +165,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             uint32_t G = 0, ic = 0;
-            for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-                const Item I = item_at(it, Hq, tile_ptr);
+            for (int it = unit; it < n_items; it += n_units) {
+                const Item I = item(it);
                 if (I.n <= 0) continue;
                 if (ic > 0) mbar_wait(&bars[Q_EMPTY], (ic - 1) & 1, err);   // the last S of the previous item is done
                 mbar_arrive_expect_tx(&bars[Q_FULL], L::kTileBytes);
@@ -157,14 +179,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const uint32_t st = G % L::kStages;
                     if (G >= (uint32_t)L::kStages) mbar_wait(&k_empty[st], (G / L::kStages - 1) & 1, err);
                     mbar_arrive_expect_tx(&k_full[st], L::kTileBytes);
-                    for (int c = 0; c < L::kChunks; ++c)
-                        tma_load_3d(sK + st * L::kTileBytes + c * kBoxBytes, &tm_k, &k_full[st], c * 64, I.h / group, kv0);
+                    for (int c = 0; c < L::kChunks; ++c) {
+                        uint8_t* dst = sK + st * L::kTileBytes + c * kBoxBytes;
+                        if (!PAIR) tma_load_3d(dst, &tm_k, &k_full[st], c * 64, I.h / group, kv0);
+                        else if ((c & 1) == rank) tma_load_3d_mc(dst, &tm_k, &k_full[st], c * 64, I.h / group, kv0, kBoth);
+                    }
                 }
                 ++ic;
             }
             // our last copies have landed before the CTA may retire
-            for (uint32_t b = G > (uint32_t)L::kStages ? G - L::kStages : 0; b < G; ++b)
+            for (uint32_t b = G > (uint32_t)L::kStages ? G - L::kStages : 0; b < G; ++b) {
                 mbar_wait(&k_full[b % L::kStages], (b / L::kStages) & 1, err);
+                mbar_wait(&k_empty[b % L::kStages], (b / L::kStages) & 1, err);   // every release has arrived
+            }
             if (ic > 0) mbar_wait(&bars[Q_FULL], (ic - 1) & 1, err);
         }
     } else if (warp == 2) {
@@ -172,8 +199,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (lane == 0) {
             tma_prefetch_desc(&tm_v);
             uint32_t G = 0;
-            for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-                const Item I = item_at(it, Hq, tile_ptr);
+            for (int it = unit; it < n_items; it += n_units) {
+                const Item I = item(it);
                 if (I.n <= 0) continue;
                 int kv_next = __ldg(tile_kv + I.s0);
                 for (int j = 0; j < I.n; ++j, ++G) {
@@ -182,12 +209,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const uint32_t st = G % L::kStages;
                     if (G >= (uint32_t)L::kStages) mbar_wait(&v_empty[st], (G / L::kStages - 1) & 1, err);
                     mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
-                    for (int c = 0; c < L::kChunks; ++c)
-                        tma_load_3d(sV + st * L::kTileBytes + c * kBoxBytes, &tm_v, &v_full[st], c * 64, I.h / group, kv0);
+                    for (int c = 0; c < L::kChunks; ++c) {
+                        uint8_t* dst = sV + st * L::kTileBytes + c * kBoxBytes;
+                        if (!PAIR) tma_load_3d(dst, &tm_v, &v_full[st], c * 64, I.h / group, kv0);
+                        else if ((c & 1) == rank) tma_load_3d_mc(dst, &tm_v, &v_full[st], c * 64, I.h / group, kv0, kBoth);
+                    }
                 }
             }
-            for (uint32_t b = G > (uint32_t)L::kStages ? G - L::kStages : 0; b < G; ++b)
+            for (uint32_t b = G > (uint32_t)L::kStages ? G - L::kStages : 0; b < G; ++b) {
                 mbar_wait(&v_full[b % L::kStages], (b / L::kStages) & 1, err);
+                mbar_wait(&v_empty[b % L::kStages], (b / L::kStages) & 1, err);
+            }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
@@ -209,12 +241,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     mma_f16_ss(dS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aKs + off, 16, 1024), idesc_qk,
                                kk > 0);
                 }
-                mma_commit(&k_empty[st]);
+                if (PAIR) mma_commit_mc(&k_empty[st], kBoth); else mma_commit(&k_empty[st]);
                 mma_commit(&bars[S_FULL0 + (Gs & 1)]);
             };
             uint32_t G = 0, ic = 0;
-            for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-                const Item I = item_at(it, Hq, tile_ptr);
+            for (int it = unit; it < n_items; it += n_units) {
+                const Item I = item(it);
                 if (I.n <= 0) continue;
                 const uint32_t G0 = G;
                 mbar_wait(&bars[Q_FULL], ic & 1, err);
@@ -238,7 +270,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     for (int kk = 0; kk < 8; ++kk)
                         mma_f16_ts(tmem + kColO, aP + kk * 8, sdesc_sw128(aVs + kk * 2048, kBoxBytes, 1024), idesc_pv,
                                    1);
-                    mma_commit(&v_empty[st]);
+                    if (PAIR) mma_commit_mc(&v_empty[st], kBoth); else mma_commit(&v_empty[st]);
                     mma_commit(&bars[O_DONE]);
                 }
                 G += I.n;
@@ -278,8 +310,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         };
         // schedule entry of the first tile of the next item with tiles, or -1
         auto first_entry_after = [&](int it) {
-            for (it += gridDim.x; it < n_items; it += gridDim.x) {
-                const Item I = item_at(it, Hq, tile_ptr);
+            for (it += n_units; it < n_items; it += n_units) {
+                const Item I = item(it);
                 if (I.n > 0) return I.s0;
             }
             return -1;
@@ -287,9 +319,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
         zero_o();
         uint32_t G = 0;
-        int next = stage_value(first_entry_after(static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x)));
-        for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-            const Item I = item_at(it, Hq, tile_ptr);
+        int next = stage_value(first_entry_after(unit - n_units));
+        for (int it = unit; it < n_items; it += n_units) {
+            const Item I = item(it);
             if (I.n <= 0) continue;
             const int q_row = I.qt * 128 + r;
             const bool real = q_row < T;
@@ -435,6 +467,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();   // nothing of the peer still lands in this CTA
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -458,19 +491,55 @@ spinf_status launch_attention(const Pass& P, const void* q, const void* k, const
     if ((st = make_tmap(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v, dk, sk, box, CU_TENSOR_MAP_SWIZZLE_128B)))
         return st;
     const int smem = AttnSmem<D>::kAlloc > kMinSmem ? AttnSmem<D>::kAlloc : kMinSmem;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(branch_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
-        configured = true;
-    }
     const float scale_log2 = scale * 1.4426950408889634f;
-    const int n_items = (P.T_pad / 128) * Hq;
-    const int grid = std::min(n_items, sm_count());
-    branch_attention_kernel<D><<<grid, kAttnThreads, smem, stream>>>(
-        tq, tk, tv, static_cast<__nv_bfloat16*>(o), P.dev.end, P.dev.pos, P.dev.tile_ptr, P.dev.tile_kv,
-        P.dev.tile_len, P.T, Hq, Hkv, n_items, scale_log2, window, err);
-    cudaError_t e = cudaGetLastError();
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(o);
+    cudaError_t e;
+    if ((Hq / Hkv) % 2 == 0) {   // clusters of two CTAs, two heads of a kv group per item
+        auto kernel = branch_attention_kernel<D, true>;
+        static bool configured = false;
+        if (!configured) {
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
+            configured = true;
+        }
+        const int n_items = (P.T_pad / 128) * (Hq / 2);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.blockDim = dim3(kAttnThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(2 * std::max(1, sm_count() / 2));
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters <= 0) {
+            cudaGetLastError();
+            clusters = std::max(1, sm_count() / 2);
+        }
+        cfg.gridDim = dim3(2 * std::min(n_items, clusters));
+        e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, out, (const int32_t*)P.dev.end, (const int32_t*)P.dev.pos,
+                               (const int32_t*)P.dev.tile_ptr, (const int32_t*)P.dev.tile_kv,
+                               (const int32_t*)P.dev.tile_len, P.T, Hq, Hkv, n_items, scale_log2, window, err);
+        if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+    } else {
+        auto kernel = branch_attention_kernel<D, false>;
+        static bool configured = false;
+        if (!configured) {
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
+            configured = true;
+        }
+        const int n_items = (P.T_pad / 128) * Hq;
+        const int grid = std::min(n_items, sm_count());
+        kernel<<<grid, kAttnThreads, smem, stream>>>(tq, tk, tv, out, P.dev.end, P.dev.pos, P.dev.tile_ptr,
+                                                     P.dev.tile_kv, P.dev.tile_len, P.T, Hq, Hkv, n_items, scale_log2,
+                                                     window, err);
+    }
+    e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
     return SPINF_OK;
 }
