@@ -24,7 +24,8 @@
 //               of one Q row (64 of the 128 key columns, D/2 of the O columns):
 //               mask, online softmax with the row maximum exchanged between the
 //               two halves, P (bf16) into TMEM over its S, rescale O when the
-//               reference maximum moves, final O / l stored to global memory
+//               reference maximum moves, final O / l written by TMA stores of 32 x 32
+//               boxes staged per warp
 // The tensor core computes S(j+1) and PV(j-1) while the softmax works on tile j;
 // the next item's Q load and first S overlap the previous item's epilogue.
 //
@@ -56,6 +57,7 @@ constexpr int kAttnThreads = 352;      // Q/K producer, MMA, V producer, 8 softm
 constexpr int kSoftmaxThreads = 256;
 constexpr int kFirstSoftmaxWarp = 3;
 constexpr int kBoxBytes = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128-byte swizzled rows)
+constexpr int kOstageBytes = 32 * 64;  // O store box of one softmax warp: 32 rows x 32 bf16, row-major
 
 enum { Q_FULL = 0, Q_EMPTY, S_FULL0, S_FULL1, P_FULL, O_DONE, N_FIXED_BARS };
 
@@ -72,7 +74,8 @@ struct AttnSmem {
     static constexpr int kXmax = kKvPos + 2 * 128 * 4;      // float [2][2][128]: row maxima of the two halves
     static constexpr int kLx = kXmax + 2 * 2 * 128 * 4;     // float [2][128]: the halves' row sums, per item
     static constexpr int kTmin = kLx + 2 * 128 * 4;         // int [2][8]: per-warp minima of end / pos
-    static constexpr int kBars = kTmin + 2 * 8 * 4;   // fixed barriers, then K_FULL, K_EMPTY, V_FULL, V_EMPTY [kStages]
+    static constexpr int kOstage = (kTmin + 2 * 8 * 4 + 1023) / 1024 * 1024;  // per softmax warp: 32 x 32 O bf16
+    static constexpr int kBars = kOstage + 8 * kOstageBytes;   // fixed barriers, then K_FULL, K_EMPTY, V_FULL, V_EMPTY [kStages]
     static constexpr int kNumBars = N_FIXED_BARS + 4 * kStages;
     static constexpr int kHolder = kBars + kNumBars * 8;
     static constexpr int kBytes = kHolder + 16;
@@ -105,7 +108,7 @@ __device__ __forceinline__ Item item_at(int it, int Hq, const int32_t* __restric
 template <int D, bool PAIR>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     branch_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                            const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
+                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                             const int32_t* __restrict__ end, const int32_t* __restrict__ pos,
                             const int32_t* __restrict__ tile_ptr, const int32_t* __restrict__ tile_kv,
                             const int32_t* __restrict__ tile_len, int T, int Hq, int Hkv, int n_items,
@@ -446,18 +449,39 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             named_bar_sync(pair_bar, 64);
             const float lrow = lx[r] + lx[128 + r];      // halves added in a fixed order
             const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
-            uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(q_row) * Hq + I.h) * D + half * (D / 2));
-#pragma unroll 1
-            for (int c = 0; c < D / 64; ++c) {
-                uint32_t rr[32];
-                tmem_ld32(tO + c * 32, rr);
+            // this warp's 32 rows x D/2 columns, 32 columns at a time, through a 2 KB staging
+            // box and a TMA store (the box's rows are the TMEM lanes of the warp)
+            uint8_t* stage = smem + L::kOstage + sw * kOstageBytes;
+            const int row0 = I.qt * 128 + quarter * 32;
+            auto store_chunk = [&](const uint32_t* rr, int col) {
                 uint32_t w[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     w[i] = real ? pack_bf16x2(__uint_as_float(rr[2 * i]) * inv, __uint_as_float(rr[2 * i + 1]) * inv)
                                 : 0u;
+                uint4* row = reinterpret_cast<uint4*>(stage + lane * 64);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) dst[c * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                for (int i = 0; i < 4; ++i) row[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(&tm_o, stage, col, I.h, row0);
+                    tma_store_commit_and_wait_read();
+                }
+                __syncwarp();
+            };
+            if constexpr (D >= 128) {
+#pragma unroll 1
+                for (int c = 0; c < D / 128; ++c) {   // 64 columns per TMEM load
+                    uint32_t rr[64];
+                    tmem_ld64(tO + c * 64, rr);
+                    store_chunk(rr, half * (D / 2) + c * 64);
+                    store_chunk(rr + 32, half * (D / 2) + c * 64 + 32);
+                }
+            } else {
+                uint32_t rr[32];
+                tmem_ld32(tO, rr);
+                store_chunk(rr, half * (D / 2));
             }
             zero_o();
             // lx is read by the partner before either writes it again (next item's epilogue)
@@ -477,7 +501,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 template <int D>
 spinf_status launch_attention(const Pass& P, const void* q, const void* k, const void* v, void* o, int Hq,
                               int Hkv, float scale, int window, int* err, cudaStream_t stream) {
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     const uint64_t dq[3] = {(uint64_t)D, (uint64_t)Hq, (uint64_t)P.T_pad};
     const uint64_t sq[2] = {(uint64_t)D * 2, (uint64_t)Hq * D * 2};
     const uint64_t dk[3] = {(uint64_t)D, (uint64_t)Hkv, (uint64_t)P.T_pad};
@@ -490,9 +514,11 @@ spinf_status launch_attention(const Pass& P, const void* q, const void* k, const
         return st;
     if ((st = make_tmap(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v, dk, sk, box, CU_TENSOR_MAP_SWIZZLE_128B)))
         return st;
+    const uint32_t obox[3] = {32, 1, 32};   // one softmax warp's rows, 32 columns
+    if ((st = make_tmap(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, o, dq, sq, obox, CU_TENSOR_MAP_SWIZZLE_NONE)))
+        return st;
     const int smem = AttnSmem<D>::kAlloc > kMinSmem ? AttnSmem<D>::kAlloc : kMinSmem;
     const float scale_log2 = scale * 1.4426950408889634f;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(o);
     cudaError_t e;
     if ((Hq / Hkv) % 2 == 0) {   // clusters of two CTAs, two heads of a kv group per item
         auto kernel = branch_attention_kernel<D, true>;
@@ -521,7 +547,7 @@ spinf_status launch_attention(const Pass& P, const void* q, const void* k, const
             clusters = std::max(1, sm_count() / 2);
         }
         cfg.gridDim = dim3(2 * std::min(n_items, clusters));
-        e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, out, (const int32_t*)P.dev.end, (const int32_t*)P.dev.pos,
+        e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, to, (const int32_t*)P.dev.end, (const int32_t*)P.dev.pos,
                                (const int32_t*)P.dev.tile_ptr, (const int32_t*)P.dev.tile_kv,
                                (const int32_t*)P.dev.tile_len, P.T, Hq, Hkv, n_items, scale_log2, window, err);
         if (e != cudaSuccess) return cuda_fail(e, "attention launch");
@@ -535,7 +561,7 @@ spinf_status launch_attention(const Pass& P, const void* q, const void* k, const
         }
         const int n_items = (P.T_pad / 128) * Hq;
         const int grid = std::min(n_items, sm_count());
-        kernel<<<grid, kAttnThreads, smem, stream>>>(tq, tk, tv, out, P.dev.end, P.dev.pos, P.dev.tile_ptr,
+        kernel<<<grid, kAttnThreads, smem, stream>>>(tq, tk, tv, to, P.dev.end, P.dev.pos, P.dev.tile_ptr,
                                                      P.dev.tile_kv, P.dev.tile_len, P.T, Hq, Hkv, n_items, scale_log2,
                                                      window, err);
     }
