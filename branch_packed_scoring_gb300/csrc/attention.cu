@@ -59,7 +59,7 @@ constexpr int kFirstSoftmaxWarp = 3;
 constexpr int kBoxBytes = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128-byte swizzled rows)
 constexpr int kOstageBytes = 32 * 64;  // O store box of one softmax warp: 32 rows x 32 bf16, row-major
 
-enum { Q_FULL = 0, Q_EMPTY, S_FULL0, S_FULL1, P_FULL, O_DONE, N_FIXED_BARS };
+enum { Q_FULL = 0, Q_EMPTY, S_FULL0, S_FULL1, P_FULL, O_DONE, PV_DONE0, PV_DONE1, N_FIXED_BARS };
 
 template <int D>
 struct AttnSmem {
@@ -230,9 +230,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
             const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-            // S(Gs) goes to buffer Gs&1, which held P(Gs-2): PV(Gs-2) must be done.  Every wait
-            // below targets the newest O_DONE phase that can have completed, never an older one.
+            // S(Gs) goes to buffer Gs&1, which held P(Gs-2): PV(Gs-2) must be done.  PV_DONE[b]
+            // completes once per PV that read buffer b, so its phases cannot be overtaken here.
             auto issue_s = [&](uint32_t Gs) {
+                if (Gs >= 2) mbar_wait(&bars[PV_DONE0 + (Gs & 1)], ((Gs - 2) >> 1) & 1, err);
                 const uint32_t st = Gs % L::kStages;
                 mbar_wait(&k_full[st], (Gs / L::kStages) & 1, err);
                 tc_fence_after();
@@ -253,13 +254,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (I.n <= 0) continue;
                 const uint32_t G0 = G;
                 mbar_wait(&bars[Q_FULL], ic & 1, err);
-                if (G0 >= 1) mbar_wait(&bars[O_DONE], (G0 - 1) & 1, err);   // previous item's last PV
                 issue_s(G0);
                 if (I.n == 1) mma_commit(&bars[Q_EMPTY]);
                 for (int j = 0; j < I.n; ++j) {
                     const uint32_t Gj = G0 + j;
                     if (j + 1 < I.n) {
-                        if (j >= 1) mbar_wait(&bars[O_DONE], (Gj - 1) & 1, err);
                         issue_s(Gj + 1);
                         if (j + 2 == I.n) mma_commit(&bars[Q_EMPTY]);   // Q is free once this S is done
                     }
@@ -275,6 +274,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                    1);
                     if (PAIR) mma_commit_mc(&v_empty[st], kBoth); else mma_commit(&v_empty[st]);
                     mma_commit(&bars[O_DONE]);
+                    mma_commit(&bars[PV_DONE0 + (Gj & 1)]);
                 }
                 G += I.n;
                 ++ic;
