@@ -25,12 +25,13 @@ struct PassDevice {
     int32_t* gather_tok = nullptr; // [G]
     int32_t* row_gptr = nullptr;   // [M + 1] gathers of each scoring row ...
     int32_t* row_glist = nullptr;  // [G]     ... sorted by token id, then gather index
+    int32_t* qt_work = nullptr;    // [n_qtiles][4] attention work order {qt, s0, n, 0}, most KV tiles first
 };
 
 struct Pass {
     int32_t T = 0, T_pad = 0;
     std::vector<int32_t> tok, parent, pos, end, anchor;
-    std::vector<int32_t> tile_ptr, tile_kv, tile_len;
+    std::vector<int32_t> tile_ptr, tile_kv, tile_len, qt_work;
     std::vector<int32_t> slot_row, gather_m, gather_tok;
     std::vector<int32_t> row_gptr, row_glist;
     std::vector<int32_t> unit_start, unit_source;

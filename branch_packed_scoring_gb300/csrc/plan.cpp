@@ -401,6 +401,21 @@ extern "C" spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inp
                 }
                 P.tile_ptr.push_back((int32_t)P.tile_kv.size());
             }
+            // attention work order: Q tiles with the most KV tiles first (ties: ascending
+            // tile), so the persistent CTAs end close together; results do not depend on
+            // it.  One 16-byte record {qt, first schedule entry, entry count, 0} per tile.
+            std::vector<int32_t> order(n_qt);
+            for (int32_t qt = 0; qt < n_qt; ++qt) order[qt] = qt;
+            std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
+                return P.tile_ptr[a + 1] - P.tile_ptr[a] > P.tile_ptr[b + 1] - P.tile_ptr[b];
+            });
+            P.qt_work.assign(4 * (size_t)n_qt, 0);
+            for (int32_t i = 0; i < n_qt; ++i) {
+                const int32_t qt = order[i];
+                P.qt_work[4 * i] = qt;
+                P.qt_work[4 * i + 1] = P.tile_ptr[qt];
+                P.qt_work[4 * i + 2] = P.tile_ptr[qt + 1] - P.tile_ptr[qt];
+            }
 
             // scoring rows: the distinct gather rows, ascending
             std::vector<int32_t> m_of(T > 0 ? T : 1, -1);

@@ -36,8 +36,10 @@ def test_tiny_every_row(spinf):
     _check(lay, o, q, k, v, shape, list(range(lay.T)))
 
 
+# one per kernel arrangement: d 64 with an even group (two CTAs sharing multicast K/V),
+# odd groups (one CTA per head), d 128 / 256 with even groups (cta_group::2 pairs)
 SHAPES = [wl.Shape(4, 2, 64, 256, 1000), wl.Shape(8, 8, 128, 256, 1000), wl.Shape(40, 8, 128, 256, 1000),
-          wl.Shape(16, 8, 256, 256, 1000)]
+          wl.Shape(8, 2, 128, 256, 1000), wl.Shape(16, 8, 256, 256, 1000)]
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"h{s.n_q_heads}-{s.n_kv_heads}-d{s.d_head}")
@@ -82,8 +84,9 @@ def _unit_rows(lay, source):
     return u.start, u.size
 
 
-@pytest.mark.parametrize("shape", [wl.Shape(4, 2, 64, 256, 1000), wl.Shape(16, 8, 256, 256, 1000)],
-                         ids=["d64", "d256"])
+@pytest.mark.parametrize("shape", [wl.Shape(4, 2, 64, 256, 1000), wl.Shape(8, 8, 128, 256, 1000),
+                                   wl.Shape(8, 2, 128, 256, 1000), wl.Shape(16, 8, 256, 256, 1000)],
+                         ids=["d64-pair", "d128-single", "d128-cg2", "d256-cg2"])
 def test_packing_invariance_bitwise(spinf, shape):
     target = wl.stress(n_questions=12, content_tokens=230, vocab=1000)[0]
     others = wl.short_inputs(vocab=1000, n=40)
