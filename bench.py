@@ -36,6 +36,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "packed tokens/s and scored questions/s per GB300; % of tensor/HBM roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes (read + write) of one score_main_kernel launch, from one ncu capture of the
+# Wikinews-shaped pass 0 with the bf16 lm head (2.020 GB read = the head once, 9.1 MB written).
+# Keyed by (workload, fp8); any other case reports null.
+NCU_SCORE_TRAFFIC = {("wikinews", False): 2.020e9 + 9.1e6}
 
 
 def _peaks():
@@ -271,7 +275,8 @@ def run_ours(args, rank, world):
                    "value_covers": "attention + scoring per pass, token-lp D2H, collect; layout resident"},
         "roofline": {"kernel": "spinf_score (gather + tcgen05 lm head + lse + combine)", "bound": "tensor",
                      "achieved": score_tflops, "peak": mma_peak, "unit": "TFLOP/s",
-                     "frac": score_tflops / mma_peak, "traffic": None,
+                     "frac": score_tflops / mma_peak,
+                     "traffic": NCU_SCORE_TRAFFIC.get((args.workload, bool(args.fp8))),
                      "peak_source": f"{peak_src} {'bf16_tflops_sustained' if peak_src == 'measured' else ''}".strip()},
         "roofline_attention": {"kernel": "spinf_branch_attention", "tensor_tflops_unmasked": attn_tflops,
                                "tensor_frac": attn_tflops / bf16_peak, "hbm_gbs": attn_gbs,
