@@ -58,15 +58,33 @@ namespace {
 
 using namespace dev;
 
-constexpr int kAttnThreads = 384;      // Q/K producer, MMA, V producer, 8 softmax warps, mask metadata
+constexpr int kAttnThreads = 384;      // TMA producer, S MMA, PV MMA, 8 softmax warps, mask metadata
 constexpr int kSoftmaxThreads = 256;
 constexpr int kFirstSoftmaxWarp = 3;
 constexpr int kMetaWarp = 11;
+constexpr int kPvWarp = 2;
 constexpr int kMetaSlots = 4;          // mask-metadata ring: tiles the metadata warp may run ahead
 constexpr int kBoxBytes = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128-byte swizzled rows)
 constexpr int kOstageBytes = 32 * 64;  // O staging of one softmax warp: 32 rows x 32 bf16
 
-enum { Q_FULL = 0, Q_EMPTY, S_FULL0, S_FULL1, P_FULL, O_DONE, PV_DONE0, PV_DONE1, N_FIXED_BARS };
+// Barrier protocol (a parity wait is only correct when its barrier is at most one phase
+// ahead of the phase waited for, so every ring below is sized for the widest lead):
+//   S_FULL[G % kSBufs]  S(G) is in TMEM: the softmax may read it; the K buffer it read is free
+//   P_FULL[G % kSBufs]  every softmax thread has written P(G).  Warps of different lane
+//                       quarters are not in lockstep: one may be at most kSBufs - 1 tiles
+//                       ahead of another (S(G) needs P(G - kSBufs) consumed), so P_FULL
+//                       has kSBufs barriers
+//   P_USED[G % 3]       PV(G) has read P(G), so S(G + 3) may overwrite that TMEM buffer
+//                       (d_head <= 128; with two S buffers V_DONE says the same).  MMAs
+//                       into different accumulators are not ordered by the tensor core.
+//   V_DONE[G & 1]       PV(G) has finished: O may be read or rescaled, its V buffer is free
+//   MMA_DONE(_PV)       all MMAs of one issuing thread have completed (before TMEM is freed)
+// In a multicast pair S_FULL and V_DONE count the commits of both CTAs, which read the
+// shared K/V buffers.
+enum {
+    Q_FULL = 0, Q_EMPTY, S_FULL0, S_FULL1, S_FULL2, P_FULL0, P_FULL1, P_FULL2, P_USED0, P_USED1, P_USED2,
+    V_DONE0, V_DONE1, MMA_DONE, MMA_DONE_PV, N_FIXED_BARS
+};
 
 template <int D, int MODE>
 struct AttnSmem {
@@ -84,20 +102,25 @@ struct AttnSmem {
     static constexpr int kXmax = kMetaHead + kMetaSlots * 4 * 4;   // float [2][2][128]: row maxima of the two halves
     static constexpr int kLx = kXmax + 2 * 2 * 128 * 4;     // float [2][128]: the halves' row sums, per item
     static constexpr int kOstage = (kLx + 2 * 128 * 4 + 1023) / 1024 * 1024;  // per softmax warp: 32 x 32 O bf16
-    // fixed barriers, then K_FULL, K_EMPTY, V_FULL, V_EMPTY [kStages], META_FULL, META_EMPTY [kMetaSlots]
+    // fixed barriers, then K_FULL, V_FULL [kStages], META_FULL, META_EMPTY [kMetaSlots]
     static constexpr int kBars = kOstage + 8 * kOstageBytes;
-    static constexpr int kNumBars = N_FIXED_BARS + 4 * kStages + 2 * kMetaSlots;
+    static constexpr int kNumBars = N_FIXED_BARS + 2 * kStages + 2 * kMetaSlots;
     static constexpr int kHolder = kBars + kNumBars * 8;
     static constexpr int kBytes = kHolder + 16;
     static constexpr int kAlloc = kBytes + 1024;            // room to align the base to 1024
     static_assert(kAlloc <= 227 * 1024, "shared memory of one CTA");
 };
 
-// TMEM columns: two S buffers [0,128) and [128,256) -- tile G uses buffer G&1,
-// and its P (bf16 pairs, 64 columns) overwrites the start of that buffer once
-// the softmax has read S -- then O [256, 256 + D).  512 columns, so one CTA per
-// SM (the shared-memory request enforces it and no allocation ever waits).
-constexpr uint32_t kColO = 256;
+// TMEM columns: S buffers of 128 columns -- tile G uses buffer G % kSBufs, and its P
+// (bf16 pairs, 64 columns) overwrites the start of that buffer once the softmax has
+// read S -- then O (D columns).  d_head 256: two buffers, O at 256; d_head <= 128: a
+// third buffer, O at 384, so S of tile G waits for the PV of tile G - 3 (usually long
+// done) rather than G - 2.  512 columns are allocated, so one CTA per SM (the
+// shared-memory request enforces it and no allocation ever waits).
+template <int D>
+constexpr int kSBufs = D <= 128 ? 3 : 2;
+template <int D>
+constexpr uint32_t kColO = kSBufs<D> * 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMinSmem = 116 * 1024;
 // Log2 headroom of the lazy softmax reference maximum: P values stay <= 2^8.
@@ -157,19 +180,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     auto item_index = [&](int k) { return k * n_units + ((k & 1) ? n_units - 1 - unit : unit); };
 
     uint64_t* k_full = bars + N_FIXED_BARS;
-    uint64_t* k_empty = k_full + L::kStages;
-    uint64_t* v_full = k_empty + L::kStages;
-    uint64_t* v_empty = v_full + L::kStages;
-    uint64_t* meta_full = v_empty + L::kStages;
+    uint64_t* v_full = k_full + L::kStages;
+    uint64_t* v_done = bars + V_DONE0;   // [2], by tile parity
+    // barrier that says P(G) has been read, and its phase index is G / kSBufs
+    auto p_used = [&](uint32_t G) { return kSBufs<D> == 3 ? &bars[P_USED0 + G % 3] : &v_done[G & 1]; };
+    uint64_t* meta_full = v_full + L::kStages;
     uint64_t* meta_empty = meta_full + kMetaSlots;
     if (threadIdx.x == 0) {
         // P_FULL: every softmax thread, or (CG2) one arrival from each CTA of the pair
-        for (int b = 0; b < N_FIXED_BARS; ++b) mbar_init(&bars[b], b == P_FULL ? (CG2 ? 2 : kSoftmaxThreads) : 1);
+        for (int b = 0; b < N_FIXED_BARS; ++b) {
+            int count = 1;
+            if (b >= P_FULL0 && b <= P_FULL2) count = CG2 ? 2 : kSoftmaxThreads;
+            if (((b >= S_FULL0 && b <= S_FULL2) || b == V_DONE0 || b == V_DONE1) && MODE == 1)
+                count = 2;   // both CTAs' MMAs
+            mbar_init(&bars[b], count);
+        }
         for (int st = 0; st < L::kStages; ++st) {
             mbar_init(&k_full[st], 1);
             mbar_init(&v_full[st], 1);
-            mbar_init(&k_empty[st], MODE == 1 ? 2 : 1);   // MODE 1: released by the MMAs of both CTAs
-            mbar_init(&v_empty[st], MODE == 1 ? 2 : 1);
         }
         for (int sl = 0; sl < kMetaSlots; ++sl) {
             mbar_init(&meta_full[sl], 32);                       // every lane of the metadata warp
@@ -194,100 +222,145 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     constexpr uint16_t kBoth = 0x3;
 
     if (warp == 0) {
-        // ---------------------------------------------------------- Q and K producer
+        // ---------------------------------------------------------- Q, K and V producer
+        // One thread walks the tile sequence with two cursors, K (with the Q of each item)
+        // and V, and issues whichever copy's buffer is free first: a K copy never waits
+        // behind a V buffer or the other way round.  Each cursor tests its barrier phases
+        // in order, so a barrier is never two phases ahead of the phase tested.
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(CG2 ? &tm_kh : &tm_k);
-            uint32_t G = 0, ic = 0;
-            for (int k = 0;; ++k) {
-                const int it = item_index(k);
-                if (it >= n_items) break;
-                const Item I = item(it);
-                if (I.n <= 0) continue;
-                if (ic > 0) mbar_wait(&bars[Q_EMPTY], (ic - 1) & 1, err);   // the last S of the previous item is done
-                if constexpr (CG2) {   // both CTAs' Q tiles are counted on the leader's barrier
-                    if (rank == 0) mbar_arrive_expect_tx(&bars[Q_FULL], 2 * L::kTileBytes);
-                    const uint32_t qf = mapa_shared(smem_u32(&bars[Q_FULL]), 0);
-                    for (int c = 0; c < L::kChunks; ++c)
-                        tma_load_3d_pair(sQ + c * kBoxBytes, &tm_q, qf, c * 64, I.h, I.qt * 128);
-                } else {
-                    mbar_arrive_expect_tx(&bars[Q_FULL], L::kTileBytes);
-                    for (int c = 0; c < L::kChunks; ++c)
-                        tma_load_3d(sQ + c * kBoxBytes, &tm_q, &bars[Q_FULL], c * 64, I.h, I.qt * 128);
-                }
-                int kv_next = __ldg(tile_kv + I.s0);
-                for (int j = 0; j < I.n; ++j, ++G) {
-                    const int kv0 = kv_next;
-                    if (j + 1 < I.n) kv_next = __ldg(tile_kv + I.s0 + j + 1);
-                    const uint32_t st = G % L::kStages;
-                    if (G >= (uint32_t)L::kStages) mbar_wait(&k_empty[st], (G / L::kStages - 1) & 1, err);
-                    if constexpr (CG2) {   // keys [64 rank, 64 rank + 64) of the tile, counted on the leader
-                        if (rank == 0) mbar_arrive_expect_tx(&k_full[st], 2 * L::kKBytes);
-                        const uint32_t kf = mapa_shared(smem_u32(&k_full[st]), 0);
-                        for (int c = 0; c < L::kChunks; ++c)
-                            tma_load_3d_pair(sK + st * L::kKBytes + c * (kBoxBytes / 2), &tm_kh, kf, c * 64,
-                                             I.h / group, kv0 + 64 * rank);
-                    } else {
-                        mbar_arrive_expect_tx(&k_full[st], L::kTileBytes);
-                        for (int c = 0; c < L::kChunks; ++c) {
-                            uint8_t* dst = sK + st * L::kKBytes + c * kBoxBytes;
-                            if (!PAIR) tma_load_3d(dst, &tm_k, &k_full[st], c * 64, I.h / group, kv0);
-                            else if ((c & 1) == rank) tma_load_3d_mc(dst, &tm_k, &k_full[st], c * 64, I.h / group, kv0, kBoth);
-                        }
-                    }
-                }
-                ++ic;
-            }
-            // our last copies have landed before the CTA may retire
-            // (CG2: a peer's copies are counted on the leader, whose release implies they landed)
-            for (uint32_t b = G > (uint32_t)L::kStages ? G - L::kStages : 0; b < G; ++b) {
-                if (!CG2 || rank == 0) mbar_wait(&k_full[b % L::kStages], (b / L::kStages) & 1, err);
-                mbar_wait(&k_empty[b % L::kStages], (b / L::kStages) & 1, err);   // every release has arrived
-            }
-            if (ic > 0) {
-                if (!CG2 || rank == 0) mbar_wait(&bars[Q_FULL], (ic - 1) & 1, err);
-                if (CG2) mbar_wait(&bars[Q_EMPTY], (ic - 1) & 1, err);
-            }
-        }
-    } else if (warp == 2) {
-        // ---------------------------------------------------------- V producer
-        if (lane == 0) {
             tma_prefetch_desc(&tm_v);
-            uint32_t G = 0;
-            for (int k = 0;; ++k) {
-                const int it = item_index(k);
-                if (it >= n_items) break;
-                const Item I = item(it);
-                if (I.n <= 0) continue;
-                int kv_next = __ldg(tile_kv + I.s0);
-                for (int j = 0; j < I.n; ++j, ++G) {
-                    const int kv0 = kv_next;
-                    if (j + 1 < I.n) kv_next = __ldg(tile_kv + I.s0 + j + 1);
-                    const uint32_t st = G % L::kStages;
-                    if (G >= (uint32_t)L::kStages) mbar_wait(&v_empty[st], (G / L::kStages - 1) & 1, err);
-                    if constexpr (CG2) {   // columns [D/2 rank, D/2 rank + D/2) of the tile, counted on the leader
-                        if (rank == 0) mbar_arrive_expect_tx(&v_full[st], 2 * L::kVBytes);
-                        const uint32_t vf = mapa_shared(smem_u32(&v_full[st]), 0);
-                        for (int cc = 0; cc < L::kChunks / 2; ++cc)
-                            tma_load_3d_pair(sV + st * L::kVBytes + cc * kBoxBytes, &tm_v, vf,
-                                             (rank * (L::kChunks / 2) + cc) * 64, I.h / group, kv0);
+            struct Cursor {
+                int k;        // item ordinal
+                Item I;
+                int j;        // tile within the item
+                uint32_t G;   // tile of the CTA's sequence
+                int kv0;      // first key of tile G
+                bool done;
+            };
+            auto seek = [&](Cursor& c) {   // from item ordinal c.k onwards, the first item with tiles
+                for (;; ++c.k) {
+                    const int it = item_index(c.k);
+                    if (it >= n_items) {
+                        c.done = true;
+                        return;
+                    }
+                    c.I = item(it);
+                    if (c.I.n > 0) break;
+                }
+                c.j = 0;
+                c.kv0 = __ldg(tile_kv + c.I.s0);
+            };
+            auto advance = [&](Cursor& c) {
+                ++c.G;
+                if (++c.j < c.I.n) {
+                    c.kv0 = __ldg(tile_kv + c.I.s0 + c.j);
+                } else {
+                    ++c.k;
+                    seek(c);
+                }
+            };
+            Cursor kc{0, Item{0, 0, 0, 0}, 0, 0, 0, false}, vc = kc;
+            seek(kc);
+            seek(vc);
+            uint32_t ic = 0;          // Q copies issued
+            bool q_pending = true;    // the K cursor's item still needs its Q
+            unsigned long long t_idle = 0;
+            while (!kc.done || !vc.done) {
+                bool progress = false;
+                if (!kc.done) {
+                    if (q_pending) {
+                        if (ic == 0 || mbar_test(&bars[Q_EMPTY], (ic - 1) & 1)) {   // the previous item's last S is done
+                            // one copy per tile: every 64-column chunk at once (4-D view, chunk-major in smem)
+                            if constexpr (CG2) {   // both CTAs' Q tiles are counted on the leader's barrier
+                                if (rank == 0) mbar_arrive_expect_tx(&bars[Q_FULL], 2 * L::kTileBytes);
+                                tma_load_4d_pair(sQ, &tm_q, mapa_shared(smem_u32(&bars[Q_FULL]), 0), 0, kc.I.qt * 128,
+                                                 0, kc.I.h);
+                            } else {
+                                mbar_arrive_expect_tx(&bars[Q_FULL], L::kTileBytes);
+                                tma_load_4d(sQ, &tm_q, &bars[Q_FULL], 0, kc.I.qt * 128, 0, kc.I.h);
+                            }
+                            ++ic;
+                            q_pending = false;
+                            progress = true;
+                        }
                     } else {
-                        mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
-                        for (int c = 0; c < L::kChunks; ++c) {
-                            uint8_t* dst = sV + st * L::kVBytes + c * kBoxBytes;
-                            if (!PAIR) tma_load_3d(dst, &tm_v, &v_full[st], c * 64, I.h / group, kv0);
-                            else if ((c & 1) == rank) tma_load_3d_mc(dst, &tm_v, &v_full[st], c * 64, I.h / group, kv0, kBoth);
+                        const uint32_t G = kc.G, Gp = G - L::kStages;   // S(Gp) was the last reader of the buffer
+                        if (G < (uint32_t)L::kStages ||
+                            mbar_test(&bars[S_FULL0 + Gp % kSBufs<D>], (Gp / kSBufs<D>) & 1)) {
+                            const uint32_t st = G % L::kStages;
+                            uint8_t* dst = sK + st * L::kKBytes;
+                            if constexpr (CG2) {   // keys [64 rank, 64 rank + 64) of the tile, counted on the leader
+                                if (rank == 0) mbar_arrive_expect_tx(&k_full[st], 2 * L::kKBytes);
+                                tma_load_4d_pair(dst, &tm_kh, mapa_shared(smem_u32(&k_full[st]), 0), 0,
+                                                 kc.kv0 + 64 * rank, 0, kc.I.h / group);
+                            } else {
+                                mbar_arrive_expect_tx(&k_full[st], L::kTileBytes);
+                                if (!PAIR) tma_load_4d(dst, &tm_k, &k_full[st], 0, kc.kv0, 0, kc.I.h / group);
+                                else if ((G & 1) == (uint32_t)rank)   // the pair's CTAs take alternate K tiles
+                                    tma_load_4d_mc(dst, &tm_k, &k_full[st], 0, kc.kv0, 0, kc.I.h / group, kBoth);
+                            }
+                            const int k_before = kc.k;
+                            advance(kc);
+                            if (kc.k != k_before) q_pending = true;
+                            progress = true;
                         }
                     }
                 }
+                if (!vc.done) {
+                    const uint32_t G = vc.G, Gp = G - L::kStages;   // PV(Gp) was the last reader of the buffer
+                    if (G < (uint32_t)L::kStages || mbar_test(&v_done[Gp & 1], (Gp >> 1) & 1)) {
+                        const uint32_t st = G % L::kStages;
+                        uint8_t* dst = sV + st * L::kVBytes;
+                        if constexpr (CG2) {   // chunks [D/128 rank, D/128 rank + D/128), counted on the leader
+                            if (rank == 0) mbar_arrive_expect_tx(&v_full[st], 2 * L::kVBytes);
+                            tma_load_4d_pair(dst, &tm_v, mapa_shared(smem_u32(&v_full[st]), 0), 0, vc.kv0,
+                                             rank * (L::kChunks / 2), vc.I.h / group);
+                        } else {
+                            mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
+                            if (!PAIR) tma_load_4d(dst, &tm_v, &v_full[st], 0, vc.kv0, 0, vc.I.h / group);
+                            else if ((G & 1) != (uint32_t)rank)   // the other CTA of the pair takes this V tile
+                                tma_load_4d_mc(dst, &tm_v, &v_full[st], 0, vc.kv0, 0, vc.I.h / group, kBoth);
+                        }
+                        advance(vc);
+                        progress = true;
+                    }
+                }
+                if (progress) {
+                    t_idle = 0;
+                } else {   // bounded like every other wait; back off so the softmax warps sharing
+                           // this scheduler keep its issue slots
+                    __nanosleep(64);
+                    if (*reinterpret_cast<volatile int*>(err) != 0) break;
+                    const unsigned long long now = globaltimer();
+                    if (t_idle == 0) t_idle = now;
+                    else if (now - t_idle > kWaitLimitNs) {
+                        atomicCAS(err, 0, kErrTimeout);
+                        break;
+                    }
+                }
             }
-            for (uint32_t b = G > (uint32_t)L::kStages ? G - L::kStages : 0; b < G; ++b) {
-                if (!CG2 || rank == 0) mbar_wait(&v_full[b % L::kStages], (b / L::kStages) & 1, err);
-                mbar_wait(&v_empty[b % L::kStages], (b / L::kStages) & 1, err);
+            // our last copies have landed before the CTA may retire, and every commit that
+            // another thread or CTA makes to our barriers has arrived
+            // (CG2: a peer's copies are counted on the leader, whose release implies they landed)
+            const uint32_t GK = kc.G, GV = vc.G;
+            for (uint32_t b = GK > (uint32_t)L::kStages ? GK - L::kStages : 0; b < GK; ++b)
+                if (!CG2 || rank == 0) mbar_drain(&k_full[b % L::kStages], (b / L::kStages) & 1, err);
+            for (uint32_t b = GK > (uint32_t)kSBufs<D> ? GK - kSBufs<D> : 0; b < GK; ++b)
+                mbar_drain(&bars[S_FULL0 + b % kSBufs<D>], (b / kSBufs<D>) & 1, err);
+            for (uint32_t b = GV > (uint32_t)L::kStages ? GV - L::kStages : 0; b < GV; ++b)
+                if (!CG2 || rank == 0) mbar_drain(&v_full[b % L::kStages], (b / L::kStages) & 1, err);
+            for (uint32_t b = GV > 2u ? GV - 2 : 0; b < GV; ++b) mbar_drain(&v_done[b & 1], (b >> 1) & 1, err);
+            if (ic > 0) {
+                if (!CG2 || rank == 0) mbar_drain(&bars[Q_FULL], (ic - 1) & 1, err);
+                if (CG2) mbar_drain(&bars[Q_EMPTY], (ic - 1) & 1, err);
             }
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || warp == kPvWarp) {
+        // ---------------------------------------------------------- MMA issuers
+        // S = Q K^T from warp 1, O += P V from warp 2: two instruction streams, so the tensor
+        // core has the other stream's MMAs to run while one thread commits or waits
         if (lane == 0 && (!CG2 || rank == 0)) {   // a pair's MMAs are all issued by its leader
             constexpr uint32_t idesc_qk = idesc_bf16(CG2 ? 256 : 128, 128, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16(CG2 ? 256 : 128, D, false, true);
@@ -295,66 +368,70 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if constexpr (CG2) mma_commit_pair(bar); else mma_commit(bar);
             };
             const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-            // S(Gs) goes to buffer Gs&1, which held P(Gs-2): PV(Gs-2) must be done.  PV_DONE[b]
-            // completes once per PV that read buffer b, so its phases cannot be overtaken here.
-            auto issue_s = [&](uint32_t Gs) {
-                if (Gs >= 2) mbar_wait(&bars[PV_DONE0 + (Gs & 1)], ((Gs - 2) >> 1) & 1, err);
-                const uint32_t st = Gs % L::kStages;
-                mbar_wait(&k_full[st], (Gs / L::kStages) & 1, err);
-                tc_fence_after();
-                const uint32_t dS = tmem + (Gs & 1) * 128;
-                const uint32_t aKs = aK + st * L::kKBytes;
-                constexpr int kKBox = CG2 ? kBoxBytes / 2 : kBoxBytes;   // K boxes hold 64 or 128 keys
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                    const uint32_t koff = (kk >> 2) * kKBox + (kk & 3) * 32;
-                    if constexpr (CG2)
-                        mma_f16_ss_pair(dS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aKs + koff, 16, 1024),
-                                        idesc_qk, kk > 0);
-                    else
-                        mma_f16_ss(dS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aKs + koff, 16, 1024), idesc_qk,
-                                   kk > 0);
-                }
-                if constexpr (MODE == 1) mma_commit_mc(&k_empty[st], kBoth); else commit(&k_empty[st]);
-                commit(&bars[S_FULL0 + (Gs & 1)]);
+            auto commit_shared = [&](uint64_t* bar) {   // a barrier that counts both CTAs of a multicast pair
+                if constexpr (MODE == 1) mma_commit_mc(bar, kBoth); else commit(bar);
             };
+            const bool s_issuer = warp == 1;
             uint32_t G = 0, ic = 0;
             for (int k = 0;; ++k) {
                 const int it = item_index(k);
                 if (it >= n_items) break;
                 const Item I = item(it);
                 if (I.n <= 0) continue;
-                const uint32_t G0 = G;
-                mbar_wait(&bars[Q_FULL], ic & 1, err);
-                issue_s(G0);
-                if (I.n == 1) commit(&bars[Q_EMPTY]);
-                for (int j = 0; j < I.n; ++j) {
-                    const uint32_t Gj = G0 + j;
-                    if (j + 1 < I.n) {
-                        issue_s(Gj + 1);
-                        if (j + 2 == I.n) commit(&bars[Q_EMPTY]);   // Q is free once this S is done
-                    }
-                    if constexpr (CG2) mbar_wait_cluster(&bars[P_FULL], Gj & 1, err);   // the peer arrives remotely
-                    else mbar_wait(&bars[P_FULL], Gj & 1, err);
-                    const uint32_t st = Gj % L::kStages;
-                    mbar_wait(&v_full[st], (Gj / L::kStages) & 1, err);
-                    tc_fence_after();
-                    const uint32_t aP = tmem + (Gj & 1) * 128;
-                    const uint32_t aVs = aV + st * L::kVBytes;
+                if (s_issuer) {
+                    mbar_wait(&bars[Q_FULL], ic & 1, err);
+                    for (int j = 0; j < I.n; ++j) {
+                        const uint32_t Gs = G + j;
+                        // buffer Gs % kSBufs held P(Gs - kSBufs): that PV has read it
+                        if (Gs >= (uint32_t)kSBufs<D>) {
+                            const uint32_t Gp = Gs - kSBufs<D>;
+                            mbar_wait(p_used(Gp), (Gp / kSBufs<D>) & 1, err);
+                        }
+                        const uint32_t st = Gs % L::kStages;
+                        mbar_wait(&k_full[st], (Gs / L::kStages) & 1, err);
+                        tc_fence_after();
+                        const uint32_t dS = tmem + (Gs % kSBufs<D>) * 128;
+                        const uint32_t aKs = aK + st * L::kKBytes;
+                        constexpr int kKBox = CG2 ? kBoxBytes / 2 : kBoxBytes;   // K boxes hold 64 or 128 keys
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {   // 16 keys: 8 TMEM columns of bf16 pairs of P
-                        const uint64_t db = sdesc_sw128(aVs + kk * 2048, kBoxBytes, 1024);
-                        if constexpr (CG2) mma_f16_ts_pair(tmem + kColO, aP + kk * 8, db, idesc_pv, 1);
-                        else mma_f16_ts(tmem + kColO, aP + kk * 8, db, idesc_pv, 1);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+                            const uint32_t koff = (kk >> 2) * kKBox + (kk & 3) * 32;
+                            const uint64_t da = sdesc_sw128(aQ + off, 16, 1024), db = sdesc_sw128(aKs + koff, 16, 1024);
+                            if constexpr (CG2) mma_f16_ss_pair(dS, da, db, idesc_qk, kk > 0);
+                            else mma_f16_ss(dS, da, db, idesc_qk, kk > 0);
+                        }
+                        commit_shared(&bars[S_FULL0 + Gs % kSBufs<D>]);
+                        if (j + 1 == I.n) commit(&bars[Q_EMPTY]);   // Q is free once the item's last S is done
                     }
-                    if constexpr (MODE == 1) mma_commit_mc(&v_empty[st], kBoth); else commit(&v_empty[st]);
-                    commit(&bars[O_DONE]);
-                    commit(&bars[PV_DONE0 + (Gj & 1)]);
+                } else {
+                    for (int j = 0; j < I.n; ++j) {
+                        const uint32_t Gj = G + j;
+                        uint64_t* pf = &bars[P_FULL0 + Gj % kSBufs<D>];
+                        if constexpr (CG2) mbar_wait_cluster(pf, (Gj / kSBufs<D>) & 1, err);   // the peer arrives remotely
+                        else mbar_wait(pf, (Gj / kSBufs<D>) & 1, err);
+                        const uint32_t st = Gj % L::kStages;
+                        mbar_wait(&v_full[st], (Gj / L::kStages) & 1, err);
+                        tc_fence_after();
+                        const uint32_t aP = tmem + (Gj % kSBufs<D>) * 128;
+                        const uint32_t aVs = aV + st * L::kVBytes;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {   // 16 keys: 8 TMEM columns of bf16 pairs of P
+                            const uint64_t db = sdesc_sw128(aVs + kk * 2048, kBoxBytes, 1024);
+                            if constexpr (CG2) mma_f16_ts_pair(tmem + kColO<D>, aP + kk * 8, db, idesc_pv, 1);
+                            else mma_f16_ts(tmem + kColO<D>, aP + kk * 8, db, idesc_pv, 1);
+                        }
+                        commit_shared(&v_done[Gj & 1]);
+                        if constexpr (kSBufs<D> == 3) commit(&bars[P_USED0 + Gj % 3]);
+                    }
                 }
                 G += I.n;
                 ++ic;
             }
+            // every MMA of this thread has completed before TMEM is freed
+            uint64_t* done = &bars[s_issuer ? MMA_DONE : MMA_DONE_PV];
+            commit(done);
+            mbar_drain(done, 0, err);
         }
     } else if (warp == kMetaWarp) {
         // ---------------------------------------------------------- mask metadata of each KV tile
@@ -399,7 +476,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int r = quarter * 32 + lane;            // Q-tile row of this thread
         const int t = sw * 32 + lane;                 // 0..255
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tO = tmem + lane_off + kColO + half * (D / 2);
+        const uint32_t tO = tmem + lane_off + kColO<D> + half * (D / 2);
         const uint32_t pair_bar = 2 + quarter;        // the two warps that share these TMEM lanes
         float* xmax = reinterpret_cast<float*>(smem + L::kXmax);
         float* lx = reinterpret_cast<float*>(smem + L::kLx);
@@ -428,13 +505,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int pos_q = __ldg(pos + q_row);
             float m = -INFINITY, l = 0.f;   // l: this half's share of the row sum
             for (int j = 0; j < I.n; ++j, ++G) {
-                const int b = G & 1;
+                const int b = G & 1;                  // xmax buffer
+                const int sb = G % kSBufs<D>;         // TMEM S buffer
                 const int slot = G % kMetaSlots;
                 mbar_wait(&meta_full[slot], (G / kMetaSlots) & 1, err);
                 const int4 head = *reinterpret_cast<const int4*>(meta_head + 4 * slot);   // min end, min pos, kv0, len
-                mbar_wait(&bars[S_FULL0 + b], (G >> 1) & 1, err);
+                mbar_wait(&bars[S_FULL0 + sb], (G / kSBufs<D>) & 1, err);
                 tc_fence_after();
-                const uint32_t tS = tmem + lane_off + b * 128;
+                const uint32_t tS = tmem + lane_off + sb * 128;
                 float s[64];
                 {
                     uint32_t rr[64];
@@ -507,16 +585,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                     if (grow) alpha = fast_exp2(fmaf(m, scale_log2, -mb));
                 }
-                if (j > 0) {   // PV of the previous tile has written O and read its P
-                    mbar_wait(&bars[O_DONE], (G - 1) & 1, err);
-                    tc_fence_after();
-                }
                 if (m_new != -INFINITY) {
                     l = l * alpha + rowsum;
                     m = m_new;
                 }
-                // TMEM traffic is warp-collective: lanes whose maximum did not move multiply by exactly 1
+                // TMEM traffic is warp-collective: lanes whose maximum did not move multiply by exactly 1.
+                // Only a rescale waits for the previous tile's PV (grow is false on an item's first
+                // tile); P(j) itself goes to a buffer whose last reader, PV(j-2), finished before S(j).
                 if (__any_sync(0xffffffffu, grow)) {
+                    const uint32_t Gp = G - 1;
+                    mbar_wait(&v_done[Gp & 1], (Gp >> 1) & 1, err);
+                    tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < D / 64; ++c) {
                         uint32_t rr[32];
@@ -534,16 +613,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if constexpr (CG2) {   // one arrival per CTA on the leader's barrier
                     named_bar_sync(1, kSoftmaxThreads);
                     if (t == 0) {
-                        if (rank == 0) mbar_arrive(&bars[P_FULL]);
-                        else mbar_arrive_cluster(mapa_shared(smem_u32(&bars[P_FULL]), 0));
+                        if (rank == 0) mbar_arrive(&bars[P_FULL0 + sb]);
+                        else mbar_arrive_cluster(mapa_shared(smem_u32(&bars[P_FULL0 + sb]), 0));
                     }
                 } else {
-                    mbar_arrive(&bars[P_FULL]);
+                    mbar_arrive(&bars[P_FULL0 + sb]);
                 }
             }
             // epilogue of the item: O / l to global memory, then O back to zero for the next item
-            mbar_wait(&bars[O_DONE], (G - 1) & 1, err);
-            tc_fence_after();
+            {   // PV(G - 2) first: only then is PV(G - 1)'s barrier known to be at most one phase ahead
+                if (G >= 2) mbar_wait(&v_done[G & 1], ((G - 2) >> 1) & 1, err);
+                mbar_wait(&v_done[(G - 1) & 1], ((G - 1) >> 1) & 1, err);
+                tc_fence_after();
+            }
             lx[half * 128 + r] = l;
             named_bar_sync(pair_bar, 64);
             const float lrow = lx[r] + lx[128 + r];      // halves added in a fixed order
@@ -661,21 +743,27 @@ spinf_status launch_mode(const Pass& P, const CUtensorMap& tq, const CUtensorMap
 template <int D>
 spinf_status launch_attention(const Pass& P, const void* q, const void* k, const void* v, void* o, int Hq,
                               int Hkv, float scale, int window, int* err, cudaStream_t stream) {
-    CUtensorMap tq, tk, tkh, tv;
-    const uint64_t dq[3] = {(uint64_t)D, (uint64_t)Hq, (uint64_t)P.T_pad};
-    const uint64_t sq[2] = {(uint64_t)D * 2, (uint64_t)Hq * D * 2};
-    const uint64_t dk[3] = {(uint64_t)D, (uint64_t)Hkv, (uint64_t)P.T_pad};
-    const uint64_t sk[2] = {(uint64_t)D * 2, (uint64_t)Hkv * D * 2};
-    const uint32_t box[3] = {64, 1, 128};
-    const uint32_t hbox[3] = {64, 1, 64};   // half a K tile: the keys one CTA of a pair holds
+    CUtensorMap tq, tk, tkh, tv, tvh;
+    // 4-D views (64 columns, rows, 64-column chunks, head): one box holds every chunk of a
+    // tile, laid out chunk after chunk (128-byte swizzled rows), as the MMA descriptors expect
+    constexpr uint32_t kCh = D / 64;
+    const uint64_t dq[4] = {64, (uint64_t)P.T_pad, kCh, (uint64_t)Hq};
+    const uint64_t sq[3] = {(uint64_t)Hq * D * 2, 128, (uint64_t)D * 2};
+    const uint64_t dk[4] = {64, (uint64_t)P.T_pad, kCh, (uint64_t)Hkv};
+    const uint64_t sk[3] = {(uint64_t)Hkv * D * 2, 128, (uint64_t)D * 2};
+    const uint32_t box[4] = {64, 128, kCh, 1};
+    const uint32_t kbox_half[4] = {64, 64, kCh, 1};                        // keys of one CTA of a pair
+    const uint32_t vbox_half[4] = {64, 128, kCh > 1 ? kCh / 2 : 1, 1};     // chunks of one CTA of a pair
     spinf_status st;
-    if ((st = make_tmap(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dq, sq, box, CU_TENSOR_MAP_SWIZZLE_128B)))
+    if ((st = make_tmap(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, q, dq, sq, box, CU_TENSOR_MAP_SWIZZLE_128B)))
         return st;
-    if ((st = make_tmap(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k, dk, sk, box, CU_TENSOR_MAP_SWIZZLE_128B)))
+    if ((st = make_tmap(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k, dk, sk, box, CU_TENSOR_MAP_SWIZZLE_128B)))
         return st;
-    if ((st = make_tmap(&tkh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k, dk, sk, hbox, CU_TENSOR_MAP_SWIZZLE_128B)))
+    if ((st = make_tmap(&tkh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k, dk, sk, kbox_half, CU_TENSOR_MAP_SWIZZLE_128B)))
         return st;
-    if ((st = make_tmap(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v, dk, sk, box, CU_TENSOR_MAP_SWIZZLE_128B)))
+    if ((st = make_tmap(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dk, sk, box, CU_TENSOR_MAP_SWIZZLE_128B)))
+        return st;
+    if ((st = make_tmap(&tvh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dk, sk, vbox_half, CU_TENSOR_MAP_SWIZZLE_128B)))
         return st;
     __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
     const float scale_log2 = scale * 1.4426950408889634f;
@@ -684,7 +772,7 @@ spinf_status launch_attention(const Pass& P, const void* q, const void* k, const
     // multicast pair measured faster: its softmax warps are not coupled across the two SMs)
     if ((Hq / Hkv) % 2 != 0) return launch_mode<D, 0>(P, tq, tk, tkh, tv, ob, Hq, Hkv, scale_log2, window, err, stream);
     if constexpr (D == 128)
-        return launch_mode<D, 2>(P, tq, tk, tkh, tv, ob, Hq, Hkv, scale_log2, window, err, stream);
+        return launch_mode<D, 2>(P, tq, tk, tkh, tvh, ob, Hq, Hkv, scale_log2, window, err, stream);
     else
         return launch_mode<D, 1>(P, tq, tk, tkh, tv, ob, Hq, Hkv, scale_log2, window, err, stream);
 }
