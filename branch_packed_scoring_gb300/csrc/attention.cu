@@ -78,12 +78,15 @@ constexpr int kOstageBytes = 32 * 64;  // O staging of one softmax warp: 32 rows
 //                       (d_head <= 128; with two S buffers V_DONE says the same).  MMAs
 //                       into different accumulators are not ordered by the tensor core.
 //   V_DONE[G & 1]       PV(G) has finished: O may be read or rescaled, its V buffer is free
-//   MMA_DONE(_PV)       all MMAs of one issuing thread have completed (before TMEM is freed)
+//   MMA_DONE(_PV)       all MMAs of one issuer thread have completed (before TMEM is freed)
+//   S_HALF, K_FULL_H1   single K buffer (d_head 256 outside a cta_group::2 pair): the tile
+//                       is copied in two halves of 128 columns; S_HALF says S(G) has read
+//                       the first half, so K(G+1)'s first half may land while S(G) finishes
 // In a multicast pair S_FULL and V_DONE count the commits of both CTAs, which read the
 // shared K/V buffers.
 enum {
     Q_FULL = 0, Q_EMPTY, S_FULL0, S_FULL1, S_FULL2, P_FULL0, P_FULL1, P_FULL2, P_USED0, P_USED1, P_USED2,
-    V_DONE0, V_DONE1, MMA_DONE, MMA_DONE_PV, N_FIXED_BARS
+    V_DONE0, V_DONE1, MMA_DONE, MMA_DONE_PV, S_HALF, K_FULL_H1, N_FIXED_BARS
 };
 
 template <int D, int MODE>
@@ -146,6 +149,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     using L = AttnSmem<D, MODE>;
     constexpr bool PAIR = MODE != 0;
     constexpr bool CG2 = MODE == 2;
+    constexpr bool kHalfK = L::kStages == 1;   // single K buffer: copied in two halves
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem + L::kQ;
@@ -191,7 +195,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int b = 0; b < N_FIXED_BARS; ++b) {
             int count = 1;
             if (b >= P_FULL0 && b <= P_FULL2) count = CG2 ? 2 : kSoftmaxThreads;
-            if (((b >= S_FULL0 && b <= S_FULL2) || b == V_DONE0 || b == V_DONE1) && MODE == 1)
+            if (((b >= S_FULL0 && b <= S_FULL2) || b == V_DONE0 || b == V_DONE1 || b == S_HALF) && MODE == 1)
                 count = 2;   // both CTAs' MMAs
             mbar_init(&bars[b], count);
         }
@@ -265,6 +269,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             seek(kc);
             seek(vc);
             uint32_t ic = 0;          // Q copies issued
+            int k_part = 0;           // half of the K tile to copy next (single K buffer)
             bool q_pending = true;    // the K cursor's item still needs its Q
             unsigned long long t_idle = 0;
             while (!kc.done || !vc.done) {
@@ -283,6 +288,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             }
                             ++ic;
                             q_pending = false;
+                            progress = true;
+                        }
+                    } else if constexpr (kHalfK) {
+                        // two copies per tile, each of half the columns: the first waits for S(G-1)
+                        // to have read the first half only
+                        const uint32_t G = kc.G, Gp = G - 1;
+                        if (G == 0 || (k_part == 0 ? mbar_test(&bars[S_HALF], Gp & 1)
+                                                   : mbar_test(&bars[S_FULL0 + Gp % kSBufs<D>], (Gp / kSBufs<D>) & 1))) {
+                            uint64_t* fb = k_part == 0 ? &k_full[0] : &bars[K_FULL_H1];
+                            uint8_t* dst = sK + k_part * (L::kTileBytes / 2);
+                            mbar_arrive_expect_tx(fb, L::kTileBytes / 2);
+                            if (!PAIR) tma_load_4d(dst, &tm_kh, fb, 0, kc.kv0, k_part * (L::kChunks / 2), kc.I.h / group);
+                            else if ((G & 1) == (uint32_t)rank)   // the pair's CTAs take alternate K tiles
+                                tma_load_4d_mc(dst, &tm_kh, fb, 0, kc.kv0, k_part * (L::kChunks / 2), kc.I.h / group,
+                                               kBoth);
+                            if (++k_part == 2) {
+                                k_part = 0;
+                                const int k_before = kc.k;
+                                advance(kc);
+                                if (kc.k != k_before) q_pending = true;
+                            }
                             progress = true;
                         }
                     } else {
@@ -345,8 +371,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // another thread or CTA makes to our barriers has arrived
             // (CG2: a peer's copies are counted on the leader, whose release implies they landed)
             const uint32_t GK = kc.G, GV = vc.G;
-            for (uint32_t b = GK > (uint32_t)L::kStages ? GK - L::kStages : 0; b < GK; ++b)
+            for (uint32_t b = GK > (uint32_t)L::kStages ? GK - L::kStages : 0; b < GK; ++b) {
                 if (!CG2 || rank == 0) mbar_drain(&k_full[b % L::kStages], (b / L::kStages) & 1, err);
+                if (kHalfK) {
+                    mbar_drain(&bars[K_FULL_H1], b & 1, err);
+                    mbar_drain(&bars[S_HALF], b & 1, err);
+                }
+            }
             for (uint32_t b = GK > (uint32_t)kSBufs<D> ? GK - kSBufs<D> : 0; b < GK; ++b)
                 mbar_drain(&bars[S_FULL0 + b % kSBufs<D>], (b / kSBufs<D>) & 1, err);
             for (uint32_t b = GV > (uint32_t)L::kStages ? GV - L::kStages : 0; b < GV; ++b)
@@ -395,6 +426,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         constexpr int kKBox = CG2 ? kBoxBytes / 2 : kBoxBytes;   // K boxes hold 64 or 128 keys
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
+                            if (kHalfK && kk == D / 32) {   // first half read; second half landed?
+                                commit_shared(&bars[S_HALF]);
+                                mbar_wait(&bars[K_FULL_H1], Gs & 1, err);
+                                tc_fence_after();
+                            }
                             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
                             const uint32_t koff = (kk >> 2) * kKBox + (kk & 3) * 32;
                             const uint64_t da = sdesc_sw128(aQ + off, 16, 1024), db = sdesc_sw128(aKs + koff, 16, 1024);
@@ -743,7 +779,7 @@ spinf_status launch_mode(const Pass& P, const CUtensorMap& tq, const CUtensorMap
 template <int D>
 spinf_status launch_attention(const Pass& P, const void* q, const void* k, const void* v, void* o, int Hq,
                               int Hkv, float scale, int window, int* err, cudaStream_t stream) {
-    CUtensorMap tq, tk, tkh, tv, tvh;
+    CUtensorMap tq, tk, tkh, tkc, tv, tvh;
     // 4-D views (64 columns, rows, 64-column chunks, head): one box holds every chunk of a
     // tile, laid out chunk after chunk (128-byte swizzled rows), as the MMA descriptors expect
     constexpr uint32_t kCh = D / 64;
@@ -761,6 +797,8 @@ spinf_status launch_attention(const Pass& P, const void* q, const void* k, const
         return st;
     if ((st = make_tmap(&tkh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k, dk, sk, kbox_half, CU_TENSOR_MAP_SWIZZLE_128B)))
         return st;
+    if ((st = make_tmap(&tkc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k, dk, sk, vbox_half, CU_TENSOR_MAP_SWIZZLE_128B)))
+        return st;   // half of a K tile's columns (single K buffer, copied in two halves)
     if ((st = make_tmap(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dk, sk, box, CU_TENSOR_MAP_SWIZZLE_128B)))
         return st;
     if ((st = make_tmap(&tvh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dk, sk, vbox_half, CU_TENSOR_MAP_SWIZZLE_128B)))
@@ -770,11 +808,13 @@ spinf_status launch_attention(const Pass& P, const void* q, const void* k, const
     // an even number of query heads per kv head pairs two heads per item: d_head 128 as a
     // cta_group::2 pair (half tiles), d_head 64 and 256 as a multicast pair (at 256 the
     // multicast pair measured faster: its softmax warps are not coupled across the two SMs)
-    if ((Hq / Hkv) % 2 != 0) return launch_mode<D, 0>(P, tq, tk, tkh, tv, ob, Hq, Hkv, scale_log2, window, err, stream);
+    // the kernel's third map: a K tile's key half (cta_group::2 pair) or column half (single K buffer)
+    const CUtensorMap& kpart = D == 256 ? tkc : tkh;
+    if ((Hq / Hkv) % 2 != 0) return launch_mode<D, 0>(P, tq, tk, kpart, tv, ob, Hq, Hkv, scale_log2, window, err, stream);
     if constexpr (D == 128)
         return launch_mode<D, 2>(P, tq, tk, tkh, tvh, ob, Hq, Hkv, scale_log2, window, err, stream);
     else
-        return launch_mode<D, 1>(P, tq, tk, tkh, tv, ob, Hq, Hkv, scale_log2, window, err, stream);
+        return launch_mode<D, 1>(P, tq, tk, kpart, tv, ob, Hq, Hkv, scale_log2, window, err, stream);
 }
 
 }  // namespace
