@@ -57,7 +57,7 @@ _P = ctypes.POINTER(ctypes.c_int32)
 class _PassInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("T", "T_pad", "n_qtiles", "n_sched", "M", "G", "n_units")] + \
                [(n, _P) for n in ("tok", "parent", "pos", "end", "anchor", "tile_ptr", "tile_kv", "tile_len", "slot_row",
-                                  "gather_m", "gather_tok", "unit_start", "unit_source")]
+                                  "gather_m", "gather_tok", "unit_start", "unit_source", "row_runs")]
 
 
 _D = ctypes.POINTER(ctypes.c_double)
@@ -170,6 +170,7 @@ class PassInfo:
     gather_tok: np.ndarray
     unit_start: np.ndarray
     unit_source: np.ndarray
+    row_runs: np.ndarray
 
 
 def _marshal(inputs):
@@ -288,7 +289,8 @@ class Plan:
             tile_ptr=arr(info.tile_ptr, info.n_qtiles + 1), tile_kv=arr(info.tile_kv, info.n_sched), tile_len=arr(info.tile_len, info.n_sched),
             slot_row=arr(info.slot_row, info.M), gather_m=arr(info.gather_m, info.G),
             gather_tok=arr(info.gather_tok, info.G), unit_start=arr(info.unit_start, info.n_units + 1),
-            unit_source=arr(info.unit_source, info.n_units))
+            unit_source=arr(info.unit_source, info.n_units),
+            row_runs=arr(info.row_runs, 8 * info.T_pad).reshape(info.T_pad, 8))
 
     def counts(self):
         nq, no = ctypes.c_int64(), ctypes.c_int64()

@@ -143,7 +143,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ o,
                             const int32_t* __restrict__ end, const int32_t* __restrict__ pos,
                             const int32_t* __restrict__ qt_work, const int32_t* __restrict__ tile_kv,
-                            const int32_t* __restrict__ tile_len, int T, int Hq, int Hkv, int n_items,
+                            const int32_t* __restrict__ tile_len, const int32_t* __restrict__ row_runs, int T,
+                            int Hq, int Hkv, int n_items,
                             float scale_log2, int window, int* __restrict__ err) {
     static_assert(MODE != 2 || D >= 128, "a cta_group::2 pair splits V into 64-column boxes");
     using L = AttnSmem<D, MODE>;
@@ -539,6 +540,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int q_row = I.qt * 128 + r;
             const bool real = q_row < T;
             const int pos_q = __ldg(pos + q_row);
+            // the row's root path as up to four runs of rows [lo, hi) (x < 0: more runs)
+            const int4 run01 = __ldg(reinterpret_cast<const int4*>(row_runs) + 2 * q_row);
+            const int4 run23 = __ldg(reinterpret_cast<const int4*>(row_runs) + 2 * q_row + 1);
             float m = -INFINITY, l = 0.f;   // l: this half's share of the row sum
             for (int j = 0; j < I.n; ++j, ++G) {
                 const int b = G & 1;                  // xmax buffer
@@ -565,6 +569,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (all_visible) {
 #pragma unroll
                     for (int i = 0; i < 64; ++i) mx = fmaxf(mx, s[i]);
+                } else if (window <= 0 && run01.x >= 0) {
+                    // visible keys of this half from the row's runs: no per-key loads
+                    const int kb = head.z + 64 * half;
+                    auto bits = [&](int lo, int hi) -> uint64_t {
+                        const int a = max(lo - kb, 0), b = min(hi - kb, 64);
+                        if (a >= b) return 0ull;
+                        const uint64_t upto = b == 64 ? ~0ull : ((1ull << b) - 1ull);
+                        return upto & ~((1ull << a) - 1ull);
+                    };
+                    uint64_t vm = bits(run01.x, run01.y) | bits(run01.z, run01.w) | bits(run23.x, run23.y) |
+                                  bits(run23.z, run23.w);
+                    // only the tile's own keys: the rest belong to the next input, whose own
+                    // anchored tiles cover them
+                    const int lim = min(max(head.w - 64 * half, 0), 64);
+                    if (lim < 64) vm &= (1ull << lim) - 1ull;
+                    if (!real) vm = 0ull;
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) {
+                        s[i] = ((vm >> i) & 1ull) ? s[i] : -INFINITY;
+                        mx = fmaxf(mx, s[i]);
+                    }
                 } else {
                     const int4* e4 = reinterpret_cast<const int4*>(meta + slot * 256 + half * 64);
                     const int4* p4 = reinterpret_cast<const int4*>(meta + slot * 256 + 128 + half * 64);
@@ -744,7 +769,8 @@ spinf_status launch_mode(const Pass& P, const CUtensorMap& tq, const CUtensorMap
     if (MODE == 0) {
         const int grid = std::min(n_items, sm_count());
         kernel<<<grid, kAttnThreads, smem, stream>>>(tq, tk, tkh, tv, o, P.dev.end, P.dev.pos, P.dev.qt_work,
-                                                     P.dev.tile_kv, P.dev.tile_len, P.T, Hq, Hkv, n_items,
+                                                     P.dev.tile_kv, P.dev.tile_len, P.dev.row_runs, P.T, Hq, Hkv,
+                                                     n_items,
                                                      scale_log2, window, err);
     } else {   // clusters of two CTAs, two heads of a kv group per item
         cudaLaunchAttribute attr[1];
@@ -767,8 +793,8 @@ spinf_status launch_mode(const Pass& P, const CUtensorMap& tq, const CUtensorMap
         cfg.gridDim = dim3(2 * std::min(n_items, clusters));
         e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tkh, tv, o, (const int32_t*)P.dev.end,
                                (const int32_t*)P.dev.pos, (const int32_t*)P.dev.qt_work,
-                               (const int32_t*)P.dev.tile_kv, (const int32_t*)P.dev.tile_len, P.T, Hq, Hkv, n_items,
-                               scale_log2, window, err);
+                               (const int32_t*)P.dev.tile_kv, (const int32_t*)P.dev.tile_len,
+                               (const int32_t*)P.dev.row_runs, P.T, Hq, Hkv, n_items, scale_log2, window, err);
         if (e != cudaSuccess) return cuda_fail(e, "attention launch");
     }
     e = cudaGetLastError();

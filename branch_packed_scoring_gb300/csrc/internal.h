@@ -26,12 +26,13 @@ struct PassDevice {
     int32_t* row_gptr = nullptr;   // [M + 1] gathers of each scoring row ...
     int32_t* row_glist = nullptr;  // [G]     ... sorted by token id, then gather index
     int32_t* qt_work = nullptr;    // [n_qtiles][4] attention work order {qt, s0, n, 0}, most KV tiles first
+    int32_t* row_runs = nullptr;   // [T_pad][8] root path of each row as <= 4 runs [lo, hi) (lo0 -1: more)
 };
 
 struct Pass {
     int32_t T = 0, T_pad = 0;
     std::vector<int32_t> tok, parent, pos, end, anchor;
-    std::vector<int32_t> tile_ptr, tile_kv, tile_len, qt_work;
+    std::vector<int32_t> tile_ptr, tile_kv, tile_len, qt_work, row_runs;
     std::vector<int32_t> slot_row, gather_m, gather_tok;
     std::vector<int32_t> row_gptr, row_glist;
     std::vector<int32_t> unit_start, unit_source;

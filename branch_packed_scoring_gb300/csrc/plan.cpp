@@ -374,6 +374,32 @@ extern "C" spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inp
                 P.anchor[q] = q;
             }
 
+            // Each row's visible keys (its root path) as at most four runs of consecutive
+            // rows [lo, hi), for the attention kernel's per-row mask; a row whose path has
+            // more runs gets lo0 = -1 and is masked key by key from end[] instead.
+            {
+                std::vector<int32_t> run_start(T_pad);
+                for (int32_t r = 0; r < T_pad; ++r)
+                    run_start[r] = (r > 0 && r < T && P.parent[r] == r - 1) ? run_start[r - 1] : r;
+                P.row_runs.assign(8 * (size_t)T_pad, 0);
+                for (int32_t q = 0; q < T_pad; ++q) {
+                    int32_t* out = &P.row_runs[8 * (size_t)q];
+                    int32_t hi = q + 1, r = q, n = 0;
+                    while (r >= 0) {
+                        if (n == 4) {
+                            out[0] = -1;
+                            break;
+                        }
+                        const int32_t lo = run_start[r];
+                        out[2 * n] = lo;
+                        out[2 * n + 1] = hi;
+                        ++n;
+                        r = lo < T ? P.parent[lo] : -1;
+                        hi = r + 1;
+                    }
+                }
+            }
+
             // KV-tile schedule: per Q tile, per intersecting unit, tiles anchored
             // at the unit start with some key k and some row q of the tile where
             // k <= q < end[k]
@@ -477,6 +503,7 @@ extern "C" spinf_status spinf_plan_pass_info(const spinf_plan* plan, int32_t pas
     out->gather_tok = P.gather_tok.data();
     out->unit_start = P.unit_start.data();
     out->unit_source = P.unit_source.data();
+    out->row_runs = P.row_runs.data();
     return SPINF_OK;
 }
 

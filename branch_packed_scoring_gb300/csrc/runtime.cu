@@ -93,9 +93,9 @@ extern "C" spinf_status spinf_plan_upload(spinf_plan* plan, int32_t pass, spinf_
     Pass& P = plan->passes[pass];
     if (P.dev.block) return SPINF_OK;
     const std::vector<int32_t>* arrays[] = {&P.end,      &P.pos,        &P.tile_ptr, &P.tile_kv,  &P.tile_len, &P.slot_row,
-                                           &P.gather_m, &P.gather_tok, &P.row_gptr, &P.row_glist, &P.qt_work};
+                                           &P.gather_m, &P.gather_tok, &P.row_gptr, &P.row_glist, &P.qt_work, &P.row_runs};
     int32_t** dst[] = {&P.dev.end,      &P.dev.pos,        &P.dev.tile_ptr, &P.dev.tile_kv,  &P.dev.tile_len, &P.dev.slot_row,
-                       &P.dev.gather_m, &P.dev.gather_tok, &P.dev.row_gptr, &P.dev.row_glist, &P.dev.qt_work};
+                       &P.dev.gather_m, &P.dev.gather_tok, &P.dev.row_gptr, &P.dev.row_glist, &P.dev.qt_work, &P.dev.row_runs};
     const int n = sizeof(arrays) / sizeof(arrays[0]);
     size_t off[16], total = 0;
     for (int i = 0; i < n; ++i) {

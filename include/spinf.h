@@ -124,6 +124,9 @@ typedef struct {
     const int32_t* gather_tok;/* [G] option token id; order: unit, question, option, token */
     const int32_t* unit_start;/* [n_units + 1] first row of each unit, then T */
     const int32_t* unit_source;/* [n_units] user input index, or -1 for a floor */
+    const int32_t* row_runs;  /* [T_pad][8] each row's visible keys (its root path) as up to four
+                                 runs [lo, hi) of consecutive rows, nearest first, unused runs
+                                 (0, 0); lo of the first run is -1 when the path has more runs */
 } spinf_pass_info;
 
 /* Per-option and per-question results, caller-owned host arrays (fp64).

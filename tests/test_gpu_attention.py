@@ -117,3 +117,17 @@ def test_wikinews_full_pass_sampled_rows(spinf):
                   | {0, lay.T - 1})
     _check(lay, o, q, k, v, shape, rows)
     assert not torch.isnan(o[:lay.T]).any()
+
+
+@pytest.mark.parametrize("shape", [wl.Shape(4, 2, 64, 256, 1000), wl.Shape(16, 8, 256, 256, 1000)], ids=["d64", "d256"])
+def test_deep_tries_every_row(spinf, shape):
+    """Rows whose root path has more than four runs take the key-by-key mask; the rest the
+    per-row runs: both against the oracle on every row."""
+    opts = [[1, 2, 5, 5, 5], [1, 3, 2, 5, 5], [1, 3, 3, 2, 5], [1, 3, 3, 3, 2]]
+    inputs = [([7, 8, 9] * 50, [([4, 4], opts), ([6], opts)]), ([], [([2, 3], opts)])] + wl.tiny(vocab=1000)
+    lay = oracle_plan(inputs, vocab=1000).passes[0]
+    plan = spinf.Plan(inputs, vocab=1000)
+    assert (plan.pass_info(0).row_runs[:, 0] == -1).any()
+    q, k, v, _ = pass_values(lay, shape, hidden_rows=False)
+    o = run_attention(spinf, plan, 0, q, k, v, shape)
+    _check(lay, o, q, k, v, shape, list(range(lay.T)))

@@ -26,7 +26,26 @@ def _compare(spinf, inputs, **opts):
             assert np.array_equal(a, b), (p, f)
         assert info.unit_start.tolist() == [u.start for u in lay.units] + [lay.T]
         assert info.unit_source.tolist() == [u.source for u in lay.units]
+        _check_runs(info, lay)
     return P, Q
+
+
+def _check_runs(info, lay, sample=512):
+    """Each row's runs (the kernel's per-row mask) cover exactly the oracle's root path."""
+    rows = np.arange(lay.T_pad)
+    if lay.T_pad > 4096:
+        g = np.random.default_rng(lay.T)
+        rows = np.unique(np.concatenate([g.choice(lay.T_pad, sample, replace=False), [0, lay.T - 1, lay.T_pad - 1]]))
+    for q in rows.tolist():
+        want = lay.visible(q) if q < lay.T else [q]
+        n_runs = 1 + sum(1 for a, b in zip(want, want[1:]) if b != a + 1)
+        r = info.row_runs[q]
+        if r[0] == -1:
+            assert n_runs > 4, q
+            continue
+        got = sorted(k for i in range(4) for k in range(r[2 * i], r[2 * i + 1]))
+        assert got == want, q
+        assert r[1] == q + 1   # nearest run first: it ends at the row itself
 
 
 @pytest.mark.parametrize("name", ["tiny", "wikinews", "moderation", "stress"])
@@ -146,3 +165,38 @@ def test_request_object_plans_identically(spinf):
         for f in FIELDS:
             assert np.array_equal(getattr(ia, f), getattr(ib, f))
             assert np.array_equal(getattr(ia, f), getattr(ic, f))
+
+
+def test_row_runs_deep_tries(spinf):
+    """Option tries whose nodes are non-first children at every level: rows whose root
+    path has more than four runs are flagged, every other row's runs are exact."""
+    opts = [[1, 2, 5, 5, 5], [1, 3, 2, 5, 5], [1, 3, 3, 2, 5], [1, 3, 3, 3, 2]]
+    inputs = [([7, 8, 9], [([4, 4], opts), ([6], opts)]), ([], [([2, 3], opts)])]
+    P, Q = _compare(spinf, inputs)
+    runs = Q.pass_info(0).row_runs
+    assert (runs[:, 0] == -1).any() and (runs[:, 0] >= 0).any()
+
+
+def test_row_runs_masks_match_visibility(spinf):
+    """The attention kernel's run mask (a row's runs intersected with a scheduled KV tile's
+    own keys, 64 columns at a time) equals k <= q < end[k] for every row of every tile."""
+    inputs = wl.stress(n_questions=24, content_tokens=300, vocab=1000) + wl.tiny(vocab=1000)
+    plan = spinf.Plan(inputs, token_budget=1024, vocab=1000)
+    for p in range(plan.num_passes):
+        info = plan.pass_info(p)
+        for qt in range(info.n_qtiles):
+            q = np.arange(qt * 128, qt * 128 + 128)
+            real = q < info.T
+            runs = info.row_runs[q].astype(np.int64)
+            for e in range(int(info.tile_ptr[qt]), int(info.tile_ptr[qt + 1])):
+                kv0, ln = int(info.tile_kv[e]), int(info.tile_len[e])
+                keys = kv0 + np.arange(128)
+                truth = (np.arange(128)[None, :] < ln) & (keys[None, :] <= q[:, None]) & \
+                    (q[:, None] < info.end[np.minimum(keys, info.T_pad - 1)][None, :]) & real[:, None]
+                got = np.zeros_like(truth)
+                for i in range(4):
+                    lo, hi = runs[:, 2 * i:2 * i + 1], runs[:, 2 * i + 1:2 * i + 2]
+                    got |= (keys[None, :] >= lo) & (keys[None, :] < hi)
+                got &= (np.arange(128)[None, :] < ln) & real[:, None]
+                use = runs[:, 0] >= 0
+                assert np.array_equal(got[use], truth[use]), (p, qt, e)
