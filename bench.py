@@ -195,6 +195,7 @@ def run_ours(args, rank, world):
             p["tlp_host"] = torch.empty(max(info.G, 1), dtype=torch.float32, pin_memory=True)
     stream.synchronize()
     tokens, questions, pairs, flops_attn, bytes_attn, flops_score = work_counts(inputs, plan, passes, shape)
+    sched_tiles = sum(int(p["info"].n_sched) for p in passes)
 
     ev = {"attn": [], "score": []}
 
@@ -280,7 +281,14 @@ def run_ours(args, rank, world):
                      "peak_source": f"{peak_src} {'bf16_tflops_sustained' if peak_src == 'measured' else ''}".strip()},
         "roofline_attention": {"kernel": "spinf_branch_attention", "tensor_tflops_unmasked": attn_tflops,
                                "tensor_frac": attn_tflops / bf16_peak, "hbm_gbs": attn_gbs,
-                               "hbm_frac": attn_gbs / hbm_peak, "unmasked_pairs": pairs},
+                               "hbm_frac": attn_gbs / hbm_peak, "unmasked_pairs": pairs,
+                               "tile_occupancy": pairs / (sched_tiles * 128 * 128),
+                               "peak_source": f"{peak_src} {'bf16_tflops_sustained' if peak_src == 'measured' else ''}".strip()},
+        # per kernel, as the scope table defines them: packed tokens per attention-kernel second
+        # (one layer call per pass) and user questions per scoring second (gather + main + combine)
+        "per_kernel": {"attention_packed_tokens_per_s": world * tokens / (attn_ms * 1e-3),
+                       "scoring_questions_per_s": world * questions / (score_ms * 1e-3),
+                       "user_questions": questions, "packed_tokens": tokens},
         "kernel_ms_per_step": {"attention": attn_ms, "score": score_ms},
         "clocks": clk,
         "gpu_launches": 4 * len(passes) * args.steps,
