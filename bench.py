@@ -241,6 +241,24 @@ def run_ours(args, rank, world):
     ms = max_over_ranks(ms, world, dev)
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["attn"]) * len(passes)
     score_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["score"]) * len(passes)
+    # workloads whose alternate layers use a sliding window: the windowed attention call is
+    # timed too (outside the step; the step holds one unwindowed layer)
+    attn_win_ms = None
+    if shape.window > 0:
+        wev = []
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, args.steps)):
+                for pi, p in enumerate(passes):
+                    q, k, v, _h = p["dev"]
+                    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a0.record(stream)
+                    spinf.branch_attention(plan, pi, q, k, v, p["o"], shape.n_q_heads, shape.n_kv_heads,
+                                           shape.d_head, window=shape.window, stream=stream)
+                    a1.record(stream)
+                    wev.append((a0, a1))
+        torch.cuda.synchronize()
+        plan.device_status(stream)
+        attn_win_ms = statistics.mean(a.elapsed_time(b) for a, b in wev) * len(passes)
 
     # end to end through the public API with host buffers
     e2e = run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev) if not args.no_e2e else None
@@ -289,7 +307,8 @@ def run_ours(args, rank, world):
         "per_kernel": {"attention_packed_tokens_per_s": world * tokens / (attn_ms * 1e-3),
                        "scoring_questions_per_s": world * questions / (score_ms * 1e-3),
                        "user_questions": questions, "packed_tokens": tokens},
-        "kernel_ms_per_step": {"attention": attn_ms, "score": score_ms},
+        "kernel_ms_per_step": {"attention": attn_ms, "score": score_ms,
+                               **({"attention_windowed": attn_win_ms, "window": shape.window} if attn_win_ms else {})},
         "clocks": clk,
         "gpu_launches": 4 * len(passes) * args.steps,
         "e2e": e2e,
