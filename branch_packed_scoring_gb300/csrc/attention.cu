@@ -39,9 +39,10 @@
 // input that owns them, so a key always lands in the same MMA column whatever
 // precedes its input in the pass; tiles are visited in a fixed order; a tile
 // with no visible key for a row is an exact no-op for that row (its maximum
-// stays, P is exactly 0 and O is multiplied by exactly 1).  O starts at zero and
-// is always accumulated, so the first visible tile takes the same path alone or
-// packed.  No result depends on which CTA runs an item.
+// stays, P is exactly 0 and O is multiplied by exactly 1).  An item's first PV
+// product overwrites O and the rest accumulate; a leading tile with no visible key
+// leaves exact zeros, to which adding the first visible tile's product gives the
+// same bits as writing it.  No result depends on which CTA runs an item.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -419,6 +420,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             const uint32_t Gp = Gs - kSBufs<D>;
                             mbar_wait(p_used(Gp), (Gp / kSBufs<D>) & 1, err);
                         }
+                        // an item's first S waits for the previous item's last PV, so that PV runs first
+                        // and the softmax warps start their epilogue sooner; this S is not needed before
+                        // that epilogue ends
+                        if (j == 0 && Gs > 0) mbar_wait(&v_done[(Gs - 1) & 1], ((Gs - 1) >> 1) & 1, err);
                         const uint32_t st = Gs % L::kStages;
                         mbar_wait(&k_full[st], (Gs / L::kStages) & 1, err);
                         tc_fence_after();
@@ -455,8 +460,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {   // 16 keys: 8 TMEM columns of bf16 pairs of P
                             const uint64_t db = sdesc_sw128(aVs + kk * 2048, kBoxBytes, 1024);
-                            if constexpr (CG2) mma_f16_ts_pair(tmem + kColO<D>, aP + kk * 8, db, idesc_pv, 1);
-                            else mma_f16_ts(tmem + kColO<D>, aP + kk * 8, db, idesc_pv, 1);
+                            // an item's first product overwrites O (adding it to zero would give the same bits)
+                            const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+                            if constexpr (CG2) mma_f16_ts_pair(tmem + kColO<D>, aP + kk * 8, db, idesc_pv, acc);
+                            else mma_f16_ts(tmem + kColO<D>, aP + kk * 8, db, idesc_pv, acc);
                         }
                         commit_shared(&v_done[Gj & 1]);
                         if constexpr (kSBufs<D> == 3) commit(&bars[P_USED0 + Gj % 3]);
@@ -518,16 +525,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         float* xmax = reinterpret_cast<float*>(smem + L::kXmax);
         float* lx = reinterpret_cast<float*>(smem + L::kLx);
 
-        auto zero_o = [&]() {
-            uint32_t z[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) z[i] = 0u;
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) tmem_st32(tO + c * 32, z);
-            tmem_st_wait();
-        };
-
-        zero_o();
         uint32_t G = 0;
         int k = 0;
         int it = item_index(0);
@@ -731,7 +728,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 tmem_ld32(tO, rr);
                 store_chunk(rr, half * (D / 2));
             }
-            zero_o();
             // lx is read by the partner before either writes it again (next item's epilogue)
             named_bar_sync(pair_bar, 64);
             }
