@@ -26,7 +26,8 @@ DTYPE_BF16, DTYPE_E4M3 = 0, 1
 #: every symbol the header declares
 SYMBOLS = [
     "spinf_plan_opts_default", "spinf_pack_plan", "spinf_plan_num_passes", "spinf_plan_pass_info",
-    "spinf_plan_counts", "spinf_plan_upload", "spinf_branch_attention", "spinf_score_workspace_bytes",
+    "spinf_plan_counts", "spinf_plan_upload", "spinf_plan_descriptor_bytes", "spinf_plan_upload_to",
+    "spinf_branch_attention", "spinf_score_workspace_bytes",
     "spinf_score", "spinf_score_static", "spinf_collect", "spinf_device_status", "spinf_plan_free", "spinf_fingerprint",
     "spinf_status_string", "spinf_last_error",
 ]
@@ -96,6 +97,9 @@ def lib():
     L.spinf_plan_pass_info.argtypes = [vp, i32, ctypes.POINTER(_PassInfo)]
     L.spinf_plan_counts.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i64)]
     L.spinf_plan_upload.argtypes = [vp, i32, vp]
+    L.spinf_plan_descriptor_bytes.argtypes = [vp, i32]
+    L.spinf_plan_descriptor_bytes.restype = sz
+    L.spinf_plan_upload_to.argtypes = [vp, i32, vp, sz, vp]
     L.spinf_branch_attention.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, f32, i32, vp]
     L.spinf_score_workspace_bytes.argtypes = [vp, i32, i32, i32, i32]
     L.spinf_score_workspace_bytes.restype = sz
@@ -109,7 +113,7 @@ def lib():
     L.spinf_status_string.argtypes = [i32]
     L.spinf_status_string.restype = ctypes.c_char_p
     L.spinf_last_error.restype = ctypes.c_char_p
-    for name in ("spinf_pack_plan", "spinf_plan_pass_info", "spinf_plan_counts", "spinf_plan_upload",
+    for name in ("spinf_pack_plan", "spinf_plan_pass_info", "spinf_plan_counts", "spinf_plan_upload", "spinf_plan_upload_to",
                  "spinf_branch_attention", "spinf_score", "spinf_score_static", "spinf_collect",
                  "spinf_device_status"):
         getattr(L, name).restype = i32
@@ -297,8 +301,17 @@ class Plan:
         _check(lib().spinf_plan_counts(self.handle, ctypes.byref(nq), ctypes.byref(no)))
         return nq.value, no.value
 
-    def upload(self, p, stream=None):
-        _check(lib().spinf_plan_upload(self.handle, p, _stream(stream)))
+    def descriptor_bytes(self, p):
+        return int(lib().spinf_plan_descriptor_bytes(self.handle, p))
+
+    def upload(self, p, stream=None, buffer=None):
+        """Descriptors of pass p to the device: into a plan-owned allocation, or into
+        `buffer` (a caller-owned uint8 device tensor of >= descriptor_bytes(p) bytes)."""
+        if buffer is None:
+            _check(lib().spinf_plan_upload(self.handle, p, _stream(stream)))
+        else:
+            _check(lib().spinf_plan_upload_to(self.handle, p, ctypes.c_void_p(buffer.data_ptr()),
+                                              buffer.numel() * buffer.element_size(), _stream(stream)))
 
     def collect(self, token_lp_per_pass):
         """Per option lp / p / floor and per question residuals from host fp32 token lps."""

@@ -15,6 +15,7 @@ constexpr int kTile = 128;  // rows of a Q tile and of a KV tile
 // Device copies of one pass's descriptors, in one allocation.
 struct PassDevice {
     void* block = nullptr;
+    bool owned = true;             // false: caller-owned memory (spinf_plan_upload_to)
     int32_t* end = nullptr;        // [T_pad]
     int32_t* pos = nullptr;        // [T_pad]
     int32_t* tile_ptr = nullptr;   // [n_qtiles + 1]
@@ -58,6 +59,7 @@ struct spinf_plan {
     std::vector<spinf::QuestionSite> floor_q;    // every floor question
     int64_t n_options_total = 0;
     int32_t* d_err = nullptr;                    // device error word (allocated at first upload)
+    bool err_owned = true;                       // false: inside a caller-owned descriptor buffer
     int device = -1;
 };
 

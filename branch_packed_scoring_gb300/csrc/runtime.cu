@@ -75,52 +75,115 @@ int sm_count() {
 
 using namespace spinf;
 
-extern "C" spinf_status spinf_plan_upload(spinf_plan* plan, int32_t pass, spinf_stream stream) {
+namespace {
+
+// The descriptor arrays of one pass, in upload order, with their device pointers.
+struct DescriptorSet {
+    const std::vector<int32_t>* arrays[12];
+    int32_t** dst[12];
+    int n = 12;
+    size_t off[12];
+    size_t total = 0;
+};
+
+DescriptorSet descriptor_set(Pass& P) {
+    DescriptorSet d{{&P.end, &P.pos, &P.tile_ptr, &P.tile_kv, &P.tile_len, &P.slot_row, &P.gather_m, &P.gather_tok,
+                     &P.row_gptr, &P.row_glist, &P.qt_work, &P.row_runs},
+                    {&P.dev.end, &P.dev.pos, &P.dev.tile_ptr, &P.dev.tile_kv, &P.dev.tile_len, &P.dev.slot_row,
+                     &P.dev.gather_m, &P.dev.gather_tok, &P.dev.row_gptr, &P.dev.row_glist, &P.dev.qt_work,
+                     &P.dev.row_runs}};
+    for (int i = 0; i < d.n; ++i) {
+        d.off[i] = d.total;
+        d.total += (d.arrays[i]->size() * sizeof(int32_t) + 255) / 256 * 256;
+    }
+    return d;
+}
+
+// Points the pass's device views into `block` and enqueues the one copy, from a
+// staging buffer the plan keeps (so the copy may still be in flight on return).
+spinf_status copy_descriptors(Pass& P, const DescriptorSet& d, void* block, cudaStream_t s) {
+    std::vector<unsigned char>& host = P.staging;
+    host.assign(d.total, 0);
+    for (int i = 0; i < d.n; ++i) {
+        if (!d.arrays[i]->empty()) std::memcpy(host.data() + d.off[i], d.arrays[i]->data(), d.arrays[i]->size() * 4);
+        *d.dst[i] = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(block) + d.off[i]);
+    }
+    if (d.total) {
+        cudaError_t e = cudaMemcpyAsync(block, host.data(), d.total, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "descriptor upload");
+    }
+    return SPINF_OK;
+}
+
+spinf_status check_device(spinf_plan* plan, int32_t pass, int* dev) {
     if (!plan) return fail(SPINF_E_INVALID, "plan is NULL");
     if (pass < 0 || pass >= (int32_t)plan->passes.size()) return fail(SPINF_E_INVALID, "bad pass index");
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = cudaGetDevice(dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (plan->device >= 0 && plan->device != dev) return fail(SPINF_E_INVALID, "plan belongs to another device");
+    if (plan->device >= 0 && plan->device != *dev) return fail(SPINF_E_INVALID, "plan belongs to another device");
+    return SPINF_OK;
+}
+
+}  // namespace
+
+extern "C" spinf_status spinf_plan_upload(spinf_plan* plan, int32_t pass, spinf_stream stream) {
+    int dev = -1;
+    spinf_status st = check_device(plan, pass, &dev);
+    if (st) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
     if (!plan->d_err) {
         e = cudaMalloc(&plan->d_err, sizeof(int32_t));
         if (e != cudaSuccess) return fail(SPINF_E_NOMEM, "device allocation of the error word failed");
+        plan->err_owned = true;
         e = cudaMemsetAsync(plan->d_err, 0, sizeof(int32_t), s);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
         plan->device = dev;
     }
     Pass& P = plan->passes[pass];
     if (P.dev.block) return SPINF_OK;
-    const std::vector<int32_t>* arrays[] = {&P.end,      &P.pos,        &P.tile_ptr, &P.tile_kv,  &P.tile_len, &P.slot_row,
-                                           &P.gather_m, &P.gather_tok, &P.row_gptr, &P.row_glist, &P.qt_work, &P.row_runs};
-    int32_t** dst[] = {&P.dev.end,      &P.dev.pos,        &P.dev.tile_ptr, &P.dev.tile_kv,  &P.dev.tile_len, &P.dev.slot_row,
-                       &P.dev.gather_m, &P.dev.gather_tok, &P.dev.row_gptr, &P.dev.row_glist, &P.dev.qt_work, &P.dev.row_runs};
-    const int n = sizeof(arrays) / sizeof(arrays[0]);
-    size_t off[16], total = 0;
-    for (int i = 0; i < n; ++i) {
-        off[i] = total;
-        total += (arrays[i]->size() * sizeof(int32_t) + 255) / 256 * 256;
-    }
+    const DescriptorSet d = descriptor_set(P);
     void* block = nullptr;
-    e = cudaMalloc(&block, total > 0 ? total : 256);
+    e = cudaMalloc(&block, d.total > 0 ? d.total : 256);
     if (e != cudaSuccess) return fail(SPINF_E_NOMEM, "device allocation of pass descriptors failed");
-    // one staging buffer so the copy is a single transfer; the plan keeps it, so
-    // the copy may still be in flight when this call returns
-    std::vector<unsigned char>& host = P.staging;
-    host.assign(total, 0);
-    for (int i = 0; i < n; ++i) {
-        if (!arrays[i]->empty()) std::memcpy(host.data() + off[i], arrays[i]->data(), arrays[i]->size() * 4);
-        *dst[i] = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(block) + off[i]);
-    }
-    if (total) {
-        e = cudaMemcpyAsync(block, host.data(), total, cudaMemcpyHostToDevice, s);
-        if (e != cudaSuccess) {
-            cudaFree(block);
-            return cuda_fail(e, "descriptor upload");
-        }
+    if ((st = copy_descriptors(P, d, block, s))) {
+        cudaFree(block);
+        return st;
     }
     P.dev.block = block;
+    P.dev.owned = true;
+    return SPINF_OK;
+}
+
+extern "C" size_t spinf_plan_descriptor_bytes(const spinf_plan* plan, int32_t pass) {
+    if (!plan || pass < 0 || pass >= (int32_t)plan->passes.size()) return 0;
+    return descriptor_set(const_cast<Pass&>(plan->passes[pass])).total + 256;   // + the error word
+}
+
+extern "C" spinf_status spinf_plan_upload_to(spinf_plan* plan, int32_t pass, void* buffer, size_t bytes,
+                                             spinf_stream stream) {
+    if (!plan) return fail(SPINF_E_INVALID, "plan is NULL");
+    if (pass < 0 || pass >= (int32_t)plan->passes.size()) return fail(SPINF_E_INVALID, "bad pass index");
+    if (!buffer || (reinterpret_cast<uintptr_t>(buffer) & 255))
+        return fail(SPINF_E_INVALID, "descriptor buffer is NULL or not 256-byte aligned");
+    Pass& P = plan->passes[pass];
+    if (P.dev.block) return fail(SPINF_E_INVALID, "pass already uploaded");
+    const DescriptorSet d = descriptor_set(P);
+    if (bytes < d.total + 256) return fail(SPINF_E_INVALID, "descriptor buffer too small");
+    int dev = -1;
+    spinf_status st = check_device(plan, pass, &dev);
+    if (st) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!plan->d_err) {   // the error word sits after this pass's descriptors
+        plan->d_err = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(buffer) + d.total);
+        plan->err_owned = false;
+        cudaError_t e = cudaMemsetAsync(plan->d_err, 0, sizeof(int32_t), s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+        plan->device = dev;
+    }
+    if ((st = copy_descriptors(P, d, buffer, s))) return st;
+    P.dev.block = buffer;
+    P.dev.owned = false;
     return SPINF_OK;
 }
 
@@ -143,8 +206,8 @@ extern "C" spinf_status spinf_device_status(const spinf_plan* plan, spinf_stream
 extern "C" void spinf_plan_free(spinf_plan* plan) {
     if (!plan) return;
     for (Pass& P : plan->passes)
-        if (P.dev.block) cudaFree(P.dev.block);
-    if (plan->d_err) cudaFree(plan->d_err);
+        if (P.dev.block && P.dev.owned) cudaFree(P.dev.block);
+    if (plan->d_err && plan->err_owned) cudaFree(plan->d_err);
     delete plan;
 }
 

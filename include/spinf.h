@@ -180,6 +180,21 @@ spinf_status spinf_plan_counts(const spinf_plan* plan, int64_t* n_questions, int
  * of this pass must run on `stream` or after it. */
 spinf_status spinf_plan_upload(spinf_plan* plan, int32_t pass, spinf_stream stream);
 
+/* Bytes of device memory that spinf_plan_upload_to needs for pass `pass` (0 for a
+ * bad plan or index).  The pages have no counterpart: it serves callers that keep
+ * one device buffer across requests instead of allocating per plan. */
+size_t spinf_plan_descriptor_bytes(const spinf_plan* plan, int32_t pass);
+
+/* spinf_plan_upload into caller-owned device memory: `buffer` (256-byte aligned,
+ * >= spinf_plan_descriptor_bytes) receives the descriptors and, for the first pass
+ * uploaded this way, the plan's device error word.  No allocation; the copy is
+ * enqueued on `stream`.  The buffer must stay valid, and must not be reused by
+ * another plan, until the last kernel of this plan that reads it has finished;
+ * spinf_plan_free does not free it.  SPINF_E_INVALID for a NULL, misaligned or
+ * short buffer, or for a pass already uploaded. */
+spinf_status spinf_plan_upload_to(spinf_plan* plan, int32_t pass, void* buffer, size_t bytes,
+                                  spinf_stream stream);
+
 /* Tree-masked GQA attention over one packed pass (spec: the branch
  * attention kernel; pages: "spinf-serve 0.1.1", "Speed and scale").
  *

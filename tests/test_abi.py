@@ -38,3 +38,17 @@ def test_device_calls_fail_loudly_without_upload(spinf):
     assert e.value.status_name == "INVALID"
     with pytest.raises(spinf.SpinfError):
         spinf.score(plan, 0, 16, 16, None, 0, 256, 1024, 16, 16, 16, 1 << 20, stream=0)
+
+
+def test_upload_to_validates_before_any_device_work(spinf):
+    """Caller-owned descriptor memory: size and alignment are checked first (no GPU needed)."""
+    L = spinf.lib()
+    plan = spinf.Plan([([1, 2, 3], [([4, 5], [[6], [7]])])])
+    need = plan.descriptor_bytes(0)
+    info = plan.pass_info(0)
+    assert need >= 256 + 4 * (2 * info.T_pad + 8 * info.T_pad)   # end, pos, row runs and the error word
+    assert plan.descriptor_bytes(5) == 0
+    for ptr, size in ((None, need), (4096 + 16, need), (4096, need - 1)):
+        st = L.spinf_plan_upload_to(plan.handle, 0, ptr, size, None)
+        assert spinf.STATUS_NAMES[st] == "INVALID"
+    assert spinf.STATUS_NAMES[L.spinf_plan_upload_to(plan.handle, 3, 4096, need, None)] == "INVALID"

@@ -35,3 +35,25 @@ def test_tiny_pipeline(spinf):
     assert np.abs(ours["option_p"] - flat_p).max() <= 4e-3
     assert np.abs(ours["option_floor_p"] - flat_fp).max() <= 4e-3
     assert np.abs(ours["residual"] - res).max() <= 4e-3
+
+
+def test_upload_into_caller_memory_gives_identical_results(spinf):
+    """spinf_plan_upload_to (descriptors and error word in caller-owned memory, reused by a
+    second plan) against the plan-owned upload: bit-identical attention and scores."""
+    inputs = wl.stress(n_questions=20, content_tokens=300, vocab=1024) + wl.tiny()
+    shape = wl.TINY
+    lay = oracle_plan(inputs, vocab=shape.vocab).passes[0]
+    q, k, v, h = pass_values(lay, shape)
+    w = sv.lm_head(shape.vocab, shape.d_model).cuda()
+    a = spinf.Plan(inputs, vocab=shape.vocab)
+    o_a = run_attention(spinf, a, 0, q, k, v, shape)
+    lse_a, tlp_a, _ = run_score(spinf, a, 0, h, w, None, spinf.DTYPE_BF16, shape)
+    buf = torch.empty(a.descriptor_bytes(0) + 4096, dtype=torch.uint8, device="cuda")
+    for _ in range(2):   # the same memory serves a second plan once the first is done
+        b = spinf.Plan(inputs, vocab=shape.vocab)
+        b.upload(0, buffer=buf)
+        o_b = run_attention(spinf, b, 0, q, k, v, shape)
+        lse_b, tlp_b, _ = run_score(spinf, b, 0, h, w, None, spinf.DTYPE_BF16, shape)
+        assert torch.equal(o_a, o_b)
+        assert np.array_equal(lse_a, lse_b) and np.array_equal(tlp_a, tlp_b)
+        b.close()
