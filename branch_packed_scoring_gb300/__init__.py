@@ -27,6 +27,7 @@ DTYPE_BF16, DTYPE_E4M3 = 0, 1
 SYMBOLS = [
     "spinf_plan_opts_default", "spinf_pack_plan", "spinf_plan_num_passes", "spinf_plan_pass_info",
     "spinf_plan_counts", "spinf_plan_upload", "spinf_plan_descriptor_bytes", "spinf_plan_upload_to",
+    "spinf_plan_window_schedule",
     "spinf_branch_attention", "spinf_score_workspace_bytes",
     "spinf_score", "spinf_score_static", "spinf_collect", "spinf_device_status", "spinf_plan_free", "spinf_fingerprint",
     "spinf_status_string", "spinf_last_error",
@@ -100,6 +101,8 @@ def lib():
     L.spinf_plan_descriptor_bytes.argtypes = [vp, i32]
     L.spinf_plan_descriptor_bytes.restype = sz
     L.spinf_plan_upload_to.argtypes = [vp, i32, vp, sz, vp]
+    L.spinf_plan_window_schedule.argtypes = [vp, i32, i32, ctypes.POINTER(_P), ctypes.POINTER(_P), ctypes.POINTER(_P),
+                                             ctypes.POINTER(i32)]
     L.spinf_branch_attention.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, f32, i32, vp]
     L.spinf_score_workspace_bytes.argtypes = [vp, i32, i32, i32, i32]
     L.spinf_score_workspace_bytes.restype = sz
@@ -114,6 +117,7 @@ def lib():
     L.spinf_status_string.restype = ctypes.c_char_p
     L.spinf_last_error.restype = ctypes.c_char_p
     for name in ("spinf_pack_plan", "spinf_plan_pass_info", "spinf_plan_counts", "spinf_plan_upload", "spinf_plan_upload_to",
+                 "spinf_plan_window_schedule",
                  "spinf_branch_attention", "spinf_score", "spinf_score_static", "spinf_collect",
                  "spinf_device_status"):
         getattr(L, name).restype = i32
@@ -300,6 +304,15 @@ class Plan:
         nq, no = ctypes.c_int64(), ctypes.c_int64()
         _check(lib().spinf_plan_counts(self.handle, ctypes.byref(nq), ctypes.byref(no)))
         return nq.value, no.value
+
+    def window_schedule(self, p, window):
+        """(tile_ptr, tile_kv, tile_len) of pass p's schedule for a sliding window."""
+        tp, tk, tl, n = _P(), _P(), _P(), ctypes.c_int32()
+        _check(lib().spinf_plan_window_schedule(self.handle, p, window, ctypes.byref(tp), ctypes.byref(tk),
+                                                ctypes.byref(tl), ctypes.byref(n)))
+        nq = self.pass_info(p).n_qtiles
+        arr = lambda ptr, k: np.ctypeslib.as_array(ptr, shape=(k,)).copy() if k > 0 else np.zeros(0, np.int32)  # noqa: E731
+        return arr(tp, nq + 1), arr(tk, n.value), arr(tl, n.value)
 
     def descriptor_bytes(self, p):
         return int(lib().spinf_plan_descriptor_bytes(self.handle, p))

@@ -747,8 +747,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
 }
 
+// The schedule a launch walks: the pass's own, or its windowed subset.
+struct Sched {
+    const int32_t* qt_work;
+    const int32_t* tile_kv;
+    const int32_t* tile_len;
+};
+
 template <int D, int MODE>
-spinf_status launch_mode(const Pass& P, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tkh,
+spinf_status launch_mode(const Pass& P, const Sched& sc, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tkh,
                          const CUtensorMap& tv, __nv_bfloat16* o, int Hq, int Hkv, float scale_log2, int window,
                          int* err, cudaStream_t stream) {
     auto kernel = branch_attention_kernel<D, MODE>;
@@ -764,8 +771,8 @@ spinf_status launch_mode(const Pass& P, const CUtensorMap& tq, const CUtensorMap
     const int n_items = (P.T_pad / 128) * (Hq / heads_per_item);
     if (MODE == 0) {
         const int grid = std::min(n_items, sm_count());
-        kernel<<<grid, kAttnThreads, smem, stream>>>(tq, tk, tkh, tv, o, P.dev.end, P.dev.pos, P.dev.qt_work,
-                                                     P.dev.tile_kv, P.dev.tile_len, P.dev.row_runs, P.T, Hq, Hkv,
+        kernel<<<grid, kAttnThreads, smem, stream>>>(tq, tk, tkh, tv, o, P.dev.end, P.dev.pos, sc.qt_work,
+                                                     sc.tile_kv, sc.tile_len, P.dev.row_runs, P.T, Hq, Hkv,
                                                      n_items,
                                                      scale_log2, window, err);
     } else {   // clusters of two CTAs, two heads of a kv group per item
@@ -788,8 +795,7 @@ spinf_status launch_mode(const Pass& P, const CUtensorMap& tq, const CUtensorMap
         }
         cfg.gridDim = dim3(2 * std::min(n_items, clusters));
         e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tkh, tv, o, (const int32_t*)P.dev.end,
-                               (const int32_t*)P.dev.pos, (const int32_t*)P.dev.qt_work,
-                               (const int32_t*)P.dev.tile_kv, (const int32_t*)P.dev.tile_len,
+                               (const int32_t*)P.dev.pos, sc.qt_work, sc.tile_kv, sc.tile_len,
                                (const int32_t*)P.dev.row_runs, P.T, Hq, Hkv, n_items, scale_log2, window, err);
         if (e != cudaSuccess) return cuda_fail(e, "attention launch");
     }
@@ -799,7 +805,7 @@ spinf_status launch_mode(const Pass& P, const CUtensorMap& tq, const CUtensorMap
 }
 
 template <int D>
-spinf_status launch_attention(const Pass& P, const void* q, const void* k, const void* v, void* o, int Hq,
+spinf_status launch_attention(const Pass& P, const Sched& sc, const void* q, const void* k, const void* v, void* o, int Hq,
                               int Hkv, float scale, int window, int* err, cudaStream_t stream) {
     CUtensorMap tq, tk, tkh, tkc, tv, tvh;
     // 4-D views (64 columns, rows, 64-column chunks, head): one box holds every chunk of a
@@ -832,11 +838,11 @@ spinf_status launch_attention(const Pass& P, const void* q, const void* k, const
     // multicast pair measured faster: its softmax warps are not coupled across the two SMs)
     // the kernel's third map: a K tile's key half (cta_group::2 pair) or column half (single K buffer)
     const CUtensorMap& kpart = D == 256 ? tkc : tkh;
-    if ((Hq / Hkv) % 2 != 0) return launch_mode<D, 0>(P, tq, tk, kpart, tv, ob, Hq, Hkv, scale_log2, window, err, stream);
+    if ((Hq / Hkv) % 2 != 0) return launch_mode<D, 0>(P, sc, tq, tk, kpart, tv, ob, Hq, Hkv, scale_log2, window, err, stream);
     if constexpr (D == 128)
-        return launch_mode<D, 2>(P, tq, tk, tkh, tvh, ob, Hq, Hkv, scale_log2, window, err, stream);
+        return launch_mode<D, 2>(P, sc, tq, tk, tkh, tvh, ob, Hq, Hkv, scale_log2, window, err, stream);
     else
-        return launch_mode<D, 1>(P, tq, tk, kpart, tv, ob, Hq, Hkv, scale_log2, window, err, stream);
+        return launch_mode<D, 1>(P, sc, tq, tk, kpart, tv, ob, Hq, Hkv, scale_log2, window, err, stream);
 }
 
 }  // namespace
@@ -856,13 +862,21 @@ extern "C" spinf_status spinf_branch_attention(const spinf_plan* plan, int32_t p
         return fail(SPINF_E_INVALID, "bad head counts");
     if (window < 0) return fail(SPINF_E_INVALID, "negative window");
     const Pass& P = plan->passes[pass];
+    if (d_head != 64 && d_head != 128 && d_head != 256) return fail(SPINF_E_UNSUPPORTED, "d_head must be 64, 128 or 256");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // with a window, the schedule without the tiles no row of a Q tile sees within it
+    Sched sc{P.dev.qt_work, P.dev.tile_kv, P.dev.tile_len};
+    if (window > 0 && P.T > 0) {
+        WindowSchedule& w = window_schedule(const_cast<Pass&>(P), window);
+        if ((st = upload_window(w, s))) return st;
+        sc = Sched{w.d_qt_work, w.d_tile_kv, w.d_tile_len};
+    }
     if (P.T == 0) return SPINF_OK;
     if (!(scale > 0.f)) scale = 1.0f / std::sqrt(static_cast<float>(d_head));
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (d_head) {
-        case 64: return launch_attention<64>(P, q, k, v, o, n_q_heads, n_kv_heads, scale, window, plan->d_err, s);
-        case 128: return launch_attention<128>(P, q, k, v, o, n_q_heads, n_kv_heads, scale, window, plan->d_err, s);
-        case 256: return launch_attention<256>(P, q, k, v, o, n_q_heads, n_kv_heads, scale, window, plan->d_err, s);
+        case 64: return launch_attention<64>(P, sc, q, k, v, o, n_q_heads, n_kv_heads, scale, window, plan->d_err, s);
+        case 128: return launch_attention<128>(P, sc, q, k, v, o, n_q_heads, n_kv_heads, scale, window, plan->d_err, s);
+        case 256: return launch_attention<256>(P, sc, q, k, v, o, n_q_heads, n_kv_heads, scale, window, plan->d_err, s);
         default: return fail(SPINF_E_UNSUPPORTED, "d_head must be 64, 128 or 256");
     }
 }

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <memory>
 #include <string>
 #include <vector>
 
@@ -30,6 +31,16 @@ struct PassDevice {
     int32_t* row_runs = nullptr;   // [T_pad][8] root path of each row as <= 4 runs [lo, hi) (lo0 -1: more)
 };
 
+// The KV-tile schedule of one pass for a sliding window W: the W = 0 schedule without
+// the tiles in which no row of the Q tile sees any key within W (built on first use).
+struct WindowSchedule {
+    int32_t window = 0;
+    std::vector<int32_t> tile_ptr, tile_kv, tile_len, qt_work;
+    void* block = nullptr;   // device copies of qt_work, tile_kv, tile_len (plan-owned)
+    int32_t *d_qt_work = nullptr, *d_tile_kv = nullptr, *d_tile_len = nullptr;
+    std::vector<unsigned char> staging;
+};
+
 struct Pass {
     int32_t T = 0, T_pad = 0;
     std::vector<int32_t> tok, parent, pos, end, anchor;
@@ -39,6 +50,7 @@ struct Pass {
     std::vector<int32_t> unit_start, unit_source;
     PassDevice dev;
     std::vector<unsigned char> staging;   // host source of the descriptor upload, kept until the plan is freed
+    std::vector<std::unique_ptr<WindowSchedule>> windows;
 };
 
 // Where the option tokens of one laid-out question sit in its pass's gather list.
@@ -66,4 +78,6 @@ struct spinf_plan {
 namespace spinf {
 spinf_status fail(spinf_status s, const std::string& msg);
 spinf_status ok();
+// The pass's schedule for window W > 0, built on first use and kept by the plan.
+WindowSchedule& window_schedule(Pass& P, int32_t window);
 }  // namespace spinf

@@ -120,6 +120,58 @@ bool ids_in_range(const spinf_tokens& t, int32_t vocab) {
 
 }  // namespace spinf
 
+namespace spinf {
+
+WindowSchedule& window_schedule(Pass& P, int32_t window) {
+    for (auto& w : P.windows)
+        if (w->window == window) return *w;
+    auto ws = std::make_unique<WindowSchedule>();
+    ws->window = window;
+    const int32_t n_qt = P.T_pad / kTile;
+    ws->tile_ptr.assign(1, 0);
+    int32_t mins[8][kTile];   // sparse table of pos over one Q tile's real rows
+    for (int32_t qt = 0; qt < n_qt; ++qt) {
+        const int32_t r0 = qt * kTile, r1 = std::min(r0 + kTile, P.T), nr = std::max(r1 - r0, 0);
+        for (int32_t i = 0; i < nr; ++i) mins[0][i] = P.pos[r0 + i];
+        for (int32_t l = 1; (1 << l) <= nr; ++l)
+            for (int32_t i = 0; i + (1 << l) <= nr; ++i)
+                mins[l][i] = std::min(mins[l - 1][i], mins[l - 1][i + (1 << (l - 1))]);
+        auto range_min = [&](int32_t lo, int32_t hi) {   // rows [lo, hi) of the tile, hi > lo
+            int32_t l = 0;
+            while ((2 << l) <= hi - lo) ++l;
+            return std::min(mins[l][lo - r0], mins[l][hi - r0 - (1 << l)]);
+        };
+        for (int32_t e = P.tile_ptr[qt]; e < P.tile_ptr[qt + 1]; ++e) {
+            const int32_t kv0 = P.tile_kv[e], len = P.tile_len[e];
+            bool keep = false;
+            for (int32_t k = kv0; k < kv0 + len && !keep; ++k) {   // rows that see k: [max(k, r0), min(end[k], r1))
+                const int32_t lo = std::max(k, r0), hi = std::min(P.end[k], r1);
+                keep = lo < hi && range_min(lo, hi) - P.pos[k] < window;
+            }
+            if (keep) {
+                ws->tile_kv.push_back(kv0);
+                ws->tile_len.push_back(len);
+            }
+        }
+        ws->tile_ptr.push_back((int32_t)ws->tile_kv.size());
+    }
+    std::vector<int32_t> order(n_qt);
+    for (int32_t qt = 0; qt < n_qt; ++qt) order[qt] = qt;
+    std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
+        return ws->tile_ptr[a + 1] - ws->tile_ptr[a] > ws->tile_ptr[b + 1] - ws->tile_ptr[b];
+    });
+    ws->qt_work.assign(4 * (size_t)n_qt, 0);
+    for (int32_t i = 0; i < n_qt; ++i) {
+        ws->qt_work[4 * i] = order[i];
+        ws->qt_work[4 * i + 1] = ws->tile_ptr[order[i]];
+        ws->qt_work[4 * i + 2] = ws->tile_ptr[order[i] + 1] - ws->tile_ptr[order[i]];
+    }
+    P.windows.push_back(std::move(ws));
+    return *P.windows.back();
+}
+
+}  // namespace spinf
+
 using namespace spinf;
 
 extern "C" void spinf_plan_opts_default(spinf_plan_opts* o) {
@@ -477,6 +529,20 @@ extern "C" spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inp
 
 extern "C" int32_t spinf_plan_num_passes(const spinf_plan* plan) {
     return plan ? (int32_t)plan->passes.size() : 0;
+}
+
+extern "C" spinf_status spinf_plan_window_schedule(const spinf_plan* plan, int32_t pass, int32_t window,
+                                                   const int32_t** tile_ptr, const int32_t** tile_kv,
+                                                   const int32_t** tile_len, int32_t* n_sched) {
+    if (!plan || pass < 0 || pass >= (int32_t)plan->passes.size()) return fail(SPINF_E_INVALID, "bad plan or pass");
+    if (window <= 0) return fail(SPINF_E_INVALID, "window must be positive");
+    if (!tile_ptr || !tile_kv || !tile_len || !n_sched) return fail(SPINF_E_INVALID, "NULL output");
+    WindowSchedule& w = window_schedule(const_cast<Pass&>(plan->passes[pass]), window);
+    *tile_ptr = w.tile_ptr.data();
+    *tile_kv = w.tile_kv.data();
+    *tile_len = w.tile_len.data();
+    *n_sched = (int32_t)w.tile_kv.size();
+    return SPINF_OK;
 }
 
 extern "C" spinf_status spinf_plan_pass_info(const spinf_plan* plan, int32_t pass, spinf_pass_info* out) {

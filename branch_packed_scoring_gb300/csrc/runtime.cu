@@ -64,6 +64,31 @@ spinf_status ensure_device_ready(const spinf_plan* plan, int32_t pass) {
     return SPINF_OK;
 }
 
+spinf_status upload_window(WindowSchedule& w, cudaStream_t stream) {
+    if (w.block) return SPINF_OK;
+    const std::vector<int32_t>* arrays[3] = {&w.qt_work, &w.tile_kv, &w.tile_len};
+    int32_t** dst[3] = {&w.d_qt_work, &w.d_tile_kv, &w.d_tile_len};
+    size_t off[3], total = 0;
+    for (int i = 0; i < 3; ++i) {
+        off[i] = total;
+        total += (arrays[i]->size() * sizeof(int32_t) + 255) / 256 * 256;
+    }
+    void* block = nullptr;
+    cudaError_t e = cudaMalloc(&block, total > 0 ? total : 256);
+    if (e != cudaSuccess) return fail(SPINF_E_NOMEM, "device allocation of a window schedule failed");
+    w.staging.assign(total, 0);
+    for (int i = 0; i < 3; ++i) {
+        if (!arrays[i]->empty()) std::memcpy(w.staging.data() + off[i], arrays[i]->data(), arrays[i]->size() * 4);
+        *dst[i] = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(block) + off[i]);
+    }
+    if (total && (e = cudaMemcpyAsync(block, w.staging.data(), total, cudaMemcpyHostToDevice, stream)) != cudaSuccess) {
+        cudaFree(block);
+        return cuda_fail(e, "window schedule upload");
+    }
+    w.block = block;
+    return SPINF_OK;
+}
+
 int sm_count() {
     int dev = 0, n = 0;
     cudaGetDevice(&dev);
@@ -205,8 +230,11 @@ extern "C" spinf_status spinf_device_status(const spinf_plan* plan, spinf_stream
 
 extern "C" void spinf_plan_free(spinf_plan* plan) {
     if (!plan) return;
-    for (Pass& P : plan->passes)
+    for (Pass& P : plan->passes) {
         if (P.dev.block && P.dev.owned) cudaFree(P.dev.block);
+        for (auto& w : P.windows)
+            if (w->block) cudaFree(w->block);
+    }
     if (plan->d_err && plan->err_owned) cudaFree(plan->d_err);
     delete plan;
 }

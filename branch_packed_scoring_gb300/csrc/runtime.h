@@ -21,4 +21,7 @@ spinf_status ensure_device_ready(const spinf_plan* plan, int32_t pass);
 
 int sm_count();
 
+// Device copies of a windowed schedule (allocated and copied on `stream` on first use).
+spinf_status upload_window(WindowSchedule& w, cudaStream_t stream);
+
 }  // namespace spinf

@@ -171,6 +171,16 @@ int32_t spinf_plan_num_passes(const spinf_plan* plan);
 /* Host views of pass `pass`.  SPINF_E_INVALID for a bad index. */
 spinf_status spinf_plan_pass_info(const spinf_plan* plan, int32_t pass, spinf_pass_info* out);
 
+/* The KV-tile schedule of pass `pass` for a sliding window `window` > 0 (what
+ * spinf_branch_attention runs with that window): the window-free schedule without the
+ * tiles in which no row of the Q tile sees any of the tile's keys within the window
+ * (pos[q] - pos[k] < window).  Skipping such a tile changes no bit of the result: it
+ * is masked for every row.  Built on first use and kept by the plan; host views valid
+ * until spinf_plan_free.  SPINF_E_INVALID for a bad pass, window <= 0 or NULL outputs. */
+spinf_status spinf_plan_window_schedule(const spinf_plan* plan, int32_t pass, int32_t window,
+                                        const int32_t** tile_ptr, const int32_t** tile_kv,
+                                        const int32_t** tile_len, int32_t* n_sched);
+
 /* Number of user questions and options over the whole request (sizes of spinf_result). */
 spinf_status spinf_plan_counts(const spinf_plan* plan, int64_t* n_questions, int64_t* n_options);
 

@@ -200,3 +200,27 @@ def test_row_runs_masks_match_visibility(spinf):
                 got &= (np.arange(128)[None, :] < ln) & real[:, None]
                 use = runs[:, 0] >= 0
                 assert np.array_equal(got[use], truth[use]), (p, qt, e)
+
+
+@pytest.mark.parametrize("window", [1, 7, 64, 200, 100000])
+def test_window_schedule_is_exact(spinf, window):
+    """A tile stays in the windowed schedule iff some row of its Q tile sees some key of
+    it within the window (oracle visible sets and depths, brute force)."""
+    inputs = wl.stress(n_questions=24, content_tokens=300, vocab=1000) + wl.tiny(vocab=1000)
+    P = op.plan(inputs, token_budget=1024, vocab=1000)
+    plan = spinf.Plan(inputs, token_budget=1024, vocab=1000)
+    for p, lay in enumerate(P.passes):
+        tp, tk, tl = plan.window_schedule(p, window)
+        want_ptr, want_kv = [0], []
+        for qt in range(lay.T_pad // 128):
+            rows = range(qt * 128, min(qt * 128 + 128, lay.T))
+            vis = {q: set(lay.visible(q)) for q in rows}
+            for e in range(lay.tile_ptr[qt], lay.tile_ptr[qt + 1]):
+                kv0, ln = int(lay.tile_kv[e]), int(lay.tile_len[e])
+                if any(k in vis[q] and lay.pos[q] - lay.pos[k] < window for q in rows for k in range(kv0, kv0 + ln)):
+                    want_kv.append((kv0, ln))
+            want_ptr.append(len(want_kv))
+        assert tp.tolist() == want_ptr
+        assert list(zip(tk.tolist(), tl.tolist())) == want_kv
+        if window >= 100000:   # a window that never bites keeps every tile
+            assert np.array_equal(tk, lay.tile_kv) and np.array_equal(tl, lay.tile_len)
