@@ -563,9 +563,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const bool all_visible =
                     cmax >= 127 && head.x > q_row && (window <= 0 || pos_q - head.y < window);
                 float mx = -INFINITY;
-                if (all_visible) {
+                // maximum of the 64 values, two independent chains of three-input maxima
+                auto max64 = [&]() {
+                    float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) mx = fmaxf(mx, s[i]);
+                    for (int i = 0; i < 64; i += 4) {
+                        m0 = fmax3(m0, s[i], s[i + 1]);
+                        m1 = fmax3(m1, s[i + 2], s[i + 3]);
+                    }
+                    return fmaxf(m0, m1);
+                };
+                if (all_visible) {
+                    mx = max64();
                 } else if (window <= 0 && run01.x >= 0) {
                     // visible keys of this half from the row's runs: no per-key loads
                     const int kb = head.z + 64 * half;
@@ -583,10 +592,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     if (lim < 64) vm &= (1ull << lim) - 1ull;
                     if (!real) vm = 0ull;
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) {
-                        s[i] = ((vm >> i) & 1ull) ? s[i] : -INFINITY;
-                        mx = fmaxf(mx, s[i]);
-                    }
+                    for (int i = 0; i < 64; ++i) s[i] = ((vm >> i) & 1ull) ? s[i] : -INFINITY;
+                    mx = max64();
                 } else {
                     const int4* e4 = reinterpret_cast<const int4*>(meta + slot * 256 + half * 64);
                     const int4* p4 = reinterpret_cast<const int4*>(meta + slot * 256 + 128 + half * 64);
@@ -633,14 +640,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     for (int i = 0; i < 32; ++i) pk[i] = 0u;
                 } else {
                     const float mb = m_new * scale_log2;
+                    const float2 sc2 = make_float2(scale_log2, scale_log2), nb2 = make_float2(-mb, -mb);
+                    float2 acc = make_float2(0.f, 0.f);   // even and odd columns, added at the end
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
-                        const float p0 = fast_exp2(fmaf(s[2 * c], scale_log2, -mb));
-                        const float p1 = fast_exp2(fmaf(s[2 * c + 1], scale_log2, -mb));
-                        rowsum += p0;
-                        rowsum += p1;
-                        pk[c] = pack_bf16x2(p0, p1);
+                        const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), sc2, nb2);
+                        const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                        acc = fadd2(acc, p);
+                        pk[c] = pack_bf16x2(p.x, p.y);
                     }
+                    rowsum = acc.x + acc.y;
                     if (grow) alpha = fast_exp2(fmaf(m, scale_log2, -mb));
                 }
                 if (m_new != -INFINITY) {
@@ -658,8 +667,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     for (int c = 0; c < D / 64; ++c) {
                         uint32_t rr[32];
                         tmem_ld32(tO + c * 32, rr);
+                        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+                        for (int i = 0; i < 32; i += 2) {
+                            const float2 y = fmul2(make_float2(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1])), a2);
+                            rr[i] = __float_as_uint(y.x);
+                            rr[i + 1] = __float_as_uint(y.y);
+                        }
                         tmem_st32(tO + c * 32, rr);
                     }
                 }
@@ -698,9 +712,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             auto store_chunk = [&](const uint32_t* rr, int col) {
                 uint32_t w[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    w[i] = real ? pack_bf16x2(__uint_as_float(rr[2 * i]) * inv, __uint_as_float(rr[2 * i + 1]) * inv)
-                                : 0u;
+                for (int i = 0; i < 16; ++i) {
+                    const float2 y = fmul2(make_float2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])),
+                                           make_float2(inv, inv));
+                    w[i] = real ? pack_bf16x2(y.x, y.y) : 0u;
+                }
                 uint4* srow = reinterpret_cast<uint4*>(stage + lane * 64);
                 const int sx = (lane >> 1) & 3;
 #pragma unroll
