@@ -80,6 +80,8 @@ constexpr int kOstageBytes = 32 * 64;  // O staging of one softmax warp: 32 rows
 //                       into different accumulators are not ordered by the tensor core.
 //   V_DONE[G & 1]       PV(G) has finished: O may be read or rescaled, its V buffer is free
 //   MMA_DONE(_PV)       all MMAs of one issuer thread have completed (before TMEM is freed)
+//   V_HALF, V_FULL_H1   the same for a single V buffer, by key halves: V_HALF says PV(G) has
+//                       read the first 64 keys (V is then kept as [key half][chunk][64 keys])
 //   S_HALF, K_FULL_H1   single K buffer (d_head 256 outside a cta_group::2 pair): the tile
 //                       is copied in two halves of 128 columns; S_HALF says S(G) has read
 //                       the first half, so K(G+1)'s first half may land while S(G) finishes
@@ -87,7 +89,7 @@ constexpr int kOstageBytes = 32 * 64;  // O staging of one softmax warp: 32 rows
 // shared K/V buffers.
 enum {
     Q_FULL = 0, Q_EMPTY, S_FULL0, S_FULL1, S_FULL2, P_FULL0, P_FULL1, P_FULL2, P_USED0, P_USED1, P_USED2,
-    V_DONE0, V_DONE1, MMA_DONE, MMA_DONE_PV, S_HALF, K_FULL_H1, N_FIXED_BARS
+    V_DONE0, V_DONE1, MMA_DONE, MMA_DONE_PV, S_HALF, K_FULL_H1, V_HALF, V_FULL_H1, N_FIXED_BARS
 };
 
 template <int D, int MODE>
@@ -197,7 +199,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int b = 0; b < N_FIXED_BARS; ++b) {
             int count = 1;
             if (b >= P_FULL0 && b <= P_FULL2) count = CG2 ? 2 : kSoftmaxThreads;
-            if (((b >= S_FULL0 && b <= S_FULL2) || b == V_DONE0 || b == V_DONE1 || b == S_HALF) && MODE == 1)
+            if (((b >= S_FULL0 && b <= S_FULL2) || b == V_DONE0 || b == V_DONE1 || b == S_HALF || b == V_HALF) &&
+                MODE == 1)
                 count = 2;   // both CTAs' MMAs
             mbar_init(&bars[b], count);
         }
@@ -272,6 +275,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             seek(vc);
             uint32_t ic = 0;          // Q copies issued
             int k_part = 0;           // half of the K tile to copy next (single K buffer)
+            int v_part = 0;           // half of the V tile to copy next (single V buffer)
             bool q_pending = true;    // the K cursor's item still needs its Q
             unsigned long long t_idle = 0;
             while (!kc.done || !vc.done) {
@@ -336,7 +340,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         }
                     }
                 }
-                if (!vc.done) {
+                if constexpr (kHalfK) {   // single V buffer: two copies per tile, by key halves
+                    const uint32_t G = vc.G, Gp = G - 1;
+                    if (!vc.done && (G == 0 || (v_part == 0 ? mbar_test(&bars[V_HALF], Gp & 1)
+                                                            : mbar_test(&v_done[Gp & 1], (Gp >> 1) & 1)))) {
+                        uint64_t* fb = v_part == 0 ? &v_full[0] : &bars[V_FULL_H1];
+                        uint8_t* dst = sV + v_part * (L::kTileBytes / 2);
+                        mbar_arrive_expect_tx(fb, L::kTileBytes / 2);
+                        if (!PAIR) tma_load_4d(dst, &tm_v, fb, 0, vc.kv0 + 64 * v_part, 0, vc.I.h / group);
+                        else if ((G & 1) != (uint32_t)rank)   // the other CTA of the pair takes this V tile
+                            tma_load_4d_mc(dst, &tm_v, fb, 0, vc.kv0 + 64 * v_part, 0, vc.I.h / group, kBoth);
+                        if (++v_part == 2) {
+                            v_part = 0;
+                            advance(vc);
+                        }
+                        progress = true;
+                    }
+                } else if (!vc.done) {
                     const uint32_t G = vc.G, Gp = G - L::kStages;   // PV(Gp) was the last reader of the buffer
                     if (G < (uint32_t)L::kStages || mbar_test(&v_done[Gp & 1], (Gp >> 1) & 1)) {
                         const uint32_t st = G % L::kStages;
@@ -382,8 +402,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             for (uint32_t b = GK > (uint32_t)kSBufs<D> ? GK - kSBufs<D> : 0; b < GK; ++b)
                 mbar_drain(&bars[S_FULL0 + b % kSBufs<D>], (b / kSBufs<D>) & 1, err);
-            for (uint32_t b = GV > (uint32_t)L::kStages ? GV - L::kStages : 0; b < GV; ++b)
+            for (uint32_t b = GV > (uint32_t)L::kStages ? GV - L::kStages : 0; b < GV; ++b) {
                 if (!CG2 || rank == 0) mbar_drain(&v_full[b % L::kStages], (b / L::kStages) & 1, err);
+                if (kHalfK) {
+                    mbar_drain(&bars[V_FULL_H1], b & 1, err);
+                    mbar_drain(&bars[V_HALF], b & 1, err);
+                }
+            }
             for (uint32_t b = GV > 2u ? GV - 2 : 0; b < GV; ++b) mbar_drain(&v_done[b & 1], (b >> 1) & 1, err);
             if (ic > 0) {
                 if (!CG2 || rank == 0) mbar_drain(&bars[Q_FULL], (ic - 1) & 1, err);
@@ -459,7 +484,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const uint32_t aVs = aV + st * L::kVBytes;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {   // 16 keys: 8 TMEM columns of bf16 pairs of P
-                            const uint64_t db = sdesc_sw128(aVs + kk * 2048, kBoxBytes, 1024);
+                            if (kHalfK && kk == 4) {   // first 64 keys read; the other half landed?
+                                commit_shared(&bars[V_HALF]);
+                                mbar_wait(&bars[V_FULL_H1], Gj & 1, err);
+                                tc_fence_after();
+                            }
+                            // V as [chunk][128 keys] boxes, or (single V buffer) [key half][chunk][64 keys]
+                            const uint64_t db =
+                                kHalfK ? sdesc_sw128(aVs + (kk >> 2) * (L::kTileBytes / 2) + (kk & 3) * 2048, kBoxBytes / 2, 1024)
+                                       : sdesc_sw128(aVs + kk * 2048, kBoxBytes, 1024);
                             // an item's first product overwrites O (adding it to zero would give the same bits)
                             const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
                             if constexpr (CG2) mma_f16_ts_pair(tmem + kColO<D>, aP + kk * 8, db, idesc_pv, acc);
@@ -852,13 +885,18 @@ spinf_status launch_attention(const Pass& P, const Sched& sc, const void* q, con
     // an even number of query heads per kv head pairs two heads per item: d_head 128 as a
     // cta_group::2 pair (half tiles), d_head 64 and 256 as a multicast pair (at 256 the
     // multicast pair measured faster: its softmax warps are not coupled across the two SMs)
-    // the kernel's third map: a K tile's key half (cta_group::2 pair) or column half (single K buffer)
+    // the kernel's third map: a K tile's key half (cta_group::2 pair) or column half (single K
+    // buffer); with a single V buffer (d_head 256) V is copied by key halves
     const CUtensorMap& kpart = D == 256 ? tkc : tkh;
-    if ((Hq / Hkv) % 2 != 0) return launch_mode<D, 0>(P, sc, tq, tk, kpart, tv, ob, Hq, Hkv, scale_log2, window, err, stream);
+    CUtensorMap tvk;
+    if ((st = make_tmap(&tvk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dk, sk, kbox_half, CU_TENSOR_MAP_SWIZZLE_128B)))
+        return st;
+    const CUtensorMap& vmap = D == 256 ? tvk : tv;
+    if ((Hq / Hkv) % 2 != 0) return launch_mode<D, 0>(P, sc, tq, tk, kpart, vmap, ob, Hq, Hkv, scale_log2, window, err, stream);
     if constexpr (D == 128)
         return launch_mode<D, 2>(P, sc, tq, tk, tkh, tvh, ob, Hq, Hkv, scale_log2, window, err, stream);
     else
-        return launch_mode<D, 1>(P, sc, tq, tk, kpart, tv, ob, Hq, Hkv, scale_log2, window, err, stream);
+        return launch_mode<D, 1>(P, sc, tq, tk, kpart, vmap, ob, Hq, Hkv, scale_log2, window, err, stream);
 }
 
 }  // namespace
