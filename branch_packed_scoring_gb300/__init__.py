@@ -29,7 +29,8 @@ SYMBOLS = [
     "spinf_plan_counts", "spinf_plan_upload", "spinf_plan_descriptor_bytes", "spinf_plan_upload_to",
     "spinf_plan_window_schedule",
     "spinf_branch_attention", "spinf_score_workspace_bytes",
-    "spinf_score", "spinf_score_static", "spinf_collect", "spinf_device_status", "spinf_plan_free", "spinf_fingerprint",
+    "spinf_score", "spinf_score_static", "spinf_collect", "spinf_device_status", "spinf_device_selftest",
+    "spinf_plan_free", "spinf_fingerprint",
     "spinf_status_string", "spinf_last_error",
 ]
 
@@ -110,6 +111,7 @@ def lib():
     L.spinf_score_static.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp]
     L.spinf_collect.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(_Result)]
     L.spinf_device_status.argtypes = [vp, vp]
+    L.spinf_device_selftest.argtypes = [vp, i32, vp]
     L.spinf_plan_free.argtypes = [vp]
     L.spinf_plan_free.restype = None
     L.spinf_fingerprint.restype = ctypes.c_char_p
@@ -119,7 +121,7 @@ def lib():
     for name in ("spinf_pack_plan", "spinf_plan_pass_info", "spinf_plan_counts", "spinf_plan_upload", "spinf_plan_upload_to",
                  "spinf_plan_window_schedule",
                  "spinf_branch_attention", "spinf_score", "spinf_score_static", "spinf_collect",
-                 "spinf_device_status"):
+                 "spinf_device_status", "spinf_device_selftest"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -342,6 +344,10 @@ class Plan:
 
     def device_status(self, stream=None):
         _check(lib().spinf_device_status(self.handle, _stream(stream)))
+
+    def device_selftest(self, wait_ms=50, stream=None):
+        """Enqueue a bounded wait that runs out (see spinf_device_selftest)."""
+        _check(lib().spinf_device_selftest(self.handle, wait_ms, _stream(stream)))
 
     def close(self):
         if self._h is not None and _lib is not None:

@@ -68,19 +68,22 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 
 // Bounded wait for the phase with the given parity.  Returns immediately (false)
 // once any wait of the launch has timed out, so a stalled launch drains quickly.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, int* err, unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63) == 0) {
             if (*reinterpret_cast<volatile int*>(err) != 0) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
+            if (globaltimer() - t0 > limit_ns) {
                 atomicCAS(err, 0, kErrTimeout);
                 return false;
             }
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+    return mbar_wait_for(bar, parity, err, kWaitLimitNs);
 }
 
 // Wait used when a CTA drains its own work before retiring: bounded in time like

@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "ptx.cuh"
 #include "runtime.h"
 
 namespace spinf {
@@ -226,6 +227,29 @@ extern "C" spinf_status spinf_device_status(const spinf_plan* plan, spinf_stream
     if (e != cudaSuccess) return cuda_fail(e, "device status reset");
     if (word == SPINF_E_DEVICE_TIMEOUT) return fail(SPINF_E_DEVICE_TIMEOUT, "a device wait timed out");
     return fail(SPINF_E_DEVICE_CHECK, "a device-side check failed");
+}
+
+namespace spinf {
+
+// One thread waits, with the kernels' bounded wait, on a barrier nothing arrives on.
+__global__ void selftest_wait_kernel(int* err, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    dev::mbar_init(&bar, 1);
+    dev::fence_mbar_init();
+    dev::mbar_wait_for(&bar, 0, err, limit_ns);
+}
+
+}  // namespace spinf
+
+extern "C" spinf_status spinf_device_selftest(const spinf_plan* plan, int32_t wait_ms, spinf_stream stream) {
+    if (!plan || !plan->d_err) return fail(SPINF_E_INVALID, "plan has no device error word (upload a pass first)");
+    if (wait_ms < 1 || wait_ms > 10000) return fail(SPINF_E_INVALID, "wait_ms must be in [1, 10000]");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    selftest_wait_kernel<<<1, 32, 0, s>>>(plan->d_err, static_cast<unsigned long long>(wait_ms) * 1000000ull);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
+    return SPINF_OK;
 }
 
 extern "C" void spinf_plan_free(spinf_plan* plan) {

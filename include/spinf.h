@@ -294,6 +294,14 @@ spinf_status spinf_collect(const spinf_plan* plan, const float* const* token_lp_
  * SPINF_OK, SPINF_E_DEVICE_TIMEOUT or SPINF_E_DEVICE_CHECK (the word is cleared). */
 spinf_status spinf_device_status(const spinf_plan* plan, spinf_stream stream);
 
+/* Failure-path self-test: enqueue on `stream` a one-thread kernel that waits on a
+ * barrier nothing arrives on, with the kernels' bounded wait shortened to `wait_ms`
+ * (1..10000); the plan's error word then holds the timeout, which the next
+ * spinf_device_status reports as SPINF_E_DEVICE_TIMEOUT (and clears), and the device
+ * stays usable.  Nothing faults or hangs.  The pages have no counterpart.
+ * SPINF_E_INVALID before any upload or for a bad wait_ms. */
+spinf_status spinf_device_selftest(const spinf_plan* plan, int32_t wait_ms, spinf_stream stream);
+
 void spinf_plan_free(spinf_plan* plan);
 
 /* Kernel version, tile configuration and precision: two results are bitwise

@@ -52,3 +52,10 @@ def test_upload_to_validates_before_any_device_work(spinf):
         st = L.spinf_plan_upload_to(plan.handle, 0, ptr, size, None)
         assert spinf.STATUS_NAMES[st] == "INVALID"
     assert spinf.STATUS_NAMES[L.spinf_plan_upload_to(plan.handle, 3, 4096, need, None)] == "INVALID"
+
+
+def test_selftest_needs_an_uploaded_plan(spinf):
+    """No device work happens for a plan without an error word (no GPU needed)."""
+    plan = spinf.Plan([([1, 2, 3], [([4, 5], [[6], [7]])])])
+    st = spinf.lib().spinf_device_selftest(plan.handle, 30, None)
+    assert spinf.STATUS_NAMES[st] == "INVALID"

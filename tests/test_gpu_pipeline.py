@@ -57,3 +57,31 @@ def test_upload_into_caller_memory_gives_identical_results(spinf):
         assert torch.equal(o_a, o_b)
         assert np.array_equal(lse_a, lse_b) and np.array_equal(tlp_a, tlp_b)
         b.close()
+
+
+def test_bounded_wait_runs_out_and_device_stays_usable(spinf):
+    """A device wait that nothing satisfies ends after its bound, the error word reports a
+    timeout once, and the next calls on the same context run normally."""
+    inputs, shape = wl.tiny(), wl.TINY
+    lay = oracle_plan(inputs, vocab=shape.vocab).passes[0]
+    plan = spinf.Plan(inputs, vocab=shape.vocab)
+    plan.upload(0)
+    plan.device_selftest(wait_ms=30)
+    with pytest.raises(spinf.SpinfError) as e:
+        plan.device_status()
+    assert e.value.status_name == "DEVICE_TIMEOUT"
+    plan.device_status()   # cleared
+    q, k, v, _ = pass_values(lay, shape, hidden_rows=False)
+    o1 = run_attention(spinf, plan, 0, q, k, v, shape)
+    o2 = run_attention(spinf, plan, 0, q, k, v, shape)
+    assert torch.equal(o1, o2) and torch.isfinite(o1).all()
+
+
+def test_selftest_rejects_bad_arguments(spinf):
+    plan = spinf.Plan(wl.tiny(), vocab=1024)
+    with pytest.raises(spinf.SpinfError):
+        plan.device_selftest(30)          # nothing uploaded yet: no error word
+    plan.upload(0)
+    for bad in (0, 10001):
+        with pytest.raises(spinf.SpinfError):
+            plan.device_selftest(bad)
