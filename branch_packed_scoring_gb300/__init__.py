@@ -30,6 +30,7 @@ SYMBOLS = [
     "spinf_plan_window_schedule",
     "spinf_branch_attention", "spinf_score_workspace_bytes",
     "spinf_score", "spinf_score_static", "spinf_collect", "spinf_device_status", "spinf_device_selftest",
+    "spinf_rope_tree", "spinf_linear",
     "spinf_plan_free", "spinf_fingerprint",
     "spinf_status_string", "spinf_last_error",
 ]
@@ -112,6 +113,8 @@ def lib():
     L.spinf_collect.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(_Result)]
     L.spinf_device_status.argtypes = [vp, vp]
     L.spinf_device_selftest.argtypes = [vp, i32, vp]
+    L.spinf_rope_tree.argtypes = [vp, i32, vp, vp, i32, i32, i32, f32, vp]
+    L.spinf_linear.argtypes = [vp, vp, vp, i64, i64, i64, vp]
     L.spinf_plan_free.argtypes = [vp]
     L.spinf_plan_free.restype = None
     L.spinf_fingerprint.restype = ctypes.c_char_p
@@ -121,7 +124,7 @@ def lib():
     for name in ("spinf_pack_plan", "spinf_plan_pass_info", "spinf_plan_counts", "spinf_plan_upload", "spinf_plan_upload_to",
                  "spinf_plan_window_schedule",
                  "spinf_branch_attention", "spinf_score", "spinf_score_static", "spinf_collect",
-                 "spinf_device_status", "spinf_device_selftest"):
+                 "spinf_device_status", "spinf_device_selftest", "spinf_rope_tree", "spinf_linear"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -364,6 +367,17 @@ class Plan:
 def branch_attention(plan, p, q, k, v, o, n_q_heads, n_kv_heads, d_head, scale=0.0, window=0, stream=None):
     _check(lib().spinf_branch_attention(plan.handle, p, _ptr(q), _ptr(k), _ptr(v), _ptr(o), n_q_heads,
                                         n_kv_heads, d_head, float(scale), int(window), _stream(stream)))
+
+
+def rope_tree(plan, p, q, k, n_q_heads, n_kv_heads, d_head, theta=10000.0, stream=None):
+    """Rotary embedding in place at each row's tree depth (spinf_rope_tree)."""
+    _check(lib().spinf_rope_tree(plan.handle, p, _ptr(q), _ptr(k), n_q_heads, n_kv_heads, d_head, float(theta),
+                                 _stream(stream)))
+
+
+def linear(x, w, y, stream=None):
+    """y = x . w^T on the device, bf16 (spinf_linear); x [rows, in], w [out, in], y [rows, out]."""
+    _check(lib().spinf_linear(_ptr(x), _ptr(w), _ptr(y), x.shape[0], x.shape[1], w.shape[0], _stream(stream)))
 
 
 def score_workspace_bytes(plan, p, vocab, d_model, w_dtype=DTYPE_BF16):

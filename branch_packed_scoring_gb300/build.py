@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspinf.so")
-SOURCES = ["plan.cpp", "runtime.cu", "attention.cu", "score.cu"]
+SOURCES = ["plan.cpp", "runtime.cu", "attention.cu", "score.cu", "layer.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -70,7 +70,7 @@ def build(verbose: bool = False, ptxas_info: bool = False, extra=()) -> str:
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
     if _stale(LIB, objs):
-        cmd = [nvcc] + ARCH + ["-shared", "-o", LIB] + objs
+        cmd = [nvcc] + ARCH + ["-shared", "-o", LIB] + objs + ["-lcublasLt"]
         r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
         if r.returncode:
             sys.stdout.write(r.stdout)

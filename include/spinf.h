@@ -294,6 +294,28 @@ spinf_status spinf_collect(const spinf_plan* plan, const float* const* token_lp_
  * SPINF_OK, SPINF_E_DEVICE_TIMEOUT or SPINF_E_DEVICE_CHECK (the word is cleared). */
 spinf_status spinf_device_status(const spinf_plan* plan, spinf_stream stream);
 
+/* ---- Around the attention call: the rest of a packed layer (QKV projection,
+ * rotary positions, output projection) with synthetic or real weights. ---- */
+
+/* Rotary position embedding in place on q [T_pad, Hq, d] and k [T_pad, Hkv, d]
+ * (bf16, device): row r's pairs (x[i], x[i + d/2]) turn by pos[r] * theta^(-2i/d),
+ * pos[r] being the row's depth on its own root path (spinf_pass_info.pos), so a
+ * branch token gets the position it has in its unpacked sequence ("spinf-serve
+ * 0.1.1" PyPI, "What it does": branches of one pass, scores equal alone or packed).
+ * Angles in fp64, rotation in fp32, bf16 round to nearest.  Pad rows have pos 0 (no
+ * change).  Needs the pass uploaded; asynchronous on `stream`.  SPINF_E_INVALID for
+ * NULL tensors, odd or > 1024 d_head, theta <= 1. */
+spinf_status spinf_rope_tree(const spinf_plan* plan, int32_t pass, void* q, void* k, int32_t n_q_heads,
+                             int32_t n_kv_heads, int32_t d_head, float theta, spinf_stream stream);
+
+/* y[rows, out] = x[rows, in] . w[out, in]^T: bf16 in and out, fp32 accumulation, all
+ * row-major on the device (a plain cuBLASLt GEMM: the QKV and output projections of
+ * a layer).  Features must be positive multiples of 8, pointers 16-byte aligned.
+ * Asynchronous on `stream`.  The pages have no counterpart beyond "one packed
+ * forward" (man page DESCRIPTION). */
+spinf_status spinf_linear(const void* x, const void* w, void* y, int64_t rows, int64_t in_features,
+                          int64_t out_features, spinf_stream stream);
+
 /* Failure-path self-test: enqueue on `stream` a one-thread kernel that waits on a
  * barrier nothing arrives on, with the kernels' bounded wait shortened to `wait_ms`
  * (1..10000); the plan's error word then holds the timeout, which the next
