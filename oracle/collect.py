@@ -11,6 +11,9 @@ the "spinf-serve" news repost (the refund question's response fragment):
   ``1 - sum_j exp(lp_j)`` (not clamped; it can only go negative when one option
   is a token prefix of another);
 * ``floor_*`` are the same quantities for the same question on empty content.
+
+A searched slot's answer (tokens and their log-probabilities, see
+:func:`oracle.score.topk_allowed`) is reported as it comes out of its pass.
 """
 from __future__ import annotations
 
@@ -50,6 +53,9 @@ def collect(plan, token_lp_per_pass):
         per_q = []
         for j in range(plan.n_questions[i]):
             home = plan.question_home[(i, j)]
+            if plan.searched[i][j]:
+                per_q.append(None)
+                continue
             lp = question_lp(home)
             p, residual = option_stats(lp)
             key = plan.passes[home[0]].questions[home[1]].key
@@ -64,3 +70,19 @@ def collect(plan, token_lp_per_pass):
                           "floor_lp": flp, "floor_p": fp, "floor_residual": fres})
         results.append(per_q)
     return results
+
+
+def collect_extract(plan, top_tok_per_pass, top_lp_per_pass):
+    """Per searched slot, in question order (input by input): ``(tokens[k], logprobs[k])``.
+
+    ``top_*_per_pass[p]`` hold pass ``p``'s answers in its extraction order.
+    """
+    out = []
+    for i in range(plan.n_inputs):
+        for j in range(plan.n_questions[i]):
+            if not plan.searched[i][j]:
+                continue
+            p, idx = plan.question_home[(i, j)]
+            x = plan.passes[p].questions[idx].extract
+            out.append((np.asarray(top_tok_per_pass[p][x]), np.asarray(top_lp_per_pass[p][x], dtype=np.float64)))
+    return out

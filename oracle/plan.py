@@ -16,6 +16,10 @@ What it restates, page by page:
   ``--max-prompts-per-input`` 10000, ``--max-options`` 1000,
   ``--max-option-tokens`` 5, ``--max-tokens`` (largest single input).
 * same page, CAVEATS: long inputs run alone.
+* "spinf-serve 0.1.1" (PyPI), "What it does" and the man page's DESCRIPTION:
+  extraction slots (``{*}`` text, ``{n}`` numbers, ``{$}`` amounts) ride the
+  same read; the engine returns the most likely answers with their
+  probabilities.
 
 Readings where the pages are silent (each is listed in the design notes):
 
@@ -34,6 +38,16 @@ Readings where the pages are silent (each is listed in the design notes):
 5. Position ids are tree depth (length of the root path minus one).
 6. The pass is padded to a multiple of 128 rows; a pad row sees nothing and
    its output is unspecified.
+7. A searched slot (``{*}``, ``{n}``, ``{$}``) is a template with no options:
+   its template rows are laid out like a scored question's, its last template
+   row is a scoring row, and the ``extract_k`` most likely next tokens there,
+   among an allowed-token set named by the question (``-1``: every token), are
+   returned with their log-probabilities.  Later decoding steps append the
+   chosen tokens to the template and plan again.  A searched slot gets no
+   floor (the pages give the floor for scored questions only).
+
+A question is ``(template, options)`` (scored) or ``(template, None, token_set)``
+(a searched slot).
 
 The visible-key set of a row is kept in its plainest form: the content rows of
 its own input up to itself (content rows) or all of them (branch rows), plus
@@ -61,7 +75,13 @@ DEFAULTS = {
     "floors": True,
     "floor_prefix": (),
     "vocab": 0,
+    "extract_k": 8,
 }
+
+
+def is_searched(question):
+    """A searched slot is written ``(template, None, token_set)``."""
+    return len(question) == 3 and question[1] is None
 
 
 class PlanError(Exception):
@@ -97,7 +117,9 @@ def trie_nodes(options):
 
 
 def question_size(template, options):
-    return len(template) + len(trie_nodes(options))
+    """Rows of one laid-out question: its template and its option-trie nodes
+    (``options`` is None for a searched slot: the template only)."""
+    return len(template) + (0 if options is None else len(trie_nodes(options)))
 
 
 @dataclass
@@ -121,6 +143,7 @@ class QuestionRecord:
     qidx: int
     key: object            # (template, options) as tuples: the floor lookup key
     option_gather: list    # per option: list of gather indices, in token order
+    extract: int = -1      # searched slot: its index in the pass's extraction list
 
 
 @dataclass
@@ -138,6 +161,8 @@ class PassLayout:
     slot_row: np.ndarray
     gather_m: np.ndarray
     gather_tok: np.ndarray
+    x_m: np.ndarray        # [X] scoring-row index of each searched slot, in layout order
+    x_set: np.ndarray      # [X] its allowed-token set (-1: any token)
     units: list
     questions: list
     # visible-set representation, per real row (global rows)
@@ -156,7 +181,9 @@ class Plan:
     passes: list
     n_inputs: int
     n_questions: list      # per user input
-    n_options: list        # per user input: list per question
+    n_options: list        # per user input: list per question (0 for a searched slot)
+    searched: list         # per user input: list per question of bools
+    extract_k: int
     question_home: dict    # (input, qidx) -> (pass, record index)
     floor_home: dict       # floor key -> (pass, record index)
 
@@ -167,6 +194,8 @@ def _key(template, options):
 
 def _validate(inputs, o):
     vocab = o["vocab"]
+    if not (1 <= o["extract_k"] <= 16):
+        raise PlanError("INVALID", "extract_k must be in 1..16")
 
     def ids_ok(ids):
         return vocab <= 0 or all(0 <= t < vocab for t in ids)
@@ -183,12 +212,20 @@ def _validate(inputs, o):
         if len(content) == 0 and len(questions) == 0:
             raise PlanError("INVALID", f"input {i}: nothing to read")
         size = len(content)
-        for j, (template, options) in enumerate(questions):
+        for j, question in enumerate(questions):
+            template, options = question[0], question[1]
             if len(template) == 0:
                 raise PlanError("INVALID", f"input {i} question {j}: empty template")
             if len(template) > o["max_query_tokens"]:
                 raise PlanError("LIMIT", f"input {i} question {j}: template longer than max_query_tokens")
-            if len(options) == 0:
+            if is_searched(question):
+                if not isinstance(question[2], int) or question[2] < -1:
+                    raise PlanError("INVALID", f"input {i} question {j}: bad token set")
+                if not ids_ok(template):
+                    raise PlanError("INVALID", f"input {i} question {j}: template token out of range")
+                size += len(template)
+                continue
+            if options is None or len(options) == 0:
                 raise PlanError("INVALID", f"input {i} question {j}: no options")
             if len(options) > o["max_options"]:
                 raise PlanError("LIMIT", f"input {i} question {j}: more options than max_options")
@@ -215,11 +252,10 @@ def _units(inputs, o):
     units = []
     for i, (content, questions) in enumerate(inputs):
         content = tuple(content)
-        sizes = [question_size(t, opts) for t, opts in questions]
+        sizes = [question_size(q[0], q[1]) for q in questions]
         total = len(content) + sum(sizes)
         if total <= budget:
-            units.append(Unit(i, list(range(len(questions))), content,
-                              [(tuple(t), [tuple(x) for x in opts]) for t, opts in questions], size=total))
+            units.append(Unit(i, list(range(len(questions))), content, [_norm(q) for q in questions], size=total))
             continue
         # long input: chunks of the full content plus a greedy run of questions
         j = 0
@@ -234,14 +270,15 @@ def _units(inputs, o):
                 j += 1
             if not held:
                 raise PlanError("LIMIT", f"input {i}: content plus question {j} do not fit the token budget")
-            units.append(Unit(i, held, content,
-                              [(tuple(questions[q][0]), [tuple(x) for x in questions[q][1]]) for q in held],
-                              size=size))
+            units.append(Unit(i, held, content, [_norm(questions[q]) for q in held], size=size))
     if o["floors"]:
         prefix = tuple(o["floor_prefix"])
         seen = {}
         for content, questions in inputs:
-            for template, options in questions:
+            for question in questions:
+                if is_searched(question):
+                    continue
+                template, options = question
                 k = _key(template, options)
                 if k in seen:
                     continue
@@ -252,6 +289,13 @@ def _units(inputs, o):
                 units.append(Unit(-1, [0], prefix, [(tuple(template), [tuple(x) for x in options])],
                                   floor_key=k, size=size))
     return units
+
+
+def _norm(question):
+    """A question as tuples: ``(template, [options])`` or ``(template, None, token_set)``."""
+    if is_searched(question):
+        return (tuple(question[0]), None, int(question[2]))
+    return (tuple(question[0]), [tuple(x) for x in question[1]])
 
 
 def _pack(units, budget):
@@ -272,6 +316,7 @@ def _layout_pass(units):
     tok, parent, content_lo, content_hi, chain, anchor = [], [], [], [], [], []
     records = []
     gather_rows, gather_tok = [], []
+    x_rows, x_set = [], []
     for u in units:
         s = len(tok)
         u.start = s
@@ -284,7 +329,8 @@ def _layout_pass(units):
             chain.append([])
             anchor.append(s)
         last_content = s + L - 1 if L > 0 else -1
-        for qn, (template, options) in enumerate(u.questions):
+        for qn, question in enumerate(u.questions):
+            template, options = question[0], question[1]
             prev = last_content
             for t in template:
                 r = len(tok)
@@ -296,6 +342,11 @@ def _layout_pass(units):
                 anchor.append(s)
                 prev = r
             slot = prev
+            if options is None:   # searched slot: the template's last row is scored, nothing else is laid out
+                records.append(QuestionRecord(u.source, u.qidx[qn], None, [], extract=len(x_rows)))
+                x_rows.append(slot)
+                x_set.append(question[2])
+                continue
             node_row = {(): slot}
             for prefix in trie_nodes(options):
                 r = len(tok)
@@ -373,13 +424,14 @@ def _layout_pass(units):
                 tile_kv.append(s + TILE * j)
                 tile_len.append(min(TILE, e - (s + TILE * j)))   # keys of the tile inside this input
         tile_ptr.append(len(tile_kv))
-    rows = sorted(set(gather_rows))
+    rows = sorted(set(gather_rows) | set(x_rows))
     m_of = {r: m for m, r in enumerate(rows)}
     i32 = lambda a: np.asarray(a, dtype=np.int32)  # noqa: E731
     return PassLayout(
         T=T, T_pad=T_pad, tok=i32(tok), parent=i32(parent), pos=i32(pos), end=i32(end), anchor=i32(anchor),
         tile_ptr=i32(tile_ptr), tile_kv=i32(tile_kv), tile_len=i32(tile_len), slot_row=i32(rows),
         gather_m=i32([m_of[r] for r in gather_rows]), gather_tok=i32(gather_tok),
+        x_m=i32([m_of[r] for r in x_rows]), x_set=i32(x_set),
         units=units, questions=records,
         content_lo=i32(content_lo), content_hi=i32(content_hi), chain=chain,
     )
@@ -388,7 +440,9 @@ def _layout_pass(units):
 def plan(inputs, **opts) -> Plan:
     """Lay ``inputs`` out in packed passes.
 
-    ``inputs`` is a list of ``(content_ids, [(template_ids, [option_ids, ...]), ...])``.
+    ``inputs`` is a list of ``(content_ids, [question, ...])``, a question being
+    ``(template_ids, [option_ids, ...])`` or, for a searched slot,
+    ``(template_ids, None, token_set)``.
     Options are keyword arguments named as in :data:`DEFAULTS`.
     """
     o = dict(DEFAULTS)
@@ -410,7 +464,9 @@ def plan(inputs, **opts) -> Plan:
         passes=passes,
         n_inputs=len(inputs),
         n_questions=[len(q) for _, q in inputs],
-        n_options=[[len(opts) for _, opts in q] for _, q in inputs],
+        n_options=[[0 if is_searched(x) else len(x[1]) for x in q] for _, q in inputs],
+        searched=[[is_searched(x) for x in q] for _, q in inputs],
+        extract_k=o["extract_k"],
         question_home=question_home,
         floor_home=floor_home,
     )

@@ -15,6 +15,12 @@ For every scoring row ``r`` (a slot or an option-prefix row, see
 * ``lse_r = log sum_v exp(z_r[v])``;
 * the log-probability of option token ``t`` read at row ``r`` is
   ``z_r[t] - lse_r``.
+
+A searched slot (``{*}``, ``{n}``, ``{$}``; PyPI page, "What it does": the
+most likely answers with their probabilities) reads the same distribution at
+its slot row and returns the ``k`` tokens of the allowed set with the largest
+``z`` (ties: the lower token id first), each with ``z - lse`` over the whole
+vocabulary.
 """
 from __future__ import annotations
 
@@ -70,3 +76,43 @@ def score_rows(h_slot, gather_m, gather_tok, w=None, w_codes=None, w_scale=None,
     gm = np.asarray(gather_m, dtype=np.int64)
     gt = np.asarray(gather_tok, dtype=np.int64)
     return lse, z[gm, gt] - lse[gm]
+
+
+def topk_allowed(z_row, lse_row, allowed, k):
+    """The searched-slot answer of one row: ``(tokens[k], logprobs[k])``.
+
+    ``allowed``: a boolean mask over the vocabulary, or None for every token.
+    The allowed tokens are ordered by ``z`` descending, then by token id, and the
+    first ``k`` are kept; missing places (fewer than ``k`` allowed tokens) are
+    ``(-1, -inf)``.
+    """
+    z_row = np.asarray(z_row, dtype=np.float64)
+    cand = np.arange(z_row.shape[0]) if allowed is None else np.flatnonzero(np.asarray(allowed, dtype=bool))
+    order = np.lexsort((cand, -z_row[cand]))      # primary key: -z; secondary: token id
+    top = cand[order[:k]]
+    tok = np.full(k, -1, dtype=np.int64)
+    lp = np.full(k, -np.inf)
+    tok[:len(top)] = top
+    lp[:len(top)] = z_row[top] - lse_row
+    return tok, lp
+
+
+def extract_rows(h_x, x_set, token_sets, k, w=None, w_codes=None, w_scale=None, chunk=16384):
+    """Searched-slot answers for the rows ``h_x`` (``[X, D]``): ``(tokens[X, k], logprobs[X, k])``.
+
+    ``x_set[x]`` names the allowed set of row ``x`` (an index into ``token_sets``,
+    boolean masks over the vocabulary), ``-1`` for every token.
+    """
+    act_fp8 = w_codes is not None
+    h = hidden_rows(h_x, act_fp8)
+    V = (w if w is not None else w_codes).shape[0]
+    z = np.empty((h.shape[0], V), dtype=np.float64)
+    for v0 in range(0, V, chunk):
+        z[:, v0:v0 + chunk] = logits(h, weight_rows(w, w_codes, w_scale, slice(v0, v0 + chunk)))
+    lse = logsumexp(z)
+    toks = np.full((h.shape[0], k), -1, dtype=np.int64)
+    lps = np.full((h.shape[0], k), -np.inf)
+    for x in range(h.shape[0]):
+        s = int(x_set[x])
+        toks[x], lps[x] = topk_allowed(z[x], lse[x], None if s < 0 else token_sets[s], k)
+    return toks, lps
