@@ -22,14 +22,16 @@ OK, E_INVALID, E_LIMIT, E_NOMEM, E_CUDA, E_UNSUPPORTED, E_DEVICE_TIMEOUT, E_DEVI
 STATUS_NAMES = {0: "OK", 1: "INVALID", 2: "LIMIT", 3: "NOMEM", 4: "CUDA", 5: "UNSUPPORTED",
                 6: "DEVICE_TIMEOUT", 7: "DEVICE_CHECK"}
 DTYPE_BF16, DTYPE_E4M3 = 0, 1
+Q_SCORED, Q_SEARCHED = 0, 1
 
 #: every symbol the header declares
 SYMBOLS = [
     "spinf_plan_opts_default", "spinf_pack_plan", "spinf_plan_num_passes", "spinf_plan_pass_info",
-    "spinf_plan_counts", "spinf_plan_upload", "spinf_plan_descriptor_bytes", "spinf_plan_upload_to",
+    "spinf_plan_counts", "spinf_plan_extract_counts", "spinf_plan_upload", "spinf_plan_descriptor_bytes", "spinf_plan_upload_to",
     "spinf_plan_window_schedule",
     "spinf_branch_attention", "spinf_score_workspace_bytes",
-    "spinf_score", "spinf_score_static", "spinf_collect", "spinf_device_status", "spinf_device_selftest",
+    "spinf_score", "spinf_score_extract", "spinf_score_static", "spinf_collect", "spinf_collect_extract",
+    "spinf_device_status", "spinf_device_selftest",
     "spinf_rope_tree", "spinf_linear",
     "spinf_plan_free", "spinf_fingerprint",
     "spinf_status_string", "spinf_last_error",
@@ -52,7 +54,7 @@ class _Opts(ctypes.Structure):
                 ("max_content_tokens", ctypes.c_int32), ("max_query_tokens", ctypes.c_int32),
                 ("max_options", ctypes.c_int32), ("max_option_tokens", ctypes.c_int32),
                 ("max_prompts_per_input", ctypes.c_int32), ("floors", ctypes.c_int32),
-                ("floor_prefix", _Tokens), ("vocab", ctypes.c_int32)]
+                ("floor_prefix", _Tokens), ("vocab", ctypes.c_int32), ("extract_k", ctypes.c_int32)]
 
 
 _P = ctypes.POINTER(ctypes.c_int32)
@@ -61,10 +63,16 @@ _P = ctypes.POINTER(ctypes.c_int32)
 class _PassInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("T", "T_pad", "n_qtiles", "n_sched", "M", "G", "n_units")] + \
                [(n, _P) for n in ("tok", "parent", "pos", "end", "anchor", "tile_ptr", "tile_kv", "tile_len", "slot_row",
-                                  "gather_m", "gather_tok", "unit_start", "unit_source", "row_runs")]
+                                  "gather_m", "gather_tok", "unit_start", "unit_source", "row_runs")] + \
+               [("X", ctypes.c_int32), ("x_m", _P), ("x_set", _P)]
 
 
 _D = ctypes.POINTER(ctypes.c_double)
+
+
+class _ExtractOut(ctypes.Structure):
+    _fields_ = [("token_sets", ctypes.c_void_p), ("n_sets", ctypes.c_int32), ("top_tok", ctypes.c_void_p),
+                ("top_lp", ctypes.c_void_p)]
 
 
 class _Result(ctypes.Structure):
@@ -75,7 +83,7 @@ class _Result(ctypes.Structure):
 # numpy views of the request structs (same layout as the header on LP64)
 _TOK = np.dtype([("ids", "<u8"), ("n", "<i4"), ("_pad", "<i4")])
 _QUE = np.dtype([("tmpl_ids", "<u8"), ("tmpl_n", "<i4"), ("_p0", "<i4"), ("options", "<u8"),
-                 ("n_options", "<i4"), ("_p1", "<i4")])
+                 ("n_options", "<i4"), ("kind", "<i4"), ("token_set", "<i4"), ("_p1", "<i4")])
 _INP = np.dtype([("content_ids", "<u8"), ("content_n", "<i4"), ("_p0", "<i4"), ("questions", "<u8"),
                  ("n_questions", "<i4"), ("_p1", "<i4")])
 
@@ -99,6 +107,7 @@ def lib():
     L.spinf_plan_num_passes.restype = i32
     L.spinf_plan_pass_info.argtypes = [vp, i32, ctypes.POINTER(_PassInfo)]
     L.spinf_plan_counts.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    L.spinf_plan_extract_counts.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i32)]
     L.spinf_plan_upload.argtypes = [vp, i32, vp]
     L.spinf_plan_descriptor_bytes.argtypes = [vp, i32]
     L.spinf_plan_descriptor_bytes.restype = sz
@@ -109,8 +118,11 @@ def lib():
     L.spinf_score_workspace_bytes.argtypes = [vp, i32, i32, i32, i32]
     L.spinf_score_workspace_bytes.restype = sz
     L.spinf_score.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.spinf_score_extract.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, vp, vp, ctypes.POINTER(_ExtractOut), vp,
+                                      sz, vp]
     L.spinf_score_static.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp]
     L.spinf_collect.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(_Result)]
+    L.spinf_collect_extract.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, vp]
     L.spinf_device_status.argtypes = [vp, vp]
     L.spinf_device_selftest.argtypes = [vp, i32, vp]
     L.spinf_rope_tree.argtypes = [vp, i32, vp, vp, i32, i32, i32, f32, vp]
@@ -121,9 +133,10 @@ def lib():
     L.spinf_status_string.argtypes = [i32]
     L.spinf_status_string.restype = ctypes.c_char_p
     L.spinf_last_error.restype = ctypes.c_char_p
-    for name in ("spinf_pack_plan", "spinf_plan_pass_info", "spinf_plan_counts", "spinf_plan_upload", "spinf_plan_upload_to",
-                 "spinf_plan_window_schedule",
-                 "spinf_branch_attention", "spinf_score", "spinf_score_static", "spinf_collect",
+    for name in ("spinf_pack_plan", "spinf_plan_pass_info", "spinf_plan_counts", "spinf_plan_extract_counts",
+                 "spinf_plan_upload", "spinf_plan_upload_to", "spinf_plan_window_schedule",
+                 "spinf_branch_attention", "spinf_score", "spinf_score_extract", "spinf_score_static", "spinf_collect",
+                 "spinf_collect_extract",
                  "spinf_device_status", "spinf_device_selftest", "spinf_rope_tree", "spinf_linear"):
         getattr(L, name).restype = i32
     _lib = L
@@ -184,11 +197,15 @@ class PassInfo:
     unit_start: np.ndarray
     unit_source: np.ndarray
     row_runs: np.ndarray
+    X: int = 0
+    x_m: np.ndarray = None
+    x_set: np.ndarray = None
 
 
 def _marshal(inputs):
     """Lay the request out as the header's structs in numpy buffers (kept alive by the caller)."""
     ids, c_off, c_n, nq, t_off, t_n, no, o_off, o_n = [], [], [], [], [], [], [], [], []
+    kind, tset = [], []
     pos = 0
     for content, questions in inputs:
         c_off.append(pos)
@@ -196,11 +213,16 @@ def _marshal(inputs):
         ids.extend(content)
         pos += len(content)
         nq.append(len(questions))
-        for template, options in questions:
+        for question in questions:
+            template, options = question[0], question[1]
             t_off.append(pos)
             t_n.append(len(template))
             ids.extend(template)
             pos += len(template)
+            searched = len(question) == 3 and options is None   # (template, None, token_set)
+            kind.append(Q_SEARCHED if searched else Q_SCORED)
+            tset.append(int(question[2]) if searched else -1)
+            options = () if searched else options
             no.append(len(options))
             for opt in options:
                 o_off.append(pos)
@@ -223,6 +245,8 @@ def _marshal(inputs):
         first_opt = np.concatenate([[0], np.cumsum(no)[:-1]]).astype(np.uint64)
         que["options"][:nt] = np.uint64(tok.ctypes.data) + np.uint64(_TOK.itemsize) * first_opt
         que["n_options"][:nt] = no
+        que["kind"][:nt] = kind
+        que["token_set"][:nt] = tset
     if len(inputs):
         c_n = np.asarray(c_n, dtype=np.int64)
         inp["content_ids"] = np.where(c_n > 0, base + four * np.asarray(c_off, dtype=np.uint64), np.uint64(0))
@@ -249,13 +273,14 @@ class Request:
 class Plan:
     """A packed layout of a request (``spinf_pack_plan``).  Owns its device copies.
 
-    ``inputs`` is a list of ``(content_ids, [(template_ids, [option_ids, ...]), ...])``
-    or a :class:`Request`.
+    ``inputs`` is a list of ``(content_ids, [question, ...])`` or a :class:`Request`;
+    a question is ``(template_ids, [option_ids, ...])`` (scored) or
+    ``(template_ids, None, token_set)`` (a searched slot, ``token_set`` -1 for any token).
     """
 
     def __init__(self, inputs, *, token_budget=None, max_tokens=None, max_content_tokens=None,
                  max_query_tokens=None, max_options=None, max_option_tokens=None, max_prompts_per_input=None,
-                 floors=True, floor_prefix=(), vocab=0):
+                 floors=True, floor_prefix=(), vocab=0, extract_k=None):
         L = lib()
         self._h = None
         opts = _Opts()
@@ -271,6 +296,8 @@ class Plan:
         opts.floor_prefix.ids = fp.ctypes.data if len(fp) else None
         opts.floor_prefix.n = len(fp)
         opts.vocab = int(vocab)
+        if extract_k is not None:
+            opts.extract_k = int(extract_k)
         if isinstance(inputs, Request):
             inp, keep, n_inputs = inputs.inp, None, inputs.n_inputs
         else:
@@ -303,12 +330,19 @@ class Plan:
             slot_row=arr(info.slot_row, info.M), gather_m=arr(info.gather_m, info.G),
             gather_tok=arr(info.gather_tok, info.G), unit_start=arr(info.unit_start, info.n_units + 1),
             unit_source=arr(info.unit_source, info.n_units),
-            row_runs=arr(info.row_runs, 8 * info.T_pad).reshape(info.T_pad, 8))
+            row_runs=arr(info.row_runs, 8 * info.T_pad).reshape(info.T_pad, 8),
+            X=info.X, x_m=arr(info.x_m, info.X), x_set=arr(info.x_set, info.X))
 
     def counts(self):
         nq, no = ctypes.c_int64(), ctypes.c_int64()
         _check(lib().spinf_plan_counts(self.handle, ctypes.byref(nq), ctypes.byref(no)))
         return nq.value, no.value
+
+    def extract_counts(self):
+        """(searched slots over the request, extract_k)."""
+        n, k = ctypes.c_int64(), ctypes.c_int32()
+        _check(lib().spinf_plan_extract_counts(self.handle, ctypes.byref(n), ctypes.byref(k)))
+        return n.value, k.value
 
     def window_schedule(self, p, window):
         """(tile_ptr, tile_kv, tile_len) of pass p's schedule for a sliding window."""
@@ -344,6 +378,20 @@ class Plan:
         ptrs = (ctypes.c_void_p * max(1, len(arrs)))(*[a.ctypes.data for a in arrs])
         _check(lib().spinf_collect(self.handle, ptrs, ctypes.byref(res)))
         return out
+
+    def collect_extract(self, top_tok_per_pass, top_lp_per_pass):
+        """Searched-slot answers in question order: (tokens [n, k] int32, lp [n, k] float64)."""
+        n, k = self.extract_counts()
+        tok = np.full((n, k), -1, dtype=np.int32)
+        lp = np.full((n, k), -np.inf)
+        if len(top_tok_per_pass) != self.num_passes or len(top_lp_per_pass) != self.num_passes:
+            raise ValueError("one answer array per pass is needed")
+        ta = [np.ascontiguousarray(a, dtype=np.int32) for a in top_tok_per_pass]
+        la = [np.ascontiguousarray(a, dtype=np.float32) for a in top_lp_per_pass]
+        tp = (ctypes.c_void_p * max(1, len(ta)))(*[a.ctypes.data for a in ta])
+        lpp = (ctypes.c_void_p * max(1, len(la)))(*[a.ctypes.data for a in la])
+        _check(lib().spinf_collect_extract(self.handle, tp, lpp, tok.ctypes.data, lp.ctypes.data))
+        return tok, lp
 
     def device_status(self, stream=None):
         _check(lib().spinf_device_status(self.handle, _stream(stream)))
@@ -385,12 +433,22 @@ def score_workspace_bytes(plan, p, vocab, d_model, w_dtype=DTYPE_BF16):
 
 
 def score(plan, p, hidden, w, w_scale, w_dtype, d_model, vocab, row_lse, token_lp, workspace, workspace_bytes=None,
-          stream=None):
+          stream=None, extract=None):
+    """``spinf_score``; with ``extract`` (a dict of ``top_tok`` [X, k] int32 and ``top_lp`` [X, k] fp32 device
+    tensors, optional ``token_sets`` [n_sets, ceil(vocab/32)] int32 bitmasks) ``spinf_score_extract``."""
     if workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size()
-    _check(lib().spinf_score(plan.handle, p, _ptr(hidden), _ptr(w), _ptr(w_scale), w_dtype, d_model, vocab,
-                             _ptr(row_lse), _ptr(token_lp), _ptr(workspace), int(workspace_bytes),
-                             _stream(stream)))
+    if extract is None:
+        _check(lib().spinf_score(plan.handle, p, _ptr(hidden), _ptr(w), _ptr(w_scale), w_dtype, d_model, vocab,
+                                 _ptr(row_lse), _ptr(token_lp), _ptr(workspace), int(workspace_bytes),
+                                 _stream(stream)))
+        return
+    sets = extract.get("token_sets")
+    ex = _ExtractOut(_ptr(sets), 0 if sets is None else int(sets.shape[0]), _ptr(extract["top_tok"]),
+                     _ptr(extract["top_lp"]))
+    _check(lib().spinf_score_extract(plan.handle, p, _ptr(hidden), _ptr(w), _ptr(w_scale), w_dtype, d_model, vocab,
+                                     _ptr(row_lse), _ptr(token_lp), ctypes.byref(ex), _ptr(workspace),
+                                     int(workspace_bytes), _stream(stream)))
 
 
 def score_static(plan, p, hidden, w, w_scale, w_dtype, d_model, vocab, row_lse, token_lp, stream=None):

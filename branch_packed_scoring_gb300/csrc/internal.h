@@ -29,6 +29,9 @@ struct PassDevice {
     int32_t* row_glist = nullptr;  // [G]     ... sorted by token id, then gather index
     int32_t* qt_work = nullptr;    // [n_qtiles][4] attention work order {qt, s0, n, 0}, most KV tiles first
     int32_t* row_runs = nullptr;   // [T_pad][8] root path of each row as <= 4 runs [lo, hi) (lo0 -1: more)
+    int32_t* row_x = nullptr;      // [M] searched-slot index of each scoring row, or -1
+    int32_t* x_m = nullptr;        // [X] scoring row of each searched slot
+    int32_t* x_set = nullptr;      // [X] allowed-token set of each searched slot (-1: every token)
 };
 
 // The KV-tile schedule of one pass for a sliding window W: the W = 0 schedule without
@@ -47,6 +50,7 @@ struct Pass {
     std::vector<int32_t> tile_ptr, tile_kv, tile_len, qt_work, row_runs;
     std::vector<int32_t> slot_row, gather_m, gather_tok;
     std::vector<int32_t> row_gptr, row_glist;
+    std::vector<int32_t> x_m, x_set, row_x;   // searched slots: scoring row, token set; per scoring row its slot or -1
     std::vector<int32_t> unit_start, unit_source;
     PassDevice dev;
     std::vector<unsigned char> staging;   // host source of the descriptor upload, kept until the plan is freed
@@ -59,6 +63,7 @@ struct QuestionSite {
     int32_t g0 = 0;          // first gather entry
     int32_t opt0 = 0;        // first entry in Plan::opt_len
     int32_t n_options = 0;
+    int32_t x = -1;          // searched slot: index in its pass's x_m / x_set
 };
 
 }  // namespace spinf
@@ -70,6 +75,8 @@ struct spinf_plan {
     std::vector<int32_t> user_q_floor;           // floor index per user question, or -1
     std::vector<spinf::QuestionSite> floor_q;    // every floor question
     int64_t n_options_total = 0;
+    int64_t n_extract = 0;                       // searched slots among the user questions
+    int32_t extract_k = 8;
     int32_t* d_err = nullptr;                    // device error word (allocated at first upload)
     bool err_owned = true;                       // false: inside a caller-owned descriptor buffer
     int device = -1;

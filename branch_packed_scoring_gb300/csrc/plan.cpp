@@ -6,7 +6,9 @@
 // another packed input; inputs are packed into passes of --token-budget rows
 // ("spinf-serve" man page, PARAMETERS); long inputs run alone, split with the
 // content repeated (man page, CAVEATS).  Options form a token trie per question
-// (PyPI page, "Layout": "templates to token tries").
+// (PyPI page, "Layout": "templates to token tries").  A searched slot ({*}, {n},
+// {$}; PyPI page, "What it does") lays out its template only and is scored at its
+// last template row.
 //
 // Visibility is encoded by two integers per row: key k is visible to exactly the
 // rows [k, end[k]) -- in a pre-order layout a row's descendants follow it
@@ -187,6 +189,7 @@ extern "C" void spinf_plan_opts_default(spinf_plan_opts* o) {
     o->floor_prefix.ids = nullptr;
     o->floor_prefix.n = 0;
     o->vocab = 0;
+    o->extract_k = 8;
 }
 
 extern "C" spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inputs,
@@ -200,6 +203,7 @@ extern "C" spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inp
     if (o.token_budget <= 0 || o.max_tokens <= 0 || o.floor_prefix.n < 0)
         return fail(SPINF_E_INVALID, "bad planner options");
     if (!ids_in_range(o.floor_prefix, o.vocab)) return fail(SPINF_E_INVALID, "floor prefix token out of range");
+    if (o.extract_k < 1 || o.extract_k > 16) return fail(SPINF_E_INVALID, "extract_k must be in 1..16");
 
     try {
         // ---- validation and tries
@@ -223,6 +227,15 @@ extern "C" spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inp
                 std::string wq = where + " question " + std::to_string(j);
                 if (q.tmpl.n <= 0) return fail(SPINF_E_INVALID, wq + ": empty template");
                 if (q.tmpl.n > o.max_query_tokens) return fail(SPINF_E_LIMIT, wq + ": template longer than max_query_tokens");
+                if (q.kind != SPINF_Q_SCORED && q.kind != SPINF_Q_SEARCHED) return fail(SPINF_E_INVALID, wq + ": unknown kind");
+                if (q.kind == SPINF_Q_SEARCHED) {   // template only: no options, no trie
+                    if (q.n_options != 0) return fail(SPINF_E_INVALID, wq + ": a searched slot has no options");
+                    if (q.token_set < -1) return fail(SPINF_E_INVALID, wq + ": bad token set");
+                    if (!ids_in_range(q.tmpl, o.vocab)) return fail(SPINF_E_INVALID, wq + ": template token out of range");
+                    qsize[i].push_back(q.tmpl.n);
+                    size += q.tmpl.n;
+                    continue;
+                }
                 if (q.n_options <= 0 || !q.options) return fail(SPINF_E_INVALID, wq + ": no options");
                 if (q.n_options > o.max_options) return fail(SPINF_E_LIMIT, wq + ": more options than max_options");
                 for (int32_t a = 0; a < q.n_options; ++a) {
@@ -289,6 +302,7 @@ extern "C" spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inp
             for (int32_t i = 0; i < n_inputs; ++i)
                 for (int32_t j = 0; j < inputs[i].n_questions; ++j) {
                     const spinf_question& q = inputs[i].questions[j];
+                    if (q.kind == SPINF_Q_SEARCHED) continue;   // floors belong to scored questions
                     std::string key = question_key(q);
                     auto it = seen.find(key);
                     if (it != seen.end()) {
@@ -318,10 +332,12 @@ extern "C" spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inp
                     QuestionSite& s = plan->user_q[q_base[i] + j];
                     s.opt0 = opt0;
                     s.n_options = q.n_options;
+                    if (q.kind == SPINF_Q_SEARCHED) ++plan->n_extract;
                     for (int32_t a = 0; a < q.n_options; ++a) plan->opt_len.push_back(q.options[a].n);
                     opt0 += q.n_options;
                 }
             plan->n_options_total = opt0;
+            plan->extract_k = o.extract_k;
             for (int32_t qi = 0; qi < n_user_q; ++qi) {
                 int32_t f = plan->user_q_floor[qi];
                 if (f >= 0) {
@@ -362,6 +378,7 @@ extern "C" spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inp
             P.end.resize(T_pad);
             P.anchor.resize(T_pad);
             std::vector<int32_t> g_row;   // packed row of each gather entry
+            std::vector<int32_t> x_row;   // packed row of each searched slot
             int32_t r = 0;
             for (const Unit* u : packs[p]) {
                 const int32_t s = r, e = r + (int32_t)u->size, L = u->content.n;
@@ -387,6 +404,14 @@ extern "C" spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inp
                         P.anchor[r] = s;
                     }
                     const int32_t slot = r - 1;
+                    if (q.kind == SPINF_Q_SEARCHED) {
+                        QuestionSite& dst = plan->user_q[u->qidx[qn]];   // floors hold scored questions only
+                        dst.pass = (int32_t)p;
+                        dst.x = (int32_t)x_row.size();
+                        x_row.push_back(slot);
+                        P.x_set.push_back(q.token_set);
+                        continue;
+                    }
                     const int32_t node0 = r;
                     for (int32_t n : t.order) {
                         P.tok[r] = t.tok[n];
@@ -495,9 +520,10 @@ extern "C" spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inp
                 P.qt_work[4 * i + 2] = P.tile_ptr[qt + 1] - P.tile_ptr[qt];
             }
 
-            // scoring rows: the distinct gather rows, ascending
+            // scoring rows: the distinct gather and searched-slot rows, ascending
             std::vector<int32_t> m_of(T > 0 ? T : 1, -1);
             for (int32_t row : g_row) m_of[row] = 0;
+            for (int32_t row : x_row) m_of[row] = 0;
             for (int32_t row = 0; row < T; ++row)
                 if (m_of[row] >= 0) {
                     m_of[row] = (int32_t)P.slot_row.size();
@@ -506,6 +532,11 @@ extern "C" spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inp
             const int32_t G = (int32_t)g_row.size(), M = (int32_t)P.slot_row.size();
             P.gather_m.resize(G);
             for (int32_t g = 0; g < G; ++g) P.gather_m[g] = m_of[g_row[g]];
+            P.row_x.assign(M, -1);
+            for (size_t x = 0; x < x_row.size(); ++x) {
+                P.x_m.push_back(m_of[x_row[x]]);
+                P.row_x[m_of[x_row[x]]] = (int32_t)x;
+            }
             P.row_gptr.assign(M + 1, 0);
             for (int32_t g = 0; g < G; ++g) P.row_gptr[P.gather_m[g] + 1]++;
             for (int32_t m = 0; m < M; ++m) P.row_gptr[m + 1] += P.row_gptr[m];
@@ -570,6 +601,9 @@ extern "C" spinf_status spinf_plan_pass_info(const spinf_plan* plan, int32_t pas
     out->unit_start = P.unit_start.data();
     out->unit_source = P.unit_source.data();
     out->row_runs = P.row_runs.data();
+    out->X = (int32_t)P.x_m.size();
+    out->x_m = P.x_m.data();
+    out->x_set = P.x_set.data();
     return SPINF_OK;
 }
 
@@ -577,6 +611,13 @@ extern "C" spinf_status spinf_plan_counts(const spinf_plan* plan, int64_t* n_que
     if (!plan) return fail(SPINF_E_INVALID, "plan is NULL");
     if (n_questions) *n_questions = (int64_t)plan->user_q.size();
     if (n_options) *n_options = plan->n_options_total;
+    return SPINF_OK;
+}
+
+extern "C" spinf_status spinf_plan_extract_counts(const spinf_plan* plan, int64_t* n_extract, int32_t* extract_k) {
+    if (!plan) return fail(SPINF_E_INVALID, "plan is NULL");
+    if (n_extract) *n_extract = plan->n_extract;
+    if (extract_k) *extract_k = plan->extract_k;
     return SPINF_OK;
 }
 
@@ -612,6 +653,11 @@ extern "C" spinf_status spinf_collect(const spinf_plan* plan, const float* const
     std::vector<double> flp, fp;
     for (size_t qi = 0; qi < plan->user_q.size(); ++qi) {
         const QuestionSite& s = plan->user_q[qi];
+        if (s.x >= 0) {   // a searched slot: no options, no floor
+            out->residual[qi] = NAN;
+            if (out->floor_residual) out->floor_residual[qi] = NAN;
+            continue;
+        }
         question_stats(plan, s, tlp[s.pass], out->option_lp + s.opt0, out->option_p + s.opt0, out->residual + qi);
         const int32_t f = plan->user_q_floor[qi];
         double fres = NAN;
@@ -626,6 +672,27 @@ extern "C" spinf_status spinf_collect(const spinf_plan* plan, const float* const
             if (out->option_floor_p) out->option_floor_p[s.opt0 + a] = fp[a];
         }
         if (out->floor_residual) out->floor_residual[qi] = fres;
+    }
+    return SPINF_OK;
+}
+
+extern "C" spinf_status spinf_collect_extract(const spinf_plan* plan, const int32_t* const* top_tok,
+                                              const float* const* top_lp, int32_t* tok, double* lp) {
+    if (!plan) return fail(SPINF_E_INVALID, "plan is NULL");
+    if (plan->n_extract == 0) return SPINF_OK;
+    if (!top_tok || !top_lp || !tok || !lp) return fail(SPINF_E_INVALID, "NULL arrays");
+    const int32_t k = plan->extract_k;
+    int64_t e = 0;
+    for (const QuestionSite& s : plan->user_q) {
+        if (s.x < 0) continue;
+        const int32_t* st = top_tok[s.pass];
+        const float* sl = top_lp[s.pass];
+        if (!st || !sl) return fail(SPINF_E_INVALID, "answers of a pass are NULL");
+        for (int32_t j = 0; j < k; ++j) {
+            tok[e * k + j] = st[(size_t)s.x * k + j];
+            lp[e * k + j] = (double)sl[(size_t)s.x * k + j];
+        }
+        ++e;
     }
     return SPINF_OK;
 }

@@ -105,19 +105,19 @@ namespace {
 
 // The descriptor arrays of one pass, in upload order, with their device pointers.
 struct DescriptorSet {
-    const std::vector<int32_t>* arrays[12];
-    int32_t** dst[12];
-    int n = 12;
-    size_t off[12];
+    const std::vector<int32_t>* arrays[15];
+    int32_t** dst[15];
+    int n = 15;
+    size_t off[15];
     size_t total = 0;
 };
 
 DescriptorSet descriptor_set(Pass& P) {
     DescriptorSet d{{&P.end, &P.pos, &P.tile_ptr, &P.tile_kv, &P.tile_len, &P.slot_row, &P.gather_m, &P.gather_tok,
-                     &P.row_gptr, &P.row_glist, &P.qt_work, &P.row_runs},
+                     &P.row_gptr, &P.row_glist, &P.qt_work, &P.row_runs, &P.row_x, &P.x_m, &P.x_set},
                     {&P.dev.end, &P.dev.pos, &P.dev.tile_ptr, &P.dev.tile_kv, &P.dev.tile_len, &P.dev.slot_row,
                      &P.dev.gather_m, &P.dev.gather_tok, &P.dev.row_gptr, &P.dev.row_glist, &P.dev.qt_work,
-                     &P.dev.row_runs}};
+                     &P.dev.row_runs, &P.dev.row_x, &P.dev.x_m, &P.dev.x_set}};
     for (int i = 0; i < d.n; ++i) {
         d.off[i] = d.total;
         d.total += (d.arrays[i]->size() * sizeof(int32_t) + 255) / 256 * 256;

@@ -15,6 +15,11 @@
 //                    an online (max, sum exp) over the tile in column order
 //   K3 combine       per row, merge the vocabulary chunks in ascending order ->
 //                    lse; token_lp = z_gathered - lse
+//   K5 extract       searched slots ({*} {n} {$}; PyPI page, "What it does":
+//                    the most likely answers with their probabilities): K2
+//                    keeps, per searched row and 256-token tile, the best k
+//                    allowed tokens; K5 merges the tiles' lists into the row's
+//                    top k (z descending, lower id first on ties), lp = z - lse
 //
 // Every reduction runs in a fixed order that depends only on the row's own
 // values and the vocabulary size, so a row's results do not depend on M or on
@@ -44,6 +49,7 @@ constexpr int kBBytes = kBN * 128;
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kScoreThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kTopCap = 16;   // largest extract_k
 
 enum { FULL0 = 0, EMPTY0 = kStages, ACC_FULL0 = 2 * kStages, ACC_EMPTY0 = 2 * kStages + 2, N_SBARS = 2 * kStages + 4 };
 
@@ -54,12 +60,14 @@ constexpr int kScoreSmem = kSmemHolder + 16 + 1024;
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct ScoreLayout {
-    int M, M_pad, G, n_vt, n_st;
-    size_t hs, sa, part, zg, total;
+    int M, M_pad, G, n_vt, n_st, X, k;
+    size_t hs, sa, part, zg, xpart, total;
 };
 
-ScoreLayout score_layout(const Pass& P, int vocab, int d_model, int w_dtype) {
+ScoreLayout score_layout(const Pass& P, int vocab, int d_model, int w_dtype, int extract_k) {
     ScoreLayout s;
+    s.X = (int)P.x_m.size();
+    s.k = extract_k;
     s.M = (int)P.slot_row.size();
     s.G = (int)P.gather_tok.size();
     s.M_pad = std::max(1, (s.M + kBM - 1) / kBM) * kBM;
@@ -70,7 +78,8 @@ ScoreLayout score_layout(const Pass& P, int vocab, int d_model, int w_dtype) {
     s.sa = s.hs + align256((size_t)s.M_pad * d_model * elt);
     s.part = s.sa + align256((size_t)s.M_pad * 4);
     s.zg = s.part + align256((size_t)s.M_pad * s.n_vt * 8);
-    s.total = s.zg + align256((size_t)std::max(s.G, 1) * 4);
+    s.xpart = s.zg + align256((size_t)std::max(s.G, 1) * 4);
+    s.total = s.xpart + align256((size_t)s.X * s.n_vt * s.k * 8);   // (z, token) per candidate
     return s;
 }
 
@@ -130,13 +139,47 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* _
 }
 
 // ---------------------------------------------------------------- K2
-template <bool FP8>
+// Searched rows (XT): a row's candidates of one tile, best first (z descending,
+// lower token first on ties; the tile is scanned in ascending token order, so a
+// new token goes after an equal one already held).
+struct TopList {
+    float z[kTopCap];
+    int t[kTopCap];
+};
+
+__device__ __forceinline__ void top_insert(TopList& L, float v, int tok) {
+    bool moved = false;
+#pragma unroll
+    for (int j = 0; j < kTopCap; ++j) {
+        const bool sw = moved || v > L.z[j];
+        const float z0 = L.z[j];
+        const int t0 = L.t[j];
+        if (sw) {
+            L.z[j] = v;
+            L.t[j] = tok;
+            v = z0;
+            tok = t0;
+        }
+        moved = sw;
+    }
+}
+
+struct ExtractArgs {
+    const int32_t* row_x;        // [M] searched slot of each scoring row, or -1
+    const int32_t* x_set;        // [X]
+    const uint32_t* token_sets;  // [n_sets][words]
+    int words;                   // ceil(V / 32)
+    int k;                       // candidates kept per tile (extract_k)
+    uint2* xpart;                // [X][n_vt][k] (z bits, token)
+};
+
+template <bool FP8, bool XT>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_main_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                       const float* __restrict__ s_act, const float* __restrict__ s_w, float2* __restrict__ part,
                       float* __restrict__ zg, const int32_t* __restrict__ row_gptr,
                       const int32_t* __restrict__ row_glist, const int32_t* __restrict__ gather_tok, int M, int V,
-                      int n_kb, int n_st, int n_vt, int* __restrict__ err) {
+                      int n_kb, int n_st, int n_vt, const ExtractArgs xa, int* __restrict__ err) {
     constexpr int kPerMma = FP8 ? 32 : 16;           // K elements of one MMA instruction
     constexpr int kMmaPerStage = (FP8 ? 128 : 64) / kPerMma;
     constexpr int kBK = FP8 ? 128 : 64;              // K elements per 128-byte row
@@ -241,6 +284,21 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 gc = lo;
             }
             const float sa = (FP8 && valid) ? s_act[m] : 1.f;
+            int xr = -1;
+            const uint32_t* allow = nullptr;
+            TopList top;
+            if constexpr (XT) {
+                xr = valid ? xa.row_x[m] : -1;
+                if (xr >= 0) {
+                    const int set = xa.x_set[xr];
+                    if (set >= 0) allow = xa.token_sets + (size_t)set * xa.words;
+#pragma unroll
+                    for (int j = 0; j < kTopCap; ++j) {
+                        top.z[j] = -INFINITY;
+                        top.t[j] = -1;
+                    }
+                }
+            }
             mbar_wait(&bars[ACC_FULL0 + acc], aph, err);
             tc_fence_after();
             float mx = -INFINITY, sum = 0.f;
@@ -264,6 +322,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 for (int i = 0; i < 32; ++i) add += fast_exp2((z[i] - nm) * kLog2e);
                 sum = (mx == -INFINITY ? 0.f : sum * fast_exp2((mx - nm) * kLog2e)) + add;
                 mx = nm;
+                if constexpr (XT) {
+                    if (xr >= 0 && vc < V) {
+                        const uint32_t bits = allow ? __ldg(allow + (vc >> 5)) : 0xffffffffu;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)   // z = -inf past the vocabulary: never inserted
+                            if (((bits >> i) & 1u) && z[i] > top.z[kTopCap - 1]) top_insert(top, z[i], vc + i);
+                    }
+                }
                 while (gc < ge) {
                     const int g = row_glist[gc];
                     const int tk = gather_tok[g];
@@ -279,6 +345,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             tc_fence_before();
             mbar_arrive(&bars[ACC_EMPTY0 + acc]);
             if (valid) part[(size_t)m * n_vt + vt] = make_float2(mx, sum);
+            if constexpr (XT) {
+                if (xr >= 0) {
+                    uint2* dst = xa.xpart + ((size_t)xr * n_vt + vt) * xa.k;
+#pragma unroll
+                    for (int j = 0; j < kTopCap; ++j)
+                        if (j < xa.k) dst[j] = make_uint2(__float_as_uint(top.z[j]), (uint32_t)top.t[j]);
+                }
+            }
         }
     }
 
@@ -324,9 +398,67 @@ __global__ void __launch_bounds__(128) score_combine_kernel(const float2* __rest
     }
 }
 
-template <bool FP8>
+// ---------------------------------------------------------------- K5
+// One warp per searched slot.  Each lane merges the lists of tiles lane, lane + 32,
+// ... (ascending, so an equal z from a later tile -- a higher token -- goes after);
+// then lane 0 takes the k best heads of the 32 lane lists, comparing z and, on
+// ties, the token id.  The result is the unique top k of the row under that order.
+__device__ __forceinline__ bool top_before(float za, int ta, float zb, int tb) {
+    return za > zb || (za == zb && ta >= 0 && (tb < 0 || ta < tb));
+}
+
+__global__ void __launch_bounds__(32) extract_combine_kernel(const uint2* __restrict__ xpart,
+                                                              const int32_t* __restrict__ x_m, int n_vt, int k,
+                                                              const float* __restrict__ row_lse,
+                                                              int32_t* __restrict__ top_tok,
+                                                              float* __restrict__ top_lp) {
+    __shared__ float sz[32][kTopCap + 1];
+    __shared__ int st[32][kTopCap + 1];
+    const int x = blockIdx.x, lane = threadIdx.x;
+    TopList L;
+#pragma unroll
+    for (int j = 0; j < kTopCap; ++j) {
+        L.z[j] = -INFINITY;
+        L.t[j] = -1;
+    }
+    for (int vt = lane; vt < n_vt; vt += 32) {
+        const uint2* src = xpart + ((size_t)x * n_vt + vt) * k;
+        for (int j = 0; j < k; ++j) {
+            const uint2 c = src[j];
+            const float z = __uint_as_float(c.x);
+            if (!(z > L.z[kTopCap - 1])) break;   // the tile's list is sorted: nothing better follows
+            top_insert(L, z, (int)c.y);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kTopCap; ++j) {
+        sz[lane][j] = L.z[j];
+        st[lane][j] = L.t[j];
+    }
+    sz[lane][kTopCap] = -INFINITY;   // list end
+    st[lane][kTopCap] = -1;
+    __syncwarp();
+    if (lane == 0) {
+        int head[32];
+        for (int l = 0; l < 32; ++l) head[l] = 0;
+        const float lse = row_lse[x_m[x]];
+        for (int j = 0; j < k; ++j) {
+            int best = 0;
+            for (int l = 1; l < 32; ++l)
+                if (top_before(sz[l][head[l]], st[l][head[l]], sz[best][head[best]], st[best][head[best]])) best = l;
+            const float z = sz[best][head[best]];
+            const int t = st[best][head[best]];
+            if (t >= 0 && head[best] < kTopCap) ++head[best];
+            top_tok[(size_t)x * k + j] = t;
+            top_lp[(size_t)x * k + j] = t >= 0 ? z - lse : -INFINITY;
+        }
+    }
+}
+
+template <bool FP8, bool XT>
 spinf_status launch_score(const Pass& P, const ScoreLayout& L, const void* hidden, const void* w, const float* w_scale,
-                          int D, int V, float* row_lse, float* token_lp, uint8_t* ws, int* err, cudaStream_t stream) {
+                          int D, int V, float* row_lse, float* token_lp, const spinf_extract_out* ex, uint8_t* ws,
+                          int* err, cudaStream_t stream) {
     void* hs = ws + L.hs;
     float* sa = reinterpret_cast<float*>(ws + L.sa);
     float2* part = reinterpret_cast<float2*>(ws + L.part);
@@ -349,7 +481,7 @@ spinf_status launch_score(const Pass& P, const ScoreLayout& L, const void* hidde
     if ((s = make_tmap(&tw, dt, 2, w, dw, st, bw, CU_TENSOR_MAP_SWIZZLE_128B))) return s;
     static bool configured = false;
     if (!configured) {
-        e = cudaFuncSetAttribute(score_main_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
+        e = cudaFuncSetAttribute(score_main_kernel<FP8, XT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(score)");
         configured = true;
     }
@@ -357,15 +489,23 @@ spinf_status launch_score(const Pass& P, const ScoreLayout& L, const void* hidde
     const int n_kb = (D + kbk - 1) / kbk;
     const int total = L.n_vt * L.n_st;
     const int grid = std::min(total, sm_count());
-    score_main_kernel<FP8><<<grid, kScoreThreads, kScoreSmem, stream>>>(
+    ExtractArgs xa{P.dev.row_x, P.dev.x_set, XT ? ex->token_sets : nullptr, (V + 31) / 32, L.k,
+                   reinterpret_cast<uint2*>(ws + L.xpart)};
+    score_main_kernel<FP8, XT><<<grid, kScoreThreads, kScoreSmem, stream>>>(
         th, tw, sa, w_scale, part, zg, P.dev.row_gptr, P.dev.row_glist, P.dev.gather_tok, L.M, V, n_kb, L.n_st,
-        L.n_vt, err);
+        L.n_vt, xa, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "score launch");
     score_combine_kernel<<<(L.M + 3) / 4, 128, 0, stream>>>(part, zg, P.dev.row_gptr, P.dev.row_glist, L.M, L.n_vt,
                                                            row_lse, token_lp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    if constexpr (XT) {
+        extract_combine_kernel<<<L.X, 32, 0, stream>>>(xa.xpart, P.dev.x_m, L.n_vt, L.k, row_lse, ex->top_tok,
+                                                       ex->top_lp);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "extract launch");
+    }
     return SPINF_OK;
 }
 
@@ -377,13 +517,13 @@ using namespace spinf;
 extern "C" size_t spinf_score_workspace_bytes(const spinf_plan* plan, int32_t pass, int32_t vocab, int32_t d_model,
                                               int32_t w_dtype) {
     if (!plan || pass < 0 || pass >= (int32_t)plan->passes.size() || vocab <= 0 || d_model <= 0) return 0;
-    return score_layout(plan->passes[pass], vocab, d_model, w_dtype).total;
+    return score_layout(plan->passes[pass], vocab, d_model, w_dtype, plan->extract_k).total;
 }
 
-extern "C" spinf_status spinf_score(const spinf_plan* plan, int32_t pass, const void* hidden, const void* w,
-                                    const float* w_scale, int32_t w_dtype, int32_t d_model, int32_t vocab,
-                                    float* row_lse, float* token_lp, void* workspace, size_t workspace_bytes,
-                                    spinf_stream stream) {
+extern "C" spinf_status spinf_score_extract(const spinf_plan* plan, int32_t pass, const void* hidden, const void* w,
+                                            const float* w_scale, int32_t w_dtype, int32_t d_model, int32_t vocab,
+                                            float* row_lse, float* token_lp, const spinf_extract_out* ex,
+                                            void* workspace, size_t workspace_bytes, spinf_stream stream) {
     spinf_status st = ensure_device_ready(plan, pass);
     if (st) return st;
     if (w_dtype != SPINF_DTYPE_BF16 && w_dtype != SPINF_DTYPE_E4M3) return fail(SPINF_E_UNSUPPORTED, "w_dtype");
@@ -397,13 +537,32 @@ extern "C" spinf_status spinf_score(const spinf_plan* plan, int32_t pass, const 
         if (reinterpret_cast<uintptr_t>(p) & 15) return fail(SPINF_E_INVALID, "buffer not 16-byte aligned");
     for (int32_t t : P.gather_tok)
         if (t < 0 || t >= vocab) return fail(SPINF_E_INVALID, "option token outside the vocabulary");
-    const ScoreLayout L = score_layout(P, vocab, d_model, w_dtype);
+    const ScoreLayout L = score_layout(P, vocab, d_model, w_dtype, plan->extract_k);
     if (workspace_bytes < L.total) return fail(SPINF_E_NOMEM, "workspace too small");
+    const bool xt = ex && L.X > 0;
+    if (xt) {
+        if (!ex->top_tok || !ex->top_lp) return fail(SPINF_E_INVALID, "NULL searched-slot outputs");
+        for (int32_t set : P.x_set)
+            if (set >= ex->n_sets) return fail(SPINF_E_INVALID, "a searched slot names an unknown token set");
+        for (int32_t set : P.x_set)
+            if (set >= 0 && !ex->token_sets) return fail(SPINF_E_INVALID, "token_sets is NULL");
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const float* wsc = w_dtype == SPINF_DTYPE_E4M3 ? w_scale : nullptr;
     if (w_dtype == SPINF_DTYPE_E4M3)
-        return launch_score<true>(P, L, hidden, w, w_scale, d_model, vocab, row_lse, token_lp, ws, plan->d_err, s);
-    return launch_score<false>(P, L, hidden, w, nullptr, d_model, vocab, row_lse, token_lp, ws, plan->d_err, s);
+        return xt ? launch_score<true, true>(P, L, hidden, w, wsc, d_model, vocab, row_lse, token_lp, ex, ws, plan->d_err, s)
+                  : launch_score<true, false>(P, L, hidden, w, wsc, d_model, vocab, row_lse, token_lp, ex, ws, plan->d_err, s);
+    return xt ? launch_score<false, true>(P, L, hidden, w, wsc, d_model, vocab, row_lse, token_lp, ex, ws, plan->d_err, s)
+              : launch_score<false, false>(P, L, hidden, w, wsc, d_model, vocab, row_lse, token_lp, ex, ws, plan->d_err, s);
+}
+
+extern "C" spinf_status spinf_score(const spinf_plan* plan, int32_t pass, const void* hidden, const void* w,
+                                    const float* w_scale, int32_t w_dtype, int32_t d_model, int32_t vocab,
+                                    float* row_lse, float* token_lp, void* workspace, size_t workspace_bytes,
+                                    spinf_stream stream) {
+    return spinf_score_extract(plan, pass, hidden, w, w_scale, w_dtype, d_model, vocab, row_lse, token_lp, nullptr,
+                               workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------- allocation-free variant
@@ -450,7 +609,7 @@ extern "C" spinf_status spinf_score_static(const spinf_plan* plan, int32_t pass,
     if (vocab <= 0) return fail(SPINF_E_INVALID, "vocab must be positive");
     const Pass& P = plan->passes[pass];
     if (P.slot_row.empty()) return SPINF_OK;
-    const ScoreLayout L = score_layout(P, vocab, d_model, w_dtype);
+    const ScoreLayout L = score_layout(P, vocab, d_model, w_dtype, plan->extract_k);
     if (L.total > (size_t)SPINF_SCORE_STATIC_SCRATCH_BYTES)
         return fail(SPINF_E_LIMIT, "this pass needs " + std::to_string(L.total) +
                                        " bytes of scoring scratch; the static area holds " +
@@ -467,6 +626,8 @@ extern "C" spinf_status spinf_score_static(const spinf_plan* plan, int32_t pass,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(scratch);
     if (w_dtype == SPINF_DTYPE_E4M3)
-        return launch_score<true>(P, L, hidden, w, w_scale, d_model, vocab, row_lse, token_lp, ws, plan->d_err, s);
-    return launch_score<false>(P, L, hidden, w, nullptr, d_model, vocab, row_lse, token_lp, ws, plan->d_err, s);
+        return launch_score<true, false>(P, L, hidden, w, w_scale, d_model, vocab, row_lse, token_lp, nullptr, ws,
+                                         plan->d_err, s);
+    return launch_score<false, false>(P, L, hidden, w, nullptr, d_model, vocab, row_lse, token_lp, nullptr, ws,
+                                      plan->d_err, s);
 }

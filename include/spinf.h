@@ -17,7 +17,10 @@
  *   spinf_branch_attention  device: tree-masked GQA attention over the pass
  *   spinf_score             device: lm-head at slot rows, full-vocabulary
  *                           log-sum-exp, option-token log-probabilities
+ *                           (spinf_score_extract: also the top tokens of
+ *                           searched slots, in the same read of the lm head)
  *   spinf_collect           host: per option lp, p, residual and floor
+ *                           (spinf_collect_extract: searched-slot answers)
  *
  * Conventions for every call:
  *   - Status codes only; nothing throws across this boundary.  The text of the
@@ -59,19 +62,31 @@ typedef enum {
 
 enum { SPINF_DTYPE_BF16 = 0, SPINF_DTYPE_E4M3 = 1 };
 
+/* Question kinds ("spinf-serve 0.1.1" PyPI page, "What it does"; man page,
+ * DESCRIPTION): a scored template ends in {?} and carries options; a searched
+ * slot ({*} text, {n} numbers, {$} amounts) carries none and returns the most
+ * likely next tokens with their probabilities. */
+enum { SPINF_Q_SCORED = 0, SPINF_Q_SEARCHED = 1 };
+
 /* A token-id array (host memory). */
 typedef struct {
     const int32_t* ids;
     int32_t n;
 } spinf_tokens;
 
-/* One scored question: template tokens up to and including the last token
- * before the {?} slot, and the options to score there (1 to max_option_tokens
- * tokens each; no duplicates). */
+/* One question: template tokens up to and including the last token before the
+ * slot.  kind SPINF_Q_SCORED (0, so a zeroed struct is a scored question): the
+ * options to score at the slot (1 to max_option_tokens tokens each; no
+ * duplicates).  kind SPINF_Q_SEARCHED: no options (n_options 0); the slot
+ * returns its extract_k most likely tokens among the allowed-token set number
+ * token_set given at scoring time (-1: every token).  Decoding a longer answer
+ * appends the chosen tokens to the template and plans again. */
 typedef struct {
     spinf_tokens tmpl;
     const spinf_tokens* options;
     int32_t n_options;
+    int32_t kind;
+    int32_t token_set;
 } spinf_question;
 
 /* One input: a content (may be empty) read once, and its questions. */
@@ -98,6 +113,7 @@ typedef struct {
     int32_t floors;                 /* 1: add one floor input per distinct (template, options) */
     spinf_tokens floor_prefix;      /* content of every floor input (default: empty) */
     int32_t vocab;                  /* > 0: reject token ids outside [0, vocab) */
+    int32_t extract_k;              /* tokens returned per searched slot, 1..16 (default 8) */
 } spinf_plan_opts;
 
 typedef struct spinf_plan spinf_plan;
@@ -127,6 +143,9 @@ typedef struct {
     const int32_t* row_runs;  /* [T_pad][8] each row's visible keys (its root path) as up to four
                                  runs [lo, hi) of consecutive rows, nearest first, unused runs
                                  (0, 0); lo of the first run is -1 when the path has more runs */
+    int32_t X;                /* searched slots of the pass */
+    const int32_t* x_m;       /* [X] scoring-row index of each searched slot, in layout order */
+    const int32_t* x_set;     /* [X] its allowed-token set (-1: every token) */
 } spinf_pass_info;
 
 /* Per-option and per-question results, caller-owned host arrays (fp64).
@@ -158,9 +177,14 @@ void spinf_plan_opts_default(spinf_plan_opts* opts);
  * visible to some row of the tile; a tile's keys beyond its input's last row
  * (tile_len) are not part of it, they are seen through their own input's tiles.
  *
+ * A searched slot lays out its template rows only; its last template row is a
+ * scoring row; it gets no floor.
+ *
  * inputs: host array of n_inputs (n_inputs >= 0); opts: NULL for defaults.
  * On success *out owns a new plan.  Errors: SPINF_E_INVALID (empty template,
- * empty or duplicate option, token id out of range, empty input),
+ * empty or duplicate option, token id out of range, empty input, a scored
+ * question without options, a searched slot with options or token_set < -1,
+ * extract_k outside 1..16, an unknown kind),
  * SPINF_E_LIMIT (a limit exceeded, or a content and one question do not fit a
  * pass), SPINF_E_NOMEM. */
 spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inputs,
@@ -183,6 +207,10 @@ spinf_status spinf_plan_window_schedule(const spinf_plan* plan, int32_t pass, in
 
 /* Number of user questions and options over the whole request (sizes of spinf_result). */
 spinf_status spinf_plan_counts(const spinf_plan* plan, int64_t* n_questions, int64_t* n_options);
+
+/* Number of searched slots over the whole request and the plan's extract_k
+ * (spinf_collect_extract writes n_extract x extract_k answers). */
+spinf_status spinf_plan_extract_counts(const spinf_plan* plan, int64_t* n_extract, int32_t* extract_k);
 
 /* Copy pass `pass`'s descriptors to the current device (allocated once per pass
  * and kept by the plan; later calls are no-ops).  The allocation is synchronous;
@@ -253,6 +281,33 @@ spinf_status spinf_score(const spinf_plan* plan, int32_t pass,
                          float* row_lse, float* token_lp,
                          void* workspace, size_t workspace_bytes, spinf_stream stream);
 
+/* Device buffers of the searched-slot answers of one pass. */
+typedef struct {
+    const uint32_t* token_sets;  /* device [n_sets][ceil(vocab / 32)]: bit (v % 32) of word v / 32 set
+                                    means token v is allowed; may be NULL when n_sets is 0 */
+    int32_t n_sets;              /* every x_set of the pass must be < n_sets */
+    int32_t* top_tok;            /* device [X][extract_k]: tokens, most likely first (ties: lower id
+                                    first); -1 past the end of a set with fewer allowed tokens */
+    float* top_lp;               /* device [X][extract_k]: z - row_lse of each token (-inf past the end) */
+} spinf_extract_out;
+
+/* spinf_score plus the searched slots of the pass, read from the same pass over
+ * the lm head ("spinf-serve 0.1.1", "What it does": extraction rides the same
+ * read; the most likely answers with their probabilities).  For searched slot x
+ * (scoring row x_m[x]) the extract_k allowed tokens with the largest z, in
+ * descending z and ascending id on ties, and their z - row_lse.  Each CTA of the
+ * lm-head kernel keeps the best extract_k of its 256-token tile per searched row;
+ * a merge kernel orders the tiles' candidates.  The answer is a function of the
+ * row's own values only.  ex NULL, or a pass without searched slots: exactly
+ * spinf_score.  Workspace: spinf_score_workspace_bytes (it includes the
+ * candidates).  Errors: those of spinf_score, and SPINF_E_INVALID for NULL
+ * outputs, an x_set >= n_sets or NULL token_sets when a set is named. */
+spinf_status spinf_score_extract(const spinf_plan* plan, int32_t pass,
+                                 const void* hidden, const void* w, const float* w_scale, int32_t w_dtype,
+                                 int32_t d_model, int32_t vocab,
+                                 float* row_lse, float* token_lp, const spinf_extract_out* ex,
+                                 void* workspace, size_t workspace_bytes, spinf_stream stream);
+
 /* Size of the device scratch area behind spinf_score_static: 64 MiB, reserved on
  * every GPU that loads this library, for as long as the process runs. */
 #define SPINF_SCORE_STATIC_SCRATCH_BYTES (64u << 20)
@@ -289,6 +344,14 @@ spinf_status spinf_score_static(const spinf_plan* plan, int32_t pass,
  * ("spinf-serve" news repost, English part: the refund example's response). */
 spinf_status spinf_collect(const spinf_plan* plan, const float* const* token_lp_per_pass,
                            const spinf_result* out);
+
+/* Searched-slot answers in question order (input by input, question by question,
+ * searched slots only), from each pass's top_tok / top_lp copied to the host:
+ * tok [n_extract][extract_k] and lp [n_extract][extract_k] (fp64 copies).  The
+ * per-option fields of spinf_collect are absent for a searched slot, and its
+ * residual and floor_residual are NaN.  SPINF_E_INVALID for NULL arrays. */
+spinf_status spinf_collect_extract(const spinf_plan* plan, const int32_t* const* top_tok_per_pass,
+                                   const float* const* top_lp_per_pass, int32_t* tok, double* lp);
 
 /* Wait for `stream`, then report the plan's device error word:
  * SPINF_OK, SPINF_E_DEVICE_TIMEOUT or SPINF_E_DEVICE_CHECK (the word is cleared). */

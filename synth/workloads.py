@@ -130,6 +130,25 @@ def invariance_packing(packing_seed, seed=0, vocab=262144, n_short=2000):
     return shorts[:idx] + [target] + shorts[idx:], idx
 
 
+def with_searched_slots(inputs, n, seed=0, vocab=262144, n_sets=2):
+    """Every input gets the same ``n`` searched slots appended to its questions:
+    templates of U[8, 16] tokens, token sets cycling -1 (any token), 0, 1, ...,
+    ``n_sets - 1`` (a question is then ``(template, None, token_set)``)."""
+    g = _rng(seed + 3000)
+    slots = [(_ids(g, int(g.integers(8, 17)), vocab), None, (i % (n_sets + 1)) - 1) for i in range(n)]
+    return [(content, list(questions) + slots) for content, questions in inputs]
+
+
+def token_sets(vocab, n_sets=2, density=0.01, seed=0):
+    """Allowed-token sets of searched slots (stand-ins for a tokenizer's digit and
+    amount tokens): ``[n_sets, vocab]`` booleans, each a seeded random ``density``
+    fraction of the vocabulary, plus the last token (the ragged end of the vocabulary)."""
+    g = _rng(seed + 4000)
+    out = g.random((n_sets, vocab)) < density
+    out[:, vocab - 1] = True
+    return out
+
+
 WORKLOADS = {
     "tiny": (tiny, TINY),
     "wikinews": (wikinews, GEMMA),

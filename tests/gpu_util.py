@@ -45,3 +45,34 @@ def oracle_plan(inputs, **kw):
 
 def real_rows(lay):
     return np.arange(lay.T)
+
+
+def pack_token_sets(sets):
+    """Boolean ``[n_sets, V]`` allowed-token sets as the ABI's bitmasks: int32
+    ``[n_sets, ceil(V / 32)]``, bit ``v % 32`` of word ``v // 32`` for token ``v``."""
+    sets = np.asarray(sets, dtype=bool)
+    n, V = sets.shape
+    padded = np.zeros((n, -(-V // 32) * 32), dtype=bool)
+    padded[:, :V] = sets
+    words = np.packbits(padded.reshape(n, -1, 8), axis=2, bitorder="little").reshape(n, -1).view("<u4")
+    return torch.from_numpy(words.view(np.int32).copy())
+
+
+def run_score_extract(spinf, plan, p, hidden, w, w_scale, w_dtype, shape, sets=None, k=None):
+    """spinf_score_extract on one pass: (lse, token lps, top tokens [X, k], top lps [X, k])."""
+    info = plan.pass_info(p)
+    k = k if k is not None else plan.extract_counts()[1]
+    plan.upload(p)
+    nbytes = spinf.score_workspace_bytes(plan, p, shape.vocab, shape.d_model, w_dtype)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    lse = torch.full((max(info.M, 1),), float("nan"), device="cuda")
+    tlp = torch.full((max(info.G, 1),), float("nan"), device="cuda")
+    top_tok = torch.full((max(info.X, 1), k), -7, dtype=torch.int32, device="cuda")
+    top_lp = torch.full((max(info.X, 1), k), float("nan"), device="cuda")
+    ex = {"top_tok": top_tok, "top_lp": top_lp,
+          "token_sets": None if sets is None else pack_token_sets(sets).cuda()}
+    spinf.score(plan, p, hidden, w, w_scale, w_dtype, shape.d_model, shape.vocab, lse, tlp, ws, extract=ex)
+    plan.device_status()
+    torch.cuda.synchronize()
+    return (lse[:info.M].cpu().numpy(), tlp[:info.G].cpu().numpy(), top_tok[:info.X].cpu().numpy(),
+            top_lp[:info.X].cpu().numpy())

@@ -11,7 +11,7 @@ from oracle import plan as op
 from synth import workloads as wl
 
 FIELDS = ("tok", "parent", "pos", "end", "anchor", "tile_ptr", "tile_kv", "tile_len", "slot_row", "gather_m",
-          "gather_tok")
+          "gather_tok", "x_m", "x_set")
 
 
 def _compare(spinf, inputs, **opts):
@@ -108,6 +108,9 @@ def test_fuzzed_requests(spinf):
     [([1], [([1], [[i] for i in range(1001)])])],
     [([1], [([1], [[2] * 6])])],
     [([1], [([1], [[2000]])])],
+    [([1], [([1], None, -2)])],
+    [([1], [([], None, 0)])],
+    [([1], [([2000], None, 0)])],
 ])
 def test_error_statuses_match(spinf, bad):
     with pytest.raises(op.PlanError) as e:
@@ -224,3 +227,73 @@ def test_window_schedule_is_exact(spinf, window):
         assert list(zip(tk.tolist(), tl.tolist())) == want_kv
         if window >= 100000:   # a window that never bites keeps every tile
             assert np.array_equal(tk, lay.tile_kv) and np.array_equal(tl, lay.tile_len)
+
+
+def _searched_request(g, n_inputs, vocab=60):
+    """Inputs mixing scored questions and searched slots (token sets -1..3)."""
+    inputs = []
+    for _ in range(n_inputs):
+        content = g.integers(0, vocab, size=int(g.integers(0, 200))).tolist()
+        qs = []
+        for _ in range(int(g.integers(0 if content else 1, 7))):
+            template = g.integers(0, vocab, size=int(g.integers(1, 15))).tolist()
+            if g.random() < 0.4:
+                qs.append((template, None, int(g.integers(-1, 4))))
+                continue
+            opts, seen = [], set()
+            for _ in range(int(g.integers(1, 4))):
+                o = tuple(g.integers(0, 6, size=int(g.integers(1, 3))).tolist())
+                if o not in seen:
+                    seen.add(o)
+                    opts.append(list(o))
+            qs.append((template, opts))
+        if not content and not qs:
+            content = [1]
+        inputs.append((content, qs))
+    return inputs
+
+
+@pytest.mark.parametrize("budget", [128, 400, 16384])
+def test_searched_slots_bit_exact(spinf, budget):
+    g = np.random.default_rng(budget)
+    for trial in range(12):
+        inputs = _searched_request(g, int(g.integers(1, 10)))
+        k = int(g.integers(1, 17))
+        try:
+            op.plan(inputs, token_budget=budget, extract_k=k)
+        except op.PlanError as e:
+            with pytest.raises(spinf.SpinfError) as ee:
+                spinf.Plan(inputs, token_budget=budget, extract_k=k)
+            assert ee.value.status_name == e.status
+            continue
+        P, Q = _compare(spinf, inputs, token_budget=budget, extract_k=k)
+        n_x = sum(sum(row) for row in P.searched)
+        assert Q.extract_counts() == (n_x, k)
+        assert Q.counts()[0] == sum(P.n_questions)
+
+
+@pytest.mark.parametrize("k", [0, 17])
+def test_extract_k_range(spinf, k):
+    with pytest.raises(op.PlanError):
+        op.plan([([1], [([2], None, -1)])], extract_k=k)
+    with pytest.raises(spinf.SpinfError) as ee:
+        spinf.Plan([([1], [([2], None, -1)])], extract_k=k)
+    assert ee.value.status_name == "INVALID"
+
+
+def test_collect_extract_matches_oracle(spinf):
+    g = np.random.default_rng(11)
+    inputs = _searched_request(g, 9)
+    P, Q = _compare(spinf, inputs, token_budget=300, extract_k=5)
+    toks = [g.integers(-1, 60, size=(len(lay.x_m), 5)).astype(np.int32) for lay in P.passes]
+    lps = [(-g.random((len(lay.x_m), 5)) * 9).astype(np.float32) for lay in P.passes]
+    tok, lp = Q.collect_extract(toks, lps)
+    ref = oc.collect_extract(P, toks, lps)
+    assert tok.shape == (len(ref), 5)
+    for i, (t, l) in enumerate(ref):
+        assert tok[i].tolist() == t.tolist()
+        np.testing.assert_array_equal(lp[i], l)
+    tlps = [(-g.random(len(lay.gather_tok)) * 5).astype(np.float32) for lay in P.passes]
+    ours = Q.collect(tlps)
+    flat_res = [np.nan if r is None else r["residual"] for per_q in oc.collect(P, tlps) for r in per_q]
+    np.testing.assert_allclose(ours["residual"], flat_res, rtol=0, atol=1e-12)
