@@ -16,6 +16,8 @@ What it restates, page by page:
   ``--max-prompts-per-input`` 10000, ``--max-options`` 1000,
   ``--max-option-tokens`` 5, ``--max-tokens`` (largest single input).
 * same page, CAVEATS: long inputs run alone.
+* same page, "What it does": placeholders turn one template into a grid of
+  questions.
 * "spinf-serve 0.1.1" (PyPI), "What it does" and the man page's DESCRIPTION:
   extraction slots (``{*}`` text, ``{n}`` numbers, ``{$}`` amounts) ride the
   same read; the engine returns the most likely answers with their
@@ -46,8 +48,17 @@ Readings where the pages are silent (each is listed in the design notes):
    chosen tokens to the template and plan again.  A searched slot gets no
    floor (the pages give the floor for scored questions only).
 
+8. A grid is a template written as literal segments around placeholders, each
+   placeholder with a list of values (token sequences).  It stands for one
+   question per combination of values, the first placeholder varying slowest;
+   every cell is an ordinary question with the grid's options (or a searched
+   slot).  An input's grid cells follow its own questions, grid by grid, and
+   count toward ``max_prompts_per_input``.
+
 A question is ``(template, options)`` (scored) or ``(template, None, token_set)``
-(a searched slot).
+(a searched slot).  A grid is ``(segments, values, options)`` or
+``(segments, values, None, token_set)``.  An input is ``(content, questions)``
+or ``(content, questions, grids)``.
 
 The visible-key set of a row is kept in its plainest form: the content rows of
 its own input up to itself (content rows) or all of them (branch rows), plus
@@ -56,6 +67,7 @@ KV-tile schedule) is derived from that set by its definition.
 """
 from __future__ import annotations
 
+import itertools
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -113,6 +125,47 @@ def trie_nodes(options):
             walk(child, p)
 
     walk(root, ())
+    return out
+
+
+def expand_grid(grid):
+    """The questions of one grid, first placeholder slowest (reading 8)."""
+    segments, values = grid[0], grid[1]
+    cells = []
+    for combo in itertools.product(*values):
+        template = list(segments[0])
+        for value, seg in zip(combo, segments[1:]):
+            template += list(value) + list(seg)
+        cells.append((template, None, grid[3]) if grid[2] is None else (template, grid[2]))
+    return cells
+
+
+def grid_size(grid):
+    """Number of cells of a grid, without expanding it."""
+    n = 1
+    for v in grid[1]:
+        n *= len(v)
+    return n
+
+
+def _expand_inputs(inputs, o):
+    """Inputs with their grids expanded into trailing questions: ``(content, questions)``."""
+    out = []
+    for i, inp in enumerate(inputs):
+        content, questions = inp[0], list(inp[1])
+        grids = inp[2] if len(inp) > 2 else ()
+        total = len(questions)
+        for grid in grids:
+            if len(grid[0]) != len(grid[1]) + 1:
+                raise PlanError("INVALID", f"input {i}: a grid needs one more segment than placeholders")
+            if any(len(v) == 0 for v in grid[1]):
+                raise PlanError("INVALID", f"input {i}: a grid placeholder without values")
+            total += grid_size(grid)
+            if total > o["max_prompts_per_input"]:
+                raise PlanError("LIMIT", f"input {i}: more questions than max_prompts_per_input")
+        for grid in grids:
+            questions += expand_grid(grid)
+        out.append((content, questions))
     return out
 
 
@@ -440,9 +493,11 @@ def _layout_pass(units):
 def plan(inputs, **opts) -> Plan:
     """Lay ``inputs`` out in packed passes.
 
-    ``inputs`` is a list of ``(content_ids, [question, ...])``, a question being
+    ``inputs`` is a list of ``(content_ids, [question, ...])`` or
+    ``(content_ids, [question, ...], [grid, ...])``, a question being
     ``(template_ids, [option_ids, ...])`` or, for a searched slot,
-    ``(template_ids, None, token_set)``.
+    ``(template_ids, None, token_set)``, and a grid
+    ``(segments, values, options)`` or ``(segments, values, None, token_set)``.
     Options are keyword arguments named as in :data:`DEFAULTS`.
     """
     o = dict(DEFAULTS)
@@ -450,6 +505,7 @@ def plan(inputs, **opts) -> Plan:
     if unknown:
         raise TypeError(f"unknown options {sorted(unknown)}")
     o.update(opts)
+    inputs = _expand_inputs(inputs, o)
     _validate(inputs, o)
     units = _units(inputs, o)
     passes = [_layout_pass(us) for us in _pack(units, o["token_budget"])]
