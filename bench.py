@@ -260,6 +260,9 @@ def run_ours(args, rank, world):
         plan.device_status(stream)
         attn_win_ms = statistics.mean(a.elapsed_time(b) for a, b in wev) * len(passes)
 
+    extract = None if args.no_extract else extract_timing(args, spinf, sv, wl, inputs, shape, w, w_scale, w_dtype,
+                                                          dev, stream)
+
     # end to end through the public API with host buffers
     e2e = run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev) if not args.no_e2e else None
 
@@ -309,6 +312,7 @@ def run_ours(args, rank, world):
                        "user_questions": questions, "packed_tokens": tokens},
         "kernel_ms_per_step": {"attention": attn_ms, "score": score_ms,
                                **({"attention_windowed": attn_win_ms, "window": shape.window} if attn_win_ms else {})},
+        "searched_slots": extract,
         "clocks": clk,
         "gpu_launches": 4 * len(passes) * args.steps,
         "e2e": e2e,
@@ -316,6 +320,58 @@ def run_ours(args, rank, world):
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args, inputs, shape, plan, passes, w, w_scale, budget_s=args.cpu_seconds)
     return out
+
+
+def extract_timing(args, spinf, sv, wl, inputs, shape, w, w_scale, w_dtype, dev, stream, n_slots=2):
+    """Scoring with searched slots: every input also gets ``n_slots`` searched slots ({*} over
+    any token, {n} over a 1% token set).  Times the scoring call of the same plan with and
+    without the searched-slot answers (outside the step)."""
+    import numpy as np
+    import torch
+
+    inputs_x = wl.with_searched_slots(inputs, n_slots, vocab=shape.vocab, n_sets=1)
+    plan = spinf.Plan(inputs_x, vocab=shape.vocab)
+    sets = wl.token_sets(shape.vocab, n_sets=1)
+    words = np.zeros((1, -(-shape.vocab // 32) * 32), dtype=bool)
+    words[:, :shape.vocab] = sets
+    packed = np.packbits(words.reshape(1, -1, 8), axis=2, bitorder="little").reshape(1, -1).view(np.int32)
+    sets_dev = torch.from_numpy(packed.copy()).to(dev)
+    k = plan.extract_counts()[1]
+    bufs = []
+    with torch.cuda.stream(stream):
+        for p in range(plan.num_passes):
+            info = plan.pass_info(p)
+            keys = sv.path_keys(info.tok, info.parent, info.T)
+            h = sv.hidden(keys, info.T_pad, shape.d_model, rows=info.slot_row.tolist()).to(dev)
+            plan.upload(p, stream)
+            nb = spinf.score_workspace_bytes(plan, p, shape.vocab, shape.d_model, w_dtype)
+            bufs.append({"h": h, "ws": torch.empty(nb, dtype=torch.uint8, device=dev),
+                         "lse": torch.empty(max(info.M, 1), device=dev), "tlp": torch.empty(max(info.G, 1), device=dev),
+                         "ex": {"token_sets": sets_dev,
+                                "top_tok": torch.empty((max(info.X, 1), k), dtype=torch.int32, device=dev),
+                                "top_lp": torch.empty((max(info.X, 1), k), device=dev)}})
+    stream.synchronize()
+
+    def run(with_x):
+        evs = []
+        for _ in range(max(3, args.steps // 2)):
+            for p, b in enumerate(bufs):
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+                spinf.score(plan, p, b["h"], w, w_scale, w_dtype, shape.d_model, shape.vocab, b["lse"], b["tlp"],
+                            b["ws"], stream=stream, extract=b["ex"] if with_x else None)
+                a1.record(stream)
+                evs.append((a0, a1))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in evs) * len(bufs)
+
+    run(True)
+    ms_plain, ms_x = run(False), run(True)
+    plan.device_status(stream)
+    n_x = plan.extract_counts()[0]
+    return {"workload": f"every input + {n_slots} searched slots ({{*}} any token, {{n}} 1% token set), k={k}",
+            "slots": n_x, "score_ms_plain": ms_plain, "score_ms_with_answers": ms_x,
+            "overhead_ms": ms_x - ms_plain, "slots_per_s": n_x / (ms_x * 1e-3)}
 
 
 def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
@@ -594,6 +650,7 @@ def main():
     ap.add_argument("--fp8", action="store_true", help="e4m3 lm head with per-row scales")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extract", action="store_true", help="skip the searched-slot scoring timing")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--ncu-case", choices=["score", "attention"], default=None,
                     help="run one boundary call on pass 0 only (small case for profiler captures)")

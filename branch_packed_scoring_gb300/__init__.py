@@ -85,7 +85,10 @@ _TOK = np.dtype([("ids", "<u8"), ("n", "<i4"), ("_pad", "<i4")])
 _QUE = np.dtype([("tmpl_ids", "<u8"), ("tmpl_n", "<i4"), ("_p0", "<i4"), ("options", "<u8"),
                  ("n_options", "<i4"), ("kind", "<i4"), ("token_set", "<i4"), ("_p1", "<i4")])
 _INP = np.dtype([("content_ids", "<u8"), ("content_n", "<i4"), ("_p0", "<i4"), ("questions", "<u8"),
-                 ("n_questions", "<i4"), ("_p1", "<i4")])
+                 ("n_questions", "<i4"), ("_p1", "<i4"), ("grids", "<u8"), ("n_grids", "<i4"), ("_p2", "<i4")])
+_GRID = np.dtype([("segments", "<u8"), ("n_placeholders", "<i4"), ("_p0", "<i4"), ("values", "<u8"),
+                  ("n_values", "<u8"), ("options", "<u8"), ("n_options", "<i4"), ("kind", "<i4"),
+                  ("token_set", "<i4"), ("_p1", "<i4")])
 
 _lib = None
 
@@ -206,8 +209,11 @@ def _marshal(inputs):
     """Lay the request out as the header's structs in numpy buffers (kept alive by the caller)."""
     ids, c_off, c_n, nq, t_off, t_n, no, o_off, o_n = [], [], [], [], [], [], [], [], []
     kind, tset = [], []
+    grids = []   # (input, grid)
     pos = 0
-    for content, questions in inputs:
+    for inp in inputs:
+        content, questions = inp[0], inp[1]
+        grids.extend((len(nq), g) for g in (inp[2] if len(inp) > 2 else ()))
         c_off.append(pos)
         c_n.append(len(content))
         ids.extend(content)
@@ -255,7 +261,63 @@ def _marshal(inputs):
         inp["questions"] = np.where(np.asarray(nq) > 0, np.uint64(que.ctypes.data) +
                                     np.uint64(_QUE.itemsize) * first_q, np.uint64(0))
         inp["n_questions"] = nq
-    return inp, (flat, que, tok)
+    keep = [flat, que, tok]
+    if grids:
+        _marshal_grids(inp, grids, keep)
+    return inp, tuple(keep)
+
+
+def _marshal_grids(inp, grids, keep):
+    """The inputs' placeholder grids as ``spinf_grid`` arrays (segments, values, options,
+    value counts), pointed to from ``inp``; every buffer is appended to ``keep``."""
+    ids, spans = [], []   # spans: (offset, n) of every token array, in the order used below
+
+    def span(seq):
+        spans.append((len(ids), len(seq)))
+        ids.extend(int(t) for t in seq)
+
+    meta = []
+    for _, g in grids:
+        segments, values, options = g[0], g[1], g[2]
+        if len(segments) != len(values) + 1:
+            raise ValueError("a grid needs one more segment than placeholders")
+        s0 = len(spans)
+        for seg in segments:
+            span(seg)
+        v0 = len(spans)
+        for vals in values:
+            for v in vals:
+                span(v)
+        o0 = len(spans)
+        for opt in (options or ()):
+            span(opt)
+        meta.append((s0, v0, o0, [len(v) for v in values]))
+    flat = np.array(ids, dtype=np.int32) if ids else np.zeros(1, dtype=np.int32)
+    tok = np.zeros(max(len(spans), 1), dtype=_TOK)
+    for i, (off, n) in enumerate(spans):
+        tok[i]["ids"] = flat.ctypes.data + 4 * off if n else 0
+        tok[i]["n"] = n
+    counts = np.array([c for m in meta for c in m[3]] or [0], dtype=np.int32)
+    arr = np.zeros(len(grids), dtype=_GRID)
+    tb, isz, c0 = tok.ctypes.data, _TOK.itemsize, 0
+    for j, ((_, g), (s0, v0, o0, nv)) in enumerate(zip(grids, meta)):
+        searched = g[2] is None
+        arr[j]["segments"] = tb + isz * s0
+        arr[j]["n_placeholders"] = len(nv)
+        arr[j]["values"] = tb + isz * v0 if nv else 0
+        arr[j]["n_values"] = counts.ctypes.data + 4 * c0 if nv else 0
+        arr[j]["options"] = 0 if searched else tb + isz * o0
+        arr[j]["n_options"] = 0 if searched else len(g[2])
+        arr[j]["kind"] = Q_SEARCHED if searched else Q_SCORED
+        arr[j]["token_set"] = int(g[3]) if searched else -1
+        c0 += len(nv)
+    first = {}
+    for j, (i, _) in enumerate(grids):
+        first.setdefault(i, j)
+        inp[i]["n_grids"] += 1
+    for i, j in first.items():
+        inp[i]["grids"] = arr.ctypes.data + _GRID.itemsize * j
+    keep += [flat, tok, counts, arr]
 
 
 class Request:

@@ -16,6 +16,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <deque>
 #include <memory>
 #include <new>
 #include <string>
@@ -109,6 +110,77 @@ struct Unit {
     std::vector<int32_t> qidx;            // flat user-question index (floors: floor index)
     int64_t size;
 };
+
+// Grid cells as ordinary questions, appended after each input's own questions
+// (first placeholder slowest).  The expanded inputs point into `store`.
+struct Expanded {
+    std::vector<spinf_input> inputs;
+    std::vector<std::vector<spinf_question>> questions;
+    std::deque<std::vector<int32_t>> templates;
+};
+
+spinf_status expand_grids(const spinf_input* inputs, int32_t n_inputs, const spinf_plan_opts& o, Expanded& x) {
+    x.inputs.assign(inputs, inputs + n_inputs);
+    x.questions.resize(n_inputs);
+    for (int32_t i = 0; i < n_inputs; ++i) {
+        const spinf_input& in = inputs[i];
+        const std::string where = "input " + std::to_string(i);
+        if (in.n_grids < 0 || (in.n_grids > 0 && !in.grids)) return fail(SPINF_E_INVALID, where + ": bad grid array");
+        if (in.n_questions < 0 || (in.n_questions > 0 && !in.questions))
+            return fail(SPINF_E_INVALID, where + ": bad arrays");
+        int64_t total = in.n_questions;
+        for (int32_t gi = 0; gi < in.n_grids; ++gi) {
+            const spinf_grid& g = in.grids[gi];
+            if (g.n_placeholders < 0 || !g.segments || (g.n_placeholders > 0 && (!g.values || !g.n_values)))
+                return fail(SPINF_E_INVALID, where + ": bad grid");
+            int64_t cells = 1;
+            for (int32_t p = 0; p < g.n_placeholders; ++p) {
+                if (g.n_values[p] < 1) return fail(SPINF_E_INVALID, where + ": a grid placeholder without values");
+                cells = std::min<int64_t>(cells * g.n_values[p], (int64_t)1 << 40);
+            }
+            total += cells;
+            if (total > o.max_prompts_per_input)
+                return fail(SPINF_E_LIMIT, where + ": more questions than max_prompts_per_input");
+        }
+        if (in.n_grids == 0) continue;
+        std::vector<spinf_question>& qs = x.questions[i];
+        qs.assign(in.questions, in.questions + in.n_questions);
+        for (int32_t gi = 0; gi < in.n_grids; ++gi) {
+            const spinf_grid& g = in.grids[gi];
+            std::vector<int32_t> first(g.n_placeholders + 1, 0);   // first value of each placeholder
+            for (int32_t p = 0; p < g.n_placeholders; ++p) first[p + 1] = first[p] + g.n_values[p];
+            std::vector<int32_t> pick(g.n_placeholders, 0);          // odometer, last placeholder fastest
+            for (;;) {
+                std::vector<int32_t> t;
+                auto put = [&](const spinf_tokens& s) {
+                    if (s.n > 0 && s.ids) t.insert(t.end(), s.ids, s.ids + s.n);
+                };
+                put(g.segments[0]);
+                for (int32_t p = 0; p < g.n_placeholders; ++p) {
+                    put(g.values[first[p] + pick[p]]);
+                    put(g.segments[p + 1]);
+                }
+                x.templates.push_back(std::move(t));
+                spinf_question q{};
+                q.tmpl.ids = x.templates.back().data();
+                q.tmpl.n = (int32_t)x.templates.back().size();
+                q.options = g.options;
+                q.n_options = g.n_options;
+                q.kind = g.kind;
+                q.token_set = g.token_set;
+                qs.push_back(q);
+                int32_t p = g.n_placeholders - 1;
+                while (p >= 0 && ++pick[p] == g.n_values[p]) pick[p--] = 0;
+                if (p < 0) break;
+            }
+        }
+        x.inputs[i].questions = qs.data();
+        x.inputs[i].n_questions = (int32_t)qs.size();
+        x.inputs[i].grids = nullptr;
+        x.inputs[i].n_grids = 0;
+    }
+    return SPINF_OK;
+}
 
 bool ids_in_range(const spinf_tokens& t, int32_t vocab) {
     if (t.n > 0 && t.ids == nullptr) return false;
@@ -206,6 +278,14 @@ extern "C" spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inp
     if (o.extract_k < 1 || o.extract_k > 16) return fail(SPINF_E_INVALID, "extract_k must be in 1..16");
 
     try {
+        // ---- grid cells become trailing questions of their input
+        Expanded expanded;
+        {
+            spinf_status gs = expand_grids(inputs, n_inputs, o, expanded);
+            if (gs) return gs;
+            inputs = expanded.inputs.data();
+        }
+
         // ---- validation and tries
         std::vector<std::vector<Trie>> tries(n_inputs);
         std::vector<std::vector<int64_t>> qsize(n_inputs);

@@ -89,11 +89,35 @@ typedef struct {
     int32_t token_set;
 } spinf_question;
 
-/* One input: a content (may be empty) read once, and its questions. */
+/* A question grid ("spinf-serve 0.1.1" PyPI page, "What it does": placeholders
+ * turn one template into a grid of questions).  The template is
+ *   segments[0] v_0 segments[1] v_1 ... v_{n-1} segments[n],  n = n_placeholders,
+ * v_i one of placeholder i's values; the grid stands for one question per
+ * combination of values, the first placeholder varying slowest, each with the
+ * grid's options (kind SPINF_Q_SCORED) or a searched slot (SPINF_Q_SEARCHED,
+ * token_set).  Segments and values may be empty token arrays; every placeholder
+ * needs at least one value. */
+typedef struct {
+    const spinf_tokens* segments;   /* [n_placeholders + 1] */
+    int32_t n_placeholders;         /* >= 0 */
+    const spinf_tokens* values;     /* every placeholder's values, placeholder by placeholder */
+    const int32_t* n_values;        /* [n_placeholders], each >= 1 */
+    const spinf_tokens* options;
+    int32_t n_options;
+    int32_t kind;
+    int32_t token_set;
+} spinf_grid;
+
+/* One input: a content (may be empty) read once, its questions, then the cells
+ * of its grids (grid by grid; a zeroed grids field means none).  Grid cells are
+ * questions like any other: they are numbered after the input's own questions
+ * and count toward max_prompts_per_input. */
 typedef struct {
     spinf_tokens content;
     const spinf_question* questions;
     int32_t n_questions;
+    const spinf_grid* grids;
+    int32_t n_grids;
 } spinf_input;
 
 /* Planner options.  Defaults (spinf_plan_opts_default) follow the man page
@@ -184,9 +208,9 @@ void spinf_plan_opts_default(spinf_plan_opts* opts);
  * On success *out owns a new plan.  Errors: SPINF_E_INVALID (empty template,
  * empty or duplicate option, token id out of range, empty input, a scored
  * question without options, a searched slot with options or token_set < -1,
- * extract_k outside 1..16, an unknown kind),
- * SPINF_E_LIMIT (a limit exceeded, or a content and one question do not fit a
- * pass), SPINF_E_NOMEM. */
+ * extract_k outside 1..16, an unknown kind, a grid placeholder without values),
+ * SPINF_E_LIMIT (a limit exceeded -- grid cells included --, or a content and one
+ * question do not fit a pass), SPINF_E_NOMEM. */
 spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inputs,
                              const spinf_plan_opts* opts, spinf_plan** out);
 

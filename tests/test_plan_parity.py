@@ -297,3 +297,47 @@ def test_collect_extract_matches_oracle(spinf):
     ours = Q.collect(tlps)
     flat_res = [np.nan if r is None else r["residual"] for per_q in oc.collect(P, tlps) for r in per_q]
     np.testing.assert_allclose(ours["residual"], flat_res, rtol=0, atol=1e-12)
+
+
+def _grid(g, vocab=60):
+    n_ph = int(g.integers(0, 4))
+    segments = [g.integers(0, vocab, size=int(g.integers(0, 5))).tolist() for _ in range(n_ph + 1)]
+    if not any(segments):
+        segments[-1] = [int(g.integers(0, vocab))]
+    values = [[g.integers(0, vocab, size=int(g.integers(0, 3))).tolist() for _ in range(int(g.integers(1, 4)))]
+              for _ in range(n_ph)]
+    if g.random() < 0.3:
+        return (segments, values, None, int(g.integers(-1, 2)))
+    opts = [[int(x)] for x in g.choice(vocab, size=int(g.integers(1, 4)), replace=False)]
+    return (segments, values, opts)
+
+
+@pytest.mark.parametrize("budget", [200, 16384])
+def test_grids_bit_exact(spinf, budget):
+    g = np.random.default_rng(budget + 1)
+    for trial in range(12):
+        inputs = []
+        for c, qs in _searched_request(g, int(g.integers(1, 6))):
+            inputs.append((c, qs, [_grid(g) for _ in range(int(g.integers(0, 3)))]))
+        try:
+            op.plan(inputs, token_budget=budget)
+        except op.PlanError as e:
+            with pytest.raises(spinf.SpinfError) as ee:
+                spinf.Plan(inputs, token_budget=budget)
+            assert ee.value.status_name == e.status
+            continue
+        P, Q = _compare(spinf, inputs, token_budget=budget)
+        assert Q.counts()[0] == sum(P.n_questions)
+
+
+@pytest.mark.parametrize("bad,status", [
+    ([([1], [], [([[1], [2]], [[]], [[3]])])], "INVALID"),
+    ([([1], [], [([[1], [2], [4]], [[[5], [6]], [[7], [8], [9]]], [[3]])])], "LIMIT"),
+    ([([1], [], [([[]], [], [[3]])])], "INVALID"),
+])
+def test_grid_error_statuses_match(spinf, bad, status):
+    with pytest.raises(op.PlanError) as e:
+        op.plan(bad, max_prompts_per_input=5)
+    with pytest.raises(spinf.SpinfError) as ee:
+        spinf.Plan(bad, max_prompts_per_input=5)
+    assert e.value.status == ee.value.status_name == status
