@@ -31,6 +31,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -49,13 +50,15 @@ constexpr int kBBytes = kBN * 128;
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kScoreThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kTopCap = 16;   // largest extract_k
 
 enum { FULL0 = 0, EMPTY0 = kStages, ACC_FULL0 = 2 * kStages, ACC_EMPTY0 = 2 * kStages + 2, N_SBARS = 2 * kStages + 4 };
 
 constexpr int kSmemBars = kStages * kStageBytes;
 constexpr int kSmemHolder = kSmemBars + N_SBARS * 8;
 constexpr int kScoreSmem = kSmemHolder + 16 + 1024;
+// searched rows: each epilogue thread stages a 32-logit chunk of its row here (33 floats apart)
+constexpr int kSmemXStage = kSmemHolder + 16;
+constexpr int kScoreSmemX = kSmemXStage + 128 * 33 * 4 + 1024;
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -139,18 +142,20 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* _
 }
 
 // ---------------------------------------------------------------- K2
-// Searched rows (XT): a row's candidates of one tile, best first (z descending,
+// Searched rows: a row's best KX candidates of one tile, best first (z descending,
 // lower token first on ties; the tile is scanned in ascending token order, so a
 // new token goes after an equal one already held).
+template <int KX>
 struct TopList {
-    float z[kTopCap];
-    int t[kTopCap];
+    float z[KX];
+    int t[KX];
 };
 
-__device__ __forceinline__ void top_insert(TopList& L, float v, int tok) {
+template <int KX>
+__device__ __forceinline__ void top_insert(TopList<KX>& L, float v, int tok) {
     bool moved = false;
 #pragma unroll
-    for (int j = 0; j < kTopCap; ++j) {
+    for (int j = 0; j < KX; ++j) {
         const bool sw = moved || v > L.z[j];
         const float z0 = L.z[j];
         const int t0 = L.t[j];
@@ -173,7 +178,8 @@ struct ExtractArgs {
     uint2* xpart;                // [X][n_vt][k] (z bits, token)
 };
 
-template <bool FP8, bool XT>
+// KX: 0 (no searched rows), or the list length (8 or 16) kept per searched row and tile
+template <bool FP8, int KX>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_main_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                       const float* __restrict__ s_act, const float* __restrict__ s_w, float2* __restrict__ part,
@@ -286,14 +292,19 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             const float sa = (FP8 && valid) ? s_act[m] : 1.f;
             int xr = -1;
             const uint32_t* allow = nullptr;
-            TopList top;
-            if constexpr (XT) {
+            TopList<KX ? KX : 1> top;
+            float* stage = reinterpret_cast<float*>(smem + kSmemXStage) + (threadIdx.x - 64) * 33;
+            uint32_t mw[kBN / 32];   // the tile's allowed-token words, fetched before the accumulator wait
+            if constexpr (KX > 0) {
                 xr = valid ? xa.row_x[m] : -1;
                 if (xr >= 0) {
                     const int set = xa.x_set[xr];
                     if (set >= 0) allow = xa.token_sets + (size_t)set * xa.words;
 #pragma unroll
-                    for (int j = 0; j < kTopCap; ++j) {
+                    for (int c = 0; c < kBN / 32; ++c)
+                        mw[c] = !allow ? 0xffffffffu : (v0 + 32 * c < V ? __ldg(allow + ((v0 >> 5) + c)) : 0u);
+#pragma unroll
+                    for (int j = 0; j < KX; ++j) {
                         top.z[j] = -INFINITY;
                         top.t[j] = -1;
                     }
@@ -322,13 +333,29 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 for (int i = 0; i < 32; ++i) add += fast_exp2((z[i] - nm) * kLog2e);
                 sum = (mx == -INFINITY ? 0.f : sum * fast_exp2((mx - nm) * kLog2e)) + add;
                 mx = nm;
-                if constexpr (XT) {
+                if constexpr (KX > 0) {
                     if (xr >= 0 && vc < V) {
-                        const uint32_t bits = allow ? __ldg(allow + (vc >> 5)) : 0xffffffffu;
+                        // candidates: allowed and above the list's last entry (z = -inf past the
+                        // vocabulary never is); they go through one copy of the insertion code,
+                        // reading their logits back from this thread's staging row
+                        const float thr = top.z[KX - 1];
+                        uint32_t cand = 0;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)   // z = -inf past the vocabulary: never inserted
-                            if (((bits >> i) & 1u) && z[i] > top.z[kTopCap - 1]) top_insert(top, z[i], vc + i);
+                        for (int i = 0; i < 32; ++i) cand |= (z[i] > thr ? 1u : 0u) << i;
+                        cand &= mw[0];
+                        if (cand) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) stage[i] = z[i];
+                            while (cand) {
+                                const int i = __ffs(cand) - 1;
+                                cand &= cand - 1;
+                                const float v = stage[i];
+                                if (v > top.z[KX - 1]) top_insert<KX>(top, v, vc + i);
+                            }
+                        }
                     }
+#pragma unroll
+                    for (int c = 0; c + 1 < kBN / 32; ++c) mw[c] = mw[c + 1];   // next chunk's word first
                 }
                 while (gc < ge) {
                     const int g = row_glist[gc];
@@ -345,11 +372,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             tc_fence_before();
             mbar_arrive(&bars[ACC_EMPTY0 + acc]);
             if (valid) part[(size_t)m * n_vt + vt] = make_float2(mx, sum);
-            if constexpr (XT) {
+            if constexpr (KX > 0) {
                 if (xr >= 0) {
                     uint2* dst = xa.xpart + ((size_t)xr * n_vt + vt) * xa.k;
 #pragma unroll
-                    for (int j = 0; j < kTopCap; ++j)
+                    for (int j = 0; j < KX; ++j)
                         if (j < xa.k) dst[j] = make_uint2(__float_as_uint(top.z[j]), (uint32_t)top.t[j]);
                 }
             }
@@ -399,63 +426,83 @@ __global__ void __launch_bounds__(128) score_combine_kernel(const float2* __rest
 }
 
 // ---------------------------------------------------------------- K5
-// One warp per searched slot.  Each lane merges the lists of tiles lane, lane + 32,
-// ... (ascending, so an equal z from a later tile -- a higher token -- goes after);
-// then lane 0 takes the k best heads of the 32 lane lists, comparing z and, on
-// ties, the token id.  The result is the unique top k of the row under that order.
+// One CTA of 256 threads per searched slot.  Thread t merges the lists of tiles t,
+// t + 256, ... (ascending, so an equal z from a later tile -- a higher token -- goes
+// after), then the 256 lists are merged pairwise in shared memory, comparing z and, on
+// ties, the token id.  Tokens are unique across tiles, so the result is the unique top
+// k of the row under that order, whatever the merge tree.
 __device__ __forceinline__ bool top_before(float za, int ta, float zb, int tb) {
     return za > zb || (za == zb && ta >= 0 && (tb < 0 || ta < tb));
 }
 
-__global__ void __launch_bounds__(32) extract_combine_kernel(const uint2* __restrict__ xpart,
-                                                              const int32_t* __restrict__ x_m, int n_vt, int k,
-                                                              const float* __restrict__ row_lse,
-                                                              int32_t* __restrict__ top_tok,
-                                                              float* __restrict__ top_lp) {
-    __shared__ float sz[32][kTopCap + 1];
-    __shared__ int st[32][kTopCap + 1];
-    const int x = blockIdx.x, lane = threadIdx.x;
-    TopList L;
+constexpr int kMergeThreads = 256;
+
+template <int KX>
+__global__ void __launch_bounds__(kMergeThreads) extract_combine_kernel(const uint2* __restrict__ xpart,
+                                                                         const int32_t* __restrict__ x_m, int n_vt,
+                                                                         int k, const float* __restrict__ row_lse,
+                                                                         int32_t* __restrict__ top_tok,
+                                                                         float* __restrict__ top_lp) {
+    __shared__ float sz[kMergeThreads][KX];
+    __shared__ int st[kMergeThreads][KX];
+    const int x = blockIdx.x, t = threadIdx.x;
+    TopList<KX> L;
 #pragma unroll
-    for (int j = 0; j < kTopCap; ++j) {
+    for (int j = 0; j < KX; ++j) {
         L.z[j] = -INFINITY;
         L.t[j] = -1;
     }
-    for (int vt = lane; vt < n_vt; vt += 32) {
+    for (int vt = t; vt < n_vt; vt += kMergeThreads) {
         const uint2* src = xpart + ((size_t)x * n_vt + vt) * k;
-        for (int j = 0; j < k; ++j) {
-            const uint2 c = src[j];
-            const float z = __uint_as_float(c.x);
-            if (!(z > L.z[kTopCap - 1])) break;   // the tile's list is sorted: nothing better follows
-            top_insert(L, z, (int)c.y);
+        uint2 c[KX];
+#pragma unroll
+        for (int j = 0; j < KX; ++j) c[j] = j < k ? src[j] : make_uint2(__float_as_uint(-INFINITY), ~0u);
+#pragma unroll
+        for (int j = 0; j < KX; ++j) {   // the tile's list is sorted: stop at the first that does not enter
+            const float z = __uint_as_float(c[j].x);
+            if (!(z > L.z[KX - 1])) break;
+            top_insert<KX>(L, z, (int)c[j].y);
         }
     }
 #pragma unroll
-    for (int j = 0; j < kTopCap; ++j) {
-        sz[lane][j] = L.z[j];
-        st[lane][j] = L.t[j];
+    for (int j = 0; j < KX; ++j) {
+        sz[t][j] = L.z[j];
+        st[t][j] = L.t[j];
     }
-    sz[lane][kTopCap] = -INFINITY;   // list end
-    st[lane][kTopCap] = -1;
-    __syncwarp();
-    if (lane == 0) {
-        int head[32];
-        for (int l = 0; l < 32; ++l) head[l] = 0;
-        const float lse = row_lse[x_m[x]];
-        for (int j = 0; j < k; ++j) {
-            int best = 0;
-            for (int l = 1; l < 32; ++l)
-                if (top_before(sz[l][head[l]], st[l][head[l]], sz[best][head[best]], st[best][head[best]])) best = l;
-            const float z = sz[best][head[best]];
-            const int t = st[best][head[best]];
-            if (t >= 0 && head[best] < kTopCap) ++head[best];
-            top_tok[(size_t)x * k + j] = t;
-            top_lp[(size_t)x * k + j] = t >= 0 ? z - lse : -INFINITY;
+    __syncthreads();
+    for (int n = kMergeThreads / 2; n >= 1; n >>= 1) {
+        if (t < n) {   // merge lists 2t and 2t + 1 into L
+            int a = 0, b = 0;
+#pragma unroll
+            for (int j = 0; j < KX; ++j) {
+                const float za = a < KX ? sz[2 * t][a] : -INFINITY, zb = b < KX ? sz[2 * t + 1][b] : -INFINITY;
+                const int ta = a < KX ? st[2 * t][a] : -1, tb = b < KX ? st[2 * t + 1][b] : -1;
+                const bool take_a = !top_before(zb, tb, za, ta);   // an exhausted list reads (-inf, -1)
+                L.z[j] = take_a ? za : zb;
+                L.t[j] = take_a ? ta : tb;
+                a += take_a ? 1 : 0;
+                b += take_a ? 0 : 1;
+            }
         }
+        __syncthreads();
+        if (t < n) {
+#pragma unroll
+            for (int j = 0; j < KX; ++j) {
+                sz[t][j] = L.z[j];
+                st[t][j] = L.t[j];
+            }
+        }
+        __syncthreads();
+    }
+    if (t < k) {
+        const float z = sz[0][t];
+        const int tok = st[0][t];
+        top_tok[(size_t)x * k + t] = tok;
+        top_lp[(size_t)x * k + t] = tok >= 0 ? z - row_lse[x_m[x]] : -INFINITY;
     }
 }
 
-template <bool FP8, bool XT>
+template <bool FP8, int KX>
 spinf_status launch_score(const Pass& P, const ScoreLayout& L, const void* hidden, const void* w, const float* w_scale,
                           int D, int V, float* row_lse, float* token_lp, const spinf_extract_out* ex, uint8_t* ws,
                           int* err, cudaStream_t stream) {
@@ -481,7 +528,8 @@ spinf_status launch_score(const Pass& P, const ScoreLayout& L, const void* hidde
     if ((s = make_tmap(&tw, dt, 2, w, dw, st, bw, CU_TENSOR_MAP_SWIZZLE_128B))) return s;
     static bool configured = false;
     if (!configured) {
-        e = cudaFuncSetAttribute(score_main_kernel<FP8, XT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
+        e = cudaFuncSetAttribute(score_main_kernel<FP8, KX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 KX ? kScoreSmemX : kScoreSmem);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(score)");
         configured = true;
     }
@@ -489,9 +537,9 @@ spinf_status launch_score(const Pass& P, const ScoreLayout& L, const void* hidde
     const int n_kb = (D + kbk - 1) / kbk;
     const int total = L.n_vt * L.n_st;
     const int grid = std::min(total, sm_count());
-    ExtractArgs xa{P.dev.row_x, P.dev.x_set, XT ? ex->token_sets : nullptr, (V + 31) / 32, L.k,
+    ExtractArgs xa{P.dev.row_x, P.dev.x_set, KX ? ex->token_sets : nullptr, (V + 31) / 32, L.k,
                    reinterpret_cast<uint2*>(ws + L.xpart)};
-    score_main_kernel<FP8, XT><<<grid, kScoreThreads, kScoreSmem, stream>>>(
+    score_main_kernel<FP8, KX><<<grid, kScoreThreads, KX ? kScoreSmemX : kScoreSmem, stream>>>(
         th, tw, sa, w_scale, part, zg, P.dev.row_gptr, P.dev.row_glist, P.dev.gather_tok, L.M, V, n_kb, L.n_st,
         L.n_vt, xa, err);
     e = cudaGetLastError();
@@ -500,8 +548,8 @@ spinf_status launch_score(const Pass& P, const ScoreLayout& L, const void* hidde
                                                            row_lse, token_lp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-    if constexpr (XT) {
-        extract_combine_kernel<<<L.X, 32, 0, stream>>>(xa.xpart, P.dev.x_m, L.n_vt, L.k, row_lse, ex->top_tok,
+    if constexpr (KX > 0) {
+        extract_combine_kernel<KX><<<L.X, kMergeThreads, 0, stream>>>(xa.xpart, P.dev.x_m, L.n_vt, L.k, row_lse, ex->top_tok,
                                                        ex->top_lp);
         e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "extract launch");
@@ -550,11 +598,20 @@ extern "C" spinf_status spinf_score_extract(const spinf_plan* plan, int32_t pass
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const float* wsc = w_dtype == SPINF_DTYPE_E4M3 ? w_scale : nullptr;
+    // list length per searched row and tile: 8 for extract_k <= 8, else 16
+    const int kx = !xt ? 0 : L.k <= 8 ? 8 : 16;
+    auto go = [&](auto fp8, auto kx_c) {
+        return launch_score<decltype(fp8)::value, decltype(kx_c)::value>(P, L, hidden, w, wsc, d_model, vocab, row_lse,
+                                                                         token_lp, ex, ws, plan->d_err, s);
+    };
+    using F = std::false_type;
+    using T = std::true_type;
+    using K0 = std::integral_constant<int, 0>;
+    using K8 = std::integral_constant<int, 8>;
+    using K16 = std::integral_constant<int, 16>;
     if (w_dtype == SPINF_DTYPE_E4M3)
-        return xt ? launch_score<true, true>(P, L, hidden, w, wsc, d_model, vocab, row_lse, token_lp, ex, ws, plan->d_err, s)
-                  : launch_score<true, false>(P, L, hidden, w, wsc, d_model, vocab, row_lse, token_lp, ex, ws, plan->d_err, s);
-    return xt ? launch_score<false, true>(P, L, hidden, w, wsc, d_model, vocab, row_lse, token_lp, ex, ws, plan->d_err, s)
-              : launch_score<false, false>(P, L, hidden, w, wsc, d_model, vocab, row_lse, token_lp, ex, ws, plan->d_err, s);
+        return kx == 0 ? go(T{}, K0{}) : kx == 8 ? go(T{}, K8{}) : go(T{}, K16{});
+    return kx == 0 ? go(F{}, K0{}) : kx == 8 ? go(F{}, K8{}) : go(F{}, K16{});
 }
 
 extern "C" spinf_status spinf_score(const spinf_plan* plan, int32_t pass, const void* hidden, const void* w,
@@ -626,8 +683,8 @@ extern "C" spinf_status spinf_score_static(const spinf_plan* plan, int32_t pass,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(scratch);
     if (w_dtype == SPINF_DTYPE_E4M3)
-        return launch_score<true, false>(P, L, hidden, w, w_scale, d_model, vocab, row_lse, token_lp, nullptr, ws,
+        return launch_score<true, 0>(P, L, hidden, w, w_scale, d_model, vocab, row_lse, token_lp, nullptr, ws,
                                          plan->d_err, s);
-    return launch_score<false, false>(P, L, hidden, w, nullptr, d_model, vocab, row_lse, token_lp, nullptr, ws,
+    return launch_score<false, 0>(P, L, hidden, w, nullptr, d_model, vocab, row_lse, token_lp, nullptr, ws,
                                       plan->d_err, s);
 }
