@@ -11,12 +11,21 @@ DESCRIPTION speaks of one packed forward.  Readings (the pages give no formula):
   branch token takes the position it has in its unpacked sequence;
 * projections are plain products ``y = x @ w.T`` (``w`` is ``[out, in]``); the QKV
   output is the concatenation q | k | v along features.
+
+The fp8 linears of the calibrated scheme (man page, DESCRIPTION and PARAMETERS
+``--quant``: ``fp8s``, scores bit-identical alone or packed) use static scales, fixed
+before the request: one per activation tensor (``x_scale``) and one per weight output
+channel (``w_scale[out]``).  Reading: the activation codes are
+``e4m3(x / x_scale)`` (fp32 division, round to nearest even, saturating at 448) and
+``y = (codes_x * x_scale) @ (codes_w * w_scale[:, None]).T``.  A static scale makes a
+row's codes a function of the row alone, whatever else is in the batch.
 """
 from __future__ import annotations
 
 import numpy as np
 
 from . import attention
+from . import fp8
 
 
 def rope(x, pos, theta):
@@ -47,3 +56,24 @@ def packed_layer_rows(layout, x, w_qkv, w_o, n_q_heads, n_kv_heads, d_head, thet
     q, k = rope(q, layout.pos, theta), rope(k, layout.pos, theta)
     o = attention.attention_rows(layout, q, k, v, n_q_heads, n_kv_heads, rows)
     return o.reshape(len(rows), n_q_heads * d_head) @ np.asarray(w_o, dtype=np.float64).T
+
+
+def qkv_rope(x, w_qkv, pos, n_q_heads, n_kv_heads, d_head, theta):
+    """q, k (turned at tree depth) and v of the packed rows, fp64: the projection
+    ``x @ w_qkv.T`` split into heads, then :func:`rope` on q and k."""
+    y = np.asarray(x, dtype=np.float64) @ np.asarray(w_qkv, dtype=np.float64).T
+    q, k, v = split_qkv(y, n_q_heads, n_kv_heads, d_head)
+    return rope(q, pos, theta), rope(k, pos, theta), v
+
+
+def quantize_static(x, x_scale):
+    """e4m3 codes of ``x`` with a static scale: ``e4m3(x / x_scale)``, the division in fp32."""
+    scaled = (np.asarray(x, dtype=np.float32) / np.float32(x_scale)).astype(np.float32)
+    return fp8.encode_rne_sat(scaled)
+
+
+def linear_fp8(x_codes, x_scale, w_codes, w_scale):
+    """``(codes_x * x_scale) @ (codes_w * w_scale[:, None]).T`` in fp64."""
+    xs = fp8.decode(x_codes) * float(np.float32(x_scale))
+    ws = fp8.decode(w_codes) * np.asarray(w_scale, dtype=np.float64)[:, None]
+    return xs @ ws.T

@@ -83,3 +83,49 @@ def test_packed_layer_equals_each_unpacked_branch():
         path = lay.visible(r)                      # the row's unpacked sequence, in order
         ref = _unpacked_layer(emb[lay.tok[path]], w_qkv, w_o, Hq, Hkv, d, theta)[-1]
         assert np.allclose(got[r], ref, atol=1e-10), r
+
+
+def test_static_quantisation_matches_torch_recipe():
+    """e4m3 codes with a static scale against torch's float8_e4m3fn cast of the fp32
+    quotient (clamped to +-448 first: torch's cast does not saturate)."""
+    import torch
+    g = np.random.default_rng(5)
+    x = (g.standard_normal((40, 96)) * 3).astype(np.float32)
+    x[0, :4] = [0.0, -0.0, 1e-9, 5000.0]
+    s = np.float32(0.0123)
+    codes = ol.quantize_static(x, s)
+    q = torch.from_numpy(x) / torch.tensor(s)
+    want = torch.clamp(q, -448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(codes, want)
+
+
+def test_fp8_linear_against_torch_decoded_values():
+    import torch
+    g = np.random.default_rng(6)
+    xc = g.integers(0, 256, size=(7, 64)).astype(np.uint8)
+    wc = g.integers(0, 256, size=(9, 64)).astype(np.uint8)
+    xc[(xc & 0x7F) == 0x7F] = 0   # no NaN codes
+    wc[(wc & 0x7F) == 0x7F] = 0
+    ws = g.random(9).astype(np.float32) + 0.5
+    xs = np.float32(0.37)
+    y = ol.linear_fp8(xc, xs, wc, ws)
+    xd = torch.from_numpy(xc).view(torch.float8_e4m3fn).double() * float(xs)
+    wd = torch.from_numpy(wc).view(torch.float8_e4m3fn).double() * torch.from_numpy(ws).double()[:, None]
+    np.testing.assert_allclose(y, (xd @ wd.T).numpy(), rtol=1e-13, atol=1e-13)
+
+
+def test_qkv_rope_is_projection_then_rotation():
+    g = np.random.default_rng(8)
+    T, D, Hq, Hkv, d = 5, 32, 2, 1, 16
+    x = g.standard_normal((T, D))
+    w = g.standard_normal(((Hq + 2 * Hkv) * d, D))
+    pos = np.array([0, 3, 1, 7, 2])
+    q, k, v = ol.qkv_rope(x, w, pos, Hq, Hkv, d, 10000.0)
+    y = x @ w.T
+    # position 0 leaves the row unturned; v is never turned
+    np.testing.assert_allclose(q[0].reshape(-1), y[0, :Hq * d], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(v.reshape(T, -1), y[:, (Hq + Hkv) * d:], rtol=0, atol=1e-12)
+    # a turn keeps each pair's norm
+    kk = y[:, Hq * d:(Hq + Hkv) * d].reshape(T, Hkv, d)
+    np.testing.assert_allclose(np.hypot(k[..., :d // 2], k[..., d // 2:]),
+                               np.hypot(kk[..., :d // 2], kk[..., d // 2:]), rtol=1e-12)
