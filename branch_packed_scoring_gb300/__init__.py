@@ -32,7 +32,7 @@ SYMBOLS = [
     "spinf_branch_attention", "spinf_score_workspace_bytes",
     "spinf_score", "spinf_score_extract", "spinf_score_static", "spinf_collect", "spinf_collect_extract",
     "spinf_device_status", "spinf_device_selftest",
-    "spinf_rope_tree", "spinf_linear",
+    "spinf_rope_tree", "spinf_linear", "spinf_qkv_rope", "spinf_quantize_static",
     "spinf_plan_free", "spinf_fingerprint",
     "spinf_status_string", "spinf_last_error",
 ]
@@ -129,7 +129,9 @@ def lib():
     L.spinf_device_status.argtypes = [vp, vp]
     L.spinf_device_selftest.argtypes = [vp, i32, vp]
     L.spinf_rope_tree.argtypes = [vp, i32, vp, vp, i32, i32, i32, f32, vp]
-    L.spinf_linear.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+    L.spinf_linear.argtypes = [vp, vp, vp, vp, f32, i32, vp, i64, i64, i64, vp]
+    L.spinf_qkv_rope.argtypes = [vp, i32, vp, vp, vp, f32, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp]
+    L.spinf_quantize_static.argtypes = [vp, f32, vp, i64, vp]
     L.spinf_plan_free.argtypes = [vp]
     L.spinf_plan_free.restype = None
     L.spinf_fingerprint.restype = ctypes.c_char_p
@@ -140,7 +142,8 @@ def lib():
                  "spinf_plan_upload", "spinf_plan_upload_to", "spinf_plan_window_schedule",
                  "spinf_branch_attention", "spinf_score", "spinf_score_extract", "spinf_score_static", "spinf_collect",
                  "spinf_collect_extract",
-                 "spinf_device_status", "spinf_device_selftest", "spinf_rope_tree", "spinf_linear"):
+                 "spinf_device_status", "spinf_device_selftest", "spinf_rope_tree", "spinf_linear",
+                 "spinf_qkv_rope", "spinf_quantize_static"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -485,9 +488,24 @@ def rope_tree(plan, p, q, k, n_q_heads, n_kv_heads, d_head, theta=10000.0, strea
                                  _stream(stream)))
 
 
-def linear(x, w, y, stream=None):
-    """y = x . w^T on the device, bf16 (spinf_linear); x [rows, in], w [out, in], y [rows, out]."""
-    _check(lib().spinf_linear(_ptr(x), _ptr(w), _ptr(y), x.shape[0], x.shape[1], w.shape[0], _stream(stream)))
+def linear(plan, x, w, y, w_scale=None, x_scale=1.0, w_dtype=DTYPE_BF16, stream=None):
+    """y = x . w^T on the tensor cores (spinf_linear); x [rows, in], w [out, in], y [rows, out] bf16.
+    With ``w_dtype=DTYPE_E4M3``, x and w are e4m3 codes (uint8), ``w_scale`` [out] fp32, ``x_scale`` static."""
+    _check(lib().spinf_linear(plan.handle, _ptr(x), _ptr(w), _ptr(w_scale), float(x_scale), w_dtype, _ptr(y),
+                              x.shape[0], x.shape[1], w.shape[0], _stream(stream)))
+
+
+def qkv_rope(plan, p, x, w, q, k, v, n_q_heads, n_kv_heads, d_head, theta=10000.0, w_scale=None, x_scale=1.0,
+             w_dtype=DTYPE_BF16, stream=None):
+    """QKV projection of pass p with the rotary turn fused (spinf_qkv_rope); writes q, k, v."""
+    _check(lib().spinf_qkv_rope(plan.handle, p, _ptr(x), _ptr(w), _ptr(w_scale), float(x_scale), w_dtype,
+                                x.shape[1], n_q_heads, n_kv_heads, d_head, float(theta), _ptr(q), _ptr(k), _ptr(v),
+                                _stream(stream)))
+
+
+def quantize_static(x, x_scale, codes, stream=None):
+    """e4m3 codes of bf16 ``x`` with a static scale (spinf_quantize_static)."""
+    _check(lib().spinf_quantize_static(_ptr(x), float(x_scale), _ptr(codes), x.numel(), _stream(stream)))
 
 
 def score_workspace_bytes(plan, p, vocab, d_model, w_dtype=DTYPE_BF16):

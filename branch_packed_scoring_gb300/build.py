@@ -70,7 +70,7 @@ def build(verbose: bool = False, ptxas_info: bool = False, extra=()) -> str:
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
     if _stale(LIB, objs):
-        cmd = [nvcc] + ARCH + ["-shared", "-o", LIB] + objs + ["-lcublasLt"]
+        cmd = [nvcc] + ARCH + ["-shared", "-o", LIB] + objs
         r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
         if r.returncode:
             sys.stdout.write(r.stdout)

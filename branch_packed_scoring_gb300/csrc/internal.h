@@ -7,6 +7,8 @@
 #include <string>
 #include <vector>
 
+#include <vector_types.h>
+
 #include "spinf.h"
 
 namespace spinf {
@@ -44,6 +46,15 @@ struct WindowSchedule {
     std::vector<unsigned char> staging;
 };
 
+// cos and sin of the rotary angles of one pass for one (d_head, theta): [max pos + 1][d / 2]
+// (built on first use, plan-owned device copy).
+struct RopeTable {
+    int32_t d = 0;
+    float theta = 0.f;
+    std::vector<float2> host;
+    float2* dev = nullptr;
+};
+
 struct Pass {
     int32_t T = 0, T_pad = 0;
     std::vector<int32_t> tok, parent, pos, end, anchor;
@@ -55,6 +66,7 @@ struct Pass {
     PassDevice dev;
     std::vector<unsigned char> staging;   // host source of the descriptor upload, kept until the plan is freed
     std::vector<std::unique_ptr<WindowSchedule>> windows;
+    std::vector<std::unique_ptr<RopeTable>> ropes;
 };
 
 // Where the option tokens of one laid-out question sit in its pass's gather list.

@@ -1,41 +1,91 @@
-// The steps around the attention call that complete a packed layer: rotary
-// position embedding at tree positions, and the bf16 linear maps of the QKV and
-// output projections.
+// The steps around the attention call that complete a packed layer: the QKV
+// projection with rotary position embedding at tree positions, the output
+// projection, and the fp8 form of both with static scales.
 //
 // The method ("spinf-serve 0.1.1", PyPI page, "What it does"): every question is
 // a branch of the packed pass, and an input's scores are the same alone or
 // packed.  A token's position is therefore its depth on its own root path (the
 // plan's pos[]), never its row in the pass: a branch token gets the positions its
-// unpacked sequence (content, question, option prefix) would give it.
-#include <cublasLt.h>
+// unpacked sequence (content, question, option prefix) would give it.  The fp8
+// scheme that keeps scores bit-identical alone or packed ("spinf-serve" man page,
+// DESCRIPTION, --quant fp8s) has static scales: one per activation tensor, one
+// per weight output channel, fixed before the request.
+//
+//   linear_kernel<FP8, MODE>   persistent tcgen05 GEMM y = x w^T: 128 rows x 256
+//                              output features per tile, fp32 in TMEM (two
+//                              accumulators), a 4-stage TMA ring.  MODE 0 writes y;
+//                              MODE 1 (QKV) turns the q and k columns by the row's
+//                              tree position in the epilogue and writes q, k, v in
+//                              the attention kernel's layouts.
+//   quantize_static_kernel     bf16 -> e4m3 codes with a static scale
+//   rope_tree_kernel           the rotary embedding alone, in place on q and k
+//
+// Each output element is one fixed-order reduction over the input features, by
+// the same tile code wherever its row sits, so a row's output does not depend on
+// the other rows of the call (no split of the reduction, no algorithm choice by
+// size).
+#include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
-#include <mutex>
 
 #include "internal.h"
+#include "ptx.cuh"
 #include "runtime.h"
 
 namespace spinf {
 namespace {
 
-// One CTA per packed row.  Rotate-half convention: the pairs (x[i], x[i + d/2]),
-// i < d/2, turn by pos * theta^(-2i/d).  The angles are formed and reduced in fp64
-// (pos reaches the tens of thousands), then the rotation runs in fp32 per head.
-__global__ void rope_tree_kernel(__nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ k,
-                                 const int32_t* __restrict__ pos, int Hq, int Hkv, int d, double log2_theta) {
-    extern __shared__ float cs[];   // [d/2] cos, then [d/2] sin
-    const int row = blockIdx.x, half = d / 2;
-    const double p = static_cast<double>(__ldg(pos + row));
-    for (int i = threadIdx.x; i < half; i += blockDim.x) {
-        const double inv_freq = exp2(-log2_theta * (2.0 * i) / d);
-        double s, c;
-        sincos(p * inv_freq, &s, &c);
-        cs[i] = static_cast<float>(c);
-        cs[half + i] = static_cast<float>(s);
+using namespace dev;
+
+// ---------------------------------------------------------------- rotary table
+// cos and sin of pos * theta^(-2i/d) for every pos of the pass (0..max pos), i < d/2,
+// formed in fp64 on the host and rounded to fp32: the fused projection and the
+// stand-alone rotation read the same values.
+spinf_status rope_table(Pass& P, int32_t d, float theta, cudaStream_t stream, const float2** out) {
+    for (auto& t : P.ropes)
+        if (t->d == d && t->theta == theta && t->dev) {
+            *out = t->dev;
+            return SPINF_OK;
+        }
+    auto t = std::make_unique<RopeTable>();
+    t->d = d;
+    t->theta = theta;
+    int32_t max_pos = 0;
+    for (int32_t r = 0; r < P.T_pad; ++r) max_pos = std::max(max_pos, P.pos[r]);
+    const int32_t half = d / 2;
+    t->host.resize((size_t)(max_pos + 1) * half);
+    const double lt = std::log2(static_cast<double>(theta));
+    for (int32_t i = 0; i < half; ++i) {
+        const double inv_freq = std::exp2(-lt * (2.0 * i) / d);
+        for (int32_t p = 0; p <= max_pos; ++p) {
+            const double a = p * inv_freq;
+            t->host[(size_t)p * half + i] = make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
+        }
     }
-    __syncthreads();
+    void* mem = nullptr;
+    cudaError_t e = cudaMalloc(&mem, t->host.size() * sizeof(float2));
+    if (e != cudaSuccess) return fail(SPINF_E_NOMEM, "device allocation of a rotary table failed");
+    e = cudaMemcpyAsync(mem, t->host.data(), t->host.size() * sizeof(float2), cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) {
+        cudaFree(mem);
+        return cuda_fail(e, "rotary table upload");
+    }
+    t->dev = static_cast<float2*>(mem);
+    *out = t->dev;
+    P.ropes.push_back(std::move(t));
+    return SPINF_OK;
+}
+
+// One CTA per packed row; the row's table entries are shared by its heads.
+__global__ void rope_tree_kernel(__nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ k,
+                                 const int32_t* __restrict__ pos, const float2* __restrict__ table, int Hq, int Hkv,
+                                 int d) {
+    const int row = blockIdx.x, half = d / 2;
+    const float2* cs = table + (size_t)__ldg(pos + row) * half;
     const int pairs_q = Hq * half, pairs = (Hq + Hkv) * half;
     for (int j = threadIdx.x; j < pairs; j += blockDim.x) {
         const bool is_q = j < pairs_q;
@@ -44,27 +94,267 @@ __global__ void rope_tree_kernel(__nv_bfloat16* __restrict__ q, __nv_bfloat16* _
         __nv_bfloat16* base = is_q ? q + (static_cast<size_t>(row) * Hq + h) * d
                                    : k + (static_cast<size_t>(row) * Hkv + h) * d;
         const float x0 = __bfloat162float(base[i]), x1 = __bfloat162float(base[i + half]);
-        const float c = cs[i], s = cs[half + i];
-        base[i] = __float2bfloat16_rn(x0 * c - x1 * s);
-        base[i + half] = __float2bfloat16_rn(x1 * c + x0 * s);
+        const float2 r = __ldg(cs + i);
+        base[i] = __float2bfloat16_rn(x0 * r.x - x1 * r.y);
+        base[i + half] = __float2bfloat16_rn(x1 * r.x + x0 * r.y);
     }
 }
 
-struct LtHandle {
-    cublasLtHandle_t h = nullptr;
-    int device = -1;
+// ---------------------------------------------------------------- static e4m3 codes
+__global__ void quantize_static_kernel(const __nv_bfloat16* __restrict__ x, float scale, uint8_t* __restrict__ out,
+                                       int64_t n8) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 u = reinterpret_cast<const uint4*>(x)[i];
+        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+        uint32_t w[2] = {0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(b[j]);
+            const float2 qv = make_float2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
+            const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(qv, __NV_SATFINITE, __NV_E4M3);
+            w[j >> 1] |= static_cast<uint32_t>(c) << ((j & 1) * 16);
+        }
+        reinterpret_cast<uint2*>(out)[i] = make_uint2(w[0], w[1]);
+    }
+}
+
+// ---------------------------------------------------------------- projection GEMM
+constexpr int kLM = 128;   // rows per tile (MMA M, TMEM lanes)
+constexpr int kLN = 256;   // output features per tile (MMA N)
+constexpr int kLStages = 4;
+constexpr int kLA = kLM * 128;
+constexpr int kLB = kLN * 128;
+constexpr int kLStage = kLA + kLB;
+constexpr int kLThreads = 192;
+enum { LFULL0 = 0, LEMPTY0 = kLStages, LACC_FULL0 = 2 * kLStages, LACC_EMPTY0 = 2 * kLStages + 2,
+       LN_BARS = 2 * kLStages + 4 };
+constexpr int kLSmemBars = kLStages * kLStage;
+constexpr int kLSmemHolder = kLSmemBars + LN_BARS * 8;
+constexpr int kLSmem = kLSmemHolder + 16 + 1024;
+
+// Where the product's columns go.  MODE 0: all to y[0] (row stride ld[0]).  MODE 1:
+// product column n belongs to output o = 0 (q), 1 (k) or 2 (v) by base[]; columns
+// below n_rot (q and k) are turned by the row's position, pairs (i, i + d/2) of
+// each d-column head.
+struct LinearOut {
+    __nv_bfloat16* y[3];
+    int ld[3];
+    int base[3];
+    int n_rot;
+    int d;
+    const float2* cs;      // [max pos + 1][d / 2]
+    const int32_t* pos;    // [rows]
 };
 
-cublasLtHandle_t lt_handle(int device) {
-    static std::mutex mu;
-    static LtHandle handles[64];
-    std::lock_guard<std::mutex> lock(mu);
-    if (device < 0 || device >= 64) return nullptr;
-    if (!handles[device].h) {
-        if (cublasLtCreate(&handles[device].h) != CUBLAS_STATUS_SUCCESS) handles[device].h = nullptr;
-        handles[device].device = device;
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&v)[32]) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        d4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+}
+
+template <bool FP8, int MODE>
+__global__ void __launch_bounds__(kLThreads, 1)
+    linear_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                  const float* __restrict__ w_scale, float x_scale, const LinearOut out, int rows, int N, int n_kb,
+                  int n_mt, int n_nt, int* __restrict__ err) {
+    constexpr int kPerMma = FP8 ? 32 : 16;
+    constexpr int kMmaPerStage = (FP8 ? 128 : 64) / kPerMma;
+    constexpr int kBK = FP8 ? 128 : 64;
+    constexpr uint32_t idesc = FP8 ? idesc_e4m3(kLM, kLN) : idesc_bf16(kLM, kLN, false, false);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kLSmemBars);
+    uint32_t* holder = reinterpret_cast<uint32_t*>(smem + kLSmemHolder);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = n_mt * n_nt;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kLStages; ++s) {
+            mbar_init(&bars[LFULL0 + s], 1);
+            mbar_init(&bars[LEMPTY0 + s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&bars[LACC_FULL0 + a], 1);
+            mbar_init(&bars[LACC_EMPTY0 + a], 128);
+        }
+        fence_mbar_init();
     }
-    return handles[device].h;
+    if (warp == 1) {
+        tmem_alloc(holder, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *holder;
+
+    // tile u: rows mt, features nt; consecutive tiles share the row block (the weights
+    // stay in L2 across row blocks, each row block is read from HBM once)
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_x);
+            tma_prefetch_desc(&tm_w);
+            uint32_t it = 0;
+            for (int u = blockIdx.x; u < total; u += gridDim.x) {
+                const int mt = u / n_nt, nt = u % n_nt;
+                for (int kb = 0; kb < n_kb; ++kb, ++it) {
+                    const int s = it % kLStages;
+                    mbar_wait(&bars[LEMPTY0 + s], ((it / kLStages) & 1) ^ 1, err);
+                    uint8_t* sa = smem + s * kLStage;
+                    mbar_arrive_expect_tx(&bars[LFULL0 + s], kLStage);
+                    tma_load_2d(sa, &tm_x, &bars[LFULL0 + s], kb * kBK, mt * kLM);
+                    tma_load_2d(sa + kLA, &tm_w, &bars[LFULL0 + s], kb * kBK, nt * kLN);
+                }
+            }
+            for (uint32_t i = it > (uint32_t)kLStages ? it - kLStages : 0; i < it; ++i)
+                mbar_drain(&bars[LFULL0 + i % kLStages], (i / kLStages) & 1, err);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t it = 0, tcount = 0;
+            for (int u = blockIdx.x; u < total; u += gridDim.x, ++tcount) {
+                const int acc = tcount & 1;
+                mbar_wait(&bars[LACC_EMPTY0 + acc], ((tcount >> 1) & 1) ^ 1, err);
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + acc * kLN;
+                for (int kb = 0; kb < n_kb; ++kb, ++it) {
+                    const int s = it % kLStages;
+                    mbar_wait(&bars[LFULL0 + s], (it / kLStages) & 1, err);
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(smem + s * kLStage);
+                    const uint32_t b_base = a_base + kLA;
+#pragma unroll
+                    for (int kk = 0; kk < kMmaPerStage; ++kk) {
+                        const uint64_t da = sdesc_sw128(a_base + kk * 32, 16, 1024);
+                        const uint64_t db = sdesc_sw128(b_base + kk * 32, 16, 1024);
+                        if (FP8) mma_f8_ss(d_tmem, da, db, idesc, (kb | kk) != 0);
+                        else mma_f16_ss(d_tmem, da, db, idesc, (kb | kk) != 0);
+                    }
+                    mma_commit(&bars[LEMPTY0 + s]);
+                }
+                mma_commit(&bars[LACC_FULL0 + acc]);
+            }
+        }
+    } else {
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        uint32_t tcount = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x, ++tcount) {
+            const int mt = u / n_nt, nt = u % n_nt;
+            const int acc = tcount & 1;
+            const int row = mt * kLM + r;
+            const int n0 = nt * kLN;
+            const bool valid = row < rows;
+            const float2* cs = nullptr;
+            if (MODE == 1 && valid) cs = out.cs + (size_t)__ldg(out.pos + row) * (out.d / 2);
+            mbar_wait(&bars[LACC_FULL0 + acc], (tcount >> 1) & 1, err);
+            tc_fence_after();
+            const uint32_t t0 = tmem + lane_off + acc * kLN;
+            auto load = [&](int c, float (&v)[32]) {   // product columns n0 + 32c .. + 31, scaled
+                uint32_t rr[32];
+                tmem_ld32(t0 + c * 32, rr);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float x = __uint_as_float(rr[i]);
+                    if (FP8) {
+                        const int n = n0 + c * 32 + i;
+                        x = (x * (n < N ? __ldg(w_scale + n) : 0.f)) * x_scale;
+                    }
+                    v[i] = x;
+                }
+            };
+#pragma unroll 1
+            for (int c = 0; c < kLN / 32; ++c) {
+                const int n = n0 + c * 32;
+                if (n >= N) break;
+                if constexpr (MODE == 0) {
+                    float v[32];
+                    load(c, v);
+                    if (valid) store_bf16x32(out.y[0] + (size_t)row * out.ld[0] + n, v);
+                } else {
+                    // the output that holds column n (selects, not an indexed parameter array)
+                    const int o = n < out.base[1] ? 0 : n < out.base[2] ? 1 : 2;
+                    const int col = n - (o == 0 ? out.base[0] : o == 1 ? out.base[1] : out.base[2]);
+                    __nv_bfloat16* dst = (o == 0 ? out.y[0] : o == 1 ? out.y[1] : out.y[2]) +
+                                         (size_t)row * (o == 0 ? out.ld[0] : o == 1 ? out.ld[1] : out.ld[2]);
+                    if (n >= out.n_rot) {   // v: no turn
+                        float v[32];
+                        load(c, v);
+                        if (valid) store_bf16x32(dst + col, v);
+                        continue;
+                    }
+                    const int half = out.d / 2, j = col % out.d;
+                    if (j >= half) continue;   // written with its first half
+                    float x0[32], x1[32];
+                    load(c, x0);
+                    load(c + half / 32, x1);
+                    if (valid) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float2 t = __ldg(cs + j + i);
+                            const float a = x0[i], b = x1[i];
+                            x0[i] = a * t.x - b * t.y;
+                            x1[i] = b * t.x + a * t.y;
+                        }
+                        store_bf16x32(dst + col, x0);
+                        store_bf16x32(dst + col + half, x1);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars[LACC_EMPTY0 + acc]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <bool FP8, int MODE>
+spinf_status launch_linear(const void* x, const void* w, const float* w_scale, float x_scale, const LinearOut& out,
+                           int64_t rows, int64_t K, int64_t N, int* err, cudaStream_t stream) {
+    CUtensorMap tx, tw;
+    const uint64_t elt = FP8 ? 1 : 2;
+    const uint64_t dx[2] = {(uint64_t)K, (uint64_t)rows};
+    const uint64_t dw[2] = {(uint64_t)K, (uint64_t)N};
+    const uint64_t st[1] = {(uint64_t)K * elt};
+    const uint32_t bx[2] = {FP8 ? 128u : 64u, (uint32_t)kLM};
+    const uint32_t bw[2] = {FP8 ? 128u : 64u, (uint32_t)kLN};
+    const CUtensorMapDataType dt = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    spinf_status s;
+    if ((s = make_tmap(&tx, dt, 2, x, dx, st, bx, CU_TENSOR_MAP_SWIZZLE_128B))) return s;
+    if ((s = make_tmap(&tw, dt, 2, w, dw, st, bw, CU_TENSOR_MAP_SWIZZLE_128B))) return s;
+    static bool configured = false;
+    cudaError_t e;
+    if (!configured) {
+        e = cudaFuncSetAttribute(linear_kernel<FP8, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLSmem);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(linear)");
+        configured = true;
+    }
+    const int kbk = FP8 ? 128 : 64;
+    const int n_kb = (int)((K + kbk - 1) / kbk);
+    const int n_mt = (int)((rows + kLM - 1) / kLM), n_nt = (int)((N + kLN - 1) / kLN);
+    const int grid = std::min(n_mt * n_nt, sm_count());
+    linear_kernel<FP8, MODE><<<grid, kLThreads, kLSmem, stream>>>(tx, tw, w_scale, x_scale, out, (int)rows, (int)N,
+                                                                 n_kb, n_mt, n_nt, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "linear launch");
+    return SPINF_OK;
+}
+
+spinf_status check_dtype_args(int32_t w_dtype, const float* w_scale, float x_scale) {
+    if (w_dtype != SPINF_DTYPE_BF16 && w_dtype != SPINF_DTYPE_E4M3) return fail(SPINF_E_UNSUPPORTED, "w_dtype");
+    if (w_dtype == SPINF_DTYPE_E4M3 && (!w_scale || !(x_scale > 0.f) || !std::isfinite(x_scale)))
+        return fail(SPINF_E_INVALID, "e4m3 needs w_scale and a positive finite x_scale");
+    return SPINF_OK;
 }
 
 }  // namespace
@@ -79,55 +369,92 @@ extern "C" spinf_status spinf_rope_tree(const spinf_plan* plan, int32_t pass, vo
     if (!q || !k) return fail(SPINF_E_INVALID, "NULL tensor");
     if (n_q_heads <= 0 || n_kv_heads <= 0 || d_head <= 0 || d_head % 2 || d_head > 1024)
         return fail(SPINF_E_INVALID, "bad head counts or d_head");
-    if (!(theta > 1.f)) return fail(SPINF_E_INVALID, "theta must be > 1");
-    const Pass& P = plan->passes[pass];
+    if (!(theta > 1.f) || !std::isfinite(theta)) return fail(SPINF_E_INVALID, "theta must be > 1");
+    Pass& P = const_cast<Pass&>(plan->passes[pass]);
     if (P.T_pad == 0) return SPINF_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    rope_tree_kernel<<<P.T_pad, 256, d_head * sizeof(float), s>>>(static_cast<__nv_bfloat16*>(q),
-                                                                  static_cast<__nv_bfloat16*>(k), P.dev.pos,
-                                                                  n_q_heads, n_kv_heads, d_head,
-                                                                  std::log2(static_cast<double>(theta)));
+    const float2* table = nullptr;
+    if ((st = rope_table(P, d_head, theta, s, &table))) return st;
+    rope_tree_kernel<<<P.T_pad, 256, 0, s>>>(static_cast<__nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(k),
+                                             P.dev.pos, table, n_q_heads, n_kv_heads, d_head);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "rope launch");
     return SPINF_OK;
 }
 
-extern "C" spinf_status spinf_linear(const void* x, const void* w, void* y, int64_t rows, int64_t in_features,
+extern "C" spinf_status spinf_quantize_static(const void* x, float x_scale, void* codes, int64_t n,
+                                              spinf_stream stream) {
+    if (!x || !codes) return fail(SPINF_E_INVALID, "NULL tensor");
+    if (n < 0 || n % 8) return fail(SPINF_E_INVALID, "n must be a non-negative multiple of 8");
+    if (!(x_scale > 0.f) || !std::isfinite(x_scale)) return fail(SPINF_E_INVALID, "x_scale must be positive");
+    if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(codes) & 7))
+        return fail(SPINF_E_INVALID, "x must be 16-byte and codes 8-byte aligned");
+    if (n == 0) return SPINF_OK;
+    const int64_t n8 = n / 8;
+    const int grid = (int)std::min<int64_t>((n8 + 255) / 256, (int64_t)sm_count() * 8);
+    quantize_static_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const __nv_bfloat16*>(x), x_scale, static_cast<uint8_t*>(codes), n8);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    return SPINF_OK;
+}
+
+extern "C" spinf_status spinf_linear(const spinf_plan* plan, const void* x, const void* w, const float* w_scale,
+                                     float x_scale, int32_t w_dtype, void* y, int64_t rows, int64_t in_features,
                                      int64_t out_features, spinf_stream stream) {
+    if (!plan || !plan->d_err) return fail(SPINF_E_INVALID, "an uploaded plan is needed (its device error word)");
+    spinf_status st = check_dtype_args(w_dtype, w_scale, x_scale);
+    if (st) return st;
     if (!x || !w || !y) return fail(SPINF_E_INVALID, "NULL tensor");
-    if (rows < 0 || in_features <= 0 || out_features <= 0 || in_features % 8 || out_features % 8)
-        return fail(SPINF_E_INVALID, "bad sizes (features must be positive multiples of 8)");
+    const bool fp8 = w_dtype == SPINF_DTYPE_E4M3;
+    if (rows < 0 || rows > INT32_MAX || in_features <= 0 || in_features % (fp8 ? 16 : 8) || out_features <= 0 ||
+        out_features % 32 || out_features > INT32_MAX)
+        return fail(SPINF_E_INVALID, "bad sizes (in_features a multiple of 8, 16 for e4m3; out_features of 32)");
     for (const void* p : {x, w, (const void*)y})
         if (reinterpret_cast<uintptr_t>(p) & 15) return fail(SPINF_E_INVALID, "tensor not 16-byte aligned");
     if (rows == 0) return SPINF_OK;
-    int dev = 0;
-    cudaError_t ce = cudaGetDevice(&dev);
-    if (ce != cudaSuccess) return cuda_fail(ce, "cudaGetDevice");
-    cublasLtHandle_t h = lt_handle(dev);
-    if (!h) return fail(SPINF_E_CUDA, "cublasLtCreate failed");
-    // column-major view: Y^T[out, rows] = W[out, in] (row-major, i.e. W^T col-major, transposed) x X^T[in, rows]
-    cublasLtMatmulDesc_t op = nullptr;
-    cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
-    spinf_status st = SPINF_OK;
-    auto ok = [&](cublasStatus_t r, const char* what) {
-        if (r != CUBLAS_STATUS_SUCCESS && st == SPINF_OK) st = fail(SPINF_E_CUDA, std::string("cublasLt: ") + what);
-        return r == CUBLAS_STATUS_SUCCESS;
-    };
-    const cublasOperation_t ta = CUBLAS_OP_T, tb = CUBLAS_OP_N;
-    if (ok(cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F), "desc") &&
-        ok(cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &ta, sizeof ta), "transa") &&
-        ok(cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &tb, sizeof tb), "transb") &&
-        ok(cublasLtMatrixLayoutCreate(&la, CUDA_R_16BF, in_features, out_features, in_features), "layout a") &&
-        ok(cublasLtMatrixLayoutCreate(&lb, CUDA_R_16BF, in_features, rows, in_features), "layout b") &&
-        ok(cublasLtMatrixLayoutCreate(&lc, CUDA_R_16BF, out_features, rows, out_features), "layout c")) {
-        const float alpha = 1.f, beta = 0.f;
-        ok(cublasLtMatmul(h, op, &alpha, w, la, x, lb, &beta, y, lc, y, lc, nullptr, nullptr, 0,
-                          reinterpret_cast<cudaStream_t>(stream)),
-           "matmul");
-    }
-    if (lc) cublasLtMatrixLayoutDestroy(lc);
-    if (lb) cublasLtMatrixLayoutDestroy(lb);
-    if (la) cublasLtMatrixLayoutDestroy(la);
-    if (op) cublasLtMatmulDescDestroy(op);
-    return st;
+    LinearOut out{};
+    out.y[0] = static_cast<__nv_bfloat16*>(y);
+    out.ld[0] = (int)out_features;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (fp8) return launch_linear<true, 0>(x, w, w_scale, x_scale, out, rows, in_features, out_features, plan->d_err, s);
+    return launch_linear<false, 0>(x, w, nullptr, 1.f, out, rows, in_features, out_features, plan->d_err, s);
+}
+
+extern "C" spinf_status spinf_qkv_rope(const spinf_plan* plan, int32_t pass, const void* x, const void* w,
+                                       const float* w_scale, float x_scale, int32_t w_dtype, int32_t d_model,
+                                       int32_t n_q_heads, int32_t n_kv_heads, int32_t d_head, float theta, void* q,
+                                       void* k, void* v, spinf_stream stream) {
+    spinf_status st = ensure_device_ready(plan, pass);
+    if (st) return st;
+    if ((st = check_dtype_args(w_dtype, w_scale, x_scale))) return st;
+    if (!x || !w || !q || !k || !v) return fail(SPINF_E_INVALID, "NULL tensor");
+    const bool fp8 = w_dtype == SPINF_DTYPE_E4M3;
+    if (d_head != 64 && d_head != 128 && d_head != 256) return fail(SPINF_E_UNSUPPORTED, "d_head must be 64, 128 or 256");
+    if (n_q_heads <= 0 || n_kv_heads <= 0) return fail(SPINF_E_INVALID, "bad head counts");
+    if (d_model <= 0 || d_model % (fp8 ? 16 : 8)) return fail(SPINF_E_INVALID, "bad d_model");
+    if (!(theta > 1.f) || !std::isfinite(theta)) return fail(SPINF_E_INVALID, "theta must be > 1");
+    for (const void* p : {x, w, (const void*)q, (const void*)k, (const void*)v})
+        if (reinterpret_cast<uintptr_t>(p) & 15) return fail(SPINF_E_INVALID, "tensor not 16-byte aligned");
+    Pass& P = const_cast<Pass&>(plan->passes[pass]);
+    if (P.T_pad == 0) return SPINF_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const float2* table = nullptr;
+    if ((st = rope_table(P, d_head, theta, s, &table))) return st;
+    LinearOut out{};
+    out.y[0] = static_cast<__nv_bfloat16*>(q);
+    out.y[1] = static_cast<__nv_bfloat16*>(k);
+    out.y[2] = static_cast<__nv_bfloat16*>(v);
+    out.ld[0] = n_q_heads * d_head;
+    out.ld[1] = out.ld[2] = n_kv_heads * d_head;
+    out.base[0] = 0;
+    out.base[1] = n_q_heads * d_head;
+    out.base[2] = (n_q_heads + n_kv_heads) * d_head;
+    out.n_rot = out.base[2];
+    out.d = d_head;
+    out.cs = table;
+    out.pos = P.dev.pos;
+    const int64_t N = (int64_t)(n_q_heads + 2 * n_kv_heads) * d_head;
+    if (fp8) return launch_linear<true, 1>(x, w, w_scale, x_scale, out, P.T_pad, d_model, N, plan->d_err, s);
+    return launch_linear<false, 1>(x, w, nullptr, 1.f, out, P.T_pad, d_model, N, plan->d_err, s);
 }

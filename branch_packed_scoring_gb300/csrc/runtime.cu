@@ -258,6 +258,8 @@ extern "C" void spinf_plan_free(spinf_plan* plan) {
         if (P.dev.block && P.dev.owned) cudaFree(P.dev.block);
         for (auto& w : P.windows)
             if (w->block) cudaFree(w->block);
+        for (auto& r : P.ropes)
+            if (r->dev) cudaFree(r->dev);
     }
     if (plan->d_err && plan->err_owned) cudaFree(plan->d_err);
     delete plan;
@@ -266,5 +268,6 @@ extern "C" void spinf_plan_free(spinf_plan* plan) {
 extern "C" const char* spinf_fingerprint(void) {
     return "spinf-gb300 k1=branch_attention/tcgen05 q128xkv128 input-anchored fp32-acc bf16-p;"
            " k2=score/tcgen05 m128xv256xk64 fp32-acc lse-chunk256 fixed-order;"
-           " fp8=e4m3 row-absmax/448 rne-sat; sm_103a";
+           " fp8=e4m3 row-absmax/448 rne-sat;"
+           " lin=tcgen05 m128xn256 fixed-order, rope fp64-table fp32-rotate, fp8 static scales; sm_103a";
 }

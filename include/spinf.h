@@ -381,27 +381,51 @@ spinf_status spinf_collect_extract(const spinf_plan* plan, const int32_t* const*
  * SPINF_OK, SPINF_E_DEVICE_TIMEOUT or SPINF_E_DEVICE_CHECK (the word is cleared). */
 spinf_status spinf_device_status(const spinf_plan* plan, spinf_stream stream);
 
-/* ---- Around the attention call: the rest of a packed layer (QKV projection,
- * rotary positions, output projection) with synthetic or real weights. ---- */
+/* ---- Around the attention call: the rest of a packed layer (QKV projection with
+ * rotary positions, output projection) and the fp8 form of its linears. ---- */
 
 /* Rotary position embedding in place on q [T_pad, Hq, d] and k [T_pad, Hkv, d]
  * (bf16, device): row r's pairs (x[i], x[i + d/2]) turn by pos[r] * theta^(-2i/d),
  * pos[r] being the row's depth on its own root path (spinf_pass_info.pos), so a
  * branch token gets the position it has in its unpacked sequence ("spinf-serve
  * 0.1.1" PyPI, "What it does": branches of one pass, scores equal alone or packed).
- * Angles in fp64, rotation in fp32, bf16 round to nearest.  Pad rows have pos 0 (no
- * change).  Needs the pass uploaded; asynchronous on `stream`.  SPINF_E_INVALID for
- * NULL tensors, odd or > 1024 d_head, theta <= 1. */
+ * cos and sin come from a table formed in fp64 on the host and rounded to fp32 (one
+ * per pass and (d, theta), built at first use with a synchronous device allocation
+ * and kept by the plan); the rotation runs in fp32, bf16 round to nearest.  Pad rows
+ * have pos 0 (no change).  Needs the pass uploaded; asynchronous on `stream`.
+ * SPINF_E_INVALID for NULL tensors, odd or > 1024 d_head, theta <= 1. */
 spinf_status spinf_rope_tree(const spinf_plan* plan, int32_t pass, void* q, void* k, int32_t n_q_heads,
                              int32_t n_kv_heads, int32_t d_head, float theta, spinf_stream stream);
 
-/* y[rows, out] = x[rows, in] . w[out, in]^T: bf16 in and out, fp32 accumulation, all
- * row-major on the device (a plain cuBLASLt GEMM: the QKV and output projections of
- * a layer).  Features must be positive multiples of 8, pointers 16-byte aligned.
- * Asynchronous on `stream`.  The pages have no counterpart beyond "one packed
- * forward" (man page DESCRIPTION). */
-spinf_status spinf_linear(const void* x, const void* w, void* y, int64_t rows, int64_t in_features,
-                          int64_t out_features, spinf_stream stream);
+/* y[rows, out] = x[rows, in] . w[out, in]^T on the tensor cores (the output
+ * projection of a layer; "one packed forward", man page DESCRIPTION).
+ * w_dtype SPINF_DTYPE_BF16: x, w bf16.  SPINF_DTYPE_E4M3 (the static-scale fp8
+ * scheme, man page --quant fp8s): x and w are e4m3 codes, w_scale [out] fp32 per
+ * output channel, x_scale the static activation scale, and
+ * y = (acc * w_scale[o]) * x_scale.  Accumulation fp32, y bf16; all row-major on the
+ * device.  Each y element is one fixed-order reduction over `in`, so a row's output
+ * does not depend on the other rows.  `plan`: any uploaded plan (its device error
+ * word receives a bounded-wait timeout).  in_features a multiple of 8 (16 for e4m3),
+ * out_features of 32, pointers 16-byte aligned.  Asynchronous on `stream`. */
+spinf_status spinf_linear(const spinf_plan* plan, const void* x, const void* w, const float* w_scale, float x_scale,
+                          int32_t w_dtype, void* y, int64_t rows, int64_t in_features, int64_t out_features,
+                          spinf_stream stream);
+
+/* The QKV projection of one pass with the rotary embedding fused into its epilogue:
+ * [q | k | v] = x[T_pad, d_model] . w[(Hq + 2 Hkv) d, d_model]^T, then q and k turned
+ * as spinf_rope_tree does (from the fp32 product, before the one bf16 rounding), and
+ * q [T_pad, Hq, d], k, v [T_pad, Hkv, d] written in the layouts spinf_branch_attention
+ * reads.  Dtypes and scales as spinf_linear.  d_head in {64, 128, 256}.  Needs the pass
+ * uploaded; asynchronous on `stream`. */
+spinf_status spinf_qkv_rope(const spinf_plan* plan, int32_t pass, const void* x, const void* w, const float* w_scale,
+                            float x_scale, int32_t w_dtype, int32_t d_model, int32_t n_q_heads, int32_t n_kv_heads,
+                            int32_t d_head, float theta, void* q, void* k, void* v, spinf_stream stream);
+
+/* e4m3 codes of n bf16 values with a static scale: codes = e4m3(x / x_scale), the
+ * division in fp32, round to nearest even, saturating at +-448 (the activation side
+ * of the fp8s linears).  n a multiple of 8; x 16-byte, codes 8-byte aligned;
+ * x_scale > 0.  Asynchronous on `stream`. */
+spinf_status spinf_quantize_static(const void* x, float x_scale, void* codes, int64_t n, spinf_stream stream);
 
 /* Failure-path self-test: enqueue on `stream` a one-thread kernel that waits on a
  * barrier nothing arrives on, with the kernels' bounded wait shortened to `wait_ms`
