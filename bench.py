@@ -260,6 +260,7 @@ def run_ours(args, rank, world):
         plan.device_status(stream)
         attn_win_ms = statistics.mean(a.elapsed_time(b) for a, b in wev) * len(passes)
 
+    layer = None if args.no_layer else layer_timing(args, spinf, shape, plan, passes, dev, stream)
     extract = None if args.no_extract else extract_timing(args, spinf, sv, wl, inputs, shape, w, w_scale, w_dtype,
                                                           dev, stream)
 
@@ -313,6 +314,7 @@ def run_ours(args, rank, world):
         "kernel_ms_per_step": {"attention": attn_ms, "score": score_ms,
                                **({"attention_windowed": attn_win_ms, "window": shape.window} if attn_win_ms else {})},
         "searched_slots": extract,
+        "layer_projections": layer,
         "clocks": clk,
         "gpu_launches": 4 * len(passes) * args.steps,
         "e2e": e2e,
@@ -320,6 +322,87 @@ def run_ours(args, rank, world):
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args, inputs, shape, plan, passes, w, w_scale, budget_s=args.cpu_seconds)
     return out
+
+
+def layer_timing(args, spinf, shape, plan, passes, dev, stream):
+    """The projections around the attention call on every pass of the job (outside the
+    step): the QKV projection with the rotary turn fused (spinf_qkv_rope) and the output
+    projection (spinf_linear), bf16 and e4m3 with static scales, seeded random weights of
+    the workload's shapes.  Tensor-bound: 2 * T_pad * in * out FLOPs per call."""
+    import torch
+
+    Hq, Hkv, d, D = shape.n_q_heads, shape.n_kv_heads, shape.d_head, shape.d_model
+    n_qkv, n_o = (Hq + 2 * Hkv) * d, Hq * d
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    w_qkv = (torch.randn(n_qkv, D, generator=g, device=dev) / D ** 0.5).to(torch.bfloat16)
+    w_o = (torch.randn(D, n_o, generator=g, device=dev) / n_o ** 0.5).to(torch.bfloat16)
+
+    def e4m3(w):
+        s_w = (w.float().abs().amax(dim=1) / 448.0).clamp_min(1e-12)
+        return (w.float() / s_w[:, None]).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8), s_w
+
+    wq8, sq8 = e4m3(w_qkv)
+    wo8, so8 = e4m3(w_o)
+    x_scale, o_scale = 5.0 / 448, 4.0 / 448   # static activation scales (calibration stand-ins)
+    bufs = []
+    for pi, p in enumerate(passes):
+        Tp = p["info"].T_pad
+        x = torch.randn(Tp, D, generator=g, device=dev).to(torch.bfloat16)
+        bufs.append({"x": x, "x8": torch.empty(Tp, D, dtype=torch.uint8, device=dev),
+                     "o8": torch.empty(Tp, n_o, dtype=torch.uint8, device=dev),
+                     "q": torch.empty(Tp, Hq, d, dtype=torch.bfloat16, device=dev),
+                     "k": torch.empty(Tp, Hkv, d, dtype=torch.bfloat16, device=dev),
+                     "v": torch.empty(Tp, Hkv, d, dtype=torch.bfloat16, device=dev),
+                     "y": torch.empty(Tp, D, dtype=torch.bfloat16, device=dev)})
+    torch.cuda.synchronize()
+    reps = max(3, args.steps // 2)
+
+    def timed(fn):
+        for pi, b in enumerate(bufs):   # warm-up
+            fn(pi, b)
+        ev = []
+        for _ in range(reps):
+            for pi, b in enumerate(bufs):
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+                fn(pi, b)
+                a1.record(stream)
+                ev.append((a0, a1))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev) * len(bufs)
+
+    def qkv16(pi, b):
+        spinf.qkv_rope(plan, pi, b["x"], w_qkv, b["q"], b["k"], b["v"], Hq, Hkv, d, stream=stream)
+
+    def o16(pi, b):
+        spinf.linear(plan, b["q"].view(-1, n_o), w_o, b["y"], stream=stream)
+
+    def quant(pi, b):
+        spinf.quantize_static(b["x"], x_scale, b["x8"], stream=stream)
+
+    def qkv8(pi, b):
+        spinf.qkv_rope(plan, pi, b["x8"], wq8, b["q"], b["k"], b["v"], Hq, Hkv, d, w_scale=sq8, x_scale=x_scale,
+                       w_dtype=spinf.DTYPE_E4M3, stream=stream)
+
+    def o8(pi, b):
+        spinf.linear(plan, b["o8"], wo8, b["y"], w_scale=so8, x_scale=o_scale, w_dtype=spinf.DTYPE_E4M3,
+                     stream=stream)
+
+    with torch.cuda.stream(stream):
+        for b in bufs:   # the e4m3 output projection reads codes of the attention output's shape
+            spinf.quantize_static(b["q"].view(-1, n_o), o_scale, b["o8"], stream=stream)
+        ms = {"qkv_rope_bf16": timed(qkv16), "o_proj_bf16": timed(o16), "quantize_x": timed(quant),
+              "qkv_rope_e4m3": timed(qkv8), "o_proj_e4m3": timed(o8)}
+    plan.device_status(stream)
+    rows = sum(p["info"].T_pad for p in passes)
+    fl_qkv, fl_o = 2.0 * rows * D * n_qkv, 2.0 * rows * n_o * D
+    peaks, _ = _peaks()
+    bf16_peak = _peak_value(peaks, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"]
+    tf = {k: (fl_qkv if k.startswith("qkv") else fl_o) / (v * 1e-3) / 1e12 for k, v in ms.items() if k != "quantize_x"}
+    return {"shapes": f"rows {rows} (all passes), QKV {D}->{n_qkv}, O {n_o}->{D}",
+            "ms": ms, "tflops": tf,
+            "frac": {k: v / (bf16_peak * (2.0 if k.endswith("e4m3") else 1.0)) for k, v in tf.items()}}
 
 
 def extract_timing(args, spinf, sv, wl, inputs, shape, w, w_scale, w_dtype, dev, stream, n_slots=2):
@@ -651,6 +734,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extract", action="store_true", help="skip the searched-slot scoring timing")
+    ap.add_argument("--no-layer", action="store_true", help="skip the projection timing")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--ncu-case", choices=["score", "attention"], default=None,
                     help="run one boundary call on pass 0 only (small case for profiler captures)")

@@ -254,55 +254,84 @@ __global__ void __launch_bounds__(kLThreads, 1)
             mbar_wait(&bars[LACC_FULL0 + acc], (tcount >> 1) & 1, err);
             tc_fence_after();
             const uint32_t t0 = tmem + lane_off + acc * kLN;
-            auto load = [&](int c, float (&v)[32]) {   // product columns n0 + 32c .. + 31, scaled
-                uint32_t rr[32];
-                tmem_ld32(t0 + c * 32, rr);
+            // product columns n0 + 32c .. + 31 (< N) of the raw accumulator, scaled for e4m3
+            auto scale = [&](int c, const uint32_t (&rr)[32], float (&v)[32]) {
+                if constexpr (FP8) {
+                    // the chunk's 32 channel scales as 8 vector loads (N is a multiple of 32)
+                    const float4* ws4 = reinterpret_cast<const float4*>(w_scale + n0 + c * 32);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float x = __uint_as_float(rr[i]);
-                    if (FP8) {
-                        const int n = n0 + c * 32 + i;
-                        x = (x * (n < N ? __ldg(w_scale + n) : 0.f)) * x_scale;
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        const float4 sc = __ldg(ws4 + q4);
+                        v[4 * q4 + 0] = (__uint_as_float(rr[4 * q4 + 0]) * sc.x) * x_scale;
+                        v[4 * q4 + 1] = (__uint_as_float(rr[4 * q4 + 1]) * sc.y) * x_scale;
+                        v[4 * q4 + 2] = (__uint_as_float(rr[4 * q4 + 2]) * sc.z) * x_scale;
+                        v[4 * q4 + 3] = (__uint_as_float(rr[4 * q4 + 3]) * sc.w) * x_scale;
                     }
-                    v[i] = x;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(rr[i]);
                 }
             };
+            auto dest = [&](int n, int& col) {   // the output that holds column n (selects, no indexed array)
+                const int o = MODE == 0 ? 0 : n < out.base[1] ? 0 : n < out.base[2] ? 1 : 2;
+                col = n - (o == 0 ? out.base[0] : o == 1 ? out.base[1] : out.base[2]);
+                return (o == 0 ? out.y[0] : o == 1 ? out.y[1] : out.y[2]) +
+                       (size_t)row * (o == 0 ? out.ld[0] : o == 1 ? out.ld[1] : out.ld[2]);
+            };
+            const int half = MODE == 1 ? out.d / 2 : 0;
 #pragma unroll 1
             for (int c = 0; c < kLN / 32; ++c) {
                 const int n = n0 + c * 32;
                 if (n >= N) break;
-                if constexpr (MODE == 0) {
-                    float v[32];
-                    load(c, v);
-                    if (valid) store_bf16x32(out.y[0] + (size_t)row * out.ld[0] + n, v);
-                } else {
-                    // the output that holds column n (selects, not an indexed parameter array)
-                    const int o = n < out.base[1] ? 0 : n < out.base[2] ? 1 : 2;
-                    const int col = n - (o == 0 ? out.base[0] : o == 1 ? out.base[1] : out.base[2]);
-                    __nv_bfloat16* dst = (o == 0 ? out.y[0] : o == 1 ? out.y[1] : out.y[2]) +
-                                         (size_t)row * (o == 0 ? out.ld[0] : o == 1 ? out.ld[1] : out.ld[2]);
-                    if (n >= out.n_rot) {   // v: no turn
-                        float v[32];
-                        load(c, v);
-                        if (valid) store_bf16x32(dst + col, v);
-                        continue;
-                    }
-                    const int half = out.d / 2, j = col % out.d;
+                if (MODE == 1 && n < out.n_rot) {   // q or k: chunk c and its partner half a head later
+                    int col;
+                    __nv_bfloat16* dst = dest(n, col);
+                    const int j = col % out.d;
                     if (j >= half) continue;   // written with its first half
+                    float4 tab[16];            // (cos, sin) pairs, fetched before the TMEM wait
+                    if (valid) {
+                        const float4* cs4 = reinterpret_cast<const float4*>(cs + j);
+#pragma unroll
+                        for (int i2 = 0; i2 < 16; ++i2) tab[i2] = __ldg(cs4 + i2);
+                    }
+                    uint32_t ra[32], rb[32];
+                    tmem_ld32x2(t0 + c * 32, t0 + (c + half / 32) * 32, ra, rb);
                     float x0[32], x1[32];
-                    load(c, x0);
-                    load(c + half / 32, x1);
+                    scale(c, ra, x0);
+                    scale(c + half / 32, rb, x1);
                     if (valid) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float2 t = __ldg(cs + j + i);
-                            const float a = x0[i], b = x1[i];
+                        for (int i2 = 0; i2 < 16; ++i2) {
+                            const float4 t = tab[i2];
+                            const int i = 2 * i2;
+                            float a = x0[i], b = x1[i];
                             x0[i] = a * t.x - b * t.y;
                             x1[i] = b * t.x + a * t.y;
+                            a = x0[i + 1];
+                            b = x1[i + 1];
+                            x0[i + 1] = a * t.z - b * t.w;
+                            x1[i + 1] = b * t.z + a * t.w;
                         }
                         store_bf16x32(dst + col, x0);
                         store_bf16x32(dst + col + half, x1);
                     }
+                    continue;
+                }
+                // no turn: this chunk and (when it is not a turned one) the next, one TMEM wait
+                const bool two = c + 1 < kLN / 32 && n + 32 < N && !(MODE == 1 && n + 32 < out.n_rot);
+                uint32_t ra[32], rb[32];
+                if (two) tmem_ld32x2(t0 + c * 32, t0 + (c + 1) * 32, ra, rb);
+                else tmem_ld32(t0 + c * 32, ra);
+                float v[32];
+                scale(c, ra, v);
+                int col;
+                __nv_bfloat16* dst = dest(n, col);
+                if (valid) store_bf16x32(dst + col, v);
+                if (two) {
+                    scale(c + 1, rb, v);
+                    __nv_bfloat16* dst1 = dest(n + 32, col);
+                    if (valid) store_bf16x32(dst1 + col, v);
+                    ++c;
                 }
             }
             tc_fence_before();
@@ -354,6 +383,8 @@ spinf_status check_dtype_args(int32_t w_dtype, const float* w_scale, float x_sca
     if (w_dtype != SPINF_DTYPE_BF16 && w_dtype != SPINF_DTYPE_E4M3) return fail(SPINF_E_UNSUPPORTED, "w_dtype");
     if (w_dtype == SPINF_DTYPE_E4M3 && (!w_scale || !(x_scale > 0.f) || !std::isfinite(x_scale)))
         return fail(SPINF_E_INVALID, "e4m3 needs w_scale and a positive finite x_scale");
+    if (w_dtype == SPINF_DTYPE_E4M3 && (reinterpret_cast<uintptr_t>(w_scale) & 15))
+        return fail(SPINF_E_INVALID, "w_scale must be 16-byte aligned");
     return SPINF_OK;
 }
 

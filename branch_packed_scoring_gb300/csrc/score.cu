@@ -320,12 +320,26 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 const int vc = v0 + c * 32;
                 float z[32];
                 float cmax = -INFINITY;
+                if (FP8 && vc + 32 <= V) {   // a whole chunk inside the vocabulary: 8 vector scale loads
+                    const float4* sw4 = reinterpret_cast<const float4*>(s_w + vc);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float x = __uint_as_float(rr[i]);
-                    if (FP8) x = (x * (vc + i < V ? s_w[vc + i] : 0.f)) * sa;
-                    z[i] = vc + i < V ? x : -INFINITY;
-                    cmax = fmaxf(cmax, z[i]);
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        const float4 sc = __ldg(sw4 + q4);
+                        z[4 * q4 + 0] = (__uint_as_float(rr[4 * q4 + 0]) * sc.x) * sa;
+                        z[4 * q4 + 1] = (__uint_as_float(rr[4 * q4 + 1]) * sc.y) * sa;
+                        z[4 * q4 + 2] = (__uint_as_float(rr[4 * q4 + 2]) * sc.z) * sa;
+                        z[4 * q4 + 3] = (__uint_as_float(rr[4 * q4 + 3]) * sc.w) * sa;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) cmax = fmaxf(cmax, z[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        float x = __uint_as_float(rr[i]);
+                        if (FP8) x = (x * (vc + i < V ? s_w[vc + i] : 0.f)) * sa;
+                        z[i] = vc + i < V ? x : -INFINITY;
+                        cmax = fmaxf(cmax, z[i]);
+                    }
                 }
                 const float nm = fmaxf(mx, cmax);
                 float add = 0.f;
@@ -581,6 +595,8 @@ extern "C" spinf_status spinf_score_extract(const spinf_plan* plan, int32_t pass
     if (P.slot_row.empty()) return SPINF_OK;
     if (!hidden || !w || !row_lse || !token_lp || !workspace) return fail(SPINF_E_INVALID, "NULL buffer");
     if (w_dtype == SPINF_DTYPE_E4M3 && !w_scale) return fail(SPINF_E_INVALID, "e4m3 weights need w_scale");
+    if (w_dtype == SPINF_DTYPE_E4M3 && (reinterpret_cast<uintptr_t>(w_scale) & 15))
+        return fail(SPINF_E_INVALID, "w_scale must be 16-byte aligned");
     for (const void* p : {hidden, w, (const void*)workspace})
         if (reinterpret_cast<uintptr_t>(p) & 15) return fail(SPINF_E_INVALID, "buffer not 16-byte aligned");
     for (int32_t t : P.gather_tok)
@@ -674,6 +690,8 @@ extern "C" spinf_status spinf_score_static(const spinf_plan* plan, int32_t pass,
                                        " (use spinf_score with a caller workspace)");
     if (!hidden || !w || !row_lse || !token_lp) return fail(SPINF_E_INVALID, "NULL buffer");
     if (w_dtype == SPINF_DTYPE_E4M3 && !w_scale) return fail(SPINF_E_INVALID, "e4m3 weights need w_scale");
+    if (w_dtype == SPINF_DTYPE_E4M3 && (reinterpret_cast<uintptr_t>(w_scale) & 15))
+        return fail(SPINF_E_INVALID, "w_scale must be 16-byte aligned");
     for (const void* p : {hidden, w})
         if (reinterpret_cast<uintptr_t>(p) & 15) return fail(SPINF_E_INVALID, "buffer not 16-byte aligned");
     for (int32_t t : P.gather_tok)

@@ -293,7 +293,7 @@ size_t spinf_score_workspace_bytes(const spinf_plan* plan, int32_t pass,
  * nearest even, saturating), and z = scale_row * w_scale[v] * (codes . codes).
  *
  * hidden: device [T_pad, d_model] bf16; w: device [vocab, d_model] bf16 or e4m3;
- * w_scale: device [vocab] fp32 (NULL for bf16); row_lse: device [M] fp32;
+ * w_scale: device [vocab] fp32, 16-byte aligned (NULL for bf16); row_lse: device [M] fp32;
  * token_lp: device [G] fp32; workspace: device, >= spinf_score_workspace_bytes.
  * d_model a multiple of 16.  The vocabulary is reduced in a fixed chunk order,
  * so results do not depend on M or on the other rows of the pass.
