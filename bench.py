@@ -39,7 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one score_main_kernel launch, from one ncu capture of the
 # Wikinews-shaped pass 0 with the bf16 lm head (2.020 GB read = the head once, 9.1 MB written).
 # Keyed by (workload, fp8); any other case reports null.
-NCU_SCORE_TRAFFIC = {("wikinews", False): 2.020e9 + 9.1e6}
+NCU_SCORE_TRAFFIC = {("wikinews", False): 2020407040 + 9282560}
 
 
 def _peaks():
@@ -695,7 +695,27 @@ def run_ncu_case(args):
     keys = sv.path_keys(info.tok, info.parent, info.T)
     plan.upload(0)
     w_dtype = spinf.DTYPE_E4M3 if args.fp8 else spinf.DTYPE_BF16
-    if args.ncu_case == "attention":
+    if args.ncu_case == "qkv":   # the fused QKV projection + rotary of pass 0, seeded random inputs
+        Hq, Hkv, d, D = shape.n_q_heads, shape.n_kv_heads, shape.d_head, shape.d_model
+        g = torch.Generator(device=dev)
+        g.manual_seed(7)
+        x = torch.randn(info.T_pad, D, generator=g, device=dev).to(torch.bfloat16)
+        w = (torch.randn((Hq + 2 * Hkv) * d, D, generator=g, device=dev) / D ** 0.5).to(torch.bfloat16)
+        q = torch.empty(info.T_pad, Hq, d, dtype=torch.bfloat16, device=dev)
+        k = torch.empty(info.T_pad, Hkv, d, dtype=torch.bfloat16, device=dev)
+        v = torch.empty_like(k)
+        kw = {}
+        if args.fp8:
+            s_w = (w.float().abs().amax(dim=1) / 448.0).clamp_min(1e-12)
+            w = (w.float() / s_w[:, None]).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+            x8 = torch.empty(info.T_pad, D, dtype=torch.uint8, device=dev)
+            spinf.quantize_static(x, 5.0 / 448, x8)
+            x = x8
+            kw = {"w_scale": s_w, "x_scale": 5.0 / 448, "w_dtype": spinf.DTYPE_E4M3}
+
+        def call():
+            spinf.qkv_rope(plan, 0, x, w, q, k, v, Hq, Hkv, d, **kw)
+    elif args.ncu_case == "attention":
         q, k, v = (t.to(dev) for t in sv.qkv(keys, info.T_pad, shape.n_q_heads, shape.n_kv_heads, shape.d_head))
         o = torch.empty_like(q)
 
@@ -736,7 +756,7 @@ def main():
     ap.add_argument("--no-extract", action="store_true", help="skip the searched-slot scoring timing")
     ap.add_argument("--no-layer", action="store_true", help="skip the projection timing")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
-    ap.add_argument("--ncu-case", choices=["score", "attention"], default=None,
+    ap.add_argument("--ncu-case", choices=["score", "attention", "qkv"], default=None,
                     help="run one boundary call on pass 0 only (small case for profiler captures)")
     ap.add_argument("--window", type=int, default=0)
     args = ap.parse_args()
