@@ -46,10 +46,11 @@ struct WindowSchedule {
     std::vector<unsigned char> staging;
 };
 
-// cos and sin of the rotary angles of one pass for one (d_head, theta): [max pos + 1][d / 2]
+// cos and sin of the rotary angles of one pass for one (d_head, theta): [d / 2][max pos + 1]
 // (built on first use, plan-owned device copy).
 struct RopeTable {
     int32_t d = 0;
+    int32_t stride = 0;   // max pos + 1
     float theta = 0.f;
     std::vector<float2> host;
     float2* dev = nullptr;

@@ -49,11 +49,14 @@ using namespace dev;
 // ---------------------------------------------------------------- rotary table
 // cos and sin of pos * theta^(-2i/d) for every pos of the pass (0..max pos), i < d/2,
 // formed in fp64 on the host and rounded to fp32: the fused projection and the
-// stand-alone rotation read the same values.
-spinf_status rope_table(Pass& P, int32_t d, float theta, cudaStream_t stream, const float2** out) {
+// stand-alone rotation read the same values.  Frequency-major ([i][pos], `stride` =
+// max pos + 1): the rows of a tile mostly hold consecutive positions (a content, a
+// template), so one warp load of a frequency touches one or two lines.
+spinf_status rope_table(Pass& P, int32_t d, float theta, cudaStream_t stream, const float2** out, int* stride) {
     for (auto& t : P.ropes)
         if (t->d == d && t->theta == theta && t->dev) {
             *out = t->dev;
+            *stride = t->stride;
             return SPINF_OK;
         }
     auto t = std::make_unique<RopeTable>();
@@ -62,13 +65,15 @@ spinf_status rope_table(Pass& P, int32_t d, float theta, cudaStream_t stream, co
     int32_t max_pos = 0;
     for (int32_t r = 0; r < P.T_pad; ++r) max_pos = std::max(max_pos, P.pos[r]);
     const int32_t half = d / 2;
-    t->host.resize((size_t)(max_pos + 1) * half);
+    t->stride = max_pos + 1;
+    t->host.resize((size_t)t->stride * half);
     const double lt = std::log2(static_cast<double>(theta));
     for (int32_t i = 0; i < half; ++i) {
         const double inv_freq = std::exp2(-lt * (2.0 * i) / d);
         for (int32_t p = 0; p <= max_pos; ++p) {
             const double a = p * inv_freq;
-            t->host[(size_t)p * half + i] = make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
+            t->host[(size_t)i * t->stride + p] =
+                make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
         }
     }
     void* mem = nullptr;
@@ -81,16 +86,17 @@ spinf_status rope_table(Pass& P, int32_t d, float theta, cudaStream_t stream, co
     }
     t->dev = static_cast<float2*>(mem);
     *out = t->dev;
+    *stride = t->stride;
     P.ropes.push_back(std::move(t));
     return SPINF_OK;
 }
 
 // One CTA per packed row; the row's table entries are shared by its heads.
 __global__ void rope_tree_kernel(__nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ k,
-                                 const int32_t* __restrict__ pos, const float2* __restrict__ table, int Hq, int Hkv,
-                                 int d) {
+                                 const int32_t* __restrict__ pos, const float2* __restrict__ table, int stride,
+                                 int Hq, int Hkv, int d) {
     const int row = blockIdx.x, half = d / 2;
-    const float2* cs = table + (size_t)__ldg(pos + row) * half;
+    const float2* cs = table + __ldg(pos + row);   // entry i at cs[i * stride]
     const int pairs_q = Hq * half, pairs = (Hq + Hkv) * half;
     for (int j = threadIdx.x; j < pairs; j += blockDim.x) {
         const bool is_q = j < pairs_q;
@@ -99,7 +105,7 @@ __global__ void rope_tree_kernel(__nv_bfloat16* __restrict__ q, __nv_bfloat16* _
         __nv_bfloat16* base = is_q ? q + (static_cast<size_t>(row) * Hq + h) * d
                                    : k + (static_cast<size_t>(row) * Hkv + h) * d;
         const float x0 = __bfloat162float(base[i]), x1 = __bfloat162float(base[i + half]);
-        const float2 r = __ldg(cs + i);
+        const float2 r = __ldg(cs + (size_t)i * stride);
         base[i] = __float2bfloat16_rn(x0 * r.x - x1 * r.y);
         base[i + half] = __float2bfloat16_rn(x1 * r.x + x0 * r.y);
     }
@@ -147,7 +153,8 @@ struct LinearOut {
     int base[3];
     int n_rot;
     int d;
-    const float2* cs;      // [max pos + 1][d / 2]
+    const float2* cs;      // [d / 2][stride] (cos, sin), frequency-major
+    int stride;            // max pos + 1
     const int32_t* pos;    // [rows]
 };
 
@@ -276,7 +283,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
             const int n0 = nt * kLN;
             const bool valid = row < rows;
             const float2* cs = nullptr;
-            if (MODE == 1 && valid) cs = out.cs + (size_t)__ldg(out.pos + row) * (out.d / 2);
+            if (MODE == 1 && valid) cs = out.cs + __ldg(out.pos + row);   // entry i at cs[i * stride]
             mbar_wait(&bars[LACC_FULL0 + acc], (tcount >> 1) & 1, err);
             tc_fence_after();
             const uint32_t t0 = tmem + lane_off + acc * kLN;
@@ -314,11 +321,11 @@ __global__ void __launch_bounds__(kLThreads, 1)
                     __nv_bfloat16* dst = dest(n, col);
                     const int j = col % out.d;
                     if (j >= half) continue;   // written with its first half
-                    float4 tab[16];            // (cos, sin) pairs, fetched before the TMEM wait
+                    float2 tab[32];            // (cos, sin), fetched before the TMEM wait
                     if (valid) {
-                        const float4* cs4 = reinterpret_cast<const float4*>(cs + j);
+                        const float2* c0 = cs + (size_t)j * out.stride;
 #pragma unroll
-                        for (int i2 = 0; i2 < 16; ++i2) tab[i2] = __ldg(cs4 + i2);
+                        for (int i = 0; i < 32; ++i) tab[i] = __ldg(c0 + (size_t)i * out.stride);
                     }
                     uint32_t ra[32], rb[32];
                     tmem_ld32x2(t0 + c * 32, t0 + (c + half / 32) * 32, ra, rb);
@@ -327,16 +334,10 @@ __global__ void __launch_bounds__(kLThreads, 1)
                     scale(c + half / 32, rb, x1);
                     if (valid) {
 #pragma unroll
-                        for (int i2 = 0; i2 < 16; ++i2) {
-                            const float4 t = tab[i2];
-                            const int i = 2 * i2;
-                            float a = x0[i], b = x1[i];
-                            x0[i] = a * t.x - b * t.y;
-                            x1[i] = b * t.x + a * t.y;
-                            a = x0[i + 1];
-                            b = x1[i + 1];
-                            x0[i + 1] = a * t.z - b * t.w;
-                            x1[i + 1] = b * t.z + a * t.w;
+                        for (int i = 0; i < 32; ++i) {
+                            const float a = x0[i], b = x1[i];
+                            x0[i] = a * tab[i].x - b * tab[i].y;
+                            x1[i] = b * tab[i].x + a * tab[i].y;
                         }
                         store_bf16x32(dst + col, x0);
                         store_bf16x32(dst + col + half, x1);
@@ -460,9 +461,10 @@ extern "C" spinf_status spinf_rope_tree(const spinf_plan* plan, int32_t pass, vo
     if (P.T_pad == 0) return SPINF_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const float2* table = nullptr;
-    if ((st = rope_table(P, d_head, theta, s, &table))) return st;
+    int stride = 0;
+    if ((st = rope_table(P, d_head, theta, s, &table, &stride))) return st;
     rope_tree_kernel<<<P.T_pad, 256, 0, s>>>(static_cast<__nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(k),
-                                             P.dev.pos, table, n_q_heads, n_kv_heads, d_head);
+                                             P.dev.pos, table, stride, n_q_heads, n_kv_heads, d_head);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "rope launch");
     return SPINF_OK;
@@ -526,7 +528,8 @@ extern "C" spinf_status spinf_qkv_rope(const spinf_plan* plan, int32_t pass, con
     if (P.T_pad == 0) return SPINF_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const float2* table = nullptr;
-    if ((st = rope_table(P, d_head, theta, s, &table))) return st;
+    int stride = 0;
+    if ((st = rope_table(P, d_head, theta, s, &table, &stride))) return st;
     LinearOut out{};
     out.y[0] = static_cast<__nv_bfloat16*>(q);
     out.y[1] = static_cast<__nv_bfloat16*>(k);
@@ -539,6 +542,7 @@ extern "C" spinf_status spinf_qkv_rope(const spinf_plan* plan, int32_t pass, con
     out.n_rot = out.base[2];
     out.d = d_head;
     out.cs = table;
+    out.stride = stride;
     out.pos = P.dev.pos;
     const int64_t N = (int64_t)(n_q_heads + 2 * n_kv_heads) * d_head;
     if (fp8) return launch_linear<true, 1>(x, w, w_scale, x_scale, out, P.T_pad, d_model, N, plan->d_err, s);
