@@ -809,13 +809,9 @@ spinf_status launch_mode(const Pass& P, const Sched& sc, const CUtensorMap& tq, 
                          int* err, cudaStream_t stream) {
     auto kernel = branch_attention_kernel<D, MODE>;
     const int smem = AttnSmem<D, MODE>::kAlloc > kMinSmem ? AttnSmem<D, MODE>::kAlloc : kMinSmem;
-    static bool configured = false;
+    spinf_status st = set_smem_limit(reinterpret_cast<const void*>(kernel), smem, "cudaFuncSetAttribute(attention)");
+    if (st) return st;
     cudaError_t e;
-    if (!configured) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
-        configured = true;
-    }
     const int heads_per_item = MODE == 0 ? 1 : 2;
     const int n_items = (P.T_pad / 128) * (Hq / heads_per_item);
     if (MODE == 0) {

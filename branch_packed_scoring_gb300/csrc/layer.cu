@@ -389,13 +389,10 @@ spinf_status launch_linear_impl(const void* x, const void* w, const float* w_sca
     spinf_status s;
     if ((s = make_tmap(&tx, dt, 2, x, dx, st, bx, CU_TENSOR_MAP_SWIZZLE_128B))) return s;
     if ((s = make_tmap(&tw, dt, 2, w, dw, st, bw, CU_TENSOR_MAP_SWIZZLE_128B))) return s;
-    static bool configured = false;
+    if ((s = set_smem_limit(reinterpret_cast<const void*>(linear_kernel<FP8, MODE, PAIR>), kLSmem,
+                            "cudaFuncSetAttribute(linear)")))
+        return s;
     cudaError_t e;
-    if (!configured) {
-        e = cudaFuncSetAttribute(linear_kernel<FP8, MODE, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLSmem);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(linear)");
-        configured = true;
-    }
     const int kbk = FP8 ? 128 : 64;
     const int n_kb = (int)((K + kbk - 1) / kbk);
     const int n_mt = (int)((rows + kLM - 1) / kLM), n_nt = (int)((N + kLN - 1) / kLN);

@@ -6,6 +6,8 @@
 
 #include <cstring>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -87,6 +89,21 @@ spinf_status upload_window(WindowSchedule& w, cudaStream_t stream) {
         return cuda_fail(e, "window schedule upload");
     }
     w.block = block;
+    return SPINF_OK;
+}
+
+spinf_status set_smem_limit(const void* kernel, int bytes, const char* what) {
+    static std::mutex mu;
+    static std::vector<std::pair<int, const void*>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lock(mu);
+    for (const auto& d : done)
+        if (d.first == dev && d.second == kernel) return SPINF_OK;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    done.emplace_back(dev, kernel);
     return SPINF_OK;
 }
 

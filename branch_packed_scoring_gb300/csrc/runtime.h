@@ -21,6 +21,11 @@ spinf_status ensure_device_ready(const spinf_plan* plan, int32_t pass);
 
 int sm_count();
 
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current device, once per
+// (device, kernel): the attribute belongs to a device context, so a process that drives
+// several GPUs sets it on each.  Thread-safe.
+spinf_status set_smem_limit(const void* kernel, int bytes, const char* what);
+
 // Device copies of a windowed schedule (allocated and copied on `stream` on first use).
 spinf_status upload_window(WindowSchedule& w, cudaStream_t stream);
 

@@ -540,13 +540,9 @@ spinf_status launch_score(const Pass& P, const ScoreLayout& L, const void* hidde
     spinf_status s;
     if ((s = make_tmap(&th, dt, 2, hs, dh, st, bh, CU_TENSOR_MAP_SWIZZLE_128B))) return s;
     if ((s = make_tmap(&tw, dt, 2, w, dw, st, bw, CU_TENSOR_MAP_SWIZZLE_128B))) return s;
-    static bool configured = false;
-    if (!configured) {
-        e = cudaFuncSetAttribute(score_main_kernel<FP8, KX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 KX ? kScoreSmemX : kScoreSmem);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(score)");
-        configured = true;
-    }
+    if ((s = set_smem_limit(reinterpret_cast<const void*>(score_main_kernel<FP8, KX>), KX ? kScoreSmemX : kScoreSmem,
+                            "cudaFuncSetAttribute(score)")))
+        return s;
     const int kbk = FP8 ? 128 : 64;
     const int n_kb = (D + kbk - 1) / kbk;
     const int total = L.n_vt * L.n_st;
