@@ -49,6 +49,12 @@ def seq_keys(tokens, seed=0):
     return keys
 
 
+def extend_key(key, token):
+    """Key of a row whose token ``token`` follows the row with key ``key`` on a root path
+    (a decoded token appended to a searched slot's path)."""
+    return _mix(int(key), int(token))
+
+
 def normal_rows(keys, stream, n):
     """``[len(keys), n]`` fp32 N(0, 1) values, one Philox stream per distinct key."""
     out = np.empty((len(keys), n), dtype=np.float32)
