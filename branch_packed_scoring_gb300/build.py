@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspinf.so")
-SOURCES = ["plan.cpp", "runtime.cu", "attention.cu", "score.cu", "layer.cu"]
+SOURCES = ["plan.cpp", "runtime.cu", "attention.cu", "score.cu", "layer.cu", "decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -634,6 +634,99 @@ extern "C" spinf_status spinf_score(const spinf_plan* plan, int32_t pass, const 
                                workspace, workspace_bytes, stream);
 }
 
+// ---------------------------------------------------------------- rows outside a plan
+// Scoring of caller-given hidden rows (the decode rows of searched slots): the rows are
+// the scoring rows, every row is searched.  The row tables that a pass would hold
+// (identity row maps, empty gather lists, token sets) are built on the host and copied to
+// the front of the workspace; the scoring kernels then run as for a pass.
+namespace spinf {
+namespace {
+
+struct RowsView {
+    Pass P;
+    size_t index_bytes = 0;
+};
+
+void rows_view(RowsView& rv, int32_t n, const int32_t* token_set) {
+    Pass& P = rv.P;
+    P.slot_row.resize(n);
+    P.x_m.resize(n);
+    P.row_x.resize(n);
+    P.x_set.resize(n);
+    for (int32_t i = 0; i < n; ++i) {
+        P.slot_row[i] = P.x_m[i] = P.row_x[i] = i;
+        P.x_set[i] = token_set ? token_set[i] : -1;
+    }
+    P.row_gptr.assign(n + 1, 0);
+    rv.index_bytes = align256((size_t)n * 4) * 4 + align256((size_t)(n + 1) * 4);
+}
+
+}  // namespace
+}  // namespace spinf
+
+extern "C" size_t spinf_score_rows_workspace_bytes(int32_t n_rows, int32_t vocab, int32_t d_model, int32_t w_dtype,
+                                                   int32_t k) {
+    if (n_rows <= 0 || vocab <= 0 || d_model <= 0 || k < 1 || k > 16) return 0;
+    RowsView rv;
+    rows_view(rv, n_rows, nullptr);
+    return rv.index_bytes + score_layout(rv.P, vocab, d_model, w_dtype, k).total;
+}
+
+extern "C" spinf_status spinf_score_rows(const spinf_plan* plan, const void* hidden, int32_t n_rows, const void* w,
+                                         const float* w_scale, int32_t w_dtype, int32_t d_model, int32_t vocab,
+                                         const int32_t* token_set, const uint32_t* token_sets, int32_t n_sets,
+                                         int32_t k, float* row_lse, int32_t* top_tok, float* top_lp, void* workspace,
+                                         size_t workspace_bytes, spinf_stream stream) {
+    if (!plan || !plan->d_err) return fail(SPINF_E_INVALID, "an uploaded plan is needed (its device error word)");
+    if (w_dtype != SPINF_DTYPE_BF16 && w_dtype != SPINF_DTYPE_E4M3) return fail(SPINF_E_UNSUPPORTED, "w_dtype");
+    if (d_model <= 0 || d_model % 16) return fail(SPINF_E_UNSUPPORTED, "d_model must be a positive multiple of 16");
+    if (vocab <= 0) return fail(SPINF_E_INVALID, "vocab must be positive");
+    if (k < 1 || k > 16) return fail(SPINF_E_INVALID, "k must be in 1..16");
+    if (n_rows < 0) return fail(SPINF_E_INVALID, "negative row count");
+    if (n_rows == 0) return SPINF_OK;
+    if (!hidden || !w || !row_lse || !top_tok || !top_lp || !workspace) return fail(SPINF_E_INVALID, "NULL buffer");
+    if (w_dtype == SPINF_DTYPE_E4M3 && (!w_scale || (reinterpret_cast<uintptr_t>(w_scale) & 15)))
+        return fail(SPINF_E_INVALID, "e4m3 weights need a 16-byte aligned w_scale");
+    for (const void* p : {hidden, w, (const void*)workspace})
+        if (reinterpret_cast<uintptr_t>(p) & 15) return fail(SPINF_E_INVALID, "buffer not 16-byte aligned");
+    if (token_set)
+        for (int32_t i = 0; i < n_rows; ++i)
+            if (token_set[i] < -1 || token_set[i] >= n_sets || (token_set[i] >= 0 && !token_sets))
+                return fail(SPINF_E_INVALID, "a row names an unknown token set");
+    RowsView rv;
+    rows_view(rv, n_rows, token_set);
+    Pass& P = rv.P;
+    const ScoreLayout L = score_layout(P, vocab, d_model, w_dtype, k);
+    if (workspace_bytes < rv.index_bytes + L.total) return fail(SPINF_E_NOMEM, "workspace too small");
+    // the row tables at the front of the workspace (pageable sources: staged before return)
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const std::vector<int32_t>* src[5] = {&P.slot_row, &P.row_x, &P.x_m, &P.x_set, &P.row_gptr};
+    int32_t** dst[5] = {&P.dev.slot_row, &P.dev.row_x, &P.dev.x_m, &P.dev.x_set, &P.dev.row_gptr};
+    size_t off = 0;
+    for (int a = 0; a < 5; ++a) {
+        *dst[a] = reinterpret_cast<int32_t*>(base + off);
+        cudaError_t e = cudaMemcpyAsync(base + off, src[a]->data(), src[a]->size() * 4, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "row table upload");
+        off += align256(src[a]->size() * 4);
+    }
+    P.dev.row_glist = P.dev.row_gptr;    // no gathers: never read
+    P.dev.gather_tok = P.dev.row_gptr;
+    spinf_extract_out ex{token_sets, n_sets, top_tok, top_lp};
+    uint8_t* ws = base + rv.index_bytes;
+    const float* wsc = w_dtype == SPINF_DTYPE_E4M3 ? w_scale : nullptr;
+    using F = std::false_type;
+    using T = std::true_type;
+    auto go = [&](auto fp8, auto kx_c) {
+        return launch_score<decltype(fp8)::value, decltype(kx_c)::value>(P, L, hidden, w, wsc, d_model, vocab, row_lse,
+                                                                         nullptr, &ex, ws, plan->d_err, s);
+    };
+    using K8 = std::integral_constant<int, 8>;
+    using K16 = std::integral_constant<int, 16>;
+    if (w_dtype == SPINF_DTYPE_E4M3) return k <= 8 ? go(T{}, K8{}) : go(T{}, K16{});
+    return k <= 8 ? go(F{}, K8{}) : go(F{}, K16{});
+}
+
 // ---------------------------------------------------------------- allocation-free variant
 // For callers that may not allocate device memory: the scratch of the scoring
 // kernels lives in one file-scope device array per GPU.  Host code must not use

@@ -332,6 +332,53 @@ spinf_status spinf_score_extract(const spinf_plan* plan, int32_t pass,
                                  float* row_lse, float* token_lp, const spinf_extract_out* ex,
                                  void* workspace, size_t workspace_bytes, spinf_stream stream);
 
+/* ---- Decoding steps of searched slots on the pass's cached keys and values. ---- */
+
+/* Bytes of device workspace spinf_decode_attention needs for n_q query rows. */
+size_t spinf_decode_workspace_bytes(int32_t n_q);
+
+/* Attention of decode rows of searched slots ("spinf-serve 0.1.1" PyPI, "What it does"
+ * and "Speed and scale": extraction slots are decoded on the same read, the content and
+ * the questions are not read again).  Decode row r extends the root path of pass row
+ * anchor[r] (a searched slot's row) by the tokens of its chain: parent[r] is an earlier
+ * decode row of the same chain (same anchor), or < 0 for the chain's first token.  Row r
+ * attends to the keys anchor[r] sees in the pass (k_pass, v_pass: the pass's
+ * [T_pad, Hkv, d] keys and values, as given to spinf_branch_attention), then to the
+ * decode rows of its chain from the first token down to itself (k_dec, v_dec:
+ * [n_dec, Hkv, d]), with the same softmax: its output equals that of the tokens written
+ * into the template and laid out in a pass.  Keys are visited in a fixed order, so a
+ * row's output does not depend on the other rows of the call.
+ *
+ * q [n_q, Hq, d] are the queries of decode rows q_row[0..n_q) and o [n_q, Hq, d]
+ * receives their outputs (bf16, device, 16-byte aligned).  anchor, parent [n_dec] and
+ * q_row [n_q] are HOST arrays, checked here (parents earlier, one anchor per chain,
+ * chains of at most 64 tokens, anchors whose root path is at most four runs) and copied
+ * to `workspace` (>= spinf_decode_workspace_bytes(n_q)) before the call returns.
+ * d_head 64, 128 or 256; 1..8 query heads per kv head; scale <= 0 means 1/sqrt(d).  No
+ * window.  Asynchronous on `stream`.  Errors: SPINF_E_INVALID, SPINF_E_LIMIT,
+ * SPINF_E_UNSUPPORTED, SPINF_E_NOMEM (workspace), SPINF_E_CUDA. */
+spinf_status spinf_decode_attention(const spinf_plan* plan, int32_t pass, const void* q, const void* k_pass,
+                                    const void* v_pass, const void* k_dec, const void* v_dec, int32_t n_dec,
+                                    const int32_t* anchor, const int32_t* parent, const int32_t* q_row, int32_t n_q,
+                                    void* o, int32_t n_q_heads, int32_t n_kv_heads, int32_t d_head, float scale,
+                                    void* workspace, size_t workspace_bytes, spinf_stream stream);
+
+/* Bytes of device workspace spinf_score_rows needs. */
+size_t spinf_score_rows_workspace_bytes(int32_t n_rows, int32_t vocab, int32_t d_model, int32_t w_dtype, int32_t k);
+
+/* Next-token answers at caller-given rows (the decode rows of searched slots): for
+ * every row r of hidden [n_rows, d_model] (bf16, device) the full-vocabulary
+ * log-sum-exp row_lse[r] and the k tokens (1..16) with the largest logit among the
+ * allowed set token_set[r] (host array, -1 = every token; NULL = every token for all
+ * rows), most likely first, ties by lower id, with their z - row_lse (top_tok, top_lp:
+ * device [n_rows][k]).  The same kernels as spinf_score_extract, every row a searched
+ * row.  `plan`: any uploaded plan (its device error word).  Asynchronous on `stream`. */
+spinf_status spinf_score_rows(const spinf_plan* plan, const void* hidden, int32_t n_rows, const void* w,
+                              const float* w_scale, int32_t w_dtype, int32_t d_model, int32_t vocab,
+                              const int32_t* token_set, const uint32_t* token_sets, int32_t n_sets, int32_t k,
+                              float* row_lse, int32_t* top_tok, float* top_lp, void* workspace, size_t workspace_bytes,
+                              spinf_stream stream);
+
 /* Size of the device scratch area behind spinf_score_static: 64 MiB, reserved on
  * every GPU that loads this library, for as long as the process runs. */
 #define SPINF_SCORE_STATIC_SCRATCH_BYTES (64u << 20)
