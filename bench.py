@@ -479,9 +479,58 @@ def extract_timing(args, spinf, sv, wl, inputs, shape, w, w_scale, w_dtype, dev,
     ms_plain, ms_x = run(False), run(True)
     plan.device_status(stream)
     n_x = plan.extract_counts()[0]
+
+    # one decoding step of beam 4 on pass 0: every slot's 4 best first tokens become decode
+    # rows (their q/k/v drawn like any token's), attention on the pass's cached K/V, then the
+    # next-token answers at those rows
+    info = plan.pass_info(0)
+    kp = sv.path_keys(info.tok, info.parent, info.T)
+    q_p, k_p, v_p = (t.to(dev) for t in sv.qkv(kp, info.T_pad, shape.n_q_heads, shape.n_kv_heads, shape.d_head))
+    top = bufs[0]["ex"]["top_tok"][:info.X, :4].cpu().numpy()
+    anchor = np.repeat(info.slot_row[info.x_m], 4)
+    dkeys = [sv.extend_key(kp[a], t) for a, t in zip(anchor, top.reshape(-1))]
+    qd, kd, vd = (t.to(dev) for t in sv.qkv(dkeys, len(dkeys), shape.n_q_heads, shape.n_kv_heads, shape.d_head))
+    hd = sv.hidden(dkeys, len(dkeys), shape.d_model).to(dev)
+    nd = len(dkeys)
+    i32 = lambda a: torch.as_tensor(np.asarray(a, dtype=np.int32)).to(dev)  # noqa: E731
+    anchor, parent, rows = i32(anchor), i32(np.full(nd, -1)), i32(np.arange(nd))
+    tsets = i32(np.repeat(info.x_set, 4))
+    od_ = torch.empty_like(qd)
+    sws = torch.empty(spinf.lib().spinf_score_rows_workspace_bytes(nd, shape.vocab, shape.d_model, w_dtype, k),
+                      dtype=torch.uint8, device=dev)
+    lse_d = torch.empty(nd, device=dev)
+    tt_d = torch.empty(nd, k, dtype=torch.int32, device=dev)
+    tl_d = torch.empty(nd, k, device=dev)
+
+    def step():
+        spinf.decode_attention(plan, 0, qd, k_p, v_p, kd, vd, anchor, parent, rows, od_, shape.n_q_heads,
+                               shape.n_kv_heads, shape.d_head, stream=stream)
+        spinf.score_rows(plan, hd, w, w_scale, w_dtype, shape.d_model, shape.vocab, k, lse_d, tt_d, tl_d,
+                         token_set=tsets, token_sets=sets_dev, workspace=sws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        step()
+        ev = []
+        for _ in range(max(3, args.steps // 2)):
+            a0, a1, a2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            a0.record(stream)
+            spinf.decode_attention(plan, 0, qd, k_p, v_p, kd, vd, anchor, parent, rows, od_, shape.n_q_heads,
+                                   shape.n_kv_heads, shape.d_head, stream=stream)
+            a1.record(stream)
+            spinf.score_rows(plan, hd, w, w_scale, w_dtype, shape.d_model, shape.vocab, k, lse_d, tt_d, tl_d,
+                             token_set=tsets, token_sets=sets_dev, workspace=sws, stream=stream)
+            a2.record(stream)
+            ev.append((a0, a1, a2))
+    torch.cuda.synchronize()
+    plan.device_status(stream)
+    dec_attn = statistics.median(a.elapsed_time(b) for a, b, _ in ev)
+    dec_score = statistics.median(b.elapsed_time(c) for _, b, c in ev)
     return {"workload": f"every input + {n_slots} searched slots ({{*}} any token, {{n}} 1% token set), k={k}",
             "slots": n_x, "score_ms_plain": ms_plain, "score_ms_with_answers": ms_x,
-            "overhead_ms": ms_x - ms_plain, "slots_per_s": n_x / (ms_x * 1e-3)}
+            "overhead_ms": ms_x - ms_plain, "slots_per_s": n_x / (ms_x * 1e-3),
+            "decode_step": {"rows": nd, "beam": 4, "pass": 0, "attention_ms": dec_attn, "score_rows_ms": dec_score,
+                            "note": "attention on the pass's cached K/V (no re-read of the questions' layout), "
+                                    "next-token top-k over the whole vocabulary per row"}}
 
 
 def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):

@@ -33,7 +33,7 @@ SYMBOLS = [
     "spinf_score", "spinf_score_extract", "spinf_score_static", "spinf_collect", "spinf_collect_extract",
     "spinf_device_status", "spinf_device_selftest",
     "spinf_rope_tree", "spinf_linear", "spinf_qkv_rope", "spinf_quantize_static",
-    "spinf_decode_workspace_bytes", "spinf_decode_attention", "spinf_score_rows_workspace_bytes", "spinf_score_rows",
+    "spinf_decode_attention", "spinf_score_rows_workspace_bytes", "spinf_score_rows",
     "spinf_plan_free", "spinf_fingerprint",
     "spinf_status_string", "spinf_last_error",
 ]
@@ -133,10 +133,8 @@ def lib():
     L.spinf_linear.argtypes = [vp, vp, vp, vp, f32, i32, vp, i64, i64, i64, vp]
     L.spinf_qkv_rope.argtypes = [vp, i32, vp, vp, vp, f32, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp]
     L.spinf_quantize_static.argtypes = [vp, f32, vp, i64, vp]
-    L.spinf_decode_workspace_bytes.argtypes = [i32]
-    L.spinf_decode_workspace_bytes.restype = sz
     L.spinf_decode_attention.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, i32, i32, i32, f32,
-                                         vp, sz, vp]
+                                         vp]
     L.spinf_score_rows_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     L.spinf_score_rows_workspace_bytes.restype = sz
     L.spinf_score_rows.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, vp, vp, i32, i32, vp, vp, vp, vp, sz, vp]
@@ -546,33 +544,25 @@ def score_static(plan, p, hidden, w, w_scale, w_dtype, d_model, vocab, row_lse, 
 
 
 def decode_attention(plan, p, q, k_pass, v_pass, k_dec, v_dec, anchor, parent, q_row, o, n_q_heads, n_kv_heads,
-                     d_head, scale=0.0, workspace=None, stream=None):
-    """One decoding step of searched slots (spinf_decode_attention).  anchor, parent and q_row
-    are host integer sequences; a workspace is allocated when none is given."""
-    import torch
-    a = np.ascontiguousarray(anchor, dtype=np.int32)
-    pa = np.ascontiguousarray(parent, dtype=np.int32)
-    qr = np.ascontiguousarray(q_row, dtype=np.int32)
-    if workspace is None:
-        workspace = torch.empty(max(1, lib().spinf_decode_workspace_bytes(len(qr))), dtype=torch.uint8,
-                                device=q.device)
+                     d_head, scale=0.0, stream=None):
+    """One decoding step of searched slots (spinf_decode_attention); anchor, parent, q_row are
+    device int32 tensors."""
     _check(lib().spinf_decode_attention(plan.handle, p, _ptr(q), _ptr(k_pass), _ptr(v_pass), _ptr(k_dec),
-                                        _ptr(v_dec), len(a), a.ctypes.data, pa.ctypes.data, qr.ctypes.data, len(qr),
-                                        _ptr(o), n_q_heads, n_kv_heads, d_head, float(scale), _ptr(workspace),
-                                        workspace.numel() * workspace.element_size(), _stream(stream)))
+                                        _ptr(v_dec), anchor.numel(), _ptr(anchor), _ptr(parent), _ptr(q_row),
+                                        q_row.numel(), _ptr(o), n_q_heads, n_kv_heads, d_head, float(scale),
+                                        _stream(stream)))
 
 
 def score_rows(plan, hidden, w, w_scale, w_dtype, d_model, vocab, k, row_lse, top_tok, top_lp, token_set=None,
                token_sets=None, workspace=None, stream=None):
-    """Next-token answers at caller-given rows (spinf_score_rows); token_set: host ints per row or None."""
+    """Next-token answers at caller-given rows (spinf_score_rows); token_set: a device int32 tensor or None."""
     import torch
     n = hidden.shape[0]
-    ts = None if token_set is None else np.ascontiguousarray(token_set, dtype=np.int32)
     if workspace is None:
         workspace = torch.empty(max(1, lib().spinf_score_rows_workspace_bytes(n, vocab, d_model, w_dtype, k)),
                                 dtype=torch.uint8, device=hidden.device)
     _check(lib().spinf_score_rows(plan.handle, _ptr(hidden), n, _ptr(w), _ptr(w_scale), w_dtype, d_model, vocab,
-                                  None if ts is None else ts.ctypes.data, _ptr(token_sets),
+                                  _ptr(token_set), _ptr(token_sets),
                                   0 if token_sets is None else int(token_sets.shape[0]), k, _ptr(row_lse),
                                   _ptr(top_tok), _ptr(top_lp), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)))

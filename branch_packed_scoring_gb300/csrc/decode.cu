@@ -21,16 +21,18 @@
 
 #include <algorithm>
 #include <cmath>
+#include <type_traits>
+#include <utility>
 #include <vector>
 
 #include "internal.h"
+#include "ptx.cuh"
 #include "runtime.h"
 
 namespace spinf {
 namespace {
 
-constexpr int kMaxChain = 64;                 // decoded tokens per chain (a searched answer is short)
-constexpr int kDescInts = 8 + 1 + kMaxChain;  // per query: 4 pass runs, chain length, chain rows
+constexpr int kMaxChain = 64;   // decoded tokens per chain (a searched answer is short)
 
 // D / 32 consecutive elements of a bf16 row as fp32 (one 4-, 8- or 16-byte load per lane).
 template <int D>
@@ -61,53 +63,172 @@ __device__ __forceinline__ void load_row(const __nv_bfloat16* __restrict__ p, fl
     }
 }
 
-template <int D>
-__global__ void __launch_bounds__(256) decode_attention_kernel(
+// Thread 0 walks the row's chain and fetches its anchor's runs into shared memory,
+// checking every index against its array; a row that fails a check is written as
+// zeros and raises the plan's error word (SPINF_E_DEVICE_CHECK).  The row's keys (the
+// anchor's path, then the chain) are split into kSlices contiguous slices, one warp per
+// slice; a warp serves all G query heads of the kv head, so each key and value row is
+// loaded once.  The slices' (max, sum, accumulator) are merged in slice order, so the
+// result depends on the row's keys and the head grouping only.
+// 8 slices, or 4 when 8 slices' partial accumulators would not fit 40 KB of shared memory
+template <int D, int G>
+constexpr int slices() { return G * D * 4 * 8 <= 40960 ? 8 : 4; }
+
+template <int D, int G>
+__global__ void __launch_bounds__(32 * slices<D, G>()) decode_attention_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_pass,
     const __nv_bfloat16* __restrict__ v_pass, const __nv_bfloat16* __restrict__ k_dec,
-    const __nv_bfloat16* __restrict__ v_dec, const int32_t* __restrict__ desc, __nv_bfloat16* __restrict__ o, int Hq,
-    int Hkv, float scale) {
+    const __nv_bfloat16* __restrict__ v_dec, const int32_t* __restrict__ anchor, const int32_t* __restrict__ parent,
+    const int32_t* __restrict__ q_row, int n_dec, const int32_t* __restrict__ row_runs, int T,
+    __nv_bfloat16* __restrict__ o, int Hkv, float scale_log2, int* __restrict__ err) {
     constexpr int E = D / 32;
+    constexpr int kSlices = slices<D, G>();
     const int i = blockIdx.x, g = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = g * (Hq / Hkv) + warp;
-    const int32_t* dsc = desc + (size_t)i * kDescInts;
-    float qv[E], acc[E];
-    load_row<D>(q + ((size_t)i * Hq + h) * D + lane * E, qv);
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    float m = -INFINITY, l = 0.f;
-    auto visit = [&](const __nv_bfloat16* kr, const __nv_bfloat16* vr) {
-        float kx[E], vx[E];
-        load_row<D>(kr + lane * E, kx);
-        load_row<D>(vr + lane * E, vx);
-        float s = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) s = fmaf(qv[e], kx[e], s);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        s *= scale;
-        const float mn = fmaxf(m, s);
-        const float corr = expf(m - mn), p = expf(s - mn);
-        l = l * corr + p;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = acc[e] * corr + p * vx[e];
-        m = mn;
-    };
-    // the anchor's path in the pass: runs stored nearest first, visited farthest first
-    for (int run = 3; run >= 0; --run)
-        for (int kk = dsc[2 * run]; kk < dsc[2 * run + 1]; ++kk)
-            visit(k_pass + ((size_t)kk * Hkv + g) * D, v_pass + ((size_t)kk * Hkv + g) * D);
-    const int n_chain = dsc[8];
-    for (int c = 0; c < n_chain; ++c) {
-        const int r = dsc[9 + c];
-        visit(k_dec + ((size_t)r * Hkv + g) * D, v_dec + ((size_t)r * Hkv + g) * D);
+    const int Hq = Hkv * G;
+    __shared__ int32_t dsc[8 + 1 + kMaxChain];   // the anchor's 4 runs, chain length, chain rows
+    __shared__ int ok;
+    __shared__ float part_m[kSlices][G], part_l[kSlices][G];
+    __shared__ float part_acc[kSlices][G][D];
+    if (threadIdx.x == 0) {
+        int good = 1, n = 0;
+        int32_t walk[kMaxChain];
+        const int r = q_row[i];
+        if (r < 0 || r >= n_dec) good = 0;
+        for (int c = r; good && c >= 0;) {
+            if (n == kMaxChain) { good = 0; break; }
+            walk[n++] = c;
+            const int p = parent[c];
+            if (p >= c) good = 0;
+            c = p;
+        }
+        int a = good ? anchor[walk[n - 1]] : -1;
+        for (int j = 0; good && j < n; ++j)
+            if (anchor[walk[j]] != a) good = 0;
+        if (good && (a < 0 || a >= T)) good = 0;
+        if (good) {
+            for (int j = 0; j < 8; ++j) dsc[j] = row_runs[8 * (size_t)a + j];
+            if (dsc[0] < 0) good = 0;
+        }
+        dsc[8] = good ? n : 0;
+        for (int j = 0; good && j < n; ++j) dsc[9 + j] = walk[n - 1 - j];   // first decoded token first
+        if (!good) {
+            for (int j = 0; j < 8; ++j) dsc[j] = 0;
+            atomicExch(err, dev::kErrCheck);
+        }
+        ok = good;
     }
-    const float inv = 1.f / l;
-    __nv_bfloat16* dst = o + ((size_t)i * Hq + h) * D + lane * E;
+    __syncthreads();
+    float qv[G][E], acc[G][E], m[G], l[G];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+        load_row<D>(q + ((size_t)i * Hq + g * G + hh) * D + lane * E, qv[hh]);
+        m[hh] = -INFINITY;
+        l[hh] = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[hh][e] = 0.f;
+    }
+    // keys in batches of up to kB: the batch's K and V loads are all issued before the first
+    // is used, then per head one max and one rescale per batch (scores in log2 units)
+    constexpr int kB = G <= 2 ? 4 : 2;
+    auto batch = [&](auto rows, int nb) {
+        float kx[kB][E], vx[kB][E];
+#pragma unroll
+        for (int b = 0; b < kB; ++b)
+            if (b < nb) {
+                const auto kv = rows(b);
+                load_row<D>(kv.first + lane * E, kx[b]);
+                load_row<D>(kv.second + lane * E, vx[b]);
+            }
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+            float s[kB];
+#pragma unroll
+            for (int b = 0; b < kB; ++b) {
+                float t = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) t = fmaf(qv[hh][e], b < nb ? kx[b][e] : 0.f, t);
+                s[b] = t;
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                for (int b = 0; b < kB; ++b) s[b] += __shfl_xor_sync(0xffffffffu, s[b], off);
+            float mb = m[hh];
+#pragma unroll
+            for (int b = 0; b < kB; ++b) {
+                s[b] = b < nb ? s[b] * scale_log2 : -INFINITY;
+                mb = fmaxf(mb, s[b]);
+            }
+            const float corr = dev::fast_exp2(m[hh] - mb);
+            l[hh] *= corr;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[hh][e] *= corr;
+#pragma unroll
+            for (int b = 0; b < kB; ++b)
+                if (b < nb) {   // keys in order within the batch
+                    const float p = dev::fast_exp2(s[b] - mb);
+                    l[hh] += p;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[hh][e] = fmaf(p, vx[b][e], acc[hh][e]);
+                }
+            m[hh] = mb;
+        }
+    };
+    using Rows = std::pair<const __nv_bfloat16*, const __nv_bfloat16*>;
+    // this warp's slice [k0, k1) of the row's keys: the anchor's runs farthest first, then the chain
+    int total = dsc[8];
+    for (int run = 0; run < 4; ++run) total += dsc[2 * run + 1] - dsc[2 * run];
+    const int per = (total + kSlices - 1) / kSlices;
+    const int k0 = min(total, warp * per), k1 = min(total, k0 + per);
+    int off = 0;
+    for (int run = 3; run >= 0; --run) {
+        const int lo = dsc[2 * run], len = dsc[2 * run + 1] - lo;
+        const int a = max(k0, off), b = min(k1, off + len);
+        for (int x = a; x < b; x += kB)
+            batch([&](int j) {
+                const size_t ro = ((size_t)(lo + x - off + j) * Hkv + g) * D;
+                return Rows(k_pass + ro, v_pass + ro);
+            }, min(kB, b - x));
+        off += len;
+    }
+    {
+        const int a = max(k0, off), b = min(k1, off + dsc[8]);
+        for (int x = a; x < b; x += kB)
+            batch([&](int j) {
+                const size_t ro = ((size_t)dsc[9 + x - off + j] * Hkv + g) * D;
+                return Rows(k_dec + ro, v_dec + ro);
+            }, min(kB, b - x));
+    }
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+        if (lane == 0) {
+            part_m[warp][hh] = m[hh];
+            part_l[warp][hh] = l[hh];
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) part_acc[warp][hh][lane * E + e] = acc[hh][e];
+    }
+    __syncthreads();
+    // warp hh < G merges head hh's slices in slice order
+    if (warp >= G) return;
+    const int hh = warp;
+    float M = -INFINITY;
+    for (int t = 0; t < kSlices; ++t) M = fmaxf(M, part_m[t][hh]);
+    float L = 0.f, out[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) out[e] = 0.f;
+    for (int t = 0; t < kSlices; ++t) {
+        const float c = part_m[t][hh] == -INFINITY ? 0.f : dev::fast_exp2(part_m[t][hh] - M);
+        L += part_l[t][hh] * c;
+#pragma unroll
+        for (int e = 0; e < E; ++e) out[e] = fmaf(part_acc[t][hh][lane * E + e], c, out[e]);
+    }
+    const float inv = ok && L > 0.f ? 1.f / L : 0.f;
+    __nv_bfloat16* dst = o + ((size_t)i * Hq + g * G + hh) * D + lane * E;
 #pragma unroll
     for (int e = 0; e < E; e += 2)
-        *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+        *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(out[e] * inv, out[e + 1] * inv);
 }
 
 }  // namespace
@@ -115,67 +236,50 @@ __global__ void __launch_bounds__(256) decode_attention_kernel(
 
 using namespace spinf;
 
-extern "C" size_t spinf_decode_workspace_bytes(int32_t n_q) {
-    return n_q > 0 ? ((size_t)n_q * kDescInts * sizeof(int32_t) + 255) / 256 * 256 : 0;
-}
-
 extern "C" spinf_status spinf_decode_attention(const spinf_plan* plan, int32_t pass, const void* q, const void* k_pass,
                                                const void* v_pass, const void* k_dec, const void* v_dec,
                                                int32_t n_dec, const int32_t* anchor, const int32_t* parent,
                                                const int32_t* q_row, int32_t n_q, void* o, int32_t n_q_heads,
-                                               int32_t n_kv_heads, int32_t d_head, float scale, void* workspace,
-                                               size_t workspace_bytes, spinf_stream stream) {
+                                               int32_t n_kv_heads, int32_t d_head, float scale, spinf_stream stream) {
     spinf_status st = ensure_device_ready(plan, pass);
     if (st) return st;
     if (n_q < 0 || n_dec < 0) return fail(SPINF_E_INVALID, "negative row counts");
     if (n_q == 0) return SPINF_OK;
-    if (!q || !k_pass || !v_pass || !k_dec || !v_dec || !o || !anchor || !parent || !q_row || !workspace)
+    if (!q || !k_pass || !v_pass || !k_dec || !v_dec || !o || !anchor || !parent || !q_row)
         return fail(SPINF_E_INVALID, "NULL argument");
     if (d_head != 64 && d_head != 128 && d_head != 256) return fail(SPINF_E_UNSUPPORTED, "d_head must be 64, 128 or 256");
-    if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads || n_q_heads / n_kv_heads > 8)
-        return fail(SPINF_E_UNSUPPORTED, "query heads must be 1..8 per kv head");
+    if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads)
+        return fail(SPINF_E_UNSUPPORTED, "query heads must be a multiple of kv heads");
+    if (n_kv_heads > 65535) return fail(SPINF_E_UNSUPPORTED, "too many kv heads");
     for (const void* p : {q, k_pass, v_pass, k_dec, v_dec, (const void*)o})
         if (reinterpret_cast<uintptr_t>(p) & 15) return fail(SPINF_E_INVALID, "tensor not 16-byte aligned");
-    if (workspace_bytes < spinf_decode_workspace_bytes(n_q)) return fail(SPINF_E_NOMEM, "workspace too small");
     const Pass& P = plan->passes[pass];
-    // per query: the anchor's pass runs and its decode chain, checked here on the host
-    std::vector<int32_t> desc((size_t)n_q * kDescInts, 0);
-    for (int32_t i = 0; i < n_q; ++i) {
-        const int32_t r = q_row[i];
-        if (r < 0 || r >= n_dec) return fail(SPINF_E_INVALID, "q_row outside the decode rows");
-        int32_t* d = &desc[(size_t)i * kDescInts];
-        std::vector<int32_t> ch;
-        for (int32_t c = r; c >= 0; c = parent[c]) {
-            if (parent[c] >= c) return fail(SPINF_E_INVALID, "a decode row's parent must be an earlier row");
-            if ((int)ch.size() == kMaxChain) return fail(SPINF_E_LIMIT, "decode chain longer than 64 tokens");
-            ch.push_back(c);
-        }
-        const int32_t a = anchor[ch.back()];
-        for (int32_t c : ch)
-            if (anchor[c] != a) return fail(SPINF_E_INVALID, "a decode chain must keep one anchor");
-        if (a < 0 || a >= P.T) return fail(SPINF_E_INVALID, "anchor outside the pass");
-        const int32_t* runs = &P.row_runs[8 * (size_t)a];
-        if (runs[0] < 0) return fail(SPINF_E_UNSUPPORTED, "anchor's root path has more than four runs");
-        for (int j = 0; j < 8; ++j) d[j] = runs[j];
-        d[8] = (int32_t)ch.size();
-        for (size_t c = 0; c < ch.size(); ++c) d[9 + c] = ch[ch.size() - 1 - c];   // first decoded token first
-    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // pageable source: the call returns once the bytes are staged, so `desc` may go
-    cudaError_t e = cudaMemcpyAsync(workspace, desc.data(), desc.size() * sizeof(int32_t), cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_fail(e, "decode descriptor upload");
     const float sc = scale > 0.f ? scale : 1.f / std::sqrt(static_cast<float>(d_head));
-    const dim3 grid(n_q, n_kv_heads), block(32 * (n_q_heads / n_kv_heads));
-    auto go = [&](auto kernel) {
-        kernel<<<grid, block, 0, s>>>(static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_pass),
+    const int G = n_q_heads / n_kv_heads;
+    const dim3 grid(n_q, n_kv_heads);
+    const float sl2 = sc * 1.4426950408889634f;
+    auto go = [&](auto kernel, int slices_) {
+        kernel<<<grid, dim3(32 * slices_), 0, s>>>(static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_pass),
                                       static_cast<const __nv_bfloat16*>(v_pass), static_cast<const __nv_bfloat16*>(k_dec),
-                                      static_cast<const __nv_bfloat16*>(v_dec), static_cast<const int32_t*>(workspace),
-                                      static_cast<__nv_bfloat16*>(o), n_q_heads, n_kv_heads, sc);
+                                      static_cast<const __nv_bfloat16*>(v_dec), anchor, parent, q_row, n_dec,
+                                      P.dev.row_runs, P.T, static_cast<__nv_bfloat16*>(o), n_kv_heads, sl2, plan->d_err);
     };
-    if (d_head == 64) go(decode_attention_kernel<64>);
-    else if (d_head == 128) go(decode_attention_kernel<128>);
-    else go(decode_attention_kernel<256>);
-    e = cudaGetLastError();
+    auto by_d = [&](auto g_c) {
+        constexpr int GG = decltype(g_c)::value;
+        if (d_head == 64) go(decode_attention_kernel<64, GG>, slices<64, GG>());
+        else if (d_head == 128) go(decode_attention_kernel<128, GG>, slices<128, GG>());
+        else go(decode_attention_kernel<256, GG>, slices<256, GG>());
+    };
+    switch (G) {
+        case 1: by_d(std::integral_constant<int, 1>{}); break;
+        case 2: by_d(std::integral_constant<int, 2>{}); break;
+        case 4: by_d(std::integral_constant<int, 4>{}); break;
+        case 5: by_d(std::integral_constant<int, 5>{}); break;
+        case 8: by_d(std::integral_constant<int, 8>{}); break;
+        default: return fail(SPINF_E_UNSUPPORTED, "query heads per kv head must be 1, 2, 4, 5 or 8");
+    }
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return SPINF_OK;
 }

@@ -173,6 +173,7 @@ struct ExtractArgs {
     const int32_t* row_x;        // [M] searched slot of each scoring row, or -1
     const int32_t* x_set;        // [X]
     const uint32_t* token_sets;  // [n_sets][words]
+    int n_sets;
     int words;                   // ceil(V / 32)
     int k;                       // candidates kept per tile (extract_k)
     uint2* xpart;                // [X][n_vt][k] (z bits, token)
@@ -298,7 +299,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             if constexpr (KX > 0) {
                 xr = valid ? xa.row_x[m] : -1;
                 if (xr >= 0) {
-                    const int set = xa.x_set[xr];
+                    int set = xa.x_set[xr];
+                    if (set >= xa.n_sets) {   // a set the call does not hold: every token, and an error
+                        atomicExch(err, kErrCheck);
+                        set = -1;
+                    }
                     if (set >= 0) allow = xa.token_sets + (size_t)set * xa.words;
 #pragma unroll
                     for (int c = 0; c < kBN / 32; ++c)
@@ -547,7 +552,7 @@ spinf_status launch_score(const Pass& P, const ScoreLayout& L, const void* hidde
     const int n_kb = (D + kbk - 1) / kbk;
     const int total = L.n_vt * L.n_st;
     const int grid = std::min(total, sm_count());
-    ExtractArgs xa{P.dev.row_x, P.dev.x_set, KX ? ex->token_sets : nullptr, (V + 31) / 32, L.k,
+    ExtractArgs xa{P.dev.row_x, P.dev.x_set, KX ? ex->token_sets : nullptr, KX ? ex->n_sets : 0, (V + 31) / 32, L.k,
                    reinterpret_cast<uint2*>(ws + L.xpart)};
     score_main_kernel<FP8, KX><<<grid, kScoreThreads, KX ? kScoreSmemX : kScoreSmem, stream>>>(
         th, tw, sa, w_scale, part, zg, P.dev.row_gptr, P.dev.row_glist, P.dev.gather_tok, L.M, V, n_kb, L.n_st,
@@ -636,28 +641,33 @@ extern "C" spinf_status spinf_score(const spinf_plan* plan, int32_t pass, const 
 
 // ---------------------------------------------------------------- rows outside a plan
 // Scoring of caller-given hidden rows (the decode rows of searched slots): the rows are
-// the scoring rows, every row is searched.  The row tables that a pass would hold
-// (identity row maps, empty gather lists, token sets) are built on the host and copied to
-// the front of the workspace; the scoring kernels then run as for a pass.
+// the scoring rows, every row is searched.  The row tables a pass would hold (identity
+// row maps, empty gather lists, the rows' token sets) are written by a small kernel at the
+// front of the workspace; the scoring kernels then run as for a pass.
 namespace spinf {
 namespace {
+
+__global__ void rows_tables_kernel(int n, const int32_t* __restrict__ token_set, int32_t* __restrict__ slot_row,
+                                   int32_t* __restrict__ row_x, int32_t* __restrict__ x_m,
+                                   int32_t* __restrict__ x_set, int32_t* __restrict__ row_gptr) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i <= n; i += gridDim.x * blockDim.x) {
+        row_gptr[i] = 0;
+        if (i < n) {
+            slot_row[i] = row_x[i] = x_m[i] = i;
+            x_set[i] = token_set ? token_set[i] : -1;
+        }
+    }
+}
 
 struct RowsView {
     Pass P;
     size_t index_bytes = 0;
 };
 
-void rows_view(RowsView& rv, int32_t n, const int32_t* token_set) {
-    Pass& P = rv.P;
+void rows_view(RowsView& rv, int32_t n) {
+    Pass& P = rv.P;   // host sizes only: the layout of the scoring workspace
     P.slot_row.resize(n);
     P.x_m.resize(n);
-    P.row_x.resize(n);
-    P.x_set.resize(n);
-    for (int32_t i = 0; i < n; ++i) {
-        P.slot_row[i] = P.x_m[i] = P.row_x[i] = i;
-        P.x_set[i] = token_set ? token_set[i] : -1;
-    }
-    P.row_gptr.assign(n + 1, 0);
     rv.index_bytes = align256((size_t)n * 4) * 4 + align256((size_t)(n + 1) * 4);
 }
 
@@ -668,7 +678,7 @@ extern "C" size_t spinf_score_rows_workspace_bytes(int32_t n_rows, int32_t vocab
                                                    int32_t k) {
     if (n_rows <= 0 || vocab <= 0 || d_model <= 0 || k < 1 || k > 16) return 0;
     RowsView rv;
-    rows_view(rv, n_rows, nullptr);
+    rows_view(rv, n_rows);
     return rv.index_bytes + score_layout(rv.P, vocab, d_model, w_dtype, k).total;
 }
 
@@ -682,36 +692,33 @@ extern "C" spinf_status spinf_score_rows(const spinf_plan* plan, const void* hid
     if (d_model <= 0 || d_model % 16) return fail(SPINF_E_UNSUPPORTED, "d_model must be a positive multiple of 16");
     if (vocab <= 0) return fail(SPINF_E_INVALID, "vocab must be positive");
     if (k < 1 || k > 16) return fail(SPINF_E_INVALID, "k must be in 1..16");
-    if (n_rows < 0) return fail(SPINF_E_INVALID, "negative row count");
+    if (n_rows < 0 || n_sets < 0) return fail(SPINF_E_INVALID, "negative count");
     if (n_rows == 0) return SPINF_OK;
     if (!hidden || !w || !row_lse || !top_tok || !top_lp || !workspace) return fail(SPINF_E_INVALID, "NULL buffer");
+    if (n_sets > 0 && !token_sets) return fail(SPINF_E_INVALID, "token_sets is NULL");
     if (w_dtype == SPINF_DTYPE_E4M3 && (!w_scale || (reinterpret_cast<uintptr_t>(w_scale) & 15)))
         return fail(SPINF_E_INVALID, "e4m3 weights need a 16-byte aligned w_scale");
     for (const void* p : {hidden, w, (const void*)workspace})
         if (reinterpret_cast<uintptr_t>(p) & 15) return fail(SPINF_E_INVALID, "buffer not 16-byte aligned");
-    if (token_set)
-        for (int32_t i = 0; i < n_rows; ++i)
-            if (token_set[i] < -1 || token_set[i] >= n_sets || (token_set[i] >= 0 && !token_sets))
-                return fail(SPINF_E_INVALID, "a row names an unknown token set");
     RowsView rv;
-    rows_view(rv, n_rows, token_set);
+    rows_view(rv, n_rows);
     Pass& P = rv.P;
     const ScoreLayout L = score_layout(P, vocab, d_model, w_dtype, k);
     if (workspace_bytes < rv.index_bytes + L.total) return fail(SPINF_E_NOMEM, "workspace too small");
-    // the row tables at the front of the workspace (pageable sources: staged before return)
     uint8_t* base = static_cast<uint8_t*>(workspace);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const std::vector<int32_t>* src[5] = {&P.slot_row, &P.row_x, &P.x_m, &P.x_set, &P.row_gptr};
-    int32_t** dst[5] = {&P.dev.slot_row, &P.dev.row_x, &P.dev.x_m, &P.dev.x_set, &P.dev.row_gptr};
-    size_t off = 0;
-    for (int a = 0; a < 5; ++a) {
-        *dst[a] = reinterpret_cast<int32_t*>(base + off);
-        cudaError_t e = cudaMemcpyAsync(base + off, src[a]->data(), src[a]->size() * 4, cudaMemcpyHostToDevice, s);
-        if (e != cudaSuccess) return cuda_fail(e, "row table upload");
-        off += align256(src[a]->size() * 4);
-    }
-    P.dev.row_glist = P.dev.row_gptr;    // no gathers: never read
+    const size_t a = align256((size_t)n_rows * 4);
+    P.dev.slot_row = reinterpret_cast<int32_t*>(base);
+    P.dev.row_x = reinterpret_cast<int32_t*>(base + a);
+    P.dev.x_m = reinterpret_cast<int32_t*>(base + 2 * a);
+    P.dev.x_set = reinterpret_cast<int32_t*>(base + 3 * a);
+    P.dev.row_gptr = reinterpret_cast<int32_t*>(base + 4 * a);
+    P.dev.row_glist = P.dev.row_gptr;   // no gathers: never read
     P.dev.gather_tok = P.dev.row_gptr;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    rows_tables_kernel<<<(n_rows + 256) / 256, 256, 0, s>>>(n_rows, token_set, P.dev.slot_row, P.dev.row_x, P.dev.x_m,
+                                                           P.dev.x_set, P.dev.row_gptr);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "row tables launch");
     spinf_extract_out ex{token_sets, n_sets, top_tok, top_lp};
     uint8_t* ws = base + rv.index_bytes;
     const float* wsc = w_dtype == SPINF_DTYPE_E4M3 ? w_scale : nullptr;

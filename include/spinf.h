@@ -334,9 +334,6 @@ spinf_status spinf_score_extract(const spinf_plan* plan, int32_t pass,
 
 /* ---- Decoding steps of searched slots on the pass's cached keys and values. ---- */
 
-/* Bytes of device workspace spinf_decode_attention needs for n_q query rows. */
-size_t spinf_decode_workspace_bytes(int32_t n_q);
-
 /* Attention of decode rows of searched slots ("spinf-serve 0.1.1" PyPI, "What it does"
  * and "Speed and scale": extraction slots are decoded on the same read, the content and
  * the questions are not read again).  Decode row r extends the root path of pass row
@@ -351,17 +348,18 @@ size_t spinf_decode_workspace_bytes(int32_t n_q);
  *
  * q [n_q, Hq, d] are the queries of decode rows q_row[0..n_q) and o [n_q, Hq, d]
  * receives their outputs (bf16, device, 16-byte aligned).  anchor, parent [n_dec] and
- * q_row [n_q] are HOST arrays, checked here (parents earlier, one anchor per chain,
- * chains of at most 64 tokens, anchors whose root path is at most four runs) and copied
- * to `workspace` (>= spinf_decode_workspace_bytes(n_q)) before the call returns.
- * d_head 64, 128 or 256; 1..8 query heads per kv head; scale <= 0 means 1/sqrt(d).  No
- * window.  Asynchronous on `stream`.  Errors: SPINF_E_INVALID, SPINF_E_LIMIT,
- * SPINF_E_UNSUPPORTED, SPINF_E_NOMEM (workspace), SPINF_E_CUDA. */
+ * q_row [n_q] are device int32 arrays (the decode loop's own state); each row is checked
+ * on the device (q_row in range, parents earlier, one anchor per chain, chains of at most
+ * 64 tokens, an anchor in the pass whose root path is at most four runs): a row that
+ * fails is written as zeros and the plan's error word becomes SPINF_E_DEVICE_CHECK
+ * (spinf_device_status).  d_head 64, 128 or 256; 1..8 query heads per kv head;
+ * scale <= 0 means 1/sqrt(d).  No window.  Needs the pass uploaded; asynchronous on
+ * `stream`.  Errors: SPINF_E_INVALID, SPINF_E_UNSUPPORTED, SPINF_E_CUDA. */
 spinf_status spinf_decode_attention(const spinf_plan* plan, int32_t pass, const void* q, const void* k_pass,
                                     const void* v_pass, const void* k_dec, const void* v_dec, int32_t n_dec,
                                     const int32_t* anchor, const int32_t* parent, const int32_t* q_row, int32_t n_q,
                                     void* o, int32_t n_q_heads, int32_t n_kv_heads, int32_t d_head, float scale,
-                                    void* workspace, size_t workspace_bytes, spinf_stream stream);
+                                    spinf_stream stream);
 
 /* Bytes of device workspace spinf_score_rows needs. */
 size_t spinf_score_rows_workspace_bytes(int32_t n_rows, int32_t vocab, int32_t d_model, int32_t w_dtype, int32_t k);
@@ -369,10 +367,12 @@ size_t spinf_score_rows_workspace_bytes(int32_t n_rows, int32_t vocab, int32_t d
 /* Next-token answers at caller-given rows (the decode rows of searched slots): for
  * every row r of hidden [n_rows, d_model] (bf16, device) the full-vocabulary
  * log-sum-exp row_lse[r] and the k tokens (1..16) with the largest logit among the
- * allowed set token_set[r] (host array, -1 = every token; NULL = every token for all
- * rows), most likely first, ties by lower id, with their z - row_lse (top_tok, top_lp:
- * device [n_rows][k]).  The same kernels as spinf_score_extract, every row a searched
- * row.  `plan`: any uploaded plan (its device error word).  Asynchronous on `stream`. */
+ * allowed set token_set[r] (device int32 [n_rows], -1 = every token; NULL = every token
+ * for all rows), most likely first, ties by lower id, with their z - row_lse (top_tok,
+ * top_lp: device [n_rows][k]).  The same kernels as spinf_score_extract, every row a
+ * searched row; a set number >= n_sets is read as every token and raises
+ * SPINF_E_DEVICE_CHECK.  `plan`: any uploaded plan (its device error word).
+ * Asynchronous on `stream`. */
 spinf_status spinf_score_rows(const spinf_plan* plan, const void* hidden, int32_t n_rows, const void* w,
                               const float* w_scale, int32_t w_dtype, int32_t d_model, int32_t vocab,
                               const int32_t* token_set, const uint32_t* token_sets, int32_t n_sets, int32_t k,

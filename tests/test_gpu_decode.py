@@ -14,6 +14,11 @@ from synth import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
+
+def _i32(a):
+    return torch.as_tensor(np.asarray(a, dtype=np.int32)).cuda()
+
+
 SHAPES = {"d64": wl.TINY, "d128": wl.Shape(40, 8, 128, 512, 1000), "d256": wl.Shape(16, 8, 256, 512, 1000)}
 
 
@@ -61,8 +66,8 @@ def test_decode_matches_oracle(spinf, name):
     rows = list(range(len(toks)))[::-1]            # any order of the step's rows
     q = qd[rows].contiguous().cuda()
     o = torch.full_like(q, float("nan"))
-    spinf.decode_attention(plan, 0, q, kp, vp, kd.cuda(), vd.cuda(), anchor, parent, rows, o, shape.n_q_heads,
-                           shape.n_kv_heads, shape.d_head)
+    spinf.decode_attention(plan, 0, q, kp, vp, kd.cuda(), vd.cuda(), _i32(anchor), _i32(parent), _i32(rows), o,
+                           shape.n_q_heads, shape.n_kv_heads, shape.d_head)
     plan.device_status()
     want = od.decode_attention(lay, qd[rows].double().numpy(), kp.double().cpu().numpy(), vp.double().cpu().numpy(),
                                kd.double().numpy(), vd.double().numpy(), anchor, parent, rows, shape.n_q_heads,
@@ -83,8 +88,8 @@ def test_decode_equals_replanned_branch_attention(spinf):
     qp, kp, vp, _ = pass_values(lay, shape, hidden_rows=False)
     r2 = len(lay.x_m)                               # the second token of slot 0
     o = torch.empty(2, shape.n_q_heads, shape.d_head, dtype=torch.bfloat16, device="cuda")
-    spinf.decode_attention(plan, 0, qd[[0, r2]].contiguous().cuda(), kp, vp, kd.cuda(), vd.cuda(), anchor, parent,
-                           [0, r2], o, shape.n_q_heads, shape.n_kv_heads, shape.d_head)
+    spinf.decode_attention(plan, 0, qd[[0, r2]].contiguous().cuda(), kp, vp, kd.cuda(), vd.cuda(), _i32(anchor),
+                           _i32(parent), _i32([0, r2]), o, shape.n_q_heads, shape.n_kv_heads, shape.d_head)
     plan.device_status()
     # slot 0 is the first searched question of input 0: write both tokens into its template
     i0 = next(i for i, (_, qs) in enumerate(inputs) if any(q[1] is None for q in qs))
@@ -114,32 +119,42 @@ def test_decode_rows_do_not_depend_on_the_step(spinf):
     qp, kp, vp, _ = pass_values(lay, shape, hidden_rows=False)
     rows = list(range(len(toks)))
     o_all = torch.empty(len(rows), shape.n_q_heads, shape.d_head, dtype=torch.bfloat16, device="cuda")
-    spinf.decode_attention(plan, 0, qd.cuda(), kp, vp, kd.cuda(), vd.cuda(), anchor, parent, rows, o_all,
-                           shape.n_q_heads, shape.n_kv_heads, shape.d_head)
+    spinf.decode_attention(plan, 0, qd.cuda(), kp, vp, kd.cuda(), vd.cuda(), _i32(anchor), _i32(parent), _i32(rows),
+                           o_all, shape.n_q_heads, shape.n_kv_heads, shape.d_head)
     for r in (0, len(rows) - 1):
         o1 = torch.empty(1, shape.n_q_heads, shape.d_head, dtype=torch.bfloat16, device="cuda")
-        spinf.decode_attention(plan, 0, qd[[r]].contiguous().cuda(), kp, vp, kd.cuda(), vd.cuda(), anchor, parent,
-                               [r], o1, shape.n_q_heads, shape.n_kv_heads, shape.d_head)
+        spinf.decode_attention(plan, 0, qd[[r]].contiguous().cuda(), kp, vp, kd.cuda(), vd.cuda(), _i32(anchor),
+                               _i32(parent), _i32([r]), o1, shape.n_q_heads, shape.n_kv_heads, shape.d_head)
         plan.device_status()
         assert torch.equal(o1[0], o_all[r])
 
 
-def test_decode_rejects_bad_chains(spinf):
+def test_decode_checks_rows_on_the_device(spinf):
+    """A bad row (parent not earlier, a chain of 70 tokens, q_row out of range) is written as
+    zeros and reported as SPINF_E_DEVICE_CHECK; the good rows of the same call are unaffected."""
     shape = wl.TINY
     inputs = _request(shape.vocab)
     lay = oracle_plan(inputs, vocab=shape.vocab).passes[0]
     plan = spinf.Plan(inputs, vocab=shape.vocab)
     plan.upload(0)
     a = int(lay.slot_row[lay.x_m[0]])
-    q = torch.zeros(1, 4, 64, dtype=torch.bfloat16, device="cuda")
-    kv = torch.zeros(70, 2, 64, dtype=torch.bfloat16, device="cuda")
     qp, kp, vp, _ = pass_values(lay, shape, hidden_rows=False)
-    cases = [([a, a], [-1, 1], [1], "INVALID"),                         # parent not earlier
-             ([a] * 70, [-1] + list(range(69)), [69], "LIMIT")]         # a chain of 70 tokens
-    for anchor, parent, rows, status in cases:
+    g = torch.Generator().manual_seed(1)
+    kv = torch.randn(72, 2, 64, generator=g).to(torch.bfloat16).cuda()
+    q = torch.randn(2, 4, 64, generator=g).to(torch.bfloat16).cuda()
+    cases = [([a, a], [-1, 1], [0, 1]),                              # row 1's parent is itself
+             ([a] * 70, [-1] + list(range(69)), [0, 69]),            # row 69's chain has 70 tokens
+             ([a, a], [-1, 0], [0, 5])]                              # q_row 5 does not exist
+    good = None
+    for anchor, parent, rows in cases:
+        o = torch.full_like(q, float("nan"))
+        spinf.decode_attention(plan, 0, q, kp, vp, kv, kv, _i32(anchor), _i32(parent), _i32(rows), o, 4, 2, 64)
         with pytest.raises(spinf.SpinfError) as e:
-            spinf.decode_attention(plan, 0, q, kp, vp, kv, kv, anchor, parent, rows, q.clone(), 4, 2, 64)
-        assert e.value.status_name == status
+            plan.device_status()
+        assert e.value.status_name == "DEVICE_CHECK"
+        assert torch.count_nonzero(o[1]).item() == 0 and torch.isfinite(o[0]).all()
+        good = o[0].clone() if good is None else good
+        assert torch.equal(o[0], good)   # row 0 (one token on the anchor) is the same each time
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
@@ -166,7 +181,7 @@ def test_score_rows_equal_searched_slot_answers(spinf, dtype):
     top_tok = torch.empty(n, k, dtype=torch.int32, device="cuda")
     top_lp = torch.empty(n, k, device="cuda")
     spinf.score_rows(plan, rows, wd, ws, wt, shape.d_model, shape.vocab, k, lse, top_tok, top_lp,
-                     token_set=lay.x_set, token_sets=pack_token_sets(sets).cuda())
+                     token_set=_i32(lay.x_set), token_sets=pack_token_sets(sets).cuda())
     plan.device_status()
     assert np.array_equal(top_tok.cpu().numpy(), tt) and np.array_equal(top_lp.cpu().numpy(), tl)
     if dtype == "bf16":
