@@ -480,13 +480,14 @@ def extract_timing(args, spinf, sv, wl, inputs, shape, w, w_scale, w_dtype, dev,
     plan.device_status(stream)
     n_x = plan.extract_counts()[0]
 
-    # one decoding step of beam 4 on pass 0: every slot's 4 best first tokens become decode
-    # rows (their q/k/v drawn like any token's), attention on the pass's cached K/V, then the
-    # next-token answers at those rows
-    info = plan.pass_info(0)
+    # one decoding step of beam 4 on the pass with the most searched slots: every slot's 4 best
+    # first tokens become decode rows (their q/k/v drawn like any token's), attention on the
+    # pass's cached K/V, then the next-token answers at those rows
+    pd = max(range(plan.num_passes), key=lambda p: plan.pass_info(p).X)
+    info = plan.pass_info(pd)
     kp = sv.path_keys(info.tok, info.parent, info.T)
     q_p, k_p, v_p = (t.to(dev) for t in sv.qkv(kp, info.T_pad, shape.n_q_heads, shape.n_kv_heads, shape.d_head))
-    top = bufs[0]["ex"]["top_tok"][:info.X, :4].cpu().numpy()
+    top = bufs[pd]["ex"]["top_tok"][:info.X, :4].cpu().numpy()
     anchor = np.repeat(info.slot_row[info.x_m], 4)
     dkeys = [sv.extend_key(kp[a], t) for a, t in zip(anchor, top.reshape(-1))]
     qd, kd, vd = (t.to(dev) for t in sv.qkv(dkeys, len(dkeys), shape.n_q_heads, shape.n_kv_heads, shape.d_head))
@@ -503,7 +504,7 @@ def extract_timing(args, spinf, sv, wl, inputs, shape, w, w_scale, w_dtype, dev,
     tl_d = torch.empty(nd, k, device=dev)
 
     def step():
-        spinf.decode_attention(plan, 0, qd, k_p, v_p, kd, vd, anchor, parent, rows, od_, shape.n_q_heads,
+        spinf.decode_attention(plan, pd, qd, k_p, v_p, kd, vd, anchor, parent, rows, od_, shape.n_q_heads,
                                shape.n_kv_heads, shape.d_head, stream=stream)
         spinf.score_rows(plan, hd, w, w_scale, w_dtype, shape.d_model, shape.vocab, k, lse_d, tt_d, tl_d,
                          token_set=tsets, token_sets=sets_dev, workspace=sws, stream=stream)
@@ -514,7 +515,7 @@ def extract_timing(args, spinf, sv, wl, inputs, shape, w, w_scale, w_dtype, dev,
         for _ in range(max(3, args.steps // 2)):
             a0, a1, a2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
             a0.record(stream)
-            spinf.decode_attention(plan, 0, qd, k_p, v_p, kd, vd, anchor, parent, rows, od_, shape.n_q_heads,
+            spinf.decode_attention(plan, pd, qd, k_p, v_p, kd, vd, anchor, parent, rows, od_, shape.n_q_heads,
                                    shape.n_kv_heads, shape.d_head, stream=stream)
             a1.record(stream)
             spinf.score_rows(plan, hd, w, w_scale, w_dtype, shape.d_model, shape.vocab, k, lse_d, tt_d, tl_d,
@@ -528,7 +529,7 @@ def extract_timing(args, spinf, sv, wl, inputs, shape, w, w_scale, w_dtype, dev,
     return {"workload": f"every input + {n_slots} searched slots ({{*}} any token, {{n}} 1% token set), k={k}",
             "slots": n_x, "score_ms_plain": ms_plain, "score_ms_with_answers": ms_x,
             "overhead_ms": ms_x - ms_plain, "slots_per_s": n_x / (ms_x * 1e-3),
-            "decode_step": {"rows": nd, "beam": 4, "pass": 0, "attention_ms": dec_attn, "score_rows_ms": dec_score,
+            "decode_step": {"rows": nd, "beam": 4, "pass": pd, "attention_ms": dec_attn, "score_rows_ms": dec_score,
                             "note": "attention on the pass's cached K/V (no re-read of the questions' layout), "
                                     "next-token top-k over the whole vocabulary per row"}}
 
