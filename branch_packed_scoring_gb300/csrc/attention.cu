@@ -48,6 +48,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <mutex>
 #include <cmath>
 
 #include "internal.h"
@@ -917,6 +918,7 @@ extern "C" spinf_status spinf_branch_attention(const spinf_plan* plan, int32_t p
     // with a window, the schedule without the tiles no row of a Q tile sees within it
     Sched sc{P.dev.qt_work, P.dev.tile_kv, P.dev.tile_len};
     if (window > 0 && P.T > 0) {
+        std::lock_guard<std::mutex> lock(const_cast<spinf_plan*>(plan)->cache_mu);
         WindowSchedule& w = window_schedule(const_cast<Pass&>(P), window);
         if ((st = upload_window(w, s))) return st;
         sc = Sched{w.d_qt_work, w.d_tile_kv, w.d_tile_len};

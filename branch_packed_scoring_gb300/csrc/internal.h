@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <memory>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -90,6 +91,7 @@ struct spinf_plan {
     int64_t n_options_total = 0;
     int64_t n_extract = 0;                       // searched slots among the user questions
     int32_t extract_k = 8;
+    std::mutex cache_mu;                         // guards the lazily built per-pass caches (windows, rotary tables)
     int32_t* d_err = nullptr;                    // device error word (allocated at first upload)
     bool err_owned = true;                       // false: inside a caller-owned descriptor buffer
     int device = -1;

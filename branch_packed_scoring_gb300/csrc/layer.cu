@@ -36,6 +36,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -459,7 +460,10 @@ extern "C" spinf_status spinf_rope_tree(const spinf_plan* plan, int32_t pass, vo
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const float2* table = nullptr;
     int stride = 0;
-    if ((st = rope_table(P, d_head, theta, s, &table, &stride))) return st;
+    {
+        std::lock_guard<std::mutex> lock(const_cast<spinf_plan*>(plan)->cache_mu);
+        if ((st = rope_table(P, d_head, theta, s, &table, &stride))) return st;
+    }
     rope_tree_kernel<<<P.T_pad, 256, 0, s>>>(static_cast<__nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(k),
                                              P.dev.pos, table, stride, n_q_heads, n_kv_heads, d_head);
     cudaError_t e = cudaGetLastError();
@@ -526,7 +530,10 @@ extern "C" spinf_status spinf_qkv_rope(const spinf_plan* plan, int32_t pass, con
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const float2* table = nullptr;
     int stride = 0;
-    if ((st = rope_table(P, d_head, theta, s, &table, &stride))) return st;
+    {
+        std::lock_guard<std::mutex> lock(const_cast<spinf_plan*>(plan)->cache_mu);
+        if ((st = rope_table(P, d_head, theta, s, &table, &stride))) return st;
+    }
     LinearOut out{};
     out.y[0] = static_cast<__nv_bfloat16*>(q);
     out.y[1] = static_cast<__nv_bfloat16*>(k);

@@ -648,6 +648,7 @@ extern "C" spinf_status spinf_plan_window_schedule(const spinf_plan* plan, int32
     if (!plan || pass < 0 || pass >= (int32_t)plan->passes.size()) return fail(SPINF_E_INVALID, "bad plan or pass");
     if (window <= 0) return fail(SPINF_E_INVALID, "window must be positive");
     if (!tile_ptr || !tile_kv || !tile_len || !n_sched) return fail(SPINF_E_INVALID, "NULL output");
+    std::lock_guard<std::mutex> lock(const_cast<spinf_plan*>(plan)->cache_mu);
     WindowSchedule& w = window_schedule(const_cast<Pass&>(plan->passes[pass]), window);
     *tile_ptr = w.tile_ptr.data();
     *tile_kv = w.tile_kv.data();

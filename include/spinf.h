@@ -35,6 +35,10 @@
  *     row-major, tokens the slowest dimension.
  *   - There is no CPU fallback: a device call on a machine without an sm_103a
  *     GPU returns SPINF_E_CUDA.
+ *   - A plan may be used from several host threads: the per-pass caches built
+ *     on first use (window schedules, rotary tables) are guarded by a lock in
+ *     the plan; uploads (spinf_plan_upload*) and spinf_plan_free are not, and
+ *     must not overlap other calls on the same plan.
  */
 #ifndef SPINF_H
 #define SPINF_H
