@@ -59,3 +59,24 @@ def test_selftest_needs_an_uploaded_plan(spinf):
     plan = spinf.Plan([([1, 2, 3], [([4, 5], [[6], [7]])])])
     st = spinf.lib().spinf_device_selftest(plan.handle, 30, None)
     assert spinf.STATUS_NAMES[st] == "INVALID"
+
+
+def test_layer_and_decode_calls_validate_before_any_device_work(spinf):
+    """Arguments of the projection, decode and row-scoring calls are checked on the host first
+    (no GPU needed): a plan that was never uploaded has no error word, bad sizes are refused."""
+    L = spinf.lib()
+    plan = spinf.Plan([([1, 2, 3], [([4, 5], [[6], [7]])])])
+    names = spinf.STATUS_NAMES
+    # spinf_linear needs an uploaded plan (its device error word)
+    assert names[L.spinf_linear(plan.handle, 4096, 4096, None, 1.0, 0, 4096, 8, 64, 64, None)] == "INVALID"
+    assert names[L.spinf_qkv_rope(plan.handle, 0, 4096, 4096, None, 1.0, 0, 256, 4, 2, 64, 10000.0, 4096, 4096,
+                                  4096, None)] == "INVALID"
+    assert names[L.spinf_decode_attention(plan.handle, 0, 4096, 4096, 4096, 4096, 4096, 1, 4096, 4096, 4096, 1,
+                                          4096, 4, 2, 64, 0.0, None)] == "INVALID"
+    assert names[L.spinf_score_rows(plan.handle, 4096, 1, 4096, None, 0, 256, 1024, None, None, 0, 8, 4096, 4096,
+                                    4096, 4096, 1 << 20, None)] == "INVALID"
+    assert names[L.spinf_quantize_static(4096, 0.0, 4096, 8, None)] == "INVALID"     # scale must be positive
+    assert names[L.spinf_quantize_static(4096, 1.0, 4096, 7, None)] == "INVALID"     # n a multiple of 8
+    assert L.spinf_score_rows_workspace_bytes(0, 1024, 256, 0, 8) == 0
+    assert L.spinf_score_rows_workspace_bytes(4, 1024, 256, 0, 17) == 0
+    assert L.spinf_score_rows_workspace_bytes(4, 1024, 256, 0, 8) > 4 * 256 * 2
