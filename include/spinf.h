@@ -59,7 +59,7 @@ typedef enum {
     SPINF_E_LIMIT = 2,          /* a limit of spinf_plan_opts exceeded */
     SPINF_E_NOMEM = 3,          /* host or device allocation failed, or workspace too small */
     SPINF_E_CUDA = 4,           /* a CUDA runtime call failed (no device, launch error, ...) */
-    SPINF_E_UNSUPPORTED = 5,    /* a shape or dtype this build does not implement */
+    SPINF_E_UNSUPPORTED = 5,    /* a shape or dtype this library does not implement */
     SPINF_E_DEVICE_TIMEOUT = 6, /* a bounded device wait ran out (reported by spinf_device_status) */
     SPINF_E_DEVICE_CHECK = 7    /* a device-side descriptor check failed */
 } spinf_status;
