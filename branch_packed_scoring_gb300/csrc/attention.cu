@@ -16,12 +16,16 @@
 // pair is a cta_group::2 MMA pair: the leader issues M = 256 products over both
 // CTAs' rows, and each CTA holds half of every K tile (64 keys) and V tile (64
 // columns).  Warp roles:
-//   warp 0      TMA producer of Q (once per item) and K tiles (two buffers, or one
-//               at d_head 256 outside a cta_group::2 pair)
-//   warp 1      TMEM owner and MMA issuer: S = Q K^T into one of two TMEM
-//               buffers (SS form, fp32), O += P V (P read from TMEM, V MN-major
-//               from shared memory)
-//   warp 2      TMA producer of V tiles (buffered like K)
+//   warp 0      one TMA producer thread for Q (once per item), K and V tiles: it
+//               polls the buffers' barriers and issues whichever copy is free first
+//               (each tile one 4-D copy of all its 64-column chunks; two K and two V
+//               buffers, or one of each at d_head 256 outside a cta_group::2 pair,
+//               then copied in two halves)
+//   warp 1      TMEM owner and S issuer: S = Q K^T into one of three (d_head <= 128)
+//               or two (d_head 256) TMEM buffers (SS form, fp32)
+//   warp 2      PV issuer: O += P V (P read from TMEM, V MN-major from shared
+//               memory); two issuing threads, so the tensor core has the other
+//               stream's MMAs to run while one thread commits or waits
 //   warps 3-10  softmax, two warps per TMEM lane quarter: each thread owns half
 //               of one Q row (64 of the 128 key columns, D/2 of the O columns):
 //               mask, online softmax with the row maximum exchanged between the
@@ -48,8 +52,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <mutex>
 #include <cmath>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
