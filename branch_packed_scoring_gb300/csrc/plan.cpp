@@ -8,7 +8,9 @@
 // content repeated (man page, CAVEATS).  Options form a token trie per question
 // (PyPI page, "Layout": "templates to token tries").  A searched slot ({*}, {n},
 // {$}; PyPI page, "What it does") lays out its template only and is scored at its
-// last template row.
+// last template row.  A placeholder grid (same section: placeholders turn one
+// template into a grid of questions) is expanded into one question per
+// combination of placeholder values before anything else.
 //
 // Visibility is encoded by two integers per row: key k is visible to exactly the
 // rows [k, end[k]) -- in a pre-order layout a row's descendants follow it

@@ -20,6 +20,8 @@
 //                    keeps, per searched row and 256-token tile, the best k
 //                    allowed tokens; K5 merges the tiles' lists into the row's
 //                    top k (z descending, lower id first on ties), lp = z - lse
+//   rows outside a plan  spinf_score_rows: the same kernels on caller-given rows
+//                    (the decode rows of searched slots), every row searched
 //
 // Every reduction runs in a fixed order that depends only on the row's own
 // values and the vocabulary size, so a row's results do not depend on M or on
