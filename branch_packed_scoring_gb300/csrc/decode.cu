@@ -119,45 +119,75 @@ __global__ void __launch_bounds__(32 * slices<D, G>()) decode_attention_kernel(
         ok = good;
     }
     __syncthreads();
-    float qv[G][E], acc[G][E], m[G], l[G];
+    // the group's queries in shared memory (fp32), read back as 16-byte pieces by the score lanes
+    __shared__ __align__(16) float qs[G][D];
+    for (int x = threadIdx.x; x < G * D; x += blockDim.x)
+        qs[x / D][x % D] = __bfloat162float(q[((size_t)i * Hq + g * G) * D + x]);
+    __syncthreads();
+    float acc[G][E], m[G], l[G];
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
-        load_row<D>(q + ((size_t)i * Hq + g * G + hh) * D + lane * E, qv[hh]);
         m[hh] = -INFINITY;
         l[hh] = 0.f;
 #pragma unroll
         for (int e = 0; e < E; ++e) acc[hh][e] = 0.f;
     }
-    // keys in batches of up to kB: the batch's K and V loads are all issued before the first
-    // is used, then per head one max and one rescale per batch (scores in log2 units)
-    constexpr int kB = G <= 2 ? 4 : 2;
+    // keys four at a time.  Scores: lane group lg = lane / 8 takes key lg, each lane 8 of every
+    // 64 columns (one 128-byte line per group and load), summed over the group's 8 lanes; then
+    // per head one max and one rescale for the four (scores in log2 units).  Values: lanes over
+    // the head dimension, every key's row loaded before the scores are used.
+    constexpr int kB = 4;
+    const int lg = lane >> 3, ls = lane & 7;
     auto batch = [&](auto rows, int nb) {
-        float kx[kB][E], vx[kB][E];
+        float vx[kB][E];
 #pragma unroll
         for (int b = 0; b < kB; ++b)
-            if (b < nb) {
-                const auto kv = rows(b);
-                load_row<D>(kv.first + lane * E, kx[b]);
-                load_row<D>(kv.second + lane * E, vx[b]);
+            if (b < nb) load_row<D>(rows(b).second + lane * E, vx[b]);
+        float pd[G];
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) pd[hh] = 0.f;
+        if (lg < nb) {
+            const __nv_bfloat16* kr = rows(lg).first;
+            uint4 kp[D / 64];
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) kp[c] = *reinterpret_cast<const uint4*>(kr + 64 * c + 8 * ls);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&kp[c]);
+                float kx[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 f = __bfloat1622float2(b2[j]);
+                    kx[2 * j] = f.x;
+                    kx[2 * j + 1] = f.y;
+                }
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    const float4 q0 = *reinterpret_cast<const float4*>(&qs[hh][64 * c + 8 * ls]);
+                    const float4 q1 = *reinterpret_cast<const float4*>(&qs[hh][64 * c + 8 * ls + 4]);
+                    float t = pd[hh];
+                    t = fmaf(q0.x, kx[0], t);
+                    t = fmaf(q0.y, kx[1], t);
+                    t = fmaf(q0.z, kx[2], t);
+                    t = fmaf(q0.w, kx[3], t);
+                    t = fmaf(q1.x, kx[4], t);
+                    t = fmaf(q1.y, kx[5], t);
+                    t = fmaf(q1.z, kx[6], t);
+                    t = fmaf(q1.w, kx[7], t);
+                    pd[hh] = t;
+                }
             }
+        }
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
+#pragma unroll
+            for (int off = 4; off > 0; off >>= 1) pd[hh] += __shfl_xor_sync(0xffffffffu, pd[hh], off);
             float s[kB];
-#pragma unroll
-            for (int b = 0; b < kB; ++b) {
-                float t = 0.f;
-#pragma unroll
-                for (int e = 0; e < E; ++e) t = fmaf(qv[hh][e], b < nb ? kx[b][e] : 0.f, t);
-                s[b] = t;
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-                for (int b = 0; b < kB; ++b) s[b] += __shfl_xor_sync(0xffffffffu, s[b], off);
             float mb = m[hh];
 #pragma unroll
             for (int b = 0; b < kB; ++b) {
-                s[b] = b < nb ? s[b] * scale_log2 : -INFINITY;
+                const float t = __shfl_sync(0xffffffffu, pd[hh], 8 * b);
+                s[b] = b < nb ? t * scale_log2 : -INFINITY;
                 mb = fmaxf(mb, s[b]);
             }
             const float corr = dev::fast_exp2(m[hh] - mb);
@@ -166,7 +196,7 @@ __global__ void __launch_bounds__(32 * slices<D, G>()) decode_attention_kernel(
             for (int e = 0; e < E; ++e) acc[hh][e] *= corr;
 #pragma unroll
             for (int b = 0; b < kB; ++b)
-                if (b < nb) {   // keys in order within the batch
+                if (b < nb) {   // keys in order within the four
                     const float p = dev::fast_exp2(s[b] - mb);
                     l[hh] += p;
 #pragma unroll
