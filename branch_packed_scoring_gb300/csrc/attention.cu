@@ -19,15 +19,15 @@
 //   warp 0      one TMA producer thread for Q (once per item), K and V tiles: it
 //               polls the buffers' barriers and issues whichever copy is free first
 //               (each tile one 4-D copy of all its 64-column chunks; two K and two V
-//               buffers, or one of each at d_head 256 outside a cta_group::2 pair,
-//               then copied in two halves)
-//   warp 1      TMEM owner and S issuer: S = Q K^T into one of three (d_head <= 128)
-//               or two (d_head 256) TMEM buffers (SS form, fp32)
+//               buffers; at d_head 256 outside a cta_group::2 pair the KV tiles are
+//               the 64-key halves of the planner's tiles, so that two of each fit)
+//   warp 1      TMEM owner and S issuer: S = Q K^T into one of three 128-column
+//               (d_head <= 128) or four 64-column (d_head 256) TMEM buffers (SS, fp32)
 //   warp 2      PV issuer: O += P V (P read from TMEM, V MN-major from shared
 //               memory); two issuing threads, so the tensor core has the other
 //               stream's MMAs to run while one thread commits or waits
 //   warps 3-10  softmax, two warps per TMEM lane quarter: each thread owns half
-//               of one Q row (64 of the 128 key columns, D/2 of the O columns):
+//               of one Q row (half of the tile's key columns, D/2 of the O columns):
 //               mask, online softmax with the row maximum exchanged between the
 //               two halves, P (bf16) into TMEM over its S, rescale O when the
 //               reference maximum moves, final O / l staged per warp in shared
@@ -52,6 +52,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <mutex>
 
@@ -87,29 +88,35 @@ constexpr int kOstageBytes = 32 * 64;  // O staging of one softmax warp: 32 rows
 //   MMA_DONE(_PV)       all MMAs of one issuer thread have completed (before TMEM is freed)
 //   V_HALF, V_FULL_H1   the same for a single V buffer, by key halves: V_HALF says PV(G) has
 //                       read the first 64 keys (V is then kept as [key half][chunk][64 keys])
-//   S_HALF, K_FULL_H1   single K buffer (d_head 256 outside a cta_group::2 pair): the tile
-//                       is copied in two halves of 128 columns; S_HALF says S(G) has read
-//                       the first half, so K(G+1)'s first half may land while S(G) finishes
+//   S_HALF, K_FULL_H1   a single K buffer copied in two halves (no configuration uses one
+//                       now: d_head 256 double-buffers 64-key tiles)
 // In a multicast pair S_FULL and V_DONE count the commits of both CTAs, which read the
 // shared K/V buffers.
 enum {
-    Q_FULL = 0, Q_EMPTY, S_FULL0, S_FULL1, S_FULL2, P_FULL0, P_FULL1, P_FULL2, P_USED0, P_USED1, P_USED2,
-    V_DONE0, V_DONE1, MMA_DONE, MMA_DONE_PV, S_HALF, K_FULL_H1, V_HALF, V_FULL_H1, N_FIXED_BARS
+    Q_FULL = 0, Q_EMPTY, S_FULL0, S_FULL1, S_FULL2, S_FULL3, P_FULL0, P_FULL1, P_FULL2, P_FULL3, P_USED0, P_USED1,
+    P_USED2, P_USED3, V_DONE0, V_DONE1, MMA_DONE, MMA_DONE_PV, S_HALF, K_FULL_H1, V_HALF, V_FULL_H1, N_FIXED_BARS
 };
+
+// Keys per KV tile: 64 at d_head 256 outside a cta_group::2 pair (Q, two K and two V buffers
+// then fit the shared memory: 64 + 4 x 32 KB), else 128.  A 64-key tile is one half of the
+// planner's input-anchored 128-key tile, so a key keeps its column whatever is packed.
+template <int D, int MODE>
+constexpr int kTK = (D == 256 && MODE != 2) ? 64 : 128;
 
 template <int D, int MODE>
 struct AttnSmem {
     static constexpr int kChunks = D / 64;
-    static constexpr int kTileBytes = kChunks * kBoxBytes;
+    static constexpr int kTileBytes = kChunks * kBoxBytes;                  // a 128-row Q tile
+    static constexpr int kKVTile = kChunks * kTK<D, MODE> * 128;           // a K or V tile
     // a cta_group::2 pair keeps half of every K tile (64 keys) and of every V tile (D/2 columns) per CTA
-    static constexpr int kKBytes = MODE == 2 ? kTileBytes / 2 : kTileBytes;
-    static constexpr int kVBytes = MODE == 2 ? kTileBytes / 2 : kTileBytes;
-    static constexpr int kStages = (MODE == 2 || D <= 128) ? 2 : 1;   // K and V buffers each (d 256 alone: one)
+    static constexpr int kKBytes = MODE == 2 ? kTileBytes / 2 : kKVTile;
+    static constexpr int kVBytes = MODE == 2 ? kTileBytes / 2 : kKVTile;
+    static constexpr int kStages = 2;   // K and V buffers each
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kTileBytes;                // K stage s at kK + s * kKBytes
     static constexpr int kV = kK + kStages * kKBytes;
-    static constexpr int kMeta = kV + kStages * kVBytes;    // int32 [kMetaSlots][2][128]: end[], pos[] of a tile's keys
-    static constexpr int kMetaHead = kMeta + kMetaSlots * 2 * 128 * 4;   // int32 [kMetaSlots][4]: min end, min pos, kv0, len
+    static constexpr int kMeta = kV + kStages * kVBytes;    // int32 [kMetaSlots][2][kTK]: end[], pos[] of a tile's keys
+    static constexpr int kMetaHead = kMeta + kMetaSlots * 2 * kTK<D, MODE> * 4;   // int32 [kMetaSlots][4]: min end, min pos, kv0, len
     static constexpr int kXmax = kMetaHead + kMetaSlots * 4 * 4;   // float [2][2][128]: row maxima of the two halves
     static constexpr int kLx = kXmax + 2 * 2 * 128 * 4;     // float [2][128]: the halves' row sums, per item
     static constexpr int kOstage = (kLx + 2 * 128 * 4 + 1023) / 1024 * 1024;  // per softmax warp: 32 x 32 O bf16
@@ -122,16 +129,16 @@ struct AttnSmem {
     static_assert(kAlloc <= 227 * 1024, "shared memory of one CTA");
 };
 
-// TMEM columns: S buffers of 128 columns -- tile G uses buffer G % kSBufs, and its P
-// (bf16 pairs, 64 columns) overwrites the start of that buffer once the softmax has
-// read S -- then O (D columns).  d_head 256: two buffers, O at 256; d_head <= 128: a
-// third buffer, O at 384, so S of tile G waits for the PV of tile G - 3 (usually long
-// done) rather than G - 2.  512 columns are allocated, so one CTA per SM (the
+// TMEM columns: S buffers of one column per key of a KV tile -- tile G uses buffer
+// G % kSBufs, and its P (bf16 pairs, half as many columns) overwrites the start of that
+// buffer once the softmax has read S -- then O (D columns).  d_head 256: four 64-column
+// buffers, O at 256; d_head <= 128: three 128-column buffers, O at 384, so S of tile G
+// waits for the PV of tile G - kSBufs (usually long done).  512 columns are allocated, so one CTA per SM (the
 // shared-memory request enforces it and no allocation ever waits).
 template <int D>
-constexpr int kSBufs = D <= 128 ? 3 : 2;
+constexpr int kSBufs = D <= 128 ? 3 : 4;
 template <int D>
-constexpr uint32_t kColO = kSBufs<D> * 128;
+constexpr uint32_t kColO = D <= 128 ? 384 : 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMinSmem = 116 * 1024;
 // Log2 headroom of the lazy softmax reference maximum: P values stay <= 2^8.
@@ -158,7 +165,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     using L = AttnSmem<D, MODE>;
     constexpr bool PAIR = MODE != 0;
     constexpr bool CG2 = MODE == 2;
-    constexpr bool kHalfK = L::kStages == 1;   // single K buffer: copied in two halves
+    constexpr bool kHalfK = L::kStages == 1;   // single K buffer: copied in two halves (not used now)
+    constexpr int TK = kTK<D, MODE>;           // keys per KV tile
+    constexpr int KH = TK / 2;                 // keys per softmax thread (half of a tile's row)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem + L::kQ;
@@ -196,15 +205,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint64_t* v_full = k_full + L::kStages;
     uint64_t* v_done = bars + V_DONE0;   // [2], by tile parity
     // barrier that says P(G) has been read, and its phase index is G / kSBufs
-    auto p_used = [&](uint32_t G) { return kSBufs<D> == 3 ? &bars[P_USED0 + G % 3] : &v_done[G & 1]; };
+    auto p_used = [&](uint32_t G) { return kSBufs<D> >= 3 ? &bars[P_USED0 + G % kSBufs<D>] : &v_done[G & 1]; };
     uint64_t* meta_full = v_full + L::kStages;
     uint64_t* meta_empty = meta_full + kMetaSlots;
     if (threadIdx.x == 0) {
         // P_FULL: every softmax thread, or (CG2) one arrival from each CTA of the pair
         for (int b = 0; b < N_FIXED_BARS; ++b) {
             int count = 1;
-            if (b >= P_FULL0 && b <= P_FULL2) count = CG2 ? 2 : kSoftmaxThreads;
-            if (((b >= S_FULL0 && b <= S_FULL2) || b == V_DONE0 || b == V_DONE1 || b == S_HALF || b == V_HALF) &&
+            if (b >= P_FULL0 && b <= P_FULL3) count = CG2 ? 2 : kSoftmaxThreads;
+            if (((b >= S_FULL0 && b <= S_FULL3) || b == V_DONE0 || b == V_DONE1 || b == S_HALF || b == V_HALF) &&
                 MODE == 1)
                 count = 2;   // both CTAs' MMAs
             mbar_init(&bars[b], count);
@@ -333,7 +342,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                 tma_load_4d_pair(dst, &tm_kh, mapa_shared(smem_u32(&k_full[st]), 0), 0,
                                                  kc.kv0 + 64 * rank, 0, kc.I.h / group);
                             } else {
-                                mbar_arrive_expect_tx(&k_full[st], L::kTileBytes);
+                                mbar_arrive_expect_tx(&k_full[st], L::kKBytes);
                                 if (!PAIR) tma_load_4d(dst, &tm_k, &k_full[st], 0, kc.kv0, 0, kc.I.h / group);
                                 else if ((G & 1) == (uint32_t)rank)   // the pair's CTAs take alternate K tiles
                                     tma_load_4d_mc(dst, &tm_k, &k_full[st], 0, kc.kv0, 0, kc.I.h / group, kBoth);
@@ -371,7 +380,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             tma_load_4d_pair(dst, &tm_v, mapa_shared(smem_u32(&v_full[st]), 0), 0, vc.kv0,
                                              rank * (L::kChunks / 2), vc.I.h / group);
                         } else {
-                            mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
+                            mbar_arrive_expect_tx(&v_full[st], L::kVBytes);
                             if (!PAIR) tma_load_4d(dst, &tm_v, &v_full[st], 0, vc.kv0, 0, vc.I.h / group);
                             else if ((G & 1) != (uint32_t)rank)   // the other CTA of the pair takes this V tile
                                 tma_load_4d_mc(dst, &tm_v, &v_full[st], 0, vc.kv0, 0, vc.I.h / group, kBoth);
@@ -425,7 +434,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // S = Q K^T from warp 1, O += P V from warp 2: two instruction streams, so the tensor
         // core has the other stream's MMAs to run while one thread commits or waits
         if (lane == 0 && (!CG2 || rank == 0)) {   // a pair's MMAs are all issued by its leader
-            constexpr uint32_t idesc_qk = idesc_bf16(CG2 ? 256 : 128, 128, false, false);
+            constexpr uint32_t idesc_qk = idesc_bf16(CG2 ? 256 : 128, TK, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16(CG2 ? 256 : 128, D, false, true);
             auto commit = [&](uint64_t* bar) {
                 if constexpr (CG2) mma_commit_pair(bar); else mma_commit(bar);
@@ -457,9 +466,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const uint32_t st = Gs % L::kStages;
                         mbar_wait(&k_full[st], (Gs / L::kStages) & 1, err);
                         tc_fence_after();
-                        const uint32_t dS = tmem + (Gs % kSBufs<D>) * 128;
+                        const uint32_t dS = tmem + (Gs % kSBufs<D>) * TK;
                         const uint32_t aKs = aK + st * L::kKBytes;
-                        constexpr int kKBox = CG2 ? kBoxBytes / 2 : kBoxBytes;   // K boxes hold 64 or 128 keys
+                        constexpr int kKBox = CG2 ? kBoxBytes / 2 : TK * 128;   // K boxes hold 64 or 128 keys
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             if (kHalfK && kk == D / 32) {   // first half read; second half landed?
@@ -485,10 +494,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const uint32_t st = Gj % L::kStages;
                         mbar_wait(&v_full[st], (Gj / L::kStages) & 1, err);
                         tc_fence_after();
-                        const uint32_t aP = tmem + (Gj % kSBufs<D>) * 128;
+                        const uint32_t aP = tmem + (Gj % kSBufs<D>) * TK;
                         const uint32_t aVs = aV + st * L::kVBytes;
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {   // 16 keys: 8 TMEM columns of bf16 pairs of P
+                        for (int kk = 0; kk < TK / 16; ++kk) {   // 16 keys: 8 TMEM columns of bf16 pairs of P
                             if (kHalfK && kk == 4) {   // first 64 keys read; the other half landed?
                                 commit_shared(&bars[V_HALF]);
                                 mbar_wait(&bars[V_FULL_H1], Gj & 1, err);
@@ -497,14 +506,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             // V as [chunk][128 keys] boxes, or (single V buffer) [key half][chunk][64 keys]
                             const uint64_t db =
                                 kHalfK ? sdesc_sw128(aVs + (kk >> 2) * (L::kTileBytes / 2) + (kk & 3) * 2048, kBoxBytes / 2, 1024)
-                                       : sdesc_sw128(aVs + kk * 2048, kBoxBytes, 1024);
+                                       : sdesc_sw128(aVs + kk * 2048, TK * 128, 1024);
                             // an item's first product overwrites O (adding it to zero would give the same bits)
                             const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
                             if constexpr (CG2) mma_f16_ts_pair(tmem + kColO<D>, aP + kk * 8, db, idesc_pv, acc);
                             else mma_f16_ts(tmem + kColO<D>, aP + kk * 8, db, idesc_pv, acc);
                         }
                         commit_shared(&v_done[Gj & 1]);
-                        if constexpr (kSBufs<D> == 3) commit(&bars[P_USED0 + Gj % 3]);
+                        if constexpr (kSBufs<D> >= 3) commit(&bars[P_USED0 + Gj % kSBufs<D>]);
                     }
                 }
                 G += I.n;
@@ -517,7 +526,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
     } else if (warp == kMetaWarp) {
         // ---------------------------------------------------------- mask metadata of each KV tile
-        // end[] and pos[] of the tile's 128 keys (keys past the tile's own input: end -1,
+        // end[] and pos[] of the tile's keys (keys past the tile's own input: end -1,
         // pos 0), their minima, kv0 and the length, into a ring read by the softmax warps;
         // this warp's global loads run up to kMetaSlots tiles ahead of the softmax
         uint32_t G = 0;
@@ -529,21 +538,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int j = 0; j < I.n; ++j, ++G) {
                 const int slot = G % kMetaSlots;
                 const int kv0 = __ldg(tile_kv + I.s0 + j), len = __ldg(tile_len + I.s0 + j);
-                int ev[4], pv[4];
+                constexpr int kPer = TK / 32;   // keys per lane
+                int ev[kPer], pv[kPer];
+                int emin = INT_MAX, pmin = INT_MAX;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < kPer; ++i) {
                     const int key = lane + 32 * i;
                     ev[i] = key < len ? __ldg(end + kv0 + key) : -1;
                     pv[i] = key < len ? __ldg(pos + kv0 + key) : 0;
+                    emin = min(emin, ev[i]);
+                    pmin = min(pmin, pv[i]);
                 }
-                const int emin = __reduce_min_sync(0xffffffffu, min(min(ev[0], ev[1]), min(ev[2], ev[3])));
-                const int pmin = __reduce_min_sync(0xffffffffu, min(min(pv[0], pv[1]), min(pv[2], pv[3])));
+                emin = __reduce_min_sync(0xffffffffu, emin);
+                pmin = __reduce_min_sync(0xffffffffu, pmin);
                 if (G >= (uint32_t)kMetaSlots) mbar_wait(&meta_empty[slot], (G / kMetaSlots - 1) & 1, err);
-                int32_t* me = meta + slot * 256;
+                int32_t* me = meta + slot * 2 * TK;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < kPer; ++i) {
                     me[lane + 32 * i] = ev[i];
-                    me[128 + lane + 32 * i] = pv[i];
+                    me[TK + lane + 32 * i] = pv[i];
                 }
                 if (lane == 0)
                     *reinterpret_cast<int4*>(meta_head + 4 * slot) = make_int4(emin, pmin, kv0, len);
@@ -587,25 +600,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const int4 head = *reinterpret_cast<const int4*>(meta_head + 4 * slot);   // min end, min pos, kv0, len
                 mbar_wait(&bars[S_FULL0 + sb], (G / kSBufs<D>) & 1, err);
                 tc_fence_after();
-                const uint32_t tS = tmem + lane_off + sb * 128;
-                float s[64];
+                const uint32_t tS = tmem + lane_off + sb * TK;
+                float s[KH];
                 {
-                    uint32_t rr[64];
-                    tmem_ld64(tS + half * 64, rr);
+                    uint32_t rr[KH];
+                    if constexpr (KH == 64) tmem_ld64(tS + half * KH, rr);
+                    else tmem_ld32(tS + half * KH, rr);
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(rr[i]);
+                    for (int i = 0; i < KH; ++i) s[i] = __uint_as_float(rr[i]);
                 }
                 // visible: kv0 + c <= q_row (causal), q_row < end[key], window on depth.
                 // A tile whose every key is visible to this row skips the per-key test.
                 const int cmax = real ? q_row - head.z : -1;
                 const bool all_visible =
-                    cmax >= 127 && head.x > q_row && (window <= 0 || pos_q - head.y < window);
+                    cmax >= TK - 1 && head.x > q_row && (window <= 0 || pos_q - head.y < window);
                 float mx = -INFINITY;
-                // maximum of the 64 values, two independent chains of three-input maxima
+                // maximum of the KH values, two independent chains of three-input maxima
                 auto max64 = [&]() {
                     float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-                    for (int i = 0; i < 64; i += 4) {
+                    for (int i = 0; i < KH; i += 4) {
                         m0 = fmax3(m0, s[i], s[i + 1]);
                         m1 = fmax3(m1, s[i + 2], s[i + 3]);
                     }
@@ -615,9 +629,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     mx = max64();
                 } else if (window <= 0 && run01.x >= 0) {
                     // visible keys of this half from the row's runs: no per-key loads
-                    const int kb = head.z + 64 * half;
+                    const int kb = head.z + KH * half;
                     auto bits = [&](int lo, int hi) -> uint64_t {
-                        const int a = max(lo - kb, 0), b = min(hi - kb, 64);
+                        const int a = max(lo - kb, 0), b = min(hi - kb, KH);
                         if (a >= b) return 0ull;
                         const uint64_t upto = b == 64 ? ~0ull : ((1ull << b) - 1ull);
                         return upto & ~((1ull << a) - 1ull);
@@ -626,18 +640,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                   bits(run23.z, run23.w);
                     // only the tile's own keys: the rest belong to the next input, whose own
                     // anchored tiles cover them
-                    const int lim = min(max(head.w - 64 * half, 0), 64);
+                    const int lim = min(max(head.w - KH * half, 0), KH);
                     if (lim < 64) vm &= (1ull << lim) - 1ull;
                     if (!real) vm = 0ull;
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) s[i] = ((vm >> i) & 1ull) ? s[i] : -INFINITY;
+                    for (int i = 0; i < KH; ++i) s[i] = ((vm >> i) & 1ull) ? s[i] : -INFINITY;
                     mx = max64();
                 } else {
-                    const int4* e4 = reinterpret_cast<const int4*>(meta + slot * 256 + half * 64);
-                    const int4* p4 = reinterpret_cast<const int4*>(meta + slot * 256 + 128 + half * 64);
-                    const int cm = cmax - half * 64;
+                    const int4* e4 = reinterpret_cast<const int4*>(meta + slot * 2 * TK + half * KH);
+                    const int4* p4 = reinterpret_cast<const int4*>(meta + slot * 2 * TK + TK + half * KH);
+                    const int cm = cmax - half * KH;
 #pragma unroll
-                    for (int c4 = 0; c4 < 16; ++c4) {
+                    for (int c4 = 0; c4 < KH / 4; ++c4) {
                         const int4 e = e4[c4];
                         bool v0 = 4 * c4 + 0 <= cm && q_row < e.x;
                         bool v1 = 4 * c4 + 1 <= cm && q_row < e.y;
@@ -670,18 +684,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const float m_hi = fmaxf(m, mx_row);
                 const bool grow = m != -INFINITY && (m_hi - m) * scale_log2 > kRescaleLog2;
                 const float m_new = (m == -INFINITY || grow) ? m_hi : m;
-                uint32_t pk[32];
+                uint32_t pk[KH / 2];
                 float alpha = 1.f;
                 float rowsum = 0.f;
                 if (m_new == -INFINITY) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) pk[i] = 0u;
+                    for (int i = 0; i < KH / 2; ++i) pk[i] = 0u;
                 } else {
                     const float mb = m_new * scale_log2;
                     const float2 sc2 = make_float2(scale_log2, scale_log2), nb2 = make_float2(-mb, -mb);
                     float2 acc = make_float2(0.f, 0.f);   // even and odd columns, added at the end
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
+                    for (int c = 0; c < KH / 2; ++c) {
                         const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), sc2, nb2);
                         const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
                         acc = fadd2(acc, p);
@@ -715,9 +729,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         tmem_st32(tO + c * 32, rr);
                     }
                 }
-                // P of keys [64 half, 64 half + 64) -> bf16 pairs in columns [32 half, 32 half + 32)
+                // P of keys [KH half, KH half + KH) -> bf16 pairs in columns [KH/2 half, KH/2 half + KH/2)
                 // of this tile's S buffer (both halves have read their S columns before the pair barrier)
-                tmem_st32(tS + half * 32, pk);
+                if constexpr (KH == 64) tmem_st32(tS + half * 32, pk);
+                else tmem_st16(tS + half * 16, pk);
                 tmem_st_wait();
                 tc_fence_before();
                 if constexpr (CG2) {   // one arrival per CTA on the leader's barrier
@@ -888,16 +903,17 @@ spinf_status launch_attention(const Pass& P, const Sched& sc, const void* q, con
     // multicast pair measured faster: its softmax warps are not coupled across the two SMs)
     // the kernel's third map: a K tile's key half (cta_group::2 pair) or column half (single K
     // buffer); with a single V buffer (d_head 256) V is copied by key halves
-    const CUtensorMap& kpart = D == 256 ? tkc : tkh;
+    // d_head 256: 64-key K and V tiles (boxes of 64 rows), on the 64-key schedule
     CUtensorMap tvk;
     if ((st = make_tmap(&tvk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dk, sk, kbox_half, CU_TENSOR_MAP_SWIZZLE_128B)))
         return st;
+    const CUtensorMap& kmap = D == 256 ? tkh : tk;
     const CUtensorMap& vmap = D == 256 ? tvk : tv;
-    if ((Hq / Hkv) % 2 != 0) return launch_mode<D, 0>(P, sc, tq, tk, kpart, vmap, ob, Hq, Hkv, scale_log2, window, err, stream);
+    if ((Hq / Hkv) % 2 != 0) return launch_mode<D, 0>(P, sc, tq, kmap, tkh, vmap, ob, Hq, Hkv, scale_log2, window, err, stream);
     if constexpr (D == 128)
         return launch_mode<D, 2>(P, sc, tq, tk, tkh, tvh, ob, Hq, Hkv, scale_log2, window, err, stream);
     else
-        return launch_mode<D, 1>(P, sc, tq, tk, kpart, vmap, ob, Hq, Hkv, scale_log2, window, err, stream);
+        return launch_mode<D, 1>(P, sc, tq, kmap, tkh, vmap, ob, Hq, Hkv, scale_log2, window, err, stream);
 }
 
 }  // namespace
@@ -919,11 +935,12 @@ extern "C" spinf_status spinf_branch_attention(const spinf_plan* plan, int32_t p
     const Pass& P = plan->passes[pass];
     if (d_head != 64 && d_head != 128 && d_head != 256) return fail(SPINF_E_UNSUPPORTED, "d_head must be 64, 128 or 256");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // with a window, the schedule without the tiles no row of a Q tile sees within it
+    // with a window, the schedule without the tiles no row of a Q tile sees within it;
+    // d_head 256 walks the 64-key halves of the schedule's tiles (those some row sees)
     Sched sc{P.dev.qt_work, P.dev.tile_kv, P.dev.tile_len};
-    if (window > 0 && P.T > 0) {
+    if ((window > 0 || d_head == 256) && P.T > 0) {
         std::lock_guard<std::mutex> lock(const_cast<spinf_plan*>(plan)->cache_mu);
-        WindowSchedule& w = window_schedule(const_cast<Pass&>(P), window);
+        WindowSchedule& w = tile_schedule(const_cast<Pass&>(P), window, d_head == 256 ? 64 : kTile);
         if ((st = upload_window(w, s))) return st;
         sc = Sched{w.d_qt_work, w.d_tile_kv, w.d_tile_len};
     }

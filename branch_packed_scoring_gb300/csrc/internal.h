@@ -40,7 +40,8 @@ struct PassDevice {
 // The KV-tile schedule of one pass for a sliding window W: the W = 0 schedule without
 // the tiles in which no row of the Q tile sees any key within W (built on first use).
 struct WindowSchedule {
-    int32_t window = 0;
+    int32_t window = 0;      // 0: no window
+    int32_t key_tile = 128;  // keys per KV tile: 128, or 64 (the halves of the 128-key tiles)
     std::vector<int32_t> tile_ptr, tile_kv, tile_len, qt_work;
     void* block = nullptr;   // device copies of qt_work, tile_kv, tile_len (plan-owned)
     int32_t *d_qt_work = nullptr, *d_tile_kv = nullptr, *d_tile_len = nullptr;
@@ -102,4 +103,6 @@ spinf_status fail(spinf_status s, const std::string& msg);
 spinf_status ok();
 // The pass's schedule for window W > 0, built on first use and kept by the plan.
 WindowSchedule& window_schedule(Pass& P, int32_t window);
+// The schedule for window W >= 0 in KV tiles of `key_tile` keys (128 or 64), built on first use.
+WindowSchedule& tile_schedule(Pass& P, int32_t window, int32_t key_tile);
 }  // namespace spinf

@@ -198,11 +198,18 @@ bool ids_in_range(const spinf_tokens& t, int32_t vocab) {
 
 namespace spinf {
 
-WindowSchedule& window_schedule(Pass& P, int32_t window) {
+WindowSchedule& window_schedule(Pass& P, int32_t window) { return tile_schedule(P, window, kTile); }
+
+// The schedule for window W (0: none) in KV tiles of `key_tile` keys (128, or 64: each
+// input-anchored 128-key tile taken as its two halves): a tile stays iff some row of the Q
+// tile sees one of its keys (within the window).  Skipping a tile that no row sees changes
+// no bit of the result.
+WindowSchedule& tile_schedule(Pass& P, int32_t window, int32_t key_tile) {
     for (auto& w : P.windows)
-        if (w->window == window) return *w;
+        if (w->window == window && w->key_tile == key_tile) return *w;
     auto ws = std::make_unique<WindowSchedule>();
     ws->window = window;
+    ws->key_tile = key_tile;
     const int32_t n_qt = P.T_pad / kTile;
     ws->tile_ptr.assign(1, 0);
     int32_t mins[8][kTile];   // sparse table of pos over one Q tile's real rows
@@ -218,15 +225,18 @@ WindowSchedule& window_schedule(Pass& P, int32_t window) {
             return std::min(mins[l][lo - r0], mins[l][hi - r0 - (1 << l)]);
         };
         for (int32_t e = P.tile_ptr[qt]; e < P.tile_ptr[qt + 1]; ++e) {
-            const int32_t kv0 = P.tile_kv[e], len = P.tile_len[e];
-            bool keep = false;
-            for (int32_t k = kv0; k < kv0 + len && !keep; ++k) {   // rows that see k: [max(k, r0), min(end[k], r1))
-                const int32_t lo = std::max(k, r0), hi = std::min(P.end[k], r1);
-                keep = lo < hi && range_min(lo, hi) - P.pos[k] < window;
-            }
-            if (keep) {
-                ws->tile_kv.push_back(kv0);
-                ws->tile_len.push_back(len);
+            for (int32_t sub = 0; sub < kTile; sub += key_tile) {
+                const int32_t kv0 = P.tile_kv[e] + sub, len = std::min(P.tile_len[e] - sub, key_tile);
+                if (len <= 0) break;
+                bool keep = false;
+                for (int32_t k = kv0; k < kv0 + len && !keep; ++k) {   // rows that see k: [max(k, r0), min(end[k], r1))
+                    const int32_t lo = std::max(k, r0), hi = std::min(P.end[k], r1);
+                    keep = lo < hi && (window <= 0 || range_min(lo, hi) - P.pos[k] < window);
+                }
+                if (keep) {
+                    ws->tile_kv.push_back(kv0);
+                    ws->tile_len.push_back(len);
+                }
             }
         }
         ws->tile_ptr.push_back((int32_t)ws->tile_kv.size());
