@@ -261,8 +261,8 @@ size_t spinf_plan_descriptor_bytes(const spinf_plan* plan, int32_t pass);
 spinf_status spinf_plan_upload_to(spinf_plan* plan, int32_t pass, void* buffer, size_t bytes,
                                   spinf_stream stream);
 
-/* Tree-masked GQA attention over one packed pass (spec: the branch
- * attention kernel; pages: "spinf-serve 0.1.1", "Speed and scale").
+/* Tree-masked GQA attention over one packed pass ("spinf-serve 0.1.1",
+ * "Speed and scale": one pass reads each content once, its questions branch off it).
  *
  * For every row q < T and query head h (kv head g = h * Hkv / Hq):
  *   o[q,h,:] = sum_k softmax_k(scale * q[q,h,:] . k[k,g,:]) v[k,g,:]
