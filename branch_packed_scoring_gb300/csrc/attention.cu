@@ -86,15 +86,11 @@ constexpr int kOstageBytes = 32 * 64;  // O staging of one softmax warp: 32 rows
 //                       into different accumulators are not ordered by the tensor core.
 //   V_DONE[G & 1]       PV(G) has finished: O may be read or rescaled, its V buffer is free
 //   MMA_DONE(_PV)       all MMAs of one issuer thread have completed (before TMEM is freed)
-//   V_HALF, V_FULL_H1   the same for a single V buffer, by key halves: V_HALF says PV(G) has
-//                       read the first 64 keys (V is then kept as [key half][chunk][64 keys])
-//   S_HALF, K_FULL_H1   a single K buffer copied in two halves (no configuration uses one
-//                       now: d_head 256 double-buffers 64-key tiles)
 // In a multicast pair S_FULL and V_DONE count the commits of both CTAs, which read the
 // shared K/V buffers.
 enum {
     Q_FULL = 0, Q_EMPTY, S_FULL0, S_FULL1, S_FULL2, S_FULL3, P_FULL0, P_FULL1, P_FULL2, P_FULL3, P_USED0, P_USED1,
-    P_USED2, P_USED3, V_DONE0, V_DONE1, MMA_DONE, MMA_DONE_PV, S_HALF, K_FULL_H1, V_HALF, V_FULL_H1, N_FIXED_BARS
+    P_USED2, P_USED3, V_DONE0, V_DONE1, MMA_DONE, MMA_DONE_PV, N_FIXED_BARS
 };
 
 // Keys per KV tile: 64 at d_head 256 outside a cta_group::2 pair (Q, two K and two V buffers
@@ -165,7 +161,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     using L = AttnSmem<D, MODE>;
     constexpr bool PAIR = MODE != 0;
     constexpr bool CG2 = MODE == 2;
-    constexpr bool kHalfK = L::kStages == 1;   // single K buffer: copied in two halves (not used now)
     constexpr int TK = kTK<D, MODE>;           // keys per KV tile
     constexpr int KH = TK / 2;                 // keys per softmax thread (half of a tile's row)
     extern __shared__ uint8_t smem_raw[];
@@ -213,8 +208,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int b = 0; b < N_FIXED_BARS; ++b) {
             int count = 1;
             if (b >= P_FULL0 && b <= P_FULL3) count = CG2 ? 2 : kSoftmaxThreads;
-            if (((b >= S_FULL0 && b <= S_FULL3) || b == V_DONE0 || b == V_DONE1 || b == S_HALF || b == V_HALF) &&
-                MODE == 1)
+            if (((b >= S_FULL0 && b <= S_FULL3) || b == V_DONE0 || b == V_DONE1) && MODE == 1)
                 count = 2;   // both CTAs' MMAs
             mbar_init(&bars[b], count);
         }
@@ -288,8 +282,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             seek(kc);
             seek(vc);
             uint32_t ic = 0;          // Q copies issued
-            int k_part = 0;           // half of the K tile to copy next (single K buffer)
-            int v_part = 0;           // half of the V tile to copy next (single V buffer)
             bool q_pending = true;    // the K cursor's item still needs its Q
             unsigned long long t_idle = 0;
             while (!kc.done || !vc.done) {
@@ -308,27 +300,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             }
                             ++ic;
                             q_pending = false;
-                            progress = true;
-                        }
-                    } else if constexpr (kHalfK) {
-                        // two copies per tile, each of half the columns: the first waits for S(G-1)
-                        // to have read the first half only
-                        const uint32_t G = kc.G, Gp = G - 1;
-                        if (G == 0 || (k_part == 0 ? mbar_test(&bars[S_HALF], Gp & 1)
-                                                   : mbar_test(&bars[S_FULL0 + Gp % kSBufs<D>], (Gp / kSBufs<D>) & 1))) {
-                            uint64_t* fb = k_part == 0 ? &k_full[0] : &bars[K_FULL_H1];
-                            uint8_t* dst = sK + k_part * (L::kTileBytes / 2);
-                            mbar_arrive_expect_tx(fb, L::kTileBytes / 2);
-                            if (!PAIR) tma_load_4d(dst, &tm_kh, fb, 0, kc.kv0, k_part * (L::kChunks / 2), kc.I.h / group);
-                            else if ((G & 1) == (uint32_t)rank)   // the pair's CTAs take alternate K tiles
-                                tma_load_4d_mc(dst, &tm_kh, fb, 0, kc.kv0, k_part * (L::kChunks / 2), kc.I.h / group,
-                                               kBoth);
-                            if (++k_part == 2) {
-                                k_part = 0;
-                                const int k_before = kc.k;
-                                advance(kc);
-                                if (kc.k != k_before) q_pending = true;
-                            }
                             progress = true;
                         }
                     } else {
@@ -354,23 +325,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         }
                     }
                 }
-                if constexpr (kHalfK) {   // single V buffer: two copies per tile, by key halves
-                    const uint32_t G = vc.G, Gp = G - 1;
-                    if (!vc.done && (G == 0 || (v_part == 0 ? mbar_test(&bars[V_HALF], Gp & 1)
-                                                            : mbar_test(&v_done[Gp & 1], (Gp >> 1) & 1)))) {
-                        uint64_t* fb = v_part == 0 ? &v_full[0] : &bars[V_FULL_H1];
-                        uint8_t* dst = sV + v_part * (L::kTileBytes / 2);
-                        mbar_arrive_expect_tx(fb, L::kTileBytes / 2);
-                        if (!PAIR) tma_load_4d(dst, &tm_v, fb, 0, vc.kv0 + 64 * v_part, 0, vc.I.h / group);
-                        else if ((G & 1) != (uint32_t)rank)   // the other CTA of the pair takes this V tile
-                            tma_load_4d_mc(dst, &tm_v, fb, 0, vc.kv0 + 64 * v_part, 0, vc.I.h / group, kBoth);
-                        if (++v_part == 2) {
-                            v_part = 0;
-                            advance(vc);
-                        }
-                        progress = true;
-                    }
-                } else if (!vc.done) {
+                if (!vc.done) {
                     const uint32_t G = vc.G, Gp = G - L::kStages;   // PV(Gp) was the last reader of the buffer
                     if (G < (uint32_t)L::kStages || mbar_test(&v_done[Gp & 1], (Gp >> 1) & 1)) {
                         const uint32_t st = G % L::kStages;
@@ -407,22 +362,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // another thread or CTA makes to our barriers has arrived
             // (CG2: a peer's copies are counted on the leader, whose release implies they landed)
             const uint32_t GK = kc.G, GV = vc.G;
-            for (uint32_t b = GK > (uint32_t)L::kStages ? GK - L::kStages : 0; b < GK; ++b) {
+            for (uint32_t b = GK > (uint32_t)L::kStages ? GK - L::kStages : 0; b < GK; ++b)
                 if (!CG2 || rank == 0) mbar_drain(&k_full[b % L::kStages], (b / L::kStages) & 1, err);
-                if (kHalfK) {
-                    mbar_drain(&bars[K_FULL_H1], b & 1, err);
-                    mbar_drain(&bars[S_HALF], b & 1, err);
-                }
-            }
             for (uint32_t b = GK > (uint32_t)kSBufs<D> ? GK - kSBufs<D> : 0; b < GK; ++b)
                 mbar_drain(&bars[S_FULL0 + b % kSBufs<D>], (b / kSBufs<D>) & 1, err);
-            for (uint32_t b = GV > (uint32_t)L::kStages ? GV - L::kStages : 0; b < GV; ++b) {
+            for (uint32_t b = GV > (uint32_t)L::kStages ? GV - L::kStages : 0; b < GV; ++b)
                 if (!CG2 || rank == 0) mbar_drain(&v_full[b % L::kStages], (b / L::kStages) & 1, err);
-                if (kHalfK) {
-                    mbar_drain(&bars[V_FULL_H1], b & 1, err);
-                    mbar_drain(&bars[V_HALF], b & 1, err);
-                }
-            }
             for (uint32_t b = GV > 2u ? GV - 2 : 0; b < GV; ++b) mbar_drain(&v_done[b & 1], (b >> 1) & 1, err);
             if (ic > 0) {
                 if (!CG2 || rank == 0) mbar_drain(&bars[Q_FULL], (ic - 1) & 1, err);
@@ -471,11 +416,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         constexpr int kKBox = CG2 ? kBoxBytes / 2 : TK * 128;   // K boxes hold 64 or 128 keys
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
-                            if (kHalfK && kk == D / 32) {   // first half read; second half landed?
-                                commit_shared(&bars[S_HALF]);
-                                mbar_wait(&bars[K_FULL_H1], Gs & 1, err);
-                                tc_fence_after();
-                            }
                             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
                             const uint32_t koff = (kk >> 2) * kKBox + (kk & 3) * 32;
                             const uint64_t da = sdesc_sw128(aQ + off, 16, 1024), db = sdesc_sw128(aKs + koff, 16, 1024);
@@ -498,15 +438,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const uint32_t aVs = aV + st * L::kVBytes;
 #pragma unroll
                         for (int kk = 0; kk < TK / 16; ++kk) {   // 16 keys: 8 TMEM columns of bf16 pairs of P
-                            if (kHalfK && kk == 4) {   // first 64 keys read; the other half landed?
-                                commit_shared(&bars[V_HALF]);
-                                mbar_wait(&bars[V_FULL_H1], Gj & 1, err);
-                                tc_fence_after();
-                            }
-                            // V as [chunk][128 keys] boxes, or (single V buffer) [key half][chunk][64 keys]
-                            const uint64_t db =
-                                kHalfK ? sdesc_sw128(aVs + (kk >> 2) * (L::kTileBytes / 2) + (kk & 3) * 2048, kBoxBytes / 2, 1024)
-                                       : sdesc_sw128(aVs + kk * 2048, TK * 128, 1024);
+                            // V as [chunk][TK keys] boxes: 16 keys of every chunk at kk * 2048
+                            const uint64_t db = sdesc_sw128(aVs + kk * 2048, TK * 128, 1024);
                             // an item's first product overwrites O (adding it to zero would give the same bits)
                             const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
                             if constexpr (CG2) mma_f16_ts_pair(tmem + kColO<D>, aP + kk * 8, db, idesc_pv, acc);
@@ -872,7 +805,7 @@ spinf_status launch_mode(const Pass& P, const Sched& sc, const CUtensorMap& tq, 
 template <int D>
 spinf_status launch_attention(const Pass& P, const Sched& sc, const void* q, const void* k, const void* v, void* o, int Hq,
                               int Hkv, float scale, int window, int* err, cudaStream_t stream) {
-    CUtensorMap tq, tk, tkh, tkc, tv, tvh;
+    CUtensorMap tq, tk, tkh, tv, tvh, tvk;
     // 4-D views (64 columns, rows, 64-column chunks, head): one box holds every chunk of a
     // tile, laid out chunk after chunk (128-byte swizzled rows), as the MMA descriptors expect
     constexpr uint32_t kCh = D / 64;
@@ -890,23 +823,19 @@ spinf_status launch_attention(const Pass& P, const Sched& sc, const void* q, con
         return st;
     if ((st = make_tmap(&tkh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k, dk, sk, kbox_half, CU_TENSOR_MAP_SWIZZLE_128B)))
         return st;
-    if ((st = make_tmap(&tkc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k, dk, sk, vbox_half, CU_TENSOR_MAP_SWIZZLE_128B)))
-        return st;   // half of a K tile's columns (single K buffer, copied in two halves)
     if ((st = make_tmap(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dk, sk, box, CU_TENSOR_MAP_SWIZZLE_128B)))
         return st;
     if ((st = make_tmap(&tvh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dk, sk, vbox_half, CU_TENSOR_MAP_SWIZZLE_128B)))
+        return st;
+    if ((st = make_tmap(&tvk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dk, sk, kbox_half, CU_TENSOR_MAP_SWIZZLE_128B)))
         return st;
     __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
     const float scale_log2 = scale * 1.4426950408889634f;
     // an even number of query heads per kv head pairs two heads per item: d_head 128 as a
     // cta_group::2 pair (half tiles), d_head 64 and 256 as a multicast pair (at 256 the
     // multicast pair measured faster: its softmax warps are not coupled across the two SMs)
-    // the kernel's third map: a K tile's key half (cta_group::2 pair) or column half (single K
-    // buffer); with a single V buffer (d_head 256) V is copied by key halves
-    // d_head 256: 64-key K and V tiles (boxes of 64 rows), on the 64-key schedule
-    CUtensorMap tvk;
-    if ((st = make_tmap(&tvk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dk, sk, kbox_half, CU_TENSOR_MAP_SWIZZLE_128B)))
-        return st;
+    // the kernel's third map: a K tile's key half (cta_group::2 pair, d_head 128); d_head 256
+    // copies 64-key K and V tiles (boxes of 64 rows) on the 64-key schedule
     const CUtensorMap& kmap = D == 256 ? tkh : tk;
     const CUtensorMap& vmap = D == 256 ? tvk : tv;
     if ((Hq / Hkv) % 2 != 0) return launch_mode<D, 0>(P, sc, tq, kmap, tkh, vmap, ob, Hq, Hkv, scale_log2, window, err, stream);
