@@ -196,6 +196,9 @@ def run_ours(args, rank, world):
     stream.synchronize()
     tokens, questions, pairs, flops_attn, bytes_attn, flops_score = work_counts(inputs, plan, passes, shape)
     sched_tiles = sum(int(p["info"].n_sched) for p in passes)
+    # the KV tiles the attention kernel executes: 64-key halves at d_head 256, else 128 keys
+    key_tile = 64 if shape.d_head == 256 else 128
+    exec_tiles = sum(len(plan.tile_schedule(pi, 0, key_tile)[1]) for pi in range(len(passes)))
 
     ev = {"attn": [], "score": []}
 
@@ -328,7 +331,9 @@ def run_ours(args, rank, world):
         "roofline_attention": {"kernel": "spinf_branch_attention", "tensor_tflops_unmasked": attn_tflops,
                                "tensor_frac": attn_tflops / bf16_peak, "hbm_gbs": attn_gbs,
                                "hbm_frac": attn_gbs / hbm_peak, "unmasked_pairs": pairs,
-                               "tile_occupancy": pairs / (sched_tiles * 128 * 128),
+                               "tile_occupancy": pairs / (exec_tiles * 128 * key_tile),
+                               "key_tile": key_tile, "executed_kv_tiles": exec_tiles,
+                               "tile_occupancy_128x128": pairs / (sched_tiles * 128 * 128),
                                "peak_source": f"{peak_src} {'bf16_tflops_sustained' if peak_src == 'measured' else ''}".strip()},
         # per kernel, as the scope table defines them: packed tokens per attention-kernel second
         # (one layer call per pass) and user questions per scoring second (gather + main + combine)

@@ -28,7 +28,7 @@ Q_SCORED, Q_SEARCHED = 0, 1
 SYMBOLS = [
     "spinf_plan_opts_default", "spinf_pack_plan", "spinf_plan_num_passes", "spinf_plan_pass_info",
     "spinf_plan_counts", "spinf_plan_extract_counts", "spinf_plan_upload", "spinf_plan_descriptor_bytes", "spinf_plan_upload_to",
-    "spinf_plan_window_schedule",
+    "spinf_plan_window_schedule", "spinf_plan_tile_schedule",
     "spinf_branch_attention", "spinf_score_workspace_bytes",
     "spinf_score", "spinf_score_extract", "spinf_score_static", "spinf_collect", "spinf_collect_extract",
     "spinf_device_status", "spinf_device_selftest",
@@ -118,6 +118,8 @@ def lib():
     L.spinf_plan_upload_to.argtypes = [vp, i32, vp, sz, vp]
     L.spinf_plan_window_schedule.argtypes = [vp, i32, i32, ctypes.POINTER(_P), ctypes.POINTER(_P), ctypes.POINTER(_P),
                                              ctypes.POINTER(i32)]
+    L.spinf_plan_tile_schedule.argtypes = [vp, i32, i32, i32, ctypes.POINTER(_P), ctypes.POINTER(_P),
+                                           ctypes.POINTER(_P), ctypes.POINTER(i32)]
     L.spinf_branch_attention.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, f32, i32, vp]
     L.spinf_score_workspace_bytes.argtypes = [vp, i32, i32, i32, i32]
     L.spinf_score_workspace_bytes.restype = sz
@@ -145,7 +147,7 @@ def lib():
     L.spinf_status_string.restype = ctypes.c_char_p
     L.spinf_last_error.restype = ctypes.c_char_p
     for name in ("spinf_pack_plan", "spinf_plan_pass_info", "spinf_plan_counts", "spinf_plan_extract_counts",
-                 "spinf_plan_upload", "spinf_plan_upload_to", "spinf_plan_window_schedule",
+                 "spinf_plan_upload", "spinf_plan_upload_to", "spinf_plan_window_schedule", "spinf_plan_tile_schedule",
                  "spinf_branch_attention", "spinf_score", "spinf_score_extract", "spinf_score_static", "spinf_collect",
                  "spinf_collect_extract",
                  "spinf_device_status", "spinf_device_selftest", "spinf_rope_tree", "spinf_linear",
@@ -420,6 +422,16 @@ class Plan:
         tp, tk, tl, n = _P(), _P(), _P(), ctypes.c_int32()
         _check(lib().spinf_plan_window_schedule(self.handle, p, window, ctypes.byref(tp), ctypes.byref(tk),
                                                 ctypes.byref(tl), ctypes.byref(n)))
+        nq = self.pass_info(p).n_qtiles
+        arr = lambda ptr, k: np.ctypeslib.as_array(ptr, shape=(k,)).copy() if k > 0 else np.zeros(0, np.int32)  # noqa: E731
+        return arr(tp, nq + 1), arr(tk, n.value), arr(tl, n.value)
+
+    def tile_schedule(self, p, window=0, key_tile=128):
+        """(tile_ptr, tile_kv, tile_len) of the schedule the attention kernel runs on pass p
+        for a window (0: none) in tiles of key_tile keys (128; 64 at d_head 256)."""
+        tp, tk, tl, n = _P(), _P(), _P(), ctypes.c_int32()
+        _check(lib().spinf_plan_tile_schedule(self.handle, p, window, key_tile, ctypes.byref(tp), ctypes.byref(tk),
+                                              ctypes.byref(tl), ctypes.byref(n)))
         nq = self.pass_info(p).n_qtiles
         arr = lambda ptr, k: np.ctypeslib.as_array(ptr, shape=(k,)).copy() if k > 0 else np.zeros(0, np.int32)  # noqa: E731
         return arr(tp, nq + 1), arr(tk, n.value), arr(tl, n.value)

@@ -669,6 +669,22 @@ extern "C" spinf_status spinf_plan_window_schedule(const spinf_plan* plan, int32
     return SPINF_OK;
 }
 
+extern "C" spinf_status spinf_plan_tile_schedule(const spinf_plan* plan, int32_t pass, int32_t window,
+                                                 int32_t key_tile, const int32_t** tile_ptr, const int32_t** tile_kv,
+                                                 const int32_t** tile_len, int32_t* n_sched) {
+    if (!plan || pass < 0 || pass >= (int32_t)plan->passes.size()) return fail(SPINF_E_INVALID, "bad plan or pass");
+    if (window < 0) return fail(SPINF_E_INVALID, "negative window");
+    if (key_tile != 64 && key_tile != kTile) return fail(SPINF_E_INVALID, "key_tile must be 64 or 128");
+    if (!tile_ptr || !tile_kv || !tile_len || !n_sched) return fail(SPINF_E_INVALID, "NULL output");
+    std::lock_guard<std::mutex> lock(const_cast<spinf_plan*>(plan)->cache_mu);
+    WindowSchedule& w = tile_schedule(const_cast<Pass&>(plan->passes[pass]), window, key_tile);
+    *tile_ptr = w.tile_ptr.data();
+    *tile_kv = w.tile_kv.data();
+    *tile_len = w.tile_len.data();
+    *n_sched = (int32_t)w.tile_kv.size();
+    return SPINF_OK;
+}
+
 extern "C" spinf_status spinf_plan_pass_info(const spinf_plan* plan, int32_t pass, spinf_pass_info* out) {
     if (!plan || !out || pass < 0 || pass >= (int32_t)plan->passes.size())
         return fail(SPINF_E_INVALID, "bad plan or pass index");

@@ -233,6 +233,19 @@ spinf_status spinf_plan_window_schedule(const spinf_plan* plan, int32_t pass, in
                                         const int32_t** tile_ptr, const int32_t** tile_kv,
                                         const int32_t** tile_len, int32_t* n_sched);
 
+/* The KV-tile schedule spinf_branch_attention runs for pass `pass`, window `window`
+ * (0: none) and tiles of `key_tile` keys: 128, or 64 (what d_head 256 runs: each
+ * input-anchored 128-key tile of the planner taken as its two 64-key halves).  A tile
+ * stays iff some row of its Q tile sees one of its keys (k <= q < end[k], and
+ * pos[q] - pos[k] < window when window > 0), in the planner's order; with window 0 and
+ * key_tile 128 this is the planner's own schedule.  tile_ptr has n_qtiles + 1 entries
+ * (spinf_pass_info); tile_kv / tile_len have *n_sched (first key, key count).  Built on
+ * first use and kept by the plan; host views valid until spinf_plan_free.
+ * SPINF_E_INVALID for a bad pass, window < 0, key_tile not 64 or 128, or NULL outputs. */
+spinf_status spinf_plan_tile_schedule(const spinf_plan* plan, int32_t pass, int32_t window, int32_t key_tile,
+                                      const int32_t** tile_ptr, const int32_t** tile_kv,
+                                      const int32_t** tile_len, int32_t* n_sched);
+
 /* Number of user questions and options over the whole request (sizes of spinf_result). */
 spinf_status spinf_plan_counts(const spinf_plan* plan, int64_t* n_questions, int64_t* n_options);
 

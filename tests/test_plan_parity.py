@@ -229,6 +229,53 @@ def test_window_schedule_is_exact(spinf, window):
             assert np.array_equal(tk, lay.tile_kv) and np.array_equal(tl, lay.tile_len)
 
 
+@pytest.mark.parametrize("window,key_tile", [(0, 128), (0, 64), (7, 64), (64, 64), (200, 64)])
+def test_tile_schedule_is_exact(spinf, window, key_tile):
+    """The schedule the attention kernel runs (64-key tiles at d_head 256): each planner
+    tile taken whole or as its two 64-key halves, a piece kept iff some row of its Q tile
+    sees one of its keys (within the window), in the planner's order (oracle visible sets
+    and depths, brute force).  Window 0 with 128-key tiles is the planner's own schedule."""
+    inputs = wl.stress(n_questions=24, content_tokens=300, vocab=1000) + wl.tiny(vocab=1000)
+    P = op.plan(inputs, token_budget=1024, vocab=1000)
+    plan = spinf.Plan(inputs, token_budget=1024, vocab=1000)
+    n_halves_dropped = 0
+    for p, lay in enumerate(P.passes):
+        tp, tk, tl = plan.tile_schedule(p, window, key_tile)
+        want_ptr, want_kv = [0], []
+        for qt in range(lay.T_pad // 128):
+            rows = range(qt * 128, min(qt * 128 + 128, lay.T))
+            vis = {q: set(lay.visible(q)) for q in rows}
+            for e in range(lay.tile_ptr[qt], lay.tile_ptr[qt + 1]):
+                kv0, ln = int(lay.tile_kv[e]), int(lay.tile_len[e])
+                for sub in range(0, 128, key_tile):
+                    n = min(ln - sub, key_tile)
+                    if n <= 0:
+                        break
+                    keys = range(kv0 + sub, kv0 + sub + n)
+                    if any(k in vis[q] and (window == 0 or lay.pos[q] - lay.pos[k] < window)
+                           for q in rows for k in keys):
+                        want_kv.append((kv0 + sub, n))
+                    else:
+                        n_halves_dropped += 1
+            want_ptr.append(len(want_kv))
+        assert tp.tolist() == want_ptr, p
+        assert list(zip(tk.tolist(), tl.tolist())) == want_kv, p
+        if (window, key_tile) == (0, 128):
+            assert np.array_equal(tk, lay.tile_kv) and np.array_equal(tl, lay.tile_len)
+    if (window, key_tile) == (0, 128):
+        assert n_halves_dropped == 0          # the planner schedules no tile that no row sees
+    else:
+        assert n_halves_dropped > 0           # the case does exercise the dropping
+
+
+def test_tile_schedule_rejects_bad_arguments(spinf):
+    plan = spinf.Plan(wl.tiny(vocab=1000), vocab=1000)
+    for args in ((0, -1, 64), (0, 0, 32), (0, 0, 256), (5, 0, 64)):
+        with pytest.raises(spinf.SpinfError) as e:
+            plan.tile_schedule(*args)
+        assert e.value.status_name == "INVALID"
+
+
 def _searched_request(g, n_inputs, vocab=60):
     """Inputs mixing scored questions and searched slots (token sets -1..3)."""
     inputs = []
