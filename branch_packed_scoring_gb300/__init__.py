@@ -184,6 +184,58 @@ def _stream(stream):
     return stream.cuda_stream
 
 
+_KINDS = None
+
+
+def _kinds():
+    global _KINDS
+    if _KINDS is None:
+        import torch
+        words = (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ())
+        _KINDS = {"bf16": (torch.bfloat16,), "f32": (torch.float32,), "i32": (torch.int32,),
+                  "e4m3": (torch.uint8, torch.float8_e4m3fn), "words": words, "bytes": None}
+    return _KINDS
+
+
+def _wkind(w_dtype):
+    return "e4m3" if w_dtype == DTYPE_E4M3 else "bf16" if w_dtype == DTYPE_BF16 else "bytes"
+
+
+class _Args:
+    """The device-buffer arguments of one call, checked before the C call.  A torch tensor
+    must have the dtype the header gives, be contiguous, hold at least the elements the call
+    reads or writes, and live on the current CUDA device; otherwise SpinfError(INVALID).  A
+    raw device address (int) or None passes unchecked, as it would through the C ABI."""
+
+    def __init__(self, call):
+        self.call = call
+        self.device = None
+
+    def bad(self, msg):
+        raise SpinfError(E_INVALID, f"{self.call}: {msg}")
+
+    def __call__(self, x, what, kind, n=None):
+        if x is None or isinstance(x, int):
+            return x
+        if not hasattr(x, "is_cuda"):
+            self.bad(f"{what} must be a torch tensor or a device address, not {type(x).__name__}")
+        dts = _kinds()[kind]
+        if dts is not None and x.dtype not in dts:
+            self.bad(f"{what} has dtype {x.dtype}; {kind} expected")
+        if not x.is_contiguous():
+            self.bad(f"{what} must be contiguous")
+        if n is not None and x.numel() < n:
+            self.bad(f"{what} holds {x.numel()} elements; the call needs {n}")
+        if not x.is_cuda:
+            self.bad(f"{what} must be a CUDA tensor (it is on {x.device})")
+        if self.device is None:
+            import torch
+            self.device = torch.cuda.current_device()
+        if x.device.index != self.device:
+            self.bad(f"{what} is on {x.device}; the current device is cuda:{self.device}")
+        return x.data_ptr()
+
+
 def fingerprint() -> str:
     return lib().spinf_fingerprint().decode()
 
@@ -356,6 +408,7 @@ class Plan:
                  floors=True, floor_prefix=(), vocab=0, extract_k=None):
         L = lib()
         self._h = None
+        self._size_cache = {}
         opts = _Opts()
         L.spinf_plan_opts_default(ctypes.byref(opts))
         for name, val in (("token_budget", token_budget), ("max_tokens", max_tokens),
@@ -387,6 +440,15 @@ class Plan:
         if self._h is None:
             raise RuntimeError("plan is closed")
         return self._h
+
+    def _sizes(self, p):
+        """(T_pad, M, G, X) of pass p, without copying its arrays (cached)."""
+        s = self._size_cache.get(p)
+        if s is None:
+            info = _PassInfo()
+            _check(lib().spinf_plan_pass_info(self.handle, p, ctypes.byref(info)))
+            s = self._size_cache[p] = (info.T_pad, info.M, info.G, info.X)
+        return s
 
     def pass_info(self, p) -> PassInfo:
         info = _PassInfo()
@@ -445,7 +507,8 @@ class Plan:
         if buffer is None:
             _check(lib().spinf_plan_upload(self.handle, p, _stream(stream)))
         else:
-            _check(lib().spinf_plan_upload_to(self.handle, p, ctypes.c_void_p(buffer.data_ptr()),
+            addr = _Args("upload")(buffer, "buffer", "bytes")
+            _check(lib().spinf_plan_upload_to(self.handle, p, ctypes.c_void_p(addr),
                                               buffer.numel() * buffer.element_size(), _stream(stream)))
 
     def collect(self, token_lp_per_pass):
@@ -496,34 +559,51 @@ class Plan:
 
 
 def branch_attention(plan, p, q, k, v, o, n_q_heads, n_kv_heads, d_head, scale=0.0, window=0, stream=None):
-    _check(lib().spinf_branch_attention(plan.handle, p, _ptr(q), _ptr(k), _ptr(v), _ptr(o), n_q_heads,
-                                        n_kv_heads, d_head, float(scale), int(window), _stream(stream)))
+    """spinf_branch_attention: q, o [T_pad, Hq, d] and k, v [T_pad, Hkv, d] bf16 on the device."""
+    a = _Args("branch_attention")
+    T = plan._sizes(p)[0]
+    nq, nkv = T * n_q_heads * d_head, T * n_kv_heads * d_head
+    _check(lib().spinf_branch_attention(plan.handle, p, a(q, "q", "bf16", nq), a(k, "k", "bf16", nkv),
+                                        a(v, "v", "bf16", nkv), a(o, "o", "bf16", nq), n_q_heads, n_kv_heads,
+                                        d_head, float(scale), int(window), _stream(stream)))
 
 
 def rope_tree(plan, p, q, k, n_q_heads, n_kv_heads, d_head, theta=10000.0, stream=None):
     """Rotary embedding in place at each row's tree depth (spinf_rope_tree)."""
-    _check(lib().spinf_rope_tree(plan.handle, p, _ptr(q), _ptr(k), n_q_heads, n_kv_heads, d_head, float(theta),
-                                 _stream(stream)))
+    a = _Args("rope_tree")
+    T = plan._sizes(p)[0]
+    _check(lib().spinf_rope_tree(plan.handle, p, a(q, "q", "bf16", T * n_q_heads * d_head),
+                                 a(k, "k", "bf16", T * n_kv_heads * d_head), n_q_heads, n_kv_heads, d_head,
+                                 float(theta), _stream(stream)))
 
 
 def linear(plan, x, w, y, w_scale=None, x_scale=1.0, w_dtype=DTYPE_BF16, stream=None):
     """y = x . w^T on the tensor cores (spinf_linear); x [rows, in], w [out, in], y [rows, out] bf16.
     With ``w_dtype=DTYPE_E4M3``, x and w are e4m3 codes (uint8), ``w_scale`` [out] fp32, ``x_scale`` static."""
-    _check(lib().spinf_linear(plan.handle, _ptr(x), _ptr(w), _ptr(w_scale), float(x_scale), w_dtype, _ptr(y),
-                              x.shape[0], x.shape[1], w.shape[0], _stream(stream)))
+    a, kind = _Args("linear"), _wkind(w_dtype)
+    rows, n_in, n_out = x.shape[0], x.shape[1], w.shape[0]
+    _check(lib().spinf_linear(plan.handle, a(x, "x", kind, rows * n_in), a(w, "w", kind, n_out * n_in),
+                              a(w_scale, "w_scale", "f32", n_out), float(x_scale), w_dtype,
+                              a(y, "y", "bf16", rows * n_out), rows, n_in, n_out, _stream(stream)))
 
 
 def qkv_rope(plan, p, x, w, q, k, v, n_q_heads, n_kv_heads, d_head, theta=10000.0, w_scale=None, x_scale=1.0,
              w_dtype=DTYPE_BF16, stream=None):
     """QKV projection of pass p with the rotary turn fused (spinf_qkv_rope); writes q, k, v."""
-    _check(lib().spinf_qkv_rope(plan.handle, p, _ptr(x), _ptr(w), _ptr(w_scale), float(x_scale), w_dtype,
-                                x.shape[1], n_q_heads, n_kv_heads, d_head, float(theta), _ptr(q), _ptr(k), _ptr(v),
-                                _stream(stream)))
+    a, kind = _Args("qkv_rope"), _wkind(w_dtype)
+    T, D = plan._sizes(p)[0], x.shape[1]
+    n_qkv, nq, nkv = (n_q_heads + 2 * n_kv_heads) * d_head, T * n_q_heads * d_head, T * n_kv_heads * d_head
+    _check(lib().spinf_qkv_rope(plan.handle, p, a(x, "x", kind, T * D), a(w, "w", kind, n_qkv * D),
+                                a(w_scale, "w_scale", "f32", n_qkv), float(x_scale), w_dtype, D, n_q_heads,
+                                n_kv_heads, d_head, float(theta), a(q, "q", "bf16", nq), a(k, "k", "bf16", nkv),
+                                a(v, "v", "bf16", nkv), _stream(stream)))
 
 
 def quantize_static(x, x_scale, codes, stream=None):
     """e4m3 codes of bf16 ``x`` with a static scale (spinf_quantize_static)."""
-    _check(lib().spinf_quantize_static(_ptr(x), float(x_scale), _ptr(codes), x.numel(), _stream(stream)))
+    a, n = _Args("quantize_static"), x.numel()
+    _check(lib().spinf_quantize_static(a(x, "x", "bf16"), float(x_scale), a(codes, "codes", "e4m3", n), n,
+                                       _stream(stream)))
 
 
 def score_workspace_bytes(plan, p, vocab, d_model, w_dtype=DTYPE_BF16):
@@ -536,32 +616,49 @@ def score(plan, p, hidden, w, w_scale, w_dtype, d_model, vocab, row_lse, token_l
     tensors, optional ``token_sets`` [n_sets, ceil(vocab/32)] int32 bitmasks) ``spinf_score_extract``."""
     if workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size()
+    a = _Args("score")
+    args = _score_args(a, plan, p, hidden, w, w_scale, w_dtype, d_model, vocab, row_lse, token_lp)
+    ws = a(workspace, "workspace", "bytes")
     if extract is None:
-        _check(lib().spinf_score(plan.handle, p, _ptr(hidden), _ptr(w), _ptr(w_scale), w_dtype, d_model, vocab,
-                                 _ptr(row_lse), _ptr(token_lp), _ptr(workspace), int(workspace_bytes),
-                                 _stream(stream)))
+        _check(lib().spinf_score(plan.handle, p, *args, ws, int(workspace_bytes), _stream(stream)))
         return
     sets = extract.get("token_sets")
-    ex = _ExtractOut(_ptr(sets), 0 if sets is None else int(sets.shape[0]), _ptr(extract["top_tok"]),
-                     _ptr(extract["top_lp"]))
-    _check(lib().spinf_score_extract(plan.handle, p, _ptr(hidden), _ptr(w), _ptr(w_scale), w_dtype, d_model, vocab,
-                                     _ptr(row_lse), _ptr(token_lp), ctypes.byref(ex), _ptr(workspace),
+    n_sets = 0 if sets is None else int(sets.shape[0])
+    X, k = plan._sizes(p)[3], plan.extract_counts()[1]
+    ex = _ExtractOut(a(sets, "token_sets", "words", n_sets * (-(-vocab // 32))), n_sets,
+                     a(extract["top_tok"], "top_tok", "i32", X * k), a(extract["top_lp"], "top_lp", "f32", X * k))
+    _check(lib().spinf_score_extract(plan.handle, p, *args, ctypes.byref(ex), ws,
                                      int(workspace_bytes), _stream(stream)))
+
+
+def _score_args(a, plan, p, hidden, w, w_scale, w_dtype, d_model, vocab, row_lse, token_lp):
+    """Checked (hidden, w, w_scale, w_dtype, d_model, vocab, row_lse, token_lp) of a scoring call."""
+    T, M, G, _ = plan._sizes(p)
+    kind = _wkind(w_dtype)
+    return (a(hidden, "hidden", "bf16", T * d_model), a(w, "w", kind, vocab * d_model),
+            a(w_scale, "w_scale", "f32", vocab), w_dtype, d_model, vocab, a(row_lse, "row_lse", "f32", M),
+            a(token_lp, "token_lp", "f32", G))
 
 
 def score_static(plan, p, hidden, w, w_scale, w_dtype, d_model, vocab, row_lse, token_lp, stream=None):
     """``spinf_score_static``: scoring with the library's own fixed device scratch (no allocation)."""
-    _check(lib().spinf_score_static(plan.handle, p, _ptr(hidden), _ptr(w), _ptr(w_scale), w_dtype, d_model, vocab,
-                                    _ptr(row_lse), _ptr(token_lp), _stream(stream)))
+    args = _score_args(_Args("score_static"), plan, p, hidden, w, w_scale, w_dtype, d_model, vocab, row_lse, token_lp)
+    _check(lib().spinf_score_static(plan.handle, p, *args, _stream(stream)))
 
 
 def decode_attention(plan, p, q, k_pass, v_pass, k_dec, v_dec, anchor, parent, q_row, o, n_q_heads, n_kv_heads,
                      d_head, scale=0.0, stream=None):
     """One decoding step of searched slots (spinf_decode_attention); anchor, parent, q_row are
     device int32 tensors."""
-    _check(lib().spinf_decode_attention(plan.handle, p, _ptr(q), _ptr(k_pass), _ptr(v_pass), _ptr(k_dec),
-                                        _ptr(v_dec), anchor.numel(), _ptr(anchor), _ptr(parent), _ptr(q_row),
-                                        q_row.numel(), _ptr(o), n_q_heads, n_kv_heads, d_head, float(scale),
+    a = _Args("decode_attention")
+    T = plan._sizes(p)[0]
+    n_dec, n_q = anchor.numel(), q_row.numel()
+    nq, nkv, ndec = n_q * n_q_heads * d_head, T * n_kv_heads * d_head, n_dec * n_kv_heads * d_head
+    _check(lib().spinf_decode_attention(plan.handle, p, a(q, "q", "bf16", nq), a(k_pass, "k_pass", "bf16", nkv),
+                                        a(v_pass, "v_pass", "bf16", nkv), a(k_dec, "k_dec", "bf16", ndec),
+                                        a(v_dec, "v_dec", "bf16", ndec), n_dec, a(anchor, "anchor", "i32", n_dec),
+                                        a(parent, "parent", "i32", n_dec), a(q_row, "q_row", "i32", n_q), n_q,
+                                        a(o, "o", "bf16", nq), n_q_heads, n_kv_heads, d_head, float(scale),
                                         _stream(stream)))
 
 
@@ -569,12 +666,15 @@ def score_rows(plan, hidden, w, w_scale, w_dtype, d_model, vocab, k, row_lse, to
                token_sets=None, workspace=None, stream=None):
     """Next-token answers at caller-given rows (spinf_score_rows); token_set: a device int32 tensor or None."""
     import torch
+    a, kind = _Args("score_rows"), _wkind(w_dtype)
     n = hidden.shape[0]
+    n_sets = 0 if token_sets is None else int(token_sets.shape[0])
+    args = (a(hidden, "hidden", "bf16", n * d_model), n, a(w, "w", kind, vocab * d_model),
+            a(w_scale, "w_scale", "f32", vocab), w_dtype, d_model, vocab, a(token_set, "token_set", "i32", n),
+            a(token_sets, "token_sets", "words", n_sets * (-(-vocab // 32))), n_sets, k,
+            a(row_lse, "row_lse", "f32", n), a(top_tok, "top_tok", "i32", n * k), a(top_lp, "top_lp", "f32", n * k))
     if workspace is None:
         workspace = torch.empty(max(1, lib().spinf_score_rows_workspace_bytes(n, vocab, d_model, w_dtype, k)),
                                 dtype=torch.uint8, device=hidden.device)
-    _check(lib().spinf_score_rows(plan.handle, _ptr(hidden), n, _ptr(w), _ptr(w_scale), w_dtype, d_model, vocab,
-                                  _ptr(token_set), _ptr(token_sets),
-                                  0 if token_sets is None else int(token_sets.shape[0]), k, _ptr(row_lse),
-                                  _ptr(top_tok), _ptr(top_lp), _ptr(workspace),
+    _check(lib().spinf_score_rows(plan.handle, *args, a(workspace, "workspace", "bytes"),
                                   workspace.numel() * workspace.element_size(), _stream(stream)))

@@ -80,3 +80,47 @@ def test_layer_and_decode_calls_validate_before_any_device_work(spinf):
     assert L.spinf_score_rows_workspace_bytes(0, 1024, 256, 0, 8) == 0
     assert L.spinf_score_rows_workspace_bytes(4, 1024, 256, 0, 17) == 0
     assert L.spinf_score_rows_workspace_bytes(4, 1024, 256, 0, 8) > 4 * 256 * 2
+
+
+def test_binding_checks_tensors_before_the_call(spinf):
+    """The binding refuses a tensor of the wrong dtype, a strided view, a buffer smaller than
+    the call reads or writes, and a host tensor, before anything reaches the library (no GPU
+    needed).  Raw addresses (ints) pass through unchecked, so each case below gives them for
+    the arguments ahead of the one under test."""
+    torch = pytest.importorskip("torch")
+    plan = spinf.Plan([([1, 2, 3], [([4, 5], [[6], [7]])])], vocab=1024)
+    info = plan.pass_info(0)
+    T, M, G = info.T_pad, info.M, info.G
+    A = 4096
+    bf = lambda *s: torch.zeros(*s, dtype=torch.bfloat16)  # noqa: E731
+    f32 = lambda n: torch.zeros(n)  # noqa: E731
+    i32 = lambda n: torch.zeros(n, dtype=torch.int32)  # noqa: E731
+    q, kv, w = bf(T, 4, 64), bf(T, 2, 64), bf(1024, 256)
+    ws = torch.zeros(16, dtype=torch.uint8)
+    cases = [
+        (lambda: spinf.branch_attention(plan, 0, q.float(), A, A, A, 4, 2, 64), "q has dtype torch.float32"),
+        (lambda: spinf.branch_attention(plan, 0, A, A, A, q.transpose(0, 1), 4, 2, 64), "o must be contiguous"),
+        (lambda: spinf.branch_attention(plan, 0, A, kv[:T - 1], A, A, 4, 2, 64), "k holds"),
+        (lambda: spinf.branch_attention(plan, 0, q, A, A, A, 4, 2, 64), "q must be a CUDA tensor"),
+        (lambda: spinf.branch_attention(plan, 0, [1], A, A, A, 4, 2, 64), "q must be a torch tensor"),
+        (lambda: spinf.score(plan, 0, A, A, None, spinf.DTYPE_BF16, 256, 1024, f32(M - 1), A, A,
+                             workspace_bytes=1 << 20), "row_lse holds"),
+        (lambda: spinf.score(plan, 0, A, w, None, spinf.DTYPE_E4M3, 256, 1024, A, A, ws), "w has dtype"),
+        (lambda: spinf.score(plan, 0, A, A, None, spinf.DTYPE_BF16, 256, 1024, A, A, A, workspace_bytes=1 << 20,
+                             extract={"top_tok": f32(8), "top_lp": A}), "top_tok has dtype"),
+        (lambda: spinf.score_static(plan, 0, bf(1, 256), A, None, spinf.DTYPE_BF16, 256, 1024, A, A),
+         "hidden holds"),
+        (lambda: spinf.rope_tree(plan, 0, A, kv[:1], 4, 2, 64), "k holds"),
+        (lambda: spinf.linear(plan, f32(512).view(8, 64), bf(32, 64), A), "x has dtype"),
+        (lambda: spinf.qkv_rope(plan, 0, bf(T, 256), A, A, A, A, 4, 2, 64, w_scale=f32(10),
+                                w_dtype=spinf.DTYPE_E4M3), "x has dtype"),
+        (lambda: spinf.quantize_static(f32(64), 0.5, A), "x has dtype"),
+        (lambda: spinf.decode_attention(plan, 0, A, A, A, A, A, torch.zeros(3, dtype=torch.int64), A, i32(2), A,
+                                        4, 2, 64), "anchor has dtype"),
+        (lambda: spinf.score_rows(plan, bf(4, 256), w, None, spinf.DTYPE_BF16, 256, 1024, 8, A, A, f32(31),
+                                  workspace=ws), "hidden must be a CUDA tensor"),
+    ]
+    for fn, words in cases:
+        with pytest.raises(spinf.SpinfError) as e:
+            fn()
+        assert e.value.status_name == "INVALID" and words in str(e.value), str(e.value)

@@ -61,7 +61,8 @@ def test_static_scratch_rejects_oversized_pass(spinf):
     plan.upload(0)
     d_model = 1 << 20            # 128 rows x 2^20 bf16 = 256 MiB of gathered rows: beyond the area
     x = torch.empty(16, dtype=torch.uint8, device="cuda")
+    a = x.data_ptr()   # raw addresses: the library's own limit check runs, not the binding's size checks
     with pytest.raises(spinf.SpinfError) as e:
-        spinf.score_static(plan, 0, x, x, None, spinf.DTYPE_BF16, d_model, 1024, x, x)
+        spinf.score_static(plan, 0, a, a, None, spinf.DTYPE_BF16, d_model, 1024, a, a)
     assert e.value.status_name == "LIMIT"
     assert "static area holds" in str(e.value)
