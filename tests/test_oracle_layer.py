@@ -24,6 +24,19 @@ def test_rope_two_dims_is_a_plane_rotation():
         assert np.allclose(got[t, 0], r @ x[t, 0], atol=1e-14)
 
 
+def test_rope_frequencies_by_hand():
+    """RoFormer's schedule theta^(-2i/d): with d = 8 and theta = 10^4 the four pairs turn at
+    exactly 1, 1/10, 1/100 and 1/1000 radians per position, so a unit vector in pair i
+    (components i and i + d/2) at position 10^i turns by one radian, towards the second half."""
+    for i in range(4):
+        x = np.zeros((1, 1, 8))
+        x[0, 0, i] = 1.0
+        y = ol.rope(x, [10.0 ** i], 10000.0)[0, 0]
+        want = np.zeros(8)
+        want[i], want[i + 4] = math.cos(1.0), math.sin(1.0)
+        assert np.allclose(y, want, atol=1e-12), i
+
+
 def test_rope_keeps_pair_norms_and_scores_depend_on_offset_only():
     g = np.random.default_rng(2)
     d = 16
