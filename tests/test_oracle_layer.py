@@ -142,3 +142,16 @@ def test_qkv_rope_is_projection_then_rotation():
     kk = y[:, Hq * d:(Hq + Hkv) * d].reshape(T, Hkv, d)
     np.testing.assert_allclose(np.hypot(k[..., :d // 2], k[..., d // 2:]),
                                np.hypot(kk[..., :d // 2], kk[..., d // 2:]), rtol=1e-12)
+
+
+def test_qkv_rope_turns_q_and_k_by_their_own_positions():
+    """Rows with the same input at positions (5, 2) and (15, 12): each q . k score depends on
+    the offset only, which holds only if both q and k are turned by their rows' positions."""
+    g = np.random.default_rng(9)
+    D, Hq, Hkv, d = 32, 2, 1, 16
+    x = np.repeat(g.standard_normal((1, D)), 4, axis=0)
+    w = g.standard_normal(((Hq + 2 * Hkv) * d, D))
+    q, k, _ = ol.qkv_rope(x, w, np.array([5, 2, 15, 12]), Hq, Hkv, d, 10000.0)
+    for h in range(Hq):
+        assert math.isclose(q[0, h] @ k[1, 0], q[2, h] @ k[3, 0], rel_tol=1e-10)
+    assert not math.isclose(q[0, 0] @ k[1, 0], q[0, 0] @ k[3, 0], rel_tol=1e-6)   # the offset does matter

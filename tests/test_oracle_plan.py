@@ -67,6 +67,8 @@ def test_option_trie_rows():
 
 def test_trie_preorder_and_first_insertion():
     assert op.trie_nodes([[5, 6, 7], [9, 1], [5, 8]]) == [(5,), (5, 6), (9,)]
+    # first insertion, not token order: 9 was inserted before 5
+    assert op.trie_nodes([[9, 1], [5, 6, 7], [5, 8], [9, 3, 4]]) == [(9,), (9, 3), (5,), (5, 6)]
     P = op.plan([([], [([2, 3], [[5, 6, 7], [9, 1], [5, 8]])])], floors=False)
     L = P.passes[0]
     # rows: 0:2 1:3(slot) 2:(5,) 3:(5,6) 4:(9,)
@@ -85,6 +87,9 @@ def test_next_fit_and_split():
     inputs = [([1, 2, 3, 4], [([5, 6], [[7]])]), ([1, 2, 3], [([8, 9], [[7]])])]
     P = op.plan(inputs, token_budget=10)
     assert [p.T for p in P.passes] == [6, 9]
+    # an input that brings the pass to exactly the budget stays in it (a pass holds <= budget rows)
+    P = op.plan(inputs, token_budget=11, floors=False)
+    assert [p.T for p in P.passes] == [11]
     # long input split: content 4 + questions of 3 each, budget 10 -> chunks of 2 questions
     inputs = [([1, 2, 3, 4], [([5, 6, 7], [[1]]), ([5, 6, 8], [[1]]), ([5, 6, 9], [[1]])])]
     P = op.plan(inputs, token_budget=10, floors=False)

@@ -68,6 +68,14 @@ def test_splits_and_tries(spinf, budget):
     _compare(spinf, inputs, token_budget=budget, floor_prefix=[5, 6, 7])
 
 
+@pytest.mark.parametrize("budget", [10, 11, 12])
+def test_exact_fit_stays_in_its_pass(spinf, budget):
+    """Inputs of 6 and 5 tokens: one pass at budget 11 (an exact fit), two at 10 and one at 12."""
+    inputs = [([1, 2, 3, 4], [([5, 6], [[7]])]), ([1, 2, 3], [([8, 9], [[7]])])]
+    P, Q = _compare(spinf, inputs, token_budget=budget, floors=False)
+    assert Q.num_passes == (2 if budget == 10 else 1)
+
+
 def test_fuzzed_requests(spinf):
     g = np.random.default_rng(7)
     for trial in range(40):
