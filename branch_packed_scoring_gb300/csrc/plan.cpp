@@ -90,9 +90,12 @@ void build_trie(const spinf_question& q, Trie& t) {
     }
 }
 
-std::string question_key(const spinf_question& q) {
-    std::string k;
-    auto put = [&](int32_t v) { k.append(reinterpret_cast<const char*>(&v), sizeof v); };
+// A floor is shared by the questions with the same template and the same option lists
+// (in the same order): a 64-bit FNV-1a hash of those ids and lengths finds the
+// candidates, and same_question decides.
+uint64_t question_hash(const spinf_question& q) {
+    uint64_t h = 14695981039346656037ull;
+    auto put = [&](int32_t v) { h = (h ^ static_cast<uint32_t>(v)) * 1099511628211ull; };
     put(q.tmpl.n);
     for (int32_t i = 0; i < q.tmpl.n; ++i) put(q.tmpl.ids[i]);
     put(q.n_options);
@@ -100,7 +103,17 @@ std::string question_key(const spinf_question& q) {
         put(q.options[o].n);
         for (int32_t i = 0; i < q.options[o].n; ++i) put(q.options[o].ids[i]);
     }
-    return k;
+    return h;
+}
+
+bool same_question(const spinf_question& a, const spinf_question& b) {
+    if (a.tmpl.n != b.tmpl.n || a.n_options != b.n_options) return false;
+    if (std::memcmp(a.tmpl.ids, b.tmpl.ids, sizeof(int32_t) * a.tmpl.n) != 0) return false;
+    for (int32_t o = 0; o < a.n_options; ++o) {
+        const spinf_tokens &x = a.options[o], &y = b.options[o];
+        if (x.n != y.n || std::memcmp(x.ids, y.ids, sizeof(int32_t) * x.n) != 0) return false;
+    }
+    return true;
 }
 
 struct Unit {
@@ -126,23 +139,23 @@ spinf_status expand_grids(const spinf_input* inputs, int32_t n_inputs, const spi
     x.questions.resize(n_inputs);
     for (int32_t i = 0; i < n_inputs; ++i) {
         const spinf_input& in = inputs[i];
-        const std::string where = "input " + std::to_string(i);
-        if (in.n_grids < 0 || (in.n_grids > 0 && !in.grids)) return fail(SPINF_E_INVALID, where + ": bad grid array");
+        auto where = [i]() { return "input " + std::to_string(i); };   // built only for an error
+        if (in.n_grids < 0 || (in.n_grids > 0 && !in.grids)) return fail(SPINF_E_INVALID, where() + ": bad grid array");
         if (in.n_questions < 0 || (in.n_questions > 0 && !in.questions))
-            return fail(SPINF_E_INVALID, where + ": bad arrays");
+            return fail(SPINF_E_INVALID, where() + ": bad arrays");
         int64_t total = in.n_questions;
         for (int32_t gi = 0; gi < in.n_grids; ++gi) {
             const spinf_grid& g = in.grids[gi];
             if (g.n_placeholders < 0 || !g.segments || (g.n_placeholders > 0 && (!g.values || !g.n_values)))
-                return fail(SPINF_E_INVALID, where + ": bad grid");
+                return fail(SPINF_E_INVALID, where() + ": bad grid");
             int64_t cells = 1;
             for (int32_t p = 0; p < g.n_placeholders; ++p) {
-                if (g.n_values[p] < 1) return fail(SPINF_E_INVALID, where + ": a grid placeholder without values");
+                if (g.n_values[p] < 1) return fail(SPINF_E_INVALID, where() + ": a grid placeholder without values");
                 cells = std::min<int64_t>(cells * g.n_values[p], (int64_t)1 << 40);
             }
             total += cells;
             if (total > o.max_prompts_per_input)
-                return fail(SPINF_E_LIMIT, where + ": more questions than max_prompts_per_input");
+                return fail(SPINF_E_LIMIT, where() + ": more questions than max_prompts_per_input");
         }
         if (in.n_grids == 0) continue;
         std::vector<spinf_question>& qs = x.questions[i];
@@ -303,50 +316,50 @@ extern "C" spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inp
         std::vector<std::vector<int64_t>> qsize(n_inputs);
         for (int32_t i = 0; i < n_inputs; ++i) {
             const spinf_input& in = inputs[i];
-            std::string where = "input " + std::to_string(i);
+            auto where = [i]() { return "input " + std::to_string(i); };   // built only for an error
             if (in.content.n < 0 || in.n_questions < 0 || (in.n_questions > 0 && !in.questions))
-                return fail(SPINF_E_INVALID, where + ": bad arrays");
+                return fail(SPINF_E_INVALID, where() + ": bad arrays");
             if (in.content.n > o.max_content_tokens)
-                return fail(SPINF_E_LIMIT, where + ": content longer than max_content_tokens");
+                return fail(SPINF_E_LIMIT, where() + ": content longer than max_content_tokens");
             if (in.n_questions > o.max_prompts_per_input)
-                return fail(SPINF_E_LIMIT, where + ": more questions than max_prompts_per_input");
-            if (!ids_in_range(in.content, o.vocab)) return fail(SPINF_E_INVALID, where + ": content token out of range");
-            if (in.content.n == 0 && in.n_questions == 0) return fail(SPINF_E_INVALID, where + ": nothing to read");
+                return fail(SPINF_E_LIMIT, where() + ": more questions than max_prompts_per_input");
+            if (!ids_in_range(in.content, o.vocab)) return fail(SPINF_E_INVALID, where() + ": content token out of range");
+            if (in.content.n == 0 && in.n_questions == 0) return fail(SPINF_E_INVALID, where() + ": nothing to read");
             int64_t size = in.content.n;
             tries[i].resize(in.n_questions);
             for (int32_t j = 0; j < in.n_questions; ++j) {
                 const spinf_question& q = in.questions[j];
-                std::string wq = where + " question " + std::to_string(j);
-                if (q.tmpl.n <= 0) return fail(SPINF_E_INVALID, wq + ": empty template");
-                if (q.tmpl.n > o.max_query_tokens) return fail(SPINF_E_LIMIT, wq + ": template longer than max_query_tokens");
-                if (q.kind != SPINF_Q_SCORED && q.kind != SPINF_Q_SEARCHED) return fail(SPINF_E_INVALID, wq + ": unknown kind");
+                auto wq = [&where, j]() { return where() + " question " + std::to_string(j); };
+                if (q.tmpl.n <= 0) return fail(SPINF_E_INVALID, wq() + ": empty template");
+                if (q.tmpl.n > o.max_query_tokens) return fail(SPINF_E_LIMIT, wq() + ": template longer than max_query_tokens");
+                if (q.kind != SPINF_Q_SCORED && q.kind != SPINF_Q_SEARCHED) return fail(SPINF_E_INVALID, wq() + ": unknown kind");
                 if (q.kind == SPINF_Q_SEARCHED) {   // template only: no options, no trie
-                    if (q.n_options != 0) return fail(SPINF_E_INVALID, wq + ": a searched slot has no options");
-                    if (q.token_set < -1) return fail(SPINF_E_INVALID, wq + ": bad token set");
-                    if (!ids_in_range(q.tmpl, o.vocab)) return fail(SPINF_E_INVALID, wq + ": template token out of range");
+                    if (q.n_options != 0) return fail(SPINF_E_INVALID, wq() + ": a searched slot has no options");
+                    if (q.token_set < -1) return fail(SPINF_E_INVALID, wq() + ": bad token set");
+                    if (!ids_in_range(q.tmpl, o.vocab)) return fail(SPINF_E_INVALID, wq() + ": template token out of range");
                     qsize[i].push_back(q.tmpl.n);
                     size += q.tmpl.n;
                     continue;
                 }
-                if (q.n_options <= 0 || !q.options) return fail(SPINF_E_INVALID, wq + ": no options");
-                if (q.n_options > o.max_options) return fail(SPINF_E_LIMIT, wq + ": more options than max_options");
+                if (q.n_options <= 0 || !q.options) return fail(SPINF_E_INVALID, wq() + ": no options");
+                if (q.n_options > o.max_options) return fail(SPINF_E_LIMIT, wq() + ": more options than max_options");
                 for (int32_t a = 0; a < q.n_options; ++a) {
                     const spinf_tokens& opt = q.options[a];
-                    if (opt.n <= 0 || !opt.ids) return fail(SPINF_E_INVALID, wq + ": empty option");
-                    if (opt.n > o.max_option_tokens) return fail(SPINF_E_LIMIT, wq + ": option longer than max_option_tokens");
+                    if (opt.n <= 0 || !opt.ids) return fail(SPINF_E_INVALID, wq() + ": empty option");
+                    if (opt.n > o.max_option_tokens) return fail(SPINF_E_LIMIT, wq() + ": option longer than max_option_tokens");
                     for (int32_t b = 0; b < a; ++b) {
                         const spinf_tokens& ob = q.options[b];
                         if (ob.n == opt.n && std::memcmp(ob.ids, opt.ids, sizeof(int32_t) * opt.n) == 0)
-                            return fail(SPINF_E_INVALID, wq + ": duplicate option");
+                            return fail(SPINF_E_INVALID, wq() + ": duplicate option");
                     }
-                    if (!ids_in_range(opt, o.vocab)) return fail(SPINF_E_INVALID, wq + ": option token out of range");
+                    if (!ids_in_range(opt, o.vocab)) return fail(SPINF_E_INVALID, wq() + ": option token out of range");
                 }
-                if (!ids_in_range(q.tmpl, o.vocab)) return fail(SPINF_E_INVALID, wq + ": template token out of range");
+                if (!ids_in_range(q.tmpl, o.vocab)) return fail(SPINF_E_INVALID, wq() + ": template token out of range");
                 build_trie(q, tries[i][j]);
                 qsize[i].push_back((int64_t)q.tmpl.n + (int64_t)tries[i][j].tok.size());
                 size += qsize[i].back();
             }
-            if (size > o.max_tokens) return fail(SPINF_E_LIMIT, where + ": larger than max_tokens");
+            if (size > o.max_tokens) return fail(SPINF_E_LIMIT, where() + ": larger than max_tokens");
         }
 
         std::unique_ptr<spinf_plan> plan(new spinf_plan());
@@ -390,19 +403,30 @@ extern "C" spinf_status spinf_pack_plan(const spinf_input* inputs, int32_t n_inp
         int32_t n_user_q = q_base[n_inputs];
         plan->user_q_floor.assign(n_user_q, -1);
         if (o.floors) {
-            std::unordered_map<std::string, int32_t> seen;
+            std::unordered_map<uint64_t, int32_t> first_of_hash;   // hash -> first floor with it
+            std::vector<int32_t> next_of_hash;                     // floor -> next floor with its hash
+            std::vector<const spinf_question*> floor_q;            // floor -> its question
             for (int32_t i = 0; i < n_inputs; ++i)
                 for (int32_t j = 0; j < inputs[i].n_questions; ++j) {
                     const spinf_question& q = inputs[i].questions[j];
                     if (q.kind == SPINF_Q_SEARCHED) continue;   // floors belong to scored questions
-                    std::string key = question_key(q);
-                    auto it = seen.find(key);
-                    if (it != seen.end()) {
-                        plan->user_q_floor[q_base[i] + j] = it->second;
+                    const uint64_t h = question_hash(q);
+                    auto it = first_of_hash.find(h);
+                    int32_t f = it == first_of_hash.end() ? -1 : it->second;
+                    while (f >= 0 && !same_question(*floor_q[f], q)) f = next_of_hash[f];
+                    if (f >= 0) {
+                        plan->user_q_floor[q_base[i] + j] = f;
                         continue;
                     }
-                    int32_t f = (int32_t)seen.size();
-                    seen.emplace(key, f);
+                    f = (int32_t)floor_q.size();
+                    floor_q.push_back(&q);
+                    if (it == first_of_hash.end()) {
+                        first_of_hash.emplace(h, f);
+                        next_of_hash.push_back(-1);
+                    } else {   // prepend to the hash's chain (the order of a chain does not matter)
+                        next_of_hash.push_back(it->second);
+                        it->second = f;
+                    }
                     plan->user_q_floor[q_base[i] + j] = f;
                     int64_t size = (int64_t)o.floor_prefix.n + qsize[i][j];
                     if (size > o.token_budget) return fail(SPINF_E_LIMIT, "a floor input does not fit the token budget");
