@@ -52,6 +52,9 @@ struct Trie {
 };
 
 void build_trie(const spinf_question& q, Trie& t) {
+    bool single = true;   // single-token options only: no node, and the layout reads no opt_node
+    for (int32_t o = 0; o < q.n_options && single; ++o) single = q.options[o].n == 1;
+    if (single) return;
     t.opt_node.resize(q.n_options);
     for (int32_t o = 0; o < q.n_options; ++o) {
         const spinf_tokens& opt = q.options[o];
