@@ -771,8 +771,11 @@ void question_stats(const spinf_plan* plan, const QuestionSite& s, const float* 
         m = std::max(m, acc);
     }
     double sum = 0.0;
-    for (int32_t a = 0; a < s.n_options; ++a) sum += std::exp(lp[a] - m);
-    for (int32_t a = 0; a < s.n_options; ++a) p[a] = std::exp(lp[a] - m) / sum;
+    for (int32_t a = 0; a < s.n_options; ++a) {
+        p[a] = std::exp(lp[a] - m);
+        sum += p[a];
+    }
+    for (int32_t a = 0; a < s.n_options; ++a) p[a] /= sum;
     *residual = -std::expm1(m + std::log(sum));
 }
 
@@ -786,7 +789,15 @@ extern "C" spinf_status spinf_collect(const spinf_plan* plan, const float* const
             return fail(SPINF_E_INVALID, "token log-probabilities of a pass are NULL");
     if (!out->option_lp || !out->option_p || !out->residual)
         return fail(SPINF_E_INVALID, "result arrays are NULL");
-    std::vector<double> flp, fp;
+    // each floor once: many user questions share one
+    const size_t n_floors = plan->floor_q.size();
+    std::vector<size_t> foff(n_floors + 1, 0);
+    for (size_t f = 0; f < n_floors; ++f) foff[f + 1] = foff[f] + plan->floor_q[f].n_options;
+    std::vector<double> flp(foff.back()), fp(foff.back()), fres(n_floors);
+    for (size_t f = 0; f < n_floors; ++f) {
+        const QuestionSite& fs = plan->floor_q[f];
+        question_stats(plan, fs, tlp[fs.pass], flp.data() + foff[f], fp.data() + foff[f], &fres[f]);
+    }
     for (size_t qi = 0; qi < plan->user_q.size(); ++qi) {
         const QuestionSite& s = plan->user_q[qi];
         if (s.x >= 0) {   // a searched slot: no options, no floor
@@ -796,18 +807,11 @@ extern "C" spinf_status spinf_collect(const spinf_plan* plan, const float* const
         }
         question_stats(plan, s, tlp[s.pass], out->option_lp + s.opt0, out->option_p + s.opt0, out->residual + qi);
         const int32_t f = plan->user_q_floor[qi];
-        double fres = NAN;
-        flp.assign(s.n_options, NAN);
-        fp.assign(s.n_options, NAN);
-        if (f >= 0) {
-            const QuestionSite& fs = plan->floor_q[f];
-            question_stats(plan, fs, tlp[fs.pass], flp.data(), fp.data(), &fres);
-        }
         for (int32_t a = 0; a < s.n_options; ++a) {
-            if (out->option_floor_lp) out->option_floor_lp[s.opt0 + a] = flp[a];
-            if (out->option_floor_p) out->option_floor_p[s.opt0 + a] = fp[a];
+            if (out->option_floor_lp) out->option_floor_lp[s.opt0 + a] = f >= 0 ? flp[foff[f] + a] : NAN;
+            if (out->option_floor_p) out->option_floor_p[s.opt0 + a] = f >= 0 ? fp[foff[f] + a] : NAN;
         }
-        if (out->floor_residual) out->floor_residual[qi] = fres;
+        if (out->floor_residual) out->floor_residual[qi] = f >= 0 ? fres[f] : NAN;
     }
     return SPINF_OK;
 }
