@@ -10,6 +10,7 @@ torch is used for device memory and streams only.
 from __future__ import annotations
 
 import ctypes
+import itertools
 import os
 from dataclasses import dataclass
 
@@ -269,61 +270,85 @@ class PassInfo:
 
 
 def _marshal(inputs):
-    """Lay the request out as the header's structs in numpy buffers (kept alive by the caller)."""
-    ids, c_off, c_n, nq, t_off, t_n, no, o_off, o_n = [], [], [], [], [], [], [], [], []
-    kind, tset = [], []
-    grids = []   # (input, grid)
-    pos = 0
-    for inp in inputs:
-        content, questions = inp[0], inp[1]
-        grids.extend((len(nq), g) for g in (inp[2] if len(inp) > 2 else ()))
-        c_off.append(pos)
-        c_n.append(len(content))
-        ids.extend(content)
-        pos += len(content)
-        nq.append(len(questions))
+    """Lay the request out as the header's structs in numpy buffers (kept alive by the caller).
+
+    Every token array is one (pointer, length) pair into a single int32 buffer; a sequence
+    object that recurs in the request (the same question list under many contents) is
+    stored once and shared by all its uses."""
+    seqs = []                 # content, then per question its template and options, in request order
+    n_q, kind, tset, n_opt = [], [], [], []
+    grids = []                # (input, grid)
+    for i, inp in enumerate(inputs):
+        questions = inp[1]
+        if len(inp) > 2:
+            grids.extend((i, g) for g in inp[2])
+        seqs.append(inp[0])
+        n_q.append(len(questions))
         for question in questions:
-            template, options = question[0], question[1]
-            t_off.append(pos)
-            t_n.append(len(template))
-            ids.extend(template)
-            pos += len(template)
-            searched = len(question) == 3 and options is None   # (template, None, token_set)
-            kind.append(Q_SEARCHED if searched else Q_SCORED)
-            tset.append(int(question[2]) if searched else -1)
-            options = () if searched else options
-            no.append(len(options))
-            for opt in options:
-                o_off.append(pos)
-                o_n.append(len(opt))
-                ids.extend(opt)
-                pos += len(opt)
-    flat = np.array(ids, dtype=np.int32) if ids else np.zeros(1, dtype=np.int32)
-    base = np.uint64(flat.ctypes.data)
-    four = np.uint64(4)
-    tok = np.zeros(max(len(o_off), 1), dtype=_TOK)
-    que = np.zeros(max(len(t_off), 1), dtype=_QUE)
+            seqs.append(question[0])
+            options = question[1]
+            if options is None and len(question) == 3:   # searched slot: (template, None, token_set)
+                kind.append(Q_SEARCHED)
+                tset.append(int(question[2]))
+                n_opt.append(0)
+            else:
+                kind.append(Q_SCORED)
+                tset.append(-1)
+                n_opt.append(len(options))
+                seqs.extend(options)
+    # one stored copy per distinct sequence object
+    slot_of, uniq = {}, []
+    where = np.empty(len(seqs), dtype=np.int64)
+    for s, seq in enumerate(seqs):
+        u = slot_of.setdefault(id(seq), len(uniq))
+        if u == len(uniq):
+            uniq.append(seq)
+        where[s] = u
+    ulen = np.fromiter(map(len, uniq), dtype=np.int64, count=len(uniq))
+    uoff = np.zeros(len(uniq) + 1, dtype=np.int64)
+    np.cumsum(ulen, out=uoff[1:])
+    total = int(uoff[-1])
+    flat = (np.fromiter(itertools.chain.from_iterable(uniq), dtype=np.int32, count=total) if total
+            else np.zeros(1, dtype=np.int32))
+    lens = ulen[where]
+    addr = np.where(lens > 0, np.uint64(flat.ctypes.data) + np.uint64(4) * uoff[:-1][where].astype(np.uint64),
+                    np.uint64(0))
+    # seq index of each input's content and each question's template (options follow their template)
+    n_q_arr = np.asarray(n_q, dtype=np.int64)
+    n_opt_arr = np.asarray(n_opt, dtype=np.int64)
+    per_q = 1 + n_opt_arr                                       # seqs of each question
+    q_first = np.zeros(len(n_opt) + 1, dtype=np.int64)
+    np.cumsum(per_q, out=q_first[1:])                           # seq offset of question q within the questions
+    in_first_q = np.zeros(len(inputs) + 1, dtype=np.int64)
+    np.cumsum(n_q_arr, out=in_first_q[1:])                      # first question of each input
+    c_idx = np.arange(len(inputs), dtype=np.int64) + q_first[in_first_q[:-1]]   # contents precede their questions
+    t_idx = q_first[:-1] + np.repeat(np.arange(len(inputs), dtype=np.int64) + 1, n_q_arr)
+    o_mask = np.ones(len(seqs), dtype=bool)
+    o_mask[c_idx] = False
+    o_mask[t_idx] = False
+    o_idx = np.flatnonzero(o_mask)
+    tok = np.zeros(max(len(o_idx), 1), dtype=_TOK)
+    que = np.zeros(max(len(n_opt), 1), dtype=_QUE)
     inp = np.zeros(len(inputs), dtype=_INP)
-    if o_off:
-        tok["ids"][:len(o_off)] = base + four * np.asarray(o_off, dtype=np.uint64)
-        tok["n"][:len(o_n)] = o_n
-    if t_off:
-        nt = len(t_off)
-        que["tmpl_ids"][:nt] = base + four * np.asarray(t_off, dtype=np.uint64)
-        que["tmpl_n"][:nt] = t_n
-        first_opt = np.concatenate([[0], np.cumsum(no)[:-1]]).astype(np.uint64)
+    if len(o_idx):
+        tok["ids"][:len(o_idx)] = addr[o_idx]
+        tok["n"][:len(o_idx)] = lens[o_idx]
+    nt = len(n_opt)
+    if nt:
+        que["tmpl_ids"][:nt] = addr[t_idx]
+        que["tmpl_n"][:nt] = lens[t_idx]
+        first_opt = np.concatenate([[0], np.cumsum(n_opt_arr)[:-1]]).astype(np.uint64)
         que["options"][:nt] = np.uint64(tok.ctypes.data) + np.uint64(_TOK.itemsize) * first_opt
-        que["n_options"][:nt] = no
+        que["n_options"][:nt] = n_opt_arr
         que["kind"][:nt] = kind
         que["token_set"][:nt] = tset
     if len(inputs):
-        c_n = np.asarray(c_n, dtype=np.int64)
-        inp["content_ids"] = np.where(c_n > 0, base + four * np.asarray(c_off, dtype=np.uint64), np.uint64(0))
-        inp["content_n"] = c_n
-        first_q = np.concatenate([[0], np.cumsum(nq)[:-1]]).astype(np.uint64)
-        inp["questions"] = np.where(np.asarray(nq) > 0, np.uint64(que.ctypes.data) +
-                                    np.uint64(_QUE.itemsize) * first_q, np.uint64(0))
-        inp["n_questions"] = nq
+        inp["content_ids"] = addr[c_idx]
+        inp["content_n"] = lens[c_idx]
+        first_q = in_first_q[:-1].astype(np.uint64)
+        inp["questions"] = np.where(n_q_arr > 0, np.uint64(que.ctypes.data) + np.uint64(_QUE.itemsize) * first_q,
+                                    np.uint64(0))
+        inp["n_questions"] = n_q_arr
     keep = [flat, que, tok]
     if grids:
         _marshal_grids(inp, grids, keep)
