@@ -335,7 +335,7 @@ def run_ours(args, rank, world):
                                "key_tile": key_tile, "executed_kv_tiles": exec_tiles,
                                "tile_occupancy_128x128": pairs / (sched_tiles * 128 * 128),
                                "peak_source": f"{peak_src} {'bf16_tflops_sustained' if peak_src == 'measured' else ''}".strip()},
-        # per kernel, as the scope table defines them: packed tokens per attention-kernel second
+        # per kernel: packed tokens per attention-kernel second
         # (one layer call per pass) and user questions per scoring second (gather + main + combine)
         "per_kernel": {"attention_packed_tokens_per_s": world * tokens / (attn_ms * 1e-3),
                        "scoring_questions_per_s": world * questions / (score_ms * 1e-3),
@@ -544,7 +544,7 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
 
     Requests are pipelined the way a server would run them: while request i computes, the
     activations of request i+1 go up on a copy stream into the other of two buffer sets and
-    its plan is built on the host; request i's token log-probs come back and are collected
+    its token lists are marshalled and planned on the host; request i's token log-probs come back and are collected
     once its kernels finish.  Every request copies every byte again and reads its results
     back; the timed region covers n whole requests.
     """
@@ -556,7 +556,6 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
     sets = [[tuple(torch.empty_like(t, device=dev) for t in hp) for hp in host] for _ in range(2)]
     obufs = [torch.empty_like(db[0]) for db in sets[0]]
     h2d = sum(t.numel() * t.element_size() for hp in host for t in hp)
-    request = spinf.Request(inputs)        # the caller's tokenised request, laid out once
     ws = [None] * len(passes)
     tl_host = [[torch.empty(max(p["info"].G, 1), dtype=torch.float32, pin_memory=True) for p in passes]
                for _ in range(2)]
@@ -564,7 +563,7 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
     lse_dev = [torch.empty(max(p["info"].M, 1), device=dev) for p in passes]
     # descriptor memory kept across requests (per-plan allocations and frees would synchronise
     # the device every request), one set per request in flight
-    probe = spinf.Plan(request, vocab=shape.vocab)
+    probe = spinf.Plan(inputs, vocab=shape.vocab)
     dbytes = [(probe.descriptor_bytes(pi) + 255) // 256 * 256 + (1 << 20) for pi in range(probe.num_passes)]
     probe.close()
     dsc = [[torch.empty(b, dtype=torch.uint8, device=dev) for b in dbytes] for _ in range(2)]
@@ -582,7 +581,7 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
                 ev = torch.cuda.Event()
                 ev.record(copy_stream)
                 ready.append(ev)
-        plan = spinf.Plan(request, vocab=shape.vocab)      # host planner overlaps the copies
+        plan = spinf.Plan(inputs, vocab=shape.vocab)       # marshal the token lists and plan, overlapping the copies
         for pi in range(plan.num_passes):
             plan.upload(pi, stream, buffer=dsc[b][pi])
         for pi in range(plan.num_passes):
@@ -627,7 +626,8 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
     return {"value": tokens / (ms * 1e-3), "unit": "packed tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": sum(p["info"].G for p in passes) * 4,
             "covers": "per request: H2D q/k/v/hidden (copy stream, overlapping the previous request's kernels) + "
-                      "plan (C planner on the request arrays) + upload into kept descriptor memory + kernels + "
+                      "plan (marshalling of the request's token lists + C planner) + "
+                      "upload into kept descriptor memory + kernels + "
                       "D2H token lps + collect; two requests in flight"}
 
 
