@@ -568,6 +568,7 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
     probe.close()
     dsc = [[torch.empty(b, dtype=torch.uint8, device=dev) for b in dbytes] for _ in range(2)]
     freed = [None, None]     # per buffer set: compute of the request that last read it is done
+    plan_ms = []             # host time to marshal and plan each request
 
     def launch(i):
         b = i % 2
@@ -581,7 +582,9 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
                 ev = torch.cuda.Event()
                 ev.record(copy_stream)
                 ready.append(ev)
+        t_plan = time.perf_counter()
         plan = spinf.Plan(inputs, vocab=shape.vocab)       # marshal the token lists and plan, overlapping the copies
+        plan_ms.append((time.perf_counter() - t_plan) * 1e3)
         for pi in range(plan.num_passes):
             plan.upload(pi, stream, buffer=dsc[b][pi])
         for pi in range(plan.num_passes):
@@ -625,6 +628,7 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
     tokens = sum(p["info"].T for p in passes)
     return {"value": tokens / (ms * 1e-3), "unit": "packed tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": sum(p["info"].G for p in passes) * 4,
+            "host_plan_ms_median": statistics.median(plan_ms[-n:]),
             "covers": "per request: H2D q/k/v/hidden (copy stream, overlapping the previous request's kernels) + "
                       "plan (marshalling of the request's token lists + C planner) + "
                       "upload into kept descriptor memory + kernels + "
