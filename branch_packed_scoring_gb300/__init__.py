@@ -273,18 +273,23 @@ def _marshal(inputs):
     """Lay the request out as the header's structs in numpy buffers (kept alive by the caller).
 
     Every token array is one (pointer, length) pair into a single int32 buffer; a sequence
-    object that recurs in the request (the same question list under many contents) is
-    stored once and shared by all its uses."""
-    seqs = []                 # content, then per question its template and options, in request order
-    n_q, kind, tset, n_opt = [], [], [], []
-    grids = []                # (input, grid)
+    object that recurs in the request is stored once.  Inputs that share one question-list
+    object (the same question set asked of many contents) share one array of question
+    structs, so each distinct list is walked once."""
+    block_of, blocks, in_block, grids = {}, [], [], []
     for i, inp in enumerate(inputs):
-        questions = inp[1]
+        qs = inp[1]
+        b = block_of.setdefault(id(qs), len(blocks))
+        if b == len(blocks):
+            blocks.append(qs)
+        in_block.append(b)
         if len(inp) > 2:
             grids.extend((i, g) for g in inp[2])
-        seqs.append(inp[0])
-        n_q.append(len(questions))
-        for question in questions:
+    seqs = [inp[0] for inp in inputs]   # the contents, then each block's templates and options
+    kind, tset, n_opt, block_q0 = [], [], [], []
+    for qs in blocks:
+        block_q0.append(len(n_opt))
+        for question in qs:
             seqs.append(question[0])
             options = question[1]
             if options is None and len(question) == 3:   # searched slot: (template, None, token_set)
@@ -313,27 +318,20 @@ def _marshal(inputs):
     lens = ulen[where]
     addr = np.where(lens > 0, np.uint64(flat.ctypes.data) + np.uint64(4) * uoff[:-1][where].astype(np.uint64),
                     np.uint64(0))
-    # seq index of each input's content and each question's template (options follow their template)
-    n_q_arr = np.asarray(n_q, dtype=np.int64)
+    n_in, nt = len(inputs), len(n_opt)
     n_opt_arr = np.asarray(n_opt, dtype=np.int64)
-    per_q = 1 + n_opt_arr                                       # seqs of each question
-    q_first = np.zeros(len(n_opt) + 1, dtype=np.int64)
-    np.cumsum(per_q, out=q_first[1:])                           # seq offset of question q within the questions
-    in_first_q = np.zeros(len(inputs) + 1, dtype=np.int64)
-    np.cumsum(n_q_arr, out=in_first_q[1:])                      # first question of each input
-    c_idx = np.arange(len(inputs), dtype=np.int64) + q_first[in_first_q[:-1]]   # contents precede their questions
-    t_idx = q_first[:-1] + np.repeat(np.arange(len(inputs), dtype=np.int64) + 1, n_q_arr)
-    o_mask = np.ones(len(seqs), dtype=bool)
-    o_mask[c_idx] = False
-    o_mask[t_idx] = False
-    o_idx = np.flatnonzero(o_mask)
+    q_first = np.zeros(nt + 1, dtype=np.int64)
+    np.cumsum(1 + n_opt_arr, out=q_first[1:])
+    t_idx = n_in + q_first[:-1]                                 # each question's template
+    o_mask = np.ones(len(seqs) - n_in, dtype=bool)
+    o_mask[q_first[:-1]] = False
+    o_idx = n_in + np.flatnonzero(o_mask)                       # options, question by question
     tok = np.zeros(max(len(o_idx), 1), dtype=_TOK)
-    que = np.zeros(max(len(n_opt), 1), dtype=_QUE)
-    inp = np.zeros(len(inputs), dtype=_INP)
+    que = np.zeros(max(nt, 1), dtype=_QUE)
+    inp = np.zeros(n_in, dtype=_INP)
     if len(o_idx):
         tok["ids"][:len(o_idx)] = addr[o_idx]
         tok["n"][:len(o_idx)] = lens[o_idx]
-    nt = len(n_opt)
     if nt:
         que["tmpl_ids"][:nt] = addr[t_idx]
         que["tmpl_n"][:nt] = lens[t_idx]
@@ -342,13 +340,13 @@ def _marshal(inputs):
         que["n_options"][:nt] = n_opt_arr
         que["kind"][:nt] = kind
         que["token_set"][:nt] = tset
-    if len(inputs):
-        inp["content_ids"] = addr[c_idx]
-        inp["content_n"] = lens[c_idx]
-        first_q = in_first_q[:-1].astype(np.uint64)
-        inp["questions"] = np.where(n_q_arr > 0, np.uint64(que.ctypes.data) + np.uint64(_QUE.itemsize) * first_q,
-                                    np.uint64(0))
-        inp["n_questions"] = n_q_arr
+    if n_in:
+        inp["content_ids"] = addr[:n_in]
+        inp["content_n"] = lens[:n_in]
+        bq = np.asarray([len(qs) for qs in blocks], dtype=np.int64)[in_block]
+        q0 = np.asarray(block_q0, dtype=np.uint64)[in_block]
+        inp["questions"] = np.where(bq > 0, np.uint64(que.ctypes.data) + np.uint64(_QUE.itemsize) * q0, np.uint64(0))
+        inp["n_questions"] = bq
     keep = [flat, que, tok]
     if grids:
         _marshal_grids(inp, grids, keep)

@@ -76,6 +76,24 @@ def test_exact_fit_stays_in_its_pass(spinf, budget):
     assert Q.num_passes == (2 if budget == 10 else 1)
 
 
+def test_shared_question_lists_plan_like_separate_ones(spinf):
+    """Inputs that share one question-list object (marshalled once) plan exactly like the
+    same request written with separate, equal lists, and like the oracle."""
+    import copy
+    shared = [([5, 6, 7], [[1], [2]]), ([8, 9], [[3, 4], [3, 5]]), ([2, 2], None, 0)]
+    other = [([4], [[1]])]
+    empty = []
+    grid = ([[1, 2], [3]], [[[7], [8, 9]]], [[1], [2]])
+    inputs = [([10, 11, 12], shared), ([13] * 40, shared), ([14, 15], other), ([16], empty, [grid]),
+              ([17, 18], shared), ([19], empty), ([], shared)]
+    P1, Q1 = _compare(spinf, inputs, vocab=100)
+    P2, Q2 = _compare(spinf, copy.deepcopy(inputs), vocab=100)
+    for p in range(Q1.num_passes):
+        a, b = Q1.pass_info(p), Q2.pass_info(p)
+        for f in FIELDS:
+            assert np.array_equal(getattr(a, f), getattr(b, f)), (p, f)
+
+
 def test_fuzzed_requests(spinf):
     g = np.random.default_rng(7)
     for trial in range(40):
