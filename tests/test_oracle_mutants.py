@@ -7,6 +7,7 @@ expects at least one pin to fail.  The product is not involved.  One mistake is
 left out on purpose: dropping e4m3's explicit saturation changes nothing, since
 the nearest-code search is already bounded by the largest finite code.
 """
+import concurrent.futures
 import json
 import os
 import subprocess
@@ -96,13 +97,26 @@ MUTANTS = [
 ]
 
 
-@pytest.mark.parametrize("module,old,new", [m[1:] for m in MUTANTS], ids=[m[0] for m in MUTANTS])
-def test_a_planted_mistake_fails_a_pin(module, old, new):
+def _run(module, old, new):
     env = dict(os.environ, ORACLE_MUTANT=json.dumps([module, old, new]),
                PYTHONPATH=os.pathsep.join([HERE, ROOT, os.environ.get("PYTHONPATH", "")]))
     files = [os.path.join(HERE, f) for f in PINS[module]]
     r = subprocess.run([sys.executable, "-m", "pytest", *files, "-q", "-x", "-m", "not gpu", "-p", "oracle_mutant_plugin",
                         "-p", "no:cacheprovider"], cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
-    out = r.stdout + r.stderr
+    return r.returncode, r.stdout + r.stderr
+
+
+@pytest.fixture(scope="module")
+def outcomes():
+    """Every mutant's pin run, several at a time (each is its own interpreter)."""
+    workers = max(1, min(8, (os.cpu_count() or 2) // 2))
+    with concurrent.futures.ThreadPoolExecutor(workers) as pool:
+        futures = {m[0]: pool.submit(_run, *m[1:]) for m in MUTANTS}
+        return {name: f.result() for name, f in futures.items()}
+
+
+@pytest.mark.parametrize("name,module,new", [(m[0], m[1], m[3]) for m in MUTANTS], ids=[m[0] for m in MUTANTS])
+def test_a_planted_mistake_fails_a_pin(outcomes, name, module, new):
+    code, out = outcomes[name]
     assert "mutant pattern occurs" not in out, out[-1500:]
-    assert r.returncode == 1, f"no pin of oracle/{module}.py caught {new!r} (pytest exit {r.returncode}):\n{out[-1500:]}"
+    assert code == 1, f"no pin of oracle/{module}.py caught {new!r} (pytest exit {code}):\n{out[-1500:]}"
