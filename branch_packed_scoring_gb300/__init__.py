@@ -410,7 +410,9 @@ class Request:
     """A request laid out once in the header's structs (``spinf_input`` arrays).
 
     Planning the same request again (``Plan(request)``) then costs only the C
-    planner, not the Python marshalling of nested lists.
+    planner, not the Python marshalling of nested lists.  Marshalling is cheapest
+    when inputs that ask the same questions share one question-list object: that
+    list is walked once and its question structs are shared.
     """
 
     def __init__(self, inputs):
@@ -421,9 +423,11 @@ class Request:
 class Plan:
     """A packed layout of a request (``spinf_pack_plan``).  Owns its device copies.
 
-    ``inputs`` is a list of ``(content_ids, [question, ...])`` or a :class:`Request`;
-    a question is ``(template_ids, [option_ids, ...])`` (scored) or
-    ``(template_ids, None, token_set)`` (a searched slot, ``token_set`` -1 for any token).
+    ``inputs`` is a list of ``(content_ids, [question, ...])`` (optionally a third
+    element, a list of placeholder grids) or a :class:`Request`; a question is
+    ``(template_ids, [option_ids, ...])`` (scored) or ``(template_ids, None, token_set)``
+    (a searched slot, ``token_set`` -1 for any token).  Inputs that ask the same
+    questions can share one question-list object, which is then marshalled once.
     """
 
     def __init__(self, inputs, *, token_budget=None, max_tokens=None, max_content_tokens=None,
