@@ -94,6 +94,18 @@ def test_shared_question_lists_plan_like_separate_ones(spinf):
             assert np.array_equal(getattr(a, f), getattr(b, f)), (p, f)
 
 
+def test_floor_keys(spinf):
+    """One floor per distinct (template, option lists in order): option order, option token
+    splits and template length tell floors apart; equal questions in separate lists share one."""
+    qs = [([1, 2], [[3], [4]]), ([1, 2], [[4], [3]]), ([1, 2], [[3, 4]]), ([1, 2], [[3], [4], [5]]),
+          ([1, 2, 2], [[3], [4]]), ([1], [[2, 3], [4]]), ([1], [[2], [3, 4]])]
+    inputs = [([9, 9, 9], [(list(q[0]), [list(o) for o in q[1]])]) for q in qs]   # one question each
+    inputs += [([8], [(list(q[0]), [list(o) for o in q[1]]) for q in qs])]   # the same questions again
+    P, Q = _compare(spinf, inputs, vocab=100)
+    n_floor_units = sum(1 for lay in P.passes for u in lay.units if u.source < 0)
+    assert n_floor_units == len(qs)
+
+
 def test_fuzzed_requests(spinf):
     g = np.random.default_rng(7)
     for trial in range(40):
