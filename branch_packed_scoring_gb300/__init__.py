@@ -511,7 +511,7 @@ class Plan:
         tp, tk, tl, n = _P(), _P(), _P(), ctypes.c_int32()
         _check(lib().spinf_plan_window_schedule(self.handle, p, window, ctypes.byref(tp), ctypes.byref(tk),
                                                 ctypes.byref(tl), ctypes.byref(n)))
-        nq = self.pass_info(p).n_qtiles
+        nq = self._sizes(p)[0] // 128   # Q tiles of the pass
         arr = lambda ptr, k: np.ctypeslib.as_array(ptr, shape=(k,)).copy() if k > 0 else np.zeros(0, np.int32)  # noqa: E731
         return arr(tp, nq + 1), arr(tk, n.value), arr(tl, n.value)
 
@@ -521,7 +521,7 @@ class Plan:
         tp, tk, tl, n = _P(), _P(), _P(), ctypes.c_int32()
         _check(lib().spinf_plan_tile_schedule(self.handle, p, window, key_tile, ctypes.byref(tp), ctypes.byref(tk),
                                               ctypes.byref(tl), ctypes.byref(n)))
-        nq = self.pass_info(p).n_qtiles
+        nq = self._sizes(p)[0] // 128   # Q tiles of the pass
         arr = lambda ptr, k: np.ctypeslib.as_array(ptr, shape=(k,)).copy() if k > 0 else np.zeros(0, np.int32)  # noqa: E731
         return arr(tp, nq + 1), arr(tk, n.value), arr(tl, n.value)
 

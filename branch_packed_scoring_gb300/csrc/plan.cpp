@@ -231,10 +231,12 @@ WindowSchedule& tile_schedule(Pass& P, int32_t window, int32_t key_tile) {
     int32_t mins[8][kTile];   // sparse table of pos over one Q tile's real rows
     for (int32_t qt = 0; qt < n_qt; ++qt) {
         const int32_t r0 = qt * kTile, r1 = std::min(r0 + kTile, P.T), nr = std::max(r1 - r0, 0);
-        for (int32_t i = 0; i < nr; ++i) mins[0][i] = P.pos[r0 + i];
-        for (int32_t l = 1; (1 << l) <= nr; ++l)
-            for (int32_t i = 0; i + (1 << l) <= nr; ++i)
-                mins[l][i] = std::min(mins[l - 1][i], mins[l - 1][i + (1 << (l - 1))]);
+        if (window > 0) {   // only the window test reads the table
+            for (int32_t i = 0; i < nr; ++i) mins[0][i] = P.pos[r0 + i];
+            for (int32_t l = 1; (1 << l) <= nr; ++l)
+                for (int32_t i = 0; i + (1 << l) <= nr; ++i)
+                    mins[l][i] = std::min(mins[l - 1][i], mins[l - 1][i + (1 << (l - 1))]);
+        }
         auto range_min = [&](int32_t lo, int32_t hi) {   // rows [lo, hi) of the tile, hi > lo
             int32_t l = 0;
             while ((2 << l) <= hi - lo) ++l;
