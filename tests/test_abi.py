@@ -124,3 +124,18 @@ def test_binding_checks_tensors_before_the_call(spinf):
         with pytest.raises(spinf.SpinfError) as e:
             fn()
         assert e.value.status_name == "INVALID" and words in str(e.value), str(e.value)
+
+
+@pytest.mark.parametrize("lang,std", [("c", "c99"), ("c++", "c++17")])
+def test_header_is_plain_c_and_cpp(lang, std):
+    """The public header compiles on its own as strict C99 (no C++ or CUDA types leak into
+    the ABI) and as C++17."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    header = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "spinf.h")
+    r = subprocess.run([cc, f"-std={std}", "-Wall", "-Wextra", "-Werror", "-pedantic", "-fsyntax-only", "-x", lang,
+                        header], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
