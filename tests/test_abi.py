@@ -139,3 +139,30 @@ def test_header_is_plain_c_and_cpp(lang, std):
     r = subprocess.run([cc, f"-std={std}", "-Wall", "-Wextra", "-Werror", "-pedantic", "-fsyntax-only", "-x", lang,
                         header], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_c_caller(spinf, tmp_path):
+    """A C program plans and collects through the library alone (host calls, no Python in
+    between); the layout and the results are the hand-derived ones: content 4 rows, template
+    2, trie node 1, floor 3 (10 rows, 4 scoring rows, 6 gathered tokens); token probabilities
+    1/2 for [7] and 1/4 * 1/2 for [8, 9] give p = 0.8 / 0.2 and residual 0.375; the floor's
+    1/2 and 1/2 * 1/2 give 2/3 / 1/3 and residual 0.25."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc")
+    if cc is None:
+        pytest.skip("no host compiler")
+    here = os.path.dirname(os.path.abspath(__file__))
+    lib_dir = os.path.dirname(spinf.LIB_PATH)
+    exe = str(tmp_path / "c_client")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        os.path.join(here, "c_client.c"), "-o", exe, "-L", lib_dir, "-lspinf",
+                        f"-Wl,-rpath,{lib_dir}", "-lm"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([exe], capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    v = out.stdout.split()
+    assert [int(x) for x in v[:6]] == [1, 10, 4, 6, 1, 2]
+    got = [float(x) for x in v[6:]]
+    want = [0.8, 0.2, 0.375, 2 / 3, 1 / 3, 0.25]
+    assert all(abs(a - b) < 1e-6 for a, b in zip(got, want)), got
