@@ -106,6 +106,24 @@ def test_floor_keys(spinf):
     assert n_floor_units == len(qs)
 
 
+def test_schedule_cache_under_concurrent_callers(spinf):
+    """The per-pass schedules are built on first use under the plan's lock: many threads
+    asking at once (the C calls run without the interpreter lock) all get the schedule a
+    single caller gets."""
+    import concurrent.futures
+    inputs = wl.stress(n_questions=24, content_tokens=300, vocab=1000) + wl.tiny(vocab=1000)
+    ref = spinf.Plan(inputs, token_budget=1024, vocab=1000)
+    keys = [(p, w, kt) for p in range(ref.num_passes) for w in (0, 7, 64) for kt in (64, 128)]
+    assert len(keys) >= 12
+    want = {k: ref.tile_schedule(*k) for k in keys}
+    plan = spinf.Plan(inputs, token_budget=1024, vocab=1000)
+    with concurrent.futures.ThreadPoolExecutor(8) as pool:
+        futures = [(k, pool.submit(plan.tile_schedule, *k)) for k in keys * 6]
+        for k, f in futures:
+            got = f.result()
+            assert all(np.array_equal(a, b) for a, b in zip(got, want[k])), k
+
+
 def test_fuzzed_requests(spinf):
     g = np.random.default_rng(7)
     for trial in range(40):
