@@ -124,6 +124,22 @@ def test_schedule_cache_under_concurrent_callers(spinf):
             assert all(np.array_equal(a, b) for a, b in zip(got, want[k])), k
 
 
+@pytest.mark.parametrize("form", ["int64 arrays", "int32 arrays", "tuples"])
+def test_token_sequences_as_arrays_or_tuples(spinf, form):
+    """Contents, templates and options given as numpy arrays or tuples plan exactly like the
+    same request written with lists."""
+    inputs = wl.stress(n_questions=20, content_tokens=120, vocab=1000) + wl.tiny(vocab=1000)
+    conv = {"int64 arrays": lambda t: np.asarray(t, dtype=np.int64),
+            "int32 arrays": lambda t: np.asarray(t, dtype=np.int32), "tuples": tuple}[form]
+    other = [(conv(c), [(conv(q[0]), [conv(o) for o in q[1]]) for q in qs]) for c, qs in inputs]
+    a, b = spinf.Plan(inputs, vocab=1000), spinf.Plan(other, vocab=1000)
+    assert a.num_passes == b.num_passes
+    for p in range(a.num_passes):
+        x, y = a.pass_info(p), b.pass_info(p)
+        for f in FIELDS:
+            assert np.array_equal(getattr(x, f), getattr(y, f)), (p, f)
+
+
 def test_fuzzed_requests(spinf):
     g = np.random.default_rng(7)
     for trial in range(40):
