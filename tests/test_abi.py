@@ -161,8 +161,14 @@ def test_c_caller(spinf, tmp_path):
     assert r.returncode == 0, r.stderr
     out = subprocess.run([exe], capture_output=True, text=True)
     assert out.returncode == 0, out.stderr
-    v = out.stdout.split()
+    first, second = out.stdout.splitlines()
+    v = first.split()
     assert [int(x) for x in v[:6]] == [1, 10, 4, 6, 1, 2]
     got = [float(x) for x in v[6:]]
     want = [0.8, 0.2, 0.375, 2 / 3, 1 / 3, 0.25]
     assert all(abs(a - b) < 1e-6 for a, b in zip(got, want)), got
+    # searched slot: one slot, k = 2, its answer returned as set; no residual for it
+    v = second.split()
+    assert [int(x) for x in v[:5]] == [1, 2, 1, 42, 17]
+    assert [float(x) for x in v[5:7]] == [-0.5, -1.5] and v[7] == "1"
+    assert all(abs(float(x) - 0.375) < 1e-6 for x in v[8:10])
