@@ -94,6 +94,14 @@ MUTANTS = [
     ("grid-first-placeholder-fastest", "plan", "for combo in itertools.product(*values):",
      "for combo in (c[::-1] for c in itertools.product(*values[::-1])):"),
     ("grid-value-after-segment", "plan", "template += list(value) + list(seg)", "template += list(seg) + list(value)"),
+    ("template-misses-last-content-row", "plan",
+     "                parent.append(prev)\n                content_lo.append(s)\n                content_hi.append(s + L)",
+     "                parent.append(prev)\n                content_lo.append(s)\n                content_hi.append(s + L - 1)"),
+    ("searched-slot-wrong-row", "plan", "x_rows.append(slot)", "x_rows.append(slot - 1)"),
+    ("allowed-set-ignored", "score", "toks[x], lps[x] = topk_allowed(z[x], lse[x], None if s < 0 else token_sets[s], k)",
+     "toks[x], lps[x] = topk_allowed(z[x], lse[x], None, k)"),
+    ("topk-one-short", "score", "top = cand[order[:k]]", "top = cand[order[:k - 1]]"),
+    ("floor-is-the-question-itself", "collect", "flp = question_lp(plan.floor_home[key])", "flp = question_lp(home)"),
 ]
 
 
