@@ -102,6 +102,13 @@ MUTANTS = [
      "toks[x], lps[x] = topk_allowed(z[x], lse[x], None, k)"),
     ("topk-one-short", "score", "top = cand[order[:k]]", "top = cand[order[:k - 1]]"),
     ("floor-is-the-question-itself", "collect", "flp = question_lp(plan.floor_home[key])", "flp = question_lp(home)"),
+    ("content-limit-exclusive", "plan", 'if len(content) > o["max_content_tokens"]:',
+     'if len(content) >= o["max_content_tokens"]:'),
+    ("template-limit-exclusive", "plan", 'if len(template) > o["max_query_tokens"]:',
+     'if len(template) >= o["max_query_tokens"]:'),
+    ("options-limit-exclusive", "plan", 'if len(options) > o["max_options"]:', 'if len(options) >= o["max_options"]:'),
+    ("option-tokens-limit-exclusive", "plan", 'if len(opt) > o["max_option_tokens"]:',
+     'if len(opt) >= o["max_option_tokens"]:'),
 ]
 
 

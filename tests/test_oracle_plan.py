@@ -128,6 +128,27 @@ def test_errors(bad, status):
     assert e.value.status == status
 
 
+def _at_limits():
+    """One input at each of the man page's limits (PARAMETERS): content 4096 tokens, template
+    256, 1000 options, an option of 5 tokens."""
+    return [([1] * 4096, [([2], [[3]])]),
+            ([1], [([2] * 256, [[3]])]),
+            ([1], [([2], [[t] for t in range(1000)])]),
+            ([1], [([2], [[3, 4, 5, 6, 7], [3]])])]
+
+
+def test_limits_are_inclusive():
+    """An input exactly at a limit is accepted; one token or option more is refused."""
+    for inp in _at_limits():
+        op.plan([inp])
+    over = [([1] * 4097, [([2], [[3]])]), ([1], [([2] * 257, [[3]])]),
+            ([1], [([2], [[t] for t in range(1001)])]), ([1], [([2], [[3, 4, 5, 6, 7, 8], [3]])])]
+    for inp in over:
+        with pytest.raises(op.PlanError) as e:
+            op.plan([inp])
+        assert e.value.status == "LIMIT"
+
+
 def test_split_error_when_question_does_not_fit():
     with pytest.raises(op.PlanError) as e:
         op.plan([([1] * 8, [([1, 2, 3], [[1]])])], token_budget=10)

@@ -140,6 +140,14 @@ def test_token_sequences_as_arrays_or_tuples(spinf, form):
             assert np.array_equal(getattr(x, f), getattr(y, f)), (p, f)
 
 
+def test_inputs_at_the_limits(spinf):
+    """Content of 4096 tokens, a 256-token template, 1000 options, a 5-token option: accepted
+    and laid out like the oracle."""
+    for inp in [([1] * 4096, [([2], [[3]])]), ([1], [([2] * 256, [[3]])]),
+                ([1], [([2], [[t] for t in range(1000)])]), ([1], [([2], [[3, 4, 5, 6, 7], [3]])])]:
+        _compare(spinf, [inp])
+
+
 def test_fuzzed_requests(spinf):
     g = np.random.default_rng(7)
     for trial in range(40):
