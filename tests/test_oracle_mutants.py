@@ -3,9 +3,11 @@
 Each case plants one mistake in a copy of an oracle module (a wrong scale or head
 map, an off-by-one, a dropped term or factor, swapped operands, another tie or
 order rule), runs that module's pins against the copy in a fresh interpreter, and
-expects at least one pin to fail.  The product is not involved.  One mistake is
-left out on purpose: dropping e4m3's explicit saturation changes nothing, since
-the nearest-code search is already bounded by the largest finite code.
+expects at least one pin to fail.  The product is not involved.  Two mistakes are
+left out on purpose, being no mistakes: dropping e4m3's explicit saturation (the
+nearest-code search is already bounded by the largest finite code), and sending an
+input of exactly the budget through the split path (the greedy split then keeps all
+of its questions in one unit, the same unit).
 """
 import concurrent.futures
 import json
@@ -109,6 +111,14 @@ MUTANTS = [
     ("options-limit-exclusive", "plan", 'if len(options) > o["max_options"]:', 'if len(options) >= o["max_options"]:'),
     ("option-tokens-limit-exclusive", "plan", 'if len(opt) > o["max_option_tokens"]:',
      'if len(opt) >= o["max_option_tokens"]:'),
+    ("split-prefix-exclusive", "plan", "while j < len(questions) and size + sizes[j] <= budget:",
+     "while j < len(questions) and size + sizes[j] < budget:"),
+    ("floor-prefix-ignored", "plan", '        prefix = tuple(o["floor_prefix"])', "        prefix = ()"),
+    ("floors-in-reverse-order", "plan",
+     "        for content, questions in inputs:\n            for question in questions:\n                if is_searched",
+     "        for content, questions in inputs[::-1]:\n            for question in questions:\n                if is_searched"),
+    ("floor-budget-exclusive", "plan", "                if size > budget:\n                    raise PlanError(\"LIMIT\", \"a floor",
+     "                if size >= budget:\n                    raise PlanError(\"LIMIT\", \"a floor"),
 ]
 
 

@@ -149,6 +149,17 @@ def test_limits_are_inclusive():
         assert e.value.status == "LIMIT"
 
 
+def test_floor_exactly_at_the_budget():
+    """A question of 10 rows (9 template tokens, one 2-token option: one trie node) at budget 10:
+    its floor is exactly 10 rows and fits; with a one-token floor prefix it does not."""
+    inputs = [([], [([2] * 9, [[3, 4]])])]
+    P = op.plan(inputs, token_budget=10)
+    assert [p.T for p in P.passes] == [10, 10]
+    with pytest.raises(op.PlanError) as e:
+        op.plan(inputs, token_budget=10, floor_prefix=[7])
+    assert e.value.status == "LIMIT"
+
+
 def test_split_error_when_question_does_not_fit():
     with pytest.raises(op.PlanError) as e:
         op.plan([([1] * 8, [([1, 2, 3], [[1]])])], token_budget=10)

@@ -146,6 +146,7 @@ def test_inputs_at_the_limits(spinf):
     for inp in [([1] * 4096, [([2], [[3]])]), ([1], [([2] * 256, [[3]])]),
                 ([1], [([2], [[t] for t in range(1000)])]), ([1], [([2], [[3, 4, 5, 6, 7], [3]])])]:
         _compare(spinf, [inp])
+    _compare(spinf, [([], [([2] * 9, [[3, 4]])])], token_budget=10)   # its floor is exactly the budget
 
 
 def test_fuzzed_requests(spinf):
