@@ -47,6 +47,25 @@ def real_rows(lay):
     return np.arange(lay.T)
 
 
+def sample_rows(lay, n, seed):
+    """At least ``n`` rows of a laid-out pass (every row when the pass is smaller): an equal
+    share drawn from every laid-out input (user chunks and floors), each input's first and
+    last rows, a spread of the scoring rows, then rows drawn from the rest up to ``n``."""
+    g = np.random.default_rng(seed)
+    starts = [u.start for u in lay.units] + [lay.T]
+    per = -(-n // max(1, len(lay.units)))
+    rows = set()
+    for a, b in zip(starts, starts[1:]):
+        if b > a:
+            rows |= set(g.choice(np.arange(a, b), size=min(per, b - a), replace=False).tolist())
+            rows |= {a, b - 1}
+    rows |= set(lay.slot_row[:: max(1, len(lay.slot_row) // 64)].tolist())
+    if len(rows) < n:   # small inputs (floors) could not fill their share: top up from the rest
+        rest = np.setdiff1d(np.arange(lay.T), np.fromiter(rows, dtype=np.int64))
+        rows |= set(g.choice(rest, size=min(n - len(rows), len(rest)), replace=False).tolist())
+    return sorted(int(r) for r in rows)
+
+
 def pack_token_sets(sets):
     """Boolean ``[n_sets, V]`` allowed-token sets as the ABI's bitmasks: int32
     ``[n_sets, ceil(V / 32)]``, bit ``v % 32`` of word ``v // 32`` for token ``v``."""

@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import oracle_plan, pass_values, run_attention
+from gpu_util import oracle_plan, pass_values, run_attention, sample_rows
 from oracle import attention as oa
 from synth import workloads as wl
 
@@ -105,16 +105,18 @@ def test_packing_invariance_bitwise(spinf, shape):
         assert torch.equal(o, outs[0][1]), s
 
 
-def test_wikinews_full_pass_sampled_rows(spinf):
+@pytest.mark.parametrize("p,n_rows", [(0, 4096), (1, 2048)], ids=["pass0-contents", "pass1-floors"])
+def test_wikinews_full_pass_sampled_rows(spinf, p, n_rows):
+    """A share of every laid-out input of the pass (pass 0: 14 contents; pass 1: 10 contents
+    and the 56 floors), each input's first and last rows, and the scoring rows."""
     f, shape = wl.WORKLOADS["wikinews"]
     inputs = f()
-    lay = oracle_plan(inputs, vocab=shape.vocab).passes[0]
+    lay = oracle_plan(inputs, vocab=shape.vocab).passes[p]
     plan = spinf.Plan(inputs, vocab=shape.vocab)
     q, k, v, _ = pass_values(lay, shape, hidden_rows=False)
-    o = run_attention(spinf, plan, 0, q, k, v, shape)
-    g = np.random.default_rng(0)
-    rows = sorted(set(g.choice(lay.T, 200, replace=False).tolist()) | set(lay.slot_row[:40].tolist())
-                  | {0, lay.T - 1})
+    o = run_attention(spinf, plan, p, q, k, v, shape)
+    rows = sample_rows(lay, n_rows, p)
+    assert len(rows) >= n_rows
     _check(lay, o, q, k, v, shape, rows)
     assert not torch.isnan(o[:lay.T]).any()
 
