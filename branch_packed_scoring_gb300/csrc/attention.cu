@@ -9,13 +9,13 @@
 // Persistent kernel: one CTA per SM walks a static list of work items, an item
 // being one 128-row Q tile of one query head.  Q tiles are taken longest schedule
 // first, in rounds over the CTAs with every other round reversed, so the CTAs
-// finish together.  When a kv group has an even number of query heads, CTAs run as
-// clusters of two that take two heads of one group on the same Q tile: at d_head
-// 64 and 256 each CTA loads half of every K and V tile and multicasts it to both
-// (a buffer is refilled once both CTAs' MMAs have released it); at d_head 128 the
-// pair is a cta_group::2 MMA pair: the leader issues M = 256 products over both
-// CTAs' rows, and each CTA holds half of every K tile (64 keys) and V tile (64
-// columns).  Warp roles:
+// finish together.  Consecutive items are the query heads of one Q tile, so the CTAs
+// of a round that share a kv head read its K and V tiles at about the same time (the
+// second read comes from L2).  At d_head 128, when a kv group has an even number of
+// query heads, CTAs run as cta_group::2 MMA pairs on two heads of one group: the
+// leader issues M = 256 products over both CTAs' rows, and each CTA holds half of
+// every K tile (64 keys) and V tile (64 columns).  Every CTA loads its own tiles
+// from this GPU's memory (no multicast copies).  Warp roles:
 //   warp 0      one TMA producer thread for Q (once per item), K and V tiles: it
 //               polls the buffers' barriers and issues whichever copy is free first
 //               (each tile one 4-D copy of all its 64-column chunks; two K and two V
@@ -74,24 +74,33 @@ constexpr int kMetaSlots = 4;          // mask-metadata ring: tiles the metadata
 constexpr int kBoxBytes = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128-byte swizzled rows)
 constexpr int kOstageBytes = 32 * 64;  // O staging of one softmax warp: 32 rows x 32 bf16
 
-// Barrier protocol (a parity wait is only correct when its barrier is at most one phase
-// ahead of the phase waited for, so every ring below is sized for the widest lead):
+// Barrier protocol.  A parity wait for the phase of tile G on a ring of n barriers is only
+// correct when the barrier's previous phase (tile G - n) is known to have completed and
+// its next one (tile G + n) cannot have: with the previous phase still open the wait
+// passes at once, with the next one done it blocks.  Every ring below is sized so that
+// each wait meets that condition:
 //   S_FULL[G % kSBufs]  S(G) is in TMEM: the softmax may read it; the K buffer it read is free
 //   P_FULL[G % kSBufs]  every softmax thread has written P(G).  Warps of different lane
 //                       quarters are not in lockstep: one may be at most kSBufs - 1 tiles
 //                       ahead of another (S(G) needs P(G - kSBufs) consumed), so P_FULL
 //                       has kSBufs barriers
-//   P_USED[G % 3]       PV(G) has read P(G), so S(G + 3) may overwrite that TMEM buffer
-//                       (d_head <= 128; with two S buffers V_DONE says the same).  MMAs
-//                       into different accumulators are not ordered by the tensor core.
-//   V_DONE[G & 1]       PV(G) has finished: O may be read or rescaled, its V buffer is free
+//   P_USED[G % kSBufs]  PV(G) has read P(G), so S(G + kSBufs) may overwrite that TMEM
+//                       buffer.  MMAs into different accumulators are not ordered by the
+//                       tensor core.
+//   V_DONE[G % 4]       PV(G) and every earlier PV have finished: O may be read or
+//                       rescaled, V buffer G % 2 is free.  While the softmax works on tile
+//                       G, S(G) has only proven PV(G - kSBufs) done, so up to kSBufs PVs
+//                       (four at d_head 256) may be in flight: with four barriers the
+//                       previous phase of PV(G - 1)'s barrier, PV(G - 5), is always done.
+//                       (A two-barrier ring by tile parity let a wait for PV(G - 1) pass
+//                       while PV(G - 3) was still open at d_head 256: O was then read or
+//                       rescaled under in-flight PV products.)
 //   MMA_DONE(_PV)       all MMAs of one issuer thread have completed (before TMEM is freed)
-// In a multicast pair S_FULL and V_DONE count the commits of both CTAs, which read the
-// shared K/V buffers.
 enum {
     Q_FULL = 0, Q_EMPTY, S_FULL0, S_FULL1, S_FULL2, S_FULL3, P_FULL0, P_FULL1, P_FULL2, P_FULL3, P_USED0, P_USED1,
-    P_USED2, P_USED3, V_DONE0, V_DONE1, MMA_DONE, MMA_DONE_PV, N_FIXED_BARS
+    P_USED2, P_USED3, V_DONE0, V_DONE1, V_DONE2, V_DONE3, MMA_DONE, MMA_DONE_PV, N_FIXED_BARS
 };
+constexpr int kVDone = 4;   // V_DONE ring
 
 // Keys per KV tile: 64 at d_head 256 outside a cta_group::2 pair (Q, two K and two V buffers
 // then fit the shared memory: 64 + 4 x 32 KB), else 128.  A 64-key tile is one half of the
@@ -144,9 +153,8 @@ struct Item {
     int qt, h, s0, n;
 };
 
-// MODE 0: one CTA per item (one query head).  MODE 1: clusters of two CTAs, two heads of a
-// kv group, K/V tiles multicast to both.  MODE 2: cta_group::2 pairs -- the leader issues
-// M = 256 MMAs over both CTAs' rows, each CTA holding half of every K and V tile.
+// MODE 0: one CTA per item (one query head).  MODE 2: cta_group::2 pairs -- the leader
+// issues M = 256 MMAs over both CTAs' rows, each CTA holding half of every K and V tile.
 template <int D, int MODE>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     branch_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -157,10 +165,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             const int32_t* __restrict__ tile_len, const int32_t* __restrict__ row_runs, int T,
                             int Hq, int Hkv, int n_items,
                             float scale_log2, int window, int* __restrict__ err) {
+    static_assert(MODE == 0 || MODE == 2, "one CTA per item, or a cta_group::2 pair");
     static_assert(MODE != 2 || D >= 128, "a cta_group::2 pair splits V into 64-column boxes");
     using L = AttnSmem<D, MODE>;
-    constexpr bool PAIR = MODE != 0;
-    constexpr bool CG2 = MODE == 2;
+    constexpr bool PAIR = MODE == 2;
+    constexpr bool CG2 = PAIR;
     constexpr int TK = kTK<D, MODE>;           // keys per KV tile
     constexpr int KH = TK / 2;                 // keys per softmax thread (half of a tile's row)
     extern __shared__ uint8_t smem_raw[];
@@ -198,9 +207,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     uint64_t* k_full = bars + N_FIXED_BARS;
     uint64_t* v_full = k_full + L::kStages;
-    uint64_t* v_done = bars + V_DONE0;   // [2], by tile parity
+    static_assert(kSBufs<D> <= kVDone, "the V_DONE ring covers every PV that may be in flight");
+    // PV(G) done: barrier V_DONE[G % 4], phase G / 4
+    auto v_done = [&](uint32_t G) { return &bars[V_DONE0 + G % kVDone]; };
+    auto v_phase = [](uint32_t G) { return (G / kVDone) & 1u; };
     // barrier that says P(G) has been read, and its phase index is G / kSBufs
-    auto p_used = [&](uint32_t G) { return kSBufs<D> >= 3 ? &bars[P_USED0 + G % kSBufs<D>] : &v_done[G & 1]; };
+    auto p_used = [&](uint32_t G) { return &bars[P_USED0 + G % kSBufs<D>]; };
     uint64_t* meta_full = v_full + L::kStages;
     uint64_t* meta_empty = meta_full + kMetaSlots;
     if (threadIdx.x == 0) {
@@ -208,8 +220,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int b = 0; b < N_FIXED_BARS; ++b) {
             int count = 1;
             if (b >= P_FULL0 && b <= P_FULL3) count = CG2 ? 2 : kSoftmaxThreads;
-            if (((b >= S_FULL0 && b <= S_FULL3) || b == V_DONE0 || b == V_DONE1) && MODE == 1)
-                count = 2;   // both CTAs' MMAs
             mbar_init(&bars[b], count);
         }
         for (int st = 0; st < L::kStages; ++st) {
@@ -233,10 +243,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (PAIR) cluster_sync();   // the peer's barriers exist before anything is multicast to them
+    if (PAIR) cluster_sync();   // the peer's barriers exist before the pair's copies and commits signal them
     tc_fence_after();
     const uint32_t tmem = *holder;
-    constexpr uint16_t kBoth = 0x3;
 
     if (warp == 0) {
         // ---------------------------------------------------------- Q, K and V producer
@@ -314,9 +323,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                                  kc.kv0 + 64 * rank, 0, kc.I.h / group);
                             } else {
                                 mbar_arrive_expect_tx(&k_full[st], L::kKBytes);
-                                if (!PAIR) tma_load_4d(dst, &tm_k, &k_full[st], 0, kc.kv0, 0, kc.I.h / group);
-                                else if ((G & 1) == (uint32_t)rank)   // the pair's CTAs take alternate K tiles
-                                    tma_load_4d_mc(dst, &tm_k, &k_full[st], 0, kc.kv0, 0, kc.I.h / group, kBoth);
+                                tma_load_4d(dst, &tm_k, &k_full[st], 0, kc.kv0, 0, kc.I.h / group);
                             }
                             const int k_before = kc.k;
                             advance(kc);
@@ -327,7 +334,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 if (!vc.done) {
                     const uint32_t G = vc.G, Gp = G - L::kStages;   // PV(Gp) was the last reader of the buffer
-                    if (G < (uint32_t)L::kStages || mbar_test(&v_done[Gp & 1], (Gp >> 1) & 1)) {
+                    if (G < (uint32_t)L::kStages || mbar_test(v_done(Gp), v_phase(Gp))) {
                         const uint32_t st = G % L::kStages;
                         uint8_t* dst = sV + st * L::kVBytes;
                         if constexpr (CG2) {   // chunks [D/128 rank, D/128 rank + D/128), counted on the leader
@@ -336,9 +343,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                              rank * (L::kChunks / 2), vc.I.h / group);
                         } else {
                             mbar_arrive_expect_tx(&v_full[st], L::kVBytes);
-                            if (!PAIR) tma_load_4d(dst, &tm_v, &v_full[st], 0, vc.kv0, 0, vc.I.h / group);
-                            else if ((G & 1) != (uint32_t)rank)   // the other CTA of the pair takes this V tile
-                                tma_load_4d_mc(dst, &tm_v, &v_full[st], 0, vc.kv0, 0, vc.I.h / group, kBoth);
+                            tma_load_4d(dst, &tm_v, &v_full[st], 0, vc.kv0, 0, vc.I.h / group);
                         }
                         advance(vc);
                         progress = true;
@@ -368,7 +373,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 mbar_drain(&bars[S_FULL0 + b % kSBufs<D>], (b / kSBufs<D>) & 1, err);
             for (uint32_t b = GV > (uint32_t)L::kStages ? GV - L::kStages : 0; b < GV; ++b)
                 if (!CG2 || rank == 0) mbar_drain(&v_full[b % L::kStages], (b / L::kStages) & 1, err);
-            for (uint32_t b = GV > 2u ? GV - 2 : 0; b < GV; ++b) mbar_drain(&v_done[b & 1], (b >> 1) & 1, err);
+            for (uint32_t b = GV > 2u ? GV - 2 : 0; b < GV; ++b) mbar_drain(v_done(b), v_phase(b), err);
             if (ic > 0) {
                 if (!CG2 || rank == 0) mbar_drain(&bars[Q_FULL], (ic - 1) & 1, err);
                 if (CG2) mbar_drain(&bars[Q_EMPTY], (ic - 1) & 1, err);
@@ -385,9 +390,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if constexpr (CG2) mma_commit_pair(bar); else mma_commit(bar);
             };
             const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-            auto commit_shared = [&](uint64_t* bar) {   // a barrier that counts both CTAs of a multicast pair
-                if constexpr (MODE == 1) mma_commit_mc(bar, kBoth); else commit(bar);
-            };
             const bool s_issuer = warp == 1;
             uint32_t G = 0, ic = 0;
             for (int k = 0;; ++k) {
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         // an item's first S waits for the previous item's last PV, so that PV runs first
                         // and the softmax warps start their epilogue sooner; this S is not needed before
                         // that epilogue ends
-                        if (j == 0 && Gs > 0) mbar_wait(&v_done[(Gs - 1) & 1], ((Gs - 1) >> 1) & 1, err);
+                        if (j == 0 && Gs > 0) mbar_wait(v_done(Gs - 1), v_phase(Gs - 1), err);
                         const uint32_t st = Gs % L::kStages;
                         mbar_wait(&k_full[st], (Gs / L::kStages) & 1, err);
                         tc_fence_after();
@@ -422,7 +424,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             if constexpr (CG2) mma_f16_ss_pair(dS, da, db, idesc_qk, kk > 0);
                             else mma_f16_ss(dS, da, db, idesc_qk, kk > 0);
                         }
-                        commit_shared(&bars[S_FULL0 + Gs % kSBufs<D>]);
+                        commit(&bars[S_FULL0 + Gs % kSBufs<D>]);
                         if (j + 1 == I.n) commit(&bars[Q_EMPTY]);   // Q is free once the item's last S is done
                     }
                 } else {
@@ -445,7 +447,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             if constexpr (CG2) mma_f16_ts_pair(tmem + kColO<D>, aP + kk * 8, db, idesc_pv, acc);
                             else mma_f16_ts(tmem + kColO<D>, aP + kk * 8, db, idesc_pv, acc);
                         }
-                        commit_shared(&v_done[Gj & 1]);
+                        commit(v_done(Gj));
                         if constexpr (kSBufs<D> >= 3) commit(&bars[P_USED0 + Gj % kSBufs<D>]);
                     }
                 }
@@ -645,8 +647,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 // Only a rescale waits for the previous tile's PV (grow is false on an item's first
                 // tile); P(j) itself goes to a buffer whose last reader, PV(j-2), finished before S(j).
                 if (__any_sync(0xffffffffu, grow)) {
-                    const uint32_t Gp = G - 1;
-                    mbar_wait(&v_done[Gp & 1], (Gp >> 1) & 1, err);
+                    mbar_wait(v_done(G - 1), v_phase(G - 1), err);   // G >= 1: grow is false on tile 0
                     tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < D / 64; ++c) {
@@ -679,11 +680,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
             }
             // epilogue of the item: O / l to global memory, then O back to zero for the next item
-            {   // PV(G - 2) first: only then is PV(G - 1)'s barrier known to be at most one phase ahead
-                if (G >= 2) mbar_wait(&v_done[G & 1], ((G - 2) >> 1) & 1, err);
-                mbar_wait(&v_done[(G - 1) & 1], ((G - 1) >> 1) & 1, err);
-                tc_fence_after();
-            }
+            mbar_wait(v_done(G - 1), v_phase(G - 1), err);   // the item's last PV, and so every PV
+            tc_fence_after();
             lx[half * 128 + r] = l;
             named_bar_sync(pair_bar, 64);
             const float lrow = lx[r] + lx[128 + r];      // halves added in a fixed order
@@ -773,7 +771,7 @@ spinf_status launch_mode(const Pass& P, const Sched& sc, const CUtensorMap& tq, 
                                                      sc.tile_kv, sc.tile_len, P.dev.row_runs, P.T, Hq, Hkv,
                                                      n_items,
                                                      scale_log2, window, err);
-    } else {   // clusters of two CTAs, two heads of a kv group per item
+    } else {   // cta_group::2 pairs: clusters of two CTAs, two heads of a kv group per item
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
@@ -831,18 +829,14 @@ spinf_status launch_attention(const Pass& P, const Sched& sc, const void* q, con
         return st;
     __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
     const float scale_log2 = scale * 1.4426950408889634f;
-    // an even number of query heads per kv head pairs two heads per item: d_head 128 as a
-    // cta_group::2 pair (half tiles), d_head 64 and 256 as a multicast pair (at 256 the
-    // multicast pair measured faster: its softmax warps are not coupled across the two SMs)
-    // the kernel's third map: a K tile's key half (cta_group::2 pair, d_head 128); d_head 256
-    // copies 64-key K and V tiles (boxes of 64 rows) on the 64-key schedule
+    // d_head 128 with an even number of query heads per kv head: a cta_group::2 pair of two
+    // heads (the kernel's third map is a K tile's key half); otherwise one CTA per head.
+    // d_head 256 copies 64-key K and V tiles (boxes of 64 rows) on the 64-key schedule
     const CUtensorMap& kmap = D == 256 ? tkh : tk;
     const CUtensorMap& vmap = D == 256 ? tvk : tv;
-    if ((Hq / Hkv) % 2 != 0) return launch_mode<D, 0>(P, sc, tq, kmap, tkh, vmap, ob, Hq, Hkv, scale_log2, window, err, stream);
     if constexpr (D == 128)
-        return launch_mode<D, 2>(P, sc, tq, tk, tkh, tvh, ob, Hq, Hkv, scale_log2, window, err, stream);
-    else
-        return launch_mode<D, 1>(P, sc, tq, kmap, tkh, vmap, ob, Hq, Hkv, scale_log2, window, err, stream);
+        if ((Hq / Hkv) % 2 == 0) return launch_mode<D, 2>(P, sc, tq, tk, tkh, tvh, ob, Hq, Hkv, scale_log2, window, err, stream);
+    return launch_mode<D, 0>(P, sc, tq, kmap, tkh, vmap, ob, Hq, Hkv, scale_log2, window, err, stream);
 }
 
 }  // namespace

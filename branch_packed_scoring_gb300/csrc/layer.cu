@@ -11,14 +11,9 @@
 // DESCRIPTION, --quant fp8s) has static scales: one per activation tensor, one
 // per weight output channel, fixed before the request.
 //
-//   linear_kernel<FP8, MODE, PAIR>  persistent tcgen05 GEMM y = x w^T: 128 rows x 256
+//   linear_kernel<FP8, MODE>   persistent tcgen05 GEMM y = x w^T: 128 rows x 256
 //                              output features per tile, fp32 in TMEM (two
-//                              accumulators), a 4-stage TMA ring.  PAIR: clusters of
-//                              two CTAs on two row blocks of the same features; each
-//                              loads half of the weight tile and multicasts it to
-//                              both, so a CTA's L2 operand traffic per k-step falls
-//                              from 48 to 32 KB (the tile rate is bound by it: ~96
-//                              bytes per SM clock at the tensor peak).  MODE 0 writes y;
+//                              accumulators), a 4-stage TMA ring.  MODE 0 writes y;
 //                              MODE 1 (QKV) turns the q and k columns by the row's
 //                              tree position in the epilogue and writes q, k, v in
 //                              the attention kernel's layouts.
@@ -139,7 +134,7 @@ constexpr int kLB = kLN * 128;
 constexpr int kLStage = kLA + kLB;
 constexpr int kLThreads = 192;
 enum { LFULL0 = 0, LEMPTY0 = kLStages, LACC_FULL0 = 2 * kLStages, LACC_EMPTY0 = 2 * kLStages + 2,
-       LN_BARS = 2 * kLStages + 4 };   // then one more: the MMA thread's final commit (PAIR)
+       LN_BARS = 2 * kLStages + 4 };
 constexpr int kLSmemBars = kLStages * kLStage;
 constexpr int kLSmemHolder = kLSmemBars + (LN_BARS + 1) * 8;
 constexpr int kLSmem = kLSmemHolder + 16 + 1024;
@@ -167,7 +162,7 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&
                            pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
 }
 
-template <bool FP8, int MODE, bool PAIR>
+template <bool FP8, int MODE>
 __global__ void __launch_bounds__(kLThreads, 1)
     linear_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                   const float* __restrict__ w_scale, float x_scale, const LinearOut out, int rows, int N, int n_kb,
@@ -182,19 +177,14 @@ __global__ void __launch_bounds__(kLThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kLSmemBars);
     uint32_t* holder = reinterpret_cast<uint32_t*>(smem + kLSmemHolder);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // PAIR: a unit is (row-block pair, feature tile) walked by both CTAs of a cluster;
-    // this CTA takes row block 2 * pair + rank
-    const int rank = PAIR ? (int)cluster_ctarank() : 0;
-    const int n_units_m = PAIR ? (n_mt + 1) / 2 : n_mt;
-    const int total = n_units_m * n_nt;
-    const int first = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-    const int stride = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-    constexpr uint16_t kBoth = 0x3;
+    const int total = n_mt * n_nt;
+    const int first = (int)blockIdx.x;
+    const int stride = (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kLStages; ++s) {
             mbar_init(&bars[LFULL0 + s], 1);
-            mbar_init(&bars[LEMPTY0 + s], PAIR ? 2 : 1);   // PAIR: both CTAs' MMAs read the stage
+            mbar_init(&bars[LEMPTY0 + s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&bars[LACC_FULL0 + a], 1);
@@ -209,7 +199,6 @@ __global__ void __launch_bounds__(kLThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (PAIR) cluster_sync();   // the peer's barriers exist before anything is multicast to them
     tc_fence_after();
     const uint32_t tmem = *holder;
 
@@ -221,20 +210,15 @@ __global__ void __launch_bounds__(kLThreads, 1)
             tma_prefetch_desc(&tm_w);
             uint32_t it = 0;
             for (int u = first; u < total; u += stride) {
-                const int mt = PAIR ? 2 * (u / n_nt) + rank : u / n_nt, nt = u % n_nt;
+                const int mt = u / n_nt, nt = u % n_nt;
                 for (int kb = 0; kb < n_kb; ++kb, ++it) {
                     const int s = it % kLStages;
                     mbar_wait(&bars[LEMPTY0 + s], ((it / kLStages) & 1) ^ 1, err);
                     uint8_t* sa = smem + s * kLStage;
-                    // the stage receives the whole tile: own rows, and both halves of the weights
+                    // the stage receives the whole tile: the row block and the weight tile
                     mbar_arrive_expect_tx(&bars[LFULL0 + s], kLStage);
-                    // a pair's second block past the last one reloads the last block (never stored)
-                    tma_load_2d(sa, &tm_x, &bars[LFULL0 + s], kb * kBK, min(mt, n_mt - 1) * kLM);
-                    if (PAIR)
-                        tma_load_2d_mc(sa + kLA + rank * (kLB / 2), &tm_w, &bars[LFULL0 + s], kb * kBK,
-                                       nt * kLN + rank * (kLN / 2), kBoth);
-                    else
-                        tma_load_2d(sa + kLA, &tm_w, &bars[LFULL0 + s], kb * kBK, nt * kLN);
+                    tma_load_2d(sa, &tm_x, &bars[LFULL0 + s], kb * kBK, mt * kLM);
+                    tma_load_2d(sa + kLA, &tm_w, &bars[LFULL0 + s], kb * kBK, nt * kLN);
                 }
             }
             for (uint32_t i = it > (uint32_t)kLStages ? it - kLStages : 0; i < it; ++i)
@@ -261,16 +245,13 @@ __global__ void __launch_bounds__(kLThreads, 1)
                         if (FP8) mma_f8_ss(d_tmem, da, db, idesc, (kb | kk) != 0);
                         else mma_f16_ss(d_tmem, da, db, idesc, (kb | kk) != 0);
                     }
-                    // PAIR: the stage holds the peer's multicast too: free it in both CTAs
-                    if (PAIR) mma_commit_mc(&bars[LEMPTY0 + s], kBoth);
-                    else mma_commit(&bars[LEMPTY0 + s]);
+                    mma_commit(&bars[LEMPTY0 + s]);
                 }
                 mma_commit(&bars[LACC_FULL0 + acc]);
             }
-            if (PAIR) {   // every MMA (and so every commit to the peer) has completed before exit
-                mma_commit(&bars[LN_BARS]);
-                mbar_drain(&bars[LN_BARS], 0, err);
-            }
+            // every MMA (and so every commit to this CTA's barriers) has completed before exit
+            mma_commit(&bars[LN_BARS]);
+            mbar_drain(&bars[LN_BARS], 0, err);
         }
     } else {
         const int quarter = warp & 3;
@@ -278,7 +259,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         uint32_t tcount = 0;
         for (int u = first; u < total; u += stride, ++tcount) {
-            const int mt = PAIR ? 2 * (u / n_nt) + rank : u / n_nt, nt = u % n_nt;
+            const int mt = u / n_nt, nt = u % n_nt;
             const int acc = tcount & 1;
             const int row = mt * kLM + r;
             const int n0 = nt * kLN;
@@ -369,15 +350,14 @@ __global__ void __launch_bounds__(kLThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (PAIR) cluster_sync();   // no CTA leaves while its peer may still signal or write it
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
 }
 
-template <bool FP8, int MODE, bool PAIR>
-spinf_status launch_linear_impl(const void* x, const void* w, const float* w_scale, float x_scale, const LinearOut& out,
+template <bool FP8, int MODE>
+spinf_status launch_linear(const void* x, const void* w, const float* w_scale, float x_scale, const LinearOut& out,
                            int64_t rows, int64_t K, int64_t N, int* err, cudaStream_t stream) {
     CUtensorMap tx, tw;
     const uint64_t elt = FP8 ? 1 : 2;
@@ -385,52 +365,24 @@ spinf_status launch_linear_impl(const void* x, const void* w, const float* w_sca
     const uint64_t dw[2] = {(uint64_t)K, (uint64_t)N};
     const uint64_t st[1] = {(uint64_t)K * elt};
     const uint32_t bx[2] = {FP8 ? 128u : 64u, (uint32_t)kLM};
-    const uint32_t bw[2] = {FP8 ? 128u : 64u, (uint32_t)(PAIR ? kLN / 2 : kLN)};
+    const uint32_t bw[2] = {FP8 ? 128u : 64u, (uint32_t)kLN};
     const CUtensorMapDataType dt = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     spinf_status s;
     if ((s = make_tmap(&tx, dt, 2, x, dx, st, bx, CU_TENSOR_MAP_SWIZZLE_128B))) return s;
     if ((s = make_tmap(&tw, dt, 2, w, dw, st, bw, CU_TENSOR_MAP_SWIZZLE_128B))) return s;
-    if ((s = set_smem_limit(reinterpret_cast<const void*>(linear_kernel<FP8, MODE, PAIR>), kLSmem,
+    if ((s = set_smem_limit(reinterpret_cast<const void*>(linear_kernel<FP8, MODE>), kLSmem,
                             "cudaFuncSetAttribute(linear)")))
         return s;
     cudaError_t e;
     const int kbk = FP8 ? 128 : 64;
     const int n_kb = (int)((K + kbk - 1) / kbk);
     const int n_mt = (int)((rows + kLM - 1) / kLM), n_nt = (int)((N + kLN - 1) / kLN);
-    if constexpr (PAIR) {
-        const int units = (n_mt + 1) / 2 * n_nt;
-        const int clusters = std::max(1, std::min(units, sm_count() / 2));
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2 * clusters);
-        cfg.blockDim = dim3(kLThreads);
-        cfg.dynamicSmemBytes = kLSmem;
-        cfg.stream = stream;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, linear_kernel<FP8, MODE, PAIR>, tx, tw, w_scale, x_scale, out, (int)rows, (int)N,
-                               n_kb, n_mt, n_nt, err);
-    } else {
-        const int grid = std::min(n_mt * n_nt, sm_count());
-        linear_kernel<FP8, MODE, PAIR><<<grid, kLThreads, kLSmem, stream>>>(tx, tw, w_scale, x_scale, out, (int)rows,
-                                                                           (int)N, n_kb, n_mt, n_nt, err);
-        e = cudaGetLastError();
-    }
+    const int grid = std::min(n_mt * n_nt, sm_count());
+    linear_kernel<FP8, MODE><<<grid, kLThreads, kLSmem, stream>>>(tx, tw, w_scale, x_scale, out, (int)rows, (int)N,
+                                                                 n_kb, n_mt, n_nt, err);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "linear launch");
     return SPINF_OK;
-}
-
-// Pairs when there are at least two row blocks (a lone block would only make its peer
-// load zeros).
-template <bool FP8, int MODE>
-spinf_status launch_linear(const void* x, const void* w, const float* w_scale, float x_scale, const LinearOut& out,
-                           int64_t rows, int64_t K, int64_t N, int* err, cudaStream_t stream) {
-    if (rows > kLM) return launch_linear_impl<FP8, MODE, true>(x, w, w_scale, x_scale, out, rows, K, N, err, stream);
-    return launch_linear_impl<FP8, MODE, false>(x, w, w_scale, x_scale, out, rows, K, N, err, stream);
 }
 
 spinf_status check_dtype_args(int32_t w_dtype, const float* w_scale, float x_scale) {

@@ -7,9 +7,9 @@ batch invariance of the target input across ten random packings.
 * many-questions stress pass (Qwen-class heads, d_head 128, 40/8 heads,
   vocabulary 151936, d_model 5120): attention with and without a window that
   bites (content of 4000 tokens), scoring of multi-token options;
-* batch invariance: a 470-token content with 56 questions, alone and inserted
-  at a random index among 2000 short inputs (10 packings); its attention rows
-  and its e4m3 scores must be bit-identical in every packing.
+* batch invariance: a 470-token content with 56 questions, alone (twice) and
+  inserted at a random index among 2000 short inputs (10 packings); its attention
+  rows and its e4m3 scores must be bit-identical in every run.
 """
 import numpy as np
 import pytest
@@ -91,7 +91,8 @@ def test_batch_invariance_ten_packings_e4m3(spinf):
     codes, scale = sv.e4m3_rows(w)
     del w
     target = wl.invariance_target()
-    runs = [([target], 0)] + [wl.invariance_packing(s) for s in range(1, 11)]
+    # alone twice (a difference there would be a race, not an order dependence), then ten packings
+    runs = [([target], 0), ([target], 0)] + [wl.invariance_packing(s) for s in range(1, 11)]
     ref = None
     offsets = set()
     for inputs, idx in runs:

@@ -54,10 +54,53 @@ def test_workloads_bit_exact(spinf, name):
     _compare(spinf, f(), vocab=shape.vocab)
 
 
-def test_invariance_packing_bit_exact(spinf):
-    inputs, _ = wl.invariance_packing(1)
+@pytest.mark.parametrize("seed", range(1, 11))
+def test_invariance_packing_bit_exact(spinf, seed):
+    """Every one of the ten packings of the batch-invariance pass plans exactly like the oracle."""
+    inputs, _ = wl.invariance_packing(seed)
     _compare(spinf, inputs, vocab=262144)
+
+
+def test_invariance_target_alone_bit_exact(spinf):
     _compare(spinf, [wl.invariance_target()], vocab=262144)
+
+
+def _target_tiles(spinf, inputs, idx, key_tile):
+    """Per row of the target input (relative to its first row): the executed KV tiles of
+    its Q tile that hold a key the row sees, as (first key, length, visible keys), all
+    relative to the input's first row; and that every other executed tile of the row's Q
+    tile holds no key the row sees."""
+    P = op.plan(inputs, vocab=262144)
+    p, u = next((p, u) for p, lay in enumerate(P.passes) for u in lay.units if u.source == idx)
+    lay = P.passes[p]
+    tp, tk, tl = spinf.Plan(inputs, vocab=262144).tile_schedule(p, 0, key_tile)
+    out = []
+    for r in range(u.start, u.start + u.size):
+        vis = set(lay.visible(r))
+        seq = []
+        for e in range(tp[r // 128], tp[r // 128 + 1]):
+            seen = tuple(k - u.start for k in range(tk[e], tk[e] + tl[e]) if k in vis)
+            if seen:
+                seq.append((int(tk[e]) - u.start, int(tl[e]), seen))
+        assert sum(len(t[2]) for t in seq) == len(vis), r   # every visible key is in an executed tile
+        out.append(tuple(seq))
+    return out, u.start
+
+
+@pytest.mark.parametrize("key_tile", [64, 128])
+def test_invariance_target_executed_tiles(spinf, key_tile):
+    """The batch-invariance target's rows meet the same anchored KV tiles, in the same order
+    and with the same visible keys at the same columns, alone and in all ten packings
+    (what makes a row's attention output bit-identical alone or packed); every other
+    executed tile of its Q tile is fully masked for it."""
+    ref, _ = _target_tiles(spinf, [wl.invariance_target()], 0, key_tile)
+    offsets = set()
+    for seed in range(1, 11):
+        inputs, idx = wl.invariance_packing(seed)
+        got, start = _target_tiles(spinf, inputs, idx, key_tile)
+        offsets.add(start % 128)
+        assert got == ref, seed
+    assert len(offsets) > 3   # the packings put the target at several offsets within a Q tile
 
 
 @pytest.mark.parametrize("budget", [256, 700, 2048])
