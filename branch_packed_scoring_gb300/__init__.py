@@ -31,7 +31,8 @@ SYMBOLS = [
     "spinf_plan_counts", "spinf_plan_extract_counts", "spinf_plan_upload", "spinf_plan_descriptor_bytes", "spinf_plan_upload_to",
     "spinf_plan_window_schedule", "spinf_plan_tile_schedule",
     "spinf_branch_attention", "spinf_score_workspace_bytes",
-    "spinf_score", "spinf_score_extract", "spinf_score_static", "spinf_collect", "spinf_collect_extract",
+    "spinf_score", "spinf_score_extract", "spinf_score_static", "spinf_score_passes_workspace_bytes",
+    "spinf_score_passes", "spinf_collect", "spinf_collect_extract",
     "spinf_device_status", "spinf_device_selftest",
     "spinf_rope_tree", "spinf_linear", "spinf_qkv_rope", "spinf_quantize_static",
     "spinf_decode_attention", "spinf_score_rows_workspace_bytes", "spinf_score_rows",
@@ -128,6 +129,9 @@ def lib():
     L.spinf_score_extract.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, vp, vp, ctypes.POINTER(_ExtractOut), vp,
                                       sz, vp]
     L.spinf_score_static.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp]
+    L.spinf_score_passes_workspace_bytes.argtypes = [vp, i32, vp, i32, i32, i32]
+    L.spinf_score_passes_workspace_bytes.restype = sz
+    L.spinf_score_passes.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
     L.spinf_collect.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(_Result)]
     L.spinf_collect_extract.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, vp]
     L.spinf_device_status.argtypes = [vp, vp]
@@ -149,7 +153,8 @@ def lib():
     L.spinf_last_error.restype = ctypes.c_char_p
     for name in ("spinf_pack_plan", "spinf_plan_pass_info", "spinf_plan_counts", "spinf_plan_extract_counts",
                  "spinf_plan_upload", "spinf_plan_upload_to", "spinf_plan_window_schedule", "spinf_plan_tile_schedule",
-                 "spinf_branch_attention", "spinf_score", "spinf_score_extract", "spinf_score_static", "spinf_collect",
+                 "spinf_branch_attention", "spinf_score", "spinf_score_extract", "spinf_score_static",
+                 "spinf_score_passes", "spinf_collect",
                  "spinf_collect_extract",
                  "spinf_device_status", "spinf_device_selftest", "spinf_rope_tree", "spinf_linear",
                  "spinf_qkv_rope", "spinf_quantize_static", "spinf_decode_attention", "spinf_score_rows"):
@@ -665,6 +670,38 @@ def _score_args(a, plan, p, hidden, w, w_scale, w_dtype, d_model, vocab, row_lse
     return (a(hidden, "hidden", "bf16", T * d_model), a(w, "w", kind, vocab * d_model),
             a(w_scale, "w_scale", "f32", vocab), w_dtype, d_model, vocab, a(row_lse, "row_lse", "f32", M),
             a(token_lp, "token_lp", "f32", G))
+
+
+def _pass_list(passes):
+    arr = np.ascontiguousarray(np.asarray(list(passes), dtype=np.int32))
+    return arr, arr.ctypes.data
+
+
+def score_passes_workspace_bytes(plan, passes, vocab, d_model, w_dtype=DTYPE_BF16):
+    arr, ptr = _pass_list(passes)
+    return lib().spinf_score_passes_workspace_bytes(plan.handle, len(arr), ptr, vocab, d_model, w_dtype)
+
+
+def score_passes(plan, passes, hidden, w, w_scale, w_dtype, d_model, vocab, row_lse, token_lp, workspace,
+                 workspace_bytes=None, stream=None):
+    """``spinf_score_passes``: the passes in ``passes`` scored in one sweep of the lm head; ``hidden``,
+    ``row_lse`` and ``token_lp`` are lists with one device tensor per listed pass."""
+    arr, ptr = _pass_list(passes)
+    n = len(arr)
+    if not (len(hidden) == len(row_lse) == len(token_lp) == n):
+        raise SpinfError(E_INVALID, "score_passes: one hidden, row_lse and token_lp per pass")
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    a, kind = _Args("score_passes"), _wkind(w_dtype)
+    hs, ls, ts = (ctypes.c_void_p * max(n, 1))(), (ctypes.c_void_p * max(n, 1))(), (ctypes.c_void_p * max(n, 1))()
+    for b, p in enumerate(arr.tolist()):
+        T, M, G, _ = plan._sizes(p)
+        hs[b] = a(hidden[b], f"hidden[{b}]", "bf16", T * d_model)
+        ls[b] = a(row_lse[b], f"row_lse[{b}]", "f32", M)
+        ts[b] = a(token_lp[b], f"token_lp[{b}]", "f32", G)
+    _check(lib().spinf_score_passes(plan.handle, n, ptr, hs, a(w, "w", kind, vocab * d_model),
+                                    a(w_scale, "w_scale", "f32", vocab), w_dtype, d_model, vocab, ls, ts,
+                                    a(workspace, "workspace", "bytes"), int(workspace_bytes), _stream(stream)))
 
 
 def score_static(plan, p, hidden, w, w_scale, w_dtype, d_model, vocab, row_lse, token_lp, stream=None):

@@ -22,6 +22,9 @@
 //                    top k (z descending, lower id first on ties), lp = z - lse
 //   rows outside a plan  spinf_score_rows: the same kernels on caller-given rows
 //                    (the decode rows of searched slots), every row searched
+//   several passes   spinf_score_passes: the scoring rows of up to 32 passes of
+//                    one plan as one list of rows, so that one sweep over the lm
+//                    head serves them all and only the last 128-row tile is padded
 //
 // Every reduction runs in a fixed order that depends only on the row's own
 // values and the vocabulary size, so a row's results do not depend on M or on
@@ -64,17 +67,58 @@ constexpr int kScoreSmemX = kSmemXStage + 128 * 33 * 4 + 1024;
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
+// The scoring rows of one call as one list: rows [m0[b], m0[b + 1]) are the scoring rows
+// of the call's b-th pass (its local rows 0, 1, ...), their gathers [g0[b], g0[b + 1]) of
+// the call's gathered logits.  A single-pass call has nb = 1.
+constexpr int kMaxScorePasses = SPINF_SCORE_MAX_PASSES;
+struct RowMap {
+    int nb;
+    int m0[kMaxScorePasses + 1];
+    int g0[kMaxScorePasses + 1];
+    const __nv_bfloat16* hidden[kMaxScorePasses];   // [T_pad, D] of each pass
+    const int32_t* slot_row[kMaxScorePasses];       // [M_b]
+    const int32_t* row_gptr[kMaxScorePasses];       // [M_b + 1]
+    const int32_t* row_glist[kMaxScorePasses];      // [G_b]
+    const int32_t* gather_tok[kMaxScorePasses];     // [G_b]
+    float* row_lse[kMaxScorePasses];                // [M_b]
+    float* token_lp[kMaxScorePasses];               // [G_b]
+};
+
+// The pass b of list row m (m < m0[nb]).
+__device__ __forceinline__ int row_pass(const RowMap& rm, int m) {
+    int b = 0;
+    while (b + 1 < rm.nb && m >= rm.m0[b + 1]) ++b;
+    return b;
+}
+
+// A one-pass map over the pass's own device descriptors.
+RowMap one_pass_map(const Pass& P, const void* hidden, float* row_lse, float* token_lp) {
+    RowMap rm{};
+    rm.nb = 1;
+    rm.m0[1] = (int)P.slot_row.size();
+    rm.g0[1] = (int)P.gather_tok.size();
+    rm.hidden[0] = static_cast<const __nv_bfloat16*>(hidden);
+    rm.slot_row[0] = P.dev.slot_row;
+    rm.row_gptr[0] = P.dev.row_gptr;
+    rm.row_glist[0] = P.dev.row_glist;
+    rm.gather_tok[0] = P.dev.gather_tok;
+    rm.row_lse[0] = row_lse;
+    rm.token_lp[0] = token_lp;
+    return rm;
+}
+
 struct ScoreLayout {
     int M, M_pad, G, n_vt, n_st, X, k;
     size_t hs, sa, part, zg, xpart, total;
 };
 
-ScoreLayout score_layout(const Pass& P, int vocab, int d_model, int w_dtype, int extract_k) {
+// Workspace layout for M scoring rows, G gathers and X searched slots.
+ScoreLayout score_layout_counts(int M, int G, int X, int vocab, int d_model, int w_dtype, int extract_k) {
     ScoreLayout s;
-    s.X = (int)P.x_m.size();
+    s.X = X;
     s.k = extract_k;
-    s.M = (int)P.slot_row.size();
-    s.G = (int)P.gather_tok.size();
+    s.M = M;
+    s.G = G;
     s.M_pad = std::max(1, (s.M + kBM - 1) / kBM) * kBM;
     s.n_st = s.M_pad / kBM;
     s.n_vt = (vocab + kBN - 1) / kBN;
@@ -88,14 +132,22 @@ ScoreLayout score_layout(const Pass& P, int vocab, int d_model, int w_dtype, int
     return s;
 }
 
+ScoreLayout score_layout(const Pass& P, int vocab, int d_model, int w_dtype, int extract_k) {
+    return score_layout_counts((int)P.slot_row.size(), (int)P.gather_tok.size(), (int)P.x_m.size(), vocab, d_model,
+                               w_dtype, extract_k);
+}
+
 // ---------------------------------------------------------------- K4
 template <bool FP8>
-__global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* __restrict__ hidden,
-                                                          const int32_t* __restrict__ slot_row, int M, int D,
+__global__ void __launch_bounds__(256) gather_rows_kernel(const __grid_constant__ RowMap rm, int M, int D,
                                                           void* __restrict__ out, float* __restrict__ s_act) {
     const int m = blockIdx.x;
     const int nv = D / 8;   // 8 elements per vector
-    const uint4* src = m < M ? reinterpret_cast<const uint4*>(hidden + (size_t)slot_row[m] * D) : nullptr;
+    const uint4* src = nullptr;
+    if (m < M) {
+        const int b = row_pass(rm, m);
+        src = reinterpret_cast<const uint4*>(rm.hidden[b] + (size_t)rm.slot_row[b][m - rm.m0[b]] * D);
+    }
     if (!FP8) {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + (size_t)m * D);
         for (int i = threadIdx.x; i < nv; i += blockDim.x) dst[i] = src ? src[i] : make_uint4(0, 0, 0, 0);
@@ -186,8 +238,7 @@ template <bool FP8, int KX>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_main_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                       const float* __restrict__ s_act, const float* __restrict__ s_w, float2* __restrict__ part,
-                      float* __restrict__ zg, const int32_t* __restrict__ row_gptr,
-                      const int32_t* __restrict__ row_glist, const int32_t* __restrict__ gather_tok, int M, int V,
+                      float* __restrict__ zg, const __grid_constant__ RowMap rm, int M, int V,
                       int n_kb, int n_st, int n_vt, const ExtractArgs xa, int* __restrict__ err) {
     constexpr int kPerMma = FP8 ? 32 : 16;           // K elements of one MMA instruction
     constexpr int kMmaPerStage = (FP8 ? 128 : 64) / kPerMma;
@@ -283,8 +334,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             const bool valid = m < M;
             const int v0 = vt * kBN;
             int gc = 0, ge = 0;
+            // this row's pass: its gather list (local gather indices) and its logits' base in zg
+            const int32_t* row_glist = nullptr;
+            const int32_t* gather_tok = nullptr;
+            float* zgb = zg;
             if (valid) {   // first gather of this row whose token is >= v0 (tokens sorted per row)
-                int lo = row_gptr[m], hi = row_gptr[m + 1];
+                const int b = row_pass(rm, m), ml = m - rm.m0[b];
+                row_glist = rm.row_glist[b];
+                gather_tok = rm.gather_tok[b];
+                zgb = zg + rm.g0[b];
+                int lo = rm.row_gptr[b][ml], hi = rm.row_gptr[b][ml + 1];
                 ge = hi;
                 while (lo < hi) {
                     const int mid = (lo + hi) >> 1;
@@ -386,7 +445,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                     float val = z[0];
 #pragma unroll
                     for (int i = 1; i < 32; ++i) val = (i == idx) ? z[i] : val;
-                    zg[g] = val;
+                    zgb[g] = val;
                     ++gc;
                 }
             }
@@ -422,13 +481,14 @@ __device__ __forceinline__ float2 lse_merge(float2 a, float2 b) {
 
 __global__ void __launch_bounds__(128) score_combine_kernel(const float2* __restrict__ part,
                                                             const float* __restrict__ zg,
-                                                            const int32_t* __restrict__ row_gptr,
-                                                            const int32_t* __restrict__ row_glist, int M, int n_vt,
-                                                            float* __restrict__ row_lse,
-                                                            float* __restrict__ token_lp) {
+                                                            const __grid_constant__ RowMap rm, int M, int n_vt) {
     const int m = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (m >= M) return;
+    const int b = row_pass(rm, m), ml = m - rm.m0[b];
+    const int32_t* row_glist = rm.row_glist[b];
+    const float* zgb = zg + rm.g0[b];
+    float* token_lp = rm.token_lp[b];
     float2 acc = make_float2(-INFINITY, 0.f);
     for (int vt = lane; vt < n_vt; vt += 32) acc = lse_merge(acc, part[(size_t)m * n_vt + vt]);
 #pragma unroll
@@ -439,10 +499,10 @@ __global__ void __launch_bounds__(128) score_combine_kernel(const float2* __rest
         acc = (lane & o) ? lse_merge(other, acc) : lse_merge(acc, other);
     }
     const float lse = acc.x + logf(acc.y);
-    if (lane == 0) row_lse[m] = lse;
-    for (int i = row_gptr[m] + lane; i < row_gptr[m + 1]; i += 32) {
+    if (lane == 0) rm.row_lse[b][ml] = lse;
+    for (int i = rm.row_gptr[b][ml] + lane; i < rm.row_gptr[b][ml + 1]; i += 32) {
         const int g = row_glist[i];
-        token_lp[g] = zg[g] - lse;
+        token_lp[g] = zgb[g] - lse;
     }
 }
 
@@ -523,16 +583,17 @@ __global__ void __launch_bounds__(kMergeThreads) extract_combine_kernel(const ui
     }
 }
 
+// The scoring kernels on the rows of `rm` (KX > 0: one pass, `P`'s searched slots).
 template <bool FP8, int KX>
-spinf_status launch_score(const Pass& P, const ScoreLayout& L, const void* hidden, const void* w, const float* w_scale,
-                          int D, int V, float* row_lse, float* token_lp, const spinf_extract_out* ex, uint8_t* ws,
-                          int* err, cudaStream_t stream) {
+spinf_status launch_score_rows(const Pass* P, const RowMap& rm, const ScoreLayout& L, const void* w,
+                               const float* w_scale, int D, int V, const spinf_extract_out* ex, uint8_t* ws, int* err,
+                               cudaStream_t stream) {
+    static_assert(sizeof(RowMap) <= 2200, "the row map travels in the kernels' parameters");
     void* hs = ws + L.hs;
     float* sa = reinterpret_cast<float*>(ws + L.sa);
     float2* part = reinterpret_cast<float2*>(ws + L.part);
     float* zg = reinterpret_cast<float*>(ws + L.zg);
-    gather_rows_kernel<FP8><<<L.M_pad, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(hidden), P.dev.slot_row,
-                                                         L.M, D, hs, sa);
+    gather_rows_kernel<FP8><<<L.M_pad, 256, 0, stream>>>(rm, L.M, D, hs, sa);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "gather launch");
 
@@ -554,24 +615,31 @@ spinf_status launch_score(const Pass& P, const ScoreLayout& L, const void* hidde
     const int n_kb = (D + kbk - 1) / kbk;
     const int total = L.n_vt * L.n_st;
     const int grid = std::min(total, sm_count());
-    ExtractArgs xa{P.dev.row_x, P.dev.x_set, KX ? ex->token_sets : nullptr, KX ? ex->n_sets : 0, (V + 31) / 32, L.k,
-                   reinterpret_cast<uint2*>(ws + L.xpart)};
+    ExtractArgs xa{KX ? P->dev.row_x : nullptr, KX ? P->dev.x_set : nullptr, KX ? ex->token_sets : nullptr,
+                   KX ? ex->n_sets : 0, (V + 31) / 32, L.k, reinterpret_cast<uint2*>(ws + L.xpart)};
     score_main_kernel<FP8, KX><<<grid, kScoreThreads, KX ? kScoreSmemX : kScoreSmem, stream>>>(
-        th, tw, sa, w_scale, part, zg, P.dev.row_gptr, P.dev.row_glist, P.dev.gather_tok, L.M, V, n_kb, L.n_st,
-        L.n_vt, xa, err);
+        th, tw, sa, w_scale, part, zg, rm, L.M, V, n_kb, L.n_st, L.n_vt, xa, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "score launch");
-    score_combine_kernel<<<(L.M + 3) / 4, 128, 0, stream>>>(part, zg, P.dev.row_gptr, P.dev.row_glist, L.M, L.n_vt,
-                                                           row_lse, token_lp);
+    score_combine_kernel<<<(L.M + 3) / 4, 128, 0, stream>>>(part, zg, rm, L.M, L.n_vt);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
     if constexpr (KX > 0) {
-        extract_combine_kernel<KX><<<L.X, kMergeThreads, 0, stream>>>(xa.xpart, P.dev.x_m, L.n_vt, L.k, row_lse, ex->top_tok,
-                                                       ex->top_lp);
+        extract_combine_kernel<KX><<<L.X, kMergeThreads, 0, stream>>>(xa.xpart, P->dev.x_m, L.n_vt, L.k, rm.row_lse[0],
+                                                                      ex->top_tok, ex->top_lp);
         e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "extract launch");
     }
     return SPINF_OK;
+}
+
+// The scoring kernels on one pass's rows.
+template <bool FP8, int KX>
+spinf_status launch_score(const Pass& P, const ScoreLayout& L, const void* hidden, const void* w, const float* w_scale,
+                          int D, int V, float* row_lse, float* token_lp, const spinf_extract_out* ex, uint8_t* ws,
+                          int* err, cudaStream_t stream) {
+    return launch_score_rows<FP8, KX>(&P, one_pass_map(P, hidden, row_lse, token_lp), L, w, w_scale, D, V, ex, ws, err,
+                                      stream);
 }
 
 }  // namespace
@@ -639,6 +707,90 @@ extern "C" spinf_status spinf_score(const spinf_plan* plan, int32_t pass, const 
                                     spinf_stream stream) {
     return spinf_score_extract(plan, pass, hidden, w, w_scale, w_dtype, d_model, vocab, row_lse, token_lp, nullptr,
                                workspace, workspace_bytes, stream);
+}
+
+// ---------------------------------------------------------------- several passes in one sweep
+namespace spinf {
+namespace {
+
+// Checks the pass list and counts its rows: M, G in total, and the row map without pointers.
+spinf_status passes_map(const spinf_plan* plan, int32_t n, const int32_t* passes, RowMap& rm, int& M, int& G) {
+    if (!plan || !passes || n <= 0) return fail(SPINF_E_INVALID, "NULL plan or pass list, or no pass");
+    if (n > kMaxScorePasses) return fail(SPINF_E_LIMIT, "more than SPINF_SCORE_MAX_PASSES passes in one call");
+    rm = RowMap{};
+    rm.nb = n;
+    M = G = 0;
+    for (int32_t b = 0; b < n; ++b) {
+        if (passes[b] < 0 || passes[b] >= (int32_t)plan->passes.size()) return fail(SPINF_E_INVALID, "bad pass index");
+        for (int32_t c = 0; c < b; ++c)
+            if (passes[c] == passes[b]) return fail(SPINF_E_INVALID, "a pass listed twice");
+        const Pass& P = plan->passes[passes[b]];
+        rm.m0[b] = M;
+        rm.g0[b] = G;
+        M += (int)P.slot_row.size();
+        G += (int)P.gather_tok.size();
+    }
+    rm.m0[n] = M;
+    rm.g0[n] = G;
+    return SPINF_OK;
+}
+
+}  // namespace
+}  // namespace spinf
+
+extern "C" size_t spinf_score_passes_workspace_bytes(const spinf_plan* plan, int32_t n_passes, const int32_t* passes,
+                                                     int32_t vocab, int32_t d_model, int32_t w_dtype) {
+    RowMap rm;
+    int M = 0, G = 0;
+    if (vocab <= 0 || d_model <= 0 || passes_map(plan, n_passes, passes, rm, M, G) != SPINF_OK) return 0;
+    return score_layout_counts(M, G, 0, vocab, d_model, w_dtype, plan->extract_k).total;
+}
+
+extern "C" spinf_status spinf_score_passes(const spinf_plan* plan, int32_t n_passes, const int32_t* passes,
+                                           const void* const* hidden, const void* w, const float* w_scale,
+                                           int32_t w_dtype, int32_t d_model, int32_t vocab, float* const* row_lse,
+                                           float* const* token_lp, void* workspace, size_t workspace_bytes,
+                                           spinf_stream stream) {
+    RowMap rm;
+    int M = 0, G = 0;
+    spinf_status st = passes_map(plan, n_passes, passes, rm, M, G);
+    if (st) return st;
+    if (!hidden || !row_lse || !token_lp) return fail(SPINF_E_INVALID, "NULL pointer array");
+    for (int32_t b = 0; b < n_passes; ++b)
+        if ((st = ensure_device_ready(plan, passes[b]))) return st;
+    if (w_dtype != SPINF_DTYPE_BF16 && w_dtype != SPINF_DTYPE_E4M3) return fail(SPINF_E_UNSUPPORTED, "w_dtype");
+    if (d_model <= 0 || d_model % 16) return fail(SPINF_E_UNSUPPORTED, "d_model must be a positive multiple of 16");
+    if (vocab <= 0) return fail(SPINF_E_INVALID, "vocab must be positive");
+    if (M == 0) return SPINF_OK;
+    if (!w || !workspace) return fail(SPINF_E_INVALID, "NULL buffer");
+    if (w_dtype == SPINF_DTYPE_E4M3 && !w_scale) return fail(SPINF_E_INVALID, "e4m3 weights need w_scale");
+    if (w_dtype == SPINF_DTYPE_E4M3 && (reinterpret_cast<uintptr_t>(w_scale) & 15))
+        return fail(SPINF_E_INVALID, "w_scale must be 16-byte aligned");
+    for (const void* p : {w, (const void*)workspace})
+        if (reinterpret_cast<uintptr_t>(p) & 15) return fail(SPINF_E_INVALID, "buffer not 16-byte aligned");
+    for (int32_t b = 0; b < n_passes; ++b) {
+        const Pass& P = plan->passes[passes[b]];
+        if (P.slot_row.empty()) continue;
+        if (!hidden[b] || !row_lse[b] || (!P.gather_tok.empty() && !token_lp[b]))
+            return fail(SPINF_E_INVALID, "NULL buffer of pass " + std::to_string(passes[b]));
+        if (reinterpret_cast<uintptr_t>(hidden[b]) & 15) return fail(SPINF_E_INVALID, "hidden not 16-byte aligned");
+        for (int32_t t : P.gather_tok)
+            if (t < 0 || t >= vocab) return fail(SPINF_E_INVALID, "option token outside the vocabulary");
+        rm.hidden[b] = static_cast<const __nv_bfloat16*>(hidden[b]);
+        rm.slot_row[b] = P.dev.slot_row;
+        rm.row_gptr[b] = P.dev.row_gptr;
+        rm.row_glist[b] = P.dev.row_glist;
+        rm.gather_tok[b] = P.dev.gather_tok;
+        rm.row_lse[b] = row_lse[b];
+        rm.token_lp[b] = token_lp[b];
+    }
+    const ScoreLayout L = score_layout_counts(M, G, 0, vocab, d_model, w_dtype, plan->extract_k);
+    if (workspace_bytes < L.total) return fail(SPINF_E_NOMEM, "workspace too small");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (w_dtype == SPINF_DTYPE_E4M3)
+        return launch_score_rows<true, 0>(nullptr, rm, L, w, w_scale, d_model, vocab, nullptr, ws, plan->d_err, s);
+    return launch_score_rows<false, 0>(nullptr, rm, L, w, nullptr, d_model, vocab, nullptr, ws, plan->d_err, s);
 }
 
 // ---------------------------------------------------------------- rows outside a plan
@@ -748,20 +900,42 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
+// per device: the context the address was looked up in, and the address
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 void* g_scratch_addr[kMaxDevices] = {};
 
-// Device address of this GPU's scratch array; the first call per device looks it up.
+// The calling thread's current driver context (nullptr if the entry point is missing).
+CUcontext current_context() {
+    using CtxGetCurrent = CUresult (*)(CUcontext*);
+    static CtxGetCurrent fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<CtxGetCurrent>(p);
+        return static_cast<CtxGetCurrent>(nullptr);
+    }();
+    CUcontext c = nullptr;
+    if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+    return c;
+}
+
+// Device address of this GPU's scratch array.  The first call per device looks it up,
+// and so does the first call after the device's context changed (a cudaDeviceReset
+// makes a new primary context, in which the array has a new address).
 spinf_status static_scratch(void** out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return fail(SPINF_E_UNSUPPORTED, "device index beyond the static scratch table");
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
+    // the runtime makes the device's primary context current before the symbol lookup
+    void* p = nullptr;
+    if (!g_scratch_addr[dev] || g_scratch_ctx[dev] != current_context()) {
         e = cudaGetSymbolAddress(&p, g_score_scratch);
         if (e != cudaSuccess || !p) return cuda_fail(e, "cudaGetSymbolAddress(scoring scratch)");
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = current_context();
     }
     *out = g_scratch_addr[dev];
     return SPINF_OK;

@@ -322,6 +322,37 @@ spinf_status spinf_score(const spinf_plan* plan, int32_t pass,
                          float* row_lse, float* token_lp,
                          void* workspace, size_t workspace_bytes, spinf_stream stream);
 
+/* At most this many passes in one spinf_score_passes call. */
+#define SPINF_SCORE_MAX_PASSES 32
+
+/* Bytes of device workspace spinf_score_passes needs for these passes (0 for an
+ * invalid list). */
+size_t spinf_score_passes_workspace_bytes(const spinf_plan* plan, int32_t n_passes, const int32_t* passes,
+                                          int32_t vocab, int32_t d_model, int32_t w_dtype);
+
+/* spinf_score over several passes of one plan in one sweep of the lm head
+ * ("spinf-serve 0.1.1", "What it does"; man page, --lm-head f32out).  The
+ * scoring rows of the listed passes are scored as one list of rows: every
+ * lm-head tile is read once for all of them, and only the last 128-row tile of
+ * the list is padded (one call per pass pads every pass's last tile and reads
+ * the whole head once per pass).  Each row's results are bit-identical to
+ * those of spinf_score on its own pass: a row's logits, log-sum-exp and token
+ * log-probabilities are computed by the same tile code in the same fixed order
+ * whatever other rows share the call.
+ *
+ * passes: host [n_passes] distinct pass indices, each uploaded;
+ * hidden, row_lse, token_lp: host arrays of n_passes device pointers, entry b
+ * for pass passes[b], with spinf_score's layouts ([T_pad, d_model] bf16, [M]
+ * and [G] fp32); w, w_scale, w_dtype, d_model, vocab as for spinf_score;
+ * workspace: device, >= spinf_score_passes_workspace_bytes.  Searched slots of
+ * these passes get their row_lse but no answers (spinf_score_extract gives
+ * those).  1 <= n_passes <= SPINF_SCORE_MAX_PASSES, else SPINF_E_INVALID /
+ * SPINF_E_LIMIT; other errors as spinf_score. */
+spinf_status spinf_score_passes(const spinf_plan* plan, int32_t n_passes, const int32_t* passes,
+                                const void* const* hidden, const void* w, const float* w_scale, int32_t w_dtype,
+                                int32_t d_model, int32_t vocab, float* const* row_lse, float* const* token_lp,
+                                void* workspace, size_t workspace_bytes, spinf_stream stream);
+
 /* Device buffers of the searched-slot answers of one pass. */
 typedef struct {
     const uint32_t* token_sets;  /* device [n_sets][ceil(vocab / 32)]: bit (v % 32) of word v / 32 set
@@ -416,7 +447,9 @@ spinf_status spinf_score_rows(const spinf_plan* plan, const void* hidden, int32_
  *
  * The first call on a device looks up the device address of its scratch array
  * (cudaGetSymbolAddress, with that device current); make that first call before
- * any stream capture.  Every call on a device shares the one array and leaves
+ * any stream capture.  The address is kept per device together with the driver
+ * context it belongs to: after a cudaDeviceReset (a new context) the next call
+ * looks it up again, so that call too should come before any stream capture.  Every call on a device shares the one array and leaves
  * its contents behind; nothing in it has to start at zero (each call writes
  * every byte it later reads).  Calls whose kernels overlap on the GPU -- two
  * streams, or two host threads -- race on the array: order them. */

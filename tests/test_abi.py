@@ -172,3 +172,21 @@ def test_c_caller(spinf, tmp_path):
     assert [int(x) for x in v[:5]] == [1, 2, 1, 42, 17]
     assert [float(x) for x in v[5:7]] == [-0.5, -1.5] and v[7] == "1"
     assert all(abs(float(x) - 0.375) < 1e-6 for x in v[8:10])
+
+
+def test_score_passes_rejects_bad_lists(spinf):
+    """spinf_score_passes checks its pass list before touching the device: a pass listed twice
+    or out of range is INVALID, more than SPINF_SCORE_MAX_PASSES passes is LIMIT; the workspace
+    query returns 0 for such lists."""
+    from synth import workloads as wl
+    plan = spinf.Plan(wl.stress(n_questions=40, content_tokens=100, vocab=1000), vocab=1000, token_budget=512)
+    n = plan.num_passes
+    assert n >= 3
+    for passes, status in (([0, 0], "INVALID"), ([n], "INVALID"), ([-1], "INVALID"), (list(range(n)) * 12, "LIMIT")):
+        assert spinf.score_passes_workspace_bytes(plan, passes, 1000, 512) == 0
+        k = len(passes)
+        with pytest.raises(spinf.SpinfError) as e:
+            spinf.score_passes(plan, passes, [0] * k, 0, None, spinf.DTYPE_BF16, 512, 1000, [0] * k, [0] * k, 0, 0,
+                               stream=0)
+        assert e.value.status_name == status, passes
+    assert spinf.score_passes_workspace_bytes(plan, [0, 1], 1000, 512) > 0
