@@ -36,10 +36,13 @@ sys.path.insert(0, ROOT)
 
 METRIC = "packed tokens/s and scored questions/s per GB300; % of tensor/HBM roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (read + write) of one score_main_kernel launch, from one ncu capture of the
-# Wikinews-shaped pass 0 with the bf16 lm head (2.020 GB read = the head once, 9.1 MB written).
-# Keyed by (workload, fp8); any other case reports null.
-NCU_SCORE_TRAFFIC = {("wikinews", False): 2020407040 + 9282560}
+# DRAM bytes (read + write) of one score_main_kernel launch of the step (every pass's slot
+# rows in one sweep), from one ncu capture of the current kernel.  Keyed by (workload, fp8);
+# any other case reports null.
+NCU_SCORE_TRAFFIC = {}
+# DRAM bytes (read + write) per step of the attention kernel (both passes of the job), from
+# ncu captures of the current kernel; any other workload reports null.
+NCU_ATTN_TRAFFIC = {}
 
 
 def _peaks():
@@ -51,6 +54,15 @@ def _peaks():
         except Exception:
             pass
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _burst_peaks():
+    """(bf16 TFLOP/s, HBM GB/s, label): the burst bf16 GEMM figure, since every kernel here is
+    timed inside steps of a few milliseconds (a sub-second region), not a seconds-long loop."""
+    peaks, src = _peaks()
+    bf16 = _peak_value(peaks, "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"]
+    hbm = _peak_value(peaks, "hbm_gbs") or FALLBACK_PEAKS["hbm_gbs"]
+    return bf16, hbm, f"{src} bf16_tflops (burst; x2 for e4m3) and hbm_gbs"
 
 
 def _peak_value(d, *names):
@@ -193,6 +205,9 @@ def run_ours(args, rank, world):
             p["lse"] = torch.empty(max(info.M, 1), device=dev)
             p["tlp"] = torch.empty(max(info.G, 1), device=dev)
             p["tlp_host"] = torch.empty(max(info.G, 1), dtype=torch.float32, pin_memory=True)
+    all_passes = list(range(len(passes)))
+    ws_all = torch.empty(spinf.score_passes_workspace_bytes(plan, all_passes, shape.vocab, shape.d_model, w_dtype),
+                         dtype=torch.uint8, device=dev)
     stream.synchronize()
     tokens, questions, pairs, flops_attn, bytes_attn, flops_score = work_counts(inputs, plan, passes, shape)
     sched_tiles = sum(int(p["info"].n_sched) for p in passes)
@@ -203,21 +218,26 @@ def run_ours(args, rank, world):
     ev = {"attn": [], "score": []}
 
     def step(record=False):
+        # the attention of every pass, then one scoring sweep over all passes' slot rows
         for pi, p in enumerate(passes):
             q, k, v, h = p["dev"]
             if record:
-                a0, a1, s1 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                a0, a1 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
                 a0.record(stream)
             spinf.branch_attention(plan, pi, q, k, v, p["o"], shape.n_q_heads, shape.n_kv_heads, shape.d_head,
                                    stream=stream)
             if record:
                 a1.record(stream)
-            spinf.score(plan, pi, h, w, w_scale, w_dtype, shape.d_model, shape.vocab, p["lse"], p["tlp"], p["ws"],
-                        stream=stream)
-            if record:
-                s1.record(stream)
                 ev["attn"].append((a0, a1))
-                ev["score"].append((a1, s1))
+        if record:
+            s0, s1 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+            s0.record(stream)
+        spinf.score_passes(plan, all_passes, [p["dev"][3] for p in passes], w, w_scale, w_dtype, shape.d_model,
+                           shape.vocab, [p["lse"] for p in passes], [p["tlp"] for p in passes], ws_all, stream=stream)
+        if record:
+            s1.record(stream)
+            ev["score"].append((s0, s1))
+        for p in passes:
             p["tlp_host"].copy_(p["tlp"], non_blocking=True)
         stream.synchronize()
         return plan.collect([p["tlp_host"][:p["info"].G].numpy() for p in passes])
@@ -243,15 +263,30 @@ def run_ours(args, rank, world):
     assert np.isfinite(res["option_lp"]).all()
     ms = max_over_ranks(ms, world, dev)
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["attn"]) * len(passes)
-    score_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["score"]) * len(passes)
+    score_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["score"])
 
-    def per_step_stats(pairs):
-        """median and min over steps of the per-step sum over passes (ms)."""
+    def per_step_stats(pairs, per_step):
+        """median and min over steps of the per-step sum of ``per_step`` intervals (ms)."""
         t = [a.elapsed_time(b) for a, b in pairs]
-        steps = [sum(t[i:i + len(passes)]) for i in range(0, len(t), len(passes))]
+        steps = [sum(t[i:i + per_step]) for i in range(0, len(t), per_step)]
         return {"median": statistics.median(steps), "min": min(steps)}
 
-    attn_stats, score_stats = per_step_stats(ev["attn"]), per_step_stats(ev["score"])
+    attn_stats, score_stats = per_step_stats(ev["attn"], len(passes)), per_step_stats(ev["score"], 1)
+    # for comparison: the same scoring as one spinf_score call per pass (each pads its own last
+    # 128-row tile and reads the whole lm head)
+    pev = []
+    with torch.cuda.stream(stream):
+        for r in range(max(3, args.steps // 2) + 1):
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for pi, p in enumerate(passes):
+                spinf.score(plan, pi, p["dev"][3], w, w_scale, w_dtype, shape.d_model, shape.vocab, p["lse"],
+                            p["tlp"], p["ws"], stream=stream)
+            a1.record(stream)
+            if r:
+                pev.append((a0, a1))
+    torch.cuda.synchronize()
+    score_per_pass_ms = statistics.median(a.elapsed_time(b) for a, b in pev)
     # the attention call again right after itself on the same pass (its q/k/v partly in L2): the
     # step's figure is the cold one (every pass's inputs exceed L2 and the lm head flushes it)
     warm = []
@@ -288,15 +323,14 @@ def run_ours(args, rank, world):
         attn_win_ms = statistics.mean(a.elapsed_time(b) for a, b in wev) * len(passes)
 
     layer = None if args.no_layer else layer_timing(args, spinf, shape, plan, passes, dev, stream)
+    per_workload = None if args.no_per_workload else per_workload_timing(args, spinf, wl, dev, stream)
     extract = None if args.no_extract else extract_timing(args, spinf, sv, wl, inputs, shape, w, w_scale, w_dtype,
                                                           dev, stream)
 
     # end to end through the public API with host buffers
     e2e = run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev) if not args.no_e2e else None
 
-    peaks, peak_src = _peaks()
-    bf16_peak = _peak_value(peaks, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"]
-    hbm_peak = _peak_value(peaks, "hbm_gbs") or FALLBACK_PEAKS["hbm_gbs"]
+    bf16_peak, hbm_peak, peak_label = _burst_peaks()
     mma_peak = bf16_peak * (2.0 if args.fp8 else 1.0)
     score_tflops = flops_score / (score_ms * 1e-3) / 1e12
     attn_tflops = flops_attn / (attn_ms * 1e-3) / 1e12
@@ -315,26 +349,24 @@ def run_ours(args, rank, world):
         "dtype": "bf16" if not args.fp8 else "e4m3",
         "data": "synthetic",
         "scored_questions_per_s": world * questions / (ms * 1e-3),
-        "config": {"workload": f"{args.workload}: {len(inputs)} contents, {questions} questions, "
-                               f"{len(passes)} passes of <=16384 tokens ({tokens} tokens)",
-                   "attention": f"Hq={shape.n_q_heads} Hkv={shape.n_kv_heads} d_head={shape.d_head} (1 layer)",
-                   "lm_head": f"d_model={shape.d_model} vocab={shape.vocab} "
-                              f"{'e4m3 per-row scaled' if args.fp8 else 'bf16'}, fp32 logits",
-                   "l2": "inputs larger than L2 (per pass q/k/v/o ~0.4 GB, lm head 2 GB)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                   "value_covers": "attention + scoring per pass, token-lp D2H, collect; layout resident"},
-        "roofline": {"kernel": "spinf_score (gather + tcgen05 lm head + lse + combine)", "bound": "tensor",
+        "config": {**_config(args, inputs, len(passes), tokens, questions, shape, world),
+                   "value_covers": "attention per pass + one scoring sweep over every pass's slot rows, token-lp "
+                                   "D2H, collect; layout resident"},
+        "roofline": {"kernel": "spinf_score_passes (gather + tcgen05 lm head + lse + combine, all passes)",
+                     "bound": "tensor",
                      "achieved": score_tflops, "peak": mma_peak, "unit": "TFLOP/s",
                      "frac": score_tflops / mma_peak,
                      "traffic": NCU_SCORE_TRAFFIC.get((args.workload, bool(args.fp8))),
-                     "peak_source": f"{peak_src} {'bf16_tflops_sustained' if peak_src == 'measured' else ''}".strip()},
+                     "peak_source": peak_label},
         "roofline_attention": {"kernel": "spinf_branch_attention", "tensor_tflops_unmasked": attn_tflops,
                                "tensor_frac": attn_tflops / bf16_peak, "hbm_gbs": attn_gbs,
                                "hbm_frac": attn_gbs / hbm_peak, "unmasked_pairs": pairs,
                                "tile_occupancy": pairs / (exec_tiles * 128 * key_tile),
                                "key_tile": key_tile, "executed_kv_tiles": exec_tiles,
                                "tile_occupancy_128x128": pairs / (sched_tiles * 128 * 128),
-                               "peak_source": f"{peak_src} {'bf16_tflops_sustained' if peak_src == 'measured' else ''}".strip()},
+                               "traffic": NCU_ATTN_TRAFFIC.get(args.workload),
+                               "compulsory_bytes": bytes_attn,
+                               "peak_source": peak_label},
         # per kernel: packed tokens per attention-kernel second
         # (one layer call per pass) and user questions per scoring second (gather + main + combine)
         "per_kernel": {"attention_packed_tokens_per_s": world * tokens / (attn_ms * 1e-3),
@@ -343,12 +375,14 @@ def run_ours(args, rank, world):
         "kernel_ms_per_step": {"attention": attn_ms, "score": score_ms,
                                "attention_median": attn_stats["median"], "attention_min": attn_stats["min"],
                                "score_median": score_stats["median"], "score_min": score_stats["min"],
+                               "score_one_call_per_pass": score_per_pass_ms,
                                "attention_l2_warm": attn_warm_ms,
                                **({"attention_windowed": attn_win_ms, "window": shape.window} if attn_win_ms else {})},
         "searched_slots": extract,
         "layer_projections": layer,
+        "per_workload": per_workload,
         "clocks": clk,
-        "gpu_launches": 4 * len(passes) * args.steps,
+        "gpu_launches": (len(passes) + 3) * args.steps,   # attention per pass; gather, lm head, combine
         "e2e": e2e,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -429,12 +463,139 @@ def layer_timing(args, spinf, shape, plan, passes, dev, stream):
     plan.device_status(stream)
     rows = sum(p["info"].T_pad for p in passes)
     fl_qkv, fl_o = 2.0 * rows * D * n_qkv, 2.0 * rows * n_o * D
-    peaks, _ = _peaks()
-    bf16_peak = _peak_value(peaks, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"]
+    bf16_peak = _burst_peaks()[0]
     tf = {k: (fl_qkv if k.startswith("qkv") else fl_o) / (v * 1e-3) / 1e12 for k, v in ms.items() if k != "quantize_x"}
     return {"shapes": f"rows {rows} (all passes), QKV {D}->{n_qkv}, O {n_o}->{D}",
             "ms": ms, "tflops": tf,
             "frac": {k: v / (bf16_peak * (2.0 if k.endswith("e4m3") else 1.0)) for k, v in tf.items()}}
+
+
+def pass_pairs(info, window=0):
+    """Unmasked (row, key) pairs of one pass: key k is seen by the rows [k, end[k]) whose depth
+    is within the window (pos[q] - pos[k] < window; 0: no window)."""
+    import numpy as np
+
+    T = info.T
+    end = info.end[:T].astype(np.int64)
+    if window <= 0:
+        return int((end - np.arange(T)).sum())
+    pos = info.pos[:T].astype(np.int64)
+    return int(sum(int((pos[k:end[k]] - pos[k] < window).sum()) for k in range(T)))
+
+
+def per_workload_timing(args, spinf, wl, dev, stream, reps=3):
+    """The other workloads of the scope table, timed outside the headline step: the
+    moderation-shaped job (plus its 1024-token windowed layer), the many-questions stress job
+    at Qwen-class shapes (plus a window that bites), and one packing of the batch-invariance
+    pass (2000 short inputs + the 470-token target) with the e4m3 per-row-scaled lm head.
+    Values are seeded N(0, 1) bf16 drawn on the device (the path-keyed values change no
+    amount of work); one attention call per pass and one scoring sweep over every pass's
+    slot rows, ``reps`` times."""
+    import torch
+
+    bf16_peak, hbm_peak, _ = _burst_peaks()
+    cases = [("moderation", False), ("stress", False), ("invariance_e4m3", True)]
+    out = {}
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    for name, fp8 in cases:
+        if name == "invariance_e4m3":
+            inputs, _ = wl.invariance_packing(1)
+            shape = wl.GEMMA
+        else:
+            f, shape = wl.WORKLOADS[name]
+            inputs = f()
+        plan = spinf.Plan(inputs, vocab=shape.vocab)
+        w_dtype = spinf.DTYPE_E4M3 if fp8 else spinf.DTYPE_BF16
+        w = (torch.randn(shape.vocab, shape.d_model, generator=g, device=dev) / shape.d_model ** 0.5).to(torch.bfloat16)
+        w_scale = None
+        if fp8:
+            w, w_scale = _e4m3_rows_dev(w)
+        bufs = []
+        Hq, Hkv, d = shape.n_q_heads, shape.n_kv_heads, shape.d_head
+        for pi in range(plan.num_passes):
+            info = plan.pass_info(pi)
+            Tp = info.T_pad
+            mk = lambda *sz: torch.randn(*sz, generator=g, device=dev).to(torch.bfloat16)  # noqa: E731
+            b = {"info": info, "q": mk(Tp, Hq, d), "k": mk(Tp, Hkv, d), "v": mk(Tp, Hkv, d), "h": mk(Tp, shape.d_model),
+                 "lse": torch.empty(max(info.M, 1), device=dev), "tlp": torch.empty(max(info.G, 1), device=dev)}
+            b["o"] = torch.empty_like(b["q"])
+            plan.upload(pi, stream)
+            bufs.append(b)
+        all_p = list(range(len(bufs)))
+        ws = torch.empty(spinf.score_passes_workspace_bytes(plan, all_p, shape.vocab, shape.d_model, w_dtype),
+                         dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+
+        def timed(fn, per_pass=True):
+            """mean ms of one call per pass (summed over the passes), or of one call for all"""
+            units = list(enumerate(bufs)) if per_pass else [(None, None)]
+            for pi, b in units:   # warm-up
+                fn(pi, b)
+            ev = []
+            for _ in range(reps):
+                for pi, b in units:
+                    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a0.record(stream)
+                    fn(pi, b)
+                    a1.record(stream)
+                    ev.append((a0, a1))
+            torch.cuda.synchronize()
+            return statistics.mean(a.elapsed_time(b) for a, b in ev) * len(units)
+
+        def attn(window):
+            return lambda pi, b: spinf.branch_attention(plan, pi, b["q"], b["k"], b["v"], b["o"], Hq, Hkv, d,
+                                                        window=window, stream=stream)
+
+        def score(_pi, _b):   # one sweep over every pass's slot rows
+            spinf.score_passes(plan, all_p, [b["h"] for b in bufs], w, w_scale, w_dtype, shape.d_model, shape.vocab,
+                               [b["lse"] for b in bufs], [b["tlp"] for b in bufs], ws, stream=stream)
+
+        with torch.cuda.stream(stream):
+            t_attn, t_score = timed(attn(0)), timed(score, per_pass=False)
+            t_win = timed(attn(shape.window)) if shape.window > 0 else None
+        plan.device_status(stream)
+        key_tile = 64 if d == 256 else 128
+        tokens = sum(b["info"].T for b in bufs)
+        rows = sum(b["info"].M for b in bufs)
+        questions = sum(len(x[1]) for x in inputs)
+        pairs = sum(pass_pairs(b["info"]) for b in bufs)
+        tiles = sum(len(plan.tile_schedule(pi, 0, key_tile)[1]) for pi in range(len(bufs)))
+        fl_attn = 4 * d * Hq * pairs
+        by_attn = tokens * (2 * Hq + 2 * Hkv) * d * 2
+        fl_score = 2 * rows * shape.vocab * shape.d_model
+        mma_peak = bf16_peak * (2.0 if fp8 else 1.0)
+        e = {"inputs": len(inputs), "user_questions": questions, "passes": len(bufs), "packed_tokens": tokens,
+             "scoring_rows": rows, "shape": f"Hq={Hq} Hkv={Hkv} d_head={d} d_model={shape.d_model} V={shape.vocab}",
+             "lm_head": "e4m3 per-row scaled" if fp8 else "bf16",
+             "ms": {"attention": t_attn, "score": t_score, "step": t_attn + t_score},
+             "packed_tokens_per_s": tokens / ((t_attn + t_score) * 1e-3),
+             "scored_questions_per_s": questions / (t_score * 1e-3),
+             "tile_occupancy": pairs / (tiles * 128 * key_tile), "key_tile": key_tile,
+             "roofline": {"attention_tensor_frac": fl_attn / (t_attn * 1e-3) / 1e12 / bf16_peak,
+                          "attention_hbm_frac": by_attn / (t_attn * 1e-3) / 1e9 / hbm_peak,
+                          "score_tensor_frac": fl_score / (t_score * 1e-3) / 1e12 / mma_peak,
+                          "score_peak_tflops": mma_peak}}
+        if t_win is not None:
+            pw = sum(pass_pairs(b["info"], shape.window) for b in bufs)
+            tw = sum(len(plan.tile_schedule(pi, shape.window, key_tile)[1]) for pi in range(len(bufs)))
+            e["windowed"] = {"window": shape.window, "attention_ms": t_win, "unmasked_pairs": pw,
+                             "tile_occupancy": pw / (tw * 128 * key_tile),
+                             "attention_tensor_frac": 4 * d * Hq * pw / (t_win * 1e-3) / 1e12 / bf16_peak}
+        out[name] = e
+        del bufs, w, w_scale, ws
+        torch.cuda.empty_cache()
+    return out
+
+
+def _e4m3_rows_dev(w):
+    """Per-row e4m3 codes and scales of a device lm head (absmax / 448, round to nearest even)."""
+    import torch
+
+    s_w = w.float().abs().amax(dim=1)
+    s_w = torch.where(s_w == 0, torch.ones_like(s_w), s_w / 448.0)
+    codes = (w.float() / s_w[:, None]).clamp_(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, s_w.contiguous()
 
 
 def extract_timing(args, spinf, sv, wl, inputs, shape, w, w_scale, w_dtype, dev, stream, n_slots=2):
@@ -556,7 +717,7 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
     sets = [[tuple(torch.empty_like(t, device=dev) for t in hp) for hp in host] for _ in range(2)]
     obufs = [torch.empty_like(db[0]) for db in sets[0]]
     h2d = sum(t.numel() * t.element_size() for hp in host for t in hp)
-    ws = [None] * len(passes)
+    ws = [None]
     tl_host = [[torch.empty(max(p["info"].G, 1), dtype=torch.float32, pin_memory=True) for p in passes]
                for _ in range(2)]
     tl_dev = [torch.empty(max(p["info"].G, 1), device=dev) for p in passes]
@@ -587,17 +748,20 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
         plan_ms.append((time.perf_counter() - t_plan) * 1e3)
         for pi in range(plan.num_passes):
             plan.upload(pi, stream, buffer=dsc[b][pi])
-        for pi in range(plan.num_passes):
-            if ws[pi] is None:
-                ws[pi] = torch.empty(spinf.score_workspace_bytes(plan, pi, shape.vocab, shape.d_model, w_dtype),
-                                     dtype=torch.uint8, device=dev)
+        all_p = list(range(plan.num_passes))
+        if ws[0] is None:
+            ws[0] = torch.empty(spinf.score_passes_workspace_bytes(plan, all_p, shape.vocab, shape.d_model, w_dtype),
+                                dtype=torch.uint8, device=dev)
+        for pi in all_p:
             stream.wait_event(ready[pi])
             q, k, v, h = sets[b][pi]
             spinf.branch_attention(plan, pi, q, k, v, obufs[pi], shape.n_q_heads, shape.n_kv_heads,
                                    shape.d_head, stream=stream)
-            spinf.score(plan, pi, h, w, w_scale, w_dtype, shape.d_model, shape.vocab, lse_dev[pi], tl_dev[pi],
-                        ws[pi], stream=stream)
-            with torch.cuda.stream(stream):
+        spinf.score_passes(plan, all_p, [sets[b][pi][3] for pi in all_p], w, w_scale, w_dtype, shape.d_model,
+                           shape.vocab, [lse_dev[pi] for pi in all_p], [tl_dev[pi] for pi in all_p], ws[0],
+                           stream=stream)
+        with torch.cuda.stream(stream):
+            for pi in all_p:
                 tl_host[b][pi].copy_(tl_dev[pi], non_blocking=True)
         done = torch.cuda.Event()
         done.record(stream)
@@ -631,55 +795,89 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
             "host_plan_ms_median": statistics.median(plan_ms[-n:]),
             "covers": "per request: H2D q/k/v/hidden (copy stream, overlapping the previous request's kernels) + "
                       "plan (marshalling of the request's token lists + C planner) + "
-                      "upload into kept descriptor memory + kernels + "
+                      "upload into kept descriptor memory + attention per pass + one scoring sweep + "
                       "D2H token lps + collect; two requests in flight"}
 
 
+# The oracle sample both CPU legs time (the repo arm's cpu_baseline and --impl reference),
+# so that the two agree: per step, the oracle planner on the whole job, the oracle attention
+# on ORACLE_ATTN_ROWS rows of pass 0 (all heads), and one oracle scoring call on
+# ORACLE_SCORE_ROWS whole slot rows of pass 0 (full vocabulary, every option token of them).
+ORACLE_ATTN_ROWS = 48
+ORACLE_SCORE_ROWS = 32
+
+
+class OracleSample:
+    """The fp64 oracle, as it stands, on a bounded sample of the job; each ``step()`` times one
+    sample and extrapolates it to the whole job: planner + attention per row x packed tokens +
+    one scoring call per ORACLE_SCORE_ROWS scoring rows of every pass (the oracle run over the
+    job in blocks of that many rows, which bounds its fp64 logits at 64 MB per block)."""
+
+    def __init__(self, inputs, shape, pass0_host, w, w_scale):
+        import numpy as np
+
+        from oracle import plan as op
+
+        self.inputs, self.shape = inputs, shape
+        self.P = op.plan(inputs, vocab=shape.vocab)
+        self.lay = self.P.passes[0]
+        q, k, v, h = pass0_host
+        self.q, self.k, self.v = (t.float().numpy() for t in (q, k, v))
+        self.h = h.float().numpy()[self.lay.slot_row]
+        self.wkw = ({"w": _BF16Rows(w.cpu())} if w_scale is None
+                    else {"w_codes": w.cpu().numpy(), "w_scale": w_scale.cpu().numpy()})
+        self.tokens = sum(p.T for p in self.P.passes)
+        self.blocks = sum(-(-len(p.slot_row) // ORACLE_SCORE_ROWS) for p in self.P.passes)
+        self.rows_total = sum(len(p.slot_row) for p in self.P.passes)
+        self.g = np.random.default_rng(0)
+
+    def step(self):
+        """(seconds this sample took, seconds the whole job is estimated to take)."""
+        import numpy as np
+
+        from oracle import attention as oa
+        from oracle import collect as oc
+        from oracle import plan as op
+        from oracle import score as osc
+
+        lay, sh = self.lay, self.shape
+        t_start = time.perf_counter()
+        op.plan(self.inputs, vocab=sh.vocab)
+        t_plan = time.perf_counter() - t_start
+        rows = self.g.choice(lay.T, size=min(lay.T, ORACLE_ATTN_ROWS), replace=False)
+        t0 = time.perf_counter()
+        oa.attention_rows(lay, self.q, self.k, self.v, sh.n_q_heads, sh.n_kv_heads, rows)
+        t_attn_row = (time.perf_counter() - t0) / len(rows)
+        n = min(ORACLE_SCORE_ROWS, len(lay.slot_row))
+        m0 = int(self.g.integers(0, len(lay.slot_row) - n + 1))
+        ms = np.arange(m0, m0 + n)
+        sel = np.isin(lay.gather_m, ms)
+        t0 = time.perf_counter()
+        _, lp = osc.score_rows(self.h[ms], lay.gather_m[sel] - m0, lay.gather_tok[sel], **self.wkw)
+        oc.option_stats(lp[:2])
+        t_block = time.perf_counter() - t0
+        sample_s = time.perf_counter() - t_start
+        job_s = t_plan + t_attn_row * self.tokens + t_block * self.blocks
+        return sample_s, job_s
+
+    def describe(self):
+        return (f"per sample: oracle planner on the whole job, oracle attention on {ORACLE_ATTN_ROWS} rows of "
+                f"pass 0 (all heads), one oracle scoring call on {ORACLE_SCORE_ROWS} whole slot rows of pass 0 "
+                f"(full vocabulary); extrapolated to {self.tokens} packed tokens and {self.rows_total} scoring "
+                f"rows ({self.blocks} calls of {ORACLE_SCORE_ROWS} rows)")
+
+
 def cpu_baseline(args, inputs, shape, plan, passes, w, w_scale, budget_s=20.0):
-    """The fp64 oracle on the host cores on a bounded sample, extrapolated to the whole job."""
-    import numpy as np
-
-    from oracle import attention as oa
-    from oracle import plan as op
-    from oracle import score as osc
-
+    """The fp64 oracle on the host cores: the same sample as --impl reference, repeated within a
+    time budget, its job estimate averaged."""
+    sample = OracleSample(inputs, shape, passes[0]["host"], w, w_scale)
     t0 = time.perf_counter()
-    P = op.plan(inputs, vocab=shape.vocab)
-    t_plan = time.perf_counter() - t0
-    lay = P.passes[0]
-    q, k, v, h = (t.float().numpy() for t in passes[0]["host"])
-    g = np.random.default_rng(0)
-    # attention: time a row sample
-    rows = g.choice(lay.T, size=min(lay.T, 96), replace=False)
-    t0 = time.perf_counter()
-    oa.attention_rows(lay, q, k, v, shape.n_q_heads, shape.n_kv_heads, rows)
-    t_attn_row = (time.perf_counter() - t0) / len(rows)
-    # scoring: two sample sizes give the per-row cost and the fixed cost of reading the lm head
-    hs = h[lay.slot_row]
-    gm, gt = lay.gather_m, lay.gather_tok
-    if w_scale is None:
-        wkw = {"w": _BF16Rows(w.cpu())}
-    else:
-        wkw = {"w_codes": w.cpu().numpy(), "w_scale": w_scale.cpu().numpy()}
-
-    def score_sample(n_rows):
-        sel = np.isin(gm, np.arange(n_rows))
-        t1 = time.perf_counter()
-        osc.score_rows(hs[:n_rows], gm[sel], gt[sel], **wkw)
-        return time.perf_counter() - t1
-
-    s1, s2 = 8, 24
-    ta = score_sample(s1)
-    tb = score_sample(s2)
-    per_row = max((tb - ta) / (s2 - s1), 1e-9)
-    fixed = max(ta - per_row * s1, 0.0)
-    total_rows = sum(p["info"].M for p in passes)
-    tokens = sum(p["info"].T for p in passes)
-    job_s = t_plan + t_attn_row * tokens + fixed * len(passes) + per_row * total_rows
-    return {"value": tokens / job_s, "unit": "packed tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"oracle planner on the whole job; attention on {len(rows)} rows of pass 0 (all heads); "
-                      f"scoring on {s1} and {s2} slot rows of pass 0 (full vocabulary); extrapolated to "
-                      f"{tokens} tokens and {total_rows} scoring rows",
+    est = []
+    while not est or (time.perf_counter() - t0 < budget_s and len(est) < 5):
+        est.append(sample.step()[1])
+    job_s = statistics.mean(est)
+    return {"value": sample.tokens / job_s, "unit": "packed tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": sample.describe() + f"; {len(est)} samples averaged",
             "job_seconds_estimate": job_s}
 
 
@@ -695,66 +893,55 @@ class _BF16Rows:
 
 
 def run_reference(args):
-    """--impl reference: the oracle, as it stands, on the host cores; one bounded sample per step."""
-    import torch  # noqa: F401  (bf16 rounding of the inputs)
-
-    import branch_packed_scoring_gb300 as spinf  # noqa: F401  (not used on this arm)
+    """--impl reference: the oracle, as it stands, on the host cores; one bounded sample of the
+    job per step (the same sample as the repo arm's cpu_baseline).  ``ms_per_step`` is the
+    measured time of one sample; ``value`` is the job's packed tokens over the job time the
+    samples extrapolate to."""
     from synth import values as sv
     from synth import workloads as wl
-    from oracle import attention as oa
-    from oracle import collect as oc
     from oracle import plan as op
-    from oracle import score as osc
-    import numpy as np
 
     f, shape = wl.WORKLOADS[args.workload]
     inputs = f()
-    P = op.plan(inputs, vocab=shape.vocab)
-    lay = P.passes[0]
+    lay = op.plan(inputs, vocab=shape.vocab).passes[0]
     keys = sv.path_keys(lay.tok, lay.parent, lay.T)
-    q, k, v = (t.float().numpy() for t in sv.qkv(keys, lay.T_pad, shape.n_q_heads, shape.n_kv_heads, shape.d_head))
-    h = sv.hidden(keys, lay.T_pad, shape.d_model, rows=lay.slot_row.tolist()).float().numpy()
-    w = _BF16Rows(sv.lm_head(shape.vocab, shape.d_model, device="cpu") if shape.vocab * shape.d_model < (1 << 28)
-                  else _cpu_lm_head(shape))
-    tokens = sum(p.T for p in P.passes)
-    rows_total = sum(len(p.slot_row) for p in P.passes)
-    g = np.random.default_rng(0)
-    n_attn, n_score = 24, 4
-
-    def sample_step():
-        t0 = time.perf_counter()
-        op.plan(inputs, vocab=shape.vocab)
-        t_plan = time.perf_counter() - t0
-        rows = g.choice(lay.T, size=n_attn, replace=False)
-        t0 = time.perf_counter()
-        oa.attention_rows(lay, q, k, v, shape.n_q_heads, shape.n_kv_heads, rows)
-        t_attn = (time.perf_counter() - t0) / n_attn
-        ms = g.choice(len(lay.slot_row), size=n_score, replace=False)
-        sel = np.isin(lay.gather_m, ms)
-        remap = {m: i for i, m in enumerate(ms)}
-        t0 = time.perf_counter()
-        _, lp = osc.score_rows(h[lay.slot_row[ms]], np.array([remap[m] for m in lay.gather_m[sel]]),
-                               lay.gather_tok[sel], w=w)
-        t_score = (time.perf_counter() - t0) / n_score
-        oc.option_stats(lp[:2])
-        return t_plan + t_attn * tokens + t_score * rows_total
-
+    q, k, v = sv.qkv(keys, lay.T_pad, shape.n_q_heads, shape.n_kv_heads, shape.d_head)
+    h = sv.hidden(keys, lay.T_pad, shape.d_model, rows=lay.slot_row.tolist())
+    w = sv.lm_head(shape.vocab, shape.d_model, device="cpu") if shape.vocab * shape.d_model < (1 << 28) \
+        else _cpu_lm_head(shape)
+    w_scale = None
+    if args.fp8:
+        w, w_scale = sv.e4m3_rows(w)
+    sample = OracleSample(inputs, shape, (q, k, v, h), w, w_scale)
     for _ in range(args.warmup):
-        sample_step()
-    est = [sample_step() for _ in range(args.steps)]
-    job_s = statistics.mean(est)
-    value = tokens / job_s
+        sample.step()
+    runs = [sample.step() for _ in range(args.steps)]
+    step_s = statistics.mean(r[0] for r in runs)
+    job_s = statistics.mean(r[1] for r in runs)
+    value = sample.tokens / job_s
+    questions = sum(len(x) for _, x in inputs)
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "packed tokens/s", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": job_s * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {len(inputs)} contents, {sum(len(x) for _, x in inputs)} "
-                               f"questions, {len(P.passes)} passes ({tokens} tokens)"},
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64" if not args.fp8 else "f64 (e4m3 codes)",
+        "data": "synthetic",
+        "config": _config(args, inputs, len(sample.P.passes), sample.tokens, questions, shape, 1),
+        "job_seconds_estimate": job_s,
         "cpu_baseline": {"kind": "oracle", "cores": os.cpu_count(), "value": value, "unit": "packed tokens/s",
-                         "sample": f"per step: planner on the whole job, attention on {n_attn} rows, scoring on "
-                                   f"{n_score} slot rows (full vocabulary), extrapolated to the whole job"},
+                         "sample": sample.describe() + "; one sample per step"},
         "e2e": {"value": value, "unit": "packed tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+
+
+def _config(args, inputs, n_passes, tokens, questions, shape, world):
+    """The ``config`` of both arms' JSON lines (the same words for the same workload)."""
+    return {"workload": f"{args.workload}: {len(inputs)} contents, {questions} questions, "
+                        f"{n_passes} passes of <=16384 tokens ({tokens} tokens)",
+            "attention": f"Hq={shape.n_q_heads} Hkv={shape.n_kv_heads} d_head={shape.d_head} (1 layer)",
+            "lm_head": f"d_model={shape.d_model} vocab={shape.vocab} "
+                       f"{'e4m3 per-row scaled' if args.fp8 else 'bf16'}, fp32 logits",
+            "l2": "inputs larger than L2 (per pass q/k/v/o ~0.4 GB, lm head 2 GB)",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
 
 
 def _cpu_lm_head(shape):
@@ -808,6 +995,25 @@ def run_ncu_case(args):
         def call():
             spinf.branch_attention(plan, 0, q, k, v, o, shape.n_q_heads, shape.n_kv_heads, shape.d_head,
                                    window=args.window)
+    elif args.ncu_case == "score_passes":   # the step's scoring launch: every pass's slot rows in one sweep
+        all_p = list(range(plan.num_passes))
+        hs, lses, tlps = [], [], []
+        for pi in all_p:
+            inf = plan.pass_info(pi)
+            kk = sv.path_keys(inf.tok, inf.parent, inf.T)
+            hs.append(sv.hidden(kk, inf.T_pad, shape.d_model, rows=inf.slot_row.tolist()).to(dev))
+            lses.append(torch.empty(max(inf.M, 1), device=dev))
+            tlps.append(torch.empty(max(inf.G, 1), device=dev))
+            plan.upload(pi)
+        w = sv.lm_head(shape.vocab, shape.d_model, device=dev)
+        w_scale = None
+        if args.fp8:
+            w, w_scale = sv.e4m3_rows(w)
+        ws = torch.empty(spinf.score_passes_workspace_bytes(plan, all_p, shape.vocab, shape.d_model, w_dtype),
+                         dtype=torch.uint8, device=dev)
+
+        def call():
+            spinf.score_passes(plan, all_p, hs, w, w_scale, w_dtype, shape.d_model, shape.vocab, lses, tlps, ws)
     else:
         h = sv.hidden(keys, info.T_pad, shape.d_model, rows=info.slot_row.tolist()).to(dev)
         w = sv.lm_head(shape.vocab, shape.d_model, device=dev)
@@ -841,8 +1047,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extract", action="store_true", help="skip the searched-slot scoring timing")
     ap.add_argument("--no-layer", action="store_true", help="skip the projection timing")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the moderation / stress / e4m3 invariance-pass timings")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
-    ap.add_argument("--ncu-case", choices=["score", "attention", "qkv"], default=None,
+    ap.add_argument("--ncu-case", choices=["score", "score_passes", "attention", "qkv"], default=None,
                     help="run one boundary call on pass 0 only (small case for profiler captures)")
     ap.add_argument("--window", type=int, default=0)
     args = ap.parse_args()

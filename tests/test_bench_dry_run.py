@@ -15,7 +15,7 @@ pytestmark = pytest.mark.slow
 
 def test_bench_line_without_a_gpu():
     r = subprocess.run([sys.executable, os.path.join(HERE, "bench_dry_run.py"), "--steps", "2", "--warmup", "1",
-                        "--no-cpu-baseline"], capture_output=True, text=True, timeout=900)
+                        "--no-cpu-baseline", "--no-per-workload"], capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stderr[-3000:]
     line = json.loads(r.stdout.strip().splitlines()[-1])
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
