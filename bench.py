@@ -39,10 +39,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one score_main_kernel launch of the step (every pass's slot
 # rows in one sweep), from one ncu capture of the current kernel.  Keyed by (workload, fp8);
 # any other case reports null.
-NCU_SCORE_TRAFFIC = {}
+NCU_SCORE_TRAFFIC = {("wikinews", False): 2024229376 + 14412032}
 # DRAM bytes (read + write) per step of the attention kernel (both passes of the job), from
 # ncu captures of the current kernel; any other workload reports null.
-NCU_ATTN_TRAFFIC = {}
+NCU_ATTN_TRAFFIC = {"wikinews": None}   # pass 0 only was captured: see per-pass figure below
+# DRAM bytes (read + write) of one attention launch on the Wikinews-shaped pass 0, from one ncu
+# capture of the current kernel (399.5 MB read, 106.4 MB written)
+NCU_ATTN_TRAFFIC_PASS0 = {"wikinews": 399459328 + 106367488}
 
 
 def _peaks():
@@ -365,6 +368,10 @@ def run_ours(args, rank, world):
                                "key_tile": key_tile, "executed_kv_tiles": exec_tiles,
                                "tile_occupancy_128x128": pairs / (sched_tiles * 128 * 128),
                                "traffic": NCU_ATTN_TRAFFIC.get(args.workload),
+                               "traffic_pass0": NCU_ATTN_TRAFFIC_PASS0.get(args.workload),
+                               "compulsory_bytes_pass0": passes[0]["info"].T_pad * (2 * shape.n_q_heads
+                                                                                     + 2 * shape.n_kv_heads)
+                               * shape.d_head * 2,
                                "compulsory_bytes": bytes_attn,
                                "peak_source": peak_label},
         # per kernel: packed tokens per attention-kernel second
@@ -711,7 +718,9 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
     """
     import torch
 
-    host = [tuple(t.pin_memory() for t in p["host"]) for p in passes]
+    # per pass: q, k, v and the hidden states of its scoring rows only (the lm head reads no other row)
+    host = [tuple(t.pin_memory() for t in (*p["host"][:3], p["host"][3][torch.as_tensor(p["info"].slot_row).long()]))
+            for p in passes]
     copy_stream = torch.cuda.Stream()
     stream = torch.cuda.Stream()
     sets = [[tuple(torch.empty_like(t, device=dev) for t in hp) for hp in host] for _ in range(2)]
@@ -759,7 +768,7 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
                                    shape.d_head, stream=stream)
         spinf.score_passes(plan, all_p, [sets[b][pi][3] for pi in all_p], w, w_scale, w_dtype, shape.d_model,
                            shape.vocab, [lse_dev[pi] for pi in all_p], [tl_dev[pi] for pi in all_p], ws[0],
-                           stream=stream)
+                           stream=stream, slot_rows=True)
         with torch.cuda.stream(stream):
             for pi in all_p:
                 tl_host[b][pi].copy_(tl_dev[pi], non_blocking=True)
@@ -793,7 +802,8 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
     return {"value": tokens / (ms * 1e-3), "unit": "packed tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": sum(p["info"].G for p in passes) * 4,
             "host_plan_ms_median": statistics.median(plan_ms[-n:]),
-            "covers": "per request: H2D q/k/v/hidden (copy stream, overlapping the previous request's kernels) + "
+            "covers": "per request: H2D q/k/v and the scoring rows' hidden states (copy stream, overlapping the "
+                      "previous request's kernels) + "
                       "plan (marshalling of the request's token lists + C planner) + "
                       "upload into kept descriptor memory + attention per pass + one scoring sweep + "
                       "D2H token lps + collect; two requests in flight"}
