@@ -23,6 +23,7 @@ OK, E_INVALID, E_LIMIT, E_NOMEM, E_CUDA, E_UNSUPPORTED, E_DEVICE_TIMEOUT, E_DEVI
 STATUS_NAMES = {0: "OK", 1: "INVALID", 2: "LIMIT", 3: "NOMEM", 4: "CUDA", 5: "UNSUPPORTED",
                 6: "DEVICE_TIMEOUT", 7: "DEVICE_CHECK"}
 DTYPE_BF16, DTYPE_E4M3 = 0, 1
+HIDDEN_PASS_ROWS, HIDDEN_SLOT_ROWS = 0, 1
 Q_SCORED, Q_SEARCHED = 0, 1
 
 #: every symbol the header declares
@@ -131,7 +132,7 @@ def lib():
     L.spinf_score_static.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp]
     L.spinf_score_passes_workspace_bytes.argtypes = [vp, i32, vp, i32, i32, i32]
     L.spinf_score_passes_workspace_bytes.restype = sz
-    L.spinf_score_passes.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.spinf_score_passes.argtypes = [vp, i32, vp, vp, i32, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
     L.spinf_collect.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(_Result)]
     L.spinf_collect_extract.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, vp]
     L.spinf_device_status.argtypes = [vp, vp]
@@ -683,9 +684,10 @@ def score_passes_workspace_bytes(plan, passes, vocab, d_model, w_dtype=DTYPE_BF1
 
 
 def score_passes(plan, passes, hidden, w, w_scale, w_dtype, d_model, vocab, row_lse, token_lp, workspace,
-                 workspace_bytes=None, stream=None):
+                 workspace_bytes=None, stream=None, slot_rows=False):
     """``spinf_score_passes``: the passes in ``passes`` scored in one sweep of the lm head; ``hidden``,
-    ``row_lse`` and ``token_lp`` are lists with one device tensor per listed pass."""
+    ``row_lse`` and ``token_lp`` are lists with one device tensor per listed pass.  ``slot_rows``:
+    each hidden tensor holds only its pass's scoring rows [M, d_model] (SPINF_HIDDEN_SLOT_ROWS)."""
     arr, ptr = _pass_list(passes)
     n = len(arr)
     if not (len(hidden) == len(row_lse) == len(token_lp) == n):
@@ -696,10 +698,11 @@ def score_passes(plan, passes, hidden, w, w_scale, w_dtype, d_model, vocab, row_
     hs, ls, ts = (ctypes.c_void_p * max(n, 1))(), (ctypes.c_void_p * max(n, 1))(), (ctypes.c_void_p * max(n, 1))()
     for b, p in enumerate(arr.tolist()):
         T, M, G, _ = plan._sizes(p)
-        hs[b] = a(hidden[b], f"hidden[{b}]", "bf16", T * d_model)
+        hs[b] = a(hidden[b], f"hidden[{b}]", "bf16", (M if slot_rows else T) * d_model)
         ls[b] = a(row_lse[b], f"row_lse[{b}]", "f32", M)
         ts[b] = a(token_lp[b], f"token_lp[{b}]", "f32", G)
-    _check(lib().spinf_score_passes(plan.handle, n, ptr, hs, a(w, "w", kind, vocab * d_model),
+    _check(lib().spinf_score_passes(plan.handle, n, ptr, hs, HIDDEN_SLOT_ROWS if slot_rows else HIDDEN_PASS_ROWS,
+                                    a(w, "w", kind, vocab * d_model),
                                     a(w_scale, "w_scale", "f32", vocab), w_dtype, d_model, vocab, ls, ts,
                                     a(workspace, "workspace", "bytes"), int(workspace_bytes), _stream(stream)))
 

@@ -75,8 +75,8 @@ struct RowMap {
     int nb;
     int m0[kMaxScorePasses + 1];
     int g0[kMaxScorePasses + 1];
-    const __nv_bfloat16* hidden[kMaxScorePasses];   // [T_pad, D] of each pass
-    const int32_t* slot_row[kMaxScorePasses];       // [M_b]
+    const __nv_bfloat16* hidden[kMaxScorePasses];   // [T_pad, D] of each pass, or its slot rows [M_b, D]
+    const int32_t* slot_row[kMaxScorePasses];       // [M_b]; nullptr: hidden holds the slot rows in order
     const int32_t* row_gptr[kMaxScorePasses];       // [M_b + 1]
     const int32_t* row_glist[kMaxScorePasses];      // [G_b]
     const int32_t* gather_tok[kMaxScorePasses];     // [G_b]
@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __grid_constant_
     const uint4* src = nullptr;
     if (m < M) {
         const int b = row_pass(rm, m);
-        src = reinterpret_cast<const uint4*>(rm.hidden[b] + (size_t)rm.slot_row[b][m - rm.m0[b]] * D);
+        const int ml = m - rm.m0[b];
+        src = reinterpret_cast<const uint4*>(rm.hidden[b] + (size_t)(rm.slot_row[b] ? rm.slot_row[b][ml] : ml) * D);
     }
     if (!FP8) {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + (size_t)m * D);
@@ -747,7 +748,8 @@ extern "C" size_t spinf_score_passes_workspace_bytes(const spinf_plan* plan, int
 }
 
 extern "C" spinf_status spinf_score_passes(const spinf_plan* plan, int32_t n_passes, const int32_t* passes,
-                                           const void* const* hidden, const void* w, const float* w_scale,
+                                           const void* const* hidden, int32_t hidden_rows, const void* w,
+                                           const float* w_scale,
                                            int32_t w_dtype, int32_t d_model, int32_t vocab, float* const* row_lse,
                                            float* const* token_lp, void* workspace, size_t workspace_bytes,
                                            spinf_stream stream) {
@@ -756,6 +758,8 @@ extern "C" spinf_status spinf_score_passes(const spinf_plan* plan, int32_t n_pas
     spinf_status st = passes_map(plan, n_passes, passes, rm, M, G);
     if (st) return st;
     if (!hidden || !row_lse || !token_lp) return fail(SPINF_E_INVALID, "NULL pointer array");
+    if (hidden_rows != SPINF_HIDDEN_PASS_ROWS && hidden_rows != SPINF_HIDDEN_SLOT_ROWS)
+        return fail(SPINF_E_INVALID, "hidden_rows must be SPINF_HIDDEN_PASS_ROWS or SPINF_HIDDEN_SLOT_ROWS");
     for (int32_t b = 0; b < n_passes; ++b)
         if ((st = ensure_device_ready(plan, passes[b]))) return st;
     if (w_dtype != SPINF_DTYPE_BF16 && w_dtype != SPINF_DTYPE_E4M3) return fail(SPINF_E_UNSUPPORTED, "w_dtype");
@@ -777,7 +781,7 @@ extern "C" spinf_status spinf_score_passes(const spinf_plan* plan, int32_t n_pas
         for (int32_t t : P.gather_tok)
             if (t < 0 || t >= vocab) return fail(SPINF_E_INVALID, "option token outside the vocabulary");
         rm.hidden[b] = static_cast<const __nv_bfloat16*>(hidden[b]);
-        rm.slot_row[b] = P.dev.slot_row;
+        rm.slot_row[b] = hidden_rows == SPINF_HIDDEN_SLOT_ROWS ? nullptr : P.dev.slot_row;
         rm.row_gptr[b] = P.dev.row_gptr;
         rm.row_glist[b] = P.dev.row_glist;
         rm.gather_tok[b] = P.dev.gather_tok;

@@ -324,6 +324,12 @@ spinf_status spinf_score(const spinf_plan* plan, int32_t pass,
 
 /* At most this many passes in one spinf_score_passes call. */
 #define SPINF_SCORE_MAX_PASSES 32
+/* What a pass's hidden buffer holds in spinf_score_passes: every packed row
+ * [T_pad, d_model] (the slot rows are read at slot_row[m]), or only the scoring
+ * rows [M, d_model], row m being the hidden state of the pass's scoring row m
+ * (the rows spinf_plan_pass_info lists in slot_row, in that order). */
+#define SPINF_HIDDEN_PASS_ROWS 0
+#define SPINF_HIDDEN_SLOT_ROWS 1
 
 /* Bytes of device workspace spinf_score_passes needs for these passes (0 for an
  * invalid list). */
@@ -342,14 +348,18 @@ size_t spinf_score_passes_workspace_bytes(const spinf_plan* plan, int32_t n_pass
  *
  * passes: host [n_passes] distinct pass indices, each uploaded;
  * hidden, row_lse, token_lp: host arrays of n_passes device pointers, entry b
- * for pass passes[b], with spinf_score's layouts ([T_pad, d_model] bf16, [M]
- * and [G] fp32); w, w_scale, w_dtype, d_model, vocab as for spinf_score;
+ * for pass passes[b]: hidden bf16 [T_pad, d_model] (hidden_rows
+ * SPINF_HIDDEN_PASS_ROWS) or [M, d_model] (SPINF_HIDDEN_SLOT_ROWS: a caller
+ * that has only the scoring rows, or copies only those to the device, passes
+ * them compacted), row_lse fp32 [M], token_lp fp32 [G];
+ * w, w_scale, w_dtype, d_model, vocab as for spinf_score;
  * workspace: device, >= spinf_score_passes_workspace_bytes.  Searched slots of
  * these passes get their row_lse but no answers (spinf_score_extract gives
  * those).  1 <= n_passes <= SPINF_SCORE_MAX_PASSES, else SPINF_E_INVALID /
  * SPINF_E_LIMIT; other errors as spinf_score. */
 spinf_status spinf_score_passes(const spinf_plan* plan, int32_t n_passes, const int32_t* passes,
-                                const void* const* hidden, const void* w, const float* w_scale, int32_t w_dtype,
+                                const void* const* hidden, int32_t hidden_rows,
+                                const void* w, const float* w_scale, int32_t w_dtype,
                                 int32_t d_model, int32_t vocab, float* const* row_lse, float* const* token_lp,
                                 void* workspace, size_t workspace_bytes, spinf_stream stream);
 

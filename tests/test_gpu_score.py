@@ -129,7 +129,7 @@ def test_gemma_full_vocab_e4m3_sampled_rows(spinf):
     np.testing.assert_array_equal(got_codes, want_codes)
 
 
-def _score_passes(spinf, plan, passes, hs, w, w_scale, w_dtype, shape):
+def _score_passes(spinf, plan, passes, hs, w, w_scale, w_dtype, shape, slot_rows=False):
     infos = [plan.pass_info(p) for p in passes]
     for p in passes:
         plan.upload(p)
@@ -137,7 +137,8 @@ def _score_passes(spinf, plan, passes, hs, w, w_scale, w_dtype, shape):
                      dtype=torch.uint8, device="cuda")
     lse = [torch.full((max(i.M, 1),), float("nan"), device="cuda") for i in infos]
     tlp = [torch.full((max(i.G, 1),), float("nan"), device="cuda") for i in infos]
-    spinf.score_passes(plan, passes, hs, w, w_scale, w_dtype, shape.d_model, shape.vocab, lse, tlp, ws)
+    spinf.score_passes(plan, passes, hs, w, w_scale, w_dtype, shape.d_model, shape.vocab, lse, tlp, ws,
+                       slot_rows=slot_rows)
     plan.device_status()
     torch.cuda.synchronize()
     return [(l[:i.M].cpu().numpy(), t[:i.G].cpu().numpy()) for l, t, i in zip(lse, tlp, infos)]
@@ -168,6 +169,11 @@ def test_score_passes_bitwise_equals_per_pass_calls(spinf, fp8):
         got = _score_passes(spinf, plan, passes, [hs[p] for p in passes], w, w_scale, w_dtype, shape)
         for p, (lse, tlp) in zip(passes, got):
             assert np.array_equal(lse, ref[p][0]) and np.array_equal(tlp, ref[p][1]), (passes, p)
+    # the hidden states of the scoring rows only, compacted in scoring-row order
+    slots = [hs[p][torch.as_tensor(lay.slot_row, device="cuda").long()].contiguous() for p, lay in enumerate(P.passes)]
+    got = _score_passes(spinf, plan, list(range(n)), slots, w, w_scale, w_dtype, shape, slot_rows=True)
+    for p, (lse, tlp) in enumerate(got):
+        assert np.array_equal(lse, ref[p][0]) and np.array_equal(tlp, ref[p][1]), ("slot rows", p)
 
 
 def test_score_passes_wikinews_job_one_sweep(spinf):
