@@ -723,6 +723,9 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
             for p in passes]
     copy_stream = torch.cuda.Stream()
     stream = torch.cuda.Stream()
+    # descriptor uploads copy from the plan's pageable host staging, which the driver does in step
+    # with the stream it is given: a stream of their own keeps them from waiting on the kernels
+    up_stream = torch.cuda.Stream()
     sets = [[tuple(torch.empty_like(t, device=dev) for t in hp) for hp in host] for _ in range(2)]
     obufs = [torch.empty_like(db[0]) for db in sets[0]]
     h2d = sum(t.numel() * t.element_size() for hp in host for t in hp)
@@ -755,8 +758,13 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
         t_plan = time.perf_counter()
         plan = spinf.Plan(inputs, vocab=shape.vocab)       # marshal the token lists and plan, overlapping the copies
         plan_ms.append((time.perf_counter() - t_plan) * 1e3)
+        if freed[b] is not None:   # the kernels that read this descriptor memory last are done
+            up_stream.wait_event(freed[b])
         for pi in range(plan.num_passes):
-            plan.upload(pi, stream, buffer=dsc[b][pi])
+            plan.upload(pi, up_stream, buffer=dsc[b][pi])
+        up_done = torch.cuda.Event()
+        up_done.record(up_stream)
+        stream.wait_event(up_done)
         all_p = list(range(plan.num_passes))
         if ws[0] is None:
             ws[0] = torch.empty(spinf.score_passes_workspace_bytes(plan, all_p, shape.vocab, shape.d_model, w_dtype),

@@ -44,6 +44,7 @@ struct WindowSchedule {
     int32_t key_tile = 128;  // keys per KV tile: 128, or 64 (the halves of the 128-key tiles)
     std::vector<int32_t> tile_ptr, tile_kv, tile_len, qt_work;
     void* block = nullptr;   // device copies of qt_work, tile_kv, tile_len (plan-owned)
+    bool in_pass_block = false;   // the copies sit in the pass's descriptor block (the 64-key schedule)
     int32_t *d_qt_work = nullptr, *d_tile_kv = nullptr, *d_tile_len = nullptr;
     std::vector<unsigned char> staging;
 };

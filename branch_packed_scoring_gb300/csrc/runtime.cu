@@ -68,7 +68,7 @@ spinf_status ensure_device_ready(const spinf_plan* plan, int32_t pass) {
 }
 
 spinf_status upload_window(WindowSchedule& w, cudaStream_t stream) {
-    if (w.block) return SPINF_OK;
+    if (w.block || w.in_pass_block) return SPINF_OK;
     const std::vector<int32_t>* arrays[3] = {&w.qt_work, &w.tile_kv, &w.tile_len};
     int32_t** dst[3] = {&w.d_qt_work, &w.d_tile_kv, &w.d_tile_len};
     size_t off[3], total = 0;
@@ -120,21 +120,29 @@ using namespace spinf;
 
 namespace {
 
-// The descriptor arrays of one pass, in upload order, with their device pointers.
+// The descriptor arrays of one pass, in upload order, with their device pointers.  The
+// pass's 64-key schedule (what d_head 256 attention walks without a window) travels in the
+// same block, so that an attention call allocates and uploads nothing.
 struct DescriptorSet {
-    const std::vector<int32_t>* arrays[15];
-    int32_t** dst[15];
-    int n = 15;
-    size_t off[15];
+    const std::vector<int32_t>* arrays[18];
+    int32_t** dst[18];
+    int n = 18;
+    size_t off[18];
     size_t total = 0;
+    WindowSchedule* w64 = nullptr;
 };
 
-DescriptorSet descriptor_set(Pass& P) {
+DescriptorSet descriptor_set(const spinf_plan* plan, Pass& P) {
+    std::lock_guard<std::mutex> lock(const_cast<spinf_plan*>(plan)->cache_mu);   // the plan's schedule cache
+    WindowSchedule& w = tile_schedule(P, 0, 64);
     DescriptorSet d{{&P.end, &P.pos, &P.tile_ptr, &P.tile_kv, &P.tile_len, &P.slot_row, &P.gather_m, &P.gather_tok,
-                     &P.row_gptr, &P.row_glist, &P.qt_work, &P.row_runs, &P.row_x, &P.x_m, &P.x_set},
+                     &P.row_gptr, &P.row_glist, &P.qt_work, &P.row_runs, &P.row_x, &P.x_m, &P.x_set, &w.qt_work,
+                     &w.tile_kv, &w.tile_len},
                     {&P.dev.end, &P.dev.pos, &P.dev.tile_ptr, &P.dev.tile_kv, &P.dev.tile_len, &P.dev.slot_row,
                      &P.dev.gather_m, &P.dev.gather_tok, &P.dev.row_gptr, &P.dev.row_glist, &P.dev.qt_work,
-                     &P.dev.row_runs, &P.dev.row_x, &P.dev.x_m, &P.dev.x_set}};
+                     &P.dev.row_runs, &P.dev.row_x, &P.dev.x_m, &P.dev.x_set, &w.d_qt_work, &w.d_tile_kv,
+                     &w.d_tile_len}};
+    d.w64 = w.block ? nullptr : &w;   // a schedule already uploaded on its own keeps its own copy
     for (int i = 0; i < d.n; ++i) {
         d.off[i] = d.total;
         d.total += (d.arrays[i]->size() * sizeof(int32_t) + 255) / 256 * 256;
@@ -155,6 +163,7 @@ spinf_status copy_descriptors(Pass& P, const DescriptorSet& d, void* block, cuda
         cudaError_t e = cudaMemcpyAsync(block, host.data(), d.total, cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess) return cuda_fail(e, "descriptor upload");
     }
+    if (d.w64) d.w64->in_pass_block = true;
     return SPINF_OK;
 }
 
@@ -185,7 +194,7 @@ extern "C" spinf_status spinf_plan_upload(spinf_plan* plan, int32_t pass, spinf_
     }
     Pass& P = plan->passes[pass];
     if (P.dev.block) return SPINF_OK;
-    const DescriptorSet d = descriptor_set(P);
+    const DescriptorSet d = descriptor_set(plan, P);
     void* block = nullptr;
     e = cudaMalloc(&block, d.total > 0 ? d.total : 256);
     if (e != cudaSuccess) return fail(SPINF_E_NOMEM, "device allocation of pass descriptors failed");
@@ -200,7 +209,7 @@ extern "C" spinf_status spinf_plan_upload(spinf_plan* plan, int32_t pass, spinf_
 
 extern "C" size_t spinf_plan_descriptor_bytes(const spinf_plan* plan, int32_t pass) {
     if (!plan || pass < 0 || pass >= (int32_t)plan->passes.size()) return 0;
-    return descriptor_set(const_cast<Pass&>(plan->passes[pass])).total + 256;   // + the error word
+    return descriptor_set(plan, const_cast<Pass&>(plan->passes[pass])).total + 256;   // + the error word
 }
 
 extern "C" spinf_status spinf_plan_upload_to(spinf_plan* plan, int32_t pass, void* buffer, size_t bytes,
@@ -211,7 +220,7 @@ extern "C" spinf_status spinf_plan_upload_to(spinf_plan* plan, int32_t pass, voi
         return fail(SPINF_E_INVALID, "descriptor buffer is NULL or not 256-byte aligned");
     Pass& P = plan->passes[pass];
     if (P.dev.block) return fail(SPINF_E_INVALID, "pass already uploaded");
-    const DescriptorSet d = descriptor_set(P);
+    const DescriptorSet d = descriptor_set(plan, P);
     if (bytes < d.total + 256) return fail(SPINF_E_INVALID, "descriptor buffer too small");
     int dev = -1;
     spinf_status st = check_device(plan, pass, &dev);

@@ -84,6 +84,25 @@ struct RowMap {
     float* token_lp[kMaxScorePasses];               // [G_b]
 };
 
+// Tile order of the main kernel: blocks of up to `rpb` 128-row tiles; within a block, vocabulary
+// tile by vocabulary tile, the block's row tiles next to each other.  A block's gathered rows
+// stay in L2 while the lm head streams past once per block (one block when all rows fit).
+__device__ __forceinline__ void unit_tile(int u, int n_st, int n_vt, int rpb, int& vt, int& st) {
+    const int per_block = n_vt * rpb;
+    const int rb = u / per_block;
+    const int rem = u - rb * per_block;
+    const int rows = min(rpb, n_st - rb * rpb);
+    vt = rem / rows;
+    st = rb * rpb + rem % rows;
+}
+
+// Row tiles per block: the gathered rows of a block take at most ~32 MB of the L2.
+int rows_per_block(int n_st, int d_model, int elt) {
+    const long long tile = (long long)kBM * d_model * elt;
+    const long long r = (32ll << 20) / (tile > 0 ? tile : 1);
+    return (int)std::max(1ll, std::min<long long>(r, n_st));
+}
+
 // The pass b of list row m (m < m0[nb]).
 __device__ __forceinline__ int row_pass(const RowMap& rm, int m) {
     int b = 0;
@@ -240,7 +259,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     score_main_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                       const float* __restrict__ s_act, const float* __restrict__ s_w, float2* __restrict__ part,
                       float* __restrict__ zg, const __grid_constant__ RowMap rm, int M, int V,
-                      int n_kb, int n_st, int n_vt, const ExtractArgs xa, int* __restrict__ err) {
+                      int n_kb, int n_st, int n_vt, int rpb, const ExtractArgs xa, int* __restrict__ err) {
     constexpr int kPerMma = FP8 ? 32 : 16;           // K elements of one MMA instruction
     constexpr int kMmaPerStage = (FP8 ? 128 : 64) / kPerMma;
     constexpr int kBK = FP8 ? 128 : 64;              // K elements per 128-byte row
@@ -279,7 +298,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             tma_prefetch_desc(&tm_w);
             uint32_t it = 0;
             for (int u = blockIdx.x; u < total; u += gridDim.x) {
-                const int vt = u / n_st, st = u % n_st;
+                int vt, st;
+                unit_tile(u, n_st, n_vt, rpb, vt, st);
                 for (int kb = 0; kb < n_kb; ++kb, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
@@ -328,7 +348,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         uint32_t tcount = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x, ++tcount) {
-            const int vt = u / n_st, st = u % n_st;
+            int vt, st;
+            unit_tile(u, n_st, n_vt, rpb, vt, st);
             const int acc = tcount & 1;
             const uint32_t aph = (tcount >> 1) & 1;
             const int m = st * kBM + r;
@@ -619,7 +640,8 @@ spinf_status launch_score_rows(const Pass* P, const RowMap& rm, const ScoreLayou
     ExtractArgs xa{KX ? P->dev.row_x : nullptr, KX ? P->dev.x_set : nullptr, KX ? ex->token_sets : nullptr,
                    KX ? ex->n_sets : 0, (V + 31) / 32, L.k, reinterpret_cast<uint2*>(ws + L.xpart)};
     score_main_kernel<FP8, KX><<<grid, kScoreThreads, KX ? kScoreSmemX : kScoreSmem, stream>>>(
-        th, tw, sa, w_scale, part, zg, rm, L.M, V, n_kb, L.n_st, L.n_vt, xa, err);
+        th, tw, sa, w_scale, part, zg, rm, L.M, V, n_kb, L.n_st, L.n_vt, rows_per_block(L.n_st, D, FP8 ? 1 : 2), xa,
+        err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "score launch");
     score_combine_kernel<<<(L.M + 3) / 4, 128, 0, stream>>>(part, zg, rm, L.M, L.n_vt);
