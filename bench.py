@@ -275,6 +275,34 @@ def run_ours(args, rank, world):
         return {"median": statistics.median(steps), "min": min(steps)}
 
     attn_stats, score_stats = per_step_stats(ev["attn"], len(passes)), per_step_stats(ev["score"], 1)
+    # The step's kernels again, back to back with no host sync between steps: each step above
+    # starts on an idle GPU, so its first launch's events also hold the host's launch time.  Here
+    # the host keeps the queue ahead of the GPU and the events time the kernels alone (still cold:
+    # the scoring sweep reads the 2 GB lm head between attention calls).  The roofline uses these.
+    bev = {"attn": [], "score": []}
+    with torch.cuda.stream(stream):
+        for r in range(max(4, args.steps) + 1):
+            for pi, p in enumerate(passes):
+                q, k, v, h = p["dev"]
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+                spinf.branch_attention(plan, pi, q, k, v, p["o"], shape.n_q_heads, shape.n_kv_heads, shape.d_head,
+                                       stream=stream)
+                a1.record(stream)
+                if r:
+                    bev["attn"].append((a0, a1))
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            spinf.score_passes(plan, all_passes, [p["dev"][3] for p in passes], w, w_scale, w_dtype, shape.d_model,
+                               shape.vocab, [p["lse"] for p in passes], [p["tlp"] for p in passes], ws_all,
+                               stream=stream)
+            s1.record(stream)
+            if r:
+                bev["score"].append((s0, s1))
+    torch.cuda.synchronize()
+    plan.device_status(stream)
+    attn_b2b = per_step_stats(bev["attn"], len(passes))["median"]
+    score_b2b = per_step_stats(bev["score"], 1)["median"]
     # for comparison: the same scoring as one spinf_score call per pass (each pads its own last
     # 128-row tile and reads the whole lm head)
     pev = []
@@ -335,9 +363,9 @@ def run_ours(args, rank, world):
 
     bf16_peak, hbm_peak, peak_label = _burst_peaks()
     mma_peak = bf16_peak * (2.0 if args.fp8 else 1.0)
-    score_tflops = flops_score / (score_ms * 1e-3) / 1e12
-    attn_tflops = flops_attn / (attn_ms * 1e-3) / 1e12
-    attn_gbs = bytes_attn / (attn_ms * 1e-3) / 1e9
+    score_tflops = flops_score / (score_b2b * 1e-3) / 1e12
+    attn_tflops = flops_attn / (attn_b2b * 1e-3) / 1e12
+    attn_gbs = bytes_attn / (attn_b2b * 1e-3) / 1e9
     out = {
         "metric": METRIC,
         "value": replica_value(tokens, world, ms),
@@ -356,6 +384,7 @@ def run_ours(args, rank, world):
                    "value_covers": "attention per pass + one scoring sweep over every pass's slot rows, token-lp "
                                    "D2H, collect; layout resident"},
         "roofline": {"kernel": "spinf_score_passes (gather + tcgen05 lm head + lse + combine, all passes)",
+                     "timing": "launches back to back, CUDA events per launch (kernel_ms_per_step.score_back_to_back)",
                      "bound": "tensor",
                      "achieved": score_tflops, "peak": mma_peak, "unit": "TFLOP/s",
                      "frac": score_tflops / mma_peak,
@@ -376,13 +405,15 @@ def run_ours(args, rank, world):
                                "peak_source": peak_label},
         # per kernel: packed tokens per attention-kernel second
         # (one layer call per pass) and user questions per scoring second (gather + main + combine)
-        "per_kernel": {"attention_packed_tokens_per_s": world * tokens / (attn_ms * 1e-3),
-                       "scoring_questions_per_s": world * questions / (score_ms * 1e-3),
+        "per_kernel": {"attention_packed_tokens_per_s": world * tokens / (attn_b2b * 1e-3),
+                       "scoring_questions_per_s": world * questions / (score_b2b * 1e-3),
+                       "timing": "kernels launched back to back (the host ahead of the GPU), CUDA events",
                        "user_questions": questions, "packed_tokens": tokens},
         "kernel_ms_per_step": {"attention": attn_ms, "score": score_ms,
                                "attention_median": attn_stats["median"], "attention_min": attn_stats["min"],
                                "score_median": score_stats["median"], "score_min": score_stats["min"],
                                "score_one_call_per_pass": score_per_pass_ms,
+                               "attention_back_to_back": attn_b2b, "score_back_to_back": score_b2b,
                                "attention_l2_warm": attn_warm_ms,
                                **({"attention_windowed": attn_win_ms, "window": shape.window} if attn_win_ms else {})},
         "searched_slots": extract,
