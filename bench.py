@@ -215,8 +215,8 @@ def run_ours(args, rank, world):
     tokens, questions, pairs, flops_attn, bytes_attn, flops_score = work_counts(inputs, plan, passes, shape)
     sched_tiles = sum(int(p["info"].n_sched) for p in passes)
     # the KV tiles the attention kernel executes: 64-key halves at d_head 256, else 128 keys
-    key_tile = 64 if shape.d_head == 256 else 128
-    exec_tiles = sum(len(plan.tile_schedule(pi, 0, key_tile)[1]) for pi in range(len(passes)))
+    key_tile, q_rows = exec_tiling(shape)
+    exec_tiles = sum(len(plan.tile_schedule(pi, 0, key_tile, q_rows)[1]) for pi in range(len(passes)))
 
     ev = {"attn": [], "score": []}
 
@@ -393,7 +393,7 @@ def run_ours(args, rank, world):
         "roofline_attention": {"kernel": "spinf_branch_attention", "tensor_tflops_unmasked": attn_tflops,
                                "tensor_frac": attn_tflops / bf16_peak, "hbm_gbs": attn_gbs,
                                "hbm_frac": attn_gbs / hbm_peak, "unmasked_pairs": pairs,
-                               "tile_occupancy": pairs / (exec_tiles * 128 * key_tile),
+                               "tile_occupancy": pairs / (exec_tiles * q_rows * key_tile), "q_rows": q_rows,
                                "key_tile": key_tile, "executed_kv_tiles": exec_tiles,
                                "tile_occupancy_128x128": pairs / (sched_tiles * 128 * 128),
                                "traffic": NCU_ATTN_TRAFFIC.get(args.workload),
@@ -508,6 +508,15 @@ def layer_timing(args, spinf, shape, plan, passes, dev, stream):
             "frac": {k: v / (bf16_peak * (2.0 if k.endswith("e4m3") else 1.0)) for k, v in tf.items()}}
 
 
+def exec_tiling(shape):
+    """(keys per KV tile, rows per Q tile) the attention kernel executes for these heads:
+    64-key tiles at d_head 256, on 64-row Q tiles when each kv head serves two query heads
+    (both heads stacked in the MMA's 128 rows)."""
+    if shape.d_head != 256:
+        return 128, 128
+    return 64, (64 if shape.n_q_heads == 2 * shape.n_kv_heads else 128)
+
+
 def pass_pairs(info, window=0):
     """Unmasked (row, key) pairs of one pass: key k is seen by the rows [k, end[k]) whose depth
     is within the window (pos[q] - pos[k] < window; 0: no window)."""
@@ -593,12 +602,12 @@ def per_workload_timing(args, spinf, wl, dev, stream, reps=3):
             t_attn, t_score = timed(attn(0)), timed(score, per_pass=False)
             t_win = timed(attn(shape.window)) if shape.window > 0 else None
         plan.device_status(stream)
-        key_tile = 64 if d == 256 else 128
+        key_tile, q_rows = exec_tiling(shape)
         tokens = sum(b["info"].T for b in bufs)
         rows = sum(b["info"].M for b in bufs)
         questions = sum(len(x[1]) for x in inputs)
         pairs = sum(pass_pairs(b["info"]) for b in bufs)
-        tiles = sum(len(plan.tile_schedule(pi, 0, key_tile)[1]) for pi in range(len(bufs)))
+        tiles = sum(len(plan.tile_schedule(pi, 0, key_tile, q_rows)[1]) for pi in range(len(bufs)))
         fl_attn = 4 * d * Hq * pairs
         by_attn = tokens * (2 * Hq + 2 * Hkv) * d * 2
         fl_score = 2 * rows * shape.vocab * shape.d_model
@@ -609,16 +618,16 @@ def per_workload_timing(args, spinf, wl, dev, stream, reps=3):
              "ms": {"attention": t_attn, "score": t_score, "step": t_attn + t_score},
              "packed_tokens_per_s": tokens / ((t_attn + t_score) * 1e-3),
              "scored_questions_per_s": questions / (t_score * 1e-3),
-             "tile_occupancy": pairs / (tiles * 128 * key_tile), "key_tile": key_tile,
+             "tile_occupancy": pairs / (tiles * q_rows * key_tile), "key_tile": key_tile, "q_rows": q_rows,
              "roofline": {"attention_tensor_frac": fl_attn / (t_attn * 1e-3) / 1e12 / bf16_peak,
                           "attention_hbm_frac": by_attn / (t_attn * 1e-3) / 1e9 / hbm_peak,
                           "score_tensor_frac": fl_score / (t_score * 1e-3) / 1e12 / mma_peak,
                           "score_peak_tflops": mma_peak}}
         if t_win is not None:
             pw = sum(pass_pairs(b["info"], shape.window) for b in bufs)
-            tw = sum(len(plan.tile_schedule(pi, shape.window, key_tile)[1]) for pi in range(len(bufs)))
+            tw = sum(len(plan.tile_schedule(pi, shape.window, key_tile, q_rows)[1]) for pi in range(len(bufs)))
             e["windowed"] = {"window": shape.window, "attention_ms": t_win, "unmasked_pairs": pw,
-                             "tile_occupancy": pw / (tw * 128 * key_tile),
+                             "tile_occupancy": pw / (tw * q_rows * key_tile),
                              "attention_tensor_frac": 4 * d * Hq * pw / (t_win * 1e-3) / 1e12 / bf16_peak}
         out[name] = e
         del bufs, w, w_scale, ws

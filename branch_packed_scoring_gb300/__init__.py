@@ -30,7 +30,7 @@ Q_SCORED, Q_SEARCHED = 0, 1
 SYMBOLS = [
     "spinf_plan_opts_default", "spinf_pack_plan", "spinf_plan_num_passes", "spinf_plan_pass_info",
     "spinf_plan_counts", "spinf_plan_extract_counts", "spinf_plan_upload", "spinf_plan_descriptor_bytes", "spinf_plan_upload_to",
-    "spinf_plan_window_schedule", "spinf_plan_tile_schedule",
+    "spinf_plan_window_schedule", "spinf_plan_tile_schedule", "spinf_plan_tile_schedule_q",
     "spinf_branch_attention", "spinf_score_workspace_bytes",
     "spinf_score", "spinf_score_extract", "spinf_score_static", "spinf_score_passes_workspace_bytes",
     "spinf_score_passes", "spinf_collect", "spinf_collect_extract",
@@ -121,6 +121,8 @@ def lib():
     L.spinf_plan_upload_to.argtypes = [vp, i32, vp, sz, vp]
     L.spinf_plan_window_schedule.argtypes = [vp, i32, i32, ctypes.POINTER(_P), ctypes.POINTER(_P), ctypes.POINTER(_P),
                                              ctypes.POINTER(i32)]
+    L.spinf_plan_tile_schedule_q.argtypes = [vp, i32, i32, i32, i32, ctypes.POINTER(_P), ctypes.POINTER(_P),
+                                             ctypes.POINTER(_P), ctypes.POINTER(i32)]
     L.spinf_plan_tile_schedule.argtypes = [vp, i32, i32, i32, ctypes.POINTER(_P), ctypes.POINTER(_P),
                                            ctypes.POINTER(_P), ctypes.POINTER(i32)]
     L.spinf_branch_attention.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, f32, i32, vp]
@@ -154,6 +156,7 @@ def lib():
     L.spinf_last_error.restype = ctypes.c_char_p
     for name in ("spinf_pack_plan", "spinf_plan_pass_info", "spinf_plan_counts", "spinf_plan_extract_counts",
                  "spinf_plan_upload", "spinf_plan_upload_to", "spinf_plan_window_schedule", "spinf_plan_tile_schedule",
+                 "spinf_plan_tile_schedule_q",
                  "spinf_branch_attention", "spinf_score", "spinf_score_extract", "spinf_score_static",
                  "spinf_score_passes", "spinf_collect",
                  "spinf_collect_extract",
@@ -521,13 +524,14 @@ class Plan:
         arr = lambda ptr, k: np.ctypeslib.as_array(ptr, shape=(k,)).copy() if k > 0 else np.zeros(0, np.int32)  # noqa: E731
         return arr(tp, nq + 1), arr(tk, n.value), arr(tl, n.value)
 
-    def tile_schedule(self, p, window=0, key_tile=128):
+    def tile_schedule(self, p, window=0, key_tile=128, q_rows=128):
         """(tile_ptr, tile_kv, tile_len) of the schedule the attention kernel runs on pass p
-        for a window (0: none) in tiles of key_tile keys (128; 64 at d_head 256)."""
+        for a window (0: none) in tiles of key_tile keys (128; 64 at d_head 256) and Q tiles of
+        q_rows rows (128; 64 at d_head 256 with two query heads per kv head)."""
         tp, tk, tl, n = _P(), _P(), _P(), ctypes.c_int32()
-        _check(lib().spinf_plan_tile_schedule(self.handle, p, window, key_tile, ctypes.byref(tp), ctypes.byref(tk),
-                                              ctypes.byref(tl), ctypes.byref(n)))
-        nq = self._sizes(p)[0] // 128   # Q tiles of the pass
+        _check(lib().spinf_plan_tile_schedule_q(self.handle, p, window, key_tile, q_rows, ctypes.byref(tp),
+                                                ctypes.byref(tk), ctypes.byref(tl), ctypes.byref(n)))
+        nq = self._sizes(p)[0] // q_rows   # Q tiles of the pass
         arr = lambda ptr, k: np.ctypeslib.as_array(ptr, shape=(k,)).copy() if k > 0 else np.zeros(0, np.int32)  # noqa: E731
         return arr(tp, nq + 1), arr(tk, n.value), arr(tl, n.value)
 

@@ -155,6 +155,9 @@ struct Item {
 
 // MODE 0: one CTA per item (one query head).  MODE 2: cta_group::2 pairs -- the leader
 // issues M = 256 MMAs over both CTAs' rows, each CTA holding half of every K and V tile.
+// MODE 3: one CTA per item of two query heads that share a kv head, 64 token rows of each
+// stacked in the MMA's 128 rows (Q tiles of 64 rows: fewer masked pairs per executed tile,
+// and each K/V tile serves both heads).
 template <int D, int MODE>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     branch_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -166,11 +169,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             const int32_t* __restrict__ tile_len, const int32_t* __restrict__ row_runs, int T,
                             int Hq, int Hkv, int n_items,
                             float scale_log2, int window, int* __restrict__ err) {
-    static_assert(MODE == 0 || MODE == 2, "one CTA per item, or a cta_group::2 pair");
+    static_assert(MODE == 0 || MODE == 2 || MODE == 3, "one CTA per item, a cta_group::2 pair, or two stacked heads");
     static_assert(MODE != 2 || D >= 128, "a cta_group::2 pair splits V into 64-column boxes");
     using L = AttnSmem<D, MODE>;
     constexpr bool PAIR = MODE == 2;
     constexpr bool CG2 = PAIR;
+    constexpr bool QG = MODE == 3;   // MMA row r: token row qt * 64 + (r & 63) of query head 2 * g + (r >> 6)
     constexpr int TK = kTK<D, MODE>;           // keys per KV tile
     constexpr int KH = TK / 2;                 // keys per softmax thread (half of a tile's row)
     extern __shared__ uint8_t smem_raw[];
@@ -190,7 +194,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
     const int n_units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
     const int heads_per_item = PAIR ? 2 : 1;
-    const int head_groups = Hq / heads_per_item;
+    const int head_groups = QG ? Hkv : Hq / heads_per_item;   // QG: an item is a kv head g
     // item it = (position it / head_groups in the work order, head group it % head_groups);
     // one 16-byte record {qt, first schedule entry, entry count, 0} per Q tile
     auto item = [&](int it) {
@@ -199,7 +203,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         I.qt = w.x;
         I.s0 = w.y;
         I.n = w.z;
-        I.h = (it % head_groups) * heads_per_item + rank;
+        I.h = QG ? it % head_groups : (it % head_groups) * heads_per_item + rank;
         return I;
     };
     // the k-th item of this CTA (pair): rounds of n_units items, every other round
@@ -306,7 +310,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                                  0, kc.I.h);
                             } else {
                                 mbar_arrive_expect_tx(&bars[Q_FULL], L::kTileBytes);
-                                tma_load_4d(sQ, &tm_q, &bars[Q_FULL], 0, kc.I.qt * 128, 0, kc.I.h);
+                                if constexpr (QG)   // (64 columns, rows, head, chunk) view: both heads' 64 rows
+                                    tma_load_4d(sQ, &tm_q, &bars[Q_FULL], 0, kc.I.qt * 64, 2 * kc.I.h, 0);
+                                else
+                                    tma_load_4d(sQ, &tm_q, &bars[Q_FULL], 0, kc.I.qt * 128, 0, kc.I.h);
                             }
                             ++ic;
                             q_pending = false;
@@ -324,7 +331,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                                  kc.kv0 + 64 * rank, 0, kc.I.h / group);
                             } else {
                                 mbar_arrive_expect_tx(&k_full[st], L::kKBytes);
-                                tma_load_4d(dst, &tm_k, &k_full[st], 0, kc.kv0, 0, kc.I.h / group);
+                                tma_load_4d(dst, &tm_k, &k_full[st], 0, kc.kv0, 0, QG ? kc.I.h : kc.I.h / group);
                             }
                             const int k_before = kc.k;
                             advance(kc);
@@ -344,7 +351,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                              rank * (L::kChunks / 2), vc.I.h / group);
                         } else {
                             mbar_arrive_expect_tx(&v_full[st], L::kVBytes);
-                            tma_load_4d(dst, &tm_v, &v_full[st], 0, vc.kv0, 0, vc.I.h / group);
+                            tma_load_4d(dst, &tm_v, &v_full[st], 0, vc.kv0, 0, QG ? vc.I.h : vc.I.h / group);
                         }
                         advance(vc);
                         progress = true;
@@ -521,7 +528,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int it_next = item_index(k + 1);
             const Item I_next = it_next < n_items ? item(it_next) : Item{0, 0, 0, 0};
             if (I.n > 0) {
-            const int q_row = I.qt * 128 + r;
+            const int q_row = QG ? I.qt * 64 + (r & 63) : I.qt * 128 + r;
             const bool real = q_row < T;
             const int pos_q = __ldg(pos + q_row);
             // the row's root path as up to four runs of rows [lo, hi) (x < 0: more runs)
@@ -709,7 +716,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {   // one 32-row x 32-column box (64-byte swizzle = the staging layout)
-                    tma_store_3d(&tm_o, stage, col, I.h, I.qt * 128 + quarter * 32);
+                    if constexpr (QG)
+                        tma_store_3d(&tm_o, stage, col, 2 * I.h + (quarter >> 1), I.qt * 64 + (quarter & 1) * 32);
+                    else
+                        tma_store_3d(&tm_o, stage, col, I.h, I.qt * 128 + quarter * 32);
                     tma_store_commit_and_wait_read();
                 }
                 __syncwarp();
@@ -763,9 +773,8 @@ spinf_status launch_mode(const Pass& P, const Sched& sc, const CUtensorMap& tq, 
     spinf_status st = set_smem_limit(reinterpret_cast<const void*>(kernel), smem, "cudaFuncSetAttribute(attention)");
     if (st) return st;
     cudaError_t e;
-    const int heads_per_item = MODE == 0 ? 1 : 2;
-    const int n_items = (P.T_pad / 128) * (Hq / heads_per_item);
-    if (MODE == 0) {
+    const int n_items = MODE == 3 ? (P.T_pad / 64) * Hkv : (P.T_pad / 128) * (Hq / (MODE == 0 ? 1 : 2));
+    if (MODE != 2) {
         const int grid = std::min(n_items, sm_count());
         kernel<<<grid, kAttnThreads, smem, stream>>>(tq, tk, tkh, tv, to, o, P.dev.end, P.dev.pos, sc.qt_work,
                                                      sc.tile_kv, sc.tile_len, P.dev.row_runs, P.T, Hq, Hkv,
@@ -838,12 +847,25 @@ spinf_status launch_attention(const Pass& P, const Sched& sc, const void* q, con
     }
     const float scale_log2 = scale * 1.4426950408889634f;
     // d_head 128 with an even number of query heads per kv head: a cta_group::2 pair of two
-    // heads (the kernel's third map is a K tile's key half); otherwise one CTA per head.
-    // d_head 256 copies 64-key K and V tiles (boxes of 64 rows) on the 64-key schedule
+    // heads (the kernel's third map is a K tile's key half).  d_head 256 with two query heads
+    // per kv head: both heads' 64-row Q tiles stacked in one CTA's MMA rows.  Otherwise one CTA
+    // per head.  d_head 256 copies 64-key K and V tiles (boxes of 64 rows) on the 64-key schedule
     const CUtensorMap& kmap = D == 256 ? tkh : tk;
     const CUtensorMap& vmap = D == 256 ? tvk : tv;
     if constexpr (D == 128)
         if ((Hq / Hkv) % 2 == 0) return launch_mode<D, 2>(P, sc, tq, tk, tkh, tvh, to, ob, Hq, Hkv, scale_log2, window, err, stream);
+    if constexpr (D == 256)
+        if (Hq / Hkv == 2) {
+            // Q as (64 columns, rows, head, 64-column chunk): a box of 64 rows of two adjacent heads
+            // lands chunk by chunk as 128 rows (head 2g, then 2g + 1), the MMA's A layout
+            CUtensorMap tq2;
+            const uint64_t dq2[4] = {64, (uint64_t)P.T_pad, (uint64_t)Hq, kCh};
+            const uint64_t sq2[3] = {(uint64_t)Hq * D * 2, (uint64_t)D * 2, 128};
+            const uint32_t box2[4] = {64, 64, 2, kCh};
+            if ((st = make_tmap(&tq2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, q, dq2, sq2, box2, CU_TENSOR_MAP_SWIZZLE_128B)))
+                return st;
+            return launch_mode<D, 3>(P, sc, tq2, kmap, tkh, vmap, to, ob, Hq, Hkv, scale_log2, window, err, stream);
+        }
     return launch_mode<D, 0>(P, sc, tq, kmap, tkh, vmap, to, ob, Hq, Hkv, scale_log2, window, err, stream);
 }
 
@@ -867,11 +889,13 @@ extern "C" spinf_status spinf_branch_attention(const spinf_plan* plan, int32_t p
     if (d_head != 64 && d_head != 128 && d_head != 256) return fail(SPINF_E_UNSUPPORTED, "d_head must be 64, 128 or 256");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // with a window, the schedule without the tiles no row of a Q tile sees within it;
-    // d_head 256 walks the 64-key halves of the schedule's tiles (those some row sees)
+    // d_head 256 walks the 64-key halves of the schedule's tiles (those some row sees), on
+    // 64-row Q tiles when a kv head serves two query heads
     Sched sc{P.dev.qt_work, P.dev.tile_kv, P.dev.tile_len};
     if ((window > 0 || d_head == 256) && P.T > 0) {
         std::lock_guard<std::mutex> lock(const_cast<spinf_plan*>(plan)->cache_mu);
-        WindowSchedule& w = tile_schedule(const_cast<Pass&>(P), window, d_head == 256 ? 64 : kTile);
+        const int q_rows = d_head == 256 && n_q_heads == 2 * n_kv_heads ? 64 : kTile;
+        WindowSchedule& w = tile_schedule(const_cast<Pass&>(P), window, d_head == 256 ? 64 : kTile, q_rows);
         if ((st = upload_window(w, s))) return st;
         sc = Sched{w.d_qt_work, w.d_tile_kv, w.d_tile_len};
     }

@@ -42,6 +42,7 @@ struct PassDevice {
 struct WindowSchedule {
     int32_t window = 0;      // 0: no window
     int32_t key_tile = 128;  // keys per KV tile: 128, or 64 (the halves of the 128-key tiles)
+    int32_t q_rows = 128;    // rows per Q tile: 128, or 64 (the halves of the planner's Q tiles)
     std::vector<int32_t> tile_ptr, tile_kv, tile_len, qt_work;
     void* block = nullptr;   // device copies of qt_work, tile_kv, tile_len (plan-owned)
     bool in_pass_block = false;   // the copies sit in the pass's descriptor block (the 64-key schedule)
@@ -104,6 +105,7 @@ spinf_status fail(spinf_status s, const std::string& msg);
 spinf_status ok();
 // The pass's schedule for window W > 0, built on first use and kept by the plan.
 WindowSchedule& window_schedule(Pass& P, int32_t window);
-// The schedule for window W >= 0 in KV tiles of `key_tile` keys (128 or 64), built on first use.
-WindowSchedule& tile_schedule(Pass& P, int32_t window, int32_t key_tile);
+// The schedule for window W >= 0 in KV tiles of `key_tile` keys (128 or 64) and Q tiles of
+// `q_rows` rows (128 or 64), built on first use.
+WindowSchedule& tile_schedule(Pass& P, int32_t window, int32_t key_tile, int32_t q_rows = kTile);
 }  // namespace spinf

@@ -214,23 +214,26 @@ bool ids_in_range(const spinf_tokens& t, int32_t vocab) {
 
 namespace spinf {
 
-WindowSchedule& window_schedule(Pass& P, int32_t window) { return tile_schedule(P, window, kTile); }
+WindowSchedule& window_schedule(Pass& P, int32_t window) { return tile_schedule(P, window, kTile, kTile); }
 
 // The schedule for window W (0: none) in KV tiles of `key_tile` keys (128, or 64: each
-// input-anchored 128-key tile taken as its two halves): a tile stays iff some row of the Q
-// tile sees one of its keys (within the window).  Skipping a tile that no row sees changes
-// no bit of the result.
-WindowSchedule& tile_schedule(Pass& P, int32_t window, int32_t key_tile) {
+// input-anchored 128-key tile taken as its two halves) and Q tiles of `q_rows` rows (128, or 64:
+// the halves of the planner's Q tiles): a KV tile stays iff some row of the Q tile sees one of
+// its keys (within the window), in the planner's order.  Skipping a tile that no row sees
+// changes no bit of the result.
+WindowSchedule& tile_schedule(Pass& P, int32_t window, int32_t key_tile, int32_t q_rows) {
     for (auto& w : P.windows)
-        if (w->window == window && w->key_tile == key_tile) return *w;
+        if (w->window == window && w->key_tile == key_tile && w->q_rows == q_rows) return *w;
     auto ws = std::make_unique<WindowSchedule>();
     ws->window = window;
     ws->key_tile = key_tile;
-    const int32_t n_qt = P.T_pad / kTile;
+    ws->q_rows = q_rows;
+    const int32_t n_qt = P.T_pad / q_rows;
     ws->tile_ptr.assign(1, 0);
     int32_t mins[8][kTile];   // sparse table of pos over one Q tile's real rows
     for (int32_t qt = 0; qt < n_qt; ++qt) {
-        const int32_t r0 = qt * kTile, r1 = std::min(r0 + kTile, P.T), nr = std::max(r1 - r0, 0);
+        const int32_t r0 = qt * q_rows, r1 = std::min(r0 + q_rows, P.T), nr = std::max(r1 - r0, 0);
+        const int32_t qp = r0 / kTile;   // the planner's Q tile that holds these rows
         if (window > 0) {   // only the window test reads the table
             for (int32_t i = 0; i < nr; ++i) mins[0][i] = P.pos[r0 + i];
             for (int32_t l = 1; (1 << l) <= nr; ++l)
@@ -242,7 +245,7 @@ WindowSchedule& tile_schedule(Pass& P, int32_t window, int32_t key_tile) {
             while ((2 << l) <= hi - lo) ++l;
             return std::min(mins[l][lo - r0], mins[l][hi - r0 - (1 << l)]);
         };
-        for (int32_t e = P.tile_ptr[qt]; e < P.tile_ptr[qt + 1]; ++e) {
+        for (int32_t e = P.tile_ptr[qp]; e < P.tile_ptr[qp + 1]; ++e) {
             for (int32_t sub = 0; sub < kTile; sub += key_tile) {
                 const int32_t kv0 = P.tile_kv[e] + sub, len = std::min(P.tile_len[e] - sub, key_tile);
                 if (len <= 0) break;
@@ -256,6 +259,12 @@ WindowSchedule& tile_schedule(Pass& P, int32_t window, int32_t key_tile) {
                     ws->tile_len.push_back(len);
                 }
             }
+        }
+        // a 64-row Q tile of pad rows only (the upper half of the last planner tile) keeps one
+        // tile, masked for all its rows, so that the kernel writes its pad rows (as zeros)
+        if (nr == 0 && ws->tile_kv.size() == (size_t)ws->tile_ptr.back() && P.tile_ptr[qp] < P.tile_ptr[qp + 1]) {
+            ws->tile_kv.push_back(P.tile_kv[P.tile_ptr[qp]]);
+            ws->tile_len.push_back(std::min(P.tile_len[P.tile_ptr[qp]], key_tile));
         }
         ws->tile_ptr.push_back((int32_t)ws->tile_kv.size());
     }
@@ -701,12 +710,20 @@ extern "C" spinf_status spinf_plan_window_schedule(const spinf_plan* plan, int32
 extern "C" spinf_status spinf_plan_tile_schedule(const spinf_plan* plan, int32_t pass, int32_t window,
                                                  int32_t key_tile, const int32_t** tile_ptr, const int32_t** tile_kv,
                                                  const int32_t** tile_len, int32_t* n_sched) {
+    return spinf_plan_tile_schedule_q(plan, pass, window, key_tile, kTile, tile_ptr, tile_kv, tile_len, n_sched);
+}
+
+extern "C" spinf_status spinf_plan_tile_schedule_q(const spinf_plan* plan, int32_t pass, int32_t window,
+                                                   int32_t key_tile, int32_t q_rows, const int32_t** tile_ptr,
+                                                   const int32_t** tile_kv, const int32_t** tile_len,
+                                                   int32_t* n_sched) {
     if (!plan || pass < 0 || pass >= (int32_t)plan->passes.size()) return fail(SPINF_E_INVALID, "bad plan or pass");
     if (window < 0) return fail(SPINF_E_INVALID, "negative window");
     if (key_tile != 64 && key_tile != kTile) return fail(SPINF_E_INVALID, "key_tile must be 64 or 128");
+    if (q_rows != 64 && q_rows != kTile) return fail(SPINF_E_INVALID, "q_rows must be 64 or 128");
     if (!tile_ptr || !tile_kv || !tile_len || !n_sched) return fail(SPINF_E_INVALID, "NULL output");
     std::lock_guard<std::mutex> lock(const_cast<spinf_plan*>(plan)->cache_mu);
-    WindowSchedule& w = tile_schedule(const_cast<Pass&>(plan->passes[pass]), window, key_tile);
+    WindowSchedule& w = tile_schedule(const_cast<Pass&>(plan->passes[pass]), window, key_tile, q_rows);
     *tile_ptr = w.tile_ptr.data();
     *tile_kv = w.tile_kv.data();
     *tile_len = w.tile_len.data();

@@ -124,25 +124,28 @@ namespace {
 // pass's 64-key schedule (what d_head 256 attention walks without a window) travels in the
 // same block, so that an attention call allocates and uploads nothing.
 struct DescriptorSet {
-    const std::vector<int32_t>* arrays[18];
-    int32_t** dst[18];
-    int n = 18;
-    size_t off[18];
+    const std::vector<int32_t>* arrays[21];
+    int32_t** dst[21];
+    int n = 21;
+    size_t off[21];
     size_t total = 0;
-    WindowSchedule* w64 = nullptr;
+    WindowSchedule* w64[2] = {nullptr, nullptr};
 };
 
 DescriptorSet descriptor_set(const spinf_plan* plan, Pass& P) {
     std::lock_guard<std::mutex> lock(const_cast<spinf_plan*>(plan)->cache_mu);   // the plan's schedule cache
-    WindowSchedule& w = tile_schedule(P, 0, 64);
+    WindowSchedule& w = tile_schedule(P, 0, 64);          // 128-row Q tiles (one query head per CTA)
+    WindowSchedule& w2 = tile_schedule(P, 0, 64, 64);     // 64-row Q tiles (two stacked query heads)
     DescriptorSet d{{&P.end, &P.pos, &P.tile_ptr, &P.tile_kv, &P.tile_len, &P.slot_row, &P.gather_m, &P.gather_tok,
                      &P.row_gptr, &P.row_glist, &P.qt_work, &P.row_runs, &P.row_x, &P.x_m, &P.x_set, &w.qt_work,
-                     &w.tile_kv, &w.tile_len},
+                     &w.tile_kv, &w.tile_len, &w2.qt_work, &w2.tile_kv, &w2.tile_len},
                     {&P.dev.end, &P.dev.pos, &P.dev.tile_ptr, &P.dev.tile_kv, &P.dev.tile_len, &P.dev.slot_row,
                      &P.dev.gather_m, &P.dev.gather_tok, &P.dev.row_gptr, &P.dev.row_glist, &P.dev.qt_work,
                      &P.dev.row_runs, &P.dev.row_x, &P.dev.x_m, &P.dev.x_set, &w.d_qt_work, &w.d_tile_kv,
-                     &w.d_tile_len}};
-    d.w64 = w.block ? nullptr : &w;   // a schedule already uploaded on its own keeps its own copy
+                     &w.d_tile_len, &w2.d_qt_work, &w2.d_tile_kv, &w2.d_tile_len}};
+    // a schedule already uploaded on its own keeps its own copy
+    d.w64[0] = w.block ? nullptr : &w;
+    d.w64[1] = w2.block ? nullptr : &w2;
     for (int i = 0; i < d.n; ++i) {
         d.off[i] = d.total;
         d.total += (d.arrays[i]->size() * sizeof(int32_t) + 255) / 256 * 256;
@@ -163,7 +166,8 @@ spinf_status copy_descriptors(Pass& P, const DescriptorSet& d, void* block, cuda
         cudaError_t e = cudaMemcpyAsync(block, host.data(), d.total, cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess) return cuda_fail(e, "descriptor upload");
     }
-    if (d.w64) d.w64->in_pass_block = true;
+    for (WindowSchedule* w : d.w64)
+        if (w) w->in_pass_block = true;
     return SPINF_OK;
 }
 

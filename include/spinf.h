@@ -246,6 +246,14 @@ spinf_status spinf_plan_tile_schedule(const spinf_plan* plan, int32_t pass, int3
                                       const int32_t** tile_ptr, const int32_t** tile_kv,
                                       const int32_t** tile_len, int32_t* n_sched);
 
+/* spinf_plan_tile_schedule for Q tiles of `q_rows` rows: 128 (as above), or 64 (what
+ * d_head 256 runs when a kv head serves two query heads: a 64-row Q tile of both heads
+ * fills the MMA's 128 rows).  tile_ptr has T_pad / q_rows + 1 entries.  SPINF_E_INVALID
+ * also for q_rows not 64 or 128. */
+spinf_status spinf_plan_tile_schedule_q(const spinf_plan* plan, int32_t pass, int32_t window, int32_t key_tile,
+                                        int32_t q_rows, const int32_t** tile_ptr, const int32_t** tile_kv,
+                                        const int32_t** tile_len, int32_t* n_sched);
+
 /* Number of user questions and options over the whole request (sizes of spinf_result). */
 spinf_status spinf_plan_counts(const spinf_plan* plan, int64_t* n_questions, int64_t* n_options);
 

@@ -36,10 +36,11 @@ def test_tiny_every_row(spinf):
     _check(lay, o, q, k, v, shape, list(range(lay.T)))
 
 
-# one per kernel arrangement: d 64 with an even group (two CTAs sharing multicast K/V),
-# odd groups (one CTA per head), d 128 / 256 with even groups (cta_group::2 pairs)
+# one per kernel arrangement: one CTA per head (d 64; d 128 with odd groups; d 256 with groups
+# other than two), cta_group::2 pairs (d 128, even groups), two query heads stacked per CTA on
+# 64-row Q tiles (d 256, groups of two)
 SHAPES = [wl.Shape(4, 2, 64, 256, 1000), wl.Shape(8, 8, 128, 256, 1000), wl.Shape(40, 8, 128, 256, 1000),
-          wl.Shape(8, 2, 128, 256, 1000), wl.Shape(16, 8, 256, 256, 1000)]
+          wl.Shape(8, 2, 128, 256, 1000), wl.Shape(16, 8, 256, 256, 1000), wl.Shape(6, 2, 256, 256, 1000)]
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"h{s.n_q_heads}-{s.n_kv_heads}-d{s.d_head}")
@@ -85,8 +86,9 @@ def _unit_rows(lay, source):
 
 
 @pytest.mark.parametrize("shape", [wl.Shape(4, 2, 64, 256, 1000), wl.Shape(8, 8, 128, 256, 1000),
-                                   wl.Shape(8, 2, 128, 256, 1000), wl.Shape(16, 8, 256, 256, 1000)],
-                         ids=["d64-pair", "d128-single", "d128-cg2", "d256-cg2"])
+                                   wl.Shape(8, 2, 128, 256, 1000), wl.Shape(16, 8, 256, 256, 1000),
+                                   wl.Shape(6, 2, 256, 256, 1000)],
+                         ids=["d64-single", "d128-single", "d128-cg2", "d256-stacked", "d256-single"])
 def test_packing_invariance_bitwise(spinf, shape):
     target = wl.stress(n_questions=12, content_tokens=230, vocab=1000)[0]
     others = wl.short_inputs(vocab=1000, n=40)
@@ -121,7 +123,8 @@ def test_wikinews_full_pass_sampled_rows(spinf, p, n_rows):
     assert not torch.isnan(o[:lay.T]).any()
 
 
-@pytest.mark.parametrize("shape", [wl.Shape(4, 2, 64, 256, 1000), wl.Shape(16, 8, 256, 256, 1000)], ids=["d64", "d256"])
+@pytest.mark.parametrize("shape", [wl.Shape(4, 2, 64, 256, 1000), wl.Shape(16, 8, 256, 256, 1000),
+                                   wl.Shape(6, 2, 256, 256, 1000)], ids=["d64", "d256-stacked", "d256-single"])
 def test_deep_tries_every_row(spinf, shape):
     """Rows whose root path has more than four runs take the key-by-key mask; the rest the
     per-row runs: both against the oracle on every row."""

@@ -65,7 +65,7 @@ def test_invariance_target_alone_bit_exact(spinf):
     _compare(spinf, [wl.invariance_target()], vocab=262144)
 
 
-def _target_tiles(spinf, inputs, idx, key_tile):
+def _target_tiles(spinf, inputs, idx, key_tile, q_rows=128):
     """Per row of the target input (relative to its first row): the executed KV tiles of
     its Q tile that hold a key the row sees, as (first key, length, visible keys), all
     relative to the input's first row; and that every other executed tile of the row's Q
@@ -73,12 +73,12 @@ def _target_tiles(spinf, inputs, idx, key_tile):
     P = op.plan(inputs, vocab=262144)
     p, u = next((p, u) for p, lay in enumerate(P.passes) for u in lay.units if u.source == idx)
     lay = P.passes[p]
-    tp, tk, tl = spinf.Plan(inputs, vocab=262144).tile_schedule(p, 0, key_tile)
+    tp, tk, tl = spinf.Plan(inputs, vocab=262144).tile_schedule(p, 0, key_tile, q_rows)
     out = []
     for r in range(u.start, u.start + u.size):
         vis = set(lay.visible(r))
         seq = []
-        for e in range(tp[r // 128], tp[r // 128 + 1]):
+        for e in range(tp[r // q_rows], tp[r // q_rows + 1]):
             seen = tuple(k - u.start for k in range(tk[e], tk[e] + tl[e]) if k in vis)
             if seen:
                 seq.append((int(tk[e]) - u.start, int(tl[e]), seen))
@@ -87,17 +87,17 @@ def _target_tiles(spinf, inputs, idx, key_tile):
     return out, u.start
 
 
-@pytest.mark.parametrize("key_tile", [64, 128])
-def test_invariance_target_executed_tiles(spinf, key_tile):
+@pytest.mark.parametrize("key_tile,q_rows", [(64, 128), (128, 128), (64, 64)])
+def test_invariance_target_executed_tiles(spinf, key_tile, q_rows):
     """The batch-invariance target's rows meet the same anchored KV tiles, in the same order
     and with the same visible keys at the same columns, alone and in all ten packings
     (what makes a row's attention output bit-identical alone or packed); every other
     executed tile of its Q tile is fully masked for it."""
-    ref, _ = _target_tiles(spinf, [wl.invariance_target()], 0, key_tile)
+    ref, _ = _target_tiles(spinf, [wl.invariance_target()], 0, key_tile, q_rows)
     offsets = set()
     for seed in range(1, 11):
         inputs, idx = wl.invariance_packing(seed)
-        got, start = _target_tiles(spinf, inputs, idx, key_tile)
+        got, start = _target_tiles(spinf, inputs, idx, key_tile, q_rows)
         offsets.add(start % 128)
         assert got == ref, seed
     assert len(offsets) > 3   # the packings put the target at several offsets within a Q tile
@@ -512,3 +512,39 @@ def test_grid_error_statuses_match(spinf, bad, status):
     with pytest.raises(spinf.SpinfError) as ee:
         spinf.Plan(bad, max_prompts_per_input=5)
     assert e.value.status == ee.value.status_name == status
+
+
+@pytest.mark.parametrize("name", ["tiny", "wikinews", "moderation"])
+@pytest.mark.parametrize("window", [0, 9])
+def test_derived_schedules_are_exact(spinf, name, window):
+    """The schedules the attention kernel runs (64-key tiles; 64-row Q tiles) against brute
+    force: a KV tile is listed for a Q tile iff some row of the Q tile sees one of its keys
+    (within the window); a 64-row Q tile of pad rows only lists one tile (masked for all its
+    rows, so that the kernel writes its pad rows).  Tiles appear in the planner's order."""
+    f, shape = wl.WORKLOADS[name]
+    inputs = f()
+    P = op.plan(inputs, vocab=shape.vocab)
+    Q = spinf.Plan(inputs, vocab=shape.vocab)
+    for p, lay in enumerate(P.passes[:2]):
+        end, pos = lay.end, lay.pos
+        for key_tile, q_rows in ((64, 128), (64, 64), (128, 64)):
+            tp, tk, tl = Q.tile_schedule(p, window, key_tile, q_rows)
+            assert len(tp) == lay.T_pad // q_rows + 1
+            for qt in range(lay.T_pad // q_rows):
+                r0, r1 = qt * q_rows, min((qt + 1) * q_rows, lay.T)
+                want = []
+                qp = qt * q_rows // 128
+                for e in range(lay.tile_ptr[qp], lay.tile_ptr[qp + 1]):
+                    for sub in range(0, 128, key_tile):
+                        kv0, n = int(lay.tile_kv[e]) + sub, min(int(lay.tile_len[e]) - sub, key_tile)
+                        if n <= 0:
+                            break
+                        if any(max(k, r0) < min(int(end[k]), r1) and
+                               (window <= 0 or min(int(pos[q]) for q in range(max(k, r0), min(int(end[k]), r1)))
+                                - int(pos[k]) < window) for k in range(kv0, kv0 + n)):
+                            want.append((kv0, n))
+                got = list(zip(tk[tp[qt]:tp[qt + 1]].tolist(), tl[tp[qt]:tp[qt + 1]].tolist()))
+                if r1 <= r0:   # pad rows only
+                    assert len(got) == 1, (qt, got)
+                else:
+                    assert got == want, (name, p, key_tile, q_rows, qt)
