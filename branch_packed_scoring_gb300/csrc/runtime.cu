@@ -296,8 +296,9 @@ extern "C" void spinf_plan_free(spinf_plan* plan) {
 }
 
 extern "C" const char* spinf_fingerprint(void) {
-    return "spinf-gb300 k1=branch_attention/tcgen05 q128xkv128 (kv64 at d256) input-anchored fp32-acc bf16-p;"
-           " k2=score/tcgen05 m128xv256xk64 fp32-acc lse-chunk256 fixed-order;"
+    return "spinf-gb300 k1=branch_attention/tcgen05 q128xkv128 (kv64 at d256; 2 heads x q64 when Hq=2Hkv) "
+           "input-anchored fp32-acc bf16-p tma-store;"
+           " k2=score/tcgen05 m128xv256xk64 fp32-acc lse-chunk256 fixed-order, multi-pass sweep in row blocks;"
            " fp8=e4m3 row-absmax/448 rne-sat;"
            " lin=tcgen05 m128xn256 fixed-order, rope fp64-table fp32-rotate, fp8 static scales; sm_103a";
 }
