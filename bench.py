@@ -44,8 +44,8 @@ NCU_SCORE_TRAFFIC = {("wikinews", False): 2024229376 + 14412032}
 # ncu captures of the current kernel; any other workload reports null.
 NCU_ATTN_TRAFFIC = {"wikinews": None}   # pass 0 only was captured: see per-pass figure below
 # DRAM bytes (read + write) of one attention launch on the Wikinews-shaped pass 0, from one ncu
-# capture of the current kernel (399.5 MB read, 106.4 MB written)
-NCU_ATTN_TRAFFIC_PASS0 = {"wikinews": 399459328 + 106367488}
+# capture of the current kernel (407.1 MB read, 105.9 MB written)
+NCU_ATTN_TRAFFIC_PASS0 = {"wikinews": 407107328 + 105860608}
 
 
 def _peaks():
@@ -220,8 +220,12 @@ def run_ours(args, rank, world):
 
     ev = {"attn": [], "score": []}
 
-    def step(record=False):
-        # the attention of every pass, then one scoring sweep over all passes' slot rows
+    for p in passes:   # two host buffers: step r + 1's copy lands while step r's results are collected
+        p["tlp_host2"] = [p["tlp_host"], torch.empty_like(p["tlp_host"]).pin_memory()]
+
+    def launch(r, record=False):
+        """Step r's GPU work: the attention of every pass, one scoring sweep over all passes'
+        slot rows, the token lps to host buffer r % 2; returns the event of its end."""
         for pi, p in enumerate(passes):
             q, k, v, h = p["dev"]
             if record:
@@ -241,12 +245,27 @@ def run_ours(args, rank, world):
             s1.record(stream)
             ev["score"].append((s0, s1))
         for p in passes:
-            p["tlp_host"].copy_(p["tlp"], non_blocking=True)
-        stream.synchronize()
-        return plan.collect([p["tlp_host"][:p["info"].G].numpy() for p in passes])
+            p["tlp_host2"][r % 2].copy_(p["tlp"], non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(stream)
+        return done
 
-    for _ in range(args.warmup):
-        step()
+    def finish(r, done):
+        """Step r's collect on the host, once its GPU work is done."""
+        done.synchronize()
+        return plan.collect([p["tlp_host2"][r % 2][:p["info"].G].numpy() for p in passes])
+
+    def run_steps(n, record=False):
+        # step r + 1's GPU work is enqueued before step r's results are collected, so the GPU
+        # is not idle while the host collects (two steps in flight, as a server would run them)
+        prev = launch(0, record)
+        for r in range(1, n):
+            cur = launch(r, record)
+            finish(r - 1, prev)
+            prev = cur
+        return finish(n - 1, prev)
+
+    run_steps(args.warmup)
     plan.device_status(stream)
     if world > 1:
         torch.distributed.barrier()
@@ -256,8 +275,7 @@ def run_ours(args, rank, world):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    for _ in range(args.steps):
-        res = step(record=True)
+    res = run_steps(args.steps, record=True)
     t_end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -381,8 +399,9 @@ def run_ours(args, rank, world):
         "data": "synthetic",
         "scored_questions_per_s": world * questions / (ms * 1e-3),
         "config": {**_config(args, inputs, len(passes), tokens, questions, shape, world),
-                   "value_covers": "attention per pass + one scoring sweep over every pass's slot rows, token-lp "
-                                   "D2H, collect; layout resident"},
+                   "value_covers": "per step: attention per pass + one scoring sweep over every pass's slot rows, "
+                                   "token-lp D2H, collect on the host; step r+1's GPU work is enqueued before "
+                                   "step r's collect (two steps in flight); layout resident"},
         "roofline": {"kernel": "spinf_score_passes (gather + tcgen05 lm head + lse + combine, all passes)",
                      "timing": "launches back to back, CUDA events per launch (kernel_ms_per_step.score_back_to_back)",
                      "bound": "tensor",
