@@ -1118,7 +1118,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="wikinews", choices=["wikinews", "moderation", "stress"])
+    ap.add_argument("--workload", default="wikinews", choices=["wikinews", "moderation", "stress", "invariance"])
     ap.add_argument("--fp8", action="store_true", help="e4m3 lm head with per-row scales")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -149,9 +149,16 @@ def token_sets(vocab, n_sets=2, density=0.01, seed=0):
     return out
 
 
+def invariance(seed=0, vocab=262144, packing_seed=1):
+    """One packing of the batch-invariance pass as a request: 2000 short inputs with the
+    470-token target inserted at a random index (its lm head is e4m3 in the benchmarks)."""
+    return invariance_packing(packing_seed, seed, vocab)[0]
+
+
 WORKLOADS = {
     "tiny": (tiny, TINY),
     "wikinews": (wikinews, GEMMA),
     "moderation": (moderation, GEMMA_WINDOWED),
     "stress": (stress, QWEN),
+    "invariance": (invariance, GEMMA),
 }
