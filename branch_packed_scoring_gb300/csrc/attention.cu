@@ -11,11 +11,14 @@
 // first, in rounds over the CTAs with every other round reversed, so the CTAs
 // finish together.  Consecutive items are the query heads of one Q tile, so the CTAs
 // of a round that share a kv head read its K and V tiles at about the same time (the
-// second read comes from L2).  At d_head 128, when a kv group has an even number of
-// query heads, CTAs run as cta_group::2 MMA pairs on two heads of one group: the
-// leader issues M = 256 products over both CTAs' rows, and each CTA holds half of
-// every K tile (64 keys) and V tile (64 columns).  Every CTA loads its own tiles
-// from this GPU's memory (no multicast copies).  Warp roles:
+// second read comes from L2).  At d_head 256 with two query heads per kv head, an
+// item is instead one kv head and a 64-row Q tile, both query heads' 64 rows stacked
+// in the MMA's 128 rows: each K/V tile serves both heads, and a 64-row tile meets
+// fewer masked keys.  At d_head 128, when a kv group has an even number of query
+// heads, CTAs run as cta_group::2 MMA pairs on two heads of one group: the leader
+// issues M = 256 products over both CTAs' rows, and each CTA holds half of every K
+// tile (64 keys) and V tile (64 columns).  Every CTA loads its own tiles from this
+// GPU's memory (no multicast copies).  Warp roles:
 //   warp 0      one TMA producer thread for Q (once per item), K and V tiles: it
 //               polls the buffers' barriers and issues whichever copy is free first
 //               (each tile one 4-D copy of all its 64-column chunks; two K and two V
