@@ -766,64 +766,63 @@ def extract_timing(args, spinf, sv, wl, inputs, shape, w, w_scale, w_dtype, dev,
                                     "next-token top-k over the whole vocabulary per row"}}
 
 
-def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
-    """Same job through the public API from pinned host buffers: H2D, plan, upload, kernels, D2H, collect.
+# requests in flight in the end-to-end leg (buffer sets of activations and descriptors)
+E2E_DEPTH = 3
 
-    Requests are pipelined the way a server would run them: while request i computes, the
-    activations of request i+1 go up on a copy stream into the other of two buffer sets and
-    its token lists are marshalled and planned on the host; request i's token log-probs come back and are collected
-    once its kernels finish.  Every request copies every byte again and reads its results
-    back; the timed region covers n whole requests.
+
+def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
+    """Same job through the public API from pinned host buffers: plan, upload, H2D, kernels, D2H, collect.
+
+    Requests are pipelined the way a server would run them, E2E_DEPTH in flight: request i is
+    planned on the host, its descriptors (from pinned staging, so the call does not wait for the
+    copy engine) and then its activations go up on the copy stream into buffer set i % E2E_DEPTH
+    while earlier requests compute; its kernels start pass by pass as each pass's copies land,
+    and its token log-probs come back and are collected two requests later.  Every request
+    copies every byte again and reads its results back; the timed region covers n whole requests.
     """
     import torch
 
+    depth = E2E_DEPTH
     # per pass: q, k, v and the hidden states of its scoring rows only (the lm head reads no other row)
     host = [tuple(t.pin_memory() for t in (*p["host"][:3], p["host"][3][torch.as_tensor(p["info"].slot_row).long()]))
             for p in passes]
     copy_stream = torch.cuda.Stream()
     stream = torch.cuda.Stream()
-    # descriptor uploads copy from the plan's pageable host staging, which the driver does in step
-    # with the stream it is given: a stream of their own keeps them from waiting on the kernels
-    up_stream = torch.cuda.Stream()
-    sets = [[tuple(torch.empty_like(t, device=dev) for t in hp) for hp in host] for _ in range(2)]
+    sets = [[tuple(torch.empty_like(t, device=dev) for t in hp) for hp in host] for _ in range(depth)]
     obufs = [torch.empty_like(db[0]) for db in sets[0]]
     h2d = sum(t.numel() * t.element_size() for hp in host for t in hp)
     ws = [None]
     tl_host = [[torch.empty(max(p["info"].G, 1), dtype=torch.float32, pin_memory=True) for p in passes]
-               for _ in range(2)]
+               for _ in range(depth)]
     tl_dev = [torch.empty(max(p["info"].G, 1), device=dev) for p in passes]
     lse_dev = [torch.empty(max(p["info"].M, 1), device=dev) for p in passes]
-    # descriptor memory kept across requests (per-plan allocations and frees would synchronise
-    # the device every request), one set per request in flight
+    # descriptor memory and its pinned staging kept across requests (per-plan allocations and
+    # frees would synchronise the device every request), one set per request in flight
     probe = spinf.Plan(inputs, vocab=shape.vocab)
     dbytes = [(probe.descriptor_bytes(pi) + 255) // 256 * 256 + (1 << 20) for pi in range(probe.num_passes)]
     probe.close()
-    dsc = [[torch.empty(b, dtype=torch.uint8, device=dev) for b in dbytes] for _ in range(2)]
-    freed = [None, None]     # per buffer set: compute of the request that last read it is done
+    dsc = [[torch.empty(b, dtype=torch.uint8, device=dev) for b in dbytes] for _ in range(depth)]
+    stg = [[torch.empty(b, dtype=torch.uint8).pin_memory() for b in dbytes] for _ in range(depth)]
+    freed = [None] * depth   # per buffer set: compute of the request that last read it is done
     plan_ms = []             # host time to marshal and plan each request
 
     def launch(i):
-        b = i % 2
+        b = i % depth
+        t_plan = time.perf_counter()
+        plan = spinf.Plan(inputs, vocab=shape.vocab)       # marshal the token lists and plan
+        plan_ms.append((time.perf_counter() - t_plan) * 1e3)
         ready = []
         with torch.cuda.stream(copy_stream):
-            if freed[b] is not None:
+            if freed[b] is not None:   # the kernels that last read this set's memory are done
                 copy_stream.wait_event(freed[b])
+            for pi in range(plan.num_passes):
+                plan.upload(pi, copy_stream, buffer=dsc[b][pi], staging=stg[b][pi])
             for pi in range(len(passes)):
                 for src, dst in zip(host[pi], sets[b][pi]):
                     dst.copy_(src, non_blocking=True)
                 ev = torch.cuda.Event()
                 ev.record(copy_stream)
                 ready.append(ev)
-        t_plan = time.perf_counter()
-        plan = spinf.Plan(inputs, vocab=shape.vocab)       # marshal the token lists and plan, overlapping the copies
-        plan_ms.append((time.perf_counter() - t_plan) * 1e3)
-        if freed[b] is not None:   # the kernels that read this descriptor memory last are done
-            up_stream.wait_event(freed[b])
-        for pi in range(plan.num_passes):
-            plan.upload(pi, up_stream, buffer=dsc[b][pi])
-        up_done = torch.cuda.Event()
-        up_done.record(up_stream)
-        stream.wait_event(up_done)
         all_p = list(range(plan.num_passes))
         if ws[0] is None:
             ws[0] = torch.empty(spinf.score_passes_workspace_bytes(plan, all_p, shape.vocab, shape.d_model, w_dtype),
@@ -846,19 +845,21 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
 
     def finish(i, plan, done):
         done.synchronize()
-        res = plan.collect([tl_host[i % 2][pi][:passes[pi]["info"].G].numpy() for pi in range(plan.num_passes)])
+        res = plan.collect([tl_host[i % depth][pi][:passes[pi]["info"].G].numpy() for pi in range(plan.num_passes)])
         plan.close()
         return res
 
     def run(n):
-        prev = launch(0)
-        for i in range(1, n):
-            cur = launch(i)
-            finish(i - 1, *prev)
-            prev = cur
-        return finish(n - 1, *prev)
+        inflight, res = [], None
+        for i in range(n):
+            inflight.append((i, *launch(i)))
+            if len(inflight) == depth:
+                res = finish(*inflight.pop(0))
+        while inflight:
+            res = finish(*inflight.pop(0))
+        return res
 
-    run(max(2, args.warmup))
+    run(max(depth, args.warmup))
     torch.cuda.synchronize()
     n = max(3, min(args.steps, 50))
     t0 = time.perf_counter()
@@ -869,11 +870,11 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
     return {"value": tokens / (ms * 1e-3), "unit": "packed tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": sum(p["info"].G for p in passes) * 4,
             "host_plan_ms_median": statistics.median(plan_ms[-n:]),
-            "covers": "per request: H2D q/k/v and the scoring rows' hidden states (copy stream, overlapping the "
-                      "previous request's kernels) + "
-                      "plan (marshalling of the request's token lists + C planner) + "
-                      "upload into kept descriptor memory + attention per pass + one scoring sweep + "
-                      "D2H token lps + collect; two requests in flight"}
+            "covers": "per request: plan (marshalling of the request's token lists + C planner) + descriptor "
+                      "upload from pinned staging into kept device memory + H2D q/k/v and the scoring rows' "
+                      "hidden states (copy stream, overlapping earlier requests' kernels) + attention per pass "
+                      "(each pass as its copies land) + one scoring sweep + D2H token lps + collect; "
+                      f"{depth} requests in flight"}
 
 
 # The oracle sample both CPU legs time (the repo arm's cpu_baseline and --impl reference),

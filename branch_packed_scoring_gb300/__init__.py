@@ -30,6 +30,7 @@ Q_SCORED, Q_SEARCHED = 0, 1
 SYMBOLS = [
     "spinf_plan_opts_default", "spinf_pack_plan", "spinf_plan_num_passes", "spinf_plan_pass_info",
     "spinf_plan_counts", "spinf_plan_extract_counts", "spinf_plan_upload", "spinf_plan_descriptor_bytes", "spinf_plan_upload_to",
+    "spinf_plan_upload_pinned",
     "spinf_plan_window_schedule", "spinf_plan_tile_schedule", "spinf_plan_tile_schedule_q",
     "spinf_branch_attention", "spinf_score_workspace_bytes",
     "spinf_score", "spinf_score_extract", "spinf_score_static", "spinf_score_passes_workspace_bytes",
@@ -119,6 +120,7 @@ def lib():
     L.spinf_plan_descriptor_bytes.argtypes = [vp, i32]
     L.spinf_plan_descriptor_bytes.restype = sz
     L.spinf_plan_upload_to.argtypes = [vp, i32, vp, sz, vp]
+    L.spinf_plan_upload_pinned.argtypes = [vp, i32, vp, sz, vp, sz, vp]
     L.spinf_plan_window_schedule.argtypes = [vp, i32, i32, ctypes.POINTER(_P), ctypes.POINTER(_P), ctypes.POINTER(_P),
                                              ctypes.POINTER(i32)]
     L.spinf_plan_tile_schedule_q.argtypes = [vp, i32, i32, i32, i32, ctypes.POINTER(_P), ctypes.POINTER(_P),
@@ -155,7 +157,7 @@ def lib():
     L.spinf_status_string.restype = ctypes.c_char_p
     L.spinf_last_error.restype = ctypes.c_char_p
     for name in ("spinf_pack_plan", "spinf_plan_pass_info", "spinf_plan_counts", "spinf_plan_extract_counts",
-                 "spinf_plan_upload", "spinf_plan_upload_to", "spinf_plan_window_schedule", "spinf_plan_tile_schedule",
+                 "spinf_plan_upload", "spinf_plan_upload_to", "spinf_plan_upload_pinned", "spinf_plan_window_schedule", "spinf_plan_tile_schedule",
                  "spinf_plan_tile_schedule_q",
                  "spinf_branch_attention", "spinf_score", "spinf_score_extract", "spinf_score_static",
                  "spinf_score_passes", "spinf_collect",
@@ -538,15 +540,26 @@ class Plan:
     def descriptor_bytes(self, p):
         return int(lib().spinf_plan_descriptor_bytes(self.handle, p))
 
-    def upload(self, p, stream=None, buffer=None):
+    def upload(self, p, stream=None, buffer=None, staging=None):
         """Descriptors of pass p to the device: into a plan-owned allocation, or into
-        `buffer` (a caller-owned uint8 device tensor of >= descriptor_bytes(p) bytes)."""
+        `buffer` (a caller-owned uint8 device tensor of >= descriptor_bytes(p) bytes);
+        with `staging` (a pinned uint8 host tensor of as many bytes) the copy is made from
+        there and the call does not wait for the copy engine (spinf_plan_upload_pinned)."""
         if buffer is None:
+            if staging is not None:
+                raise ValueError("staging needs a caller-owned device buffer")
             _check(lib().spinf_plan_upload(self.handle, p, _stream(stream)))
-        else:
-            addr = _Args("upload")(buffer, "buffer", "bytes")
-            _check(lib().spinf_plan_upload_to(self.handle, p, ctypes.c_void_p(addr),
-                                              buffer.numel() * buffer.element_size(), _stream(stream)))
+            return
+        addr = _Args("upload")(buffer, "buffer", "bytes")
+        nbytes = buffer.numel() * buffer.element_size()
+        if staging is None:
+            _check(lib().spinf_plan_upload_to(self.handle, p, ctypes.c_void_p(addr), nbytes, _stream(stream)))
+            return
+        if staging.is_cuda or not staging.is_contiguous():
+            raise ValueError("staging must be a contiguous host tensor")
+        _check(lib().spinf_plan_upload_pinned(self.handle, p, ctypes.c_void_p(addr), nbytes,
+                                              ctypes.c_void_p(staging.data_ptr()),
+                                              staging.numel() * staging.element_size(), _stream(stream)))
 
     def collect(self, token_lp_per_pass):
         """Per option lp / p / floor and per question residuals from host fp32 token lps."""

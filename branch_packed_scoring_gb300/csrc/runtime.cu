@@ -154,16 +154,23 @@ DescriptorSet descriptor_set(const spinf_plan* plan, Pass& P) {
 }
 
 // Points the pass's device views into `block` and enqueues the one copy, from a
-// staging buffer the plan keeps (so the copy may still be in flight on return).
-spinf_status copy_descriptors(Pass& P, const DescriptorSet& d, void* block, cudaStream_t s) {
-    std::vector<unsigned char>& host = P.staging;
-    host.assign(d.total, 0);
+// staging buffer the plan keeps (so the copy may still be in flight on return), or from
+// the caller's page-locked `stage` when one is given.
+spinf_status copy_descriptors(Pass& P, const DescriptorSet& d, void* block, cudaStream_t s,
+                              unsigned char* stage = nullptr) {
+    unsigned char* host = stage;
+    if (!host) {
+        P.staging.assign(d.total, 0);
+        host = P.staging.data();
+    } else {
+        std::memset(host, 0, d.total);
+    }
     for (int i = 0; i < d.n; ++i) {
-        if (!d.arrays[i]->empty()) std::memcpy(host.data() + d.off[i], d.arrays[i]->data(), d.arrays[i]->size() * 4);
+        if (!d.arrays[i]->empty()) std::memcpy(host + d.off[i], d.arrays[i]->data(), d.arrays[i]->size() * 4);
         *d.dst[i] = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(block) + d.off[i]);
     }
     if (d.total) {
-        cudaError_t e = cudaMemcpyAsync(block, host.data(), d.total, cudaMemcpyHostToDevice, s);
+        cudaError_t e = cudaMemcpyAsync(block, host, d.total, cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess) return cuda_fail(e, "descriptor upload");
     }
     for (WindowSchedule* w : d.w64)
@@ -216,8 +223,10 @@ extern "C" size_t spinf_plan_descriptor_bytes(const spinf_plan* plan, int32_t pa
     return descriptor_set(plan, const_cast<Pass&>(plan->passes[pass])).total + 256;   // + the error word
 }
 
-extern "C" spinf_status spinf_plan_upload_to(spinf_plan* plan, int32_t pass, void* buffer, size_t bytes,
-                                             spinf_stream stream) {
+namespace {
+
+spinf_status upload_into(spinf_plan* plan, int32_t pass, void* buffer, size_t bytes, unsigned char* stage,
+                         size_t stage_bytes, spinf_stream stream) {
     if (!plan) return fail(SPINF_E_INVALID, "plan is NULL");
     if (pass < 0 || pass >= (int32_t)plan->passes.size()) return fail(SPINF_E_INVALID, "bad pass index");
     if (!buffer || (reinterpret_cast<uintptr_t>(buffer) & 255))
@@ -226,6 +235,7 @@ extern "C" spinf_status spinf_plan_upload_to(spinf_plan* plan, int32_t pass, voi
     if (P.dev.block) return fail(SPINF_E_INVALID, "pass already uploaded");
     const DescriptorSet d = descriptor_set(plan, P);
     if (bytes < d.total + 256) return fail(SPINF_E_INVALID, "descriptor buffer too small");
+    if (stage && stage_bytes < d.total) return fail(SPINF_E_INVALID, "staging buffer too small");
     int dev = -1;
     spinf_status st = check_device(plan, pass, &dev);
     if (st) return st;
@@ -237,10 +247,31 @@ extern "C" spinf_status spinf_plan_upload_to(spinf_plan* plan, int32_t pass, voi
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
         plan->device = dev;
     }
-    if ((st = copy_descriptors(P, d, buffer, s))) return st;
+    if ((st = copy_descriptors(P, d, buffer, s, stage))) return st;
     P.dev.block = buffer;
     P.dev.owned = false;
     return SPINF_OK;
+}
+
+}  // namespace
+
+extern "C" spinf_status spinf_plan_upload_to(spinf_plan* plan, int32_t pass, void* buffer, size_t bytes,
+                                             spinf_stream stream) {
+    return upload_into(plan, pass, buffer, bytes, nullptr, 0, stream);
+}
+
+// A copy from pageable memory returns to the host only once the driver has staged it, and
+// the staging waits behind the transfers already queued on the copy engine: a caller that
+// overlaps the next request's activation copies with this one's kernels would stall there.
+// From page-locked memory the copy is enqueued and the call returns at once.
+extern "C" spinf_status spinf_plan_upload_pinned(spinf_plan* plan, int32_t pass, void* buffer, size_t bytes,
+                                                 void* staging, size_t staging_bytes, spinf_stream stream) {
+    if (!staging) return fail(SPINF_E_INVALID, "staging buffer is NULL");
+    cudaPointerAttributes a{};
+    cudaError_t e = cudaPointerGetAttributes(&a, staging);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(staging)");
+    if (a.type != cudaMemoryTypeHost) return fail(SPINF_E_INVALID, "staging buffer is not page-locked host memory");
+    return upload_into(plan, pass, buffer, bytes, static_cast<unsigned char*>(staging), staging_bytes, stream);
 }
 
 extern "C" spinf_status spinf_device_status(const spinf_plan* plan, spinf_stream stream) {

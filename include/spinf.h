@@ -282,6 +282,19 @@ size_t spinf_plan_descriptor_bytes(const spinf_plan* plan, int32_t pass);
 spinf_status spinf_plan_upload_to(spinf_plan* plan, int32_t pass, void* buffer, size_t bytes,
                                   spinf_stream stream);
 
+/* spinf_plan_upload_to, with the copy made from caller-owned page-locked host memory
+ * `staging` (cudaHostAlloc / cudaHostRegister; >= spinf_plan_descriptor_bytes): the
+ * descriptors are written there and the call returns as soon as the copy is enqueued.
+ * From pageable memory (the plan's own staging) the call returns only once the driver
+ * has staged the copy, behind every transfer already queued on the copy engine, which
+ * stalls a caller that overlaps the next request's activation copies with this one's
+ * kernels.  `staging` must not be written again until the copy has completed on
+ * `stream`; it stays the caller's.  SPINF_E_INVALID as for spinf_plan_upload_to, and for
+ * a NULL, short or pageable staging buffer.  The pages have no counterpart: it serves
+ * pipelined callers. */
+spinf_status spinf_plan_upload_pinned(spinf_plan* plan, int32_t pass, void* buffer, size_t bytes,
+                                      void* staging, size_t staging_bytes, spinf_stream stream);
+
 /* Tree-masked GQA attention over one packed pass ("spinf-serve 0.1.1",
  * "Speed and scale": one pass reads each content once, its questions branch off it).
  *

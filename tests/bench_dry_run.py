@@ -66,7 +66,7 @@ torch.Tensor.copy_ = lambda self, src, non_blocking=False: _copy(self, src)
 
 import branch_packed_scoring_gb300 as spinf  # noqa: E402
 real = spinf.lib()
-DEVICE = {"spinf_plan_upload", "spinf_plan_upload_to", "spinf_branch_attention", "spinf_score", "spinf_score_extract",
+DEVICE = {"spinf_plan_upload", "spinf_plan_upload_to", "spinf_plan_upload_pinned", "spinf_branch_attention", "spinf_score", "spinf_score_extract",
           "spinf_score_passes",
           "spinf_score_static", "spinf_device_status", "spinf_device_selftest", "spinf_rope_tree", "spinf_linear",
           "spinf_qkv_rope", "spinf_quantize_static", "spinf_decode_attention", "spinf_score_rows"}

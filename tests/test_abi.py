@@ -52,6 +52,8 @@ def test_upload_to_validates_before_any_device_work(spinf):
         st = L.spinf_plan_upload_to(plan.handle, 0, ptr, size, None)
         assert spinf.STATUS_NAMES[st] == "INVALID"
     assert spinf.STATUS_NAMES[L.spinf_plan_upload_to(plan.handle, 3, 4096, need, None)] == "INVALID"
+    # the pinned-staging variant refuses a NULL staging buffer first
+    assert spinf.STATUS_NAMES[L.spinf_plan_upload_pinned(plan.handle, 0, 4096, need, None, need, None)] == "INVALID"
 
 
 def test_selftest_needs_an_uploaded_plan(spinf):

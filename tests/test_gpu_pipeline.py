@@ -59,6 +59,35 @@ def test_upload_into_caller_memory_gives_identical_results(spinf):
         b.close()
 
 
+def test_upload_from_pinned_staging_gives_identical_results(spinf):
+    """spinf_plan_upload_pinned (descriptors written into caller-owned page-locked memory, then
+    copied) against the plan-owned upload: bit-identical attention and scores; pageable or
+    short staging is refused before any copy."""
+    inputs = wl.stress(n_questions=20, content_tokens=300, vocab=1024) + wl.tiny()
+    shape = wl.TINY
+    lay = oracle_plan(inputs, vocab=shape.vocab).passes[0]
+    q, k, v, h = pass_values(lay, shape)
+    w = sv.lm_head(shape.vocab, shape.d_model).cuda()
+    a = spinf.Plan(inputs, vocab=shape.vocab)
+    o_a = run_attention(spinf, a, 0, q, k, v, shape)
+    lse_a, tlp_a, _ = run_score(spinf, a, 0, h, w, None, spinf.DTYPE_BF16, shape)
+    need = a.descriptor_bytes(0)
+    buf = torch.empty(need, dtype=torch.uint8, device="cuda")
+    b = spinf.Plan(inputs, vocab=shape.vocab)
+    for bad in (torch.empty(need, dtype=torch.uint8),                       # pageable
+                torch.empty(need - 257, dtype=torch.uint8).pin_memory()):  # short
+        with pytest.raises(spinf.SpinfError) as e:
+            b.upload(0, buffer=buf, staging=bad)
+        assert e.value.status_name == "INVALID"
+    stage = torch.full((need,), 0xAB, dtype=torch.uint8).pin_memory()   # stale bytes must not leak in
+    b.upload(0, buffer=buf, staging=stage)
+    o_b = run_attention(spinf, b, 0, q, k, v, shape)
+    lse_b, tlp_b, _ = run_score(spinf, b, 0, h, w, None, spinf.DTYPE_BF16, shape)
+    assert torch.equal(o_a, o_b)
+    assert np.array_equal(lse_a, lse_b) and np.array_equal(tlp_a, tlp_b)
+    b.close()
+
+
 def test_bounded_wait_runs_out_and_device_stays_usable(spinf):
     """A device wait that nothing satisfies ends after its bound, the error word reports a
     timeout once, and the next calls on the same context run normally."""
