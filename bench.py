@@ -1041,12 +1041,33 @@ def run_ncu_case(args):
     dev = torch.device("cuda", 0)
     f, shape = wl.WORKLOADS[args.workload]
     inputs = f()
+    if args.ncu_case == "decode":   # two searched slots per input, as in the searched-slot timing
+        inputs = wl.with_searched_slots(inputs, 2, vocab=shape.vocab, n_sets=1)
     plan = spinf.Plan(inputs, vocab=shape.vocab)
     info = plan.pass_info(0)
     keys = sv.path_keys(info.tok, info.parent, info.T)
     plan.upload(0)
     w_dtype = spinf.DTYPE_E4M3 if args.fp8 else spinf.DTYPE_BF16
-    if args.ncu_case == "qkv":   # the fused QKV projection + rotary of pass 0, seeded random inputs
+    if args.ncu_case == "decode":
+        # one decoding step of beam 4 on pass 0: every searched slot's row extended by 4 tokens
+        # (token ids 0-3 stand in for its best four), attention on the pass's cached K/V
+        import numpy as np
+
+        q_p, k_p, v_p = (t.to(dev) for t in sv.qkv(keys, info.T_pad, shape.n_q_heads, shape.n_kv_heads,
+                                                   shape.d_head))
+        anchor = np.repeat(info.slot_row[info.x_m], 4)
+        dkeys = [sv.extend_key(keys[a], t) for a, t in zip(anchor, np.tile(np.arange(4), len(info.x_m)))]
+        qd, kd, vd = (t.to(dev) for t in sv.qkv(dkeys, len(dkeys), shape.n_q_heads, shape.n_kv_heads,
+                                                shape.d_head))
+        nd = len(dkeys)
+        i32 = lambda a: torch.as_tensor(np.asarray(a, dtype=np.int32)).to(dev)  # noqa: E731
+        anchor, parent, rows = i32(anchor), i32(np.full(nd, -1)), i32(np.arange(nd))
+        od = torch.empty_like(qd)
+
+        def call():
+            spinf.decode_attention(plan, 0, qd, k_p, v_p, kd, vd, anchor, parent, rows, od, shape.n_q_heads,
+                                   shape.n_kv_heads, shape.d_head)
+    elif args.ncu_case == "qkv":   # the fused QKV projection + rotary of pass 0, seeded random inputs
         Hq, Hkv, d, D = shape.n_q_heads, shape.n_kv_heads, shape.d_head, shape.d_model
         g = torch.Generator(device=dev)
         g.manual_seed(7)
@@ -1128,7 +1149,7 @@ def main():
     ap.add_argument("--no-per-workload", action="store_true",
                     help="skip the moderation / stress / e4m3 invariance-pass timings")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
-    ap.add_argument("--ncu-case", choices=["score", "score_passes", "attention", "qkv"], default=None,
+    ap.add_argument("--ncu-case", choices=["score", "score_passes", "attention", "qkv", "decode"], default=None,
                     help="run one boundary call on pass 0 only (small case for profiler captures)")
     ap.add_argument("--window", type=int, default=0)
     args = ap.parse_args()

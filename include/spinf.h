@@ -422,8 +422,10 @@ spinf_status spinf_score_extract(const spinf_plan* plan, int32_t pass,
  * [T_pad, Hkv, d] keys and values, as given to spinf_branch_attention), then to the
  * decode rows of its chain from the first token down to itself (k_dec, v_dec:
  * [n_dec, Hkv, d]), with the same softmax: its output equals that of the tokens written
- * into the template and laid out in a pass.  Keys are visited in a fixed order, so a
- * row's output does not depend on the other rows of the call.
+ * into the template and laid out in a pass.  Keys are visited and merged in a fixed
+ * order, so a row's output does not depend on the other rows of the call or on where it
+ * sits among them.  Rows of one anchor placed next to each other in q_row (a beam's
+ * rows) share the reads of their anchor's keys and values.
  *
  * q [n_q, Hq, d] are the queries of decode rows q_row[0..n_q) and o [n_q, Hq, d]
  * receives their outputs (bf16, device, 16-byte aligned).  anchor, parent [n_dec] and

@@ -129,6 +129,53 @@ def test_decode_rows_do_not_depend_on_the_step(spinf):
         assert torch.equal(o1[0], o_all[r])
 
 
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_beam_rows_share_their_anchor_and_match_alone(spinf, name):
+    """Beam layout: four decode rows per searched slot next to each other (first tokens), then
+    four second tokens each extending one of them.  Rows of one anchor are computed together;
+    each row equals, bit for bit, the same row computed alone, and the oracle."""
+    shape = SHAPES[name]
+    inputs = _request(shape.vocab)
+    lay = oracle_plan(inputs, vocab=shape.vocab).passes[0]
+    plan = spinf.Plan(inputs, vocab=shape.vocab)
+    plan.upload(0)
+    g = np.random.default_rng(3)
+    anchors = [int(lay.slot_row[m]) for m in lay.x_m]
+    anchor, parent, toks = [], [], []
+    for a in anchors:                       # step 1: beam of 4 first tokens per slot
+        for _ in range(4):
+            anchor.append(a)
+            parent.append(-1)
+            toks.append(int(g.integers(0, shape.vocab)))
+    n1 = len(toks)
+    for s in range(len(anchors)):           # step 2: each beam extends one of its first tokens
+        for b in range(4):
+            anchor.append(anchors[s])
+            parent.append(4 * s + int(g.integers(0, 4)))
+            toks.append(int(g.integers(0, shape.vocab)))
+    anchor, parent = np.array(anchor), np.array(parent)
+    _, _, qd, kd, vd = _values(lay, anchor, parent, toks, shape)
+    qp, kp, vp, _ = pass_values(lay, shape, hidden_rows=False)
+    kd, vd = kd.cuda(), vd.cuda()
+    for rows in (list(range(n1)), list(range(n1, len(toks)))):
+        q = qd[rows].contiguous().cuda()
+        o = torch.full_like(q, float("nan"))
+        spinf.decode_attention(plan, 0, q, kp, vp, kd, vd, _i32(anchor), _i32(parent), _i32(rows), o,
+                               shape.n_q_heads, shape.n_kv_heads, shape.d_head)
+        plan.device_status()
+        want = od.decode_attention(lay, qd[rows].double().numpy(), kp.double().cpu().numpy(),
+                                   vp.double().cpu().numpy(), kd.double().cpu().numpy(), vd.double().cpu().numpy(),
+                                   anchor, parent, rows, shape.n_q_heads, shape.n_kv_heads)
+        assert np.abs(o.float().cpu().numpy() - want).max() <= 2e-2
+        for j in (0, 1, 5, len(rows) - 1):
+            o1 = torch.empty(1, shape.n_q_heads, shape.d_head, dtype=torch.bfloat16, device="cuda")
+            spinf.decode_attention(plan, 0, qd[[rows[j]]].contiguous().cuda(), kp, vp, kd, vd, _i32(anchor),
+                                   _i32(parent), _i32([rows[j]]), o1, shape.n_q_heads, shape.n_kv_heads,
+                                   shape.d_head)
+            plan.device_status()
+            assert torch.equal(o1[0], o[j])
+
+
 def test_decode_checks_rows_on_the_device(spinf):
     """A bad row (parent not earlier, a chain of 70 tokens, q_row out of range) is written as
     zeros and reported as SPINF_E_DEVICE_CHECK; the good rows of the same call are unaffected."""
