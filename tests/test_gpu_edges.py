@@ -5,12 +5,15 @@
 * a pass of exactly 16,384 tokens (the token budget: no pad rows at all);
 * options of the maximal 5 tokens (the man page's option-token limit), scored
   through their option-trie rows;
-* vocabularies smaller than one 256-token tile (100) and one token past a tile (257).
+* vocabularies smaller than one 256-token tile (100) and one token past a tile (257);
+* a question at the 1000-option limit, and one of 1000 two-token options (1000 trie rows);
+* a content at the 4096-token limit with a question at the 256-token limit, with and without
+  a window that bites.
 """
 import numpy as np
 import pytest
 
-from gpu_util import oracle_plan, pass_values, run_attention, run_score
+from gpu_util import oracle_plan, pass_values, run_attention, run_score, sample_rows
 from oracle import attention as oa
 from oracle import collect as oc
 from oracle import score as osc
@@ -104,3 +107,50 @@ def test_small_and_ragged_vocabularies(spinf, vocab):
         lse, tlp, _ = run_score(spinf, plan, p, h, w.cuda(), None, spinf.DTYPE_BF16, shape)
         el, et, _ = _score(lay, h, w, lse, tlp)
         assert el <= 2e-3 and et <= 2e-3
+
+
+def test_thousand_options(spinf):
+    """A question at the option limit (1000 single-token options) and one of 1000 two-token
+    options (1000 option-trie rows): scores and option p against the oracle."""
+    shape = wl.Shape(4, 2, 64, 256, 4096)
+    g = np.random.default_rng(11)
+    single = [[int(t)] for t in g.choice(4096, size=1000, replace=False)]
+    firsts = g.choice(4096, size=1000, replace=False)
+    double = [[int(a), int(g.integers(0, 4096))] for a in firsts]
+    inputs = [([int(x) for x in g.integers(0, 4096, 120)], [([5, 6, 7], single), ([8, 9], double)])]
+    P = oracle_plan(inputs, vocab=4096)
+    plan = spinf.Plan(inputs, vocab=4096)
+    w = sv.lm_head(4096, 256)
+    lps, ref = [], []
+    for p, lay in enumerate(P.passes):
+        _, _, _, h = pass_values(lay, shape)
+        lse, tlp, _ = run_score(spinf, plan, p, h, w.cuda(), None, spinf.DTYPE_BF16, shape)
+        el, et, rt = _score(lay, h, w, lse, tlp)
+        assert el <= 2e-3 and et <= 2e-3
+        lps.append(tlp)
+        ref.append(rt)
+    res = plan.collect(lps)
+    want = oc.collect(P, ref)[0]
+    assert res["option_p"].shape == (2000,)
+    assert np.abs(res["option_p"] - np.concatenate([want[0]["p"], want[1]["p"]])).max() <= 4e-3
+    assert np.abs(res["residual"] - np.array([want[0]["residual"], want[1]["residual"]])).max() <= 4e-3
+
+
+@pytest.mark.parametrize("d_head", [128, 256])
+def test_longest_content_and_question(spinf, d_head):
+    """A content at the 4096-token limit with a question at the 256-token limit, with and
+    without a window that bites: sampled rows of every part against the oracle."""
+    shape = wl.Shape(8, 4 if d_head == 256 else 2, d_head, 256, 1000)
+    g = np.random.default_rng(12)
+    inputs = [([int(x) for x in g.integers(0, 1000, 4096)],
+               [([int(x) for x in g.integers(0, 1000, 256)], [[1], [2, 3]]), ([4, 5], [[6], [7]])])]
+    P = oracle_plan(inputs, vocab=1000)
+    plan = spinf.Plan(inputs, vocab=1000)
+    lay = P.passes[0]
+    q, k, v, _ = pass_values(lay, shape, hidden_rows=False)
+    rows = sample_rows(lay, 160, 4)
+    for window in (0, 1024):
+        o = run_attention(spinf, plan, 0, q, k, v, shape, window=window)
+        ref = oa.attention_rows(lay, q.float().cpu().numpy(), k.float().cpu().numpy(), v.float().cpu().numpy(),
+                                shape.n_q_heads, shape.n_kv_heads, rows, window=window)
+        assert float(np.abs(o[rows].float().cpu().numpy() - ref).max()) <= 2e-2
