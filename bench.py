@@ -83,19 +83,69 @@ def _peak_value(d, *names):
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples during the timed region."""
+    """SM clock and clock-event reasons during the timed region: NVML (the driver's
+    libnvidia-ml, read-only queries) polled every 2 ms from a thread, else nvidia-smi at 200 ms."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # clock-event reason bits of the NVML API
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
 
     def __init__(self, index):
         self.index = index
-        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.f = None
         self.p = None
+        self.nvml = None
+        self.thread = None
+        self.samples = []
+        self.stop_flag = False
+        try:
+            self.nvml = self._nvml_handle(index)
+        except Exception:
+            self.nvml = None
+
+    @staticmethod
+    def _nvml_handle(index):
+        import ctypes
+
+        import torch
+
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit")
+        prop = torch.cuda.get_device_properties(index)
+        bus = f"{prop.pci_domain_id:08X}:{prop.pci_bus_id:02X}:{prop.pci_device_id:02X}.0".encode()
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByPciBusId")
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h, reasons
+
+    def _poll(self):
+        import ctypes
+
+        lib, h, reasons = self.nvml
+        mhz, mx, bits = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))   # NVML_CLOCK_SM
+        while not self.stop_flag:
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0 and reasons(h, ctypes.byref(bits)) == 0:
+                self.samples.append((mhz.value, mx.value, bits.value))
+            time.sleep(0.002)
 
     def start(self):
+        if self.nvml is not None:
+            import threading
+
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            t0 = time.time()
+            while not self.samples and time.time() - t0 < 1.0:   # the first sample precedes the region
+                time.sleep(0.001)
+            return
         try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
                                        "--format=csv,noheader,nounits", "-lms", "200"],
                                       stdout=self.f, stderr=subprocess.DEVNULL)
@@ -103,6 +153,14 @@ class ClockSampler:
             self.p = None
 
     def stop(self):
+        if self.thread is not None:
+            self.stop_flag = True
+            self.thread.join(timeout=1.0)
+            sm = [s[0] for s in self.samples]
+            reasons = {n for _, _, b in self.samples for bit, n in self.REASONS.items() if b & bit}
+            return {"sm_mhz": statistics.median(sm) if sm else None,
+                    "sm_max_mhz": max(s[1] for s in self.samples) if sm else None,
+                    "samples": len(sm), "source": "nvml, 2 ms", "reasons": sorted(reasons)}
         if self.p is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.p.terminate()
@@ -128,7 +186,7 @@ class ClockSampler:
                     reasons.add(n)
         os.unlink(self.f.name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "source": "nvidia-smi, 200 ms", "reasons": sorted(reasons)}
 
 
 def max_over_ranks(ms, world, device):
