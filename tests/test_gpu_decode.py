@@ -20,6 +20,9 @@ def _i32(a):
 
 
 SHAPES = {"d64": wl.TINY, "d128": wl.Shape(40, 8, 128, 512, 1000), "d256": wl.Shape(16, 8, 256, 512, 1000)}
+# head groupings of the decode kernel's row blocks: 8 rows of 1 head, 2 rows of 4 heads, 1 row of 8 heads
+GROUPS = {"d128-g1": wl.Shape(8, 8, 128, 512, 1000), "d256-g4": wl.Shape(16, 4, 256, 512, 1000),
+          "d64-g8": wl.Shape(64, 8, 64, 512, 1000)}
 
 
 def _request(vocab):
@@ -53,9 +56,9 @@ def _values(lay, anchor, parent, toks, shape):
     return kp, keys, q, k, v
 
 
-@pytest.mark.parametrize("name", list(SHAPES))
+@pytest.mark.parametrize("name", list(SHAPES) + list(GROUPS))
 def test_decode_matches_oracle(spinf, name):
-    shape = SHAPES[name]
+    shape = {**SHAPES, **GROUPS}[name]
     inputs = _request(shape.vocab)
     lay = oracle_plan(inputs, vocab=shape.vocab).passes[0]
     plan = spinf.Plan(inputs, vocab=shape.vocab)
@@ -129,12 +132,12 @@ def test_decode_rows_do_not_depend_on_the_step(spinf):
         assert torch.equal(o1[0], o_all[r])
 
 
-@pytest.mark.parametrize("name", list(SHAPES))
+@pytest.mark.parametrize("name", list(SHAPES) + list(GROUPS))
 def test_beam_rows_share_their_anchor_and_match_alone(spinf, name):
     """Beam layout: four decode rows per searched slot next to each other (first tokens), then
     four second tokens each extending one of them.  Rows of one anchor are computed together;
     each row equals, bit for bit, the same row computed alone, and the oracle."""
-    shape = SHAPES[name]
+    shape = {**SHAPES, **GROUPS}[name]
     inputs = _request(shape.vocab)
     lay = oracle_plan(inputs, vocab=shape.vocab).passes[0]
     plan = spinf.Plan(inputs, vocab=shape.vocab)
