@@ -162,11 +162,30 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&
                            pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
 }
 
+// Tile order.  rpb == 0: row tile by row tile, every feature tile of a row tile next to each other,
+// so each row tile is read from HBM once and the weights stay in L2 (when they fit beside the
+// output stream).  rpb > 0: blocks of up to rpb row tiles; within a block, feature tile by
+// feature tile, the block's row tiles next to each other: a block's rows (at most ~32 MB) stay in
+// L2 while weights too large to stay there stream past once per block.
+__device__ __forceinline__ void linear_tile(int u, int n_mt, int n_nt, int rpb, int& mt, int& nt) {
+    if (rpb == 0) {
+        mt = u / n_nt;
+        nt = u % n_nt;
+        return;
+    }
+    const int per_block = n_nt * rpb;
+    const int rb = u / per_block;
+    const int rem = u - rb * per_block;
+    const int rows = min(rpb, n_mt - rb * rpb);
+    nt = rem / rows;
+    mt = rb * rpb + rem % rows;
+}
+
 template <bool FP8, int MODE>
 __global__ void __launch_bounds__(kLThreads, 1)
     linear_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                   const float* __restrict__ w_scale, float x_scale, const LinearOut out, int rows, int N, int n_kb,
-                  int n_mt, int n_nt, int* __restrict__ err) {
+                  int n_mt, int n_nt, int rpb, int* __restrict__ err) {
     constexpr int kPerMma = FP8 ? 32 : 16;
     constexpr int kMmaPerStage = (FP8 ? 128 : 64) / kPerMma;
     constexpr int kBK = FP8 ? 128 : 64;
@@ -202,15 +221,14 @@ __global__ void __launch_bounds__(kLThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *holder;
 
-    // tile u: rows mt, features nt; consecutive tiles share the row block (the weights
-    // stay in L2 across row blocks, each row block is read from HBM once)
     if (warp == 0) {
         if (lane == 0) {
             tma_prefetch_desc(&tm_x);
             tma_prefetch_desc(&tm_w);
             uint32_t it = 0;
             for (int u = first; u < total; u += stride) {
-                const int mt = u / n_nt, nt = u % n_nt;
+                int mt, nt;
+                linear_tile(u, n_mt, n_nt, rpb, mt, nt);
                 for (int kb = 0; kb < n_kb; ++kb, ++it) {
                     const int s = it % kLStages;
                     mbar_wait(&bars[LEMPTY0 + s], ((it / kLStages) & 1) ^ 1, err);
@@ -259,7 +277,8 @@ __global__ void __launch_bounds__(kLThreads, 1)
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         uint32_t tcount = 0;
         for (int u = first; u < total; u += stride, ++tcount) {
-            const int mt = u / n_nt, nt = u % n_nt;
+            int mt, nt;
+            linear_tile(u, n_mt, n_nt, rpb, mt, nt);
             const int acc = tcount & 1;
             const int row = mt * kLM + r;
             const int n0 = nt * kLN;
@@ -378,8 +397,13 @@ spinf_status launch_linear(const void* x, const void* w, const float* w_scale, f
     const int n_kb = (int)((K + kbk - 1) / kbk);
     const int n_mt = (int)((rows + kLM - 1) / kLM), n_nt = (int)((N + kLN - 1) / kLN);
     const int grid = std::min(n_mt * n_nt, sm_count());
+    // weights of more than 48 MB do not stay in L2 beside the output stream (measured: the bf16
+    // QKV weights, 63 MB, were read ~14 times from HBM in row-tile order); smaller ones do
+    const long long row_tile = (long long)kLM * K * (long long)elt;
+    const bool big_w = (long long)N * K * (long long)elt > (48ll << 20);
+    const int rpb = big_w ? (int)std::max(1ll, std::min<long long>((32ll << 20) / std::max(1ll, row_tile), n_mt)) : 0;
     linear_kernel<FP8, MODE><<<grid, kLThreads, kLSmem, stream>>>(tx, tw, w_scale, x_scale, out, (int)rows, (int)N,
-                                                                 n_kb, n_mt, n_nt, err);
+                                                                 n_kb, n_mt, n_nt, rpb, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "linear launch");
     return SPINF_OK;
