@@ -573,8 +573,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 };
                 if (all_visible) {
                     mx = max64();
-                } else if (window <= 0 && run01.x >= 0) {
-                    // visible keys of this half from the row's runs: no per-key loads
+                } else if ((window <= 0 || pos_q - head.y < window) && run01.x >= 0) {
+                    // visible keys of this half from the row's runs: no per-key loads (with a window,
+                    // when every key of the tile is within it: no key is shallower than head.y)
                     const int kb = head.z + KH * half;
                     auto bits = [&](int lo, int hi) -> uint64_t {
                         const int a = max(lo - kb, 0), b = min(hi - kb, KH);
