@@ -435,7 +435,7 @@ def run_ours(args, rank, world):
                                                           dev, stream)
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev) if not args.no_e2e else None
+    e2e = run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev, res) if not args.no_e2e else None
 
     bf16_peak, hbm_peak, peak_label = _burst_peaks()
     mma_peak = bf16_peak * (2.0 if args.fp8 else 1.0)
@@ -828,7 +828,7 @@ def extract_timing(args, spinf, sv, wl, inputs, shape, w, w_scale, w_dtype, dev,
 E2E_DEPTH = 3
 
 
-def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
+def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev, resident):
     """Same job through the public API from pinned host buffers: plan, upload, H2D, kernels, D2H, collect.
 
     Requests are pipelined the way a server would run them, E2E_DEPTH in flight: request i is
@@ -838,6 +838,7 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
     and its token log-probs come back and are collected two requests later.  Every request
     copies every byte again and reads its results back; the timed region covers n whole requests.
     """
+    import numpy as np
     import torch
 
     depth = E2E_DEPTH
@@ -924,8 +925,11 @@ def run_e2e(args, spinf, inputs, shape, passes, w, w_scale, w_dtype, dev):
     res = run(n)
     ms = (time.perf_counter() - t0) * 1e3 / n
     assert res["option_lp"].size > 0
+    # the same kernels on the same values as the resident step: the results must agree bit for bit
+    same = all(np.array_equal(res[k], resident[k], equal_nan=True) for k in res)
     tokens = sum(p["info"].T for p in passes)
     return {"value": tokens / (ms * 1e-3), "unit": "packed tokens/s", "ms_per_step": ms,
+            "results_bitwise_equal_to_resident_step": bool(same),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": sum(p["info"].G for p in passes) * 4,
             "host_plan_ms_median": statistics.median(plan_ms[-n:]),
             "covers": "per request: plan (marshalling of the request's token lists + C planner) + descriptor "

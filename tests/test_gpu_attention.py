@@ -89,7 +89,10 @@ def _unit_rows(lay, source):
                                    wl.Shape(8, 2, 128, 256, 1000), wl.Shape(16, 8, 256, 256, 1000),
                                    wl.Shape(6, 2, 256, 256, 1000)],
                          ids=["d64-single", "d128-single", "d128-cg2", "d256-stacked", "d256-single"])
-def test_packing_invariance_bitwise(spinf, shape):
+@pytest.mark.parametrize("window", [0, 100], ids=["no-window", "window-100"])
+def test_packing_invariance_bitwise(spinf, shape, window):
+    """The target's rows alone-ish and at five offsets among short inputs are bit-identical, with
+    no window and with a window that bites on its 230-token content."""
     target = wl.stress(n_questions=12, content_tokens=230, vocab=1000)[0]
     others = wl.short_inputs(vocab=1000, n=40)
     outs = []
@@ -98,9 +101,12 @@ def test_packing_invariance_bitwise(spinf, shape):
         lay = oracle_plan(inputs, vocab=1000, floors=False).passes[0]
         plan = spinf.Plan(inputs, vocab=1000, floors=False)
         q, k, v, _ = pass_values(lay, shape, hidden_rows=False)
-        o = run_attention(spinf, plan, 0, q, k, v, shape)
+        o = run_attention(spinf, plan, 0, q, k, v, shape, window=window)
         s, n = _unit_rows(lay, offset)
         outs.append((s, o[s:s + n].clone()))
+        if offset == 7 and window:   # the windowed rows against the oracle too
+            rows = list(range(s, s + n, 7))
+            _check(lay, o, q, k, v, shape, rows, window=window)
     starts = {s % 128 for s, _ in outs}
     assert len(starts) > 2
     for s, o in outs[1:]:
