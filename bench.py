@@ -618,22 +618,40 @@ def pass_pairs(info, window=0):
 def per_workload_timing(args, spinf, wl, dev, stream, reps=3):
     """The other workloads of the scope table, timed outside the headline step: the
     moderation-shaped job (plus its 1024-token windowed layer), the many-questions stress job
-    at Qwen-class shapes (plus a window that bites), and one packing of the batch-invariance
-    pass (2000 short inputs + the 470-token target) with the e4m3 per-row-scaled lm head.
+    at Qwen-class shapes (plus a window that bites), one packing of the batch-invariance
+    pass (2000 short inputs + the 470-token target) with the e4m3 per-row-scaled lm head, and
+    the Wikinews job asked as placeholder grids (with the host planning time of the grid
+    request and of the same questions written out).
     Values are seeded N(0, 1) bf16 drawn on the device (the path-keyed values change no
     amount of work); one attention call per pass and one scoring sweep over every pass's
     slot rows, ``reps`` times."""
     import torch
 
     bf16_peak, hbm_peak, _ = _burst_peaks()
-    cases = [("moderation", False), ("stress", False), ("invariance_e4m3", True)]
+    cases = [("moderation", False), ("stress", False), ("invariance_e4m3", True), ("wikinews_grid", False)]
     out = {}
     g = torch.Generator(device=dev)
     g.manual_seed(11)
+
+    def plan_ms(inputs, vocab, n=5):
+        """median host time to marshal and plan a request (ms)"""
+        ts = []
+        for _ in range(n):
+            t0 = time.perf_counter()
+            spinf.Plan(inputs, vocab=vocab).close()
+            ts.append((time.perf_counter() - t0) * 1e3)
+        return statistics.median(ts)
+
     for name, fp8 in cases:
+        extra = {}
         if name == "invariance_e4m3":
             inputs, _ = wl.invariance_packing(1)
             shape = wl.GEMMA
+        elif name == "wikinews_grid":   # the Wikinews job with its questions as one grid per content
+            inputs, shape = wl.wikinews_grid(), wl.GEMMA
+            extra = {"grid": "per content: 2 placeholders of 7 and 8 values -> 56 cells, 2 single-token options",
+                     "host_plan_ms": plan_ms(inputs, shape.vocab),
+                     "host_plan_ms_written_out": plan_ms(wl.written_out(inputs), shape.vocab)}
         else:
             f, shape = wl.WORKLOADS[name]
             inputs = f()
@@ -690,14 +708,14 @@ def per_workload_timing(args, spinf, wl, dev, stream, reps=3):
         key_tile, q_rows = exec_tiling(shape)
         tokens = sum(b["info"].T for b in bufs)
         rows = sum(b["info"].M for b in bufs)
-        questions = sum(len(x[1]) for x in inputs)
+        questions = plan.counts()[0]
         pairs = sum(pass_pairs(b["info"]) for b in bufs)
         tiles = sum(len(plan.tile_schedule(pi, 0, key_tile, q_rows)[1]) for pi in range(len(bufs)))
         fl_attn = 4 * d * Hq * pairs
         by_attn = tokens * (2 * Hq + 2 * Hkv) * d * 2
         fl_score = 2 * rows * shape.vocab * shape.d_model
         mma_peak = bf16_peak * (2.0 if fp8 else 1.0)
-        e = {"inputs": len(inputs), "user_questions": questions, "passes": len(bufs), "packed_tokens": tokens,
+        e = {**extra, "inputs": len(inputs), "user_questions": questions, "passes": len(bufs), "packed_tokens": tokens,
              "scoring_rows": rows, "shape": f"Hq={Hq} Hkv={Hkv} d_head={d} d_model={shape.d_model} V={shape.vocab}",
              "lm_head": "e4m3 per-row scaled" if fp8 else "bf16",
              "ms": {"attention": t_attn, "score": t_score, "step": t_attn + t_score},

@@ -155,6 +155,37 @@ def invariance(seed=0, vocab=262144, packing_seed=1):
     return invariance_packing(packing_seed, seed, vocab)[0]
 
 
+def wikinews_grid(seed=0, vocab=262144, n_contents=24):
+    """The Wikinews-shaped job with its questions as one placeholder grid per content: literal
+    pieces of 4, 3 and 2 tokens around two placeholders of 7 and 8 values (1-2 tokens each),
+    two single-token options: 56 cells of 11-13 tokens per content.  A grid is
+    ``(pieces, values per placeholder, options)``; the input is ``(content, [], [grid])``."""
+    g = _rng(seed + 5000)
+    pieces = [_ids(g, 4, vocab), _ids(g, 3, vocab), _ids(g, 2, vocab)]
+    values = [[_ids(g, int(g.integers(1, 3)), vocab) for _ in range(7)],
+              [_ids(g, int(g.integers(1, 3)), vocab) for _ in range(8)]]
+    grid = (pieces, values, [[t] for t in _distinct(g, 2, vocab)])
+    return [(_ids(g, int(g.integers(400, 541)), vocab), [], [grid]) for _ in range(n_contents)]
+
+
+def written_out(inputs):
+    """The same inputs with every grid cell written out as a question, first placeholder
+    slowest (the order a grid's cells take in the plan)."""
+    out = []
+    for content, questions, *rest in inputs:
+        qs = list(questions)
+        for pieces, values, options in (rest[0] if rest else []):
+            def cells(i, acc):
+                if i == len(values):
+                    yield acc + pieces[-1]
+                    return
+                for val in values[i]:
+                    yield from cells(i + 1, acc + pieces[i] + val)
+            qs.extend((tmpl, options) for tmpl in cells(0, []))
+        out.append((content, qs))
+    return out
+
+
 WORKLOADS = {
     "tiny": (tiny, TINY),
     "wikinews": (wikinews, GEMMA),
