@@ -174,14 +174,16 @@ def written_out(inputs):
     out = []
     for content, questions, *rest in inputs:
         qs = list(questions)
-        for pieces, values, options in (rest[0] if rest else []):
+        for grid in (rest[0] if rest else []):
+            pieces, values, options, tail = grid[0], grid[1], grid[2], tuple(grid[3:])   # tail: a searched token set
+
             def cells(i, acc):
                 if i == len(values):
                     yield acc + pieces[-1]
                     return
                 for val in values[i]:
                     yield from cells(i + 1, acc + pieces[i] + val)
-            qs.extend((tmpl, options) for tmpl in cells(0, []))
+            qs.extend((tmpl, options, *tail) for tmpl in cells(0, []))
         out.append((content, qs))
     return out
 

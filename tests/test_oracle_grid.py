@@ -46,3 +46,19 @@ def test_grid_errors():
     with pytest.raises(op.PlanError) as e:
         op.plan([([1], [], [([[]], [], [[3]])])])                  # a cell with an empty template
     assert e.value.status == "INVALID"
+
+
+def test_synthetic_written_out_form_matches_the_expansion():
+    """synth's written-out form of a grid request (the bench's comparison input) has the cells
+    in the plan's order: the same layout as the grid request itself."""
+    from synth import workloads as wl
+
+    searched = ([[], [5]], [[[7], [], [8, 9]]], None, 2)
+    inputs = [([9, 9, 9], [([50], [[60], [61]])], [GRID, searched])] + wl.wikinews_grid(vocab=1000, n_contents=3)
+    written = wl.written_out(inputs)
+    assert written[0][1][1:] == [tuple(c) for c in op.expand_grid(GRID)] + op.expand_grid(searched)
+    P, Q = op.plan(inputs, vocab=1000), op.plan(written, vocab=1000)
+    assert len(P.passes) == len(Q.passes)
+    for a, b in zip(P.passes, Q.passes):
+        for f in ("tok", "parent", "pos", "end", "slot_row", "gather_tok"):
+            assert getattr(a, f).tolist() == getattr(b, f).tolist(), f
