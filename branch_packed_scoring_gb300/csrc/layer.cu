@@ -13,10 +13,11 @@
 //
 //   linear_kernel<FP8, MODE>   persistent tcgen05 GEMM y = x w^T: 128 rows x 256
 //                              output features per tile, fp32 in TMEM (two
-//                              accumulators), a 4-stage TMA ring.  MODE 0 writes y;
-//                              MODE 1 (QKV) turns the q and k columns by the row's
-//                              tree position in the epilogue and writes q, k, v in
-//                              the attention kernel's layouts.
+//                              accumulators), a 4-stage TMA ring, the output
+//                              staged per warp and written by TMA stores.  MODE 0
+//                              writes y; MODE 1 (QKV) turns the q and k columns by
+//                              the row's tree position in the epilogue and writes
+//                              q, k, v in the attention kernel's layouts.
 //   quantize_static_kernel     bf16 -> e4m3 codes with a static scale
 //   rope_tree_kernel           the rotary embedding alone, in place on q and k
 //
@@ -137,7 +138,11 @@ enum { LFULL0 = 0, LEMPTY0 = kLStages, LACC_FULL0 = 2 * kLStages, LACC_EMPTY0 = 
        LN_BARS = 2 * kLStages + 4 };
 constexpr int kLSmemBars = kLStages * kLStage;
 constexpr int kLSmemHolder = kLSmemBars + (LN_BARS + 1) * 8;
-constexpr int kLSmem = kLSmemHolder + 16 + 1024;
+// output staging: per epilogue warp two 32-row x 32-column bf16 boxes, written by TMA stores
+constexpr int kLStageBytes = 32 * 32 * 2;
+constexpr int kLStageOff = (kLSmemHolder + 16 + 1023) / 1024 * 1024;
+constexpr int kLSmem = kLStageOff + 4 * 2 * kLStageBytes + 1024;
+static_assert(kLSmem <= 227 * 1024, "shared memory of one CTA");
 
 // Where the product's columns go.  MODE 0: all to y[0] (row stride ld[0]).  MODE 1:
 // product column n belongs to output o = 0 (q), 1 (k) or 2 (v) by base[]; columns
@@ -153,14 +158,6 @@ struct LinearOut {
     int stride;            // max pos + 1
     const int32_t* pos;    // [rows]
 };
-
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&v)[32]) {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        d4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-}
 
 // Tile order.  rpb == 0: row tile by row tile, every feature tile of a row tile next to each other,
 // so each row tile is read from HBM once and the weights stay in L2 (when they fit beside the
@@ -184,6 +181,8 @@ __device__ __forceinline__ void linear_tile(int u, int n_mt, int n_nt, int rpb, 
 template <bool FP8, int MODE>
 __global__ void __launch_bounds__(kLThreads, 1)
     linear_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                  const __grid_constant__ CUtensorMap tm_y0, const __grid_constant__ CUtensorMap tm_y1,
+                  const __grid_constant__ CUtensorMap tm_y2,
                   const float* __restrict__ w_scale, float x_scale, const LinearOut out, int rows, int N, int n_kb,
                   int n_mt, int n_nt, int rpb, int* __restrict__ err) {
     constexpr int kPerMma = FP8 ? 32 : 16;
@@ -275,6 +274,8 @@ __global__ void __launch_bounds__(kLThreads, 1)
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        uint8_t* stage_base = smem + kLStageOff + (warp - 2) * 2 * kLStageBytes;
+        int sb = 0;   // the staging box the next chunk goes to
         uint32_t tcount = 0;
         for (int u = first; u < total; u += stride, ++tcount) {
             int mt, nt;
@@ -306,21 +307,38 @@ __global__ void __launch_bounds__(kLThreads, 1)
                     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(rr[i]);
                 }
             };
-            auto dest = [&](int n, int& col) {   // the output that holds column n (selects, no indexed array)
-                const int o = MODE == 0 ? 0 : n < out.base[1] ? 0 : n < out.base[2] ? 1 : 2;
-                col = n - (o == 0 ? out.base[0] : o == 1 ? out.base[1] : out.base[2]);
-                return (o == 0 ? out.y[0] : o == 1 ? out.y[1] : out.y[2]) +
-                       (size_t)row * (o == 0 ? out.ld[0] : o == 1 ? out.ld[1] : out.ld[2]);
-            };
             const int half = MODE == 1 ? out.d / 2 : 0;
+            // the 32 columns from product column n of this warp's 32 rows: each lane writes its row
+            // into a staging box (16-byte pieces at slots piece ^ ((row >> 1) & 3), the 64-byte
+            // swizzle of the output maps), then one TMA store writes the box; rows past the end are
+            // clipped by the map.  A box is rewritten only after its previous store has read it.
+            auto put = [&](int n, const float (&v)[32]) {
+                const int o = MODE == 0 ? 0 : n < out.base[1] ? 0 : n < out.base[2] ? 1 : 2;
+                const int col = n - (o == 0 ? out.base[0] : o == 1 ? out.base[1] : out.base[2]);
+                uint8_t* st = stage_base + sb * kLStageBytes;
+                if (lane == 0) tma_store_wait_read1();
+                __syncwarp();
+                uint4* srow = reinterpret_cast<uint4*>(st + lane * 64);
+                const int sx = (lane >> 1) & 3;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    srow[i ^ sx] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                              pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
+                                              pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && mt * kLM + quarter * 32 < rows) {   // a box wholly past the last row is not stored
+                    tma_store_2d(o == 0 ? &tm_y0 : o == 1 ? &tm_y1 : &tm_y2, st, col, mt * kLM + quarter * 32);
+                    tma_store_commit();
+                }
+                sb ^= 1;
+            };
 #pragma unroll 1
             for (int c = 0; c < kLN / 32; ++c) {
                 const int n = n0 + c * 32;
                 if (n >= N) break;
                 if (MODE == 1 && n < out.n_rot) {   // q or k: chunk c and its partner half a head later
-                    int col;
-                    __nv_bfloat16* dst = dest(n, col);
-                    const int j = col % out.d;
+                    const int j = (n - (n < out.base[1] ? out.base[0] : out.base[1])) % out.d;
                     if (j >= half) continue;   // written with its first half
                     float2 tab[32];            // (cos, sin), fetched before the TMEM wait
                     if (valid) {
@@ -340,9 +358,9 @@ __global__ void __launch_bounds__(kLThreads, 1)
                             x0[i] = a * tab[i].x - b * tab[i].y;
                             x1[i] = b * tab[i].x + a * tab[i].y;
                         }
-                        store_bf16x32(dst + col, x0);
-                        store_bf16x32(dst + col + half, x1);
                     }
+                    put(n, x0);
+                    put(n + half, x1);
                     continue;
                 }
                 // no turn: this chunk and (when it is not a turned one) the next, one TMEM wait
@@ -352,19 +370,17 @@ __global__ void __launch_bounds__(kLThreads, 1)
                 else tmem_ld32(t0 + c * 32, ra);
                 float v[32];
                 scale(c, ra, v);
-                int col;
-                __nv_bfloat16* dst = dest(n, col);
-                if (valid) store_bf16x32(dst + col, v);
+                put(n, v);
                 if (two) {
                     scale(c + 1, rb, v);
-                    __nv_bfloat16* dst1 = dest(n + 32, col);
-                    if (valid) store_bf16x32(dst1 + col, v);
+                    put(n + 32, v);
                     ++c;
                 }
             }
             tc_fence_before();
             mbar_arrive(&bars[LACC_EMPTY0 + acc]);
         }
+        if (lane == 0) tma_store_wait_all();   // this warp's stores have completed before the CTA retires
     }
 
     tc_fence_before();
@@ -402,8 +418,23 @@ spinf_status launch_linear(const void* x, const void* w, const float* w_scale, f
     const long long row_tile = (long long)kLM * K * (long long)elt;
     const bool big_w = (long long)N * K * (long long)elt > (48ll << 20);
     const int rpb = big_w ? (int)std::max(1ll, std::min<long long>((32ll << 20) / std::max(1ll, row_tile), n_mt)) : 0;
-    linear_kernel<FP8, MODE><<<grid, kLThreads, kLSmem, stream>>>(tx, tw, w_scale, x_scale, out, (int)rows, (int)N,
-                                                                 n_kb, n_mt, n_nt, rpb, err);
+    // outputs as 2-D (columns, rows) maps, 32 x 32 boxes with the 64-byte swizzle of the staging
+    CUtensorMap ty[3];
+    const int n_out = MODE == 0 ? 1 : 3;
+    for (int o = 0; o < 3; ++o) {
+        if (o >= n_out) {
+            ty[o] = ty[0];
+            continue;
+        }
+        const int64_t width = MODE == 0 ? N : (o == 0 ? out.base[1] : o == 1 ? out.base[2] - out.base[1] : N - out.base[2]);
+        const uint64_t dy[2] = {(uint64_t)width, (uint64_t)rows};
+        const uint64_t sy[1] = {(uint64_t)out.ld[o] * 2};
+        const uint32_t by[2] = {32u, 32u};
+        if ((s = make_tmap(&ty[o], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out.y[o], dy, sy, by, CU_TENSOR_MAP_SWIZZLE_64B)))
+            return s;
+    }
+    linear_kernel<FP8, MODE><<<grid, kLThreads, kLSmem, stream>>>(tx, tw, ty[0], ty[1], ty[2], w_scale, x_scale, out,
+                                                                 (int)rows, (int)N, n_kb, n_mt, n_nt, rpb, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "linear launch");
     return SPINF_OK;
